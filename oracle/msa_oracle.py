@@ -1,0 +1,375 @@
+"""fp64 CPU oracle for the MiniMax Sparse Attention (MSA) hot path.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, the package's smoke check and
+the benchmark's CPU-baseline leg may import this module; the product path
+(the CUDA library and its Python binding) never does, and it shares no code
+with them.  Everything here is plain numpy in float64, written for a reader
+to check against the pages by eye: no tiling, fusion or reordering beyond
+what the method states.
+
+Sources (page title, section):
+  [README]  "MiniMax-AI/MSA" README (pigsec.cn mirror), section "Usage":
+            the three-stage flow -- a dense proxy pass with
+            num_kv_heads=1 and output_maxscore=True that yields a per-block
+            max score, sparse_topk_select(max_score, topk, num_valid_pages)
+            that yields kv_block_indexes, and a plan with kv_block_num=topk
+            whose attention visits only those blocks through the page table
+            kv_indices; page_size 128.
+  [NEWS]    news.ditty.ir, "MSA: MiniMax sparse attention kernels for SM100
+            GPUs", paragraph on the three-stage flow (same three stages).
+  [FLASH]   iitog.ru, "Flash-MSA: open kernels for training models with
+            sparse attention on millions of tokens":
+              - "three key differences" paragraph: whole 128-token blocks
+                picked by max-pooling proxy scores; GQA main attention;
+                each proxy head picks its own block set per GQA group;
+              - "kernel design" paragraph: the token's own (local) block is
+                always visible, block indexes are cached from the forward
+                and reused by the backward;
+              - "backward pass" paragraph: the gradient of the KL loss with
+                respect to a proxy score is p_proxy - p_main.
+
+Readings where the pages are silent (each is listed in the design doc):
+  R1  causal alignment is bottom-right: query row r of a sequence with
+      qo_len rows and kv_len keys sits at position kv_len - qo_len + r and
+      sees key k iff k <= that position.
+  R2  the proxy pools LOGITS (q.k/sqrt(dp)), not probabilities; -inf where a
+      block holds no visible key for any row of the tile.
+  R3  the diagonal block of a tile is the block holding the tile's last
+      row's position: j_d = num_valid_pages - 1; it is selected first and
+      counts inside topk.  The other topk-1 blocks are the largest finite
+      max_score values among j < j_d, ties to the lower block index.
+      Output is ascending, padded with -1.  If topk >= num_valid_pages all
+      valid blocks are selected.
+  R4  main attention scale is 1/sqrt(d); LSE is natural-log.
+  R5  FP8 e4m3 K/V carry one fp32 scale per KV head: logit =
+      (q.k_code)*k_scale/sqrt(d), value = v_code*v_scale.
+  R6  the KL term is KL(p_main || p_proxy) per (query row, GQA group) over
+      the selected visible keys, p_main = mean of the group's G head
+      distributions (detached), summed over rows, weight w; the LM loss
+      sends no gradient into the proxy and the KL none into main Q/K/V.
+      Parity of R6's domain and mean is unpinned by the pages.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+
+import numpy as np
+
+PAGE = 128   # tokens per KV block / page  ([README] "page_size, topk = 128, 16")
+TILE = 128   # query rows per tile
+
+
+# ---------------------------------------------------------------------------
+# exact decoding of the stored bit patterns
+# ---------------------------------------------------------------------------
+
+def bf16_to_f64(bits) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) -> float64, exactly (bf16 is the upper
+    half of an IEEE binary32)."""
+    u = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def e4m3_to_f64(bits) -> np.ndarray:
+    """OCP FP8 E4M3 ("e4m3fn") bit patterns -> float64 from the format's
+    definition: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+    field 0 is subnormal (2^-6 * m/8); S.1111.111 is NaN; no infinities."""
+    b = np.ascontiguousarray(bits).view(np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = b & 0x7
+    normal = np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64))
+    sub = np.ldexp(m / 8.0, -6)
+    v = sign * np.where(e == 0, sub, normal)
+    v = np.where((e == 15) & (m == 7), np.nan, v)
+    return v
+
+
+# ---------------------------------------------------------------------------
+# tiling and page table (R1, R3)
+# ---------------------------------------------------------------------------
+
+@dataclass(frozen=True)
+class Tile:
+    seq: int        # sequence index in the batch
+    q_begin: int    # first global query row of the tile
+    q_end: int      # one past the last global query row
+    pos0: int       # key position of the tile's first row (R1)
+    kv_len: int     # keys in the tile's sequence
+    nvp: int        # num_valid_pages: blocks holding a key visible to some row
+
+
+def kv_indptr(kv_lens) -> np.ndarray:
+    """Start of each sequence's pages in the flat kv_indices list: one page
+    per 128 keys, ceil(kv_len/128) pages per sequence."""
+    nb = [(int(k) + PAGE - 1) // PAGE for k in kv_lens]
+    return np.concatenate([[0], np.cumsum(nb)]).astype(np.int64)
+
+
+def tiles_of(qo_lens, kv_lens) -> list[Tile]:
+    """Query tiles of 128 rows, numbered across the whole batch (R1, R3)."""
+    out = []
+    q0 = 0
+    for s, (ql, kl) in enumerate(zip(qo_lens, kv_lens)):
+        ql, kl = int(ql), int(kl)
+        assert 0 <= ql <= kl
+        off = kl - ql
+        for t in range((ql + TILE - 1) // TILE):
+            r0, r1 = t * TILE, min((t + 1) * TILE, ql)
+            last_pos = off + r1 - 1
+            out.append(Tile(s, q0 + r0, q0 + r1, off + r0, kl, last_pos // PAGE + 1))
+        q0 += ql
+    return out
+
+
+def num_valid_pages(qo_lens, kv_lens) -> np.ndarray:
+    return np.array([t.nvp for t in tiles_of(qo_lens, kv_lens)], dtype=np.int32)
+
+
+def max_blocks(kv_lens) -> int:
+    return max([(int(k) + PAGE - 1) // PAGE for k in kv_lens] + [0])
+
+
+def gather_seq(pages: np.ndarray, kv_indices, indptr, seq: int, kv_len: int) -> np.ndarray:
+    """Keys of one sequence in logical order through the page table
+    ([README] "kv_indices"): pages [P, H, 128, D] -> [kv_len, H, D]."""
+    nb = (kv_len + PAGE - 1) // PAGE
+    ids = np.asarray(kv_indices[indptr[seq]: indptr[seq] + nb], dtype=np.int64)
+    blocks = pages[ids]                                  # [nb, H, 128, D]
+    return blocks.transpose(0, 2, 1, 3).reshape(nb * PAGE, pages.shape[1], pages.shape[3])[:kv_len]
+
+
+# ---------------------------------------------------------------------------
+# stage 1: proxy max score (R2)
+# ---------------------------------------------------------------------------
+
+def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=None):
+    """max_score[t, h, j] = max over rows i of tile t and keys k of block j
+    with k visible to i of pq[i,h].pk[k]/sqrt(dp), rounded once to fp32;
+    -inf where no pair is visible.  pq: [total_q, Hp, dp] bf16 bits;
+    pk: [P, 1, 128, dp] bf16 bits (one shared proxy K head, [README]
+    "num_kv_heads=1").  Returns float32 [n_tiles, Hp, nb_max]; tiles not in
+    tile_ids stay -inf."""
+    pq = bf16_to_f64(pq_bits)
+    pk = bf16_to_f64(pk_bits)
+    tiles = tiles_of(qo_lens, kv_lens)
+    indptr = kv_indptr(kv_lens)
+    hp, dp = pq.shape[1], pq.shape[2]
+    out = np.full((len(tiles), hp, max_blocks(kv_lens)), -np.inf, dtype=np.float64)
+    for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
+        tl = tiles[ti]
+        keys = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]   # [kv_len, dp]
+        nk = min(tl.nvp * PAGE, tl.kv_len)
+        keys = keys[:nk]
+        qrows = pq[tl.q_begin: tl.q_end]                                       # [R, hp, dp]
+        logits = np.einsum("rhc,kc->hrk", qrows, keys) / math.sqrt(dp)          # [hp, R, nk]
+        qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
+        visible = np.arange(nk)[None, :] <= qpos[:, None]                       # [R, nk]
+        logits = np.where(visible[None], logits, -np.inf)
+        for j in range(tl.nvp):
+            out[ti, :, j] = logits[:, :, j * PAGE: (j + 1) * PAGE].max(axis=(1, 2))
+    return out.astype(np.float32)
+
+
+# ---------------------------------------------------------------------------
+# stage 2: top-k block selection (R3)
+# ---------------------------------------------------------------------------
+
+def topk_row(scores, nvp: int, topk: int) -> list[int]:
+    """Block indexes selected for one (tile, proxy head) row of max_score."""
+    jd = nvp - 1
+    if topk >= nvp:
+        return list(range(nvp))
+    cands = [j for j in range(jd) if scores[j] > -np.inf]
+    # descending score, then ascending block index; -0.0 == +0.0 here
+    cands.sort(key=lambda j: (-float(scores[j]), j))
+    return sorted(cands[: topk - 1] + [jd])
+
+
+def topk_select(max_score, topk: int, nvp) -> np.ndarray:
+    """kv_block_indexes [n_tiles, H, topk] int32, ascending, -1 padded
+    ([README] sparse_topk_select(max_score, topk, num_valid_pages);
+    [FLASH] local block always visible, one block set per proxy head)."""
+    ms = np.asarray(max_score, dtype=np.float32)
+    n, h, _ = ms.shape
+    out = np.full((n, h, topk), -1, dtype=np.int32)
+    for t in range(n):
+        for g in range(h):
+            sel = topk_row(ms[t, g], int(nvp[t]), topk)
+            out[t, g, : len(sel)] = sel
+    return out
+
+
+# ---------------------------------------------------------------------------
+# stage 3: block-sparse GQA attention (R1, R4, R5)
+# ---------------------------------------------------------------------------
+
+def _selected_keys(tl: Tile, idx_row) -> np.ndarray:
+    """Logical key positions of the selected blocks, ascending."""
+    blocks = [int(j) for j in idx_row if j >= 0]
+    ks = [np.arange(j * PAGE, min((j + 1) * PAGE, tl.kv_len)) for j in blocks]
+    return np.concatenate(ks) if ks else np.zeros(0, dtype=np.int64)
+
+
+def _decode_kv(bits, fp8: bool):
+    return e4m3_to_f64(bits) if fp8 else bf16_to_f64(bits)
+
+
+def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
+                     k_scale=None, v_scale=None, tile_ids=None):
+    """For query i of tile t and head h (group g = h // G): softmax over the
+    keys of the blocks kv_block_indexes[t, g, :] that are visible to i of
+    q.k/sqrt(d), O = P.V, LSE = ln sum exp.  bf16 K/V, or e4m3 K/V with
+    per-KV-head scales when k_scale/v_scale are given.  Returns (O, LSE) in
+    float64; rows of tiles not in tile_ids are NaN."""
+    fp8 = k_scale is not None
+    q = bf16_to_f64(q_bits)
+    kp = _decode_kv(k_bits, fp8)
+    vp = _decode_kv(v_bits, fp8)
+    tiles = tiles_of(qo_lens, kv_lens)
+    indptr = kv_indptr(kv_lens)
+    hq, d = q.shape[1], q.shape[2]
+    hkv = kp.shape[1]
+    grp = hq // hkv
+    o = np.full(q.shape, np.nan)
+    lse = np.full(q.shape[:2], np.nan)
+    for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
+        tl = tiles[ti]
+        kseq = gather_seq(kp, kv_indices, indptr, tl.seq, tl.kv_len)
+        vseq = gather_seq(vp, kv_indices, indptr, tl.seq, tl.kv_len)
+        qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
+        for h in range(hq):
+            g = h // grp
+            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+            kmat = kseq[ks, g, :]
+            vmat = vseq[ks, g, :]
+            if fp8:
+                kmat = kmat * float(k_scale[g])
+                vmat = vmat * float(v_scale[g])
+            s = q[tl.q_begin: tl.q_end, h, :] @ kmat.T / math.sqrt(d)
+            s = np.where(ks[None, :] <= qpos[:, None], s, -np.inf)
+            m = s.max(axis=1, keepdims=True)
+            e = np.exp(s - m)
+            l = e.sum(axis=1, keepdims=True)
+            lse[tl.q_begin: tl.q_end, h] = (m + np.log(l))[:, 0]
+            o[tl.q_begin: tl.q_end, h, :] = (e / l) @ vmat
+    return o, lse
+
+
+# ---------------------------------------------------------------------------
+# training extension: backward with the KL-coupled proxy gradient (R6)
+# ---------------------------------------------------------------------------
+
+def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
+                         dout_bits, pq_bits, pk_bits, kl_weight=1.0, tile_ids=None):
+    """Gradients of sum(O * dO) with respect to q, k, v restricted to the
+    cached blocks, plus the proxy gradients of w * sum_rows KL(p_main ||
+    p_proxy), whose logit gradient is w*(p_proxy - p_main) ([FLASH]
+    backward-pass paragraph).  bf16 inputs.  Returns a dict of float64
+    arrays: dq [total_q,Hq,d], dk, dv [P,Hkv,128,d], dpq [total_q,Hp,dp],
+    dpk [P,1,128,dp], plus o and lse of the forward.  Only tiles in tile_ids
+    contribute (rows of other tiles in dq/dpq are NaN)."""
+    q = bf16_to_f64(q_bits)
+    kp = bf16_to_f64(k_bits)
+    vp = bf16_to_f64(v_bits)
+    do = bf16_to_f64(dout_bits)
+    pq = bf16_to_f64(pq_bits)
+    pk = bf16_to_f64(pk_bits)
+    tiles = tiles_of(qo_lens, kv_lens)
+    indptr = kv_indptr(kv_lens)
+    hq, d = q.shape[1], q.shape[2]
+    hkv = kp.shape[1]
+    grp = hq // hkv
+    dp = pq.shape[2]
+    dq = np.full(q.shape, np.nan)
+    dpq = np.full(pq.shape, np.nan)
+    dk = np.zeros(kp.shape)
+    dv = np.zeros(vp.shape)
+    dpk = np.zeros(pk.shape)
+    o = np.full(q.shape, np.nan)
+    lse = np.full(q.shape[:2], np.nan)
+    for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
+        tl = tiles[ti]
+        rows = slice(tl.q_begin, tl.q_end)
+        nb = (tl.kv_len + PAGE - 1) // PAGE
+        page_ids = np.asarray(kv_indices[indptr[tl.seq]: indptr[tl.seq] + nb], dtype=np.int64)
+        kseq = gather_seq(kp, kv_indices, indptr, tl.seq, tl.kv_len)
+        vseq = gather_seq(vp, kv_indices, indptr, tl.seq, tl.kv_len)
+        pkseq = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]
+        qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
+        for g in range(hkv):
+            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+            vis = ks[None, :] <= qpos[:, None]
+            kmat, vmat = kseq[ks, g, :], vseq[ks, g, :]
+            dkmat = np.zeros_like(kmat)
+            dvmat = np.zeros_like(vmat)
+            p_main = np.zeros(vis.shape)
+            for h in range(g * grp, (g + 1) * grp):
+                s = np.where(vis, q[rows, h, :] @ kmat.T / math.sqrt(d), -np.inf)
+                m = s.max(axis=1, keepdims=True)
+                l = np.exp(s - m).sum(axis=1, keepdims=True)
+                lse_h = m + np.log(l)
+                p = np.exp(s - lse_h)                                   # [R, n]
+                oh = p @ vmat
+                o[rows, h, :] = oh
+                lse[rows, h] = lse_h[:, 0]
+                dov = do[rows, h, :]
+                dP = dov @ vmat.T
+                D = (dov * oh).sum(axis=1, keepdims=True)
+                dS = p * (dP - D)
+                dq[rows, h, :] = dS @ kmat / math.sqrt(d)
+                dkmat += dS.T @ q[rows, h, :] / math.sqrt(d)
+                dvmat += p.T @ dov
+                p_main += p / grp
+            # proxy distribution over the same selected, visible keys
+            z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
+            zm = z.max(axis=1, keepdims=True)
+            ez = np.exp(z - zm)
+            p_proxy = ez / ez.sum(axis=1, keepdims=True)
+            dz = kl_weight * (p_proxy - p_main)
+            dpq[rows, g, :] = dz @ pkseq[ks] / math.sqrt(dp)
+            dpk_keys = dz.T @ pq[rows, g, :] / math.sqrt(dp)            # [n, dp]
+            # scatter per-key gradients back to physical pages
+            pg = page_ids[ks // PAGE]
+            np.add.at(dk, (pg, g, ks % PAGE), dkmat)
+            np.add.at(dv, (pg, g, ks % PAGE), dvmat)
+            np.add.at(dpk, (pg, 0, ks % PAGE), dpk_keys)
+    return dict(dq=dq, dk=dk, dv=dv, dpq=dpq, dpk=dpk, o=o, lse=lse)
+
+
+def kl_objective(pq, pk, q_bits, k_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
+                 kl_weight=1.0):
+    """w * sum over rows and groups of KL(p_main || p_proxy) as a function of
+    float64 proxy inputs pq [total_q,Hp,dp], pk [P,1,128,dp], with p_main
+    from the bf16 main q/k (held fixed).  Used to pin the closed-form proxy
+    gradient by finite differences."""
+    q = bf16_to_f64(q_bits)
+    kp = bf16_to_f64(k_bits)
+    tiles = tiles_of(qo_lens, kv_lens)
+    indptr = kv_indptr(kv_lens)
+    hq, d = q.shape[1], q.shape[2]
+    hkv = kp.shape[1]
+    grp = hq // hkv
+    dp = pq.shape[2]
+    total = 0.0
+    for ti, tl in enumerate(tiles):
+        rows = slice(tl.q_begin, tl.q_end)
+        kseq = gather_seq(kp, kv_indices, indptr, tl.seq, tl.kv_len)
+        pkseq = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]
+        qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
+        for g in range(hkv):
+            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+            vis = ks[None, :] <= qpos[:, None]
+            p_main = np.zeros(vis.shape)
+            for h in range(g * grp, (g + 1) * grp):
+                s = np.where(vis, q[rows, h, :] @ kseq[ks, g, :].T / math.sqrt(d), -np.inf)
+                e = np.exp(s - s.max(axis=1, keepdims=True))
+                p_main += e / e.sum(axis=1, keepdims=True) / grp
+            z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
+            zm = z.max(axis=1, keepdims=True)
+            log_pp = z - zm - np.log(np.exp(z - zm).sum(axis=1, keepdims=True))
+            with np.errstate(divide="ignore", invalid="ignore"):
+                terms = np.where(p_main > 0, p_main * (np.log(p_main) - log_pp), 0.0)
+            total += kl_weight * terms.sum()
+    return total

@@ -1,0 +1,451 @@
+"""Pins for the fp64 oracle: every check here compares the oracle with a
+route that does not go through the oracle's own formula -- torch's library
+attention and autograd, max-pooling, closed forms, brute force over subsets
+and central finite differences -- chosen so that a dropped term, a wrong
+sign, index, mask boundary or a transposed operand in the oracle fails."""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import msa_oracle as O
+from block_sparse_long_proxy_gb300 import synth
+
+PAGE = 128
+
+
+# ---------------------------------------------------------------- decoding --
+
+def test_bf16_decode_all_patterns():
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ours = O.bf16_to_f64(pats)
+    ref = torch.from_numpy(pats.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+
+
+def test_e4m3_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    ours = O.e4m3_to_f64(codes)
+    ref = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).double().numpy()
+    nan = np.isnan(ref)
+    assert nan.sum() == 2  # 0x7f and 0xff
+    assert np.array_equal(np.isnan(ours), nan)
+    assert np.array_equal(ours[~nan], ref[~nan])
+    assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+
+
+# ------------------------------------------------------------------ tiling --
+
+def test_tiles_closed_form():
+    tl = O.tiles_of([1024], [1024])
+    assert [t.nvp for t in tl] == list(range(1, 9))
+    assert all(t.pos0 == 128 * i for i, t in enumerate(tl))
+    dec = O.tiles_of([1] * 3, [131072, 200, 129])
+    assert [t.nvp for t in dec] == [1024, 2, 2]
+    # ragged tail with a prefix: offset 800, rows 0..199
+    rag = O.tiles_of([200], [1000])
+    assert [(t.q_begin, t.q_end, t.pos0, t.nvp) for t in rag] == [(0, 128, 800, 8), (128, 200, 928, 8)]
+    assert list(O.kv_indptr([1000, 128, 129])) == [0, 8, 9, 11]
+    assert O.tiles_of([0, 5], [10, 5])[0].seq == 1
+
+
+# ------------------------------------------------------------------- top-k --
+
+def _precedes(a, b, s):
+    return (s[a] > s[b]) or (s[a] == s[b] and a < b)
+
+
+def _brute_topk(scores, nvp, k):
+    """Unique subset where every member precedes every non-member, by
+    enumeration over all subsets of the right size."""
+    jd = nvp - 1
+    if k >= nvp:
+        return list(range(nvp))
+    cands = [j for j in range(jd) if scores[j] > -np.inf]
+    m = min(k - 1, len(cands))
+    hits = []
+    for sub in itertools.combinations(cands, m):
+        rest = [j for j in cands if j not in sub]
+        if all(_precedes(a, b, scores) for a in sub for b in rest):
+            hits.append(sorted(list(sub) + [jd]))
+    assert len(hits) == 1
+    return hits[0]
+
+
+def test_topk_brute_force_tiny():
+    rng = np.random.default_rng(0)
+    for trial in range(400):
+        nb = int(rng.integers(1, 10))
+        nvp = int(rng.integers(1, nb + 1))
+        k = int(rng.integers(1, 7))
+        # few distinct values -> many ties; some -inf; a -0.0 next to +0.0
+        vals = np.array([-np.inf, -1.5, -0.0, 0.0, 0.25, 2.0], dtype=np.float32)
+        sc = vals[rng.integers(0, len(vals), nb)]
+        assert O.topk_row(sc, nvp, k) == _brute_topk(sc, nvp, k), (sc, nvp, k)
+
+
+def test_topk_special_cases():
+    eq = np.zeros(10, dtype=np.float32)
+    assert O.topk_row(eq, 10, 4) == [0, 1, 2, 9]            # ties -> lower index
+    ninf = np.full(10, -np.inf, dtype=np.float32)
+    assert O.topk_row(ninf, 10, 4) == [9]                    # never picks -inf
+    assert O.topk_row(eq, 3, 4) == [0, 1, 2]                 # K >= nvp: all valid
+    sc = np.array([5, 1, 9, 3, -100, 7], dtype=np.float32)
+    assert O.topk_row(sc, 5, 3) == [0, 2, 4]                 # diagonal forced even if lowest
+    ms = np.stack([sc[None].repeat(2, 0)])                   # [1, 2, 6]
+    out = O.topk_select(ms, 4, np.array([5]))
+    assert out.shape == (1, 2, 4) and list(out[0, 0]) == [0, 2, 3, 4]
+    pad = O.topk_select(np.stack([ninf[None]]), 4, np.array([10]))
+    assert list(pad[0, 0]) == [9, -1, -1, -1]
+
+
+# -------------------------------------------------------------- proxy max --
+
+def _mk(case):
+    return synth.make_inputs(case)
+
+
+def _pool_route(inp, case):
+    """max_score by a different route: dense masked logits with torch.matmul,
+    then F.max_pool2d over 128x128 windows (ceil mode)."""
+    pq = inp["pq"].double()
+    pk = inp["pk_pages"].double()
+    table = inp["kv_indices"].long()
+    outs = []
+    q0, p0 = 0, 0
+    nbmax = max((k + PAGE - 1) // PAGE for k in case.kv_lens)
+    for ql, kl in zip(case.qo_lens, case.kv_lens):
+        nb = (kl + PAGE - 1) // PAGE
+        keys = torch.cat([pk[table[p0 + j], 0] for j in range(nb)], 0)[:kl]     # [kl, dp]
+        qs = pq[q0:q0 + ql]                                                     # [ql, hp, dp]
+        lg = torch.einsum("rhc,kc->hrk", qs, keys) / math.sqrt(case.dp)
+        qpos = (kl - ql) + torch.arange(ql)
+        vis = torch.arange(kl)[None, :] <= qpos[:, None]
+        lg = lg.masked_fill(~vis[None], -math.inf)
+        pooled = F.max_pool2d(lg[:, None], kernel_size=PAGE, stride=PAGE, ceil_mode=True)[:, 0]
+        pooled = pooled.permute(1, 0, 2)                                        # [tiles, hp, nb]
+        full = torch.full((pooled.shape[0], case.hp, nbmax), -math.inf, dtype=torch.float64)
+        full[:, :, :nb] = pooled
+        outs.append(full)
+        q0 += ql
+        p0 += nb
+    return torch.cat(outs, 0).float().numpy()
+
+
+@pytest.mark.parametrize("qo,kv,perm", [([1024], [1024], None), ([200, 77], [1000, 300], 3),
+                                        ([1, 1], [700, 129], 5)])
+def test_proxy_max_pool_route(qo, kv, perm):
+    case = synth.Case("t", qo, kv, 4, 2, 64, 2, 32, 4, page_perm_seed=perm, extra_pages=2)
+    inp = _mk(case)
+    ms = O.proxy_max_score(synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]),
+                           inp["kv_indices"].numpy(), qo, kv)
+    ref = _pool_route(inp, case)
+    assert ms.shape == ref.shape
+    assert np.array_equal(np.isneginf(ms), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    np.testing.assert_allclose(ms[fin], ref[fin], rtol=1e-6, atol=1e-6)
+
+
+def test_proxy_closed_form_constant_keys():
+    """All proxy keys equal c and pq[i] = (i+1) c: logit = (i+1)|c|^2/sqrt(dp),
+    so max_score[t, j] is attained at the last row of tile t that sees any
+    key of block j."""
+    qo, kv, dp = 300, 500, 32
+    off = kv - qo
+    c = np.zeros(dp)
+    c[3] = 0.5
+    nb = (kv + PAGE - 1) // PAGE
+    pk = torch.zeros(nb, 1, PAGE, dp, dtype=torch.float64)
+    pk[:, 0, :, :] = torch.from_numpy(c)
+    pq = torch.from_numpy(np.arange(1, qo + 1)[:, None, None] * c[None, None, :])  # [qo,1,dp]
+    ms = O.proxy_max_score(synth.bits(pq.to(torch.bfloat16)), synth.bits(pk.to(torch.bfloat16)),
+                           np.arange(nb), [qo], [kv])
+    for t in range(3):
+        r_last = min((t + 1) * 128, qo) - 1
+        for j in range(nb):
+            rows = [r for r in range(t * 128, r_last + 1) if off + r >= j * PAGE]
+            want = (max(rows) + 1) * 0.25 / math.sqrt(dp) if rows else -math.inf
+            got = float(ms[t, 0, j])
+            assert (got == want) or abs(got - want) <= 1e-6 * abs(want), (t, j, got, want)
+
+
+def test_proxy_mask_boundary():
+    """One planted large pair on the causal boundary counts; one key further
+    right does not."""
+    qo = kv = 256
+    dp = 32
+    pq = torch.zeros(qo, 1, dp)
+    pk = torch.zeros(2, 1, PAGE, dp)
+    pq[130, 0, 0] = 4.0
+    pk[1, 0, 130 - 128, 0] = 2.0      # key 130 is visible to row 130
+    pk[1, 0, 140 - 128, 1] = 9.0      # key 140: future for rows < 140
+    pq[135, 0, 1] = 1.0               # row 135 must not see key 140
+    ms = O.proxy_max_score(synth.bits(pq.to(torch.bfloat16)), synth.bits(pk.to(torch.bfloat16)),
+                           np.arange(2), [qo], [kv])
+    assert float(ms[1, 0, 1]) == pytest.approx(8.0 / math.sqrt(dp))
+    assert float(ms[1, 0, 0]) == 0.0
+    assert float(ms[0, 0, 1]) == -math.inf
+
+
+# ----------------------------------------------------- sparse attention ----
+
+def _dense_route(inp, case, idx, fp8=False):
+    """Attention by torch's library routine with an explicit boolean mask:
+    visible (bottom-right causal) and block selected for (tile, group)."""
+    q = inp["q"].double()
+    if fp8:
+        k = inp["k_pages"].double() * inp["k_scale"].double().view(1, -1, 1, 1)
+        v = inp["v_pages"].double() * inp["v_scale"].double().view(1, -1, 1, 1)
+    else:
+        k, v = inp["k_pages"].double(), inp["v_pages"].double()
+    table = inp["kv_indices"].long()
+    grp = case.hq // case.hkv
+    outs = []
+    q0, p0, t0 = 0, 0, 0
+    for ql, kl in zip(case.qo_lens, case.kv_lens):
+        nb = (kl + PAGE - 1) // PAGE
+        ks = torch.cat([k[table[p0 + j]] for j in range(nb)], 1)[:, :kl]  # [hkv, kl, d]
+        vs = torch.cat([v[table[p0 + j]] for j in range(nb)], 1)[:, :kl]
+        qpos = (kl - ql) + torch.arange(ql)
+        vis = torch.arange(kl)[None, :] <= qpos[:, None]
+        o = torch.zeros(ql, case.hq, case.d, dtype=torch.float64)
+        for h in range(case.hq):
+            g = h // grp
+            sel = torch.zeros(ql, kl, dtype=torch.bool)
+            for r in range(ql):
+                for j in idx[t0 + r // 128, g]:
+                    if j >= 0:
+                        sel[r, j * PAGE:(j + 1) * PAGE] = True
+            o[:, h] = F.scaled_dot_product_attention(q[q0:q0 + ql, h][None], ks[g][None],
+                                                     vs[g][None], attn_mask=(vis & sel)[None])[0]
+        outs.append(o)
+        q0 += ql
+        p0 += nb
+        t0 += (ql + 127) // 128
+    return torch.cat(outs, 0).numpy()
+
+
+def _rand_idx(case, rng):
+    tl = O.tiles_of(case.qo_lens, case.kv_lens)
+    idx = np.full((len(tl), case.hkv, case.topk), -1, np.int32)
+    for t, tile in enumerate(tl):
+        for g in range(case.hkv):
+            others = rng.permutation(tile.nvp - 1)[: case.topk - 1]
+            sel = sorted(list(others) + [tile.nvp - 1])
+            idx[t, g, :len(sel)] = sel
+    return idx
+
+
+@pytest.mark.parametrize("qo,kv,topk", [([1024], [1024], 8), ([1024], [1024], 3),
+                                        ([200, 64], [333, 64], 2), ([1, 1], [500, 128], 2)])
+def test_sparse_attention_vs_library(qo, kv, topk):
+    case = synth.Case("t", qo, kv, 4, 2, 64, 2, 32, topk, page_perm_seed=2)
+    inp = _mk(case)
+    idx = _rand_idx(case, np.random.default_rng(1))
+    o, lse = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]),
+                                synth.bits(inp["v_pages"]), inp["kv_indices"].numpy(), idx, qo, kv)
+    ref = _dense_route(inp, case, idx)
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+    assert np.all(np.isfinite(lse))
+
+
+def test_topk_all_blocks_is_dense_causal():
+    case = synth.tiny()
+    case.topk = 8
+    inp = _mk(case)
+    nvp = O.num_valid_pages(case.qo_lens, case.kv_lens)
+    ms = O.proxy_max_score(synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]),
+                           inp["kv_indices"].numpy(), case.qo_lens, case.kv_lens)
+    idx = O.topk_select(ms, 8, nvp)
+    o, _ = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]),
+                              synth.bits(inp["v_pages"]), inp["kv_indices"].numpy(), idx,
+                              case.qo_lens, case.kv_lens)
+    q = inp["q"].double().permute(1, 0, 2)                          # [hq, S, d]
+    k = inp["k_pages"].double().permute(1, 0, 2, 3).reshape(2, 1024, 64)
+    v = inp["v_pages"].double().permute(1, 0, 2, 3).reshape(2, 1024, 64)
+    ref = F.scaled_dot_product_attention(q, k.repeat_interleave(4, 0), v.repeat_interleave(4, 0),
+                                         is_causal=True).permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_zero_keys_closed_form():
+    """K == 0: every visible logit is 0, so O is the mean of V over the
+    visible selected keys and LSE = ln(count)."""
+    case = synth.Case("t", [300], [300], 2, 1, 64, 1, 32, 2)
+    inp = _mk(case)
+    inp["k_pages"].zero_()
+    idx = _rand_idx(case, np.random.default_rng(4))
+    o, lse = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]),
+                                synth.bits(inp["v_pages"]), inp["kv_indices"].numpy(), idx, [300], [300])
+    v = inp["v_pages"].double()[:, 0].reshape(-1, 64)[:300].numpy()
+    for r in [0, 5, 127, 128, 200, 299]:
+        keys = [kk for j in idx[r // 128, 0] if j >= 0 for kk in range(j * 128, min(j * 128 + 128, 300))
+                if kk <= r]
+        np.testing.assert_allclose(o[r, 0], v[keys].mean(0), rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[r, 0], math.log(len(keys)), rtol=1e-12)
+
+
+def test_fp8_scales_vs_library():
+    case = synth.Case("t", [1, 1, 1], [640, 300, 129], 8, 2, 64, 2, 32, 3, kv_dtype="e4m3",
+                      page_perm_seed=9)
+    inp = _mk(case)
+    idx = _rand_idx(case, np.random.default_rng(3))
+    o, _ = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]),
+                              synth.bits(inp["v_pages"]), inp["kv_indices"].numpy(), idx,
+                              case.qo_lens, case.kv_lens, inp["k_scale"].numpy(), inp["v_scale"].numpy())
+    ref = _dense_route(inp, case, idx, fp8=True)
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+
+
+# --------------------------------------------------------------- backward --
+
+def _autograd_route(inp, case, idx, w):
+    """Main gradients by autograd through torch's attention with the block
+    mask; proxy gradients by autograd through torch's kl_div."""
+    grp = case.hq // case.hkv
+    q = inp["q"].double().requires_grad_()
+    kp = inp["k_pages"].double().requires_grad_()
+    vp = inp["v_pages"].double().requires_grad_()
+    pq = inp["pq"].double().requires_grad_()
+    pk = inp["pk_pages"].double().requires_grad_()
+    do = inp["dout"].double()
+    table = inp["kv_indices"].long()
+    loss_main = 0.0
+    loss_kl = 0.0
+    q0, p0, t0 = 0, 0, 0
+    for ql, kl in zip(case.qo_lens, case.kv_lens):
+        nb = (kl + PAGE - 1) // PAGE
+        ks = torch.cat([kp[table[p0 + j]] for j in range(nb)], 1)[:, :kl]
+        vs = torch.cat([vp[table[p0 + j]] for j in range(nb)], 1)[:, :kl]
+        pks = torch.cat([pk[table[p0 + j], 0] for j in range(nb)], 0)[:kl]
+        qpos = (kl - ql) + torch.arange(ql)
+        vis = torch.arange(kl)[None, :] <= qpos[:, None]
+        for g in range(case.hkv):
+            sel = torch.zeros(ql, kl, dtype=torch.bool)
+            for r in range(ql):
+                for j in idx[t0 + r // 128, g]:
+                    if j >= 0:
+                        sel[r, j * PAGE:(j + 1) * PAGE] = True
+            m = vis & sel
+            pmain = 0.0
+            for h in range(g * grp, (g + 1) * grp):
+                qh = q[q0:q0 + ql, h]
+                oh = F.scaled_dot_product_attention(qh[None], ks[g][None], vs[g][None], attn_mask=m[None])[0]
+                loss_main = loss_main + (oh * do[q0:q0 + ql, h]).sum()
+                s = (qh @ ks[g].T / math.sqrt(case.d)).masked_fill(~m, -math.inf)
+                pmain = pmain + torch.softmax(s, -1).detach() / grp
+            z = (pq[q0:q0 + ql, g] @ pks.T / math.sqrt(case.dp)).masked_fill(~m, -math.inf)
+            logp = torch.log_softmax(z, -1).masked_fill(~m, 0.0)
+            loss_kl = loss_kl + w * F.kl_div(logp, pmain, reduction="sum")
+        q0 += ql
+        p0 += nb
+        t0 += (ql + 127) // 128
+    (loss_main + loss_kl).backward()
+    return q.grad.numpy(), kp.grad.numpy(), vp.grad.numpy(), pq.grad.numpy(), pk.grad.numpy()
+
+
+@pytest.mark.parametrize("qo,kv,topk,w", [([256], [256], 2, 1.0), ([150, 40], [300, 200], 2, 0.5)])
+def test_bwd_vs_autograd(qo, kv, topk, w):
+    case = synth.Case("t", qo, kv, 4, 2, 64, 2, 32, topk, page_perm_seed=4, extra_pages=1)
+    inp = synth.make_inputs(case, with_dout=True)
+    idx = _rand_idx(case, np.random.default_rng(5))
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, qo, kv, synth.bits(inp["dout"]),
+                               synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]), kl_weight=w)
+    dq, dk, dv, dpq, dpk = _autograd_route(inp, case, idx, w)
+    for name, ref in [("dq", dq), ("dk", dk), ("dv", dv), ("dpq", dpq), ("dpk", dpk)]:
+        np.testing.assert_allclose(g[name], ref, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_kl_grad_finite_differences():
+    """The closed-form proxy gradient equals central differences of the
+    fp64 KL objective (w=1), for entries of pq and of pk."""
+    case = synth.Case("t", [256], [256], 4, 2, 64, 2, 32, 2)
+    inp = synth.make_inputs(case, with_dout=True)
+    idx = _rand_idx(case, np.random.default_rng(6))
+    args = (synth.bits(inp["q"]), synth.bits(inp["k_pages"]), inp["kv_indices"].numpy(), idx,
+            case.qo_lens, case.kv_lens)
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens,
+                               synth.bits(inp["dout"]), synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]))
+    pq = O.bf16_to_f64(synth.bits(inp["pq"]))
+    pk = O.bf16_to_f64(synth.bits(inp["pk_pages"]))
+    h = 1e-6
+    rng = np.random.default_rng(7)
+    for _ in range(6):
+        i, hh, c = int(rng.integers(0, 256)), int(rng.integers(0, 2)), int(rng.integers(0, 32))
+        a, b = pq.copy(), pq.copy()
+        a[i, hh, c] += h
+        b[i, hh, c] -= h
+        fd = (O.kl_objective(a, pk, *args) - O.kl_objective(b, pk, *args)) / (2 * h)
+        assert abs(fd - g["dpq"][i, hh, c]) <= 1e-6 * max(1.0, abs(fd)), (i, hh, c, fd, g["dpq"][i, hh, c])
+    for _ in range(6):
+        p, r, c = int(rng.integers(0, 2)), int(rng.integers(0, 128)), int(rng.integers(0, 32))
+        a, b = pk.copy(), pk.copy()
+        a[p, 0, r, c] += h
+        b[p, 0, r, c] -= h
+        fd = (O.kl_objective(pq, a, *args) - O.kl_objective(pq, b, *args)) / (2 * h)
+        assert abs(fd - g["dpk"][p, 0, r, c]) <= 1e-6 * max(1.0, abs(fd)), (p, r, c, fd)
+
+
+def test_main_bwd_finite_differences():
+    """dq/dk/dv equal central differences of sum(O * dO)."""
+    case = synth.Case("t", [256], [256], 2, 1, 64, 1, 32, 2)
+    inp = synth.make_inputs(case, with_dout=True)
+    idx = _rand_idx(case, np.random.default_rng(8))
+    bits = {k: synth.bits(inp[k]) for k in ("q", "k_pages", "v_pages", "dout", "pq", "pk_pages")}
+    g = O.sparse_attention_bwd(bits["q"], bits["k_pages"], bits["v_pages"], inp["kv_indices"].numpy(), idx,
+                               [256], [256], bits["dout"], bits["pq"], bits["pk_pages"])
+    do = O.bf16_to_f64(bits["dout"])
+
+    def objective(qf, kf, vf):
+        # forward in float64 from float inputs, through the oracle's own
+        # attention applied to exactly-representable perturbed inputs is not
+        # possible (bf16 inputs), so evaluate the masked softmax directly
+        ks = np.concatenate([np.arange(j * 128, j * 128 + 128) for j in idx[0, 0] if j >= 0] or [[]])
+        tot = 0.0
+        for t in range(2):
+            ks_t = np.concatenate([np.arange(j * 128, j * 128 + 128) for j in idx[t, 0] if j >= 0])
+            for r in range(t * 128, t * 128 + 128):
+                kk = ks_t[ks_t <= r]
+                for hh in range(2):
+                    s = kf.reshape(-1, 64)[kk] @ qf[r, hh] / 8.0
+                    p = np.exp(s - s.max())
+                    p /= p.sum()
+                    tot += (p @ vf.reshape(-1, 64)[kk]) @ do[r, hh]
+        del ks
+        return tot
+
+    qf = O.bf16_to_f64(bits["q"])
+    kf = O.bf16_to_f64(bits["k_pages"])[:, 0]
+    vf = O.bf16_to_f64(bits["v_pages"])[:, 0]
+    eps = 1e-6
+    rng = np.random.default_rng(9)
+    for name, arr, grad in [("q", qf, g["dq"]), ("k", kf, g["dk"][:, 0]), ("v", vf, g["dv"][:, 0])]:
+        for _ in range(4):
+            ix = tuple(int(rng.integers(0, n)) for n in arr.shape)
+            a, b = arr.copy(), arr.copy()
+            a[ix] += eps
+            b[ix] -= eps
+            qa, ka, va = (a if name == "q" else qf), (a if name == "k" else kf), (a if name == "v" else vf)
+            qb, kb, vb = (b if name == "q" else qf), (b if name == "k" else kf), (b if name == "v" else vf)
+            fd = (objective(qa, ka, va) - objective(qb, kb, vb)) / (2 * eps)
+            assert abs(fd - grad[ix]) <= 1e-6 * max(1.0, abs(fd)), (name, ix, fd, grad[ix])
+
+
+def test_kl_grad_constant_proxy_keys_is_zero():
+    """sum_k (p_proxy - p_main) = 0 per row, so with every proxy key equal
+    the pq gradient vanishes."""
+    case = synth.Case("t", [256], [256], 4, 2, 64, 2, 32, 2)
+    inp = synth.make_inputs(case, with_dout=True)
+    inp["pk_pages"][:] = inp["pk_pages"][0, 0, 0]
+    idx = _rand_idx(case, np.random.default_rng(10))
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, [256], [256], synth.bits(inp["dout"]),
+                               synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]))
+    assert np.abs(g["dpq"]).max() < 1e-12

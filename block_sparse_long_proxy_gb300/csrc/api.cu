@@ -1,0 +1,281 @@
+// Host side of libmsa: argument validation, the plan (tile table, page
+// offsets, workspace), dispatch to the kernels, error reporting.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "msa_internal.h"
+
+namespace msa {
+
+static thread_local std::string g_last_error;
+
+msa_status set_error(msa_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+msa_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return MSA_OK;
+  return set_error(MSA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, int dtype_bf16_or_u8,
+                       int swizzle_bytes) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gdim[5], gstride[4];
+  cuuint32_t bdim[5], estride[5];
+  for (int i = 0; i < rank; ++i) {
+    gdim[i] = dims[i];
+    bdim[i] = box[i];
+    estride[i] = 1;
+    if (i > 0) gstride[i - 1] = strides_bytes[i - 1];
+  }
+  CUtensorMapSwizzle sw = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
+  CUtensorMapDataType dt = dtype_bf16_or_u8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  CUresult r = fn(reinterpret_cast<CUtensorMap*>(map), dt, rank, const_cast<void*>(base), gdim, gstride, bdim,
+                  estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace msa
+
+using namespace msa;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" {
+
+const char* msa_last_error(void) { return g_last_error.c_str(); }
+const char* msa_version(void) { return "0.1.0"; }
+
+msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batch, int32_t num_qo_heads,
+                    int32_t num_kv_heads, int32_t num_proxy_heads, int32_t head_dim, int32_t proxy_head_dim,
+                    int32_t page_size, int32_t topk, int64_t num_pages, msa_kv_dtype kv_dtype, uint32_t flags,
+                    msa_stream_t stream, msa_plan_t* out) {
+  if (!out) return set_error(MSA_ERR_INVALID_ARG, "msa_plan: out is NULL");
+  *out = nullptr;
+  if (batch < 1 || !qo_lens || !kv_lens) return set_error(MSA_ERR_INVALID_ARG, "msa_plan: empty batch");
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_proxy_heads < 1)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_plan: head counts must be >= 1");
+  if (num_qo_heads % num_kv_heads != 0)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_plan: num_qo_heads %% num_kv_heads != 0");
+  if (num_proxy_heads != num_kv_heads)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: one proxy head per GQA group is required (Hp == Hkv)");
+  if (head_dim != 64 && head_dim != 128) return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: head_dim must be 64 or 128");
+  if (proxy_head_dim != 32 && proxy_head_dim != 64)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: proxy_head_dim must be 32 or 64");
+  if (page_size != kPage) return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: page_size must be 128");
+  if (topk < 1 || topk > 1024) return set_error(MSA_ERR_INVALID_ARG, "msa_plan: topk must be in [1, 1024]");
+  if (num_pages < 1 || num_pages > (int64_t(1) << 24))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_plan: num_pages out of range");
+  if (kv_dtype != MSA_KV_BF16 && kv_dtype != MSA_KV_FP8_E4M3)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_plan: unknown kv_dtype");
+  if (flags != 0) return set_error(MSA_ERR_INVALID_ARG, "msa_plan: flags must be 0");
+
+  auto* p = new msa_plan_s();
+  p->batch = batch;
+  p->hq = num_qo_heads;
+  p->hkv = num_kv_heads;
+  p->hp = num_proxy_heads;
+  p->d = head_dim;
+  p->dp = proxy_head_dim;
+  p->topk = topk;
+  p->num_pages = num_pages;
+  p->kv_dtype = kv_dtype;
+  p->qo_lens.assign(qo_lens, qo_lens + batch);
+  p->kv_lens.assign(kv_lens, kv_lens + batch);
+
+  int64_t q0 = 0, page_base = 0;
+  bool all_one = true;
+  for (int s = 0; s < batch; ++s) {
+    const int64_t ql = qo_lens[s], kl = kv_lens[s];
+    if (ql < 0 || kl < 1 || ql > kl) {
+      delete p;
+      return set_error(MSA_ERR_INVALID_ARG, "msa_plan: sequence %d needs 0 <= qo_len <= kv_len and kv_len >= 1", s);
+    }
+    if (ql != 1) all_one = false;
+    const int64_t nb = (kl + kPage - 1) / kPage;
+    p->max_blocks = static_cast<int32_t>(std::max<int64_t>(p->max_blocks, nb));
+    const int64_t off = kl - ql;
+    for (int64_t t = 0; t * kTile < ql; ++t) {
+      TileInfo ti{};
+      const int64_t r0 = t * kTile, r1 = std::min<int64_t>(ql, r0 + kTile);
+      ti.seq = s;
+      ti.q_begin = static_cast<int32_t>(q0 + r0);
+      ti.rows = static_cast<int32_t>(r1 - r0);
+      ti.pos0 = static_cast<int32_t>(off + r0);
+      ti.kv_len = static_cast<int32_t>(kl);
+      ti.nvp = static_cast<int32_t>((off + r1 - 1) / kPage + 1);
+      ti.page_base = static_cast<int32_t>(page_base);
+      p->tiles.push_back(ti);
+    }
+    q0 += ql;
+    page_base += nb;
+    if (q0 > (int64_t(1) << 31) - 1 || page_base > (int64_t(1) << 31) - 1) {
+      delete p;
+      return set_error(MSA_ERR_INVALID_ARG, "msa_plan: batch too large for 32-bit row / page indexing");
+    }
+  }
+  p->total_q = q0;
+  p->n_tiles = static_cast<int32_t>(p->tiles.size());
+  p->decode = all_one;
+  if (p->n_tiles == 0) {
+    delete p;
+    return set_error(MSA_ERR_INVALID_ARG, "msa_plan: no query rows in the batch");
+  }
+
+  if (cudaGetDevice(&p->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+    delete p;
+    return set_error(MSA_ERR_CUDA, "msa_plan: no CUDA device");
+  }
+
+  // device block: tiles | nvp | error word | decode partials
+  const size_t tiles_bytes = sizeof(TileInfo) * p->n_tiles;
+  const size_t nvp_off = (tiles_bytes + 255) & ~size_t(255);
+  const size_t err_off = nvp_off + ((sizeof(int32_t) * p->n_tiles + 255) & ~size_t(255));
+  const size_t part_off = err_off + 256;
+  const size_t part_bytes = sizeof(float) * decode_partial_floats(p);
+  const size_t total = part_off + part_bytes;
+  if (cudaMalloc(&p->dev_block, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return set_error(MSA_ERR_NO_MEMORY, "msa_plan: cudaMalloc of %zu bytes failed", total);
+  }
+  char* base = static_cast<char*>(p->dev_block);
+  p->tiles_d = reinterpret_cast<TileInfo*>(base);
+  p->nvp_d = reinterpret_cast<int32_t*>(base + nvp_off);
+  p->err_d = reinterpret_cast<uint32_t*>(base + err_off);
+  p->partial_d = part_bytes ? reinterpret_cast<float*>(base + part_off) : nullptr;
+
+  std::vector<char> host(part_off, 0);
+  memcpy(host.data(), p->tiles.data(), tiles_bytes);
+  for (int t = 0; t < p->n_tiles; ++t)
+    memcpy(host.data() + nvp_off + sizeof(int32_t) * t, &p->tiles[t].nvp, sizeof(int32_t));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  msa_status s = cuda_check(cudaMemcpyAsync(p->dev_block, host.data(), part_off, cudaMemcpyHostToDevice, st),
+                            "msa_plan: upload");
+  if (s == MSA_OK) s = cuda_check(cudaStreamSynchronize(st), "msa_plan: upload sync");
+  if (s != MSA_OK) {
+    cudaFree(p->dev_block);
+    delete p;
+    return s;
+  }
+  *out = p;
+  return MSA_OK;
+}
+
+void msa_plan_destroy(msa_plan_t plan) {
+  if (!plan) return;
+  if (plan->dev_block) cudaFree(plan->dev_block);
+  delete plan;
+}
+
+int32_t msa_plan_num_tiles(msa_plan_t plan) { return plan ? plan->n_tiles : 0; }
+int32_t msa_plan_max_blocks(msa_plan_t plan) { return plan ? plan->max_blocks : 0; }
+int64_t msa_plan_total_q(msa_plan_t plan) { return plan ? plan->total_q : 0; }
+const int32_t* msa_plan_num_valid_pages(msa_plan_t plan) { return plan ? plan->nvp_d : nullptr; }
+
+msa_status msa_proxy_maxscore(msa_plan_t plan, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                              float* max_score, msa_stream_t stream) {
+  if (!plan || !pq || !pk_pages || !kv_indices || !max_score)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore: NULL argument");
+  if (!aligned16(pq) || !aligned16(pk_pages))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore: pq and pk_pages must be 16-byte aligned");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->decode) return launch_proxy_decode(plan, pq, pk_pages, kv_indices, max_score, st);
+  return launch_proxy_prefill(plan, pq, pk_pages, kv_indices, max_score, st);
+}
+
+msa_status msa_topk_select(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,
+                           int32_t topk, const int32_t* num_valid_pages, int32_t* kv_block_indexes,
+                           msa_stream_t stream) {
+  if (!max_score || !num_valid_pages || !kv_block_indexes)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_topk_select: NULL argument");
+  if (n_tiles < 1 || heads < 1 || max_blocks < 1 || max_blocks > 65536 || topk < 1 || topk > 1024)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_topk_select: sizes out of range");
+  if (int64_t(n_tiles) * heads > (int64_t(1) << 31) - 1)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_topk_select: too many rows");
+  return launch_topk(max_score, n_tiles, heads, max_blocks, topk, num_valid_pages, kv_block_indexes,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_sparse_attn(msa_plan_t plan, const void* q, const void* k_pages, const void* v_pages,
+                           const int32_t* kv_indices, const int32_t* kv_block_indexes, const float* k_scale,
+                           const float* v_scale, void* out, float* lse, msa_stream_t stream) {
+  if (!plan || !q || !k_pages || !v_pages || !kv_indices || !kv_block_indexes || !out)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn: NULL argument");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn: q, k_pages, v_pages, out must be 16-byte aligned");
+  const bool fp8 = plan->kv_dtype == MSA_KV_FP8_E4M3;
+  if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn: k_scale/v_scale must be given exactly for FP8 K/V");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (plan->decode)
+    return launch_attn_decode(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale, out,
+                              lse, st);
+  if (fp8) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 K/V is implemented for decode batches only");
+  return launch_attn_prefill(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, st);
+}
+
+msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pages, const void* v_pages,
+                               const int32_t* kv_indices, const int32_t* kv_block_indexes, const void* out,
+                               const float* lse, const void* dout, const void* pq, const void* pk_pages,
+                               float kl_weight, float* dq, float* dk_pages, float* dv_pages, float* dpq,
+                               float* dpk_pages, msa_stream_t stream) {
+  if (!plan || !q || !k_pages || !v_pages || !kv_indices || !kv_block_indexes || !out || !lse || !dout || !pq ||
+      !pk_pages || !dq || !dk_pages || !dv_pages || !dpq || !dpk_pages)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn_bwd: NULL argument");
+  if (plan->kv_dtype != MSA_KV_BF16)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: bf16 K/V only");
+  return launch_attn_bwd(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, dout, pq, pk_pages,
+                         kl_weight, dq, dk_pages, dv_pages, dpq, dpk_pages, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream) {
+  if (!plan) return set_error(MSA_ERR_INVALID_ARG, "msa_check_errors: NULL plan");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  msa_status s = cuda_check(cudaStreamSynchronize(st), "msa_check_errors: sync");
+  if (s != MSA_OK) return s;
+  s = cuda_check(cudaMemcpy(&word, plan->err_d, sizeof(word), cudaMemcpyDeviceToHost), "msa_check_errors: read");
+  if (s != MSA_OK) return s;
+  if (word == 0) return MSA_OK;
+  s = cuda_check(cudaMemset(plan->err_d, 0, sizeof(uint32_t)), "msa_check_errors: clear");
+  if (s != MSA_OK) return s;
+  if (word & kErrTimeout) return set_error(MSA_ERR_TIMEOUT, "a bounded device-side wait gave up (word 0x%x)", word);
+  return set_error(MSA_ERR_DEVICE_CHECK, "a device-side bounds check fired: page id out of range (word 0x%x)", word);
+}
+
+}  // extern "C"

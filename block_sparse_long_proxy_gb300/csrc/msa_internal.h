@@ -1,0 +1,93 @@
+// Internal declarations of libmsa: plan layout, device tables and the kernel
+// launchers each translation unit provides.  Host-only C++ plus plain
+// structs shared with device code.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/msa.h"
+
+namespace msa {
+
+constexpr int kPage = 128;   // tokens per KV block / page
+constexpr int kTile = 128;   // query rows per tile
+
+// One query tile.  Positions follow bottom-right causal alignment: row r of
+// a sequence with qo_len rows and kv_len keys sits at key position
+// kv_len - qo_len + r.
+struct TileInfo {
+  int32_t seq;        // sequence index
+  int32_t q_begin;    // global index of the tile's first query row
+  int32_t rows;       // rows in this tile, 1..128
+  int32_t pos0;       // key position of the first row
+  int32_t kv_len;     // keys of the sequence
+  int32_t nvp;        // num_valid_pages: blocks up to the diagonal block
+  int32_t page_base;  // offset of the sequence's pages in kv_indices
+  int32_t pad;
+};
+static_assert(sizeof(TileInfo) == 32, "TileInfo is uploaded as raw bytes");
+
+// Bits of the device error word.
+enum : uint32_t { kErrDeviceCheck = 1u, kErrTimeout = 2u };
+
+}  // namespace msa
+
+struct msa_plan_s {
+  int device = 0;
+  int num_sms = 0;
+  int32_t batch = 0, hq = 0, hkv = 0, hp = 0, d = 0, dp = 0, topk = 0;
+  int64_t num_pages = 0;
+  msa_kv_dtype kv_dtype = MSA_KV_BF16;
+  int32_t n_tiles = 0, max_blocks = 0;
+  int64_t total_q = 0;
+  bool decode = false;               // every qo_len == 1
+  std::vector<int32_t> qo_lens, kv_lens;
+  std::vector<msa::TileInfo> tiles;  // host copy
+  // device memory owned by the plan (one allocation, carved up)
+  void* dev_block = nullptr;
+  msa::TileInfo* tiles_d = nullptr;
+  int32_t* nvp_d = nullptr;
+  uint32_t* err_d = nullptr;
+  float* partial_d = nullptr;        // decode split-K partials (O, m, l)
+  int32_t decode_ctas = 0;           // persistent decode grid size
+};
+
+namespace msa {
+
+msa_status set_error(msa_status s, const char* fmt, ...);
+msa_status cuda_check(cudaError_t e, const char* what);
+
+// ---- launchers (each returns MSA_OK or an error with its message set) ----
+msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,
+                       int32_t topk, const int32_t* nvp, int32_t* out, cudaStream_t st);
+
+msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages,
+                                const int32_t* kv_indices, float* max_score, cudaStream_t st);
+msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages,
+                               const int32_t* kv_indices, float* max_score, cudaStream_t st);
+
+msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages,
+                               const void* v_pages, const int32_t* kv_indices, const int32_t* idx,
+                               void* out, float* lse, cudaStream_t st);
+msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_pages,
+                              const void* v_pages, const int32_t* kv_indices, const int32_t* idx,
+                              const float* k_scale, const float* v_scale, void* out, float* lse,
+                              cudaStream_t st);
+size_t decode_partial_floats(const msa_plan_s* p);
+
+msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pages,
+                           const void* v_pages, const int32_t* kv_indices, const int32_t* idx,
+                           const void* out, const float* lse, const void* dout, const void* pq,
+                           const void* pk_pages, float kl_weight, float* dq, float* dk, float* dv,
+                           float* dpq, float* dpk, cudaStream_t st);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box, int dtype_bf16_or_u8,
+                       int swizzle_bytes);
+
+}  // namespace msa

@@ -1,0 +1,50 @@
+"""msa_topk_select on the GPU against the oracle, bit-exact on identical
+max_score inputs (ties, -inf, signed zeros, ragged num_valid_pages)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import msa_oracle as O
+
+pytestmark = pytest.mark.gpu
+
+
+def _scores(rng, n, h, nb, kind):
+    if kind == "ties":
+        vals = np.array([-np.inf, -2.0, -0.0, 0.0, 0.5, 1.0, 3.0], dtype=np.float32)
+        return vals[rng.integers(0, len(vals), (n, h, nb))]
+    x = rng.standard_normal((n, h, nb)).astype(np.float32)
+    x[rng.random((n, h, nb)) < 0.05] = -np.inf
+    return x
+
+
+@pytest.mark.parametrize("nb,topk,kind", [(8, 4, "ties"), (8, 1, "normal"), (200, 16, "normal"),
+                                          (256, 16, "ties"), (257, 16, "normal"), (1000, 40, "ties"),
+                                          (1024, 16, "normal"), (3000, 16, "ties"), (3000, 300, "normal"),
+                                          (64, 64, "normal"), (64, 65, "normal")])
+def test_topk_bit_exact(cuda_dev, nb, topk, kind):
+    from block_sparse_long_proxy_gb300 import msa
+    rng = np.random.default_rng(nb * 7 + topk)
+    n, h = 37, 3
+    ms = _scores(rng, n, h, nb, kind)
+    nvp = rng.integers(1, nb + 1, n).astype(np.int32)
+    nvp[0], nvp[1] = 1, nb
+    got = msa.topk_select(torch.from_numpy(ms).to(cuda_dev), topk,
+                          torch.from_numpy(nvp).to(cuda_dev)).cpu().numpy()
+    want = O.topk_select(ms, topk, nvp)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("n,h,nb", [(256, 8, 256), (1472, 8, 1024), (32, 8, 1024)])
+def test_topk_config_shapes(cuda_dev, n, h, nb):
+    """Shapes of the 32K prefill, the varlen prefill and the decode batch."""
+    from block_sparse_long_proxy_gb300 import msa
+    rng = np.random.default_rng(n)
+    ms = rng.standard_normal((n, h, nb)).astype(np.float32)
+    nvp = np.minimum(np.arange(n) % nb + 1, nb).astype(np.int32)
+    if n == 32:
+        nvp[:] = nb
+    for t in range(n):                       # -inf past the valid blocks
+        ms[t, :, nvp[t]:] = -np.inf
+    got = msa.topk_select(torch.from_numpy(ms).to(cuda_dev), 16, torch.from_numpy(nvp).to(cuda_dev)).cpu().numpy()
+    assert np.array_equal(got, O.topk_select(ms, 16, nvp))

@@ -161,11 +161,16 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
     return set_error(MSA_ERR_CUDA, "msa_plan: no CUDA device");
   }
 
-  // device block: tiles | nvp | error word | decode partials
+  std::vector<int32_t> aux;
+  proxy_plan_tables(p, aux);
+  attn_plan_tables(p, aux);
+
+  // device block: tiles | nvp | error word | aux tables | decode partials
   const size_t tiles_bytes = sizeof(TileInfo) * p->n_tiles;
   const size_t nvp_off = (tiles_bytes + 255) & ~size_t(255);
   const size_t err_off = nvp_off + ((sizeof(int32_t) * p->n_tiles + 255) & ~size_t(255));
-  const size_t part_off = err_off + 256;
+  const size_t aux_off = err_off + 256;
+  const size_t part_off = aux_off + ((sizeof(int32_t) * aux.size() + 255) & ~size_t(255));
   const size_t part_bytes = sizeof(float) * decode_partial_floats(p);
   const size_t total = part_off + part_bytes;
   if (cudaMalloc(&p->dev_block, total) != cudaSuccess) {
@@ -177,12 +182,14 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   p->tiles_d = reinterpret_cast<TileInfo*>(base);
   p->nvp_d = reinterpret_cast<int32_t*>(base + nvp_off);
   p->err_d = reinterpret_cast<uint32_t*>(base + err_off);
+  p->aux_d = reinterpret_cast<int32_t*>(base + aux_off);
   p->partial_d = part_bytes ? reinterpret_cast<float*>(base + part_off) : nullptr;
 
   std::vector<char> host(part_off, 0);
   memcpy(host.data(), p->tiles.data(), tiles_bytes);
   for (int t = 0; t < p->n_tiles; ++t)
     memcpy(host.data() + nvp_off + sizeof(int32_t) * t, &p->tiles[t].nvp, sizeof(int32_t));
+  if (!aux.empty()) memcpy(host.data() + aux_off, aux.data(), sizeof(int32_t) * aux.size());
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   msa_status s = cuda_check(cudaMemcpyAsync(p->dev_block, host.data(), part_off, cudaMemcpyHostToDevice, st),
                             "msa_plan: upload");

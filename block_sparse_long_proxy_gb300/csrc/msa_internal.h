@@ -54,12 +54,23 @@ struct msa_plan_s {
   uint32_t* err_d = nullptr;
   float* partial_d = nullptr;        // decode split-K partials (O, m, l)
   int32_t decode_ctas = 0;           // persistent decode grid size
+  // per-kernel work tables, one int32 array carved by offsets
+  int32_t* aux_d = nullptr;
+  int64_t proxy_units_off = 0;       // prefill proxy work units
+  int32_t n_proxy_units = 0;
+  int64_t proxy_unit_start_off = 0;  // decode proxy: first unit of each tile
+  int64_t attn_units_off = 0;        // prefill attention work units
+  int32_t n_attn_units = 0;
 };
 
 namespace msa {
 
 msa_status set_error(msa_status s, const char* fmt, ...);
 msa_status cuda_check(cudaError_t e, const char* what);
+
+// ---- plan-time tables (host), appended to the plan's aux array ----
+void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
+void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 
 // ---- launchers (each returns MSA_OK or an error with its message set) ----
 msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,

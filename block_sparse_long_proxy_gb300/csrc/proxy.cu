@@ -1,0 +1,454 @@
+// Stage 1: the proxy pass.  max_score[t, h, j] = max over rows i of tile t and
+// keys k of block j with k visible to i of pq[i,h].pk[k]/sqrt(dp), -inf where
+// nothing is visible ("MiniMax-AI/MSA" README, section "Usage": the dense
+// proxy pass with num_kv_heads=1 and output_maxscore=True; Flash-MSA
+// article, "three key differences": 128-token blocks chosen by max-pooling
+// proxy scores).  Only the logits' block maxima leave the chip: no softmax,
+// no P.V.
+//
+// Prefill kernel (tcgen05): one CTA per work unit = (tile, up to 8 proxy
+// heads, a chunk of up to 32 KV blocks).  Warp 0 streams the tile's Q slices
+// once and the paged proxy-K blocks through a 4-stage TMA ring; warp 1 issues
+// one 128x128xdp MMA per (block, head) into a ring of four 128-column TMEM
+// accumulators; warps 2-9 read each accumulator back (tcgen05.ld), apply the
+// causal mask on diagonal blocks, and reduce it to one value.  The proxy K
+// block is read once per tile and shared by all heads (there is one proxy K
+// head).
+//
+// Decode kernel (every qo_len == 1): one query row per sequence, so the pass
+// is an HBM stream over the proxy-K pages.  Each warp owns a 3-stage TMA ring
+// of pages and computes S^T = K_block . pq^T with mma.sync (M = 128 keys,
+// N = 8 heads), then a max over keys.
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+#include <algorithm>
+
+namespace msa {
+namespace {
+
+constexpr int kHeadsPerCta = 8;
+constexpr int kChunk = 32;
+constexpr int kStages = 4;
+constexpr int kNBuf = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+
+// work unit of the prefill kernel
+struct ProxyUnit {
+  int32_t tile, h0, nh, j0, j1, fill_tail, pad0, pad1;
+};
+
+__device__ __forceinline__ int32_t f2ord(float f) {
+  const int32_t b = __float_as_int(f);
+  return b ^ ((b >> 31) & 0x7FFFFFFF);
+}
+__device__ __forceinline__ float ord2f(int32_t o) { return __int_as_float(o ^ ((o >> 31) & 0x7FFFFFFF)); }
+
+template <int DP>
+struct ProxySmem {
+  static constexpr int kQBytes = 128 * DP * 2;   // one head's Q tile
+  static constexpr int kKBytes = 128 * DP * 2;   // one proxy K block
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + kHeadsPerCta * kQBytes;
+  static constexpr int kPartOff = kKOff + kStages * kKBytes;
+  static constexpr int kBarOff = kPartOff + kChunk * kHeadsPerCta * kEpiWarps * 4;
+  static constexpr int kBytes = kBarOff + 8 * (1 + 2 * kStages + 2 * kNBuf + 1) + 16;
+};
+
+template <int DP>
+__global__ void __launch_bounds__(kThreads, 1)
+    proxy_prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                         const ProxyUnit* __restrict__ units, const TileInfo* __restrict__ tiles,
+                         const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
+                         int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+  using L = ProxySmem<DP>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem + L::kQOff;
+  uint8_t* k_s = smem + L::kKOff;
+  int32_t* part = reinterpret_cast<int32_t*>(smem + L::kPartOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* k_empty = k_full + kStages;
+  uint64_t* t_full = k_empty + kStages;
+  uint64_t* t_empty = t_full + kNBuf;
+  uint64_t* drain = t_empty + kNBuf;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const ProxyUnit u = units[blockIdx.x];
+  const TileInfo tl = tiles[u.tile];
+  const int nblk = u.j1 - u.j0;
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&q_map);
+    prefetch_tmap(&k_map);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int b = 0; b < kNBuf; ++b) {
+      mbar_init(t_full + b, 1);
+      mbar_init(t_empty + b, kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      mbar_expect_tx(q_full, u.nh * L::kQBytes);
+      for (int h = 0; h < u.nh; ++h) tma_load_3d(q_s + h * L::kQBytes, &q_map, q_full, 0, u.h0 + h, tl.q_begin);
+      for (int i = 0; i < nblk; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(k_empty + s, ((i / kStages) & 1) ^ 1, err)) break;
+        int64_t page = kv_indices[tl.page_base + u.j0 + i];
+        if (page < 0 || page >= num_pages) {
+          atomicOr(err, kErrDeviceCheck);
+          page = 0;
+        }
+        mbar_expect_tx(k_full + s, L::kKBytes);
+        tma_load_2d(k_s + s * L::kKBytes, &k_map, k_full + s, 0, static_cast<int>(page * 128));
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t sw = DP == 64 ? kSwizzle128 : kSwizzle64;
+      constexpr uint32_t sbo = DP == 64 ? 1024 : 512;
+      bool ok = mbar_wait(q_full, 0, err);
+      int item = 0;
+      for (int i = 0; ok && i < nblk; ++i) {
+        const int s = i % kStages;
+        if (!(ok = mbar_wait(k_full + s, (i / kStages) & 1, err))) break;
+        tc_fence_after();
+        const uint32_t kaddr = smem_u32(k_s + s * L::kKBytes);
+        for (int h = 0; h < u.nh; ++h, ++item) {
+          const int b = item % kNBuf;
+          if (!(ok = mbar_wait(t_empty + b, ((item / kNBuf) & 1) ^ 1, err))) break;
+          tc_fence_after();
+          const uint32_t qaddr = smem_u32(q_s + h * L::kQBytes);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk)
+            mma_ss(tmem + b * 128, smem_desc(qaddr + kk * 32, 16, sbo, sw), smem_desc(kaddr + kk * 32, 16, sbo, sw),
+                   idesc, kk > 0);
+          mma_commit(t_full + b);
+        }
+        mma_commit(k_empty + s);
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, err);
+    }
+  } else {
+    // epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the columns
+    const int ew = warp - 2;
+    const int quarter = warp & 3;
+    const int half = ew >> 2;
+    const int r = quarter * 32 + lane;
+    const bool row_ok = r < tl.rows;
+    const int qpos = tl.pos0 + r;
+    int item = 0;
+    bool ok = true;
+    for (int i = 0; ok && i < nblk; ++i) {
+      const int j = u.j0 + i;
+      const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
+      const int limit = qpos - j * 128 - half * 64;  // columns c (of this half) with c <= limit are visible
+      for (int h = 0; h < u.nh; ++h, ++item) {
+        const int b = item % kNBuf;
+        if (!(ok = mbar_wait(t_full + b, (item / kNBuf) & 1, err))) break;
+        tc_fence_after();
+        uint32_t v[64];
+        const uint32_t taddr = tmem + b * 128 + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
+        tmem_ld32(taddr, v);
+        tmem_ld32(taddr + 32, v + 32);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(t_empty + b);
+        float m = -INFINITY;
+        if (!need_mask) {
+          float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
+          float m2 = __uint_as_float(v[2]), m3 = __uint_as_float(v[3]);
+#pragma unroll
+          for (int c = 4; c < 64; c += 4) {
+            m0 = fmaxf(m0, __uint_as_float(v[c]));
+            m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
+            m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
+            m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
+          }
+          m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+        } else if (row_ok) {
+#pragma unroll
+          for (int c = 0; c < 64; ++c) m = fmaxf(m, c <= limit ? __uint_as_float(v[c]) : -INFINITY);
+        }
+        if (!row_ok) m = -INFINITY;
+        const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
+        if (lane == 0) part[(i * kHeadsPerCta + h) * kEpiWarps + ew] = wm;
+      }
+    }
+    // all epilogue warps: combine the eight partial maxima of each item
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+    const int et = threadIdx.x - 64;
+    if (ok) {
+      for (int it = et; it < nblk * u.nh; it += 32 * kEpiWarps) {
+        const int h = it / nblk, i = it % nblk;
+        int32_t m = part[(i * kHeadsPerCta + h) * kEpiWarps];
+#pragma unroll
+        for (int w = 1; w < kEpiWarps; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
+        max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = ord2f(m) * scale;
+      }
+    }
+    if (u.fill_tail) {
+      const int tail = max_blocks - tl.nvp;
+      for (int it = et; it < tail * u.nh; it += 32 * kEpiWarps) {
+        const int h = it / tail, j = tl.nvp + it % tail;
+        max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + j] = -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ------------------------------------------------------------------ decode
+
+constexpr int kDecWarps = 4;
+constexpr int kDecStages = 3;
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                          uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Units are (sequence, block) pairs in order; unit_start[t] is the first unit
+// of tile (sequence) t.
+template <int DP>
+__global__ void __launch_bounds__(32 * kDecWarps)
+    proxy_decode_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ pq,
+                        const TileInfo* __restrict__ tiles, const int32_t* __restrict__ unit_start, int32_t n_tiles,
+                        const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
+                        int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+  constexpr int kBlk = 128 * DP * 2;
+  constexpr int kRowBytes = DP * 2;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + warp * kDecStages * kBlk;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecWarps * kDecStages * kBlk) + warp * kDecStages;
+
+  const int total_units = unit_start[n_tiles];
+  // -inf past each sequence's valid blocks
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       e < static_cast<int64_t>(n_tiles) * hp * max_blocks; e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(e % max_blocks);
+    const int t = static_cast<int>(e / (static_cast<int64_t>(hp) * max_blocks));
+    if (j >= tiles[t].nvp) max_score[e] = -INFINITY;
+  }
+
+  if (lane == 0) {
+    for (int s = 0; s < kDecStages; ++s) mbar_init(bars + s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int gw = blockIdx.x * kDecWarps + warp;
+  const int nw = gridDim.x * kDecWarps;
+
+  auto locate = [&](int unit, int& t, int& j) {
+    int lo = 0, hi = n_tiles - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (unit_start[mid] <= unit) lo = mid; else hi = mid - 1;
+    }
+    t = lo;
+    j = unit - unit_start[lo];
+  };
+  auto issue = [&](int k) {  // k-th unit of this warp into stage k % kDecStages
+    const int unit = gw + k * nw;
+    if (unit >= total_units) return;
+    int t, j;
+    locate(unit, t, j);
+    int64_t page = kv_indices[tiles[t].page_base + j];
+    if (page < 0 || page >= num_pages) {
+      atomicOr(err, kErrDeviceCheck);
+      page = 0;
+    }
+    uint64_t* bar = bars + (k % kDecStages);
+    mbar_expect_tx(bar, kBlk);
+    tma_load_2d(ring + (k % kDecStages) * kBlk, &k_map, bar, 0, static_cast<int>(page * 128));
+  };
+  if (lane == 0)
+    for (int k = 0; k < kDecStages; ++k) issue(k);
+
+  const int g = lane >> 2, t4 = lane & 3;
+  for (int k = 0;; ++k) {
+    const int unit = gw + k * nw;
+    if (unit >= total_units) break;
+    int t, j;
+    locate(unit, t, j);
+    const TileInfo tl = tiles[t];
+    // B fragments: pq[row, head n = g, dims]; heads >= hp contribute zeros
+    uint32_t bf[DP / 16][2];
+    const __nv_bfloat16* qrow = pq + (static_cast<int64_t>(tl.q_begin) * hp + g) * DP;
+#pragma unroll
+    for (int kt = 0; kt < DP / 16; ++kt) {
+      if (g < hp) {
+        bf[kt][0] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 2 * t4);
+        bf[kt][1] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 8 + 2 * t4);
+      } else {
+        bf[kt][0] = bf[kt][1] = 0u;
+      }
+    }
+    const int s = k % kDecStages;
+    if (!mbar_wait(bars + s, (k / kDecStages) & 1, err)) break;
+    const uint32_t base = smem_u32(ring + s * kBlk);
+    const int nkeys = min(128, tl.kv_len - j * 128);  // keys past kv_len are not visible
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kt = 0; kt < DP / 16; ++kt) {
+        const int row = mt * 16 + (lane & 15);
+        const int chunk = kt * 2 + (lane >> 4);
+        const int sw = DP == 64 ? (chunk ^ (row & 7)) : (chunk ^ ((row >> 1) & 3));
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(base + row * kRowBytes + sw * 16, a0, a1, a2, a3);
+        mma_16816(c, a0, a1, a2, a3, bf[kt][0], bf[kt][1]);
+      }
+      const int r0 = mt * 16 + g, r1 = r0 + 8;
+      if (r0 < nkeys) { mx0 = fmaxf(mx0, c[0]); mx1 = fmaxf(mx1, c[1]); }
+      if (r1 < nkeys) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
+    }
+    __syncwarp();
+    if (lane == 0) issue(k + kDecStages);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+    }
+    if (lane < 4) {
+      const int h0 = 2 * lane, h1 = 2 * lane + 1;
+      float* dst = max_score + static_cast<int64_t>(t) * hp * max_blocks + j;
+      if (h0 < hp) dst[static_cast<int64_t>(h0) * max_blocks] = mx0 * scale;
+      if (h1 < hp) dst[static_cast<int64_t>(h1) * max_blocks] = mx1 * scale;
+    }
+  }
+}
+
+}  // namespace
+
+// --------------------------------------------------------------- host side
+
+void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
+  // prefill work units, longest first
+  std::vector<ProxyUnit> us;
+  for (int t = 0; t < p->n_tiles; ++t) {
+    const int nvp = p->tiles[t].nvp;
+    for (int h0 = 0; h0 < p->hp; h0 += kHeadsPerCta)
+      for (int j0 = 0; j0 < nvp; j0 += kChunk) {
+        ProxyUnit u{};
+        u.tile = t;
+        u.h0 = h0;
+        u.nh = std::min(kHeadsPerCta, p->hp - h0);
+        u.j0 = j0;
+        u.j1 = std::min(nvp, j0 + kChunk);
+        u.fill_tail = (u.j1 == nvp) && (nvp < p->max_blocks);
+        us.push_back(u);
+      }
+  }
+  std::stable_sort(us.begin(), us.end(),
+                   [](const ProxyUnit& a, const ProxyUnit& b) { return (a.j1 - a.j0) > (b.j1 - b.j0); });
+  p->proxy_units_off = static_cast<int64_t>(aux.size());
+  p->n_proxy_units = static_cast<int32_t>(us.size());
+  const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
+  aux.insert(aux.end(), raw, raw + us.size() * (sizeof(ProxyUnit) / 4));
+  // decode: first unit of each tile
+  p->proxy_unit_start_off = static_cast<int64_t>(aux.size());
+  int32_t acc = 0;
+  for (int t = 0; t < p->n_tiles; ++t) {
+    aux.push_back(acc);
+    acc += p->tiles[t].nvp;
+  }
+  aux.push_back(acc);
+}
+
+static bool make_pk_map(CUtensorMap* m, const msa_plan_s* p, const void* pk_pages) {
+  const uint64_t dims[2] = {static_cast<uint64_t>(p->dp), static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t strides[1] = {static_cast<uint64_t>(p->dp) * 2};
+  const uint32_t box[2] = {static_cast<uint32_t>(p->dp), 128};
+  return encode_tensor_map(m, 2, pk_pages, dims, strides, box, 1, p->dp * 2);
+}
+
+msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                                float* max_score, cudaStream_t st) {
+  CUtensorMap qm, km;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(p->dp), static_cast<uint64_t>(p->hp),
+                             static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {static_cast<uint64_t>(p->dp) * 2, static_cast<uint64_t>(p->hp) * p->dp * 2};
+  const uint32_t qbox[3] = {static_cast<uint32_t>(p->dp), 1, 128};
+  if (!encode_tensor_map(&qm, 3, pq, qdims, qstr, qbox, 1, p->dp * 2) || !make_pk_map(&km, p, pk_pages))
+    return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore: tensor map encoding failed");
+  const ProxyUnit* units = reinterpret_cast<const ProxyUnit*>(p->aux_d + p->proxy_units_off);
+  const float scale = 1.0f / sqrtf(static_cast<float>(p->dp));
+  if (p->dp == 64) {
+    const int smem = ProxySmem<64>::kBytes + 1024;
+    cudaFuncSetAttribute(proxy_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    proxy_prefill_kernel<64><<<p->n_proxy_units, kThreads, smem, st>>>(
+        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
+  } else {
+    const int smem = ProxySmem<32>::kBytes + 1024;
+    cudaFuncSetAttribute(proxy_prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    proxy_prefill_kernel<32><<<p->n_proxy_units, kThreads, smem, st>>>(
+        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
+  }
+  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: prefill launch");
+}
+
+msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                               float* max_score, cudaStream_t st) {
+  if (p->hp > 8) return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore: decode path supports up to 8 proxy heads");
+  CUtensorMap km;
+  if (!make_pk_map(&km, p, pk_pages)) return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore: tensor map encoding failed");
+  const int32_t* ustart = p->aux_d + p->proxy_unit_start_off;
+  const float scale = 1.0f / sqrtf(static_cast<float>(p->dp));
+  const int grid = p->num_sms;
+  const auto* q = static_cast<const __nv_bfloat16*>(pq);
+  if (p->dp == 64) {
+    const int smem = kDecWarps * kDecStages * 128 * 64 * 2 + kDecWarps * kDecStages * 8 + 1024;
+    cudaFuncSetAttribute(proxy_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    proxy_decode_kernel<64><<<grid, 32 * kDecWarps, smem, st>>>(km, q, p->tiles_d, ustart, p->n_tiles, kv_indices,
+                                                                 p->num_pages, max_score, p->hp, p->max_blocks, scale,
+                                                                 p->err_d);
+  } else {
+    const int smem = kDecWarps * kDecStages * 128 * 32 * 2 + kDecWarps * kDecStages * 8 + 1024;
+    cudaFuncSetAttribute(proxy_decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    proxy_decode_kernel<32><<<grid, 32 * kDecWarps, smem, st>>>(km, q, p->tiles_d, ustart, p->n_tiles, kv_indices,
+                                                                 p->num_pages, max_score, p->hp, p->max_blocks, scale,
+                                                                 p->err_d);
+  }
+  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: decode launch");
+}
+
+}  // namespace msa

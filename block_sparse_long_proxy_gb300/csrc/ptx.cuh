@@ -3,6 +3,8 @@
 // instructions, plus the UMMA shared-memory and instruction descriptors.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 

@@ -48,6 +48,9 @@ Readings where the pages are silent (each is listed in the design doc):
       distributions (detached), summed over rows, weight w; the LM loss
       sends no gradient into the proxy and the KL none into main Q/K/V.
       Parity of R6's domain and mean is unpinned by the pages.
+  R7  a query row that sees no key of its tile's selected blocks (possible
+      only when a tile straddles two blocks and its earlier block is not
+      selected) has O = 0 and LSE = -inf.
 """
 from __future__ import annotations
 
@@ -249,11 +252,14 @@ def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_le
                 vmat = vmat * float(v_scale[g])
             s = q[tl.q_begin: tl.q_end, h, :] @ kmat.T / math.sqrt(d)
             s = np.where(ks[None, :] <= qpos[:, None], s, -np.inf)
-            m = s.max(axis=1, keepdims=True)
+            m = s.max(axis=1, keepdims=True) if s.shape[1] else np.full((s.shape[0], 1), -np.inf)
+            empty = np.isneginf(m)                      # R7: no visible key
+            m = np.where(empty, 0.0, m)
             e = np.exp(s - m)
             l = e.sum(axis=1, keepdims=True)
-            lse[tl.q_begin: tl.q_end, h] = (m + np.log(l))[:, 0]
-            o[tl.q_begin: tl.q_end, h, :] = (e / l) @ vmat
+            with np.errstate(divide="ignore", invalid="ignore"):
+                lse[tl.q_begin: tl.q_end, h] = np.where(empty, -np.inf, m + np.log(l))[:, 0]
+                o[tl.q_begin: tl.q_end, h, :] = np.where(empty, 0.0, (e / np.where(empty, 1.0, l)) @ vmat)
     return o, lse
 
 

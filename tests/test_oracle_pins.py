@@ -449,3 +449,18 @@ def test_kl_grad_constant_proxy_keys_is_zero():
                                inp["kv_indices"].numpy(), idx, [256], [256], synth.bits(inp["dout"]),
                                synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]))
     assert np.abs(g["dpq"]).max() < 1e-12
+
+
+def test_rows_without_visible_keys():
+    """R7: a tile straddling two blocks with only its diagonal block
+    selected leaves its early rows without keys: O = 0, LSE = -inf; the
+    other rows still match the library attention."""
+    case = synth.Case("t", [128], [200], 2, 1, 64, 1, 32, 1)   # offset 72: rows 0..55 sit in block 0
+    inp = _mk(case)
+    idx = np.array([[[1]]], dtype=np.int32)                       # diagonal block only
+    o, lse = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                                inp["kv_indices"].numpy(), idx, [128], [200])
+    early = np.arange(128) + 72 < 128
+    assert np.all(o[early] == 0.0) and np.all(np.isneginf(lse[early]))
+    ref = _dense_route(inp, case, idx)
+    np.testing.assert_allclose(o[~early], ref[~early], rtol=1e-10, atol=1e-12)

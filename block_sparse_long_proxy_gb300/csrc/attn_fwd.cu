@@ -1,0 +1,368 @@
+// Stage 3 (prefill): GQA block-sparse flash attention forward with bf16 K/V.
+//
+// For query row i of tile t and head h (group g = h / G): softmax over the
+// keys of the selected blocks kv_block_indexes[t, g, :] that are visible to
+// i, of q.k/sqrt(d); out = P.V and lse = ln sum exp ("MiniMax-AI/MSA"
+// README, section "Usage": fmha_sm100(q, k_pages, v_pages, sparse_plan,
+// kv_indices, kv_block_indexes); Flash-MSA article, "three key
+// differences": the main attention is GQA).
+//
+// One CTA per (tile, GQA group, pair of query heads of the group): both heads
+// share every K/V block the TMA producer gathers through the page table.
+// Tensor memory holds S0, S1 (128 columns each) and O0, O1 (d columns each);
+// the bf16 probabilities P_h overwrite the first 64 columns of S_h and feed
+// the P.V MMA straight from tensor memory.  Roles:
+//   warps 0-3  softmax of head 0 (thread = query row), warps 4-7 head 1,
+//   warp 8     TMA producer (Q once, then K/V blocks in a 2-stage ring),
+//   warp 9     MMA issuer: S_h = Q_h K^T (smem x smem), O_h += P_h V
+//              (tmem x smem), ordered QK0 QK1 | PV0 QK0' PV1 QK1' | ... so
+//              that one head's softmax overlaps the other head's MMAs.
+// Online softmax in the log2 domain; the O rescale runs in the softmax
+// warps between P.V steps.
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+#include <algorithm>
+
+namespace msa {
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kMaxTopk = 1024;
+
+struct AttnUnit {
+  int32_t tile, g, h0, nh;
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+  tmem_st16(taddr, r);
+  tmem_st16(taddr + 16, r + 16);
+}
+
+template <int D>
+struct AttnSmem {
+  static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16, in D/64 swizzled chunks of 16 KB
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kQOff + 2 * kTileBytes;
+  static constexpr int kVOff = kKOff + kStages * kTileBytes;
+  static constexpr int kBlkOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kBlkOff + kMaxTopk * 4;
+  static constexpr int kBytes = kBarOff + 8 * 24;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
+                    const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units,
+                    const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
+                    const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
+                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
+                    uint32_t* err) {
+  using L = AttnSmem<D>;
+  constexpr int kChunks = D / 64;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* q_s = smem + L::kQOff;
+  uint8_t* k_s = smem + L::kKOff;
+  uint8_t* v_s = smem + L::kVOff;
+  int32_t* blocks = reinterpret_cast<int32_t*>(smem + L::kBlkOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + kStages;
+  uint64_t* kv_empty = v_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;  // [2]
+  uint64_t* p_full = s_full + 2;          // [2]
+  uint64_t* o_done = p_full + 2;          // [2]
+  uint64_t* drain = o_done + 2;
+  int32_t* nblk_s = reinterpret_cast<int32_t*>(drain + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const AttnUnit u = units[blockIdx.x];
+  const TileInfo tl = tiles[u.tile];
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&q_map);
+    prefetch_tmap(&k_map);
+    prefetch_tmap(&v_map);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(v_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(s_full + h, 1);
+      mbar_init(p_full + h, 4);
+      mbar_init(o_done + h, 1);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+    // the selected blocks of this (tile, group), skipping padding
+    const int32_t* row = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
+    int n = 0;
+    for (int k = 0; k < topk; ++k) {
+      const int j = row[k];
+      if (j < 0) continue;
+      if (j >= tl.nvp) {
+        atomicOr(err, kErrDeviceCheck);
+        continue;
+      }
+      blocks[n++] = j;
+    }
+    *nblk_s = n;
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n = *nblk_s;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_expect_tx(q_full, u.nh * L::kTileBytes);
+      for (int h = 0; h < u.nh; ++h)
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_3d(q_s + h * L::kTileBytes + c * 16384, &q_map, q_full, c * 64, u.h0 + h, tl.q_begin);
+      for (int i = 0; i < n; ++i) {
+        const int s = i % kStages;
+        if (!mbar_wait(kv_empty + s, ((i / kStages) & 1) ^ 1, err)) break;
+        int64_t page = kv_indices[tl.page_base + blocks[i]];
+        if (page < 0 || page >= num_pages) {
+          atomicOr(err, kErrDeviceCheck);
+          page = 0;
+        }
+        const int row = static_cast<int>((page * hkv + u.g) * 128);
+        mbar_expect_tx(k_full + s, L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
+        mbar_expect_tx(v_full + s, L::kTileBytes);
+        for (int c = 0; c < kChunks; ++c)
+          tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, v_full + s, c * 64, row);
+      }
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      const uint32_t q0 = smem_u32(q_s), k0 = smem_u32(k_s), v0 = smem_u32(v_s);
+      auto qk = [&](int h, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + h * 128, smem_desc(q0 + h * L::kTileBytes + off, 16, 1024, kSwizzle128),
+                 smem_desc(k0 + s * L::kTileBytes + off, 16, 1024, kSwizzle128), id_qk, kk > 0);
+        }
+        mma_commit(s_full + h);
+      };
+      auto pv = [&](int h, int s, int i) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tmem + 256 + h * D, tmem + h * 128 + kk * 8,
+                 smem_desc(v0 + s * L::kTileBytes + kk * 2048, 16384, 1024, kSwizzle128), id_pv, (i > 0) || (kk > 0));
+        mma_commit(o_done + h);
+      };
+      bool ok = mbar_wait(q_full, 0, err);
+      if (ok && n > 0) {
+        ok = mbar_wait(k_full, 0, err);
+        tc_fence_after();
+        for (int h = 0; ok && h < u.nh; ++h) qk(h, 0);
+        for (int i = 0; ok && i < n; ++i) {
+          const int s = i % kStages;
+          const int s1 = (i + 1) % kStages;
+          for (int h = 0; h < u.nh; ++h) {
+            if (!(ok = mbar_wait(p_full + h, i & 1, err))) break;
+            if (h == 0 && !(ok = mbar_wait(v_full + s, (i / kStages) & 1, err))) break;
+            tc_fence_after();
+            pv(h, s, i);
+            if (h == u.nh - 1) mma_commit(kv_empty + s);
+            if (i + 1 < n) {
+              if (h == 0 && !(ok = mbar_wait(k_full + s1, ((i + 1) / kStages) & 1, err))) break;
+              tc_fence_after();
+              qk(h, s1);
+            }
+          }
+        }
+      }
+      mma_commit(drain);
+      mbar_wait(drain, 0, err);
+    }
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int h = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const bool row_ok = r < tl.rows;
+    const int qpos = tl.pos0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + h * 128;
+    const uint32_t o_addr = tmem + lane_base + 256 + h * D;
+    float m = -INFINITY, l = 0.f;
+    bool ok = h < u.nh;
+    for (int i = 0; ok && i < n; ++i) {
+      if (!(ok = mbar_wait(s_full + h, i & 1, err))) break;
+      tc_fence_after();
+      uint32_t sv[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
+      tmem_wait_ld();
+      const int j = blocks[i];
+      const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
+      float mx = -INFINITY;
+      if (need_mask) {
+        const int limit = row_ok ? qpos - j * 128 : -1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          if (c > limit) sv[c] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sv[c]));
+        }
+      } else {
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4) {
+          a0 = fmaxf(a0, __uint_as_float(sv[c]));
+          a1 = fmaxf(a1, __uint_as_float(sv[c + 1]));
+          a2 = fmaxf(a2, __uint_as_float(sv[c + 2]));
+          a3 = fmaxf(a3, __uint_as_float(sv[c + 3]));
+        }
+        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+      }
+      const float m_new = fmaxf(m, mx * scale_log2);
+      const float m_use = m_new == -INFINITY ? 0.f : m_new;
+      const float alpha = ex2_approx(m - m_use);
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -m_use));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -m_use));
+        sum0 += p0;
+        sum1 += p1;
+        pk[c] = pack_bf16x2(p0, p1);
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st16(s_addr + c * 16, pk + c * 16);
+      l = l * alpha + (sum0 + sum1);
+      // rescale O_h (written by P.V of the previous block, already complete
+      // because the S_h MMA of this block was issued after it)
+      if (i > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        if (!(ok = mbar_wait(o_done + h, (i - 1) & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(o_addr + c * 32, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full + h);
+      m = m_new;
+    }
+    if (ok && h < u.nh) {
+      if (n > 0) ok = mbar_wait(o_done + h, (n - 1) & 1, err);
+      tc_fence_after();
+      const int hg = u.h0 + h;
+      const int64_t orow = static_cast<int64_t>(tl.q_begin + r) * hq + hg;
+      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        if (n > 0) {
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ov[e] = 0u;
+        }
+        if (ok && row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow * D + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
+            dst[e] = w;
+          }
+        }
+      }
+      if (ok && row_ok && lse != nullptr)
+        lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
+  std::vector<AttnUnit> us;
+  const int grp = p->hq / p->hkv;
+  for (int t = 0; t < p->n_tiles; ++t)
+    for (int g = 0; g < p->hkv; ++g)
+      for (int h = 0; h < grp; h += 2) us.push_back(AttnUnit{t, g, g * grp + h, std::min(2, grp - h)});
+  // heaviest first: a unit visits at most min(num_valid_pages, topk) blocks
+  std::stable_sort(us.begin(), us.end(), [&](const AttnUnit& a, const AttnUnit& b) {
+    return std::min(p->tiles[a.tile].nvp, p->topk) > std::min(p->tiles[b.tile].nvp, p->topk);
+  });
+  p->attn_units_off = static_cast<int64_t>(aux.size());
+  p->n_attn_units = static_cast<int32_t>(us.size());
+  const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
+  aux.insert(aux.end(), raw, raw + us.size() * 4);
+}
+
+msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                               const int32_t* kv_indices, const int32_t* idx, void* out, float* lse,
+                               cudaStream_t st) {
+  if (p->topk > kMaxTopk) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: topk above 1024");
+  CUtensorMap qm, km, vm;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->hq),
+                             static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {static_cast<uint64_t>(p->d) * 2, static_cast<uint64_t>(p->hq) * p->d * 2};
+  const uint32_t qbox[3] = {64, 1, 128};
+  const uint64_t kdims[2] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t kstr[1] = {static_cast<uint64_t>(p->d) * 2};
+  const uint32_t kbox[2] = {64, 128};
+  if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, 1, 128))
+    return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
+  const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->attn_units_off);
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->d));
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if (p->d == 128) {
+    const int smem = AttnSmem<128>::kBytes + 1024;
+    cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<128><<<p->n_attn_units, kThreads, smem, st>>>(qm, km, vm, units, p->tiles_d, idx, kv_indices,
+                                                                   p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+                                                                   scale_log2, p->err_d);
+  } else {
+    const int smem = AttnSmem<64>::kBytes + 1024;
+    cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<64><<<p->n_attn_units, kThreads, smem, st>>>(qm, km, vm, units, p->tiles_d, idx, kv_indices,
+                                                                 p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+                                                                 scale_log2, p->err_d);
+  }
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
+}
+
+}  // namespace msa

@@ -1,16 +1,11 @@
 // Launchers not yet implemented report MSA_ERR_UNSUPPORTED.
 #include "msa_internal.h"
 namespace msa {
-msa_status launch_attn_prefill(const msa_plan_s*, const void*, const void*, const void*, const int32_t*,
-                               const int32_t*, void*, float*, cudaStream_t) {
-  return set_error(MSA_ERR_UNSUPPORTED, "attn prefill not built");
-}
 msa_status launch_attn_decode(const msa_plan_s*, const void*, const void*, const void*, const int32_t*,
                               const int32_t*, const float*, const float*, void*, float*, cudaStream_t) {
   return set_error(MSA_ERR_UNSUPPORTED, "attn decode not built");
 }
 size_t decode_partial_floats(const msa_plan_s*) { return 0; }
-void attn_plan_tables(msa_plan_s*, std::vector<int32_t>&) {}
 msa_status launch_attn_bwd(const msa_plan_s*, const void*, const void*, const void*, const int32_t*, const int32_t*,
                            const void*, const float*, const void*, const void*, const void*, float, float*, float*,
                            float*, float*, float*, cudaStream_t) {

@@ -166,7 +166,7 @@ def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=Non
         nk = min(tl.nvp * PAGE, tl.kv_len)
         keys = keys[:nk]
         qrows = pq[tl.q_begin: tl.q_end]                                       # [R, hp, dp]
-        logits = np.einsum("rhc,kc->hrk", qrows, keys) / math.sqrt(dp)          # [hp, R, nk]
+        logits = np.matmul(qrows.transpose(1, 0, 2), keys.T) / math.sqrt(dp)   # [hp, R, nk]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
         visible = np.arange(nk)[None, :] <= qpos[:, None]                       # [R, nk]
         logits = np.where(visible[None], logits, -np.inf)

@@ -1,0 +1,475 @@
+#!/usr/bin/env python
+"""Benchmark of the MSA hot path on GB300.
+
+One step = one pass of the sparse-prefill hot path over the S=32768
+workload (batch 1, 32 query / 8 KV heads, d=128, 8 proxy heads of 64, one
+shared proxy K head, 128-token pages, topk=16, identity page table,
+bf16 N(0,1) inputs): msa_proxy_maxscore -> msa_topk_select ->
+msa_sparse_attn.  The JSON line reports tokens/s of that step (value),
+the attention kernel's TFLOP/s counted on the selected blocks against the
+tensor roofline, the FP8 paged decode's HBM GB/s (32 sequences x 131072
+keys, 64/8 heads, e4m3 K/V), an end-to-end figure through host buffers,
+and the fp64 oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (the path
+needs no exchange between GPUs); value = all ranks' tokens / the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-prefill tokens/s & TFLOP/s (selected blocks) at S=32K; decode HBM GB/s"
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# dram bytes of one attention-forward launch at the 32K prefill workload from
+# an ncu capture, valid only for the kernel source it was taken on.
+# Captured on S=16384 (15424 selected tile-blocks: 248.6 MB read + 114.2 MB
+# written) and scaled by selected tile-blocks to the S=32768 launch (31808).
+NCU_TRAFFIC = {"attn_fwd.cu": {"src": "7840dac208c29e10", "bytes": int((247637248 + 114182400) * 31808 / 15424),
+                               "source": "profiles/attn_fwd_prefill.md"}}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def src_hash(name):
+    with open(os.path.join(ROOT, "block_sparse_long_proxy_gb300", "csrc", name), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out = ""
+        else:
+            self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def allreduce_max(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def oracle_sample(case, inp_cpu, n_tiles_sample, seed=0):
+    """Run the fp64 oracle's whole chain (proxy max-score, top-k, attention)
+    on a seeded sample of tiles; returns (query rows processed, seconds)."""
+    import numpy as np
+    from block_sparse_long_proxy_gb300 import synth
+    from oracle import msa_oracle as O
+    tiles = O.tiles_of(case.qo_lens, case.kv_lens)
+    rng = np.random.default_rng(seed)
+    ids = sorted(rng.choice(len(tiles), size=min(n_tiles_sample, len(tiles)), replace=False).tolist())
+    table = inp_cpu["kv_indices"].numpy()
+    nvp = O.num_valid_pages(case.qo_lens, case.kv_lens)
+    bits = {k: synth.bits(inp_cpu[k]) for k in ("pq", "pk_pages", "q", "k_pages", "v_pages")}
+    t0 = time.perf_counter()
+    ms = O.proxy_max_score(bits["pq"], bits["pk_pages"], table, case.qo_lens, case.kv_lens, tile_ids=ids)
+    idx = np.full((len(tiles), case.hkv, case.topk), -1, np.int32)
+    idx[ids] = O.topk_select(ms[ids], case.topk, nvp[ids])
+    kw = {}
+    if case.kv_dtype != "bf16":
+        kw = dict(k_scale=inp_cpu["k_scale"].numpy(), v_scale=inp_cpu["v_scale"].numpy())
+    O.sparse_attention(bits["q"], bits["k_pages"], bits["v_pages"], table, idx, case.qo_lens, case.kv_lens,
+                       tile_ids=ids, **kw)
+    dt = time.perf_counter() - t0
+    rows = sum(tiles[i].q_end - tiles[i].q_begin for i in ids)
+    return rows, dt, ids
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores, on the same workload."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from block_sparse_long_proxy_gb300 import synth
+    case = synth.prefill_32k()
+    inp = synth.make_inputs(case, device="cpu")
+    per_step_tiles = 2
+    for w in range(args.warmup):
+        oracle_sample(case, inp, per_step_tiles, seed=1000 + w)
+    rows = 0
+    secs = 0.0
+    for k in range(args.steps):
+        r, dt, _ = oracle_sample(case, inp, per_step_tiles, seed=k)
+        rows += r
+        secs += dt
+    value = rows / secs
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
+                       "proxy_heads": 8, "proxy_dim": 64, "topk": 16},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+                             "sample": "%d random query tiles of 128 rows per step through the whole oracle chain "
+                                       "(proxy max-score, top-k, attention)" % per_step_tiles},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- ours (GPU)
+
+def selected_flops(idx_cpu, case):
+    """4*T*B*d per (tile, head, selected block), counting whole blocks."""
+    n_sel = int((idx_cpu >= 0).sum())             # (tile, group, block) triples
+    return n_sel * (case.hq // case.hkv) * 4.0 * 128 * 128 * case.d, n_sel
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_setup(args)
+    from block_sparse_long_proxy_gb300 import msa, synth
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pk_info, peak_kind = peaks()
+    case = synth.prefill_32k()
+    case.seed = rank
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0])
+    ms = torch.empty((plan.n_tiles, case.hp, plan.max_blocks), dtype=torch.float32, device=dev)
+    idx = torch.empty((plan.n_tiles, case.hkv, case.topk), dtype=torch.int32, device=dev)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((plan.total_q, case.hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        if ev:
+            ev[1].record(stream)
+        msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
+        if ev:
+            ev[2].record(stream)
+        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out=out, lse=lse)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    plan.check_errors()
+    flops, n_sel = selected_flops(idx.cpu().numpy(), case)
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.zero_()                      # evict L2 between timed steps (untimed)
+            step(evs[k])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    barrier(world)
+    plan.check_errors()
+    st = [[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(3)] for k in range(args.steps)]
+    step_ms = [sum(s) for s in st]
+    total_ms = allreduce_max(sum(step_ms), world)
+    proxy_ms = statistics.mean(s[0] for s in st)
+    topk_ms = statistics.mean(s[1] for s in st)
+    attn_ms = statistics.mean(s[2] for s in st)
+    tokens = case.total_q * world * args.steps
+    value = tokens / (total_ms / 1e3)
+
+    # proxy FLOPs: causal lower triangle of 128x128 blocks per proxy head
+    proxy_flops = sum(t.nvp for t in plan_tiles(case)) * case.hp * 2.0 * 128 * 128 * case.dp
+    attn_tflops = flops / (attn_ms / 1e3) / 1e12
+    proxy_tflops = proxy_flops / (proxy_ms / 1e3) / 1e12
+    peak_bf16 = pk_info.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    traffic = NCU_TRAFFIC.get("attn_fwd.cu")
+    if traffic and traffic.get("src") != src_hash("attn_fwd.cu"):
+        traffic = None
+    roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel<128> (msa_sparse_attn)", "achieved": attn_tflops,
+                "peak": peak_bf16, "unit": "TFLOP/s", "frac": attn_tflops / peak_bf16,
+                "traffic": traffic["bytes"] if traffic else None,
+                "peak_kind": "%s bf16 dense burst (cuBLAS)" % peak_kind,
+                "flops_per_launch": flops, "selected_blocks": n_sel,
+                "nominal_frac": attn_tflops / 2250.0}
+
+    # end to end through host buffers: H2D of every input, the step, D2H of out
+    names = ["q", "k_pages", "v_pages", "pq", "pk_pages", "kv_indices"]
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = out_host.numel() * out_host.element_size()
+    e2e_steps = max(1, min(args.steps, 5))
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        for n in names:
+            inp[n].copy_(host[n], non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = allreduce_max(e0.elapsed_time(e1), world)
+    e2e_value = case.total_q * world * e2e_steps / (e2e_ms / 1e3)
+
+    decode = bench_decode(args, dev, pk_info, peak_kind, world)
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
+                       "proxy_heads": 8, "proxy_dim": 64, "topk": 16, "page_size": 128,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "flushed between timed steps (256 MiB write)"},
+            "stages_ms": {"proxy_maxscore": proxy_ms, "topk_select": topk_ms, "sparse_attn": attn_ms},
+            "tflops_selected": attn_tflops, "proxy_tflops": proxy_tflops,
+            "roofline": roofline,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk.summary(),
+            "wall_s": t_wall}
+    if decode:
+        line["decode"] = decode
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def _tiles_nvp(case):
+    """num_valid_pages of every tile (bottom-right causal, 128-row tiles)."""
+    out = []
+    for ql, kl in zip(case.qo_lens, case.kv_lens):
+        off = kl - ql
+        for t in range((ql + 127) // 128):
+            r1 = min((t + 1) * 128, ql)
+            out.append((off + r1 - 1) // 128 + 1)
+    return out
+
+
+class _T:
+    def __init__(self, nvp):
+        self.nvp = nvp
+
+
+def plan_tiles(case):
+    return [_T(n) for n in _tiles_nvp(case)]
+
+
+def cpu_baseline(case):
+    import torch
+    from block_sparse_long_proxy_gb300 import synth
+    inp = synth.make_inputs(case, device="cpu")
+    rows, dt, ids = oracle_sample(case, inp, 1, seed=123)      # calibrate
+    n = max(1, min(64, int(15.0 / max(dt, 1e-3))))
+    rows, dt, ids = oracle_sample(case, inp, n, seed=7)
+    return {"value": rows / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": "%d random 128-row query tiles of the same workload through the whole fp64 oracle chain "
+                      "(proxy max-score, top-k, attention), %.1f s" % (len(ids), dt)}
+
+
+def bench_decode(args, dev, pk_info, peak_kind, world):
+    """FP8 paged sparse decode: HBM GB/s of msa_sparse_attn on its selected
+    K/V blocks (32 x 131072 keys, 64/8 heads, topk 16)."""
+    import torch
+    from block_sparse_long_proxy_gb300 import msa, synth
+    case = synth.paged_decode()
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype="e4m3")
+    try:
+        ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+        idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+        out = torch.empty_like(inp["q"])
+        lse = torch.empty((plan.total_q, case.hq), dtype=torch.float32, device=dev)
+
+        def attn():
+            plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx,
+                             k_scale=inp["k_scale"], v_scale=inp["v_scale"], out=out, lse=lse)
+        attn()
+    except msa.MsaError as e:
+        return {"unavailable": str(e)}
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    n_sel = int((idx >= 0).sum().item())
+    kv_bytes = n_sel * 2 * 128 * case.d          # e4m3 K and V of each selected (seq, group, block)
+    io_bytes = 2 * out.numel() * 2 + lse.numel() * 4
+    reps = max(10, args.steps)
+    times, ptimes = [], []
+    for _ in range(3):
+        attn()
+    for _ in range(reps):
+        flush.zero_()
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        b.record(stream)
+        attn()
+        c.record(stream)
+        torch.cuda.synchronize()
+        ptimes.append(a.elapsed_time(b))
+        times.append(b.elapsed_time(c))
+    t = statistics.median(times) / 1e3
+    tp = statistics.median(ptimes) / 1e3
+    gbs = (kv_bytes + io_bytes) / t / 1e9
+    proxy_bytes = sum((k + 127) // 128 for k in case.kv_lens) * 128 * case.dp * 2
+    hbm = pk_info.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    return {"workload": case.name, "sparse_attn_us": t * 1e6, "hbm_gbs": gbs, "bytes": kv_bytes + io_bytes,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "peak_kind": "%s HBM copy" % peak_kind, "nominal_frac": gbs / 8000.0},
+            "proxy_scan_us": tp * 1e6, "proxy_scan_gbs": proxy_bytes / tp / 1e9,
+            "proxy_scan_frac": proxy_bytes / tp / 1e9 / hbm}
+
+
+def run_ncu_case(args):
+    """A small case of one kernel for profiler captures (no JSON line):
+    inputs above the 129 MB L2 but a few hundred MB on the device.
+      attn / proxy / topk: sparse prefill S=16384 (32q/8kv, d=128, topk 16)
+      decode: FP8 paged decode, 32 sequences x 16384 keys."""
+    import torch
+    from block_sparse_long_proxy_gb300 import msa, synth
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda:0")
+    if args.ncu_case == "decode":
+        case = synth.Case("decode 32x16384 fp8", [1] * 32, [16384] * 32, 64, 8, 128, 8, 64, 16, kv_dtype="e4m3",
+                          page_perm_seed=1)
+    else:
+        case = synth.Case("prefill S=16384", [16384], [16384], 32, 8, 128, 8, 64, 16)
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    kw = {}
+    if case.kv_dtype != "bf16":
+        kw = dict(k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    for _ in range(args.steps):
+        if args.ncu_case in ("proxy", "decode"):
+            plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        if args.ncu_case == "topk":
+            msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
+        if args.ncu_case in ("attn", "decode"):
+            plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, **kw)
+    torch.cuda.synchronize()
+    plan.check_errors()
+    print("ncu case %s done: %d launches" % (args.ncu_case, args.steps))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--ncu-case", choices=["attn", "proxy", "topk", "decode"], default=None,
+                    help="run a small case of one kernel for a profiler capture and exit")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.ncu_case:
+        run_ncu_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

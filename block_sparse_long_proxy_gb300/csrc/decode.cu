@@ -1,0 +1,457 @@
+// Stage 3 (decode): paged sparse attention with FP8 e4m3 K/V, one query row
+// per sequence ("MiniMax-AI/MSA" README, section "Stacks": paged FP8 decode
+// next to the BF16 sparse prefill).  For each sequence and query head h of
+// group g: softmax over the keys of the blocks kv_block_indexes[t, g, :] of
+// q.(k_code*k_scale[g])/sqrt(d); out = P.(v_code*v_scale[g]).
+//
+// The work is HBM-bound (every selected block is read once; 8 query heads
+// share it), so the kernel is a stream over (tile, group, slot) units:
+// CTA c takes a contiguous range of units, a producer warp gathers each
+// selected block's K and V page (16 KB each at d = 128) through a 3-stage
+// TMA ring with 128-byte swizzle, and four consumer warps each take 32 of
+// the block's 128 keys.  Tensor cores via mma.sync (f16 in, f32 out):
+//   S^T = K . q^T     M = keys, N = 8 heads, K = d   (e4m3 -> f16 in registers)
+//   O^T += V^T . P^T  M = d,    N = 8 heads, K = keys (P^T by movmatrix)
+// The d index of both products is permuted so that every shared-memory
+// read is one conflict-free 32-bit word; the output is un-permuted on store.
+// Each warp keeps its own online-softmax state (m, l, O); the four warps'
+// states are merged in shared memory whenever the CTA's range leaves a
+// (tile, group) row, giving one partial per row segment.  A second kernel
+// merges the (at most a few) segments of each row, applies v_scale and
+// writes out and lse.
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+namespace msa {
+namespace {
+
+constexpr int kD = 128;                 // head dim of this kernel
+constexpr int kCWarps = 4;              // consumer warps
+constexpr int kDThreads = 32 * (kCWarps + 1);
+constexpr int kDStages = 2;
+constexpr int kBlk = 128 * kD;          // bytes of one e4m3 K (or V) block
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
+  uint32_t r;
+  const uint16_t h = static_cast<uint16_t>(v16 & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(h));
+  return r;
+}
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+  uint32_t r;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_f16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+// byte offset of (row, byte col) in a 128-row x 128-byte tile written by TMA
+// with 128-byte swizzle: the 16-byte chunk index is XORed with row % 8.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return row * 128 + ((((col >> 4) ^ row) & 7) << 4) + (col & 15);
+}
+
+// first unit of CTA c when U units are cut into C near-equal ranges
+__host__ __device__ __forceinline__ int range_start(int c, int U, int C) {
+  const int q = U / C, r = U % C;
+  return c * q + (c < r ? c : r);
+}
+__device__ __forceinline__ bool is_range_start(int u, int U, int C) {
+  const int q = U / C, r = U % C;
+  if (u < r * (q + 1)) return u % (q + 1) == 0;
+  return q > 0 && (u - r * (q + 1)) % q == 0;
+}
+
+template <int NT>
+struct DecodeSmem {
+  static constexpr int kRingOff = 0;
+  static constexpr int kScratchOff = kDStages * 2 * kBlk;
+  static constexpr int kScratchFloats = kCWarps * 8 * NT * (kD + 2);
+  static constexpr int kBarOff = kScratchOff + kScratchFloats * 4;
+  static constexpr int kBytes = kBarOff + 8 * 2 * kDStages;
+};
+
+template <int NT>  // n-tiles of 8 heads: group size G <= 8*NT
+__global__ void __launch_bounds__(kDThreads)
+    decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                  const __nv_bfloat16* __restrict__ q, const TileInfo* __restrict__ tiles,
+                  const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
+                  const float* __restrict__ k_scale, float* __restrict__ part_o, float* __restrict__ part_ml,
+                  int32_t n_units, int32_t hq, int32_t hkv, int32_t topk, float scale_log2, uint32_t* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  using L = DecodeSmem<NT>;
+  constexpr int kSlots = 8 * NT;  // head slots of the per-warp scratch
+  uint8_t* ring = smem + L::kRingOff;
+  float* scratch = reinterpret_cast<float*>(smem + L::kScratchOff);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* empty = full + kDStages;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = hq / hkv;
+  const int ub = range_start(blockIdx.x, n_units, gridDim.x);
+  const int ue = range_start(blockIdx.x + 1, n_units, gridDim.x);
+
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&k_map);
+    prefetch_tmap(&v_map);
+    for (int s = 0; s < kDStages; ++s) {
+      mbar_init(full + s, 1);
+      mbar_init(empty + s, kCWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kCWarps) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int i = 0;
+      for (int u = ub; u < ue; ++u) {
+        const int row = u / topk;
+        const int t = row / hkv, g = row % hkv;
+        const int j = idx[u];
+        const TileInfo tl = tiles[t];
+        if (j < 0 || j >= tl.nvp) continue;
+        const int s = i % kDStages;
+        if (!mbar_wait(empty + s, ((i / kDStages) & 1) ^ 1, err)) break;
+        int64_t page = kv_indices[tl.page_base + j];
+        if (page < 0 || page >= num_pages) {
+          atomicOr(err, kErrDeviceCheck);
+          page = 0;
+        }
+        const int r = static_cast<int>((page * hkv + g) * 128);
+        mbar_expect_tx(full + s, 2 * kBlk);
+        tma_load_2d(ring + s * 2 * kBlk, &k_map, full + s, 0, r);
+        tma_load_2d(ring + s * 2 * kBlk + kBlk, &v_map, full + s, 0, r);
+        ++i;
+      }
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int gi = lane >> 2, t4 = lane & 3;
+  const int w = warp;
+  int cur_row = -1, seg = 0, i = 0;
+  float m[NT][2], l[NT][2], oacc[8][NT][4];
+  uint32_t qf[NT][kD / 16][2];
+  float sl2 = 0.f;
+  int qpos = 0;
+  bool ok = true;
+
+  auto flush = [&](int row, int slot) {
+    // per-warp totals of l (sum over the 8 key lanes of each head column)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float v = l[nt][c];
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 4);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 8);
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
+        l[nt][c] = v;
+      }
+    float* wsc = scratch + w * kSlots * (kD + 2);  // [head][kD + 2]: O, m, l
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = 8 * nt + 2 * t4 + c;
+        if (h < G) {
+          if (gi == 0) {
+            wsc[h * (kD + 2) + kD] = m[nt][c];
+            wsc[h * (kD + 2) + kD + 1] = l[nt][c];
+          }
+#pragma unroll
+          for (int md = 0; md < 8; ++md) {
+            const int d0 = 32 * (md >> 1) + 4 * gi + 2 * (md & 1);
+            wsc[h * (kD + 2) + d0] = oacc[md][nt][c];
+            wsc[h * (kD + 2) + d0 + 1] = oacc[md][nt][2 + c];
+          }
+        }
+      }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+    for (int e = threadIdx.x; e < G * kD; e += 32 * kCWarps) {
+      const int h = e / kD, d = e % kD;
+      float mm = -INFINITY;
+#pragma unroll
+      for (int ww = 0; ww < kCWarps; ++ww) mm = fmaxf(mm, scratch[(ww * kSlots + h) * (kD + 2) + kD]);
+      float L = 0.f, o = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < kCWarps; ++ww) {
+        const float* p = scratch + (ww * kSlots + h) * (kD + 2);
+        const float sc = p[kD] == -INFINITY ? 0.f : ex2_approx(p[kD] - mm);
+        L += p[kD + 1] * sc;
+        o += p[d] * sc;
+      }
+      const int64_t base = static_cast<int64_t>(slot) * G + h;
+      part_o[base * kD + d] = o;
+      if (d == 0) {
+        part_ml[base * 2] = mm;
+        part_ml[base * 2 + 1] = L;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+    (void)row;
+  };
+
+  for (int u = ub; u < ue; ++u) {
+    const int row = u / topk;
+    const int t = row / hkv, g = row % hkv;
+    if (row != cur_row) {
+      if (cur_row >= 0) flush(cur_row, seg);
+      cur_row = row;
+      seg = u;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        m[nt][0] = m[nt][1] = -INFINITY;
+        l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+        for (int md = 0; md < 8; ++md) oacc[md][nt][0] = oacc[md][nt][1] = oacc[md][nt][2] = oacc[md][nt][3] = 0.f;
+      }
+      const TileInfo tl = tiles[t];
+      qpos = tl.pos0;
+      sl2 = scale_log2 * k_scale[g];
+      // q^T fragments: head n = gi + 8nt of the group, d = 16kc + 4t4 + {0,1} | {2,3}
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int hl = gi + 8 * nt;
+        const __nv_bfloat16* qr = q + (static_cast<int64_t>(tl.q_begin) * hq + g * G + hl) * kD;
+#pragma unroll
+        for (int kc = 0; kc < kD / 16; ++kc) {
+          if (hl < G) {
+            const uint2 v = *reinterpret_cast<const uint2*>(qr + kc * 16 + 4 * t4);
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+            const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+            qf[nt][kc][0] = pack_f16x2(f0.x, f0.y);
+            qf[nt][kc][1] = pack_f16x2(f1.x, f1.y);
+          } else {
+            qf[nt][kc][0] = qf[nt][kc][1] = 0u;
+          }
+        }
+      }
+    }
+    const int j = idx[u];
+    if (j < 0 || j >= tiles[t].nvp) {
+      if (j >= 0 && w == 0 && lane == 0) atomicOr(err, kErrDeviceCheck);
+      continue;
+    }
+    const int s = i % kDStages;
+    if (!ok || !(ok = mbar_wait(full + s, (i / kDStages) & 1, err))) continue;  // after a timeout: no compute,
+    ++i;                                                                          // but every flush still runs
+    const uint32_t kb = smem_u32(ring + s * 2 * kBlk);
+    const uint32_t vb = kb + kBlk;
+
+    // S^T for this warp's 32 keys
+    float sacc[2][NT][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) sacc[mt][nt][0] = sacc[mt][nt][1] = sacc[mt][nt][2] = sacc[mt][nt][3] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int ra = 32 * w + 16 * mt + gi, rb = ra + 8;
+#pragma unroll
+      for (int kc = 0; kc < kD / 16; ++kc) {
+        const uint32_t wa = lds32(kb + swz(ra, kc * 16 + 4 * t4));
+        const uint32_t wb = lds32(kb + swz(rb, kc * 16 + 4 * t4));
+        const uint32_t a0 = e4m3x2_to_f16x2(wa), a1 = e4m3x2_to_f16x2(wb);
+        const uint32_t a2 = e4m3x2_to_f16x2(wa >> 16), a3 = e4m3x2_to_f16x2(wb >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_f16(sacc[mt][nt], a0, a1, a2, a3, qf[nt][kc][0], qf[nt][kc][1]);
+      }
+    }
+    // mask keys past the query position, scale into the log2 domain
+    const int kpos0 = j * 128 + 32 * w + gi;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const bool va = kpos0 + 16 * mt <= qpos, vb2 = kpos0 + 16 * mt + 8 <= qpos;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        sacc[mt][nt][0] = va ? sacc[mt][nt][0] * sl2 : -INFINITY;
+        sacc[mt][nt][1] = va ? sacc[mt][nt][1] * sl2 : -INFINITY;
+        sacc[mt][nt][2] = vb2 ? sacc[mt][nt][2] * sl2 : -INFINITY;
+        sacc[mt][nt][3] = vb2 ? sacc[mt][nt][3] * sl2 : -INFINITY;
+      }
+    }
+    // online softmax per head column
+    uint32_t pb[2][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      float alpha[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float mx = fmaxf(fmaxf(sacc[0][nt][c], sacc[0][nt][2 + c]), fmaxf(sacc[1][nt][c], sacc[1][nt][2 + c]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
+        const float m_new = fmaxf(m[nt][c], mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        alpha[c] = ex2_approx(m[nt][c] - m_use);
+        m[nt][c] = m_new;
+        float sum = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          sacc[mt][nt][c] = ex2_approx(sacc[mt][nt][c] - m_use);
+          sacc[mt][nt][2 + c] = ex2_approx(sacc[mt][nt][2 + c] - m_use);
+          sum += sacc[mt][nt][c] + sacc[mt][nt][2 + c];
+        }
+        l[nt][c] = l[nt][c] * alpha[c] + sum;
+      }
+#pragma unroll
+      for (int md = 0; md < 8; ++md) {
+        oacc[md][nt][0] *= alpha[0];
+        oacc[md][nt][2] *= alpha[0];
+        oacc[md][nt][1] *= alpha[1];
+        oacc[md][nt][3] *= alpha[1];
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        pb[mt][nt][0] = movmatrix_t(pack_f16x2(sacc[mt][nt][0], sacc[mt][nt][1]));
+        pb[mt][nt][1] = movmatrix_t(pack_f16x2(sacc[mt][nt][2], sacc[mt][nt][3]));
+      }
+    }
+    // O^T += V^T P^T over this warp's 32 keys
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+      const int r0 = 32 * w + 16 * mt + 2 * t4;
+#pragma unroll
+      for (int qg = 0; qg < kD / 32; ++qg) {
+        const int col = 32 * qg + 4 * gi;
+        const uint32_t w0 = lds32(vb + swz(r0, col)), w1 = lds32(vb + swz(r0 + 1, col));
+        const uint32_t w2 = lds32(vb + swz(r0 + 8, col)), w3 = lds32(vb + swz(r0 + 9, col));
+        const uint32_t x01 = prmt(w0, w1, 0x5140), x23 = prmt(w2, w3, 0x5140);
+        const uint32_t y01 = prmt(w0, w1, 0x7362), y23 = prmt(w2, w3, 0x7362);
+        const uint32_t a0 = e4m3x2_to_f16x2(x01), a1 = e4m3x2_to_f16x2(x01 >> 16);
+        const uint32_t a2 = e4m3x2_to_f16x2(x23), a3 = e4m3x2_to_f16x2(x23 >> 16);
+        const uint32_t b0 = e4m3x2_to_f16x2(y01), b1 = e4m3x2_to_f16x2(y01 >> 16);
+        const uint32_t b2 = e4m3x2_to_f16x2(y23), b3 = e4m3x2_to_f16x2(y23 >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_f16(oacc[2 * qg][nt], a0, a1, a2, a3, pb[mt][nt][0], pb[mt][nt][1]);
+          mma_f16(oacc[2 * qg + 1][nt], b0, b1, b2, b3, pb[mt][nt][0], pb[mt][nt][1]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty + s);
+  }
+  if (cur_row >= 0) flush(cur_row, seg);
+}
+
+// Merge the segment partials of each (tile, group) row; apply v_scale.
+__global__ void __launch_bounds__(128)
+    decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                          const TileInfo* __restrict__ tiles, const float* __restrict__ v_scale,
+                          __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t n_units, int32_t n_ctas,
+                          int32_t hq, int32_t hkv, int32_t topk) {
+  const int row = blockIdx.x;
+  const int t = row / hkv, g = row % hkv;
+  const int G = hq / hkv;
+  const int u0 = row * topk, u1 = u0 + topk;
+  const TileInfo tl = tiles[t];
+  const float vs = v_scale[g];
+  for (int e = threadIdx.x; e < G * kD; e += blockDim.x) {
+    const int h = e / kD, d = e % kD;
+    float mm = -INFINITY;
+    for (int u = u0; u < u1; ++u)
+      if (u == u0 || is_range_start(u, n_units, n_ctas)) mm = fmaxf(mm, part_ml[(static_cast<int64_t>(u) * G + h) * 2]);
+    float L = 0.f, o = 0.f;
+    if (mm != -INFINITY) {
+      for (int u = u0; u < u1; ++u) {
+        if (!(u == u0 || is_range_start(u, n_units, n_ctas))) continue;
+        const int64_t b = static_cast<int64_t>(u) * G + h;
+        const float ms = part_ml[b * 2];
+        if (ms == -INFINITY) continue;
+        const float sc = ex2_approx(ms - mm);
+        L += part_ml[b * 2 + 1] * sc;
+        o += part_o[b * kD + d] * sc;
+      }
+    }
+    const int64_t orow = static_cast<int64_t>(tl.q_begin) * hq + g * G + h;
+    out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? o / L * vs : 0.f);
+    if (d == 0 && lse != nullptr) lse[orow] = L > 0.f ? (mm + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+int decode_grid(const msa_plan_s* p, int n_units) {
+  const int per_sm = (p->hq / p->hkv) <= 8 ? 2 : 1;
+  return std::max(1, std::min(n_units, p->num_sms * per_sm));
+}
+
+}  // namespace
+
+size_t decode_partial_floats(const msa_plan_s* p) {
+  if (!p->decode) return 0;
+  const size_t units = static_cast<size_t>(p->n_tiles) * p->hkv * p->topk;
+  const size_t g = p->hq / p->hkv;
+  return units * g * (kD + 2);
+}
+
+msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                              const int32_t* kv_indices, const int32_t* idx, const float* k_scale,
+                              const float* v_scale, void* out, float* lse, cudaStream_t st) {
+  if (p->d != kD) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs head_dim 128");
+  if (p->hq / p->hkv > 16) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs G <= 16");
+  CUtensorMap km, vm;
+  const uint64_t dims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t str[1] = {static_cast<uint64_t>(kD)};
+  const uint32_t box[2] = {static_cast<uint32_t>(kD), 128};
+  if (!encode_tensor_map(&km, 2, k_pages, dims, str, box, 0, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, dims, str, box, 0, 128))
+    return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
+  const int n_units = p->n_tiles * p->hkv * p->topk;
+  const int grid = decode_grid(p, n_units);
+  const size_t units = static_cast<size_t>(n_units);
+  const int G = p->hq / p->hkv;
+  float* part_o = p->partial_d;
+  float* part_ml = p->partial_d + units * G * kD;
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
+  const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  if (G <= 8) {
+    const int smem = DecodeSmem<1>::kBytes + 1024;
+    cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
+                                                     part_o, part_ml, n_units, p->hq, p->hkv, p->topk, scale_log2,
+                                                     p->err_d);
+  } else {
+    const int smem = DecodeSmem<2>::kBytes + 1024;
+    cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
+                                                     part_o, part_ml, n_units, p->hq, p->hkv, p->topk, scale_log2,
+                                                     p->err_d);
+  }
+  msa_status s = cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
+  if (s != MSA_OK) return s;
+  decode_combine_kernel<<<p->n_tiles * p->hkv, 128, 0, st>>>(part_o, part_ml, p->tiles_d, v_scale,
+                                                             static_cast<__nv_bfloat16*>(out), lse, n_units, grid,
+                                                             p->hq, p->hkv, p->topk);
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode combine launch");
+}
+
+}  // namespace msa

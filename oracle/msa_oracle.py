@@ -154,18 +154,18 @@ def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=Non
     pk: [P, 1, 128, dp] bf16 bits (one shared proxy K head, [README]
     "num_kv_heads=1").  Returns float32 [n_tiles, Hp, nb_max]; tiles not in
     tile_ids stay -inf."""
-    pq = bf16_to_f64(pq_bits)
-    pk = bf16_to_f64(pk_bits)
+    # bit patterns are decoded per tile (the decode is exact), so that large
+    # page pools never need a float64 copy
+    pq_bits, pk_bits = np.asarray(pq_bits), np.asarray(pk_bits)
     tiles = tiles_of(qo_lens, kv_lens)
     indptr = kv_indptr(kv_lens)
-    hp, dp = pq.shape[1], pq.shape[2]
+    hp, dp = pq_bits.shape[1], pq_bits.shape[2]
     out = np.full((len(tiles), hp, max_blocks(kv_lens)), -np.inf, dtype=np.float64)
     for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
         tl = tiles[ti]
-        keys = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]   # [kv_len, dp]
         nk = min(tl.nvp * PAGE, tl.kv_len)
-        keys = keys[:nk]
-        qrows = pq[tl.q_begin: tl.q_end]                                       # [R, hp, dp]
+        keys = bf16_to_f64(gather_seq(pk_bits, kv_indices, indptr, tl.seq, tl.kv_len)[:nk, 0, :])  # [nk, dp]
+        qrows = bf16_to_f64(pq_bits[tl.q_begin: tl.q_end])                     # [R, hp, dp]
         logits = np.matmul(qrows.transpose(1, 0, 2), keys.T) / math.sqrt(dp)   # [hp, R, nk]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
         visible = np.arange(nk)[None, :] <= qpos[:, None]                       # [R, nk]
@@ -227,30 +227,30 @@ def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_le
     per-KV-head scales when k_scale/v_scale are given.  Returns (O, LSE) in
     float64; rows of tiles not in tile_ids are NaN."""
     fp8 = k_scale is not None
-    q = bf16_to_f64(q_bits)
-    kp = _decode_kv(k_bits, fp8)
-    vp = _decode_kv(v_bits, fp8)
+    q_bits, k_bits, v_bits = np.asarray(q_bits), np.asarray(k_bits), np.asarray(v_bits)
     tiles = tiles_of(qo_lens, kv_lens)
     indptr = kv_indptr(kv_lens)
-    hq, d = q.shape[1], q.shape[2]
-    hkv = kp.shape[1]
+    hq, d = q_bits.shape[1], q_bits.shape[2]
+    hkv = k_bits.shape[1]
     grp = hq // hkv
-    o = np.full(q.shape, np.nan)
-    lse = np.full(q.shape[:2], np.nan)
+    o = np.full(q_bits.shape, np.nan)
+    lse = np.full(q_bits.shape[:2], np.nan)
     for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
         tl = tiles[ti]
-        kseq = gather_seq(kp, kv_indices, indptr, tl.seq, tl.kv_len)
-        vseq = gather_seq(vp, kv_indices, indptr, tl.seq, tl.kv_len)
+        # only the selected keys' bit patterns are decoded (exactly)
+        kseq = gather_seq(k_bits, kv_indices, indptr, tl.seq, tl.kv_len)
+        vseq = gather_seq(v_bits, kv_indices, indptr, tl.seq, tl.kv_len)
+        qt = bf16_to_f64(q_bits[tl.q_begin: tl.q_end])
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
         for h in range(hq):
             g = h // grp
             ks = _selected_keys(tl, kv_block_indexes[ti, g])
-            kmat = kseq[ks, g, :]
-            vmat = vseq[ks, g, :]
+            kmat = _decode_kv(kseq[ks, g, :], fp8)
+            vmat = _decode_kv(vseq[ks, g, :], fp8)
             if fp8:
                 kmat = kmat * float(k_scale[g])
                 vmat = vmat * float(v_scale[g])
-            s = q[tl.q_begin: tl.q_end, h, :] @ kmat.T / math.sqrt(d)
+            s = qt[:, h, :] @ kmat.T / math.sqrt(d)
             s = np.where(ks[None, :] <= qpos[:, None], s, -np.inf)
             m = s.max(axis=1, keepdims=True) if s.shape[1] else np.full((s.shape[0], 1), -np.inf)
             empty = np.isneginf(m)                      # R7: no visible key

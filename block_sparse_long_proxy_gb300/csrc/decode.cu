@@ -25,6 +25,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <mutex>
 
 namespace msa {
 namespace {
@@ -455,3 +456,170 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
 }
 
 }  // namespace msa
+
+// ---------------------------------------------------------------------------
+// Allocation-free FP8 decode (msa_sparse_decode_noalloc).
+//
+// Some callers cannot allocate device memory at the time they decode: a
+// serving process that hands all of the GPU's memory to its own pool at
+// start-up, or a decode loop that must not pay for cudaMalloc's implicit
+// synchronisation.  Such a caller cannot create a plan (msa_plan
+// allocates), so this entry point takes the batch description as device
+// arrays and keeps every piece of scratch -- the tile table and the split-K
+// partials of the decode kernel above -- in one file-scope device array of
+// fixed size, which every GPU that loads libmsa holds until the process
+// exits.  Its device address is fetched once per device with
+// cudaGetSymbolAddress; host code never hands the symbol itself to a kernel.
+// ---------------------------------------------------------------------------
+
+namespace msa {
+
+constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
+constexpr int kStaticMaxBatch = 4096;
+constexpr size_t kStaticTilesBytes = sizeof(TileInfo) * kStaticMaxBatch;
+constexpr size_t kStaticErrOff = kStaticTilesBytes;
+constexpr size_t kStaticPartOff = kStaticTilesBytes + 256;
+
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+namespace {
+
+struct StaticDevice {
+  unsigned char* base = nullptr;  // device address of g_decode_scratch on this device
+  int num_sms = 0;
+  bool ready = false;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+StaticDevice g_static[kMaxDevices];
+
+// One-time set-up per device, run with that device current.
+msa_status static_scratch(StaticDevice* out) {
+  int dev = -1;
+  msa_status s = cuda_check(cudaGetDevice(&dev), "msa_sparse_decode_noalloc: cudaGetDevice");
+  if (s != MSA_OK) return s;
+  if (dev < 0 || dev >= kMaxDevices)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_decode_noalloc: device index %d above %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  StaticDevice& sd = g_static[dev];
+  if (!sd.ready) {
+    void* ptr = nullptr;
+    s = cuda_check(cudaGetSymbolAddress(&ptr, g_decode_scratch), "msa_sparse_decode_noalloc: cudaGetSymbolAddress");
+    if (s != MSA_OK) return s;
+    int sms = 0;
+    s = cuda_check(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev),
+                   "msa_sparse_decode_noalloc: SM count");
+    if (s != MSA_OK) return s;
+    sd.base = static_cast<unsigned char*>(ptr);
+    sd.num_sms = sms;
+    sd.ready = true;
+  }
+  *out = sd;
+  return MSA_OK;
+}
+
+// Tile table of a decode batch (one query row per sequence) from device
+// kv_lens / kv_indptr.  A sequence whose page range is shorter than its
+// kv_len needs gets no valid blocks and raises the device-check bit.
+__global__ void decode_tiles_kernel(const int32_t* __restrict__ kv_lens, const int32_t* __restrict__ kv_indptr,
+                                    int32_t batch, TileInfo* __restrict__ tiles, uint32_t* err) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= batch) return;
+  TileInfo ti;
+  const int kl = kv_lens[t];
+  const int base = kv_indptr[t], next = kv_indptr[t + 1];
+  ti.seq = t;
+  ti.q_begin = t;
+  ti.rows = 1;
+  ti.kv_len = kl;
+  ti.pos0 = kl - 1;
+  ti.nvp = kl >= 1 ? (kl + 127) / 128 : 0;
+  ti.page_base = base;
+  ti.pad = 0;
+  if (kl < 1 || next - base < ti.nvp) {
+    atomicOr(err, kErrDeviceCheck);
+    ti.nvp = 0;
+  }
+  tiles[t] = ti;
+}
+
+}  // namespace
+}  // namespace msa
+
+using namespace msa;
+
+extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                                const int32_t* kv_lens, const int32_t* kv_indptr,
+                                                const int32_t* kv_indices, const int32_t* kv_block_indexes,
+                                                const float* k_scale, const float* v_scale, int32_t batch,
+                                                int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                int32_t topk, int64_t num_pages, void* out, float* lse,
+                                                uint32_t* err_word, msa_stream_t stream) {
+  const char* fn = "msa_sparse_decode_noalloc";
+  if (!q || !k_pages || !v_pages || !kv_lens || !kv_indptr || !kv_indices || !kv_block_indexes || !k_scale ||
+      !v_scale || !out)
+    return set_error(MSA_ERR_INVALID_ARG, "%s: NULL argument", fn);
+  if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_pages) | reinterpret_cast<uintptr_t>(v_pages) |
+       reinterpret_cast<uintptr_t>(out)) & 15u)
+    return set_error(MSA_ERR_INVALID_ARG, "%s: q, k_pages, v_pages, out must be 16-byte aligned", fn);
+  if (batch < 1 || batch > kStaticMaxBatch)
+    return set_error(MSA_ERR_INVALID_ARG, "%s: batch %d outside [1, %d]", fn, batch, kStaticMaxBatch);
+  if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0)
+    return set_error(MSA_ERR_INVALID_ARG, "%s: bad head counts", fn);
+  if (head_dim != kD) return set_error(MSA_ERR_UNSUPPORTED, "%s: head_dim must be 128", fn);
+  const int G = num_qo_heads / num_kv_heads;
+  if (G > 16) return set_error(MSA_ERR_UNSUPPORTED, "%s: at most 16 query heads per KV head", fn);
+  if (topk < 1 || topk > 1024) return set_error(MSA_ERR_INVALID_ARG, "%s: topk outside [1, 1024]", fn);
+  if (num_pages < 1 || num_pages > (int64_t(1) << 24)) return set_error(MSA_ERR_INVALID_ARG, "%s: num_pages", fn);
+  const size_t n_units = static_cast<size_t>(batch) * num_kv_heads * topk;
+  const size_t part_bytes = n_units * G * (kD + 2) * sizeof(float);
+  if (n_units > size_t(1) << 30 || part_bytes > kStaticScratchBytes - kStaticPartOff)
+    return set_error(MSA_ERR_INVALID_ARG,
+                     "%s: batch*num_kv_heads*topk*(num_qo_heads/num_kv_heads) = %zu exceeds the static scratch "
+                     "limit of %zu (24 MiB at head_dim 128)",
+                     fn, n_units * G, (kStaticScratchBytes - kStaticPartOff) / ((kD + 2) * sizeof(float)));
+
+  StaticDevice sd;
+  msa_status s = static_scratch(&sd);
+  if (s != MSA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  TileInfo* tiles = reinterpret_cast<TileInfo*>(sd.base);
+  uint32_t* err = err_word ? err_word : reinterpret_cast<uint32_t*>(sd.base + kStaticErrOff);
+  float* part_o = reinterpret_cast<float*>(sd.base + kStaticPartOff);
+  float* part_ml = part_o + n_units * G * kD;
+
+  CUtensorMap km, vm;
+  const uint64_t dims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(num_pages) * num_kv_heads * 128};
+  const uint64_t str[1] = {static_cast<uint64_t>(kD)};
+  const uint32_t box[2] = {static_cast<uint32_t>(kD), 128};
+  if (!encode_tensor_map(&km, 2, k_pages, dims, str, box, 0, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, dims, str, box, 0, 128))
+    return set_error(MSA_ERR_CUDA, "%s: tensor map encoding failed", fn);
+
+  decode_tiles_kernel<<<(batch + 127) / 128, 128, 0, st>>>(kv_lens, kv_indptr, batch, tiles, err);
+  s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: tile table launch");
+  if (s != MSA_OK) return s;
+  const int nu = static_cast<int>(n_units);
+  const int grid = std::max(1, std::min(nu, sd.num_sms * (G <= 8 ? 2 : 1)));
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
+  const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  if (G <= 8) {
+    const int smem = DecodeSmem<1>::kBytes + 1024;
+    cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
+                                                     k_scale, part_o, part_ml, nu, num_qo_heads, num_kv_heads, topk,
+                                                     scale_log2, err);
+  } else {
+    const int smem = DecodeSmem<2>::kBytes + 1024;
+    cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
+                                                     k_scale, part_o, part_ml, nu, num_qo_heads, num_kv_heads, topk,
+                                                     scale_log2, err);
+  }
+  s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: decode launch");
+  if (s != MSA_OK) return s;
+  decode_combine_kernel<<<batch * num_kv_heads, 128, 0, st>>>(part_o, part_ml, tiles, v_scale,
+                                                              static_cast<__nv_bfloat16*>(out), lse, nu, grid,
+                                                              num_qo_heads, num_kv_heads, topk);
+  return cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: combine launch");
+}

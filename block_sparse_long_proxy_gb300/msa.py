@@ -42,6 +42,8 @@ SIGNATURES = {
     "msa_topk_select": (_i32, [_p, _i32, _i32, _i32, _i32, _p, _p, _p]),
     "msa_sparse_attn": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
     "msa_sparse_attn_bwd": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _p, _p]),
+    "msa_sparse_decode_noalloc": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i64,
+                                         _p, _p, _p, _p]),
     "msa_check_errors": (_i32, [_p, _p]),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_version": (ctypes.c_char_p, []),
@@ -98,6 +100,36 @@ def topk_select(max_score, topk, num_valid_pages, out=None, stream=None):
     _check(_lib.msa_topk_select(_ptr(max_score), n, h, nb, topk, _ptr(num_valid_pages), _ptr(out),
                                 _stream(stream)), "msa_topk_select")
     return out
+
+
+def sparse_decode_noalloc(q, k_pages, v_pages, kv_lens, kv_indptr, kv_indices, kv_block_indexes, k_scale,
+                          v_scale, out=None, lse=None, err_word=None, stream=None):
+    """FP8 paged decode without a plan and without any device allocation by
+    the library (msa_sparse_decode_noalloc): the batch comes as device
+    int32 kv_lens [B] and kv_indptr [B+1]; scratch is libmsa's static
+    array.  Outputs may be passed in (out bf16 [B, Hq, 128], lse fp32
+    [B, Hq], err_word uint32/int32 [1])."""
+    b, hq, d = q.shape
+    hkv = k_pages.shape[1]
+    topk = kv_block_indexes.shape[2]
+    _need(q, torch.bfloat16, (b, hq, d), "q")
+    _need(k_pages, torch.float8_e4m3fn, tuple(k_pages.shape), "k_pages")
+    _need(v_pages, torch.float8_e4m3fn, tuple(k_pages.shape), "v_pages")
+    _need(kv_lens, torch.int32, (b,), "kv_lens")
+    _need(kv_indptr, torch.int32, (b + 1,), "kv_indptr")
+    _need(kv_block_indexes, torch.int32, (b, hkv, topk), "kv_block_indexes")
+    _need(k_scale, torch.float32, (hkv,), "k_scale")
+    _need(v_scale, torch.float32, (hkv,), "v_scale")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.bfloat16, (b, hq, d), "out")
+    if lse is not None:
+        _need(lse, torch.float32, (b, hq), "lse")
+    _check(_lib.msa_sparse_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_lens), _ptr(kv_indptr),
+                                          _ptr(kv_indices), _ptr(kv_block_indexes), _ptr(k_scale), _ptr(v_scale),
+                                          b, hq, hkv, d, topk, k_pages.shape[0], _ptr(out), _ptr(lse),
+                                          _ptr(err_word), _stream(stream)), "msa_sparse_decode_noalloc")
+    return out, lse
 
 
 class Plan:

@@ -225,6 +225,46 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
                                float* dpq, float* dpk_pages, msa_stream_t stream);
 
 /*
+ * msa_sparse_decode_noalloc -- the FP8 paged decode of msa_sparse_attn for
+ * callers that cannot allocate device memory when they decode (for example
+ * a server that gives the GPU's memory to its own pool at start-up, or a
+ * decode loop that must not pay for cudaMalloc's implicit synchronisation;
+ * neither can create a plan, since msa_plan allocates).  The paper has no
+ * counterpart: this is a deployment variant of the decode kernel.
+ *
+ * Computes exactly what msa_sparse_attn computes for a decode batch (one
+ * query row per sequence) with e4m3 K/V, head_dim 128, up to 16 query heads
+ * per KV head.  The batch comes as DEVICE arrays instead of a plan:
+ *   kv_lens    int32 [batch], keys per sequence (>= 1);
+ *   kv_indptr  int32 [batch+1], offset of each sequence's pages in
+ *              kv_indices (kv_indptr[s+1] - kv_indptr[s] >= ceil(kv_len/128)).
+ * q, k_pages, v_pages, kv_indices, kv_block_indexes ([batch, Hkv, topk]),
+ * k_scale, v_scale, out and lse (nullable) are as in msa_sparse_attn.
+ * err_word: optional DEVICE uint32 that device-side bounds checks OR into
+ * (bit 0: a bad page id or page range; the block is skipped or read from
+ * page 0); NULL discards them.
+ *
+ * Scratch: all of it (a tile table and the split-K partials) lives in one
+ * fixed 24 MiB device array inside libmsa, held by every GPU that loads the
+ * library until the process exits.  The call allocates nothing and calls no
+ * allocating routine.  It rejects, with MSA_ERR_INVALID_ARG, batch > 4096 or
+ * batch * num_qo_heads * topk above 48,143 (the partials that fit in the
+ * array at head_dim 128).  The first call on a device looks up the array's
+ * device address for that device (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call on a
+ * device shares the one array and overwrites what it needs: calls that
+ * overlap on the GPU (other streams, or other host threads) race and give
+ * wrong results; issue them one after another.
+ */
+msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                     const int32_t* kv_lens, const int32_t* kv_indptr,
+                                     const int32_t* kv_indices, const int32_t* kv_block_indexes,
+                                     const float* k_scale, const float* v_scale, int32_t batch,
+                                     int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t topk, int64_t num_pages, void* out, float* lse,
+                                     uint32_t* err_word, msa_stream_t stream);
+
+/*
  * msa_check_errors -- waits for `stream`, then reads and clears the plan's
  * device error word: MSA_OK, MSA_ERR_DEVICE_CHECK (a kernel skipped a block
  * whose page id was out of range) or MSA_ERR_TIMEOUT (a bounded wait inside

@@ -33,7 +33,7 @@ namespace {
 constexpr int kD = 128;                 // head dim of this kernel
 constexpr int kCWarps = 4;              // consumer warps
 constexpr int kDThreads = 32 * (kCWarps + 1);
-constexpr int kDStages = 2;
+constexpr int kDStages = 3;
 constexpr int kBlk = 128 * kD;          // bytes of one e4m3 K (or V) block
 
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v16) {
@@ -91,9 +91,11 @@ template <int NT>
 struct DecodeSmem {
   static constexpr int kRingOff = 0;
   static constexpr int kScratchOff = kDStages * 2 * kBlk;
-  static constexpr int kScratchFloats = kCWarps * 8 * NT * (kD + 2);
+  // per-warp merge scratch, one half of d at a time: [warp][head slot][64 + 2]
+  static constexpr int kScratchFloats = kCWarps * 8 * NT * (kD / 2 + 2);
   static constexpr int kBarOff = kScratchOff + kScratchFloats * 4;
-  static constexpr int kBytes = kBarOff + 8 * 2 * kDStages;
+  static constexpr int kStageJOff = kBarOff + 8 * 2 * kDStages;
+  static constexpr int kBytes = kStageJOff + 4 * kDStages;
 };
 
 template <int NT>  // n-tiles of 8 heads: group size G <= 8*NT
@@ -107,10 +109,12 @@ __global__ void __launch_bounds__(kDThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DecodeSmem<NT>;
   constexpr int kSlots = 8 * NT;  // head slots of the per-warp scratch
+  constexpr int kHalf = kD / 2;
   uint8_t* ring = smem + L::kRingOff;
   float* scratch = reinterpret_cast<float*>(smem + L::kScratchOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + kDStages;
+  volatile int32_t* stage_j = reinterpret_cast<int32_t*>(smem + L::kStageJOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = hq / hkv;
@@ -130,26 +134,54 @@ __global__ void __launch_bounds__(kDThreads)
 
   if (warp == kCWarps) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int i = 0;
-      for (int u = ub; u < ue; ++u) {
+    // One ring stage per unit, in unit order.  The block index travels with
+    // the stage (stage_j, -1 for a padding slot, which loads nothing).  The
+    // metadata of 32 units at a time is fetched lane-parallel so that its
+    // dependent global loads stay off the per-unit critical path.
+    bool ok = true;
+    int i = 0;
+    for (int base = ub; ok && base < ue; base += 32) {
+      const int u = base + lane;
+      int j = -1, row_off = 0;
+      if (u < ue) {
         const int row = u / topk;
         const int t = row / hkv, g = row % hkv;
-        const int j = idx[u];
+        j = idx[u];
         const TileInfo tl = tiles[t];
-        if (j < 0 || j >= tl.nvp) continue;
-        const int s = i % kDStages;
-        if (!mbar_wait(empty + s, ((i / kDStages) & 1) ^ 1, err)) break;
-        int64_t page = kv_indices[tl.page_base + j];
-        if (page < 0 || page >= num_pages) {
+        if (j >= tl.nvp) {
           atomicOr(err, kErrDeviceCheck);
-          page = 0;
+          j = -1;
         }
-        const int r = static_cast<int>((page * hkv + g) * 128);
-        mbar_expect_tx(full + s, 2 * kBlk);
-        tma_load_2d(ring + s * 2 * kBlk, &k_map, full + s, 0, r);
-        tma_load_2d(ring + s * 2 * kBlk + kBlk, &v_map, full + s, 0, r);
-        ++i;
+        if (j >= 0) {
+          int64_t page = kv_indices[tl.page_base + j];
+          if (page < 0 || page >= num_pages) {
+            atomicOr(err, kErrDeviceCheck);
+            page = 0;
+          }
+          row_off = static_cast<int>((page * hkv + g) * 128);
+        }
+      }
+      const int n = min(32, ue - base);
+      for (int k = 0; k < n; ++k, ++i) {
+        const int jk = __shfl_sync(0xFFFFFFFFu, j, k);
+        const int rk = __shfl_sync(0xFFFFFFFFu, row_off, k);
+        if (lane == 0) {
+          const int s = i % kDStages;
+          if (!(ok = mbar_wait(empty + s, ((i / kDStages) & 1) ^ 1, err))) {
+            // leave the loop below too
+          } else {
+            stage_j[s] = jk;
+            if (jk >= 0) {
+              mbar_expect_tx(full + s, 2 * kBlk);
+              tma_load_2d(ring + s * 2 * kBlk, &k_map, full + s, 0, rk);
+              tma_load_2d(ring + s * 2 * kBlk + kBlk, &v_map, full + s, 0, rk);
+            } else {
+              mbar_arrive(full + s);
+            }
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
       }
     }
     return;
@@ -177,47 +209,52 @@ __global__ void __launch_bounds__(kDThreads)
         v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
         l[nt][c] = v;
       }
-    float* wsc = scratch + w * kSlots * (kD + 2);  // [head][kD + 2]: O, m, l
+    // merge the four warps' states one half of d at a time (two rounds)
+    float* wsc = scratch + w * kSlots * (kHalf + 2);  // [head slot][64 + 2]: O half, m, l
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int rnd = 0; rnd < 2; ++rnd) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int h = 8 * nt + 2 * t4 + c;
-        if (h < G) {
-          if (gi == 0) {
-            wsc[h * (kD + 2) + kD] = m[nt][c];
-            wsc[h * (kD + 2) + kD + 1] = l[nt][c];
-          }
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int md = 0; md < 8; ++md) {
-            const int d0 = 32 * (md >> 1) + 4 * gi + 2 * (md & 1);
-            wsc[h * (kD + 2) + d0] = oacc[md][nt][c];
-            wsc[h * (kD + 2) + d0 + 1] = oacc[md][nt][2 + c];
+        for (int c = 0; c < 2; ++c) {
+          const int h = 8 * nt + 2 * t4 + c;
+          if (h < G) {
+            if (gi == 0) {
+              wsc[h * (kHalf + 2) + kHalf] = m[nt][c];
+              wsc[h * (kHalf + 2) + kHalf + 1] = l[nt][c];
+            }
+#pragma unroll
+            for (int mh = 0; mh < 4; ++mh) {
+              const int md = 4 * rnd + mh;  // m-tiles 4rnd..4rnd+3 hold d in [64rnd, 64rnd+64)
+              const int d0 = 32 * (md >> 1) + 4 * gi + 2 * (md & 1) - kHalf * rnd;
+              wsc[h * (kHalf + 2) + d0] = oacc[md][nt][c];
+              wsc[h * (kHalf + 2) + d0 + 1] = oacc[md][nt][2 + c];
+            }
           }
         }
-      }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
-    for (int e = threadIdx.x; e < G * kD; e += 32 * kCWarps) {
-      const int h = e / kD, d = e % kD;
-      float mm = -INFINITY;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+      for (int e = threadIdx.x; e < G * kHalf; e += 32 * kCWarps) {
+        const int h = e / kHalf, d = e % kHalf;
+        float mm = -INFINITY;
 #pragma unroll
-      for (int ww = 0; ww < kCWarps; ++ww) mm = fmaxf(mm, scratch[(ww * kSlots + h) * (kD + 2) + kD]);
-      float L = 0.f, o = 0.f;
+        for (int ww = 0; ww < kCWarps; ++ww) mm = fmaxf(mm, scratch[(ww * kSlots + h) * (kHalf + 2) + kHalf]);
+        float Lsum = 0.f, o = 0.f;
 #pragma unroll
-      for (int ww = 0; ww < kCWarps; ++ww) {
-        const float* p = scratch + (ww * kSlots + h) * (kD + 2);
-        const float sc = p[kD] == -INFINITY ? 0.f : ex2_approx(p[kD] - mm);
-        L += p[kD + 1] * sc;
-        o += p[d] * sc;
+        for (int ww = 0; ww < kCWarps; ++ww) {
+          const float* p = scratch + (ww * kSlots + h) * (kHalf + 2);
+          const float sc = p[kHalf] == -INFINITY ? 0.f : ex2_approx(p[kHalf] - mm);
+          Lsum += p[kHalf + 1] * sc;
+          o += p[d] * sc;
+        }
+        const int64_t base = static_cast<int64_t>(slot) * G + h;
+        part_o[base * kD + kHalf * rnd + d] = o;
+        if (d == 0 && rnd == 0) {
+          part_ml[base * 2] = mm;
+          part_ml[base * 2 + 1] = Lsum;
+        }
       }
-      const int64_t base = static_cast<int64_t>(slot) * G + h;
-      part_o[base * kD + d] = o;
-      if (d == 0) {
-        part_ml[base * 2] = mm;
-        part_ml[base * 2 + 1] = L;
-      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
     (void)row;
   };
 
@@ -257,14 +294,15 @@ __global__ void __launch_bounds__(kDThreads)
         }
       }
     }
-    const int j = idx[u];
-    if (j < 0 || j >= tiles[t].nvp) {
-      if (j >= 0 && w == 0 && lane == 0) atomicOr(err, kErrDeviceCheck);
+    const int s = i % kDStages;
+    ++i;
+    if (!ok || !(ok = mbar_wait(full + s, ((i - 1) / kDStages) & 1, err))) continue;  // after a timeout: no
+    const int j = stage_j[s];                                                         // compute, but every
+    if (j < 0) {                                                                      // flush still runs
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + s);
       continue;
     }
-    const int s = i % kDStages;
-    if (!ok || !(ok = mbar_wait(full + s, (i / kDStages) & 1, err))) continue;  // after a timeout: no compute,
-    ++i;                                                                          // but every flush still runs
     const uint32_t kb = smem_u32(ring + s * 2 * kBlk);
     const uint32_t vb = kb + kBlk;
 
@@ -365,40 +403,72 @@ __global__ void __launch_bounds__(kDThreads)
   if (cur_row >= 0) flush(cur_row, seg);
 }
 
-// Merge the segment partials of each (tile, group) row; apply v_scale.
-__global__ void __launch_bounds__(128)
+// Merge the segment partials of each (tile, group) row; apply v_scale.  One
+// warp per (row, head): lanes scan the row's slots for segment starts, then
+// each lane combines four consecutive d values with float4 loads.
+constexpr int kCombineWarps = 8;
+__global__ void __launch_bounds__(32 * kCombineWarps)
     decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                           const TileInfo* __restrict__ tiles, const float* __restrict__ v_scale,
                           __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t n_units, int32_t n_ctas,
                           int32_t hq, int32_t hkv, int32_t topk) {
-  const int row = blockIdx.x;
-  const int t = row / hkv, g = row % hkv;
+  const int lane = threadIdx.x & 31;
   const int G = hq / hkv;
-  const int u0 = row * topk, u1 = u0 + topk;
-  const TileInfo tl = tiles[t];
-  const float vs = v_scale[g];
-  for (int e = threadIdx.x; e < G * kD; e += blockDim.x) {
-    const int h = e / kD, d = e % kD;
-    float mm = -INFINITY;
-    for (int u = u0; u < u1; ++u)
-      if (u == u0 || is_range_start(u, n_units, n_ctas)) mm = fmaxf(mm, part_ml[(static_cast<int64_t>(u) * G + h) * 2]);
-    float L = 0.f, o = 0.f;
-    if (mm != -INFINITY) {
-      for (int u = u0; u < u1; ++u) {
-        if (!(u == u0 || is_range_start(u, n_units, n_ctas))) continue;
-        const int64_t b = static_cast<int64_t>(u) * G + h;
-        const float ms = part_ml[b * 2];
-        if (ms == -INFINITY) continue;
-        const float sc = ex2_approx(ms - mm);
-        L += part_ml[b * 2 + 1] * sc;
-        o += part_o[b * kD + d] * sc;
+  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
+  const int rows = n_units / topk;
+  if (wid >= static_cast<int64_t>(rows) * G) return;
+  const int row = static_cast<int>(wid / G), h = static_cast<int>(wid % G);
+  const int t = row / hkv, g = row % hkv;
+  const int u0 = row * topk;
+  float mm = -INFINITY;
+  for (int k0 = 0; k0 < topk; k0 += 32) {
+    const int k = k0 + lane;
+    const int u = u0 + k;
+    const bool st = k < topk && (k == 0 || is_range_start(u, n_units, n_ctas));
+    if (st) mm = fmaxf(mm, part_ml[(static_cast<int64_t>(u) * G + h) * 2]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
+  float lsum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mm != -INFINITY) {
+    for (int k0 = 0; k0 < topk; k0 += 32) {
+      const int k = k0 + lane;
+      const int u = u0 + k;
+      float sc = 0.f;
+      if (k < topk && (k == 0 || is_range_start(u, n_units, n_ctas))) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(u) * G + h) * 2);
+        if (ml.x != -INFINITY) {
+          sc = ex2_approx(ml.x - mm);
+          lsum += ml.y * sc;
+        }
+      }
+      uint32_t mask = __ballot_sync(0xFFFFFFFFu, sc > 0.f);
+      while (mask) {
+        const int src = __ffs(mask) - 1;
+        mask &= mask - 1;
+        const float scs = __shfl_sync(0xFFFFFFFFu, sc, src);
+        const int64_t b = (static_cast<int64_t>(u0 + k0 + src) * G + h) * kD;
+        const float4 v = *reinterpret_cast<const float4*>(part_o + b + 4 * lane);
+        acc.x += v.x * scs;
+        acc.y += v.y * scs;
+        acc.z += v.z * scs;
+        acc.w += v.w * scs;
       }
     }
-    const int64_t orow = static_cast<int64_t>(tl.q_begin) * hq + g * G + h;
-    out[orow * kD + d] = __float2bfloat16_rn(L > 0.f ? o / L * vs : 0.f);
-    if (d == 0 && lse != nullptr) lse[orow] = L > 0.f ? (mm + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+  const float f = lsum > 0.f ? v_scale[g] / lsum : 0.f;
+  const int64_t orow = static_cast<int64_t>(tiles[t].q_begin) * hq + g * G + h;
+  uint2 w;
+  w.x = pack_bf16x2(acc.x * f, acc.y * f);
+  w.y = pack_bf16x2(acc.z * f, acc.w * f);
+  *reinterpret_cast<uint2*>(out + orow * kD + 4 * lane) = w;
+  if (lane == 0 && lse != nullptr) lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
 }
+
+int combine_grid(int rows, int G) { return (rows * G + kCombineWarps - 1) / kCombineWarps; }
 
 int decode_grid(const msa_plan_s* p, int n_units) {
   const int per_sm = (p->hq / p->hkv) <= 8 ? 2 : 1;
@@ -449,7 +519,7 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
   }
   msa_status s = cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
   if (s != MSA_OK) return s;
-  decode_combine_kernel<<<p->n_tiles * p->hkv, 128, 0, st>>>(part_o, part_ml, p->tiles_d, v_scale,
+  decode_combine_kernel<<<combine_grid(p->n_tiles * p->hkv, G), 32 * kCombineWarps, 0, st>>>(part_o, part_ml, p->tiles_d, v_scale,
                                                              static_cast<__nv_bfloat16*>(out), lse, n_units, grid,
                                                              p->hq, p->hkv, p->topk);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode combine launch");
@@ -618,7 +688,7 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
   }
   s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: decode launch");
   if (s != MSA_OK) return s;
-  decode_combine_kernel<<<batch * num_kv_heads, 128, 0, st>>>(part_o, part_ml, tiles, v_scale,
+  decode_combine_kernel<<<combine_grid(batch * num_kv_heads, G), 32 * kCombineWarps, 0, st>>>(part_o, part_ml, tiles, v_scale,
                                                               static_cast<__nv_bfloat16*>(out), lse, nu, grid,
                                                               num_qo_heads, num_kv_heads, topk);
   return cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: combine launch");

@@ -148,6 +148,7 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
     }
   }
   p->total_q = q0;
+  p->n_page_entries = static_cast<int32_t>(page_base);
   p->n_tiles = static_cast<int32_t>(p->tiles.size());
   p->decode = all_one;
   if (p->n_tiles == 0) {
@@ -164,6 +165,7 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   std::vector<int32_t> aux;
   proxy_plan_tables(p, aux);
   attn_plan_tables(p, aux);
+  bwd_plan_tables(p, aux);
 
   // device block: tiles | nvp | error word | aux tables | decode partials
   const size_t tiles_bytes = sizeof(TileInfo) * p->n_tiles;
@@ -171,8 +173,9 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   const size_t err_off = nvp_off + ((sizeof(int32_t) * p->n_tiles + 255) & ~size_t(255));
   const size_t aux_off = err_off + 256;
   const size_t part_off = aux_off + ((sizeof(int32_t) * aux.size() + 255) & ~size_t(255));
-  const size_t part_bytes = sizeof(float) * decode_partial_floats(p);
-  const size_t total = part_off + part_bytes;
+  const size_t part_bytes = (sizeof(float) * decode_partial_floats(p) + 255) & ~size_t(255);
+  const size_t bwd_off = part_off + part_bytes;
+  const size_t total = bwd_off + bwd_scratch_bytes(p);
   if (cudaMalloc(&p->dev_block, total) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -184,6 +187,7 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   p->err_d = reinterpret_cast<uint32_t*>(base + err_off);
   p->aux_d = reinterpret_cast<int32_t*>(base + aux_off);
   p->partial_d = part_bytes ? reinterpret_cast<float*>(base + part_off) : nullptr;
+  p->bwd_d = bwd_scratch_bytes(p) ? base + bwd_off : nullptr;
 
   std::vector<char> host(part_off, 0);
   memcpy(host.data(), p->tiles.data(), tiles_bytes);

@@ -61,6 +61,9 @@ struct msa_plan_s {
   int64_t proxy_unit_start_off = 0;  // decode proxy: first unit of each tile
   int64_t attn_units_off = 0;        // prefill attention work units
   int32_t n_attn_units = 0;
+  int64_t blk_j_off = 0;             // backward: logical block of each page-table entry
+  int32_t n_page_entries = 0;        // sum over sequences of ceil(kv_len / 128)
+  void* bwd_d = nullptr;             // backward scratch (D, proxy LSE, inverse index)
 };
 
 namespace msa {
@@ -71,6 +74,8 @@ msa_status cuda_check(cudaError_t e, const char* what);
 // ---- plan-time tables (host), appended to the plan's aux array ----
 void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
+void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
+size_t bwd_scratch_bytes(const msa_plan_s* p);
 
 // ---- launchers (each returns MSA_OK or an error with its message set) ----
 msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,

@@ -1,0 +1,86 @@
+"""msa_sparse_attn_bwd on the GPU against the oracle: dq, dk, dv and the KL
+proxy gradients dpq, dpk, each within max-abs 2e-2 and cosine >= 0.99."""
+import numpy as np
+import pytest
+import torch
+
+from block_sparse_long_proxy_gb300 import synth
+from oracle import msa_oracle as O
+from tests.gpu_cases import O_ATOL_BF16, compare_out, make_plan, random_idx, rows_of_tiles
+
+pytestmark = pytest.mark.gpu
+PAGE = 128
+
+
+def _run_gpu(case, inp, idx_t, w):
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t)
+    grads = plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t, out, lse,
+                                 inp["dout"], inp["pq"], inp["pk_pages"], kl_weight=w)
+    torch.cuda.synchronize()
+    plan.check_errors()
+    return {k: v.cpu().numpy() for k, v in grads.items()}
+
+
+def _oracle(case, inp, idx, w, tile_ids=None):
+    return O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                                  inp["kv_indices"].cpu().numpy(), idx, case.qo_lens, case.kv_lens,
+                                  synth.bits(inp["dout"]), synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]),
+                                  kl_weight=w, tile_ids=tile_ids)
+
+
+SMALL = [
+    (synth.Case("S=256 G=4", [256], [256], 8, 2, 128, 2, 64, 2), 1.0),
+    (synth.Case("ragged varlen paged offsets", [300, 77, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
+                page_perm_seed=3, extra_pages=2), 0.5),
+    (synth.Case("G=1", [384], [384], 2, 2, 128, 2, 64, 2, page_perm_seed=1), 1.0),
+    (synth.Case("long rows topk 16", [2048], [2048], 8, 2, 128, 2, 64, 16, page_perm_seed=5), 1.0),
+]
+
+
+@pytest.mark.parametrize("case,w", SMALL, ids=lambda c: c.name if hasattr(c, "name") else str(c))
+def test_bwd_small(cuda_dev, case, w):
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    idx = random_idx(case, np.random.default_rng(9))
+    got = _run_gpu(case, inp, torch.from_numpy(idx).to(cuda_dev), w)
+    ref = _oracle(case, inp, idx, w)
+    for name in ("dq", "dpq", "dk", "dv", "dpk"):
+        compare_out(got[name], ref[name], O_ATOL_BF16, name)
+
+
+def test_bwd_unsupported_head_dim(cuda_dev):
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("d64", [256], [256], 4, 2, 64, 2, 32, 2)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    idx = torch.from_numpy(random_idx(case, np.random.default_rng(0))).to(cuda_dev)
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    with pytest.raises(msa.MsaError) as e:
+        plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out, lse,
+                             inp["dout"], inp["pq"], inp["pk_pages"])
+    assert e.value.status == 2
+
+
+def test_bwd_training_64k_sampled(cuda_dev):
+    """S=65536, 32/8 heads, topk 16, the GPU's own proxy -> top-k -> forward
+    -> backward.  dq/dpq on sampled tiles; dk/dv/dpk on sampled blocks, with
+    the oracle run over every tile that cached those blocks."""
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.training_64k()
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    plan = make_plan(case, inp)
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx_t = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    got = _run_gpu(case, inp, idx_t, 1.0)
+    idx = idx_t.cpu().numpy()
+    # blocks late in the sequence are cached by few tiles: cheap for the oracle
+    blocks = [511, 480, 300]
+    tiles = sorted({t for t in range(idx.shape[0]) for b in blocks if (idx[t] == b).any()} | {0, 7, 255})
+    ref = _oracle(case, inp, idx, 1.0, tile_ids=tiles)
+    rows = rows_of_tiles(case, [0, 7, 255])
+    compare_out(got["dq"][rows], ref["dq"][rows], O_ATOL_BF16, "dq")
+    compare_out(got["dpq"][rows], ref["dpq"][rows], O_ATOL_BF16, "dpq")
+    pages = inp["kv_indices"].cpu().numpy()[blocks]
+    compare_out(got["dk"][pages], ref["dk"][pages], O_ATOL_BF16, "dk")
+    compare_out(got["dv"][pages], ref["dv"][pages], O_ATOL_BF16, "dv")
+    compare_out(got["dpk"][pages], ref["dpk"][pages], O_ATOL_BF16, "dpk")

@@ -305,6 +305,7 @@ def run_ours(args):
     e2e_value = case.total_q * world * e2e_steps / (e2e_ms / 1e3)
 
     decode = bench_decode(args, dev, pk_info, peak_kind, world)
+    train = bench_train(args, dev, pk_info, peak_kind)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -322,6 +323,8 @@ def run_ours(args):
             "wall_s": t_wall}
     if decode:
         line["decode"] = decode
+    if train:
+        line["training"] = train
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case)
     if rank == 0:
@@ -451,12 +454,74 @@ def run_ncu_case(args):
     print("ncu case %s done: %d launches" % (args.ncu_case, args.steps))
 
 
+def bench_train(args, dev, pk_info, peak_kind):
+    """Training step at S=65536 (32q/8kv, d=128, 8 proxy heads x 64, topk
+    16): forward (proxy, top-k, attention with LSE) and the KL-coupled
+    backward, each timed with CUDA events; FLOPs counted on the selected
+    blocks (forward 4*T*B*d, backward 10*T*B*d per tile, head and block) plus
+    the KL products (proxy logits twice, p.pk and p^T.pq: 8*T*B*dp per tile,
+    group and block)."""
+    import torch
+    from block_sparse_long_proxy_gb300 import msa, synth
+    case = synth.training_64k()
+    inp = synth.make_inputs(case, device=dev, with_dout=True)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0])
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    grads = dict(dq=torch.empty(inp["q"].shape, dtype=torch.float32, device=dev),
+                 dk=torch.zeros(inp["k_pages"].shape, dtype=torch.float32, device=dev),
+                 dv=torch.zeros(inp["v_pages"].shape, dtype=torch.float32, device=dev),
+                 dpq=torch.empty(inp["pq"].shape, dtype=torch.float32, device=dev),
+                 dpk=torch.zeros(inp["pk_pages"].shape, dtype=torch.float32, device=dev))
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def fwd():
+        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
+        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out=out, lse=lse)
+
+    def bwd():
+        plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out, lse, inp["dout"],
+                             inp["pq"], inp["pk_pages"], kl_weight=1.0, grads=grads)
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    plan.check_errors()
+    n_sel = int((idx >= 0).sum().item())
+    grp = case.hq // case.hkv
+    f_fwd = n_sel * grp * 4.0 * 128 * 128 * case.d
+    f_bwd = n_sel * grp * 10.0 * 128 * 128 * case.d + n_sel * 8.0 * 128 * 128 * case.dp
+    tf, tb = [], []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record(stream)
+        fwd()
+        b.record(stream)
+        bwd()
+        c.record(stream)
+        torch.cuda.synchronize()
+        tf.append(a.elapsed_time(b))
+        tb.append(b.elapsed_time(c))
+    fms, bms = statistics.median(tf), statistics.median(tb)
+    peak = pk_info.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    bt = f_bwd / (bms / 1e3) / 1e12
+    return {"workload": case.name, "fwd_ms": fms, "bwd_ms": bms, "tokens_per_s": case.total_q / ((fms + bms) / 1e3),
+            "fwd_sparse_flops": f_fwd, "bwd_flops": f_bwd, "bwd_tflops": bt,
+            "roofline_bwd": {"bound": "tensor", "achieved": bt, "peak": peak, "unit": "TFLOP/s", "frac": bt / peak,
+                             "peak_kind": "%s bf16 dense burst" % peak_kind}}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--ncu-case", choices=["attn", "proxy", "topk", "decode"], default=None,
                     help="run a small case of one kernel for a profiler capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -217,36 +217,37 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       const int j = blocks[i];
       const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
-      float mx = -INFINITY;
-      if (need_mask) {
+      if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
         const int limit = row_ok ? qpos - j * 128 : -1;
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
+        for (int c = 0; c < 128; ++c)
           if (c > limit) sv[c] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sv[c]));
-        }
-      } else {
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+      }
+      float mx;
+      {
+        float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 128; c += 4) {
-          a0 = fmaxf(a0, __uint_as_float(sv[c]));
-          a1 = fmaxf(a1, __uint_as_float(sv[c + 1]));
-          a2 = fmaxf(a2, __uint_as_float(sv[c + 2]));
-          a3 = fmaxf(a3, __uint_as_float(sv[c + 3]));
+          a0 = fmax3(a0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+          a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
         }
-        mx = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+        mx = fmaxf(a0, a1);
       }
-      const float m_new = fmaxf(m, mx * scale_log2);
+      // lazy rescaling: the reference max moves only when the row max grows
+      // by more than 2^8, so probabilities stay below 256 and O is rescaled
+      // rarely
+      const float mx2 = mx * scale_log2;
+      const float m_new = mx2 > m + 8.f ? mx2 : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = ex2_approx(m - m_use);
+      const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
       float sum0 = 0.f, sum1 = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * c]), scale_log2, -m_use));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * c + 1]), scale_log2, -m_use));
-        sum0 += p0;
-        sum1 += p1;
+        float x0, x1;
+        ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2, -m_use);
+        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+        fadd2(sum0, sum1, p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
       }
 #pragma unroll

@@ -37,9 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # dram bytes of one attention-forward launch at the 32K prefill workload from
 # an ncu capture, valid only for the kernel source it was taken on.
-# Captured on S=16384 (15424 selected tile-blocks: 248.6 MB read + 114.2 MB
+# Captured on S=16384 (15424 selected tile-blocks: 246.3 MB read + 112.9 MB
 # written) and scaled by selected tile-blocks to the S=32768 launch (31808).
-NCU_TRAFFIC = {"attn_fwd.cu": {"src": "7840dac208c29e10", "bytes": int((247637248 + 114182400) * 31808 / 15424),
+NCU_TRAFFIC = {"attn_fwd.cu": {"src": "f06e313925f79092", "bytes": int((246285312 + 112910336) * 31808 / 15424),
                                "source": "profiles/attn_fwd_prefill.md"}}
 
 

@@ -224,14 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c > limit) sv[c] = __float_as_uint(-INFINITY);
       }
       float mx;
-      {
-        float a0 = -INFINITY, a1 = -INFINITY;
+      {  // four independent chains keep the max off the latency path
+        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; c += 4) {
+        for (int c = 0; c < 128; c += 8) {
           a0 = fmax3(a0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
           a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+          a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+          a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
         }
-        mx = fmaxf(a0, a1);
+        mx = fmax3(fmaxf(a0, a1), a2, a3);
       }
       // lazy rescaling: the reference max moves only when the row max grows
       // by more than 2^8, so probabilities stay below 256 and O is rescaled
@@ -240,16 +242,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = mx2 > m + 8.f ? mx2 : m;
       const float m_use = m_new == -INFINITY ? 0.f : m_new;
       const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-      float sum0 = 0.f, sum1 = 0.f;
+      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
         float x0, x1;
         ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2, -m_use);
         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        fadd2(sum0, sum1, p0, p1);
+        if (c & 1)
+          fadd2(sum2, sum3, p0, p1);
+        else
+          fadd2(sum0, sum1, p0, p1);
         pk[c] = pack_bf16x2(p0, p1);
       }
+      sum0 += sum2;
+      sum1 += sum3;
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_st16(s_addr + c * 16, pk + c * 16);
       l = l * alpha + (sum0 + sum1);

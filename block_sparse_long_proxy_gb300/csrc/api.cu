@@ -197,6 +197,8 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   msa_status s = cuda_check(cudaMemcpyAsync(p->dev_block, host.data(), part_off, cudaMemcpyHostToDevice, st),
                             "msa_plan: upload");
+  if (s == MSA_OK && part_bytes)  // decode partials and per-row counters start at zero
+    s = cuda_check(cudaMemsetAsync(base + part_off, 0, part_bytes, st), "msa_plan: clear decode workspace");
   if (s == MSA_OK) s = cuda_check(cudaStreamSynchronize(st), "msa_plan: upload sync");
   if (s != MSA_OK) {
     cudaFree(p->dev_block);

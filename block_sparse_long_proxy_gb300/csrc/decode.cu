@@ -95,7 +95,8 @@ struct DecodeSmem {
   static constexpr int kScratchFloats = kCWarps * 8 * NT * (kD / 2 + 2);
   static constexpr int kBarOff = kScratchOff + kScratchFloats * 4;
   static constexpr int kStageJOff = kBarOff + 8 * 2 * kDStages;
-  static constexpr int kBytes = kStageJOff + 4 * kDStages;
+  static constexpr int kFlagOff = kStageJOff + 4 * kDStages;
+  static constexpr int kBytes = kFlagOff + 4;
 };
 
 template <int NT>  // n-tiles of 8 heads: group size G <= 8*NT
@@ -103,8 +104,10 @@ __global__ void __launch_bounds__(kDThreads)
     decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                   const __nv_bfloat16* __restrict__ q, const TileInfo* __restrict__ tiles,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
-                  const float* __restrict__ k_scale, float* __restrict__ part_o, float* __restrict__ part_ml,
-                  int32_t n_units, int32_t hq, int32_t hkv, int32_t topk, float scale_log2, uint32_t* err) {
+                  const float* __restrict__ k_scale, const float* __restrict__ v_scale, float* __restrict__ part_o,
+                  float* __restrict__ part_ml, int32_t* __restrict__ row_cnt, __nv_bfloat16* __restrict__ out,
+                  float* __restrict__ lse, int32_t n_units, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
+                  uint32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DecodeSmem<NT>;
@@ -115,6 +118,7 @@ __global__ void __launch_bounds__(kDThreads)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* empty = full + kDStages;
   volatile int32_t* stage_j = reinterpret_cast<int32_t*>(smem + L::kStageJOff);
+  volatile int32_t* merge_flag = reinterpret_cast<int32_t*>(smem + L::kFlagOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = hq / hkv;
@@ -198,6 +202,7 @@ __global__ void __launch_bounds__(kDThreads)
   bool ok = true;
 
   auto flush = [&](int row, int slot) {
+    const bool whole = slot == row * topk && ue >= (row + 1) * topk;
     // per-warp totals of l (sum over the 8 key lanes of each head column)
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -246,16 +251,67 @@ __global__ void __launch_bounds__(kDThreads)
           Lsum += p[kHalf + 1] * sc;
           o += p[d] * sc;
         }
-        const int64_t base = static_cast<int64_t>(slot) * G + h;
-        part_o[base * kD + kHalf * rnd + d] = o;
-        if (d == 0 && rnd == 0) {
-          part_ml[base * 2] = mm;
-          part_ml[base * 2 + 1] = Lsum;
+        if (whole) {  // this CTA holds the whole row: write the result directly
+          const int t = row / hkv, g = row % hkv;
+          const int64_t orow = static_cast<int64_t>(tiles[t].q_begin) * hq + g * G + h;
+          out[orow * kD + kHalf * rnd + d] = __float2bfloat16_rn(Lsum > 0.f ? o / Lsum * v_scale[g] : 0.f);
+          if (d == 0 && rnd == 0 && lse != nullptr)
+            lse[orow] = Lsum > 0.f ? (mm + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        } else {
+          const int64_t base = static_cast<int64_t>(slot) * G + h;
+          part_o[base * kD + kHalf * rnd + d] = o;
+          if (d == 0 && rnd == 0) {
+            part_ml[base * 2] = mm;
+            part_ml[base * 2 + 1] = Lsum;
+          }
         }
       }
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
     }
-    (void)row;
+    if (whole) return;
+    // The CTA that completes a row's last segment merges all of them:
+    // partials are made visible with a fence, then counted per row.
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+    if (threadIdx.x == 0) {
+      int nseg = 1;
+      for (int k = 1; k < topk; ++k) nseg += is_range_start(row * topk + k, n_units, gridDim.x);
+      const int old = atomicAdd(row_cnt + row, 1);
+      const bool last = old == nseg - 1;
+      if (last) row_cnt[row] = 0;  // ready for the next call
+      *merge_flag = last;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+    if (*merge_flag) {
+      __threadfence();
+      const int t = row / hkv, g = row % hkv;
+      const int u0 = row * topk;
+      const float vs = v_scale[g];
+      const int64_t q_row = tiles[t].q_begin;
+      for (int e = threadIdx.x; e < G * kD; e += 32 * kCWarps) {
+        const int h = e / kD, d = e % kD;
+        float mm = -INFINITY;
+        for (int k = 0; k < topk; ++k)
+          if (k == 0 || is_range_start(u0 + k, n_units, gridDim.x))
+            mm = fmaxf(mm, __ldcg(part_ml + (static_cast<int64_t>(u0 + k) * G + h) * 2));
+        float Lsum = 0.f, o = 0.f;
+        if (mm != -INFINITY)
+          for (int k = 0; k < topk; ++k) {
+            if (!(k == 0 || is_range_start(u0 + k, n_units, gridDim.x))) continue;
+            const int64_t b = static_cast<int64_t>(u0 + k) * G + h;
+            const float ms = __ldcg(part_ml + b * 2);
+            if (ms == -INFINITY) continue;
+            const float sc = ex2_approx(ms - mm);
+            Lsum += __ldcg(part_ml + b * 2 + 1) * sc;
+            o += __ldcg(part_o + b * kD + d) * sc;
+          }
+        const int64_t orow = q_row * hq + g * G + h;
+        out[orow * kD + d] = __float2bfloat16_rn(Lsum > 0.f ? o / Lsum * vs : 0.f);
+        if (d == 0 && lse != nullptr)
+          lse[orow] = Lsum > 0.f ? (mm + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
   };
 
   for (int u = ub; u < ue; ++u) {
@@ -403,76 +459,13 @@ __global__ void __launch_bounds__(kDThreads)
   if (cur_row >= 0) flush(cur_row, seg);
 }
 
-// Merge the segment partials of each (tile, group) row; apply v_scale.  One
-// warp per (row, head): lanes scan the row's slots for segment starts, then
-// each lane combines four consecutive d values with float4 loads.
-constexpr int kCombineWarps = 8;
-__global__ void __launch_bounds__(32 * kCombineWarps)
-    decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                          const TileInfo* __restrict__ tiles, const float* __restrict__ v_scale,
-                          __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t n_units, int32_t n_ctas,
-                          int32_t hq, int32_t hkv, int32_t topk) {
-  const int lane = threadIdx.x & 31;
-  const int G = hq / hkv;
-  const int64_t wid = static_cast<int64_t>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-  const int rows = n_units / topk;
-  if (wid >= static_cast<int64_t>(rows) * G) return;
-  const int row = static_cast<int>(wid / G), h = static_cast<int>(wid % G);
-  const int t = row / hkv, g = row % hkv;
-  const int u0 = row * topk;
-  float mm = -INFINITY;
-  for (int k0 = 0; k0 < topk; k0 += 32) {
-    const int k = k0 + lane;
-    const int u = u0 + k;
-    const bool st = k < topk && (k == 0 || is_range_start(u, n_units, n_ctas));
-    if (st) mm = fmaxf(mm, part_ml[(static_cast<int64_t>(u) * G + h) * 2]);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xFFFFFFFFu, mm, o));
-  float lsum = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (mm != -INFINITY) {
-    for (int k0 = 0; k0 < topk; k0 += 32) {
-      const int k = k0 + lane;
-      const int u = u0 + k;
-      float sc = 0.f;
-      if (k < topk && (k == 0 || is_range_start(u, n_units, n_ctas))) {
-        const float2 ml = *reinterpret_cast<const float2*>(part_ml + (static_cast<int64_t>(u) * G + h) * 2);
-        if (ml.x != -INFINITY) {
-          sc = ex2_approx(ml.x - mm);
-          lsum += ml.y * sc;
-        }
-      }
-      uint32_t mask = __ballot_sync(0xFFFFFFFFu, sc > 0.f);
-      while (mask) {
-        const int src = __ffs(mask) - 1;
-        mask &= mask - 1;
-        const float scs = __shfl_sync(0xFFFFFFFFu, sc, src);
-        const int64_t b = (static_cast<int64_t>(u0 + k0 + src) * G + h) * kD;
-        const float4 v = *reinterpret_cast<const float4*>(part_o + b + 4 * lane);
-        acc.x += v.x * scs;
-        acc.y += v.y * scs;
-        acc.z += v.z * scs;
-        acc.w += v.w * scs;
-      }
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
-  const float f = lsum > 0.f ? v_scale[g] / lsum : 0.f;
-  const int64_t orow = static_cast<int64_t>(tiles[t].q_begin) * hq + g * G + h;
-  uint2 w;
-  w.x = pack_bf16x2(acc.x * f, acc.y * f);
-  w.y = pack_bf16x2(acc.z * f, acc.w * f);
-  *reinterpret_cast<uint2*>(out + orow * kD + 4 * lane) = w;
-  if (lane == 0 && lse != nullptr) lse[orow] = lsum > 0.f ? (mm + log2f(lsum)) * 0.69314718055994531f : -INFINITY;
-}
-
-int combine_grid(int rows, int G) { return (rows * G + kCombineWarps - 1) / kCombineWarps; }
-
-int decode_grid(const msa_plan_s* p, int n_units) {
-  const int per_sm = (p->hq / p->hkv) <= 8 ? 2 : 1;
-  return std::max(1, std::min(n_units, p->num_sms * per_sm));
+// One CTA per (sequence, group) row when there are enough rows to fill the
+// GPU (no partials, no merge); otherwise rows are cut into near-equal unit
+// ranges over all SMs and merged by the last CTA of each row.
+int decode_grid_rows(int rows, int topk, int num_sms, int G) {
+  if (rows >= num_sms) return rows;
+  const int per_sm = G <= 8 ? 2 : 1;
+  return std::max(1, std::min(rows * topk, num_sms * per_sm));
 }
 
 }  // namespace
@@ -481,7 +474,7 @@ size_t decode_partial_floats(const msa_plan_s* p) {
   if (!p->decode) return 0;
   const size_t units = static_cast<size_t>(p->n_tiles) * p->hkv * p->topk;
   const size_t g = p->hq / p->hkv;
-  return units * g * (kD + 2);
+  return units * g * (kD + 2) + static_cast<size_t>(p->n_tiles) * p->hkv;  // partials + per-row counters
 }
 
 msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
@@ -497,32 +490,29 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
       !encode_tensor_map(&vm, 2, v_pages, dims, str, box, 0, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
   const int n_units = p->n_tiles * p->hkv * p->topk;
-  const int grid = decode_grid(p, n_units);
+  const int grid = decode_grid_rows(p->n_tiles * p->hkv, p->topk, p->num_sms, p->hq / p->hkv);
   const size_t units = static_cast<size_t>(n_units);
   const int G = p->hq / p->hkv;
   float* part_o = p->partial_d;
   float* part_ml = p->partial_d + units * G * kD;
+  int32_t* row_cnt = reinterpret_cast<int32_t*>(part_ml + units * G * 2);  // zeroed by msa_plan
+  auto* o_ptr = static_cast<__nv_bfloat16*>(out);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   if (G <= 8) {
     const int smem = DecodeSmem<1>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
-                                                     part_o, part_ml, n_units, p->hq, p->hkv, p->topk, scale_log2,
-                                                     p->err_d);
+                                                     v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
+                                                     p->hkv, p->topk, scale_log2, p->err_d);
   } else {
     const int smem = DecodeSmem<2>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
-                                                     part_o, part_ml, n_units, p->hq, p->hkv, p->topk, scale_log2,
-                                                     p->err_d);
+                                                     v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
+                                                     p->hkv, p->topk, scale_log2, p->err_d);
   }
-  msa_status s = cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
-  if (s != MSA_OK) return s;
-  decode_combine_kernel<<<combine_grid(p->n_tiles * p->hkv, G), 32 * kCombineWarps, 0, st>>>(part_o, part_ml, p->tiles_d, v_scale,
-                                                             static_cast<__nv_bfloat16*>(out), lse, n_units, grid,
-                                                             p->hq, p->hkv, p->topk);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode combine launch");
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
 }
 
 }  // namespace msa
@@ -548,7 +538,9 @@ constexpr size_t kStaticScratchBytes = size_t(24) << 20;  // 24 MiB
 constexpr int kStaticMaxBatch = 4096;
 constexpr size_t kStaticTilesBytes = sizeof(TileInfo) * kStaticMaxBatch;
 constexpr size_t kStaticErrOff = kStaticTilesBytes;
-constexpr size_t kStaticPartOff = kStaticTilesBytes + 256;
+constexpr int kStaticMaxRows = 65536;  // batch * num_kv_heads
+constexpr size_t kStaticCntOff = kStaticTilesBytes + 256;
+constexpr size_t kStaticPartOff = kStaticCntOff + sizeof(int32_t) * kStaticMaxRows;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
@@ -634,6 +626,8 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
     return set_error(MSA_ERR_INVALID_ARG, "%s: q, k_pages, v_pages, out must be 16-byte aligned", fn);
   if (batch < 1 || batch > kStaticMaxBatch)
     return set_error(MSA_ERR_INVALID_ARG, "%s: batch %d outside [1, %d]", fn, batch, kStaticMaxBatch);
+  if (static_cast<int64_t>(batch) * num_kv_heads > kStaticMaxRows)
+    return set_error(MSA_ERR_INVALID_ARG, "%s: batch * num_kv_heads above %d", fn, kStaticMaxRows);
   if (num_qo_heads < 1 || num_kv_heads < 1 || num_qo_heads % num_kv_heads != 0)
     return set_error(MSA_ERR_INVALID_ARG, "%s: bad head counts", fn);
   if (head_dim != kD) return set_error(MSA_ERR_UNSUPPORTED, "%s: head_dim must be 128", fn);
@@ -657,6 +651,10 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
   uint32_t* err = err_word ? err_word : reinterpret_cast<uint32_t*>(sd.base + kStaticErrOff);
   float* part_o = reinterpret_cast<float*>(sd.base + kStaticPartOff);
   float* part_ml = part_o + n_units * G * kD;
+  // per-row arrival counters: zero when the module loads, reset to zero by
+  // the CTA that merges a row, so every call finds them at zero
+  int32_t* row_cnt = reinterpret_cast<int32_t*>(sd.base + kStaticCntOff);
+  auto* o_ptr = static_cast<__nv_bfloat16*>(out);
 
   CUtensorMap km, vm;
   const uint64_t dims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(num_pages) * num_kv_heads * 128};
@@ -670,26 +668,21 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
   s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: tile table launch");
   if (s != MSA_OK) return s;
   const int nu = static_cast<int>(n_units);
-  const int grid = std::max(1, std::min(nu, sd.num_sms * (G <= 8 ? 2 : 1)));
+  const int grid = decode_grid_rows(batch * num_kv_heads, topk, sd.num_sms, G);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
   if (G <= 8) {
     const int smem = DecodeSmem<1>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
-                                                     k_scale, part_o, part_ml, nu, num_qo_heads, num_kv_heads, topk,
-                                                     scale_log2, err);
+                                                     k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, nu,
+                                                     num_qo_heads, num_kv_heads, topk, scale_log2, err);
   } else {
     const int smem = DecodeSmem<2>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
-                                                     k_scale, part_o, part_ml, nu, num_qo_heads, num_kv_heads, topk,
-                                                     scale_log2, err);
+                                                     k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, nu,
+                                                     num_qo_heads, num_kv_heads, topk, scale_log2, err);
   }
-  s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: decode launch");
-  if (s != MSA_OK) return s;
-  decode_combine_kernel<<<combine_grid(batch * num_kv_heads, G), 32 * kCombineWarps, 0, st>>>(part_o, part_ml, tiles, v_scale,
-                                                              static_cast<__nv_bfloat16*>(out), lse, nu, grid,
-                                                              num_qo_heads, num_kv_heads, topk);
-  return cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: combine launch");
+  return cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: decode launch");
 }

@@ -248,8 +248,8 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
  * fixed 24 MiB device array inside libmsa, held by every GPU that loads the
  * library until the process exits.  The call allocates nothing and calls no
  * allocating routine.  It rejects, with MSA_ERR_INVALID_ARG, batch > 4096 or
- * batch * num_qo_heads * topk above 48,143 (the partials that fit in the
- * array at head_dim 128).  The first call on a device looks up the array's
+ * batch * num_qo_heads * topk above 47,639 (the partials that fit in the
+ * array at head_dim 128) or batch * num_kv_heads above 65,536.  The first call on a device looks up the array's
  * device address for that device (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Every call on a
  * device shares the one array and overwrites what it needs: calls that

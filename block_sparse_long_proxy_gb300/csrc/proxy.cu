@@ -243,7 +243,15 @@ __device__ __forceinline__ void mma_16816(float* c, uint32_t a0, uint32_t a1, ui
 }
 
 // Units are (sequence, block) pairs in order; unit_start[t] is the first unit
-// of tile (sequence) t.
+// of tile (sequence) t.  Warp w takes the contiguous unit range
+// [U*w/W, U*(w+1)/W).  Unit metadata (sequence, block, page row) is computed
+// lane-parallel 32 units at a time, one chunk ahead of the loads, so that
+// the dependent global lookups stay off the per-unit path.
+__device__ __forceinline__ int warp_range_start(int w, int U, int W) {
+  const int q = U / W, r = U % W;
+  return w * q + (w < r ? w : r);
+}
+
 template <int DP>
 __global__ void __launch_bounds__(32 * kDecWarps)
     proxy_decode_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ pq,
@@ -272,41 +280,66 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     fence_mbar_init();
   }
   __syncwarp();
-  const int gw = blockIdx.x * kDecWarps + warp;
   const int nw = gridDim.x * kDecWarps;
+  const int gw = blockIdx.x * kDecWarps + warp;
+  const int ub = warp_range_start(gw, total_units, nw), ue = warp_range_start(gw + 1, total_units, nw);
+  const int n = ue - ub;
 
-  auto locate = [&](int unit, int& t, int& j) {
-    int lo = 0, hi = n_tiles - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (unit_start[mid] <= unit) lo = mid; else hi = mid - 1;
+  // lane l: metadata of unit (chunk_base + l)
+  auto meta = [&](int chunk_base, int& t, int& j, int& row) {
+    const int unit = chunk_base + lane;
+    t = 0;
+    j = 0;
+    row = 0;
+    if (unit < ue) {
+      int lo = 0, hi = n_tiles - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(unit_start + mid) <= unit) lo = mid; else hi = mid - 1;
+      }
+      t = lo;
+      j = unit - __ldg(unit_start + lo);
+      int64_t page = kv_indices[tiles[t].page_base + j];
+      if (page < 0 || page >= num_pages) {
+        atomicOr(err, kErrDeviceCheck);
+        page = 0;
+      }
+      row = static_cast<int>(page * 128);
     }
-    t = lo;
-    j = unit - unit_start[lo];
   };
-  auto issue = [&](int k) {  // k-th unit of this warp into stage k % kDecStages
-    const int unit = gw + k * nw;
-    if (unit >= total_units) return;
-    int t, j;
-    locate(unit, t, j);
-    int64_t page = kv_indices[tiles[t].page_base + j];
-    if (page < 0 || page >= num_pages) {
-      atomicOr(err, kErrDeviceCheck);
-      page = 0;
+  int ct, cj, crow, nt_, nj, nrow;  // current chunk and next chunk metadata
+  meta(ub, ct, cj, crow);
+  meta(ub + 32, nt_, nj, nrow);
+  auto row_of = [&](int i) {  // page row of the warp's i-th unit (i in this or the next chunk)
+    const int c = i >> 5, cur = 0;
+    (void)cur;
+    const int r_cur = __shfl_sync(0xFFFFFFFFu, crow, i & 31);
+    const int r_nxt = __shfl_sync(0xFFFFFFFFu, nrow, i & 31);
+    return c == 0 ? r_cur : r_nxt;
+  };
+  int chunk = 0;  // index of the chunk held in (ct, cj, crow)
+  auto issue = [&](int i) {  // load the warp's i-th unit into stage i % kDecStages
+    if (i >= n) return;
+    const int r = row_of(i - 32 * chunk);
+    if (lane == 0) {
+      uint64_t* bar = bars + (i % kDecStages);
+      mbar_expect_tx(bar, kBlk);
+      tma_load_2d(ring + (i % kDecStages) * kBlk, &k_map, bar, 0, r);
     }
-    uint64_t* bar = bars + (k % kDecStages);
-    mbar_expect_tx(bar, kBlk);
-    tma_load_2d(ring + (k % kDecStages) * kBlk, &k_map, bar, 0, static_cast<int>(page * 128));
   };
-  if (lane == 0)
-    for (int k = 0; k < kDecStages; ++k) issue(k);
+  for (int i = 0; i < kDecStages; ++i) issue(i);
 
   const int g = lane >> 2, t4 = lane & 3;
-  for (int k = 0;; ++k) {
-    const int unit = gw + k * nw;
-    if (unit >= total_units) break;
-    int t, j;
-    locate(unit, t, j);
+  for (int i = 0; i < n; ++i) {
+    if (i - 32 * chunk == 32) {  // move to the next chunk of metadata
+      ct = nt_;
+      cj = nj;
+      crow = nrow;
+      ++chunk;
+      meta(ub + 32 * (chunk + 1), nt_, nj, nrow);
+    }
+    const int t = __shfl_sync(0xFFFFFFFFu, ct, i & 31);
+    const int j = __shfl_sync(0xFFFFFFFFu, cj, i & 31);
     const TileInfo tl = tiles[t];
     // B fragments: pq[row, head n = g, dims]; heads >= hp contribute zeros
     uint32_t bf[DP / 16][2];
@@ -320,8 +353,8 @@ __global__ void __launch_bounds__(32 * kDecWarps)
         bf[kt][0] = bf[kt][1] = 0u;
       }
     }
-    const int s = k % kDecStages;
-    if (!mbar_wait(bars + s, (k / kDecStages) & 1, err)) break;
+    const int s = i % kDecStages;
+    if (!mbar_wait(bars + s, (i / kDecStages) & 1, err)) break;
     const uint32_t base = smem_u32(ring + s * kBlk);
     const int nkeys = min(128, tl.kv_len - j * 128);  // keys past kv_len are not visible
     float mx0 = -INFINITY, mx1 = -INFINITY;
@@ -331,8 +364,8 @@ __global__ void __launch_bounds__(32 * kDecWarps)
 #pragma unroll
       for (int kt = 0; kt < DP / 16; ++kt) {
         const int row = mt * 16 + (lane & 15);
-        const int chunk = kt * 2 + (lane >> 4);
-        const int sw = DP == 64 ? (chunk ^ (row & 7)) : (chunk ^ ((row >> 1) & 3));
+        const int chunk16 = kt * 2 + (lane >> 4);
+        const int sw = DP == 64 ? (chunk16 ^ (row & 7)) : (chunk16 ^ ((row >> 1) & 3));
         uint32_t a0, a1, a2, a3;
         ldmatrix_x4(base + row * kRowBytes + sw * 16, a0, a1, a2, a3);
         mma_16816(c, a0, a1, a2, a3, bf[kt][0], bf[kt][1]);
@@ -342,7 +375,7 @@ __global__ void __launch_bounds__(32 * kDecWarps)
       if (r1 < nkeys) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
     }
     __syncwarp();
-    if (lane == 0) issue(k + kDecStages);
+    issue(i + kDecStages);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));

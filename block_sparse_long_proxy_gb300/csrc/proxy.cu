@@ -10,8 +10,9 @@
 // heads, a chunk of up to 32 KV blocks).  Warp 0 streams the tile's Q slices
 // once and the paged proxy-K blocks through a 4-stage TMA ring; warp 1 issues
 // one 128x128xdp MMA per (block, head) into a ring of four 128-column TMEM
-// accumulators; warps 2-9 read each accumulator back (tcgen05.ld), apply the
-// causal mask on diagonal blocks, and reduce it to one value.  The proxy K
+// accumulators; warps 2-9, as two groups taking alternate accumulators, read
+// each back (tcgen05.ld), apply the causal mask on diagonal blocks, and
+// reduce it to one value.  The proxy K
 // block is read once per tile and shared by all heads (there is one proxy K
 // head).
 //
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNBuf; ++b) {
       mbar_init(t_full + b, 1);
-      mbar_init(t_empty + b, kEpiWarps);
+      mbar_init(t_empty + b, kEpiWarps / 2);  // one group of four warps per accumulator
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -151,10 +152,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(drain, 0, err);
     }
   } else {
-    // epilogue: warp w reads TMEM lanes 32*(w%4).. and one half of the columns
+    // epilogue: two groups of four warps take alternate accumulators (items
+    // 0, 2, 4, ... and 1, 3, 5, ...), so one group's TMEM loads overlap the
+    // other group's reduction; warp w reads TMEM lanes 32*(w%4).. and all
+    // 128 columns of its items
     const int ew = warp - 2;
     const int quarter = warp & 3;
-    const int half = ew >> 2;
+    const int grp = ew >> 2;
     const int r = quarter * 32 + lane;
     const bool row_ok = r < tl.rows;
     const int qpos = tl.pos0 + r;
@@ -163,38 +167,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; ok && i < nblk; ++i) {
       const int j = u.j0 + i;
       const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
-      const int limit = qpos - j * 128 - half * 64;  // columns c (of this half) with c <= limit are visible
+      const int limit = row_ok ? qpos - j * 128 : -1;  // columns c <= limit are visible
       for (int h = 0; h < u.nh; ++h, ++item) {
+        if ((item & 1) != grp) continue;
         const int b = item % kNBuf;
         if (!(ok = mbar_wait(t_full + b, (item / kNBuf) & 1, err))) break;
         tc_fence_after();
-        uint32_t v[64];
-        const uint32_t taddr = tmem + b * 128 + (static_cast<uint32_t>(quarter * 32) << 16) + half * 64;
+        uint32_t v[128];
+        const uint32_t taddr = tmem + b * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
         tmem_ld32(taddr, v);
         tmem_ld32(taddr + 32, v + 32);
+        tmem_ld32(taddr + 64, v + 64);
+        tmem_ld32(taddr + 96, v + 96);
         tmem_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(t_empty + b);
-        float m = -INFINITY;
-        if (!need_mask) {
-          float m0 = __uint_as_float(v[0]), m1 = __uint_as_float(v[1]);
-          float m2 = __uint_as_float(v[2]), m3 = __uint_as_float(v[3]);
+        if (need_mask) {
 #pragma unroll
-          for (int c = 4; c < 64; c += 4) {
-            m0 = fmaxf(m0, __uint_as_float(v[c]));
-            m1 = fmaxf(m1, __uint_as_float(v[c + 1]));
-            m2 = fmaxf(m2, __uint_as_float(v[c + 2]));
-            m3 = fmaxf(m3, __uint_as_float(v[c + 3]));
-          }
-          m = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
-        } else if (row_ok) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c) m = fmaxf(m, c <= limit ? __uint_as_float(v[c]) : -INFINITY);
+          for (int c = 0; c < 128; ++c)
+            if (c > limit) v[c] = __float_as_uint(-INFINITY);
         }
-        if (!row_ok) m = -INFINITY;
+        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 128; c += 8) {
+          m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+          m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+          m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+          m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+        }
+        const float m = fmax3(fmaxf(m0, m1), m2, m3);
         const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
-        if (lane == 0) part[(i * kHeadsPerCta + h) * kEpiWarps + ew] = wm;
+        if (lane == 0) part[(i * kHeadsPerCta + h) * kEpiWarps + quarter] = wm;
       }
     }
     // all epilogue warps: combine the eight partial maxima of each item
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = it / nblk, i = it % nblk;
         int32_t m = part[(i * kHeadsPerCta + h) * kEpiWarps];
 #pragma unroll
-        for (int w = 1; w < kEpiWarps; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
+        for (int w = 1; w < 4; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
         max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = ord2f(m) * scale;
       }
     }

@@ -47,15 +47,38 @@ struct AttnSmem {
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kBlkOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kBlkOff + kMaxTopk * 4;
-  static constexpr int kBytes = kBarOff + 8 * 24;
+  static constexpr int kListOff = kVOff + kStages * kTileBytes;  // block lists: producer, MMA, softmax
+  static constexpr int kBarOff = kListOff + 3 * kMaxTopk * 4;
+  static constexpr int kBytes = kBarOff + 8 * 32;
 };
 
+// The cached blocks of a unit's (tile, group), padding skipped; entries past
+// the tile's valid blocks are dropped (and reported when `report`).
+__device__ __forceinline__ int unit_blocks(const AttnUnit& u, const TileInfo& tl, const int32_t* __restrict__ idx,
+                                           int hkv, int topk, int32_t* out, uint32_t* err, bool report) {
+  const int32_t* row = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
+  int n = 0;
+  for (int k = 0; k < topk; ++k) {
+    const int j = row[k];
+    if (j < 0) continue;
+    if (j >= tl.nvp) {
+      if (report) atomicOr(err, kErrDeviceCheck);
+      continue;
+    }
+    out[n++] = j;
+  }
+  return n;
+}
+
+// Persistent: CTA b takes units b, b + gridDim.x, ... (heaviest first).
+// Tensor memory, barriers and the K/V ring live across units; every
+// barrier's phase comes from a running count (per head for the S / P / O
+// barriers), and Q is released right after a unit's last QK so the next
+// unit's Q load overlaps the tail of the current one.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                    const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units,
+                    const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
@@ -67,28 +90,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = smem + L::kQOff;
   uint8_t* k_s = smem + L::kKOff;
   uint8_t* v_s = smem + L::kVOff;
-  int32_t* blocks = reinterpret_cast<int32_t*>(smem + L::kBlkOff);
+  int32_t* list_p = reinterpret_cast<int32_t*>(smem + L::kListOff);
+  int32_t* list_m = list_p + kMaxTopk;
+  int32_t* list_s = list_m + kMaxTopk;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* k_full = bars + 1;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;
   uint64_t* v_full = k_full + kStages;
   uint64_t* kv_empty = v_full + kStages;
   uint64_t* s_full = kv_empty + kStages;  // [2]
   uint64_t* p_full = s_full + 2;          // [2]
   uint64_t* o_done = p_full + 2;          // [2]
-  uint64_t* drain = o_done + 2;
-  int32_t* nblk_s = reinterpret_cast<int32_t*>(drain + 1);
+  uint64_t* o_free = o_done + 2;          // [2]
+  uint64_t* drain = o_free + 2;
+  volatile int32_t* n_soft = reinterpret_cast<int32_t*>(drain + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const AttnUnit u = units[blockIdx.x];
-  const TileInfo tl = tiles[u.tile];
-
   if (threadIdx.x == 0) {
     prefetch_tmap(&q_map);
     prefetch_tmap(&k_map);
     prefetch_tmap(&v_map);
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(v_full + s, 1);
@@ -98,22 +123,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_full + h, 1);
       mbar_init(p_full + h, 4);
       mbar_init(o_done + h, 1);
+      mbar_init(o_free + h, 4);
     }
     mbar_init(drain, 1);
     fence_mbar_init();
-    // the selected blocks of this (tile, group), skipping padding
-    const int32_t* row = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
-    int n = 0;
-    for (int k = 0; k < topk; ++k) {
-      const int j = row[k];
-      if (j < 0) continue;
-      if (j >= tl.nvp) {
-        atomicOr(err, kErrDeviceCheck);
-        continue;
-      }
-      blocks[n++] = j;
-    }
-    *nblk_s = n;
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -123,30 +136,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n = *nblk_s;
 
   if (warp == 8) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_expect_tx(q_full, u.nh * L::kTileBytes);
-      for (int h = 0; h < u.nh; ++h)
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_3d(q_s + h * L::kTileBytes + c * 16384, &q_map, q_full, c * 64, u.h0 + h, tl.q_begin);
-      for (int i = 0; i < n; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(kv_empty + s, ((i / kStages) & 1) ^ 1, err)) break;
-        int64_t page = kv_indices[tl.page_base + blocks[i]];
-        if (page < 0 || page >= num_pages) {
-          atomicOr(err, kErrDeviceCheck);
-          page = 0;
+      int kv_it = 0;
+      bool ok = true;
+      for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
+        const AttnUnit u = units[ui];
+        const TileInfo tl = tiles[u.tile];
+        const int n = unit_blocks(u, tl, idx, hkv, topk, list_p, err, true);
+        if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, err))) break;
+        mbar_expect_tx(q_full, u.nh * L::kTileBytes);
+        for (int h = 0; h < u.nh; ++h)
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_3d(q_s + h * L::kTileBytes + c * 16384, &q_map, q_full, c * 64, u.h0 + h, tl.q_begin);
+        for (int i = 0; i < n; ++i, ++kv_it) {
+          const int s = kv_it % kStages;
+          if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
+          int64_t page = kv_indices[tl.page_base + list_p[i]];
+          if (page < 0 || page >= num_pages) {
+            atomicOr(err, kErrDeviceCheck);
+            page = 0;
+          }
+          const int row = static_cast<int>((page * hkv + u.g) * 128);
+          mbar_expect_tx(k_full + s, L::kTileBytes);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
+          mbar_expect_tx(v_full + s, L::kTileBytes);
+          for (int c = 0; c < kChunks; ++c)
+            tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, v_full + s, c * 64, row);
         }
-        const int row = static_cast<int>((page * hkv + u.g) * 128);
-        mbar_expect_tx(k_full + s, L::kTileBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
-        mbar_expect_tx(v_full + s, L::kTileBytes);
-        for (int c = 0; c < kChunks; ++c)
-          tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, v_full + s, c * 64, row);
       }
     }
   } else if (warp == 9) {
@@ -164,34 +184,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(s_full + h);
       };
-      auto pv = [&](int h, int s, int i) {
+      auto pv = [&](int h, int s, bool acc) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + 256 + h * D, tmem + h * 128 + kk * 8,
-                 smem_desc(v0 + s * L::kTileBytes + kk * 2048, 16384, 1024, kSwizzle128), id_pv, (i > 0) || (kk > 0));
+                 smem_desc(v0 + s * L::kTileBytes + kk * 2048, 16384, 1024, kSwizzle128), id_pv, acc || (kk > 0));
         mma_commit(o_done + h);
       };
-      bool ok = mbar_wait(q_full, 0, err);
-      if (ok && n > 0) {
-        ok = mbar_wait(k_full, 0, err);
+      int kv_it = 0, ch[2] = {0, 0};
+      bool ok = true;
+      for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
+        const AttnUnit u = units[ui];
+        const TileInfo tl = tiles[u.tile];
+        const int n = unit_blocks(u, tl, idx, hkv, topk, list_m, err, false);
+        if (!(ok = mbar_wait(q_full, k & 1, err))) break;
         tc_fence_after();
-        for (int h = 0; ok && h < u.nh; ++h) qk(h, 0);
+        if (n == 0) {
+          mma_commit(q_empty);
+          continue;
+        }
+        if (!(ok = mbar_wait(k_full + kv_it % kStages, (kv_it / kStages) & 1, err))) break;
+        tc_fence_after();
+        for (int h = 0; h < u.nh; ++h) qk(h, kv_it % kStages);
+        if (n == 1) mma_commit(q_empty);  // the unit's last QK is issued
         for (int i = 0; ok && i < n; ++i) {
-          const int s = i % kStages;
-          const int s1 = (i + 1) % kStages;
+          const int it = kv_it + i;
+          const int s = it % kStages, s1 = (it + 1) % kStages;
           for (int h = 0; h < u.nh; ++h) {
-            if (!(ok = mbar_wait(p_full + h, i & 1, err))) break;
-            if (h == 0 && !(ok = mbar_wait(v_full + s, (i / kStages) & 1, err))) break;
+            if (!(ok = mbar_wait(p_full + h, (ch[h] + i) & 1, err))) break;
+            if (h == 0 && !(ok = mbar_wait(v_full + s, (it / kStages) & 1, err))) break;
+            // the first P.V of a unit overwrites O_h: the previous unit's
+            // epilogue must have read it (the QKs above already overlap it)
+            if (i == 0 && k > 0 && !(ok = mbar_wait(o_free + h, (k - 1) & 1, err))) break;
             tc_fence_after();
-            pv(h, s, i);
+            pv(h, s, i > 0);
             if (h == u.nh - 1) mma_commit(kv_empty + s);
             if (i + 1 < n) {
-              if (h == 0 && !(ok = mbar_wait(k_full + s1, ((i + 1) / kStages) & 1, err))) break;
+              if (h == 0 && !(ok = mbar_wait(k_full + s1, ((it + 1) / kStages) & 1, err))) break;
               tc_fence_after();
               qk(h, s1);
+              if (i + 1 == n - 1 && h == u.nh - 1) mma_commit(q_empty);
             }
           }
         }
+        for (int h = 0; h < u.nh; ++h) ch[h] += n;
+        kv_it += n;
       }
       mma_commit(drain);
       mbar_wait(drain, 0, err);
@@ -201,117 +238,131 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    const bool row_ok = r < tl.rows;
-    const int qpos = tl.pos0 + r;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + h * 128;
     const uint32_t o_addr = tmem + lane_base + 256 + h * D;
-    float m = -INFINITY, l = 0.f;
-    bool ok = h < u.nh;
-    for (int i = 0; ok && i < n; ++i) {
-      if (!(ok = mbar_wait(s_full + h, i & 1, err))) break;
-      tc_fence_after();
-      uint32_t sv[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
-      tmem_wait_ld();
-      const int j = blocks[i];
-      const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
-      if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
-        const int limit = row_ok ? qpos - j * 128 : -1;
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c > limit) sv[c] = __float_as_uint(-INFINITY);
-      }
-      float mx;
-      {  // four independent chains keep the max off the latency path
-        float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          a0 = fmax3(a0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-          a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-          a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
-          a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
-        }
-        mx = fmax3(fmaxf(a0, a1), a2, a3);
-      }
-      // lazy rescaling: the reference max moves only when the row max grows
-      // by more than 2^8, so probabilities stay below 256 and O is rescaled
-      // rarely
-      const float mx2 = mx * scale_log2;
-      const float m_new = mx2 > m + 8.f ? mx2 : m;
-      const float m_use = m_new == -INFINITY ? 0.f : m_new;
-      const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
-      float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x0, x1;
-        ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2, -m_use);
-        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-        if (c & 1)
-          fadd2(sum2, sum3, p0, p1);
-        else
-          fadd2(sum0, sum1, p0, p1);
-        pk[c] = pack_bf16x2(p0, p1);
-      }
-      sum0 += sum2;
-      sum1 += sum3;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st16(s_addr + c * 16, pk + c * 16);
-      l = l * alpha + (sum0 + sum1);
-      // rescale O_h (written by P.V of the previous block, already complete
-      // because the S_h MMA of this block was issued after it)
-      if (i > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-        if (!(ok = mbar_wait(o_done + h, (i - 1) & 1, err))) break;
+    int ch = 0;
+    bool ok = true;
+    for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
+      const AttnUnit u = units[ui];
+      const TileInfo tl = tiles[u.tile];
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kSoftWarps) : "memory");  // previous list no longer read
+      if (threadIdx.x == 0) *n_soft = unit_blocks(u, tl, idx, hkv, topk, list_s, err, false);
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * kSoftWarps) : "memory");
+      const int n = *n_soft;
+      const bool active = ok && h < u.nh;
+      const bool row_ok = r < tl.rows;
+      const int qpos = tl.pos0 + r;
+      float m = -INFINITY, l = 0.f;
+      for (int i = 0; active && ok && i < n; ++i) {
+        if (!(ok = mbar_wait(s_full + h, (ch + i) & 1, err))) break;
         tc_fence_after();
+        uint32_t sv[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
+        tmem_wait_ld();
+        const int j = list_s[i];
+        const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
+        if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
+          const int limit = row_ok ? qpos - j * 128 : -1;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > limit) sv[c] = __float_as_uint(-INFINITY);
+        }
+        float mx;
+        {  // four independent chains keep the max off the latency path
+          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 128; c += 8) {
+            a0 = fmax3(a0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+            a1 = fmax3(a1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+            a2 = fmax3(a2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+            a3 = fmax3(a3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+          }
+          mx = fmax3(fmaxf(a0, a1), a2, a3);
+        }
+        // lazy rescaling: the reference max moves only when the row max grows
+        // by more than 2^8, so probabilities stay below 256 and O is rescaled
+        // rarely
+        const float mx2 = mx * scale_log2;
+        const float m_new = mx2 > m + 8.f ? mx2 : m;
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
+        float sum0 = 0.f, sum1 = 0.f, sum2 = 0.f, sum3 = 0.f;
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float x0, x1;
+          ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2, -m_use);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (c & 1)
+            fadd2(sum2, sum3, p0, p1);
+          else
+            fadd2(sum0, sum1, p0, p1);
+          pk[c] = pack_bf16x2(p0, p1);
+        }
+        sum0 += sum2;
+        sum1 += sum3;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_st16(s_addr + c * 16, pk + c * 16);
+        l = l * alpha + (sum0 + sum1);
+        // rescale O_h (written by P.V of the previous block, already complete
+        // because the S_h MMA of this block was issued after it)
+        if (i > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+          if (!(ok = mbar_wait(o_done + h, (ch + i - 1) & 1, err))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(o_addr + c * 32, ov);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            tmem_st32(o_addr + c * 32, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full + h);
+        m = m_new;
+      }
+      if (active && ok) {
+        if (n > 0) ok = mbar_wait(o_done + h, (ch + n - 1) & 1, err);
+        tc_fence_after();
+        const int64_t orow = static_cast<int64_t>(tl.q_begin + r) * hq + u.h0 + h;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_wait_ld();
+          if (n > 0) {
+            tmem_ld32(o_addr + c * 32, ov);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-          tmem_st32(o_addr + c * 32, ov);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full + h);
-      m = m_new;
-    }
-    if (ok && h < u.nh) {
-      if (n > 0) ok = mbar_wait(o_done + h, (n - 1) & 1, err);
-      tc_fence_after();
-      const int hg = u.h0 + h;
-      const int64_t orow = static_cast<int64_t>(tl.q_begin + r) * hq + hg;
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          }
+          if (ok && row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(out + orow * D + c * 32);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        if (n > 0) {
-          tmem_ld32(o_addr + c * 32, ov);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) ov[e] = 0u;
-        }
-        if (ok && row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(out + orow * D + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
-            dst[e] = w;
+            for (int e = 0; e < 4; ++e) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
+              dst[e] = w;
+            }
           }
         }
+        if (ok && row_ok && lse != nullptr)
+          lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (ok && row_ok && lse != nullptr)
-        lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      if (h < u.nh) ch += n;
+      // O_h may be overwritten by the next unit (every warp arrives, active or not)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free + h);
     }
   }
   tc_fence_before();
@@ -357,16 +408,17 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
   const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->attn_units_off);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->d));
   auto* o = static_cast<__nv_bfloat16*>(out);
+  const int grid = std::min(p->n_attn_units, p->num_sms);  // persistent: one CTA per SM
   if (p->d == 128) {
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<128><<<p->n_attn_units, kThreads, smem, st>>>(qm, km, vm, units, p->tiles_d, idx, kv_indices,
+    attn_fwd_kernel<128><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
                                                                    p->num_pages, o, lse, p->hq, p->hkv, p->topk,
                                                                    scale_log2, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<64><<<p->n_attn_units, kThreads, smem, st>>>(qm, km, vm, units, p->tiles_d, idx, kv_indices,
+    attn_fwd_kernel<64><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
                                                                  p->num_pages, o, lse, p->hq, p->hkv, p->topk,
                                                                  scale_log2, p->err_d);
   }

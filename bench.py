@@ -424,7 +424,8 @@ def run_ncu_case(args):
     """A small case of one kernel for profiler captures (no JSON line):
     inputs above the 129 MB L2 but a few hundred MB on the device.
       attn / proxy / topk: sparse prefill S=16384 (32q/8kv, d=128, topk 16)
-      decode: FP8 paged decode, 32 sequences x 16384 keys."""
+      decode: FP8 paged decode, 32 sequences x 16384 keys
+      bwd: the KL-coupled backward of the S=16384 prefill."""
     import torch
     from block_sparse_long_proxy_gb300 import msa, synth
     torch.cuda.set_device(0)
@@ -434,7 +435,7 @@ def run_ncu_case(args):
                           page_perm_seed=1)
     else:
         case = synth.Case("prefill S=16384", [16384], [16384], 32, 8, 128, 8, 64, 16)
-    inp = synth.make_inputs(case, device=dev)
+    inp = synth.make_inputs(case, device=dev, with_dout=args.ncu_case == "bwd")
     plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
                     num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
     ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
@@ -442,7 +443,12 @@ def run_ncu_case(args):
     kw = {}
     if case.kv_dtype != "bf16":
         kw = dict(k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    if args.ncu_case == "bwd":
+        out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
     for _ in range(args.steps):
+        if args.ncu_case == "bwd":
+            plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out, lse,
+                                 inp["dout"], inp["pq"], inp["pk_pages"])
         if args.ncu_case in ("proxy", "decode"):
             plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
         if args.ncu_case == "topk":
@@ -518,7 +524,7 @@ def bench_train(args, dev, pk_info, peak_kind):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--ncu-case", choices=["attn", "proxy", "topk", "decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["attn", "proxy", "topk", "decode", "bwd"], default=None,
                     help="run a small case of one kernel for a profiler capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)

@@ -9,10 +9,12 @@
 // Prefill kernel (tcgen05): one CTA per work unit = (tile, up to 8 proxy
 // heads, a chunk of up to 32 KV blocks).  Warp 0 streams the tile's Q slices
 // once and the paged proxy-K blocks through a 4-stage TMA ring; warp 1 issues
-// one 128x128xdp MMA per (block, head) into a ring of four 128-column TMEM
-// accumulators; warps 2-9, as two groups taking alternate accumulators, read
-// each back (tcgen05.ld), apply the causal mask on diagonal blocks, and
-// reduce it to one value.  The proxy K
+// one 128x256xdp MMA per (pair of consecutive blocks, head) -- N = 256 keeps
+// the shared-memory operand traffic below the SMEM bandwidth, which a
+// 128x128 MMA saturates -- into two 256-column TMEM accumulators; warps 2-9,
+// as two groups each owning one accumulator, read it back (tcgen05.ld),
+// apply the causal mask on diagonal blocks, and reduce each block to one
+// value.  The proxy K
 // block is read once per tile and shared by all heads (there is one proxy K
 // head).
 //
@@ -31,7 +33,7 @@ namespace {
 constexpr int kHeadsPerCta = 8;
 constexpr int kChunk = 32;
 constexpr int kStages = 4;
-constexpr int kNBuf = 4;
+constexpr int kNBuf = 2;  // TMEM accumulators of 256 columns (one per epilogue group)
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < kNBuf; ++b) {
       mbar_init(t_full + b, 1);
-      mbar_init(t_empty + b, kEpiWarps / 2);  // one group of four warps per accumulator
+      mbar_init(t_empty + b, kEpiWarps / 2);  // the group of four warps reading accumulator b
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -125,37 +127,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+      // one MMA covers two consecutive K blocks (N = 256): the pair sits in
+      // adjacent ring stages, so its 256 rows form one K-major operand
+      constexpr uint32_t id256 = idesc_bf16_f32(128, 256, false, false);
+      constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t sw = DP == 64 ? kSwizzle128 : kSwizzle64;
       constexpr uint32_t sbo = DP == 64 ? 1024 : 512;
       bool ok = mbar_wait(q_full, 0, err);
       int item = 0;
-      for (int i = 0; ok && i < nblk; ++i) {
+      for (int i = 0; ok && i < nblk; i += 2) {
+        const bool pair = i + 1 < nblk;
         const int s = i % kStages;
         if (!(ok = mbar_wait(k_full + s, (i / kStages) & 1, err))) break;
+        if (pair && !(ok = mbar_wait(k_full + s + 1, ((i + 1) / kStages) & 1, err))) break;
         tc_fence_after();
         const uint32_t kaddr = smem_u32(k_s + s * L::kKBytes);
         for (int h = 0; h < u.nh; ++h, ++item) {
-          const int b = item % kNBuf;
-          if (!(ok = mbar_wait(t_empty + b, ((item / kNBuf) & 1) ^ 1, err))) break;
+          const int b = item & 1;  // accumulator b: 256 columns, read by epilogue group b
+          if (!(ok = mbar_wait(t_empty + b, ((item >> 1) & 1) ^ 1, err))) break;
           tc_fence_after();
           const uint32_t qaddr = smem_u32(q_s + h * L::kQBytes);
 #pragma unroll
           for (int kk = 0; kk < DP / 16; ++kk)
-            mma_ss(tmem + b * 128, smem_desc(qaddr + kk * 32, 16, sbo, sw), smem_desc(kaddr + kk * 32, 16, sbo, sw),
-                   idesc, kk > 0);
+            mma_ss(tmem + b * 256, smem_desc(qaddr + kk * 32, 16, sbo, sw), smem_desc(kaddr + kk * 32, 16, sbo, sw),
+                   pair ? id256 : id128, kk > 0);
           mma_commit(t_full + b);
         }
         mma_commit(k_empty + s);
+        if (pair) mma_commit(k_empty + s + 1);
       }
       mma_commit(drain);
       mbar_wait(drain, 0, err);
     }
   } else {
-    // epilogue: two groups of four warps take alternate accumulators (items
-    // 0, 2, 4, ... and 1, 3, 5, ...), so one group's TMEM loads overlap the
-    // other group's reduction; warp w reads TMEM lanes 32*(w%4).. and all
-    // 128 columns of its items
+    // epilogue: two groups of four warps, group b reading accumulator b
+    // (items alternate between them, so one group's TMEM loads overlap the
+    // other group's reduction); an item is one head over a pair of blocks;
+    // warp w reads TMEM lanes 32*(w%4).. and each block's 128 columns
     const int ew = warp - 2;
     const int quarter = warp & 3;
     const int grp = ew >> 2;
@@ -164,41 +172,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qpos = tl.pos0 + r;
     int item = 0;
     bool ok = true;
-    for (int i = 0; ok && i < nblk; ++i) {
-      const int j = u.j0 + i;
-      const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
-      const int limit = row_ok ? qpos - j * 128 : -1;  // columns c <= limit are visible
+    for (int i = 0; ok && i < nblk; i += 2) {
+      const int nb = i + 1 < nblk ? 2 : 1;
       for (int h = 0; h < u.nh; ++h, ++item) {
         if ((item & 1) != grp) continue;
-        const int b = item % kNBuf;
-        if (!(ok = mbar_wait(t_full + b, (item / kNBuf) & 1, err))) break;
+        if (!(ok = mbar_wait(t_full + grp, (item >> 1) & 1, err))) break;
         tc_fence_after();
-        uint32_t v[128];
-        const uint32_t taddr = tmem + b * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
-        tmem_ld32(taddr, v);
-        tmem_ld32(taddr + 32, v + 32);
-        tmem_ld32(taddr + 64, v + 64);
-        tmem_ld32(taddr + 96, v + 96);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(t_empty + b);
-        if (need_mask) {
+        for (int bi = 0; bi < nb; ++bi) {
+          uint32_t v[128];
+          const uint32_t taddr = tmem + grp * 256 + bi * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
+          tmem_ld32(taddr, v);
+          tmem_ld32(taddr + 32, v + 32);
+          tmem_ld32(taddr + 64, v + 64);
+          tmem_ld32(taddr + 96, v + 96);
+          tmem_wait_ld();
+          if (bi == nb - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(t_empty + grp);
+          }
+          const int j = u.j0 + i + bi;
+          if ((j * 128 + 127 > tl.pos0) || (tl.rows < 128)) {  // diagonal / ragged: mask the future
+            const int limit = row_ok ? qpos - j * 128 : -1;
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c > limit) v[c] = __float_as_uint(-INFINITY);
-        }
-        float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+            for (int c = 0; c < 128; ++c)
+              if (c > limit) v[c] = __float_as_uint(-INFINITY);
+          }
+          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; c += 8) {
-          m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-          m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-          m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-          m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+          for (int c = 0; c < 128; c += 8) {
+            m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+            m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+            m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+            m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+          }
+          const float m = fmax3(fmaxf(m0, m1), m2, m3);
+          const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
+          if (lane == 0) part[((i + bi) * kHeadsPerCta + h) * kEpiWarps + quarter] = wm;
         }
-        const float m = fmax3(fmaxf(m0, m1), m2, m3);
-        const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
-        if (lane == 0) part[(i * kHeadsPerCta + h) * kEpiWarps + quarter] = wm;
       }
     }
     // all epilogue warps: combine the eight partial maxima of each item

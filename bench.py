@@ -37,9 +37,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # dram bytes of one attention-forward launch at the 32K prefill workload from
 # an ncu capture, valid only for the kernel source it was taken on.
-# Captured on S=16384 (15424 selected tile-blocks: 246.3 MB read + 112.9 MB
+# Captured on S=16384 (15424 selected tile-blocks: 247.8 MB read + 108.4 MB
 # written) and scaled by selected tile-blocks to the S=32768 launch (31808).
-NCU_TRAFFIC = {"attn_fwd.cu": {"src": "f06e313925f79092", "bytes": int((246285312 + 112910336) * 31808 / 15424),
+NCU_TRAFFIC = {"attn_fwd.cu": {"src": "03f16e76199c16f4", "bytes": int((247794176 + 108398848) * 31808 / 15424),
                                "source": "profiles/attn_fwd_prefill.md"}}
 
 

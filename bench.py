@@ -106,27 +106,46 @@ class ClockSampler:
 
 
 def dist_setup(args):
+    """One process per GPU under torchrun; NCCL on GPUs, gloo on a host-only run."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local if world > 1 else 0)
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
 
-def allreduce_max(x, world):
+def _reduce(x, world, op):
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def allreduce_max(x, world):
+    import torch.distributed as dist
+    return _reduce(x, world, dist.ReduceOp.MAX if world > 1 else None)
+
+
+def allreduce_sum(x, world):
+    import torch.distributed as dist
+    return _reduce(x, world, dist.ReduceOp.SUM if world > 1 else None)
+
+
+def job_throughput(units_local, ms_local, world):
+    """Whole-job throughput of independent replicas: the units every rank
+    processed divided by the slowest rank's time.  Returns (units/s, max ms)."""
+    ms = allreduce_max(ms_local, world)
+    units = allreduce_sum(units_local, world)
+    return units / (ms / 1e3), ms
 
 
 def barrier(world):
@@ -260,12 +279,10 @@ def run_ours(args):
     plan.check_errors()
     st = [[evs[k][i].elapsed_time(evs[k][i + 1]) for i in range(3)] for k in range(args.steps)]
     step_ms = [sum(s) for s in st]
-    total_ms = allreduce_max(sum(step_ms), world)
+    value, total_ms = job_throughput(case.total_q * args.steps, sum(step_ms), world)
     proxy_ms = statistics.mean(s[0] for s in st)
     topk_ms = statistics.mean(s[1] for s in st)
     attn_ms = statistics.mean(s[2] for s in st)
-    tokens = case.total_q * world * args.steps
-    value = tokens / (total_ms / 1e3)
 
     # proxy FLOPs: causal lower triangle of 128x128 blocks per proxy head
     proxy_flops = sum(t.nvp for t in plan_tiles(case)) * case.hp * 2.0 * 128 * 128 * case.dp
@@ -301,8 +318,7 @@ def run_ours(args):
         out_host.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = allreduce_max(e0.elapsed_time(e1), world)
-    e2e_value = case.total_q * world * e2e_steps / (e2e_ms / 1e3)
+    e2e_value, e2e_ms = job_throughput(case.total_q * e2e_steps, e0.elapsed_time(e1), world)
 
     decode = bench_decode(args, dev, pk_info, peak_kind, world)
     train = bench_train(args, dev, pk_info, peak_kind)

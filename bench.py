@@ -105,6 +105,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class L2Flush:
+    """Evicts L2 between timed steps, outside the timed region: a 256 MiB
+    write followed by a 256 MiB read of a second buffer, so that the dirty
+    lines of the write are written back before the next step starts and the
+    step finds L2 holding only clean, unrelated lines."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+        self.r = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.sum()
+
+
 def dist_setup(args):
     """One process per GPU under torchrun; NCCL on GPUs, gloo on a host-only run."""
     import torch
@@ -243,7 +259,7 @@ def run_ours(args):
     idx = torch.empty((plan.n_tiles, case.hkv, case.topk), dtype=torch.int32, device=dev)
     out = torch.empty_like(inp["q"])
     lse = torch.empty((plan.total_q, case.hq), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
 
     def step(ev=None):
@@ -271,7 +287,7 @@ def run_ours(args):
     with ClockSampler(local) as clk:
         t_wall = time.perf_counter()
         for k in range(args.steps):
-            flush.zero_()                      # evict L2 between timed steps (untimed)
+            flush()                            # evict L2 between timed steps (untimed)
             step(evs[k])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
@@ -329,7 +345,7 @@ def run_ours(args):
             "config": {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
                        "proxy_heads": 8, "proxy_dim": 64, "topk": 16, "page_size": 128,
                        "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "flushed between timed steps (256 MiB write)"},
+                       "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)"},
             "stages_ms": {"proxy_maxscore": proxy_ms, "topk_select": topk_ms, "sparse_attn": attn_ms},
             "tflops_selected": attn_tflops, "proxy_tflops": proxy_tflops,
             "roofline": roofline,
@@ -405,7 +421,7 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
         return {"unavailable": str(e)}
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
     n_sel = int((idx >= 0).sum().item())
     kv_bytes = n_sel * 2 * 128 * case.d          # e4m3 K and V of each selected (seq, group, block)
     io_bytes = 2 * out.numel() * 2 + lse.numel() * 4
@@ -414,7 +430,7 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
     for _ in range(3):
         attn()
     for _ in range(reps):
-        flush.zero_()
+        flush()
         a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         a.record(stream)
         plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
@@ -424,8 +440,9 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
         torch.cuda.synchronize()
         ptimes.append(a.elapsed_time(b))
         times.append(b.elapsed_time(c))
-    t = statistics.median(times) / 1e3
-    tp = statistics.median(ptimes) / 1e3
+    # mean, not median: the event clock ticks in ~2 us steps, a mean averages over them
+    t = statistics.mean(times) / 1e3
+    tp = statistics.mean(ptimes) / 1e3
     gbs = (kv_bytes + io_bytes) / t / 1e9
     proxy_bytes = sum((k + 127) // 128 for k in case.kv_lens) * 128 * case.dp * 2
     hbm = pk_info.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -498,7 +515,7 @@ def bench_train(args, dev, pk_info, peak_kind):
                  dpq=torch.empty(inp["pq"].shape, dtype=torch.float32, device=dev),
                  dpk=torch.zeros(inp["pk_pages"].shape, dtype=torch.float32, device=dev))
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = L2Flush(dev)
 
     def fwd():
         plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
@@ -519,7 +536,7 @@ def bench_train(args, dev, pk_info, peak_kind):
     f_bwd = n_sel * grp * 10.0 * 128 * 128 * case.d + n_sel * 8.0 * 128 * 128 * case.dp
     tf, tb = [], []
     for _ in range(max(3, min(args.steps, 10))):
-        flush.zero_()
+        flush()
         a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
         a.record(stream)
         fwd()

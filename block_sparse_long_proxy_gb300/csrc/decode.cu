@@ -32,6 +32,12 @@ namespace {
 
 constexpr int kD = 128;                 // head dim of this kernel
 constexpr int kCWarps = 4;              // consumer warps
+constexpr int kKeysW = 128 / kCWarps;   // keys of a block per consumer warp
+constexpr int kMT = kKeysW / 16;        // 16-key m-tiles per consumer warp
+constexpr int kRounds = 2;              // the merge moves d in kRounds slices
+constexpr int kDR = 128 / kRounds;      // d per merge slice
+static_assert(kRounds == 1 || kRounds == 2 || kRounds == 4, "a merge slice holds whole m-tile pairs");
+static_assert(kMT >= 1 && kKeysW % 16 == 0, "consumer warps take whole 16-key m-tiles");
 constexpr int kDThreads = 32 * (kCWarps + 1);
 constexpr int kDStages = 3;
 constexpr int kBlk = 128 * kD;          // bytes of one e4m3 K (or V) block
@@ -81,18 +87,18 @@ __host__ __device__ __forceinline__ int range_start(int c, int U, int C) {
   const int q = U / C, r = U % C;
   return c * q + (c < r ? c : r);
 }
-__device__ __forceinline__ bool is_range_start(int u, int U, int C) {
+// the CTA whose range holds unit u (inverse of range_start)
+__device__ __forceinline__ int range_owner(int u, int U, int C) {
   const int q = U / C, r = U % C;
-  if (u < r * (q + 1)) return u % (q + 1) == 0;
-  return q > 0 && (u - r * (q + 1)) % q == 0;
+  return u < r * (q + 1) ? u / (q + 1) : r + (u - r * (q + 1)) / q;
 }
 
 template <int NT>
 struct DecodeSmem {
   static constexpr int kRingOff = 0;
   static constexpr int kScratchOff = kDStages * 2 * kBlk;
-  // per-warp merge scratch, one half of d at a time: [warp][head slot][64 + 2]
-  static constexpr int kScratchFloats = kCWarps * 8 * NT * (kD / 2 + 2);
+  // per-warp merge scratch, one slice of d at a time: [warp][head slot][kDR + 2]
+  static constexpr int kScratchFloats = kCWarps * 8 * NT * (kDR + 2);
   static constexpr int kBarOff = kScratchOff + kScratchFloats * 4;
   static constexpr int kStageJOff = kBarOff + 8 * 2 * kDStages;
   static constexpr int kFlagOff = kStageJOff + 4 * kDStages;
@@ -100,7 +106,7 @@ struct DecodeSmem {
 };
 
 template <int NT>  // n-tiles of 8 heads: group size G <= 8*NT
-__global__ void __launch_bounds__(kDThreads)
+__global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
     decode_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                   const __nv_bfloat16* __restrict__ q, const TileInfo* __restrict__ tiles,
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(kDThreads)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DecodeSmem<NT>;
   constexpr int kSlots = 8 * NT;  // head slots of the per-warp scratch
-  constexpr int kHalf = kD / 2;
+  constexpr int kHalf = kDR;
   uint8_t* ring = smem + L::kRingOff;
   float* scratch = reinterpret_cast<float*>(smem + L::kScratchOff);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
@@ -214,10 +220,10 @@ __global__ void __launch_bounds__(kDThreads)
         v += __shfl_xor_sync(0xFFFFFFFFu, v, 16);
         l[nt][c] = v;
       }
-    // merge the four warps' states one half of d at a time (two rounds)
-    float* wsc = scratch + w * kSlots * (kHalf + 2);  // [head slot][64 + 2]: O half, m, l
+    // merge the consumer warps' states one slice of d at a time
+    float* wsc = scratch + w * kSlots * (kHalf + 2);  // [head slot][kDR + 2]: O slice, m, l
 #pragma unroll
-    for (int rnd = 0; rnd < 2; ++rnd) {
+    for (int rnd = 0; rnd < kRounds; ++rnd) {
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -229,8 +235,8 @@ __global__ void __launch_bounds__(kDThreads)
               wsc[h * (kHalf + 2) + kHalf + 1] = l[nt][c];
             }
 #pragma unroll
-            for (int mh = 0; mh < 4; ++mh) {
-              const int md = 4 * rnd + mh;  // m-tiles 4rnd..4rnd+3 hold d in [64rnd, 64rnd+64)
+            for (int mh = 0; mh < 8 / kRounds; ++mh) {
+              const int md = 8 / kRounds * rnd + mh;  // m-tile md holds d in [32(md/2), 32(md/2)+32)
               const int d0 = 32 * (md >> 1) + 4 * gi + 2 * (md & 1) - kHalf * rnd;
               wsc[h * (kHalf + 2) + d0] = oacc[md][nt][c];
               wsc[h * (kHalf + 2) + d0 + 1] = oacc[md][nt][2 + c];
@@ -273,43 +279,62 @@ __global__ void __launch_bounds__(kDThreads)
     // partials are made visible with a fence, then counted per row.
     __threadfence();
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
+    // The row's segments start at u0 and at every range start inside it:
+    // one per CTA from the owner of u0 to the owner of its last unit.
+    const int u0 = row * topk;
+    const int c0 = range_owner(u0, n_units, gridDim.x);
+    const int c1 = range_owner(u0 + topk - 1, n_units, gridDim.x);
+    const int rq = n_units / gridDim.x, rr = n_units % gridDim.x;
     if (threadIdx.x == 0) {
-      int nseg = 1;
-      for (int k = 1; k < topk; ++k) nseg += is_range_start(row * topk + k, n_units, gridDim.x);
       const int old = atomicAdd(row_cnt + row, 1);
-      const bool last = old == nseg - 1;
+      const bool last = old == c1 - c0;
       if (last) row_cnt[row] = 0;  // ready for the next call
       *merge_flag = last;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
     if (*merge_flag) {
+      // Online merge over the row's segments, one segment per step: every
+      // thread owns one d column of all G heads, so the loads of a segment
+      // (m, l and O of each head) are independent and issue together.
       __threadfence();
       const int t = row / hkv, g = row % hkv;
-      const int u0 = row * topk;
       const float vs = v_scale[g];
       const int64_t q_row = tiles[t].q_begin;
-      for (int e = threadIdx.x; e < G * kD; e += 32 * kCWarps) {
-        const int h = e / kD, d = e % kD;
-        float mm = -INFINITY;
-        for (int k = 0; k < topk; ++k)
-          if (k == 0 || is_range_start(u0 + k, n_units, gridDim.x))
-            mm = fmaxf(mm, __ldcg(part_ml + (static_cast<int64_t>(u0 + k) * G + h) * 2));
-        float Lsum = 0.f, o = 0.f;
-        if (mm != -INFINITY)
-          for (int k = 0; k < topk; ++k) {
-            if (!(k == 0 || is_range_start(u0 + k, n_units, gridDim.x))) continue;
-            const int64_t b = static_cast<int64_t>(u0 + k) * G + h;
-            const float ms = __ldcg(part_ml + b * 2);
-            if (ms == -INFINITY) continue;
-            const float sc = ex2_approx(ms - mm);
-            Lsum += __ldcg(part_ml + b * 2 + 1) * sc;
-            o += __ldcg(part_o + b * kD + d) * sc;
+      for (int d = threadIdx.x; d < kD; d += 32 * kCWarps)
+#pragma unroll 1
+        for (int hb = 0; hb < G; hb += 8) {  // eight heads at a time
+          float M[8], Ls[8], Od[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) M[k] = -INFINITY, Ls[k] = 0.f, Od[k] = 0.f;
+          for (int c = c0; c <= c1; ++c) {
+            const int64_t b0 = static_cast<int64_t>(max(u0, c * rq + min(c, rr))) * G + hb;
+            float ms[8], ls[8], po[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (hb + k < G) {
+                ms[k] = __ldcg(part_ml + (b0 + k) * 2);
+                ls[k] = __ldcg(part_ml + (b0 + k) * 2 + 1);
+                po[k] = __ldcg(part_o + (b0 + k) * kD + d);
+              }
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              if (hb + k < G && ms[k] != -INFINITY) {
+                const float mn = fmaxf(M[k], ms[k]);
+                const float a = ex2_approx(M[k] - mn), sc = ex2_approx(ms[k] - mn);
+                Ls[k] = Ls[k] * a + ls[k] * sc;
+                Od[k] = Od[k] * a + po[k] * sc;
+                M[k] = mn;
+              }
           }
-        const int64_t orow = q_row * hq + g * G + h;
-        out[orow * kD + d] = __float2bfloat16_rn(Lsum > 0.f ? o / Lsum * vs : 0.f);
-        if (d == 0 && lse != nullptr)
-          lse[orow] = Lsum > 0.f ? (mm + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-      }
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (hb + k < G) {
+              const int64_t orow = q_row * hq + g * G + hb + k;
+              out[orow * kD + d] = __float2bfloat16_rn(Ls[k] > 0.f ? Od[k] / Ls[k] * vs : 0.f);
+              if (d == 0 && lse != nullptr)
+                lse[orow] = Ls[k] > 0.f ? (M[k] + log2f(Ls[k])) * 0.69314718055994531f : -INFINITY;
+            }
+        }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kCWarps) : "memory");
   };
@@ -363,14 +388,14 @@ __global__ void __launch_bounds__(kDThreads)
     const uint32_t vb = kb + kBlk;
 
     // S^T for this warp's 32 keys
-    float sacc[2][NT][4];
+    float sacc[kMT][NT][4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+    for (int mt = 0; mt < kMT; ++mt)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) sacc[mt][nt][0] = sacc[mt][nt][1] = sacc[mt][nt][2] = sacc[mt][nt][3] = 0.f;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int ra = 32 * w + 16 * mt + gi, rb = ra + 8;
+    for (int mt = 0; mt < kMT; ++mt) {
+      const int ra = kKeysW * w + 16 * mt + gi, rb = ra + 8;
 #pragma unroll
       for (int kc = 0; kc < kD / 16; ++kc) {
         const uint32_t wa = lds32(kb + swz(ra, kc * 16 + 4 * t4));
@@ -382,9 +407,9 @@ __global__ void __launch_bounds__(kDThreads)
       }
     }
     // mask keys past the query position, scale into the log2 domain
-    const int kpos0 = j * 128 + 32 * w + gi;
+    const int kpos0 = j * 128 + kKeysW * w + gi;
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
+    for (int mt = 0; mt < kMT; ++mt) {
       const bool va = kpos0 + 16 * mt <= qpos, vb2 = kpos0 + 16 * mt + 8 <= qpos;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -395,13 +420,15 @@ __global__ void __launch_bounds__(kDThreads)
       }
     }
     // online softmax per head column
-    uint32_t pb[2][NT][2];
+    uint32_t pb[kMT][NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       float alpha[2];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
-        float mx = fmaxf(fmaxf(sacc[0][nt][c], sacc[0][nt][2 + c]), fmaxf(sacc[1][nt][c], sacc[1][nt][2 + c]));
+        float mx = fmaxf(sacc[0][nt][c], sacc[0][nt][2 + c]);
+#pragma unroll
+        for (int mt = 1; mt < kMT; ++mt) mx = fmaxf(mx, fmaxf(sacc[mt][nt][c], sacc[mt][nt][2 + c]));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 4));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 8));
         mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));
@@ -411,7 +438,7 @@ __global__ void __launch_bounds__(kDThreads)
         m[nt][c] = m_new;
         float sum = 0.f;
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
+        for (int mt = 0; mt < kMT; ++mt) {
           sacc[mt][nt][c] = ex2_approx(sacc[mt][nt][c] - m_use);
           sacc[mt][nt][2 + c] = ex2_approx(sacc[mt][nt][2 + c] - m_use);
           sum += sacc[mt][nt][c] + sacc[mt][nt][2 + c];
@@ -426,15 +453,15 @@ __global__ void __launch_bounds__(kDThreads)
         oacc[md][nt][3] *= alpha[1];
       }
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
+      for (int mt = 0; mt < kMT; ++mt) {
         pb[mt][nt][0] = movmatrix_t(pack_f16x2(sacc[mt][nt][0], sacc[mt][nt][1]));
         pb[mt][nt][1] = movmatrix_t(pack_f16x2(sacc[mt][nt][2], sacc[mt][nt][3]));
       }
     }
     // O^T += V^T P^T over this warp's 32 keys
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-      const int r0 = 32 * w + 16 * mt + 2 * t4;
+    for (int mt = 0; mt < kMT; ++mt) {
+      const int r0 = kKeysW * w + 16 * mt + 2 * t4;
 #pragma unroll
       for (int qg = 0; qg < kD / 32; ++qg) {
         const int col = 32 * qg + 4 * gi;

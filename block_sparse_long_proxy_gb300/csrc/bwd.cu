@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(kThreads)
     bwd_prep_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, const __nv_bfloat16* __restrict__ out,
                     const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ pq,
-                    const __nv_bfloat16* __restrict__ pk, float* __restrict__ dsum, float* __restrict__ lsep,
-                    float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, float kl_weight, uint32_t* err) {
+                    const __nv_bfloat16* __restrict__ pk, const float* __restrict__ lse, float* __restrict__ dsumt,
+                    float* __restrict__ lse2t, float* __restrict__ lsept, float* __restrict__ dpq, int32_t hq,
+                    int32_t hkv, int32_t topk, int32_t total_q, float kl_weight, uint32_t* err) {
   __shared__ __align__(16) __nv_bfloat16 pqs[128 * kLdP];
   __shared__ __align__(16) __nv_bfloat16 pks[128 * kLdP];
   const int t = blockIdx.x / hkv, g = blockIdx.x % hkv;
@@ -140,7 +141,11 @@ __global__ void __launch_bounds__(kThreads)
         }
       }
       acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-      if ((lane & 1) == 0 && r < tl.rows) dsum[static_cast<int64_t>(tl.q_begin + r) * hq + h] = acc;
+      if ((lane & 1) == 0 && r < tl.rows) {
+        const int64_t q_row = tl.q_begin + r;
+        dsumt[static_cast<int64_t>(h) * total_q + q_row] = acc;
+        lse2t[static_cast<int64_t>(h) * total_q + q_row] = lse[q_row * hq + h] * kLog2e;
+      }
     }
 
   // proxy softmax over the cached visible keys (online), O_proxy = p_proxy.pk
@@ -243,8 +248,8 @@ __global__ void __launch_bounds__(kThreads)
   }
   const float f = kl_weight * rsqrtf(static_cast<float>(kDP));
   const float i0 = l0 > 0.f ? f / l0 : 0.f, i1 = l1 > 0.f ? f / l1 : 0.f;
-  if (ok0 && t4 == 0) lsep[static_cast<int64_t>(tl.q_begin + r0) * hkv + g] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-  if (ok1 && t4 == 0) lsep[static_cast<int64_t>(tl.q_begin + r1) * hkv + g] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  if (ok0 && t4 == 0) lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r0] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
+  if (ok1 && t4 == 0) lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r1] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < 8; ++nt) {
     const int c = nt * 8 + 2 * t4;
@@ -278,8 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const int32_t* __restrict__ kv_indices, int64_t num_pages, const __nv_bfloat16* __restrict__ q,
                   const __nv_bfloat16* __restrict__ kp, const __nv_bfloat16* __restrict__ vp,
                   const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                  const float* __restrict__ dsum, const __nv_bfloat16* __restrict__ pk, float* __restrict__ dq,
-                  float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, float kl_weight) {
+                  const float* __restrict__ dsumt, const __nv_bfloat16* __restrict__ pk, float* __restrict__ dq,
+                  float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, int32_t total_q, float kl_weight) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_raw);
   const int t = blockIdx.x / hq, h = blockIdx.x % hq;
@@ -295,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool ok = r < tl.rows;
     const int64_t e = static_cast<int64_t>(tl.q_begin + r) * hq + h;
     sm.lse2[r] = ok ? lse[e] * kLog2e : 0.f;
-    sm.dsum[r] = ok ? dsum[e] : 0.f;
+    sm.dsum[r] = ok ? dsumt[static_cast<int64_t>(h) * total_q + tl.q_begin + r] : 0.f;
   }
   const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
   const int r0 = warp * 16 + gr, r1 = r0 + 8;
@@ -486,279 +491,12 @@ __global__ void bwd_zero_dpk_kernel(const int32_t* __restrict__ kv_indices, int3
   for (int i = threadIdx.x; i < 128 * kDP / 4; i += blockDim.x) p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// ---------------------------------------------------------------- dk / dv
-
-constexpr int kMaxList = 2048;  // tiles per (block, group) sorted in shared memory
-
-struct DkvSmem {
-  __nv_bfloat16 k[128 * kLd];
-  __nv_bfloat16 v[128 * kLd];
-  __nv_bfloat16 q[128 * kLd];
-  __nv_bfloat16 dout[128 * kLd];
-  __nv_bfloat16 pk[128 * kLdP];
-  __nv_bfloat16 pq[128 * kLdP];
-  float dpk[128 * kDP];
-  float lse2[128];
-  float dsum[128];
-  float lsep[128];
-  int32_t list[kMaxList];
-};
-
-// (rows of two n8-tiles) -> A fragments: see the C->A reuse note in the prep
-// kernel.  Writes pa[kc][0..3] for k chunk kc from C tiles 2kc, 2kc+1.
-template <int NTILES>
-__device__ __forceinline__ void c_to_a(const float (*c)[4], uint32_t (*a)[4]) {
-#pragma unroll
-  for (int nt = 0; nt < NTILES; ++nt) {
-    a[nt >> 1][(nt & 1) * 2 + 0] = pack2(c[nt][0], c[nt][1]);
-    a[nt >> 1][(nt & 1) * 2 + 1] = pack2(c[nt][2], c[nt][3]);
-  }
-}
-
-// Per (page-table entry e, group g): the tiles that cached block e for group
-// g, sorted ascending.  Warp w owns keys 16w..16w+15 of the block; query
-// rows are taken 64 at a time.
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_dkv_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ blk_j,
-                   const int32_t* __restrict__ inv_off, const int32_t* __restrict__ inv_list,
-                   const int32_t* __restrict__ kv_indices, int64_t num_pages, const __nv_bfloat16* __restrict__ q,
-                   const __nv_bfloat16* __restrict__ kp, const __nv_bfloat16* __restrict__ vp,
-                   const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                   const float* __restrict__ dsum, const float* __restrict__ lsep,
-                   const __nv_bfloat16* __restrict__ pq, const __nv_bfloat16* __restrict__ pk, float* __restrict__ dk,
-                   float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, float kl_weight) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  DkvSmem& sm = *reinterpret_cast<DkvSmem*>(smem_raw);
-  const int e = blockIdx.x / hkv, g = blockIdx.x % hkv;
-  const int G = hq / hkv;
-  const int j = blk_j[e];
-  int64_t page = kv_indices[e];
-  const bool page_ok = page >= 0 && page < num_pages;
-  if (!page_ok) page = 0;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t4 = lane & 3;
-  const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
-
-  // the tile list, sorted so that every run sums in the same order
-  const bool sorted = n <= kMaxList;
-  if (sorted) {
-    int pow2 = 1;
-    while (pow2 < n) pow2 <<= 1;
-    for (int i = threadIdx.x; i < pow2; i += blockDim.x) sm.list[i] = i < n ? inv_list[lb + i] : 0x7FFFFFFF;
-    __syncthreads();
-    for (int size = 2; size <= pow2; size <<= 1)
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
-          const int o = i ^ stride;
-          if (o > i) {
-            const bool up = (i & size) == 0;
-            const int a = sm.list[i], b = sm.list[o];
-            if ((a > b) == up) {
-              sm.list[i] = b;
-              sm.list[o] = a;
-            }
-          }
-        }
-        __syncthreads();
-      }
-  }
-  const int64_t kv_off = (page * hkv + g) * 128 * kD;
-  load_tile<kD>(sm.k, kp + kv_off, kD, 128);
-  load_tile<kD>(sm.v, vp + kv_off, kD, 128);
-  load_tile<kDP>(sm.pk, pk + page * 128 * kDP, kDP, 128);
-  for (int i = threadIdx.x; i < 128 * kDP; i += blockDim.x) sm.dpk[i] = 0.f;
-  __syncthreads();
-
-  const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
-  const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
-  const float f_proxy = kl_weight * rsqrtf(static_cast<float>(kDP));
-  const float f_main = -f_proxy / static_cast<float>(G);
-  const int key0 = warp * 16 + gr;
-  const int kp0 = j * 128 + key0, kp1 = kp0 + 8;
-  float dka[16][4], dva[16][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    dka[i][0] = dka[i][1] = dka[i][2] = dka[i][3] = 0.f;
-    dva[i][0] = dva[i][1] = dva[i][2] = dva[i][3] = 0.f;
-  }
-
-  for (int it = 0; it < n; ++it) {
-    const int t = sorted ? sm.list[it] : inv_list[lb + it];
-    const TileInfo tl = tiles[t];
-    __syncthreads();  // previous tile's reads of pq / lsep are done
-    load_tile<kDP>(sm.pq, pq + (static_cast<int64_t>(tl.q_begin) * hkv + g) * kDP, static_cast<int64_t>(hkv) * kDP,
-                   tl.rows);
-    for (int r = threadIdx.x; r < 128; r += blockDim.x)
-      sm.lsep[r] = r < tl.rows ? lsep[static_cast<int64_t>(tl.q_begin + r) * hkv + g] : 0.f;
-    cp_async_wait_all();
-    __syncthreads();
-    // proxy term: dpk += w/sqrt(dp) * p_proxy^T . pq
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float z[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) z[i][0] = z[i][1] = z[i][2] = z[i][3] = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < kDP / 16; ++kc) {
-        uint32_t a[4];
-        frag_a(sm.pk, kLdP, warp * 16, kc * 16, a);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b[4];
-          frag_b_nk(sm.pq, kLdP, c * 64 + np * 16, kc * 16, b);
-          mma_bf16(z[2 * np], a, b[0], b[1]);
-          mma_bf16(z[2 * np + 1], a, b[2], b[3]);
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int r = c * 64 + nt * 8 + 2 * t4 + cc;
-          const int qp = tl.pos0 + r;
-          const bool rok = r < tl.rows;
-          z[nt][cc] = (rok && kp0 <= qp) ? ex2_approx(z[nt][cc] * zsl2 - sm.lsep[r]) : 0.f;
-          z[nt][2 + cc] = (rok && kp1 <= qp) ? ex2_approx(z[nt][2 + cc] * zsl2 - sm.lsep[r]) : 0.f;
-        }
-      uint32_t pa[4][4];
-      c_to_a<8>(z, pa);
-      float tmp[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) tmp[i][0] = tmp[i][1] = tmp[i][2] = tmp[i][3] = 0.f;
-#pragma unroll
-      for (int kc = 0; kc < 4; ++kc)
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b[4];
-          frag_b_kn(sm.pq, kLdP, c * 64 + kc * 16, np * 16, b);
-          mma_bf16(tmp[2 * np], pa[kc], b[0], b[1]);
-          mma_bf16(tmp[2 * np + 1], pa[kc], b[2], b[3]);
-        }
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        const int col = nt * 8 + 2 * t4;
-        sm.dpk[key0 * kDP + col] += tmp[nt][0] * f_proxy;
-        sm.dpk[key0 * kDP + col + 1] += tmp[nt][1] * f_proxy;
-        sm.dpk[(key0 + 8) * kDP + col] += tmp[nt][2] * f_proxy;
-        sm.dpk[(key0 + 8) * kDP + col + 1] += tmp[nt][3] * f_proxy;
-      }
-    }
-    for (int h = g * G; h < (g + 1) * G; ++h) {
-      __syncthreads();  // previous head's reads of q / dout / lse2 / dsum are done
-      const int64_t qoff = (static_cast<int64_t>(tl.q_begin) * hq + h) * kD;
-      load_tile<kD>(sm.q, q + qoff, static_cast<int64_t>(hq) * kD, tl.rows);
-      load_tile<kD>(sm.dout, dout + qoff, static_cast<int64_t>(hq) * kD, tl.rows);
-      for (int r = threadIdx.x; r < 128; r += blockDim.x) {
-        const bool ok = r < tl.rows;
-        const int64_t ei = static_cast<int64_t>(tl.q_begin + r) * hq + h;
-        sm.lse2[r] = ok ? lse[ei] * kLog2e : 0.f;
-        sm.dsum[r] = ok ? dsum[ei] : 0.f;
-      }
-      cp_async_wait_all();
-      __syncthreads();
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        float st[8][4], dpt[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          st[i][0] = st[i][1] = st[i][2] = st[i][3] = 0.f;
-          dpt[i][0] = dpt[i][1] = dpt[i][2] = dpt[i][3] = 0.f;
-        }
-#pragma unroll
-        for (int kc = 0; kc < kD / 16; ++kc) {
-          uint32_t ak[4], av[4];
-          frag_a(sm.k, kLd, warp * 16, kc * 16, ak);
-          frag_a(sm.v, kLd, warp * 16, kc * 16, av);
-#pragma unroll
-          for (int np = 0; np < 4; ++np) {
-            uint32_t b[4];
-            frag_b_nk(sm.q, kLd, c * 64 + np * 16, kc * 16, b);
-            mma_bf16(st[2 * np], ak, b[0], b[1]);
-            mma_bf16(st[2 * np + 1], ak, b[2], b[3]);
-            frag_b_nk(sm.dout, kLd, c * 64 + np * 16, kc * 16, b);
-            mma_bf16(dpt[2 * np], av, b[0], b[1]);
-            mma_bf16(dpt[2 * np + 1], av, b[2], b[3]);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int r = c * 64 + nt * 8 + 2 * t4 + cc;
-            const int qp = tl.pos0 + r;
-            const bool rok = r < tl.rows;
-            const float l2 = sm.lse2[r], dd = sm.dsum[r];
-            const float p0 = (rok && kp0 <= qp) ? ex2_approx(st[nt][cc] * sl2 - l2) : 0.f;
-            const float p1 = (rok && kp1 <= qp) ? ex2_approx(st[nt][2 + cc] * sl2 - l2) : 0.f;
-            dpt[nt][cc] = p0 * (dpt[nt][cc] - dd);
-            dpt[nt][2 + cc] = p1 * (dpt[nt][2 + cc] - dd);
-            st[nt][cc] = p0;
-            st[nt][2 + cc] = p1;
-          }
-        uint32_t pa[4][4], sa[4][4];
-        c_to_a<8>(st, pa);
-        c_to_a<8>(dpt, sa);
-        float tmp[8][4];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) tmp[i][0] = tmp[i][1] = tmp[i][2] = tmp[i][3] = 0.f;
-#pragma unroll
-        for (int kc = 0; kc < 4; ++kc) {
-#pragma unroll
-          for (int np = 0; np < 8; ++np) {
-            uint32_t b[4];
-            frag_b_kn(sm.dout, kLd, c * 64 + kc * 16, np * 16, b);
-            mma_bf16(dva[2 * np], pa[kc], b[0], b[1]);
-            mma_bf16(dva[2 * np + 1], pa[kc], b[2], b[3]);
-            frag_b_kn(sm.q, kLd, c * 64 + kc * 16, np * 16, b);
-            mma_bf16(dka[2 * np], sa[kc], b[0], b[1]);
-            mma_bf16(dka[2 * np + 1], sa[kc], b[2], b[3]);
-          }
-#pragma unroll
-          for (int np = 0; np < 4; ++np) {
-            uint32_t b[4];
-            frag_b_kn(sm.pq, kLdP, c * 64 + kc * 16, np * 16, b);
-            mma_bf16(tmp[2 * np], pa[kc], b[0], b[1]);
-            mma_bf16(tmp[2 * np + 1], pa[kc], b[2], b[3]);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int col = nt * 8 + 2 * t4;
-          sm.dpk[key0 * kDP + col] += tmp[nt][0] * f_main;
-          sm.dpk[key0 * kDP + col + 1] += tmp[nt][1] * f_main;
-          sm.dpk[(key0 + 8) * kDP + col] += tmp[nt][2] * f_main;
-          sm.dpk[(key0 + 8) * kDP + col + 1] += tmp[nt][3] * f_main;
-        }
-      }
-    }
-  }
-  cp_async_wait_all();
-  if (!page_ok) return;  // nothing of a bad page is written (the error was raised by prep)
-  const float ks = rsqrtf(static_cast<float>(kD));
-  float* dkr = dk + (page * hkv + g) * 128 * kD;
-  float* dvr = dv + (page * hkv + g) * 128 * kD;
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int col = nt * 8 + 2 * t4;
-    *reinterpret_cast<float2*>(dkr + key0 * kD + col) = make_float2(dka[nt][0] * ks, dka[nt][1] * ks);
-    *reinterpret_cast<float2*>(dkr + (key0 + 8) * kD + col) = make_float2(dka[nt][2] * ks, dka[nt][3] * ks);
-    *reinterpret_cast<float2*>(dvr + key0 * kD + col) = make_float2(dva[nt][0], dva[nt][1]);
-    *reinterpret_cast<float2*>(dvr + (key0 + 8) * kD + col) = make_float2(dva[nt][2], dva[nt][3]);
-  }
-  __syncwarp();
-  float* dpkr = dpk + page * 128 * kDP;
-  for (int i = lane; i < 16 * kDP; i += 32) {
-    const int r = warp * 16 + i / kDP, c = i % kDP;
-    atomicAdd(dpkr + r * kDP + c, sm.dpk[r * kDP + c]);
-  }
-}
-
 }  // namespace
 
 size_t bwd_scratch_bytes(const msa_plan_s* p) {
   if (p->decode) return 0;
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
-  const size_t bytes = sizeof(float) * static_cast<size_t>(p->total_q) * (p->hq + p->hkv) +
+  const size_t bytes = sizeof(float) * static_cast<size_t>(p->total_q) * (2 * p->hq + p->hkv) +
                        sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk);
   return (bytes + 255) & ~size_t(255);
 }
@@ -781,9 +519,10 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   if (p->bwd_d == nullptr) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: plan has no backward scratch");
   const int n_ent = p->n_page_entries;
   const size_t ent = static_cast<size_t>(n_ent) * p->hkv;
-  float* dsum = reinterpret_cast<float*>(p->bwd_d);
-  float* lsep = dsum + static_cast<size_t>(p->total_q) * p->hq;
-  int32_t* cnt = reinterpret_cast<int32_t*>(lsep + static_cast<size_t>(p->total_q) * p->hkv);
+  float* dsumt = reinterpret_cast<float*>(p->bwd_d);               // [hq][total_q]
+  float* lse2t = dsumt + static_cast<size_t>(p->total_q) * p->hq;  // [hq][total_q], lse * log2(e)
+  float* lsept = lse2t + static_cast<size_t>(p->total_q) * p->hq;  // [hkv][total_q], log2 units
+  int32_t* cnt = reinterpret_cast<int32_t*>(lsept + static_cast<size_t>(p->total_q) * p->hkv);
   int32_t* off = cnt + ent;
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
@@ -799,8 +538,8 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
 
   bwd_zero_dpk_kernel<<<n_ent, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, dpk);
   bwd_prep_kernel<<<p->n_tiles * p->hkv, kThreads, 0, st>>>(p->tiles_d, idx, kv_indices, p->num_pages, O, dO, PQ, PK,
-                                                           dsum, lsep, dpq, p->hq, p->hkv, p->topk, kl_weight,
-                                                           p->err_d);
+                                                           lse, dsumt, lse2t, lsept, dpq, p->hq, p->hkv, p->topk,
+                                                           static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
   msa_status s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s != MSA_OK) return s;
   const int sel_blocks = static_cast<int>((n_sel + 255) / 256);
@@ -810,14 +549,12 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   const int dq_smem = sizeof(DqSmem);
   cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem);
   bwd_dq_kernel<<<p->n_tiles * p->hq, kThreads, dq_smem, st>>>(p->tiles_d, idx, kv_indices, p->num_pages, Q, K, V, dO,
-                                                              lse, dsum, PK, dq, dpq, p->hq, p->hkv, p->topk,
-                                                              kl_weight);
-  const int dkv_smem = sizeof(DkvSmem);
-  cudaFuncSetAttribute(bwd_dkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dkv_smem);
-  bwd_dkv_kernel<<<n_ent * p->hkv, kThreads, dkv_smem, st>>>(p->tiles_d, blk_j, off, list, kv_indices, p->num_pages,
-                                                             Q, K, V, dO, lse, dsum, lsep, PQ, PK, dk, dv, dpk, p->hq,
-                                                             p->hkv, kl_weight);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
+                                                              lse, dsumt, PK, dq, dpq, p->hq, p->hkv, p->topk,
+                                                              static_cast<int32_t>(p->total_q), kl_weight);
+  s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
+  if (s != MSA_OK) return s;
+  return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, blk_j, off, list, lse2t, dsumt,
+                           lsept, dk, dv, dpk, kl_weight, st);
 }
 
 }  // namespace msa

@@ -1,0 +1,452 @@
+// Training extension, key side: dK, dV and the proxy-key gradient dpk of
+// block-sparse GQA attention with the KL-coupled proxy (Flash-MSA article,
+// backward-pass paragraph), on the tcgen05 tensor cores.
+//
+// One CTA per (cached block e, GQA group g).  It walks the tiles that cached
+// block e for group g (the inverse index, sorted so sums are deterministic),
+// 64 query rows at a time, and for each of the group's G heads:
+//   S^T  = K . Q_h^T            dP^T = V . dO_h^T       (M = keys, N = rows)
+//   P^T  = exp2(S^T sl2 - lse2)  dS^T = P^T * (dP^T - D)  (masked: causal, ragged)
+//   dV  += P^T . dO_h           dK  += dS^T . Q_h       (P^T, dS^T from TMEM)
+//   dpk += P^T . pq
+// and once per 64 rows, for the proxy distribution over the same keys:
+//   Sp^T = pk . pq^T,  Pp^T = exp2(Sp^T zsl2 - lsep),  dpk += (-G Pp^T) . pq
+// so that at the end dpk * (-w / (G sqrt(dp))) = w/sqrt(dp) (Pp - mean_h P_h)^T pq,
+// this group's share of the KL gradient with respect to the proxy keys.
+//
+// Tensor memory (512 columns): S^T 64 | dP^T 64 | Sp^T 64 | dV 128 | dpk 64 | dK 128.
+// The softmax warps overwrite S^T, dP^T and Sp^T in place with bf16 pairs.
+// Each warpgroup owns 32 of the 64 rows, and each writes its packed pairs
+// into the first half of its own 32 columns, so a k-step of 16 rows of an
+// A operand in TMEM starts at column (kk / 2) * 32 + (kk % 2) * 8.
+// Roles: warps 0-7 softmax (warp w reads TMEM lanes 32 (w % 4) ...), warp 8
+// TMA producer (K, V, pk once; then rings of Q/dO halves and pq halves,
+// with their per-row lse2 / D / lsep staged by the same warp), warp 9 MMA.
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kDP = 64;
+constexpr int kQStages = 3;
+constexpr int kPqStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kMaxList = 2048;
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr uint32_t kColS = 0, kColDP = 64, kColSP = 128, kColDV = 192, kColDPK = 320, kColDK = 384;
+
+struct DkvSmem {
+  static constexpr int kKOff = 0;                               // K block: 2 x [128 keys][128 B]
+  static constexpr int kVOff = kKOff + 32768;                   // V block
+  static constexpr int kPkOff = kVOff + 32768;                  // pk block: [128 keys][128 B]
+  static constexpr int kQdOff = kPkOff + 16384;                 // ring: Q half 2 x [64][128 B] | dO half
+  static constexpr int kQdBytes = 32768;
+  static constexpr int kPqOff = kQdOff + kQStages * kQdBytes;   // ring: pq half [64 rows][128 B]
+  static constexpr int kRowOff = kPqOff + kPqStages * 8192;     // Q stage s: lse2[64], D[64]; pq stage: lsep[64]
+  static constexpr int kLsepOff = kRowOff + kQStages * 128 * 4;
+  static constexpr int kListOff = kLsepOff + kPqStages * 64 * 4;
+  static constexpr int kBarOff = kListOff + kMaxList * 4;
+  static constexpr int kBytes = kBarOff + 8 * 24;
+};
+
+__device__ __forceinline__ uint32_t ts_col(uint32_t base, int kk) {
+  return base + static_cast<uint32_t>((kk >> 1) * 32 + (kk & 1) * 8);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
+                      const __grid_constant__ CUtensorMap pq_map, const __grid_constant__ CUtensorMap k_map,
+                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap pk_map,
+                      const TileInfo* __restrict__ tiles, const int32_t* __restrict__ blk_j,
+                      const int32_t* __restrict__ inv_off, const int32_t* __restrict__ inv_list,
+                      const int32_t* __restrict__ kv_indices, int64_t num_pages, const float* __restrict__ lse2t,
+                      const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
+                      float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, int32_t total_q,
+                      float kl_weight, uint32_t* err) {
+  using L = DkvSmem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int e = blockIdx.x / hkv, g = blockIdx.x % hkv;
+  const int G = hq / hkv;
+  const int j = blk_j[e];
+  int64_t page = kv_indices[e];
+  const bool page_ok = page >= 0 && page < num_pages;
+  if (!page_ok) page = 0;
+  const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
+  const int64_t kv_off = (page * hkv + g) * 128 * kD;
+
+  if (n == 0) {  // never cached: dK = dV = 0, nothing to add to dpk
+    if (!page_ok) return;
+    float4* a = reinterpret_cast<float4*>(dk + kv_off);
+    float4* b = reinterpret_cast<float4*>(dv + kv_off);
+    for (int i = threadIdx.x; i < 128 * kD / 4; i += blockDim.x) {
+      a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      b[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    return;
+  }
+
+  uint8_t* k_s = smem + L::kKOff;
+  uint8_t* v_s = smem + L::kVOff;
+  uint8_t* pk_s = smem + L::kPkOff;
+  uint8_t* qd_s = smem + L::kQdOff;
+  uint8_t* pq_s = smem + L::kPqOff;
+  float* row_s = reinterpret_cast<float*>(smem + L::kRowOff);
+  float* lsep_s = reinterpret_cast<float*>(smem + L::kLsepOff);
+  int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* kv_full = bars;
+  uint64_t* zero_done = bars + 1;
+  uint64_t* qd_full = bars + 2;                 // [kQStages]
+  uint64_t* qd_empty = qd_full + kQStages;      // [kQStages]
+  uint64_t* pq_full = qd_empty + kQStages;      // [kPqStages]
+  uint64_t* pq_empty = pq_full + kPqStages;     // [kPqStages]
+  uint64_t* sp_full = pq_empty + kPqStages;
+  uint64_t* pp_full = sp_full + 1;
+  uint64_t* s_full = pp_full + 1;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* done = p_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&q_map);
+    prefetch_tmap(&do_map);
+    prefetch_tmap(&pq_map);
+    prefetch_tmap(&k_map);
+    prefetch_tmap(&v_map);
+    prefetch_tmap(&pk_map);
+    mbar_init(kv_full, 1);
+    mbar_init(zero_done, kSoftWarps);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(qd_full + s, 2);  // expect_tx arrival + the staged lse2 / D
+      mbar_init(qd_empty + s, 1);
+    }
+    for (int s = 0; s < kPqStages; ++s) {
+      mbar_init(pq_full + s, 2);
+      mbar_init(pq_empty + s, 1);
+    }
+    mbar_init(sp_full, 1);
+    mbar_init(pp_full, kSoftWarps);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kSoftWarps);
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  // the tile list, sorted so that every run sums in the same order
+  const bool sorted = n <= kMaxList;
+  if (sorted) {
+    int pow2 = 1;
+    while (pow2 < n) pow2 <<= 1;
+    for (int i = threadIdx.x; i < pow2; i += blockDim.x) list[i] = i < n ? inv_list[lb + i] : 0x7FFFFFFF;
+    __syncthreads();
+    for (int size = 2; size <= pow2; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+          const int o = i ^ stride;
+          if (o > i) {
+            const bool up = (i & size) == 0;
+            const int a = list[i], b = list[o];
+            if ((a > b) == up) {
+              list[i] = b;
+              list[o] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  auto tile_at = [&](int it) { return sorted ? list[it] : inv_list[lb + it]; };
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- producer
+    bool ok = true;
+    if (lane == 0) {
+      mbar_expect_tx(kv_full, 2 * 32768 + 16384);
+      const int row = static_cast<int>((page * hkv + g) * 128);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_2d(k_s + c * 16384, &k_map, kv_full, c * 64, row);
+        tma_load_2d(v_s + c * 16384, &v_map, kv_full, c * 64, row);
+      }
+      tma_load_2d(pk_s, &pk_map, kv_full, 0, static_cast<int>(page * 128));
+    }
+    int qi = 0, pi = 0;
+    for (int it = 0; ok && it < n; ++it) {
+      const TileInfo tl = tiles[tile_at(it)];
+      const int halves = tl.rows > 64 ? 2 : 1;
+      for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
+        const int r0 = tl.q_begin + hf * 64;
+        const int ps = pi % kPqStages;
+        if (!(ok = mbar_wait(pq_empty + ps, ((pi / kPqStages) & 1) ^ 1, err))) break;
+        if (lane == 0) {
+          mbar_expect_tx(pq_full + ps, 8192);
+          tma_load_3d(pq_s + ps * 8192, &pq_map, pq_full + ps, 0, g, r0);
+        }
+        for (int rr = lane; rr < 64; rr += 32) {
+          const int r = hf * 64 + rr;
+          lsep_s[ps * 64 + rr] = r < tl.rows ? lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r] : 0.f;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pq_full + ps);
+        for (int hh = 0; hh < G; ++hh, ++qi) {
+          const int h = g * G + hh;
+          const int s = qi % kQStages;
+          if (!(ok = mbar_wait(qd_empty + s, ((qi / kQStages) & 1) ^ 1, err))) break;
+          uint8_t* st = qd_s + s * L::kQdBytes;
+          if (lane == 0) {
+            mbar_expect_tx(qd_full + s, L::kQdBytes);
+            for (int c = 0; c < 2; ++c) {
+              tma_load_3d(st + c * 8192, &q_map, qd_full + s, c * 64, h, r0);
+              tma_load_3d(st + 16384 + c * 8192, &do_map, qd_full + s, c * 64, h, r0);
+            }
+          }
+          for (int rr = lane; rr < 64; rr += 32) {
+            const int r = hf * 64 + rr;
+            const bool rok = r < tl.rows;
+            const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
+            row_s[s * 128 + rr] = rok ? lse2t[ei] : 0.f;
+            row_s[s * 128 + 64 + rr] = rok ? dsumt[ei] : 0.f;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(qd_full + s);
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T, Sp^T
+      constexpr uint32_t id_d = idesc_bf16_f32(128, 128, false, true);   // dV, dK (B rows-major)
+      constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpk
+      const uint32_t k0 = smem_u32(k_s), v0 = smem_u32(v_s), pk0 = smem_u32(pk_s);
+      const uint32_t qd0 = smem_u32(qd_s), pq0 = smem_u32(pq_s);
+      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(zero_done, 0, err);
+      tc_fence_after();
+      int qi = 0, pi = 0;
+      for (int it = 0; ok && it < n; ++it) {
+        const TileInfo tl = tiles[tile_at(it)];
+        const int halves = tl.rows > 64 ? 2 : 1;
+        for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
+          const int ps = pi % kPqStages;
+          const uint32_t pqa = pq0 + ps * 8192;
+          if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kDP / 16; ++kk)
+            mma_ss(tmem + kColSP, smem_desc(pk0 + kk * 32, 16, 1024, kSwizzle128),
+                   smem_desc(pqa + kk * 32, 16, 1024, kSwizzle128), id_s, kk > 0);
+          mma_commit(sp_full);
+          for (int hh = 0; ok && hh < G; ++hh, ++qi) {
+            const int s = qi % kQStages;
+            const uint32_t qa = qd0 + s * L::kQdBytes, da = qa + 16384;
+            if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
+              mma_ss(tmem + kColS, smem_desc(k0 + oa, 16, 1024, kSwizzle128),
+                     smem_desc(qa + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
+              mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
+                     smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+            }
+            mma_commit(s_full);
+            if (!(ok = mbar_wait(p_full, qi & 1, err))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), smem_desc(da + kk * 2048, 8192, 1024, kSwizzle128),
+                     id_d, 1);
+              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128),
+                     id_p, 1);
+              mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), smem_desc(qa + kk * 2048, 8192, 1024, kSwizzle128),
+                     id_d, 1);
+            }
+            mma_commit(qd_empty + s);
+          }
+          if (!ok || !(ok = mbar_wait(pp_full, pi & 1, err))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kColDPK, ts_col(tmem + kColSP, kk), smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128),
+                   id_p, 1);
+          mma_commit(pq_empty + ps);
+        }
+      }
+      mma_commit(done);
+    }
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int wg = warp >> 2, quarter = warp & 3;
+    const int key = quarter * 32 + lane;
+    const int c0 = wg * 32;  // this warpgroup's rows within the 64-row half
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const int kpos = j * 128 + key;
+    const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
+    const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
+    const float neg_g = -static_cast<float>(G);
+    {  // dV, dpk, dK start at zero: columns 192..511, 160 per warpgroup
+      uint32_t z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+#pragma unroll
+      for (int c = 0; c < 10; ++c) tmem_st16(lane_base + kColDV + wg * 160 + c * 16, z);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(zero_done);
+    }
+    bool ok = true;
+    int qi = 0, pi = 0;
+    for (int it = 0; ok && it < n; ++it) {
+      const TileInfo tl = tiles[tile_at(it)];
+      const int halves = tl.rows > 64 ? 2 : 1;
+      for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
+        const int ps = pi % kPqStages;
+        const int rbase = hf * 64 + c0;  // tile row of column 0 of this warpgroup
+        // proxy probabilities over this block's keys, scaled by -G
+        if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
+        if (!(ok = mbar_wait(sp_full, pi & 1, err))) break;
+        tc_fence_after();
+        {
+          uint32_t sv[32], pk[16];
+          tmem_ld32(lane_base + kColSP + c0, sv);
+          tmem_wait_ld();
+          const float* lp = lsep_s + ps * 64 + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int r = rbase + c;
+            const bool ok0 = r < tl.rows && kpos <= tl.pos0 + r;
+            const bool ok1 = r + 1 < tl.rows && kpos <= tl.pos0 + r + 1;
+            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[c]) * zsl2 - lp[c]) : 0.f;
+            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[c + 1]) * zsl2 - lp[c + 1]) : 0.f;
+            pk[c >> 1] = pack_bf16x2(p0 * neg_g, p1 * neg_g);
+          }
+          tmem_st16(lane_base + kColSP + c0, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pp_full);
+        for (int hh = 0; ok && hh < G; ++hh, ++qi) {
+          const int s = qi % kQStages;
+          if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
+          if (!(ok = mbar_wait(s_full, qi & 1, err))) break;
+          tc_fence_after();
+          uint32_t sv[32], dv_[32], pa[16], da[16];
+          tmem_ld32(lane_base + kColS + c0, sv);
+          tmem_ld32(lane_base + kColDP + c0, dv_);
+          tmem_wait_ld();
+          const float* l2 = row_s + s * 128 + c0;
+          const float* dd = row_s + s * 128 + 64 + c0;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int r = rbase + c;
+            const bool ok0 = r < tl.rows && kpos <= tl.pos0 + r;
+            const bool ok1 = r + 1 < tl.rows && kpos <= tl.pos0 + r + 1;
+            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[c]) * sl2 - l2[c]) : 0.f;
+            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[c + 1]) * sl2 - l2[c + 1]) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dv_[c]) - dd[c]);
+            const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dd[c + 1]);
+            pa[c >> 1] = pack_bf16x2(p0, p1);
+            da[c >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(lane_base + kColS + c0, pa);
+          tmem_st16(lane_base + kColDP + c0, da);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
+        }
+      }
+    }
+    // epilogue: dV and dK rows are owned (plain stores), dpk is shared by the
+    // groups (fp32 atomics)
+    if (ok) ok = mbar_wait(done, 0, err);
+    tc_fence_after();
+    if (ok && page_ok) {
+      const float ks = rsqrtf(static_cast<float>(kD));
+      const float f_main = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
+      float* dvr = dv + kv_off + static_cast<int64_t>(key) * kD + wg * 64;
+      float* dkr = dk + kv_off + static_cast<int64_t>(key) * kD + wg * 64;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(lane_base + kColDV + wg * 64 + c * 32, a);
+        tmem_ld32(lane_base + kColDK + wg * 64 + c * 32, b);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          reinterpret_cast<float4*>(dvr + c * 32)[i] =
+              make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]), __uint_as_float(a[4 * i + 2]),
+                          __uint_as_float(a[4 * i + 3]));
+          reinterpret_cast<float4*>(dkr + c * 32)[i] =
+              make_float4(__uint_as_float(b[4 * i]) * ks, __uint_as_float(b[4 * i + 1]) * ks,
+                          __uint_as_float(b[4 * i + 2]) * ks, __uint_as_float(b[4 * i + 3]) * ks);
+        }
+      }
+      uint32_t a[32];
+      tmem_ld32(lane_base + kColDPK + wg * 32, a);
+      tmem_wait_ld();
+      float* dpkr = dpk + (page * 128 + key) * kDP + wg * 32;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) atomicAdd(dpkr + i, __uint_as_float(a[i]) * f_main);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                             const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                             const int32_t* blk_j, const int32_t* inv_off, const int32_t* inv_list,
+                             const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
+                             float* dpk, float kl_weight, cudaStream_t st) {
+  CUtensorMap qm, dom, pqm, km, vm, pkm;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
+                             static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(p->hq) * kD * 2};
+  const uint32_t qbox[3] = {64, 1, 64};
+  const uint64_t pqdims[3] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->hkv),
+                              static_cast<uint64_t>(p->total_q)};
+  const uint64_t pqstr[2] = {static_cast<uint64_t>(kDP) * 2, static_cast<uint64_t>(p->hkv) * kDP * 2};
+  const uint64_t kdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t kstr[1] = {static_cast<uint64_t>(kD) * 2};
+  const uint32_t kbox[2] = {64, 128};
+  const uint64_t pkdims[2] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t pkstr[1] = {static_cast<uint64_t>(kDP) * 2};
+  if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&dom, 3, dout, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&pqm, 3, pq, pqdims, pqstr, qbox, 1, 128) ||
+      !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, 1, 128) ||
+      !encode_tensor_map(&pkm, 2, pk_pages, pkdims, pkstr, kbox, 1, 128))
+    return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
+  const int smem = DkvSmem::kBytes + 1024;
+  cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
+      qm, dom, pqm, km, vm, pkm, p->tiles_d, blk_j, inv_off, inv_list, kv_indices, p->num_pages, lse2t, dsumt, lsept,
+      dk, dv, dpk, p->hq, p->hkv, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
+}
+
+}  // namespace msa

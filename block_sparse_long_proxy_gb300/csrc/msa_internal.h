@@ -76,6 +76,13 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
+// dK, dV and dpk on the tensor cores (bwd_dkv.cu); lse2t, dsumt, lsept are
+// the row statistics written by the prep kernel, [heads][total_q].
+msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                             const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                             const int32_t* blk_j, const int32_t* inv_off, const int32_t* inv_list,
+                             const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
+                             float* dpk, float kl_weight, cudaStream_t st);
 
 // ---- launchers (each returns MSA_OK or an error with its message set) ----
 msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,

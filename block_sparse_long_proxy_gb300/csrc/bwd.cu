@@ -17,16 +17,18 @@
 //
 // Kernels, in stream order:
 //   zero     dpk rows of every referenced page (it is reduced by atomics)
-//   prep     per (tile, group): D of the group's heads; the proxy LSE over
-//            Omega (online softmax) and dpq's proxy term (plain store)
+//   prep     per (tile, group): D of the group's heads and lse * log2(e),
+//            both stored [head][row]; the proxy LSE over Omega (online
+//            softmax, [group][row]) and dpq's proxy term (plain store)
 //   index    block -> tiles inverse index of the cached selections
-//   dq       per (tile, head): dq (owned, plain store) and dpq's main term
-//            (fp32 atomics, G per element)
-//   dkv      per (cached block, group): loops over the tiles that selected
-//            the block (sorted, so sums are deterministic); dk, dv (owned,
-//            plain store) and dpk (both terms, fp32 atomics across groups)
-// The matrix products use mma.sync m16n8k16 (bf16 in, f32 accumulate) with
-// ldmatrix fragments from padded shared-memory tiles.
+//   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
+//            store) and dpq's main term (fp32 atomics, G per element)
+//   dkv      per (cached block, group), tcgen05 (bwd_dkv.cu): loops over
+//            the tiles that selected the block (sorted, so sums are
+//            deterministic); dk, dv (owned, plain store) and dpk (both
+//            terms, fp32 atomics across groups)
+// The prep kernel's small products use mma.sync m16n8k16 (bf16 in, f32
+// accumulate) with ldmatrix fragments from padded shared-memory tiles.
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -37,7 +39,6 @@ namespace {
 
 constexpr int kD = 128;    // head dim of this kernel
 constexpr int kDP = 64;    // proxy head dim of this kernel
-constexpr int kLd = kD + 8;    // padded smem row (bf16) of 128-wide tiles: 272 B
 constexpr int kLdP = kDP + 8;  // padded smem row of 64-wide tiles: 144 B
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
@@ -262,169 +263,6 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// -------------------------------------------------------------------- dq
-
-struct DqSmem {
-  __nv_bfloat16 q[128 * kLd];
-  __nv_bfloat16 dout[128 * kLd];
-  __nv_bfloat16 k[128 * kLd];
-  __nv_bfloat16 v[128 * kLd];
-  __nv_bfloat16 pk[128 * kLdP];
-  float lse2[128];
-  float dsum[128];
-};
-
-// Per (tile, head): dq over the cached blocks (plain store) and dpq's main
-// term -(w / (G sqrt(dp))) P.pk (fp32 atomics: the G heads of a group add
-// into the same dpq row).  Warp w owns rows 16w..16w+15; keys are taken 64
-// at a time.
-__global__ void __launch_bounds__(kThreads, 1)
-    bwd_dq_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
-                  const int32_t* __restrict__ kv_indices, int64_t num_pages, const __nv_bfloat16* __restrict__ q,
-                  const __nv_bfloat16* __restrict__ kp, const __nv_bfloat16* __restrict__ vp,
-                  const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
-                  const float* __restrict__ dsumt, const __nv_bfloat16* __restrict__ pk, float* __restrict__ dq,
-                  float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, int32_t total_q, float kl_weight) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_raw);
-  const int t = blockIdx.x / hq, h = blockIdx.x % hq;
-  const int G = hq / hkv, g = h / G;
-  const TileInfo tl = tiles[t];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t4 = lane & 3;
-  const int64_t rs = static_cast<int64_t>(hq) * kD;  // row stride of q / dout / dq
-
-  load_tile<kD>(sm.q, q + (static_cast<int64_t>(tl.q_begin) * hq + h) * kD, rs, tl.rows);
-  load_tile<kD>(sm.dout, dout + (static_cast<int64_t>(tl.q_begin) * hq + h) * kD, rs, tl.rows);
-  for (int r = threadIdx.x; r < 128; r += blockDim.x) {
-    const bool ok = r < tl.rows;
-    const int64_t e = static_cast<int64_t>(tl.q_begin + r) * hq + h;
-    sm.lse2[r] = ok ? lse[e] * kLog2e : 0.f;
-    sm.dsum[r] = ok ? dsumt[static_cast<int64_t>(h) * total_q + tl.q_begin + r] : 0.f;
-  }
-  const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
-  const int r0 = warp * 16 + gr, r1 = r0 + 8;
-  const bool ok0 = r0 < tl.rows, ok1 = r1 < tl.rows;
-  const int qp0 = tl.pos0 + r0, qp1 = tl.pos0 + r1;
-  float acc[16][4], opk[8][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) opk[i][0] = opk[i][1] = opk[i][2] = opk[i][3] = 0.f;
-  float l2a = 0.f, l2b = 0.f, da = 0.f, db = 0.f;
-  bool first = true;
-
-  const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hkv + g) * topk;
-  for (int kk = 0; kk < topk; ++kk) {
-    const int j = row_idx[kk];
-    if (j < 0 || j >= tl.nvp) continue;
-    int64_t page = kv_indices[tl.page_base + j];
-    if (page < 0 || page >= num_pages) page = 0;  // reported by the prep kernel
-    __syncthreads();  // previous block's reads of k / v / pk are done
-    const int64_t kv_off = (page * hkv + g) * 128 * kD;
-    load_tile<kD>(sm.k, kp + kv_off, kD, 128);
-    load_tile<kD>(sm.v, vp + kv_off, kD, 128);
-    load_tile<kDP>(sm.pk, pk + page * 128 * kDP, kDP, 128);
-    cp_async_wait_all();
-    __syncthreads();
-    if (first) {
-      l2a = sm.lse2[r0];
-      l2b = sm.lse2[r1];
-      da = sm.dsum[r0];
-      db = sm.dsum[r1];
-      first = false;
-    }
-#pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-      const int kb = half * 64;
-      float sc[8][4], dp[8][4];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        sc[i][0] = sc[i][1] = sc[i][2] = sc[i][3] = 0.f;
-        dp[i][0] = dp[i][1] = dp[i][2] = dp[i][3] = 0.f;
-      }
-#pragma unroll
-      for (int kc = 0; kc < kD / 16; ++kc) {
-        uint32_t aq[4], ad[4];
-        frag_a(sm.q, kLd, warp * 16, kc * 16, aq);
-        frag_a(sm.dout, kLd, warp * 16, kc * 16, ad);
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b[4];
-          frag_b_nk(sm.k, kLd, kb + np * 16, kc * 16, b);
-          mma_bf16(sc[2 * np], aq, b[0], b[1]);
-          mma_bf16(sc[2 * np + 1], aq, b[2], b[3]);
-          frag_b_nk(sm.v, kLd, kb + np * 16, kc * 16, b);
-          mma_bf16(dp[2 * np], ad, b[0], b[1]);
-          mma_bf16(dp[2 * np + 1], ad, b[2], b[3]);
-        }
-      }
-      uint32_t pa[4][4], sa[4][4];
-#pragma unroll
-      for (int nt = 0; nt < 8; ++nt) {
-        float p[4], ds[4];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int kpos = j * 128 + kb + nt * 8 + 2 * t4 + c;
-          const bool v0 = ok0 && kpos <= qp0, v1 = ok1 && kpos <= qp1;
-          p[c] = v0 ? ex2_approx(sc[nt][c] * sl2 - l2a) : 0.f;
-          p[2 + c] = v1 ? ex2_approx(sc[nt][2 + c] * sl2 - l2b) : 0.f;
-          ds[c] = p[c] * (dp[nt][c] - da);
-          ds[2 + c] = p[2 + c] * (dp[nt][2 + c] - db);
-        }
-        pa[nt >> 1][(nt & 1) * 2 + 0] = pack2(p[0], p[1]);
-        pa[nt >> 1][(nt & 1) * 2 + 1] = pack2(p[2], p[3]);
-        sa[nt >> 1][(nt & 1) * 2 + 0] = pack2(ds[0], ds[1]);
-        sa[nt >> 1][(nt & 1) * 2 + 1] = pack2(ds[2], ds[3]);
-      }
-#pragma unroll
-      for (int kc = 0; kc < 4; ++kc) {
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {
-          uint32_t b[4];
-          frag_b_kn(sm.k, kLd, kb + kc * 16, np * 16, b);
-          mma_bf16(acc[2 * np], sa[kc], b[0], b[1]);
-          mma_bf16(acc[2 * np + 1], sa[kc], b[2], b[3]);
-        }
-#pragma unroll
-        for (int np = 0; np < 4; ++np) {
-          uint32_t b[4];
-          frag_b_kn(sm.pk, kLdP, kb + kc * 16, np * 16, b);
-          mma_bf16(opk[2 * np], pa[kc], b[0], b[1]);
-          mma_bf16(opk[2 * np + 1], pa[kc], b[2], b[3]);
-        }
-      }
-    }
-  }
-  cp_async_wait_all();
-  const float qs = rsqrtf(static_cast<float>(kD));
-#pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
-    const int c = nt * 8 + 2 * t4;
-    if (ok0)
-      *reinterpret_cast<float2*>(dq + static_cast<int64_t>(tl.q_begin + r0) * rs + static_cast<int64_t>(h) * kD + c) =
-          make_float2(acc[nt][0] * qs, acc[nt][1] * qs);
-    if (ok1)
-      *reinterpret_cast<float2*>(dq + static_cast<int64_t>(tl.q_begin + r1) * rs + static_cast<int64_t>(h) * kD + c) =
-          make_float2(acc[nt][2] * qs, acc[nt][3] * qs);
-  }
-  const float f = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * t4;
-    if (ok0) {
-      float* d0 = dpq + (static_cast<int64_t>(tl.q_begin + r0) * hkv + g) * kDP + c;
-      atomicAdd(d0, opk[nt][0] * f);
-      atomicAdd(d0 + 1, opk[nt][1] * f);
-    }
-    if (ok1) {
-      float* d1 = dpq + (static_cast<int64_t>(tl.q_begin + r1) * hkv + g) * kDP + c;
-      atomicAdd(d1, opk[nt][2] * f);
-      atomicAdd(d1 + 1, opk[nt][3] * f);
-    }
-  }
-}
-
 // ------------------------------------------------------------ inverse index
 
 // count[e*hkv + g] = number of tiles whose cached blocks of group g include
@@ -527,9 +365,6 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
   const int32_t* blk_j = p->aux_d + p->blk_j_off;
-  const auto* Q = static_cast<const __nv_bfloat16*>(q);
-  const auto* K = static_cast<const __nv_bfloat16*>(k_pages);
-  const auto* V = static_cast<const __nv_bfloat16*>(v_pages);
   const auto* O = static_cast<const __nv_bfloat16*>(out);
   const auto* dO = static_cast<const __nv_bfloat16*>(dout);
   const auto* PQ = static_cast<const __nv_bfloat16*>(pq);
@@ -546,12 +381,9 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, cnt);
   bwd_scan_kernel<<<1, 1024, 0, st>>>(cnt, static_cast<int32_t>(ent), off, cur);
   bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, cur, list);
-  const int dq_smem = sizeof(DqSmem);
-  cudaFuncSetAttribute(bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dq_smem);
-  bwd_dq_kernel<<<p->n_tiles * p->hq, kThreads, dq_smem, st>>>(p->tiles_d, idx, kv_indices, p->num_pages, Q, K, V, dO,
-                                                              lse, dsumt, PK, dq, dpq, p->hq, p->hkv, p->topk,
-                                                              static_cast<int32_t>(p->total_q), kl_weight);
   s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
+  if (s != MSA_OK) return s;
+  s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
   if (s != MSA_OK) return s;
   return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, blk_j, off, list, lse2t, dsumt,
                            lsept, dk, dv, dpk, kl_weight, st);

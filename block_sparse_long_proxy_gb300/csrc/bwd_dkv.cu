@@ -379,6 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // groups (fp32 atomics)
     if (ok) ok = mbar_wait(done, 0, err);
     tc_fence_after();
+    ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
     if (ok && page_ok) {
       const float ks = rsqrtf(static_cast<float>(kD));
       const float f_main = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);

@@ -1,0 +1,293 @@
+// Training extension, query side: dQ and the main term of the proxy-query
+// gradient dpq of block-sparse GQA attention with the KL-coupled proxy
+// (Flash-MSA article, backward-pass paragraph), on the tcgen05 tensor cores.
+//
+// One CTA per (query tile t, head h of group g).  Q_h and dO_h of the tile
+// stay in shared memory; the tile's cached blocks stream through a 2-stage
+// TMA ring (K, V and pk of each block).  Per block j:
+//   S  = Q_h . K_j^T     dP = dO_h . V_j^T            (M = rows, N = keys)
+//   P  = exp2(S sl2 - lse2) (masked)   dS = P * (dP - D)
+//   dQ += dS . K_j       dpq += P . pk_j              (dS, P from TMEM)
+// At the end dQ / sqrt(d) is stored and dpq * (-w / (G sqrt(dp))) is added
+// with fp32 atomics: the G heads of a group add into the same dpq row, whose
+// proxy term the prep kernel stored first.
+//
+// Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 columns.  Warpgroup w of
+// the softmax owns keys 64w..64w+63 and writes its bf16 pairs into the first
+// 32 of its 64 columns, so k-step kk (16 keys) of an A operand in TMEM
+// starts at column (kk / 4) * 64 + (kk % 4) * 8.
+// Roles: warps 0-7 softmax (thread = query row), warp 8 TMA producer,
+// warp 9 MMA issuer.
+#include "msa_internal.h"
+#include "ptx.cuh"
+
+namespace msa {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kDP = 64;
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr float kLog2e = 1.4426950408889634f;
+
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDPQ = 384;
+
+struct DqSmem {
+  static constexpr int kQOff = 0;                     // Q_h: 2 x [128 rows][128 B]
+  static constexpr int kDOOff = kQOff + 32768;        // dO_h
+  static constexpr int kRingOff = kDOOff + 32768;     // stage: K 32 KB | V 32 KB | pk 16 KB
+  static constexpr int kStageBytes = 81920;
+  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kBytes = kBarOff + 8 * 12;
+};
+
+__device__ __forceinline__ uint32_t ts_col(uint32_t base, int kk) {
+  return base + static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
+}
+
+__device__ __forceinline__ bool valid_block(int j, int nvp) { return j >= 0 && j < nvp; }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
+                     const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                     const __grid_constant__ CUtensorMap pk_map, const TileInfo* __restrict__ tiles,
+                     const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
+                     const float* __restrict__ lse2t, const float* __restrict__ dsumt, float* __restrict__ dq,
+                     float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, int32_t total_q,
+                     float kl_weight, uint32_t* err) {
+  using L = DqSmem;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int t = blockIdx.x / hq, h = blockIdx.x % hq;
+  const int G = hq / hkv, g = h / G;
+  const TileInfo tl = tiles[t];
+  const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hkv + g) * topk;
+
+  uint8_t* q_s = smem + L::kQOff;
+  uint8_t* do_s = smem + L::kDOOff;
+  uint8_t* ring = smem + L::kRingOff;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+  uint64_t* q_full = bars;
+  uint64_t* kv_full = bars + 1;              // [kStages]
+  uint64_t* kv_empty = kv_full + kStages;    // [kStages]
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* done = p_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&q_map);
+    prefetch_tmap(&do_map);
+    prefetch_tmap(&k_map);
+    prefetch_tmap(&v_map);
+    prefetch_tmap(&pk_map);
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(kv_full + s, 1);
+      mbar_init(kv_empty + s, 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kSoftWarps);
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_expect_tx(q_full, 65536);
+      for (int c = 0; c < 2; ++c) {
+        tma_load_3d(q_s + c * 16384, &q_map, q_full, c * 64, h, tl.q_begin);
+        tma_load_3d(do_s + c * 16384, &do_map, q_full, c * 64, h, tl.q_begin);
+      }
+      int it = 0;
+      for (int k = 0; k < topk; ++k) {
+        const int j = row_idx[k];
+        if (!valid_block(j, tl.nvp)) continue;
+        const int s = it % kStages;
+        if (!mbar_wait(kv_empty + s, ((it / kStages) & 1) ^ 1, err)) break;
+        int64_t page = kv_indices[tl.page_base + j];
+        if (page < 0 || page >= num_pages) page = 0;  // reported by the prep kernel
+        uint8_t* st = ring + s * L::kStageBytes;
+        const int row = static_cast<int>((page * hkv + g) * 128);
+        mbar_expect_tx(kv_full + s, L::kStageBytes);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_2d(st + c * 16384, &k_map, kv_full + s, c * 64, row);
+          tma_load_2d(st + 32768 + c * 16384, &v_map, kv_full + s, c * 64, row);
+        }
+        tma_load_2d(st + 65536, &pk_map, kv_full + s, 0, static_cast<int>(page * 128));
+        ++it;
+      }
+    }
+  } else if (warp == 9) {
+    // --------------------------------------------------------------- MMA
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
+      constexpr uint32_t id_q = idesc_bf16_f32(128, 128, false, true);   // dQ (B keys-major)
+      constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpq
+      const uint32_t q0 = smem_u32(q_s), d0 = smem_u32(do_s), r0 = smem_u32(ring);
+      bool ok = mbar_wait(q_full, 0, err);
+      tc_fence_after();
+      int it = 0;
+      for (int k = 0; ok && k < topk; ++k) {
+        const int j = row_idx[k];
+        if (!valid_block(j, tl.nvp)) continue;
+        const int s = it % kStages;
+        const uint32_t ka = r0 + s * L::kStageBytes, va = ka + 32768, pa = ka + 65536;
+        if (!(ok = mbar_wait(kv_full + s, (it / kStages) & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + kColS, smem_desc(q0 + off, 16, 1024, kSwizzle128), smem_desc(ka + off, 16, 1024, kSwizzle128),
+                 id_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_ss(tmem + kColDP, smem_desc(d0 + off, 16, 1024, kSwizzle128),
+                 smem_desc(va + off, 16, 1024, kSwizzle128), id_s, kk > 0);
+        }
+        mma_commit(s_full);
+        if (!(ok = mbar_wait(p_full, it & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ts(tmem + kColDQ, ts_col(tmem + kColDP, kk), smem_desc(ka + kk * 2048, 16384, 1024, kSwizzle128), id_q,
+                 it > 0 || kk > 0);
+          mma_ts(tmem + kColDPQ, ts_col(tmem + kColS, kk), smem_desc(pa + kk * 2048, 16384, 1024, kSwizzle128),
+                 id_p, it > 0 || kk > 0);
+        }
+        mma_commit(kv_empty + s);
+        ++it;
+      }
+      mma_commit(done);
+    }
+  } else {
+    // ----------------------------------------------------------- softmax
+    const int wg = warp >> 2, quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // query row of the tile
+    const int kc0 = wg * 64;            // this warpgroup's keys within the block
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool row_ok = r < tl.rows;
+    const int qpos = tl.pos0 + r;
+    const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
+    const float l2 = row_ok ? lse2t[ei] : 0.f;
+    const float dd = row_ok ? dsumt[ei] : 0.f;
+    const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
+    bool ok = true;
+    int it = 0;
+    for (int k = 0; ok && k < topk; ++k) {
+      const int j = row_idx[k];
+      if (!valid_block(j, tl.nvp)) continue;
+      if (!(ok = mbar_wait(s_full, it & 1, err))) break;
+      tc_fence_after();
+      const int kbase = j * 128 + kc0;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {  // 32 keys at a time; packed pairs land in columns already read
+        uint32_t sv[32], dv_[32], pa[16], da[16];
+        tmem_ld32(lane_base + kColS + kc0 + 32 * c, sv);
+        tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const int kp = kbase + 32 * c + i;
+          const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
+          const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
+          const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
+          pa[i >> 1] = pack_bf16x2(p0, p1);
+          da[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv_[i]) - dd), p1 * (__uint_as_float(dv_[i + 1]) - dd));
+        }
+        tmem_st16(lane_base + kColS + kc0 + 16 * c, pa);
+        tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      ++it;
+    }
+    if (ok) ok = mbar_wait(done, 0, err);
+    tc_fence_after();
+    ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
+    // tcgen05.ld is warp-collective: every lane loads, only valid rows store
+    if (ok) {
+      const int64_t q_row = tl.q_begin + r;
+      float* dqr = dq + (q_row * hq + h) * kD + wg * 64;
+      const float qs = rsqrtf(static_cast<float>(kD));
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t a[32];
+        if (it > 0) {
+          tmem_ld32(lane_base + kColDQ + wg * 64 + c * 32, a);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) a[i] = 0u;
+        }
+        if (row_ok)
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            reinterpret_cast<float4*>(dqr + c * 32)[i] =
+                make_float4(__uint_as_float(a[4 * i]) * qs, __uint_as_float(a[4 * i + 1]) * qs,
+                            __uint_as_float(a[4 * i + 2]) * qs, __uint_as_float(a[4 * i + 3]) * qs);
+      }
+      if (it > 0) {
+        const float f = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
+        uint32_t a[32];
+        tmem_ld32(lane_base + kColDPQ + wg * 32, a);
+        tmem_wait_ld();
+        float* dpr = dpq + (q_row * hkv + g) * kDP + wg * 32;
+        if (row_ok)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) atomicAdd(dpr + i, __uint_as_float(a[i]) * f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                            const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
+                            cudaStream_t st) {
+  CUtensorMap qm, dom, km, vm, pkm;
+  const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
+                             static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(p->hq) * kD * 2};
+  const uint32_t qbox[3] = {64, 1, 128};
+  const uint64_t kdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t kstr[1] = {static_cast<uint64_t>(kD) * 2};
+  const uint32_t kbox[2] = {64, 128};
+  const uint64_t pkdims[2] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t pkstr[1] = {static_cast<uint64_t>(kDP) * 2};
+  if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&dom, 3, dout, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, 1, 128) ||
+      !encode_tensor_map(&pkm, 2, pk_pages, pkdims, pkstr, kbox, 1, 128))
+    return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
+  const int smem = DqSmem::kBytes + 1024;
+  cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  bwd_dq_tc_kernel<<<p->n_tiles * p->hq, kThreads, smem, st>>>(
+      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, p->hq, p->hkv, p->topk,
+      static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
+}
+
+}  // namespace msa

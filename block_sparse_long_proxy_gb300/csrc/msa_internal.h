@@ -76,6 +76,11 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
+// dQ and dpq's main term on the tensor cores (bwd_dq.cu).
+msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
+                            const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
+                            cudaStream_t st);
 // dK, dV and dpk on the tensor cores (bwd_dkv.cu); lse2t, dsumt, lsept are
 // the row statistics written by the prep kernel, [heads][total_q].
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,

@@ -56,16 +56,31 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // loop so that the CTA drains and exits instead of hanging the GPU.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// try_wait with a suspend-time hint: the thread sleeps at most ~hint_ns
+// before the instruction reports the phase as not yet complete.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// The clock is read after every unsuccessful poll, and each poll sleeps at
+// most 100 us, so a wait that cannot complete gives up within the limit.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* err) {
   const uint64_t t0 = global_timer_ns();
-  while (true) {
-    for (int i = 0; i < 256; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+  while (!mbar_try_wait_hint(bar, parity, 100000u)) {
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       if (err) atomicOr(err, 2u);
       return false;
     }
   }
+  return true;
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -9,13 +9,16 @@
 //   P^T  = exp2(S^T sl2 - lse2)  dS^T = P^T * (dP^T - D)  (masked: causal, ragged)
 //   dV  += P^T . dO_h           dK  += dS^T . Q_h       (P^T, dS^T from TMEM)
 //   dpk += P^T . pq
-// and once per 64 rows, for the proxy distribution over the same keys:
+// and once per 64 rows, before the heads, for the proxy distribution over
+// the same keys (in the S^T columns):
 //   Sp^T = pk . pq^T,  Pp^T = exp2(Sp^T zsl2 - lsep),  dpk += (-G Pp^T) . pq
 // so that at the end dpk * (-w / (G sqrt(dp))) = w/sqrt(dp) (Pp - mean_h P_h)^T pq,
 // this group's share of the KL gradient with respect to the proxy keys.
 //
-// Tensor memory (512 columns): S^T 64 | dP^T 64 | Sp^T 64 | dV 128 | dpk 64 | dK 128.
-// The softmax warps overwrite S^T, dP^T and Sp^T in place with bf16 pairs.
+// Tensor memory (512 columns): S^T 64 | dP^T 64 | dV 128 | dpk 64 | dK 128 | K 64.
+// K is copied into tensor memory once, so S^T = K . Q^T reads only Q from
+// shared memory (the products are bound by shared-memory operand reads).
+// The softmax warps overwrite S^T (or Sp^T) and dP^T in place with bf16 pairs.
 // Each warpgroup owns 32 of the 64 rows, and each writes its packed pairs
 // into the first half of its own 32 columns, so a k-step of 16 rows of an
 // A operand in TMEM starts at column (kk / 2) * 32 + (kk % 2) * 8.
@@ -37,7 +40,7 @@ constexpr int kThreads = 32 * (kSoftWarps + 2);
 constexpr int kMaxList = 2048;
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr uint32_t kColS = 0, kColDP = 64, kColSP = 128, kColDV = 192, kColDPK = 320, kColDK = 384;
+constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDPK = 256, kColDK = 320, kColK = 448;
 
 struct DkvSmem {
   static constexpr int kKOff = 0;                               // K block: 2 x [128 keys][128 B]
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* kv_full = bars;
-  uint64_t* zero_done = bars + 1;
+  uint64_t* init_done = bars + 1;  // accumulators zeroed, K in tensor memory
   uint64_t* qd_full = bars + 2;                 // [kQStages]
   uint64_t* qd_empty = qd_full + kQStages;      // [kQStages]
   uint64_t* pq_full = qd_empty + kQStages;      // [kPqStages]
@@ -121,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&v_map);
     prefetch_tmap(&pk_map);
     mbar_init(kv_full, 1);
-    mbar_init(zero_done, kSoftWarps);
+    mbar_init(init_done, kSoftWarps);
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(qd_full + s, 2);  // expect_tx arrival + the staged lse2 / D
       mbar_init(qd_empty + s, 1);
@@ -196,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int rr = lane; rr < 64; rr += 32) {
           const int r = hf * 64 + rr;
-          lsep_s[ps * 64 + rr] = r < tl.rows ? lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r] : 0.f;
+          lsep_s[ps * 64 + rr] = r < tl.rows ? -lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r] : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(pq_full + ps);
@@ -216,8 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int r = hf * 64 + rr;
             const bool rok = r < tl.rows;
             const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
-            row_s[s * 128 + rr] = rok ? lse2t[ei] : 0.f;
-            row_s[s * 128 + 64 + rr] = rok ? dsumt[ei] : 0.f;
+            row_s[s * 128 + rr] = rok ? -lse2t[ei] : 0.f;  // negated: the softmax adds them
+            row_s[s * 128 + 64 + rr] = rok ? -dsumt[ei] : 0.f;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(qd_full + s);
@@ -230,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T, Sp^T
       constexpr uint32_t id_d = idesc_bf16_f32(128, 128, false, true);   // dV, dK (B rows-major)
       constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpk
-      const uint32_t k0 = smem_u32(k_s), v0 = smem_u32(v_s), pk0 = smem_u32(pk_s);
+      const uint32_t v0 = smem_u32(v_s), pk0 = smem_u32(pk_s);
       const uint32_t qd0 = smem_u32(qd_s), pq0 = smem_u32(pq_s);
-      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(zero_done, 0, err);
+      bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(init_done, 0, err);
       tc_fence_after();
       int qi = 0, pi = 0;
       for (int it = 0; ok && it < n; ++it) {
@@ -245,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < kDP / 16; ++kk)
-            mma_ss(tmem + kColSP, smem_desc(pk0 + kk * 32, 16, 1024, kSwizzle128),
+            mma_ss(tmem + kColS, smem_desc(pk0 + kk * 32, 16, 1024, kSwizzle128),
                    smem_desc(pqa + kk * 32, 16, 1024, kSwizzle128), id_s, kk > 0);
           mma_commit(sp_full);
           for (int hh = 0; ok && hh < G; ++hh, ++qi) {
@@ -256,14 +259,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
               const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
-              mma_ss(tmem + kColS, smem_desc(k0 + oa, 16, 1024, kSwizzle128),
-                     smem_desc(qa + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+              mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
+                     smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+            }
+            if (hh == 0) {  // dP^T of the first head overlaps the proxy softmax
+              if (!(ok = mbar_wait(pp_full, pi & 1, err))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk),
+                       smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128), id_p, 1);
             }
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
-              mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
-                     smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+              const uint32_t ob = (kk / 4) * 8192 + (kk % 4) * 32;
+              mma_ts(tmem + kColS, tmem + kColK + kk * 8, smem_desc(qa + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
             }
             mma_commit(s_full);
             if (!(ok = mbar_wait(p_full, qi & 1, err))) break;
@@ -279,12 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(qd_empty + s);
           }
-          if (!ok || !(ok = mbar_wait(pp_full, pi & 1, err))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tmem + kColDPK, ts_col(tmem + kColSP, kk), smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128),
-                   id_p, 1);
+          if (!ok) break;
           mma_commit(pq_empty + ps);
         }
       }
@@ -300,18 +305,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
     const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
     const float neg_g = -static_cast<float>(G);
-    {  // dV, dpk, dK start at zero: columns 192..511, 160 per warpgroup
+    bool ok = mbar_wait(kv_full, 0, err);
+    {  // dV, dpk, dK start at zero (columns 128..447, 160 per warpgroup); K row
+       // `key`, d in [64 wg, 64 wg + 64), goes to tensor memory as bf16 pairs
       uint32_t z[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
       for (int c = 0; c < 10; ++c) tmem_st16(lane_base + kColDV + wg * 160 + c * 16, z);
+      const uint8_t* krow = k_s + wg * 16384 + key * 128;
+      uint32_t kv[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4*>(krow + ((u ^ (key & 7)) << 4));
+        kv[4 * u] = v.x;
+        kv[4 * u + 1] = v.y;
+        kv[4 * u + 2] = v.z;
+        kv[4 * u + 3] = v.w;
+      }
+      tmem_st16(lane_base + kColK + 32 * wg, kv);
+      tmem_st16(lane_base + kColK + 32 * wg + 16, kv + 16);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(zero_done);
+      if (lane == 0) mbar_arrive(init_done);
     }
-    bool ok = true;
     int qi = 0, pi = 0;
     for (int it = 0; ok && it < n; ++it) {
       const TileInfo tl = tiles[tile_at(it)];
@@ -319,25 +337,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
         const int ps = pi % kPqStages;
         const int rbase = hf * 64 + c0;  // tile row of column 0 of this warpgroup
+        // every key of the block visible to all 32 rows: no per-element mask
+        const bool need_mask = j * 128 + 127 > tl.pos0 + rbase || rbase + 32 > tl.rows;
         // proxy probabilities over this block's keys, scaled by -G
         if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
         if (!(ok = mbar_wait(sp_full, pi & 1, err))) break;
         tc_fence_after();
         {
           uint32_t sv[32], pk[16];
-          tmem_ld32(lane_base + kColSP + c0, sv);
+          tmem_ld32(lane_base + kColS + c0, sv);
           tmem_wait_ld();
-          const float* lp = lsep_s + ps * 64 + c0;
+          const float2* nlp = reinterpret_cast<const float2*>(lsep_s + ps * 64 + c0);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const int r = rbase + c;
-            const bool ok0 = r < tl.rows && kpos <= tl.pos0 + r;
-            const bool ok1 = r + 1 < tl.rows && kpos <= tl.pos0 + r + 1;
-            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[c]) * zsl2 - lp[c]) : 0.f;
-            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[c + 1]) * zsl2 - lp[c + 1]) : 0.f;
+            const float2 nl = nlp[c >> 1];
+            float x0, x1;
+            ffma2v(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), zsl2, zsl2, nl.x, nl.y);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (need_mask) {
+              const int r = rbase + c;
+              if (!(r < tl.rows && kpos <= tl.pos0 + r)) p0 = 0.f;
+              if (!(r + 1 < tl.rows && kpos <= tl.pos0 + r + 1)) p1 = 0.f;
+            }
             pk[c >> 1] = pack_bf16x2(p0 * neg_g, p1 * neg_g);
           }
-          tmem_st16(lane_base + kColSP + c0, pk);
+          tmem_st16(lane_base + kColS + c0, pk);
           tmem_wait_st();
         }
         tc_fence_before();
@@ -352,17 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_base + kColS + c0, sv);
           tmem_ld32(lane_base + kColDP + c0, dv_);
           tmem_wait_ld();
-          const float* l2 = row_s + s * 128 + c0;
-          const float* dd = row_s + s * 128 + 64 + c0;
+          const float2* nl2 = reinterpret_cast<const float2*>(row_s + s * 128 + c0);
+          const float2* ndd = reinterpret_cast<const float2*>(row_s + s * 128 + 64 + c0);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const int r = rbase + c;
-            const bool ok0 = r < tl.rows && kpos <= tl.pos0 + r;
-            const bool ok1 = r + 1 < tl.rows && kpos <= tl.pos0 + r + 1;
-            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[c]) * sl2 - l2[c]) : 0.f;
-            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[c + 1]) * sl2 - l2[c + 1]) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dv_[c]) - dd[c]);
-            const float d1 = p1 * (__uint_as_float(dv_[c + 1]) - dd[c + 1]);
+            const float2 nl = nl2[c >> 1], nd = ndd[c >> 1];
+            float x0, x1, t0, t1, d0, d1;
+            ffma2v(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, nl.x, nl.y);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (need_mask) {
+              const int r = rbase + c;
+              if (!(r < tl.rows && kpos <= tl.pos0 + r)) p0 = 0.f;
+              if (!(r + 1 < tl.rows && kpos <= tl.pos0 + r + 1)) p1 = 0.f;
+            }
+            fadd2v(t0, t1, __uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1]), nd.x, nd.y);
+            fmul2(d0, d1, t0, t1, p0, p1);
             pa[c >> 1] = pack_bf16x2(p0, p1);
             da[c >> 1] = pack_bf16x2(d0, d1);
           }

@@ -2,19 +2,22 @@
 // gradient dpq of block-sparse GQA attention with the KL-coupled proxy
 // (Flash-MSA article, backward-pass paragraph), on the tcgen05 tensor cores.
 //
-// One CTA per (query tile t, head h of group g).  Q_h and dO_h of the tile
-// stay in shared memory; the tile's cached blocks stream through a 2-stage
-// TMA ring (K, V and pk of each block).  Per block j:
-//   S  = Q_h . K_j^T     dP = dO_h . V_j^T            (M = rows, N = keys)
+// One CTA per (query tile t, head h of group g).  Q_h is copied into tensor
+// memory once, dO_h stays in shared memory, and the tile's cached blocks
+// stream through a 2-stage TMA ring (K, V and pk of each block).  Per block j:
+//   S  = Q_h . K_j^T (Q from TMEM)   dP = dO_h . V_j^T        (M = rows, N = 128 keys)
 //   P  = exp2(S sl2 - lse2) (masked)   dS = P * (dP - D)
-//   dQ += dS . K_j       dpq += P . pk_j              (dS, P from TMEM)
+//   dQ += dS . K_j       dpq += P . pk_j                     (dS, P from TMEM)
+// The products are bound by shared-memory operand reads, so they use the
+// widest N and take Q from tensor memory; the softmax of a block runs
+// between its products (its two warpgroups split the 128 keys).
 // At the end dQ / sqrt(d) is stored and dpq * (-w / (G sqrt(dp))) is added
 // with fp32 atomics: the G heads of a group add into the same dpq row, whose
 // proxy term the prep kernel stored first.
 //
-// Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 columns.  Warpgroup w of
-// the softmax owns keys 64w..64w+63 and writes its bf16 pairs into the first
-// 32 of its 64 columns, so k-step kk (16 keys) of an A operand in TMEM
+// Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 | Q 64 columns.  Warpgroup
+// w owns keys 64w..64w+63 and writes its bf16 pairs into the first 32 of
+// its 64 S / dP columns, so k-step kk (16 keys) of an A operand in TMEM
 // starts at column (kk / 4) * 64 + (kk % 4) * 8.
 // Roles: warps 0-7 softmax (thread = query row), warp 8 TMA producer,
 // warp 9 MMA issuer.
@@ -31,7 +34,7 @@ constexpr int kSoftWarps = 8;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
 constexpr float kLog2e = 1.4426950408889634f;
 
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDPQ = 384;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDPQ = 384, kColQ = 448;
 
 struct DqSmem {
   static constexpr int kQOff = 0;                     // Q_h: 2 x [128 rows][128 B]
@@ -39,12 +42,8 @@ struct DqSmem {
   static constexpr int kRingOff = kDOOff + 32768;     // stage: K 32 KB | V 32 KB | pk 16 KB
   static constexpr int kStageBytes = 81920;
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kBytes = kBarOff + 8 * 12;
+  static constexpr int kBytes = kBarOff + 8 * 14;
 };
-
-__device__ __forceinline__ uint32_t ts_col(uint32_t base, int kk) {
-  return base + static_cast<uint32_t>((kk >> 2) * 64 + (kk & 3) * 8);
-}
 
 __device__ __forceinline__ bool valid_block(int j, int nvp) { return j >= 0 && j < nvp; }
 
@@ -69,7 +68,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* ring = smem + L::kRingOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;              // [kStages]
+  uint64_t* q_tm = bars + 1;                 // Q copied into tensor memory
+  uint64_t* kv_full = bars + 2;              // [kStages]
   uint64_t* kv_empty = kv_full + kStages;    // [kStages]
   uint64_t* s_full = kv_empty + kStages;
   uint64_t* p_full = s_full + 1;
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&v_map);
     prefetch_tmap(&pk_map);
     mbar_init(q_full, 1);
+    mbar_init(q_tm, kSoftWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
@@ -135,13 +136,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
       constexpr uint32_t id_q = idesc_bf16_f32(128, 128, false, true);   // dQ (B keys-major)
       constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpq
-      const uint32_t q0 = smem_u32(q_s), d0 = smem_u32(do_s), r0 = smem_u32(ring);
-      bool ok = mbar_wait(q_full, 0, err);
+      const uint32_t d0 = smem_u32(do_s), r0 = smem_u32(ring);
+      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(q_tm, 0, err);
       tc_fence_after();
       int it = 0;
       for (int k = 0; ok && k < topk; ++k) {
-        const int j = row_idx[k];
-        if (!valid_block(j, tl.nvp)) continue;
+        if (!valid_block(row_idx[k], tl.nvp)) continue;
         const int s = it % kStages;
         const uint32_t ka = r0 + s * L::kStageBytes, va = ka + 32768, pa = ka + 65536;
         if (!(ok = mbar_wait(kv_full + s, (it / kStages) & 1, err))) break;
@@ -149,8 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + kColS, smem_desc(q0 + off, 16, 1024, kSwizzle128), smem_desc(ka + off, 16, 1024, kSwizzle128),
-                 id_s, kk > 0);
+          mma_ts(tmem + kColS, tmem + kColQ + kk * 8, smem_desc(ka + off, 16, 1024, kSwizzle128), id_s, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
@@ -163,10 +162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tmem + kColDQ, ts_col(tmem + kColDP, kk), smem_desc(ka + kk * 2048, 16384, 1024, kSwizzle128), id_q,
+          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
+          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, smem_desc(ka + kk * 2048, 16384, 1024, kSwizzle128), id_q,
                  it > 0 || kk > 0);
-          mma_ts(tmem + kColDPQ, ts_col(tmem + kColS, kk), smem_desc(pa + kk * 2048, 16384, 1024, kSwizzle128),
-                 id_p, it > 0 || kk > 0);
+          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, smem_desc(pa + kk * 2048, 16384, 1024, kSwizzle128), id_p,
+                 it > 0 || kk > 0);
         }
         mma_commit(kv_empty + s);
         ++it;
@@ -185,7 +185,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float l2 = row_ok ? lse2t[ei] : 0.f;
     const float dd = row_ok ? dsumt[ei] : 0.f;
     const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
-    bool ok = true;
+    bool ok = mbar_wait(q_full, 0, err);
+    {  // Q_h row r, d in [64 wg, 64 wg + 64), into tensor memory as bf16 pairs
+      const uint8_t* qrow = q_s + wg * 16384 + r * 128;
+      uint32_t qv[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+        qv[4 * u] = v.x;
+        qv[4 * u + 1] = v.y;
+        qv[4 * u + 2] = v.z;
+        qv[4 * u + 3] = v.w;
+      }
+      tmem_st16(lane_base + kColQ + 32 * wg, qv);
+      tmem_st16(lane_base + kColQ + 32 * wg + 16, qv + 16);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_tm);
+    }
     int it = 0;
     for (int k = 0; ok && k < topk; ++k) {
       const int j = row_idx[k];
@@ -193,20 +211,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait(s_full, it & 1, err))) break;
       tc_fence_after();
       const int kbase = j * 128 + kc0;
+      const bool need_mask = j * 128 + 127 > tl.pos0 || tl.rows < 128;  // diagonal block or ragged tile
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // 32 keys at a time; packed pairs land in columns already read
         uint32_t sv[32], dv_[32], pa[16], da[16];
         tmem_ld32(lane_base + kColS + kc0 + 32 * c, sv);
         tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
         tmem_wait_ld();
+        if (!need_mask) {
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const int kp = kbase + 32 * c + i;
-          const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
-          const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
-          const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
-          pa[i >> 1] = pack_bf16x2(p0, p1);
-          da[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv_[i]) - dd), p1 * (__uint_as_float(dv_[i + 1]) - dd));
+          for (int i = 0; i < 32; i += 2) {
+            float x0, x1, t0, t1, d0, d1;
+            ffma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, -l2);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            fadd2v(t0, t1, __uint_as_float(dv_[i]), __uint_as_float(dv_[i + 1]), -dd, -dd);
+            fmul2(d0, d1, t0, t1, p0, p1);
+            pa[i >> 1] = pack_bf16x2(p0, p1);
+            da[i >> 1] = pack_bf16x2(d0, d1);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            const int kp = kbase + 32 * c + i;
+            const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
+            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
+            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
+            pa[i >> 1] = pack_bf16x2(p0, p1);
+            da[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv_[i]) - dd), p1 * (__uint_as_float(dv_[i + 1]) - dd));
+          }
         }
         tmem_st16(lane_base + kColS + kc0 + 16 * c, pa);
         tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);

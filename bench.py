@@ -443,6 +443,20 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
     # mean, not median: the event clock ticks in ~2 us steps, a mean averages over them
     t = statistics.mean(times) / 1e3
     tp = statistics.mean(ptimes) / 1e3
+    # the same scan over the e4m3 proxy K (msa_proxy_maxscore_fp8)
+    p8 = []
+    for _ in range(3):
+        plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
+    for _ in range(reps):
+        flush()
+        a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+        a.record(stream)
+        plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
+        b.record(stream)
+        torch.cuda.synchronize()
+        p8.append(a.elapsed_time(b))
+    plan.check_errors()
+    tp8 = statistics.mean(p8) / 1e3
     gbs = (kv_bytes + io_bytes) / t / 1e9
     proxy_bytes = sum((k + 127) // 128 for k in case.kv_lens) * 128 * case.dp * 2
     hbm = pk_info.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -450,7 +464,9 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
                          "peak_kind": "%s HBM copy" % peak_kind, "nominal_frac": gbs / 8000.0},
             "proxy_scan_us": tp * 1e6, "proxy_scan_gbs": proxy_bytes / tp / 1e9,
-            "proxy_scan_frac": proxy_bytes / tp / 1e9 / hbm}
+            "proxy_scan_frac": proxy_bytes / tp / 1e9 / hbm,
+            "proxy_scan_fp8_us": tp8 * 1e6, "proxy_scan_fp8_gbs": proxy_bytes / 2 / tp8 / 1e9,
+            "proxy_scan_fp8_frac": proxy_bytes / 2 / tp8 / 1e9 / hbm}
 
 
 def run_ncu_case(args):

@@ -231,6 +231,18 @@ msa_status msa_proxy_maxscore(msa_plan_t plan, const void* pq, const void* pk_pa
   return launch_proxy_prefill(plan, pq, pk_pages, kv_indices, max_score, st);
 }
 
+msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* pk_pages, const float* pk_scale,
+                                  const int32_t* kv_indices, float* max_score, msa_stream_t stream) {
+  if (!plan || !pq || !pk_pages || !pk_scale || !kv_indices || !max_score)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore_fp8: NULL argument");
+  if (!aligned16(pq) || !aligned16(pk_pages))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore_fp8: pq and pk_pages must be 16-byte aligned");
+  if (!plan->decode)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore_fp8: FP8 proxy K is implemented for decode batches only");
+  return launch_proxy_decode_fp8(plan, pq, pk_pages, pk_scale, kv_indices, max_score,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
 msa_status msa_topk_select(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,
                            int32_t topk, const int32_t* num_valid_pages, int32_t* kv_block_indexes,
                            msa_stream_t stream) {

@@ -97,6 +97,9 @@ msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void*
                                 const int32_t* kv_indices, float* max_score, cudaStream_t st);
 msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages,
                                const int32_t* kv_indices, float* max_score, cudaStream_t st);
+// decode proxy scan over e4m3 proxy K pages with one fp32 scale (device pointer)
+msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const void* pk_pages, const float* pk_scale,
+                                   const int32_t* kv_indices, float* max_score, cudaStream_t st);
 
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages,
                                const void* v_pages, const int32_t* kv_indices, const int32_t* idx,

@@ -405,6 +405,152 @@ __global__ void __launch_bounds__(32 * kDecWarps)
   }
 }
 
+// FP8 proxy K at decode: the same scan over e4m3 proxy K pages (64 bytes a
+// row at dp = 64) with one fp32 scale for the shared proxy head, so the
+// dominant decode read is halved.  logit = (pq . pk_code) * pk_scale / sqrt(dp)
+// and, the scale being positive, the block max is taken on the codes' dot
+// products and scaled once.  A row of a page is loaded by TMA with 64-byte
+// swizzle; lane (g, t4) reads the 4 bytes at dims 16 kc + 4 t4 of keys g and
+// g + 8 of an m-tile, which is one conflict-free 32-bit word per lane, and the
+// pq fragments use the same dim order (the dot product is order-free).
+constexpr int kDec8Warps = 24;  // warps per CTA, one CTA per SM (measured best of 4..24)
+constexpr int kDec8Stages = 1;  // ring stages per warp: the parallelism is across warps
+
+template <int W, int S>
+__global__ void __launch_bounds__(32 * W)
+    proxy_decode_fp8_kernel(const __grid_constant__ CUtensorMap k_map, const __nv_bfloat16* __restrict__ pq,
+                            const float* __restrict__ pk_scale, const TileInfo* __restrict__ tiles,
+                            const int32_t* __restrict__ unit_start, int32_t n_tiles,
+                            const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
+                            int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+  constexpr int DP = 64;
+  constexpr int kBlk = 128 * DP;  // bytes of one e4m3 proxy K page
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + warp * S * kBlk;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + W * S * kBlk) + warp * S;
+  const float out_scale = scale * pk_scale[0];
+
+  const int total_units = unit_start[n_tiles];
+  for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+       e < static_cast<int64_t>(n_tiles) * hp * max_blocks; e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(e % max_blocks);
+    const int t = static_cast<int>(e / (static_cast<int64_t>(hp) * max_blocks));
+    if (j >= tiles[t].nvp) max_score[e] = -INFINITY;
+  }
+
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bars + s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int nw = gridDim.x * W;
+  const int gw = blockIdx.x * W + warp;
+  const int ub = warp_range_start(gw, total_units, nw), ue = warp_range_start(gw + 1, total_units, nw);
+  const int n = ue - ub;
+
+  auto meta = [&](int chunk_base, int& t, int& j, int& row) {
+    const int unit = chunk_base + lane;
+    t = 0;
+    j = 0;
+    row = 0;
+    if (unit < ue) {
+      int lo = 0, hi = n_tiles - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(unit_start + mid) <= unit) lo = mid; else hi = mid - 1;
+      }
+      t = lo;
+      j = unit - __ldg(unit_start + lo);
+      int64_t page = kv_indices[tiles[t].page_base + j];
+      if (page < 0 || page >= num_pages) {
+        atomicOr(err, kErrDeviceCheck);
+        page = 0;
+      }
+      row = static_cast<int>(page * 128);
+    }
+  };
+  int ct, cj, crow, nt_, nj, nrow;
+  meta(ub, ct, cj, crow);
+  meta(ub + 32, nt_, nj, nrow);
+  int chunk = 0;
+  auto issue = [&](int i) {
+    if (i >= n) return;
+    const int ii = i - 32 * chunk;
+    const int r_cur = __shfl_sync(0xFFFFFFFFu, crow, ii & 31);
+    const int r_nxt = __shfl_sync(0xFFFFFFFFu, nrow, ii & 31);
+    const int r = (ii >> 5) == 0 ? r_cur : r_nxt;
+    if (lane == 0) {
+      uint64_t* bar = bars + (i % S);
+      mbar_expect_tx(bar, kBlk);
+      tma_load_2d(ring + (i % S) * kBlk, &k_map, bar, 0, r);
+    }
+  };
+  for (int i = 0; i < S; ++i) issue(i);
+
+  const int g = lane >> 2, t4 = lane & 3;
+  for (int i = 0; i < n; ++i) {
+    if (i - 32 * chunk == 32) {
+      ct = nt_;
+      cj = nj;
+      crow = nrow;
+      ++chunk;
+      meta(ub + 32 * (chunk + 1), nt_, nj, nrow);
+    }
+    const int t = __shfl_sync(0xFFFFFFFFu, ct, i & 31);
+    const int j = __shfl_sync(0xFFFFFFFFu, cj, i & 31);
+    const TileInfo tl = tiles[t];
+    // B fragments: pq[row, head g, dims 16 kc + 4 t4 .. +3] as f16 pairs
+    uint32_t bf[DP / 16][2];
+    const __nv_bfloat16* qrow = pq + (static_cast<int64_t>(tl.q_begin) * hp + g) * DP;
+#pragma unroll
+    for (int kc = 0; kc < DP / 16; ++kc) {
+      if (g < hp) {
+        const uint2 v = *reinterpret_cast<const uint2*>(qrow + kc * 16 + 4 * t4);
+        const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 f1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        bf[kc][0] = pack_f16x2(f0.x, f0.y);
+        bf[kc][1] = pack_f16x2(f1.x, f1.y);
+      } else {
+        bf[kc][0] = bf[kc][1] = 0u;
+      }
+    }
+    const int s = i % S;
+    if (!mbar_wait(bars + s, (i / S) & 1, err)) break;
+    const uint32_t base = smem_u32(ring + s * kBlk);
+    const int nkeys = min(128, tl.kv_len - j * 128);
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      const int ra = mt * 16 + g, rb = ra + 8;
+#pragma unroll
+      for (int kc = 0; kc < DP / 16; ++kc) {
+        const uint32_t wa = lds32(base + ra * 64 + ((kc ^ ((ra >> 1) & 3)) << 4) + 4 * t4);
+        const uint32_t wb = lds32(base + rb * 64 + ((kc ^ ((rb >> 1) & 3)) << 4) + 4 * t4);
+        mma_f16(c, e4m3x2_to_f16x2(wa), e4m3x2_to_f16x2(wb), e4m3x2_to_f16x2(wa >> 16), e4m3x2_to_f16x2(wb >> 16),
+                bf[kc][0], bf[kc][1]);
+      }
+      if (ra < nkeys) { mx0 = fmaxf(mx0, c[0]); mx1 = fmaxf(mx1, c[1]); }
+      if (rb < nkeys) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
+    }
+    __syncwarp();
+    issue(i + S);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+    }
+    if (lane < 4) {
+      const int h0 = 2 * lane, h1 = 2 * lane + 1;
+      float* dst = max_score + static_cast<int64_t>(t) * hp * max_blocks + j;
+      if (h0 < hp) dst[static_cast<int64_t>(h0) * max_blocks] = mx0 * out_scale;
+      if (h1 < hp) dst[static_cast<int64_t>(h1) * max_blocks] = mx1 * out_scale;
+    }
+  }
+}
+
 }  // namespace
 
 // --------------------------------------------------------------- host side
@@ -497,6 +643,27 @@ msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* 
                                                                  p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: decode launch");
+}
+
+msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const void* pk_pages, const float* pk_scale,
+                                   const int32_t* kv_indices, float* max_score, cudaStream_t st) {
+  if (p->hp > 8) return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore_fp8: up to 8 proxy heads");
+  if (p->dp != 64) return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore_fp8: proxy_head_dim 64 only");
+  CUtensorMap km;
+  const uint64_t dims[2] = {64, static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t strides[1] = {64};
+  const uint32_t box[2] = {64, 128};
+  if (!encode_tensor_map(&km, 2, pk_pages, dims, strides, box, 0, 64))
+    return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore_fp8: tensor map encoding failed");
+  const int32_t* ustart = p->aux_d + p->proxy_unit_start_off;
+  const float scale = 1.0f / sqrtf(64.0f);
+  constexpr int W = kDec8Warps, S = kDec8Stages;
+  const int smem = W * S * 128 * 64 + W * S * 8 + 1024;
+  cudaFuncSetAttribute(proxy_decode_fp8_kernel<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  proxy_decode_fp8_kernel<W, S><<<p->num_sms, 32 * W, smem, st>>>(
+      km, static_cast<const __nv_bfloat16*>(pq), pk_scale, p->tiles_d, ustart, p->n_tiles, kv_indices, p->num_pages,
+      max_score, p->hp, p->max_blocks, scale, p->err_d);
+  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore_fp8: launch");
 }
 
 }  // namespace msa

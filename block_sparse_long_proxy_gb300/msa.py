@@ -39,6 +39,7 @@ SIGNATURES = {
     "msa_plan_total_q": (_i64, [_p]),
     "msa_plan_num_valid_pages": (_p, [_p]),
     "msa_proxy_maxscore": (_i32, [_p, _p, _p, _p, _p, _p]),
+    "msa_proxy_maxscore_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _p]),
     "msa_topk_select": (_i32, [_p, _i32, _i32, _i32, _i32, _p, _p, _p]),
     "msa_sparse_attn": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
     "msa_sparse_attn_bwd": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _p, _p]),
@@ -178,6 +179,20 @@ class Plan:
         _need(out, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
         _check(_lib.msa_proxy_maxscore(self._h, _ptr(pq), _ptr(pk_pages), _ptr(kv_indices), _ptr(out),
                                        _stream(stream)), "msa_proxy_maxscore")
+        return out
+
+    def proxy_maxscore_fp8(self, pq, pk_pages, pk_scale, kv_indices, out=None, stream=None):
+        """Decode proxy pass over e4m3 proxy K pages with one fp32 scale
+        (msa_proxy_maxscore_fp8)."""
+        _need(pq, torch.bfloat16, (self.total_q, self.hp, self.dp), "pq")
+        _need(pk_pages, torch.float8_e4m3fn, (self.num_pages, 1, 128, self.dp), "pk_pages")
+        _need(pk_scale, torch.float32, (1,), "pk_scale")
+        _need(kv_indices, torch.int32, (self.n_page_entries,), "kv_indices")
+        if out is None:
+            out = torch.empty((self.n_tiles, self.hp, self.max_blocks), dtype=torch.float32, device=pq.device)
+        _need(out, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
+        _check(_lib.msa_proxy_maxscore_fp8(self._h, _ptr(pq), _ptr(pk_pages), _ptr(pk_scale), _ptr(kv_indices),
+                                           _ptr(out), _stream(stream)), "msa_proxy_maxscore_fp8")
         return out
 
     # -- stage 3

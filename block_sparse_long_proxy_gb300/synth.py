@@ -7,6 +7,7 @@ fp64 oracle (the oracle reads the identical bf16 / e4m3 bytes).
 Layouts (shared contract, see include/msa.h):
   q, dout        [total_q, Hq, d]          bf16
   k_pages,v_pages[P, Hkv, 128, d]          bf16, or e4m3 with k_scale/v_scale [Hkv] fp32
+  pk_pages_e4m3 [P, 1, 128, dp], pk_scale [1]  e4m3 proxy K (e4m3 cases only)
   pq             [total_q, Hp, dp]         bf16
   pk_pages       [P, 1, 128, dp]           bf16 (one shared proxy K head)
   kv_indices     [sum_s ceil(kv_len_s/128)] int32 page table, logical -> physical
@@ -144,6 +145,10 @@ def make_inputs(case: Case, device="cpu", with_dout=False):
         out["v_pages"] = (v / vs.view(1, -1, 1, 1)).to(torch.float8_e4m3fn)
         out["k_scale"] = ks.float().contiguous()
         out["v_scale"] = vs.float().contiguous()
+        # the shared proxy K head as e4m3 codes with one fp32 scale (decode)
+        ps = pk.abs().amax() / 448.0
+        out["pk_pages_e4m3"] = (pk / ps).to(torch.float8_e4m3fn)
+        out["pk_scale"] = ps.float().reshape(1).contiguous()
     if with_dout:
         out["dout"] = _randn((tq, case.hq, case.d), gen, dev).to(torch.bfloat16)
     del q, k, v, pq, pk

@@ -139,6 +139,24 @@ msa_status msa_proxy_maxscore(msa_plan_t plan, const void* pq, const void* pk_pa
                               const int32_t* kv_indices, float* max_score, msa_stream_t stream);
 
 /*
+ * msa_proxy_maxscore_fp8 -- stage 1 at decode with the proxy K stored as
+ * FP8 e4m3 ("MiniMax-AI/MSA" README, section "Stacks": the FP8 paged decode
+ * stack; an FP8 proxy K halves the proxy scan, which is the largest read of
+ * a decode step).  The logit of a pair is (pq[i,h] . pk_code[k]) *
+ * pk_scale[0] / sqrt(dp), the same dequantisation as the FP8 main K;
+ * otherwise max_score is defined as in msa_proxy_maxscore.
+ *
+ *  pq         bf16 [total_q, Hp, dp].
+ *  pk_pages   e4m3 codes [num_pages, 1, 128, dp], 16-byte aligned.
+ *  pk_scale   device pointer to one fp32 scale (> 0) for the shared proxy head.
+ * Plans whose sequences all have qo_len = 1, dp = 64 and Hp <= 8 only;
+ * others return MSA_ERR_UNSUPPORTED.
+ */
+msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* pk_pages,
+                                  const float* pk_scale, const int32_t* kv_indices, float* max_score,
+                                  msa_stream_t stream);
+
+/*
  * msa_topk_select -- stage 2 ([README] sparse_topk_select(max_score, topk,
  * num_valid_pages); [FLASH]: each proxy head picks its own block set, the
  * local block is always visible).  Plan-free, like the reference call.

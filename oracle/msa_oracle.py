@@ -51,6 +51,9 @@ Readings where the pages are silent (each is listed in the design doc):
   R7  a query row that sees no key of its tile's selected blocks (possible
       only when a tile straddles two blocks and its earlier block is not
       selected) has O = 0 and LSE = -inf.
+  R11 an FP8 e4m3 proxy K (decode) carries one fp32 scale for the single
+      shared proxy head, dequantised like R5: logit =
+      (pq.pk_code)*pk_scale/sqrt(dp).
 """
 from __future__ import annotations
 
@@ -147,12 +150,13 @@ def gather_seq(pages: np.ndarray, kv_indices, indptr, seq: int, kv_len: int) -> 
 # stage 1: proxy max score (R2)
 # ---------------------------------------------------------------------------
 
-def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=None):
+def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=None, pk_scale=None):
     """max_score[t, h, j] = max over rows i of tile t and keys k of block j
     with k visible to i of pq[i,h].pk[k]/sqrt(dp), rounded once to fp32;
     -inf where no pair is visible.  pq: [total_q, Hp, dp] bf16 bits;
     pk: [P, 1, 128, dp] bf16 bits (one shared proxy K head, [README]
-    "num_kv_heads=1").  Returns float32 [n_tiles, Hp, nb_max]; tiles not in
+    "num_kv_heads=1"), or e4m3 codes (uint8) with pk_scale, pk = code *
+    pk_scale (R11).  Returns float32 [n_tiles, Hp, nb_max]; tiles not in
     tile_ids stay -inf."""
     # bit patterns are decoded per tile (the decode is exact), so that large
     # page pools never need a float64 copy
@@ -164,7 +168,8 @@ def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=Non
     for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
         tl = tiles[ti]
         nk = min(tl.nvp * PAGE, tl.kv_len)
-        keys = bf16_to_f64(gather_seq(pk_bits, kv_indices, indptr, tl.seq, tl.kv_len)[:nk, 0, :])  # [nk, dp]
+        raw = gather_seq(pk_bits, kv_indices, indptr, tl.seq, tl.kv_len)[:nk, 0, :]
+        keys = bf16_to_f64(raw) if pk_scale is None else e4m3_to_f64(raw) * float(pk_scale)  # [nk, dp]
         qrows = bf16_to_f64(pq_bits[tl.q_begin: tl.q_end])                     # [R, hp, dp]
         logits = np.matmul(qrows.transpose(1, 0, 2), keys.T) / math.sqrt(dp)   # [hp, R, nk]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)

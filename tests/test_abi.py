@@ -14,7 +14,7 @@ HDR = os.path.join(ROOT, "include", "msa.h")
 def declared_functions():
     text = open(HDR).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(msa_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(msa_[a-z0-9_]+)\s*\(", text)))
 
 
 @pytest.fixture(scope="module")

@@ -192,6 +192,25 @@ def test_proxy_mask_boundary():
     assert float(ms[0, 0, 1]) == -math.inf
 
 
+def test_proxy_fp8_keys_reduce_to_bf16_route():
+    """R11: with e4m3 codes and a power-of-two scale every code * scale is a
+    bf16 value, so the e4m3 route of proxy_max_score must equal the (pinned)
+    bf16 route on those values exactly; a wrong scale or decode would not."""
+    qo, kv, dp = [1, 1, 1], [700, 129, 300], 64
+    gen = torch.Generator().manual_seed(4)
+    nb = sum((k + PAGE - 1) // PAGE for k in kv)
+    codes = (torch.randn(nb + 2, 1, PAGE, dp, generator=gen) * 60).to(torch.float8_e4m3fn)
+    scale = 0.125
+    values = codes.to(torch.float64) * scale
+    assert torch.equal(values.to(torch.bfloat16).to(torch.float64), values)   # exact in bf16
+    pq = torch.randn(3, 2, dp, generator=gen).to(torch.bfloat16)
+    table = torch.randperm(nb + 2, generator=gen)[:nb].numpy()
+    ref = O.proxy_max_score(synth.bits(pq), synth.bits(values.to(torch.bfloat16)), table, qo, kv)
+    got = O.proxy_max_score(synth.bits(pq), synth.bits(codes), table, qo, kv, pk_scale=scale)
+    assert np.array_equal(got, ref)
+    assert np.isfinite(got[:, :, 0]).all()
+
+
 # ----------------------------------------------------- sparse attention ----
 
 def _dense_route(inp, case, idx, fp8=False):

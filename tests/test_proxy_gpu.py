@@ -63,3 +63,50 @@ def test_proxy_prefill_32k_sampled(cuda_dev):
 def test_proxy_decode_full_size_sampled(cuda_dev):
     case = synth.paged_decode()
     _run(case, cuda_dev, tile_ids=[0, 7, 31])
+
+
+def _run_fp8(case, dev, tile_ids=None):
+    """msa_proxy_maxscore_fp8 (e4m3 proxy K with one scale) against the
+    oracle's R11 route on the same codes."""
+    from block_sparse_long_proxy_gb300 import msa
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
+    ms = plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"])
+    torch.cuda.synchronize()
+    plan.check_errors()
+    got = ms.cpu().numpy()
+    ref = O.proxy_max_score(synth.bits(inp["pq"]), synth.bits(inp["pk_pages_e4m3"]), inp["kv_indices"].cpu().numpy(),
+                            case.qo_lens, case.kv_lens, tile_ids=tile_ids, pk_scale=float(inp["pk_scale"][0]))
+    if tile_ids is not None:
+        got, ref = got[tile_ids], ref[tile_ids]
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    err = np.abs(got[fin] - ref[fin]).max() if fin.any() else 0.0
+    assert err <= ATOL, err
+    return err
+
+
+@pytest.mark.parametrize("case", [
+    synth.Case("fp8 proxy decode ragged", [1] * 5, [700, 129, 128, 1, 5000], 16, 8, 128, 8, 64, 4,
+               kv_dtype="e4m3", page_perm_seed=2, extra_pages=3),
+    synth.Case("fp8 proxy decode 3 heads", [1] * 3, [300, 4096, 77], 6, 3, 128, 3, 64, 4, kv_dtype="e4m3",
+               page_perm_seed=4),
+], ids=lambda c: c.name)
+def test_proxy_decode_fp8_small(cuda_dev, case):
+    _run_fp8(case, cuda_dev)
+
+
+def test_proxy_decode_fp8_full_size_sampled(cuda_dev):
+    _run_fp8(synth.paged_decode(), cuda_dev, tile_ids=[0, 7, 31])
+
+
+def test_proxy_fp8_rejects_prefill_plans(cuda_dev):
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("fp8 proxy prefill", [256], [256], 4, 2, 128, 2, 64, 2, kv_dtype="e4m3")
+    inp = synth.make_inputs(case, device=cuda_dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
+    with pytest.raises(msa.MsaError) as e:
+        plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"])
+    assert e.value.status == 2

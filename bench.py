@@ -425,38 +425,35 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
     n_sel = int((idx >= 0).sum().item())
     kv_bytes = n_sel * 2 * 128 * case.d          # e4m3 K and V of each selected (seq, group, block)
     io_bytes = 2 * out.numel() * 2 + lse.numel() * 4
-    reps = max(10, args.steps)
-    times, ptimes = [], []
-    for _ in range(3):
-        attn()
-    for _ in range(reps):
-        flush()
-        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record(stream)
-        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
-        b.record(stream)
-        attn()
-        c.record(stream)
+    # The event clock ticks in ~2 us steps, as long as a third of a decode
+    # launch, so each kernel is timed as T(N x [flush, kernel]) - T(N x
+    # [flush]) over N launches (events around each batch, L2 flushed before
+    # every launch), the median of 5 such differences.
+    n_batch = max(10, min(args.steps, 50))
+
+    def batch(kernel):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        ev[0].record(stream)
+        for _ in range(n_batch):
+            flush()
+            if kernel is not None:
+                kernel()
+        ev[1].record(stream)
         torch.cuda.synchronize()
-        ptimes.append(a.elapsed_time(b))
-        times.append(b.elapsed_time(c))
-    # mean, not median: the event clock ticks in ~2 us steps, a mean averages over them
-    t = statistics.mean(times) / 1e3
-    tp = statistics.mean(ptimes) / 1e3
+        return ev[0].elapsed_time(ev[1])
+
+    def per_launch_s(kernel):
+        for _ in range(3):
+            kernel()
+        diffs = [(batch(kernel) - batch(None)) / n_batch for _ in range(5)]
+        return statistics.median(diffs) / 1e3
+
+    t = per_launch_s(attn)
+    tp = per_launch_s(lambda: plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms))
     # the same scan over the e4m3 proxy K (msa_proxy_maxscore_fp8)
-    p8 = []
-    for _ in range(3):
-        plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
-    for _ in range(reps):
-        flush()
-        a, b = (torch.cuda.Event(enable_timing=True) for _ in range(2))
-        a.record(stream)
-        plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
-        b.record(stream)
-        torch.cuda.synchronize()
-        p8.append(a.elapsed_time(b))
+    tp8 = per_launch_s(lambda: plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"],
+                                                       inp["kv_indices"], out=ms))
     plan.check_errors()
-    tp8 = statistics.mean(p8) / 1e3
     gbs = (kv_bytes + io_bytes) / t / 1e9
     proxy_bytes = sum((k + 127) // 128 for k in case.kv_lens) * 128 * case.dp * 2
     hbm = pk_info.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -466,7 +463,8 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
             "proxy_scan_us": tp * 1e6, "proxy_scan_gbs": proxy_bytes / tp / 1e9,
             "proxy_scan_frac": proxy_bytes / tp / 1e9 / hbm,
             "proxy_scan_fp8_us": tp8 * 1e6, "proxy_scan_fp8_gbs": proxy_bytes / 2 / tp8 / 1e9,
-            "proxy_scan_fp8_frac": proxy_bytes / 2 / tp8 / 1e9 / hbm}
+            "proxy_scan_fp8_frac": proxy_bytes / 2 / tp8 / 1e9 / hbm,
+            "timing": "per launch = (T(N x [L2 flush, kernel]) - T(N x [L2 flush])) / N, N = %d, median of 5" % n_batch}
 
 
 def run_ncu_case(args):

@@ -475,6 +475,8 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
                               const float* v_scale, void* out, float* lse, cudaStream_t st) {
   if (p->d != kD) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs head_dim 128");
   if (p->hq / p->hkv > 16) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs G <= 16");
+  if (decode_ws_applies(p))
+    return launch_attn_decode_ws(p, q, k_pages, v_pages, kv_indices, idx, k_scale, v_scale, out, lse, st);
   CUtensorMap km, vm;
   const uint64_t dims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
   const uint64_t str[1] = {static_cast<uint64_t>(kD)};

@@ -498,6 +498,8 @@ def run_ncu_case(args):
                                  inp["dout"], inp["pq"], inp["pk_pages"])
         if args.ncu_case in ("proxy", "decode"):
             plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        if args.ncu_case == "decode":
+            plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
         if args.ncu_case == "topk":
             msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
         if args.ncu_case in ("attn", "decode"):

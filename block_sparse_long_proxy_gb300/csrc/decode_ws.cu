@@ -5,17 +5,17 @@
 // out = P.(v_code*v_scale).
 //
 // Used when the batch has at least as many (sequence, group) rows as SMs and
-// G <= 8.  Every warp of the CTA streams its own half-blocks (64 keys of K
-// and of V, 8 KB each) through one private 16 KB buffer and keeps its own
+// G <= 8.  Every warp of the CTA streams its own units (kKeys keys of K
+// and of V of one selected block) through a private buffer and keeps its own
 // online-softmax state; the warps' states are merged once, at the end of the
-// row.  With two CTAs per SM that is 12 independent warps per SM, each with
-// one load in flight, and no producer warp or per-block CTA barrier.  Half
-// u of the row (slot u / 2 of kv_block_indexes, keys 64 (u % 2) ...) goes to
-// warp u % kWsWarps.
+// row.  With two CTAs per SM that is 16 independent warps per SM, each with
+// one load in flight, and no producer warp or per-block CTA barrier.  Unit
+// u of the row (slot u / kParts of kv_block_indexes, keys kKeys (u % kParts)
+// ...) goes to warp u % kWsWarps.
 //
-// Per half-block, on mma.sync (f16 in, f32 out), exactly as decode_kernel:
-//   S^T = K . q^T     M = 64 keys, N = 8 heads, K = d (e4m3 -> f16 in registers)
-//   O^T += V^T . P^T  M = d,  N = 8 heads, K = 64 keys (P^T by movmatrix)
+// Per unit, on mma.sync (f16 in, f32 out), exactly as decode_kernel:
+//   S^T = K . q^T     M = kKeys keys, N = 8 heads, K = d (e4m3 -> f16 in registers)
+//   O^T += V^T . P^T  M = d,  N = 8 heads, K = kKeys keys (P^T by movmatrix)
 // with d permuted so that every shared-memory read is one conflict-free word.
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -27,10 +27,13 @@ namespace {
 
 constexpr int kD = 128;
 // a unit is kKeys keys of one selected block (K and V), streamed by one warp
-// through kStg private stages; kWsWarps warps per CTA, two CTAs per SM
-constexpr int kKeys = 64;
+// through kStg private stages; kWsWarps warps per CTA, two CTAs per SM.
+// Measured at 32 x 131072 (keys, stages, warps): (64,1,6) 29.9 us,
+// (32,2,6) 30.4, (64,2,3) 31.0, (64,1,4) 29.7, (32,1,12) 35.5 (spills),
+// (32,1,8) 28.9: 16 warps per SM and the same unit count for every warp.
+constexpr int kKeys = 32;
 constexpr int kStg = 1;
-constexpr int kWsWarps = 6;
+constexpr int kWsWarps = 8;
 constexpr int kWsThreads = 32 * kWsWarps;
 constexpr int kParts = 128 / kKeys;             // units per block
 constexpr int kPartBytes = kKeys * kD;          // K (or V) bytes of one unit

@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
-                    uint32_t* err) {
+                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t kv_pool_heads, int32_t topk,
+                    float scale_log2, uint32_t* err) {
   using L = AttnSmem<D>;
   constexpr int kChunks = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -159,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicOr(err, kErrDeviceCheck);
             page = 0;
           }
-          const int row = static_cast<int>((page * hkv + u.g) * 128);
+          // K/V head of the unit's group, or the single head of a one-head pool
+          const int row = static_cast<int>((page * kv_pool_heads + (kv_pool_heads == 1 ? 0 : u.g)) * 128);
           mbar_expect_tx(k_full + s, L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
             tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
@@ -387,6 +388,17 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   p->n_attn_units = static_cast<int32_t>(us.size());
   const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
   aux.insert(aux.end(), raw, raw + us.size() * 4);
+  // the proxy softmax of the backward: proxy head g over group g's blocks
+  std::vector<AttnUnit> ps;
+  for (int t = 0; t < p->n_tiles; ++t)
+    for (int g = 0; g < p->hkv; ++g) ps.push_back(AttnUnit{t, g, g, 1});
+  std::stable_sort(ps.begin(), ps.end(), [&](const AttnUnit& a, const AttnUnit& b) {
+    return std::min(p->tiles[a.tile].nvp, p->topk) > std::min(p->tiles[b.tile].nvp, p->topk);
+  });
+  p->proxy_attn_units_off = static_cast<int64_t>(aux.size());
+  p->n_proxy_attn_units = static_cast<int32_t>(ps.size());
+  raw = reinterpret_cast<const int32_t*>(ps.data());
+  aux.insert(aux.end(), raw, raw + ps.size() * 4);
 }
 
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
@@ -413,16 +425,47 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attn_fwd_kernel<128><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
-                                                                   p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-                                                                   scale_log2, p->err_d);
+                                                                   p->num_pages, o, lse, p->hq, p->hkv, p->hkv,
+                                                                   p->topk, scale_log2, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attn_fwd_kernel<64><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
-                                                                 p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-                                                                 scale_log2, p->err_d);
+                                                                 p->num_pages, o, lse, p->hq, p->hkv, p->hkv,
+                                                                 p->topk, scale_log2, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
+}
+
+// The proxy softmax of the backward (the KL term's p_proxy): for proxy head g
+// of each tile, over group g's cached visible keys, Op = sum_k p(k) pk[k]
+// and its natural-log LSE, with scores pq.pk/sqrt(dp).  It is the forward
+// above with pq as the queries, the one shared proxy K head as both keys and
+// values, and one head per unit.  Op: bf16 [total_q, Hp, 64]; lse: fp32
+// [total_q, Hp].
+msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                                const int32_t* idx, void* op, float* lse, cudaStream_t st) {
+  if (p->dp != 64) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: proxy_head_dim 64 only");
+  if (p->topk > kMaxTopk) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: topk above 1024");
+  CUtensorMap qm, km;
+  const uint64_t qdims[3] = {64, static_cast<uint64_t>(p->hp), static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {128, static_cast<uint64_t>(p->hp) * 128};
+  const uint32_t qbox[3] = {64, 1, 128};
+  const uint64_t kdims[2] = {64, static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t kstr[1] = {128};
+  const uint32_t kbox[2] = {64, 128};
+  if (!encode_tensor_map(&qm, 3, pq, qdims, qstr, qbox, 1, 128) ||
+      !encode_tensor_map(&km, 2, pk_pages, kdims, kstr, kbox, 1, 128))
+    return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
+  const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->proxy_attn_units_off);
+  const float scale_log2 = 1.4426950408889634f / 8.0f;  // 1 / sqrt(64)
+  const int grid = std::min(p->n_proxy_attn_units, p->num_sms);
+  const int smem = AttnSmem<64>::kBytes + 1024;
+  cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  attn_fwd_kernel<64><<<grid, kThreads, smem, st>>>(qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx,
+                                                    kv_indices, p->num_pages, static_cast<__nv_bfloat16*>(op), lse,
+                                                    p->hp, p->hkv, 1, p->topk, scale_log2, p->err_d);
+  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: proxy softmax launch");
 }
 
 }  // namespace msa

@@ -17,9 +17,12 @@
 //
 // Kernels, in stream order:
 //   zero     dpk rows of every referenced page (it is reduced by atomics)
+//   proxy    the proxy softmax over Omega on the tensor cores: the forward
+//            attention kernel (attn_fwd.cu) with pq as queries and the shared
+//            proxy K head as keys and values gives p_proxy . pk and its LSE
 //   prep     per (tile, group): D of the group's heads and lse * log2(e),
-//            both stored [head][row]; the proxy LSE over Omega (online
-//            softmax, [group][row]) and dpq's proxy term (plain store)
+//            both stored [head][row]; the proxy LSE in log2 units
+//            ([group][row]) and dpq's proxy term (plain store)
 //   index    block -> tiles inverse index of the cached selections
 //   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
 //            store) and dpq's main term (fp32 atomics, G per element)
@@ -27,8 +30,7 @@
 //            the tiles that selected the block (sorted, so sums are
 //            deterministic); dk, dv (owned, plain store) and dpk (both
 //            terms, fp32 atomics across groups)
-// The prep kernel's small products use mma.sync m16n8k16 (bf16 in, f32
-// accumulate) with ldmatrix fragments from padded shared-memory tiles.
+
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -39,86 +41,25 @@ namespace {
 
 constexpr int kD = 128;    // head dim of this kernel
 constexpr int kDP = 64;    // proxy head dim of this kernel
-constexpr int kLdP = kDP + 8;  // padded smem row of 64-wide tiles: 144 B
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// ---------------------------------------------------------------- helpers
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* r) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-// cp.async of 16 bytes; src_bytes = 0 zero-fills the destination.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-
-// A fragment (16 x 16, row-major) at (r0, c0) of a bf16 smem tile with row
-// pitch `ld` elements.
-__device__ __forceinline__ void frag_a(const __nv_bfloat16* tile, int ld, int r0, int c0, uint32_t* a) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4(smem_u32(tile + (r0 + (lane & 15)) * ld + c0 + (lane >> 4) * 8), a);
-}
-// B fragments of two n8-tiles for S = A . T^T where T is stored row-major
-// with rows = n: n in [n0, n0+16), k in [k0, k0+16).
-// b[0..1]: n-tile n0, b[2..3]: n-tile n0+8.
-__device__ __forceinline__ void frag_b_nk(const __nv_bfloat16* tile, int ld, int n0, int k0, uint32_t* b) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4(smem_u32(tile + (n0 + (lane & 7) + ((lane >> 4) << 3)) * ld + k0 + ((lane >> 3) & 1) * 8), b);
-}
-// B fragments of two n8-tiles for O = A . T where T is stored row-major with
-// rows = k: k in [k0, k0+16), n in [n0, n0+16).
-__device__ __forceinline__ void frag_b_kn(const __nv_bfloat16* tile, int ld, int k0, int n0, uint32_t* b) {
-  const int lane = threadIdx.x & 31;
-  ldsm_x4_t(smem_u32(tile + (k0 + (lane & 7) + ((lane >> 3) & 1) * 8) * ld + n0 + (lane >> 4) * 8), b);
-}
-// Load `rows` valid rows (others zero) of a [128 x W] bf16 tile from global
-// rows at `src` with row stride `stride` elements into a padded smem tile.
-template <int W>
-__device__ __forceinline__ void load_tile(__nv_bfloat16* dst, const __nv_bfloat16* src, int64_t stride, int rows) {
-  constexpr int kChunks = W / 8;  // 16-byte chunks per row
-  for (int e = threadIdx.x; e < 128 * kChunks; e += blockDim.x) {
-    const int r = e / kChunks, c = e % kChunks;
-    const bool ok = r < rows;
-    cp_async16(dst + r * (W + 8) + c * 8, ok ? src + r * stride + c * 8 : src, ok ? 16 : 0);
-  }
-}
-__device__ __forceinline__ uint32_t pack2(float lo, float hi) { return pack_bf16x2(lo, hi); }
-
 // ------------------------------------------------------------------ prep
 
-// Per (tile, group): D[row, h] for the group's heads, the proxy LSE over the
-// cached visible keys (log2 units, scale included) and dpq's proxy term.
+// Per (tile, group): D[row, h] = rowsum(dout * out) and lse * log2(e) of the
+// group's heads, both stored [head][row]; the proxy LSE of the group in log2
+// units, [group][row]; and dpq's proxy term w/sqrt(dp) * p_proxy . pk, from
+// the proxy softmax (launch_proxy_softmax) run just before.
 __global__ void __launch_bounds__(kThreads)
-    bwd_prep_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
-                    const int32_t* __restrict__ kv_indices, int64_t num_pages, const __nv_bfloat16* __restrict__ out,
-                    const __nv_bfloat16* __restrict__ dout, const __nv_bfloat16* __restrict__ pq,
-                    const __nv_bfloat16* __restrict__ pk, const float* __restrict__ lse, float* __restrict__ dsumt,
-                    float* __restrict__ lse2t, float* __restrict__ lsept, float* __restrict__ dpq, int32_t hq,
-                    int32_t hkv, int32_t topk, int32_t total_q, float kl_weight, uint32_t* err) {
-  __shared__ __align__(16) __nv_bfloat16 pqs[128 * kLdP];
-  __shared__ __align__(16) __nv_bfloat16 pks[128 * kLdP];
+    bwd_prep_kernel(const TileInfo* __restrict__ tiles, const __nv_bfloat16* __restrict__ out,
+                    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
+                    const __nv_bfloat16* __restrict__ op, const float* __restrict__ lse_p,
+                    float* __restrict__ dsumt, float* __restrict__ lse2t, float* __restrict__ lsept,
+                    float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t total_q, float kl_weight) {
   const int t = blockIdx.x / hkv, g = blockIdx.x % hkv;
   const TileInfo tl = tiles[t];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gr = lane >> 2, t4 = lane & 3;
   const int G = hq / hkv;
 
   // D = rowsum(dout * out): two lanes per row, 64 d values each
@@ -149,117 +90,24 @@ __global__ void __launch_bounds__(kThreads)
       }
     }
 
-  // proxy softmax over the cached visible keys (online), O_proxy = p_proxy.pk
-  load_tile<kDP>(pqs, pq + (static_cast<int64_t>(tl.q_begin) * hkv + g) * kDP, static_cast<int64_t>(hkv) * kDP,
-                 tl.rows);
-  const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
-  const int r0 = warp * 16 + gr, r1 = r0 + 8;
-  const int qp0 = tl.pos0 + r0, qp1 = tl.pos0 + r1;
-  const bool ok0 = r0 < tl.rows, ok1 = r1 < tl.rows;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  float o[8][4];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hkv + g) * topk;
-  for (int k = 0; k < topk; ++k) {
-    const int j = row_idx[k];
-    if (j < 0 || j >= tl.nvp) continue;
-    int64_t page = kv_indices[tl.page_base + j];
-    if (page < 0 || page >= num_pages) {
-      if (threadIdx.x == 0) atomicOr(err, kErrDeviceCheck);
-      page = 0;
-    }
-    __syncthreads();  // previous block's pks reads are done
-    load_tile<kDP>(pks, pk + page * 128 * kDP, kDP, 128);
-    cp_async_wait_all();
-    __syncthreads();
-    float z[16][4];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) z[i][0] = z[i][1] = z[i][2] = z[i][3] = 0.f;
-#pragma unroll
-    for (int kc = 0; kc < kDP / 16; ++kc) {
-      uint32_t a[4];
-      frag_a(pqs, kLdP, warp * 16, kc * 16, a);
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        uint32_t b[4];
-        frag_b_nk(pks, kLdP, np * 16, kc * 16, b);
-        mma_bf16(z[2 * np], a, b[0], b[1]);
-        mma_bf16(z[2 * np + 1], a, b[2], b[3]);
-      }
-    }
-    // mask and row max (rows r0: z[.][0..1], r1: z[.][2..3])
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int kp = j * 128 + nt * 8 + 2 * t4 + c;
-        z[nt][c] = (ok0 && kp <= qp0) ? z[nt][c] * zsl2 : -INFINITY;
-        z[nt][2 + c] = (ok1 && kp <= qp1) ? z[nt][2 + c] * zsl2 : -INFINITY;
-        mx0 = fmaxf(mx0, z[nt][c]);
-        mx1 = fmaxf(mx1, z[nt][2 + c]);
-      }
-#pragma unroll
-    for (int s = 1; s < 4; s <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, s));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, s));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = ex2_approx(m0 - mu0), al1 = ex2_approx(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float s0 = 0.f, s1 = 0.f;
-    uint32_t pa[8][4];
-#pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
-      const float p00 = ex2_approx(z[nt][0] - mu0), p01 = ex2_approx(z[nt][1] - mu0);
-      const float p10 = ex2_approx(z[nt][2] - mu1), p11 = ex2_approx(z[nt][3] - mu1);
-      s0 += p00 + p01;
-      s1 += p10 + p11;
-      // C -> A fragment: k chunk nt/2; even n-tile fills a0a1/a2a3, odd a4a5/a6a7
-      pa[nt >> 1][(nt & 1) * 2 + 0] = pack2(p00, p01);
-      pa[nt >> 1][(nt & 1) * 2 + 1] = pack2(p10, p11);
-    }
-    l0 = l0 * al0 + s0;
-    l1 = l1 * al1 + s1;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      o[i][0] *= al0;
-      o[i][1] *= al0;
-      o[i][2] *= al1;
-      o[i][3] *= al1;
-    }
-#pragma unroll
-    for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        uint32_t b[4];
-        frag_b_kn(pks, kLdP, kc * 16, np * 16, b);
-        mma_bf16(o[2 * np], pa[kc], b[0], b[1]);
-        mma_bf16(o[2 * np + 1], pa[kc], b[2], b[3]);
-      }
-  }
-  cp_async_wait_all();
-#pragma unroll
-  for (int s = 1; s < 4; s <<= 1) {
-    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, s);
-    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, s);
-  }
+  // proxy LSE in log2 units, and dpq's proxy term
   const float f = kl_weight * rsqrtf(static_cast<float>(kDP));
-  const float i0 = l0 > 0.f ? f / l0 : 0.f, i1 = l1 > 0.f ? f / l1 : 0.f;
-  if (ok0 && t4 == 0) lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r0] = l0 > 0.f ? m0 + log2f(l0) : -INFINITY;
-  if (ok1 && t4 == 0) lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r1] = l1 > 0.f ? m1 + log2f(l1) : -INFINITY;
+  for (int r = threadIdx.x; r < tl.rows; r += blockDim.x) {
+    const int64_t q_row = tl.q_begin + r;
+    lsept[static_cast<int64_t>(g) * total_q + q_row] = lse_p[q_row * hkv + g] * kLog2e;
+  }
+  for (int e = threadIdx.x; e < tl.rows * (kDP / 8); e += blockDim.x) {
+    const int r = e / (kDP / 8), c = e % (kDP / 8);
+    const int64_t base = (static_cast<int64_t>(tl.q_begin + r) * hkv + g) * kDP + c * 8;
+    const uint4 v = *reinterpret_cast<const uint4*>(op + base);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float4* dst = reinterpret_cast<float4*>(dpq + base);
 #pragma unroll
-  for (int nt = 0; nt < 8; ++nt) {
-    const int c = nt * 8 + 2 * t4;
-    if (ok0)
-      *reinterpret_cast<float2*>(dpq + (static_cast<int64_t>(tl.q_begin + r0) * hkv + g) * kDP + c) =
-          make_float2(o[nt][0] * i0, o[nt][1] * i0);
-    if (ok1)
-      *reinterpret_cast<float2*>(dpq + (static_cast<int64_t>(tl.q_begin + r1) * hkv + g) * kDP + c) =
-          make_float2(o[nt][2] * i1, o[nt][3] * i1);
+    for (int k = 0; k < 2; ++k) {
+      const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * k]));
+      const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * k + 1]));
+      dst[k] = make_float4(lo.x * f, lo.y * f, hi.x * f, hi.y * f);
+    }
   }
 }
 
@@ -331,12 +179,17 @@ __global__ void bwd_zero_dpk_kernel(const int32_t* __restrict__ kv_indices, int3
 
 }  // namespace
 
+// The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
+// fp32), lsept ([Hkv][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
+// Hp, dp]) and LSE (fp32 [total_q, Hp]), then the inverse index (int32).
+static size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
+
 size_t bwd_scratch_bytes(const msa_plan_s* p) {
   if (p->decode) return 0;
+  const size_t tq = static_cast<size_t>(p->total_q);
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
-  const size_t bytes = sizeof(float) * static_cast<size_t>(p->total_q) * (2 * p->hq + p->hkv) +
-                       sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk);
-  return (bytes + 255) & ~size_t(255);
+  return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hkv) + al256(2 * tq * p->hkv * kDP) + al256(4 * tq * p->hkv) +
+         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk));
 }
 
 void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
@@ -357,25 +210,34 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   if (p->bwd_d == nullptr) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: plan has no backward scratch");
   const int n_ent = p->n_page_entries;
   const size_t ent = static_cast<size_t>(n_ent) * p->hkv;
-  float* dsumt = reinterpret_cast<float*>(p->bwd_d);               // [hq][total_q]
-  float* lse2t = dsumt + static_cast<size_t>(p->total_q) * p->hq;  // [hq][total_q], lse * log2(e)
-  float* lsept = lse2t + static_cast<size_t>(p->total_q) * p->hq;  // [hkv][total_q], log2 units
-  int32_t* cnt = reinterpret_cast<int32_t*>(lsept + static_cast<size_t>(p->total_q) * p->hkv);
+  const size_t tq = static_cast<size_t>(p->total_q);
+  char* sp = static_cast<char*>(p->bwd_d);
+  float* dsumt = reinterpret_cast<float*>(sp);                        // [hq][total_q]
+  sp += al256(4 * tq * p->hq);
+  float* lse2t = reinterpret_cast<float*>(sp);                        // [hq][total_q], lse * log2(e)
+  sp += al256(4 * tq * p->hq);
+  float* lsept = reinterpret_cast<float*>(sp);                        // [hkv][total_q], log2 units
+  sp += al256(4 * tq * p->hkv);
+  auto* op = reinterpret_cast<__nv_bfloat16*>(sp);                    // [total_q, hp, dp] bf16
+  sp += al256(2 * tq * p->hkv * kDP);
+  float* lse_p = reinterpret_cast<float*>(sp);                        // [total_q, hp], natural log
+  sp += al256(4 * tq * p->hkv);
+  int32_t* cnt = reinterpret_cast<int32_t*>(sp);
   int32_t* off = cnt + ent;
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
   const int32_t* blk_j = p->aux_d + p->blk_j_off;
   const auto* O = static_cast<const __nv_bfloat16*>(out);
   const auto* dO = static_cast<const __nv_bfloat16*>(dout);
-  const auto* PQ = static_cast<const __nv_bfloat16*>(pq);
-  const auto* PK = static_cast<const __nv_bfloat16*>(pk_pages);
   const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hkv * p->topk;
 
   bwd_zero_dpk_kernel<<<n_ent, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, dpk);
-  bwd_prep_kernel<<<p->n_tiles * p->hkv, kThreads, 0, st>>>(p->tiles_d, idx, kv_indices, p->num_pages, O, dO, PQ, PK,
-                                                           lse, dsumt, lse2t, lsept, dpq, p->hq, p->hkv, p->topk,
-                                                           static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
-  msa_status s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
+  msa_status s = launch_proxy_softmax(p, pq, pk_pages, kv_indices, idx, op, lse_p, st);
+  if (s != MSA_OK) return s;
+  bwd_prep_kernel<<<p->n_tiles * p->hkv, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
+                                                           dpq, p->hq, p->hkv, static_cast<int32_t>(p->total_q),
+                                                           kl_weight);
+  s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s != MSA_OK) return s;
   const int sel_blocks = static_cast<int>((n_sel + 255) / 256);
   bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, cnt);

@@ -61,6 +61,8 @@ struct msa_plan_s {
   int64_t proxy_unit_start_off = 0;  // decode proxy: first unit of each tile
   int64_t attn_units_off = 0;        // prefill attention work units
   int32_t n_attn_units = 0;
+  int64_t proxy_attn_units_off = 0;  // backward proxy softmax work units
+  int32_t n_proxy_attn_units = 0;
   int64_t blk_j_off = 0;             // backward: logical block of each page-table entry
   int32_t n_page_entries = 0;        // sum over sequences of ceil(kv_len / 128)
   void* bwd_d = nullptr;             // backward scratch (D, proxy LSE, inverse index)
@@ -76,6 +78,10 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
+// The backward's proxy softmax (attn_fwd.cu): Op = sum_k p_proxy(k) pk[k]
+// (bf16 [total_q, Hp, 64]) and its natural-log LSE ([total_q, Hp]).
+msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                                const int32_t* idx, void* op, float* lse, cudaStream_t st);
 // dQ and dpq's main term on the tensor cores (bwd_dq.cu).
 msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,

@@ -48,6 +48,25 @@ def test_fp8_decode_random_indexes(cuda_dev, case):
     _check(case, cuda_dev)
 
 
+# batches with at least as many (sequence, group) rows as SMs take the
+# warp-streaming kernel (one CTA per row); these cover it at sizes the
+# oracle runs in seconds: ragged kv, padded slots (topk above a sequence's
+# blocks), G = 8 and G = 4, partial last pages.
+_LENS = [int(x) for x in np.random.default_rng(21).integers(1, 3000, size=40)]
+WS_CASES = [
+    synth.Case("rows>=SMs G=8 ragged", [1] * 20, _LENS[:20], 64, 8, 128, 8, 64, 8, kv_dtype="e4m3",
+               page_perm_seed=9, extra_pages=5),
+    synth.Case("rows>=SMs G=4 padded slots", [1] * 40, _LENS, 16, 4, 128, 4, 64, 12, kv_dtype="e4m3",
+               page_perm_seed=10),
+]
+
+
+@pytest.mark.parametrize("case", WS_CASES, ids=lambda c: c.name)
+def test_fp8_decode_one_cta_per_row(cuda_dev, case):
+    assert len(case.qo_lens) * case.hkv >= torch.cuda.get_device_properties(cuda_dev).multi_processor_count
+    _check(case, cuda_dev)
+
+
 def test_fp8_decode_two_calls_reuse_workspace(cuda_dev):
     """The split-K partials live in the plan; a second call with other
     indexes overwrites them completely."""

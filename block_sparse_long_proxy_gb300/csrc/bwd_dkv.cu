@@ -53,7 +53,7 @@ struct DkvSmem {
   static constexpr int kLsepOff = kRowOff + kQStages * 128 * 4;
   static constexpr int kListOff = kLsepOff + kPqStages * 64 * 4;
   static constexpr int kBarOff = kListOff + kMaxList * 4;
-  static constexpr int kBytes = kBarOff + 8 * 24;
+  static constexpr int kBytes = kBarOff + 8 * 26;
 };
 
 __device__ __forceinline__ uint32_t ts_col(uint32_t base, int kk) {
@@ -110,9 +110,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pq_empty = pq_full + kPqStages;     // [kPqStages]
   uint64_t* sp_full = pq_empty + kPqStages;
   uint64_t* pp_full = sp_full + 1;
-  uint64_t* s_full = pp_full + 1;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* done = p_full + 1;
+  uint64_t* s_full = pp_full + 1;    // S^T computed
+  uint64_t* dp_full = s_full + 1;    // dP^T computed
+  uint64_t* p_full = dp_full + 1;    // P^T written (bf16, in place of S^T)
+  uint64_t* ds_full = p_full + 1;    // dS^T written (bf16, in place of dP^T)
+  uint64_t* done = ds_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sp_full, 1);
     mbar_init(pp_full, kSoftWarps);
     mbar_init(s_full, 1);
+    mbar_init(dp_full, 1);
     mbar_init(p_full, kSoftWarps);
+    mbar_init(ds_full, kSoftWarps);
     mbar_init(done, 1);
     fence_mbar_init();
   }
@@ -256,13 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t qa = qd0 + s * L::kQdBytes, da = qa + 16384;
             if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
             tc_fence_after();
+            auto dpt = [&]() {  // dP^T = V . dO^T
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
-              mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
-                     smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
-            }
+              for (int kk = 0; kk < kD / 16; ++kk) {
+                const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
+                mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
+                       smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
+              }
+              mma_commit(dp_full);
+            };
             if (hh == 0) {  // dP^T of the first head overlaps the proxy softmax
+              dpt();
               if (!(ok = mbar_wait(pp_full, pi & 1, err))) break;
               tc_fence_after();
 #pragma unroll
@@ -276,6 +284,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ts(tmem + kColS, tmem + kColK + kk * 8, smem_desc(qa + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
             }
             mma_commit(s_full);
+            if (hh > 0) dpt();  // the softmax starts on S^T while dP^T runs
+            // dV and dpk need only P^T; dK waits for dS^T
             if (!(ok = mbar_wait(p_full, qi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
@@ -284,9 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                      id_d, 1);
               mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128),
                      id_p, 1);
+            }
+            if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), smem_desc(qa + kk * 2048, 8192, 1024, kSwizzle128),
                      id_d, 1);
-            }
             mma_commit(qd_empty + s);
           }
           if (!ok) break;
@@ -372,16 +386,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
           if (!(ok = mbar_wait(s_full, qi & 1, err))) break;
           tc_fence_after();
-          uint32_t sv[32], dv_[32], pa[16], da[16];
+          // P^T first (dP^T may still be running), then dS^T
+          uint32_t sv[32], pa[16], da[16];
+          float pr[32];
           tmem_ld32(lane_base + kColS + c0, sv);
-          tmem_ld32(lane_base + kColDP + c0, dv_);
           tmem_wait_ld();
           const float2* nl2 = reinterpret_cast<const float2*>(row_s + s * 128 + c0);
           const float2* ndd = reinterpret_cast<const float2*>(row_s + s * 128 + 64 + c0);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float2 nl = nl2[c >> 1], nd = ndd[c >> 1];
-            float x0, x1, t0, t1, d0, d1;
+            const float2 nl = nl2[c >> 1];
+            float x0, x1;
             ffma2v(x0, x1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), sl2, sl2, nl.x, nl.y);
             float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             if (need_mask) {
@@ -389,17 +404,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(r < tl.rows && kpos <= tl.pos0 + r)) p0 = 0.f;
               if (!(r + 1 < tl.rows && kpos <= tl.pos0 + r + 1)) p1 = 0.f;
             }
-            fadd2v(t0, t1, __uint_as_float(dv_[c]), __uint_as_float(dv_[c + 1]), nd.x, nd.y);
-            fmul2(d0, d1, t0, t1, p0, p1);
+            pr[c] = p0;
+            pr[c + 1] = p1;
             pa[c >> 1] = pack_bf16x2(p0, p1);
-            da[c >> 1] = pack_bf16x2(d0, d1);
           }
           tmem_st16(lane_base + kColS + c0, pa);
-          tmem_st16(lane_base + kColDP + c0, da);
           tmem_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(p_full);
+          if (!(ok = mbar_wait(dp_full, qi & 1, err))) break;
+          tc_fence_after();
+          tmem_ld32(lane_base + kColDP + c0, sv);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 nd = ndd[c >> 1];
+            float t0, t1, d0, d1;
+            fadd2v(t0, t1, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]), nd.x, nd.y);
+            fmul2(d0, d1, t0, t1, pr[c], pr[c + 1]);
+            da[c >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(lane_base + kColDP + c0, da);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ds_full);
         }
       }
     }

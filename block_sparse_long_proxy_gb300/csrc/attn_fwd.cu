@@ -75,14 +75,14 @@ __device__ __forceinline__ int unit_blocks(const AttnUnit& u, const TileInfo& tl
 // barrier's phase comes from a running count (per head for the S / P / O
 // barriers), and Q is released right after a unit's last QK so the next
 // unit's Q load overlaps the tail of the current one.
-template <int D>
+template <int D, bool kOneKvHead>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t kv_pool_heads, int32_t topk,
-                    float scale_log2, uint32_t* err) {
+                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
+                    uint32_t* err) {
   using L = AttnSmem<D>;
   constexpr int kChunks = D / 64;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             page = 0;
           }
           // K/V head of the unit's group, or the single head of a one-head pool
-          const int row = static_cast<int>((page * kv_pool_heads + (kv_pool_heads == 1 ? 0 : u.g)) * 128);
+          const int row = static_cast<int>((kOneKvHead ? page : page * hkv + u.g) * 128);
           mbar_expect_tx(k_full + s, L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
             tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
@@ -423,16 +423,16 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
   const int grid = std::min(p->n_attn_units, p->num_sms);  // persistent: one CTA per SM
   if (p->d == 128) {
     const int smem = AttnSmem<128>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<128><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
-                                                                   p->num_pages, o, lse, p->hq, p->hkv, p->hkv,
-                                                                   p->topk, scale_log2, p->err_d);
+    cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<128, false><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx,
+                                                              kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+                                                              scale_log2, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<64><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices,
-                                                                 p->num_pages, o, lse, p->hq, p->hkv, p->hkv,
-                                                                 p->topk, scale_log2, p->err_d);
+    cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<64, false><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx,
+                                                             kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+                                                             scale_log2, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
 }
@@ -461,10 +461,10 @@ msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void*
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // 1 / sqrt(64)
   const int grid = std::min(p->n_proxy_attn_units, p->num_sms);
   const int smem = AttnSmem<64>::kBytes + 1024;
-  cudaFuncSetAttribute(attn_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  attn_fwd_kernel<64><<<grid, kThreads, smem, st>>>(qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx,
-                                                    kv_indices, p->num_pages, static_cast<__nv_bfloat16*>(op), lse,
-                                                    p->hp, p->hkv, 1, p->topk, scale_log2, p->err_d);
+  cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  attn_fwd_kernel<64, true><<<grid, kThreads, smem, st>>>(qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx,
+                                                          kv_indices, p->num_pages, static_cast<__nv_bfloat16*>(op),
+                                                          lse, p->hp, p->hkv, p->topk, scale_log2, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: proxy softmax launch");
 }
 

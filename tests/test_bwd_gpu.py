@@ -84,3 +84,26 @@ def test_bwd_training_64k_sampled(cuda_dev):
     compare_out(got["dk"][pages], ref["dk"][pages], O_ATOL_BF16, "dk")
     compare_out(got["dv"][pages], ref["dv"][pages], O_ATOL_BF16, "dv")
     compare_out(got["dpk"][pages], ref["dpk"][pages], O_ATOL_BF16, "dpk")
+
+
+def test_warmup_mode_dense_all_blocks(cuda_dev):
+    """Warmup mode (dense main attention and a dense-domain KL) is the sparse
+    path with every valid block selected: msa_topk_select with topk >=
+    max_blocks picks them all, and the forward and backward then cover all
+    causal keys.  The whole chain runs on the GPU; the oracle checks the
+    selection, the forward and every gradient."""
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("warmup dense", [1024, 300], [1024, 700], 8, 2, 128, 2, 64, 8, page_perm_seed=2)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    plan = make_plan(case, inp)
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx_t = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    idx = idx_t.cpu().numpy()
+    for t, tl in enumerate(O.tiles_of(case.qo_lens, case.kv_lens)):
+        for g in range(case.hkv):
+            want = list(range(tl.nvp)) + [-1] * (case.topk - tl.nvp)
+            assert list(idx[t, g]) == want, (t, g, idx[t, g])
+    got = _run_gpu(case, inp, idx_t, 1.0)
+    ref = _oracle(case, inp, idx, 1.0)
+    for name in ("dq", "dpq", "dk", "dv", "dpk"):
+        compare_out(got[name], ref[name], O_ATOL_BF16, name)

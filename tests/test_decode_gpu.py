@@ -58,6 +58,9 @@ WS_CASES = [
                page_perm_seed=9, extra_pages=5),
     synth.Case("rows>=SMs G=4 padded slots", [1] * 40, _LENS, 16, 4, 128, 4, 64, 12, kv_dtype="e4m3",
                page_perm_seed=10),
+    # topk above the warp-streaming kernel's limit: the ring kernel, one CTA per row
+    synth.Case("rows>=SMs topk 80", [1] * 20, _LENS[:20], 64, 8, 128, 8, 64, 80, kv_dtype="e4m3",
+               page_perm_seed=11),
 ]
 
 

@@ -49,16 +49,6 @@ struct WsSmem {
   static constexpr int kBytes = kBarOff + 8 * kWsWarps * kStg;
 };
 
-__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
-  uint32_t r;
-  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(x));
-  return r;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
 // byte offset of (row, byte col) in a tile of 128-byte rows written by TMA
 // with 128-byte swizzle: the 16-byte chunk index is XORed with row % 8.
 __device__ __forceinline__ uint32_t swz(int row, int col) {

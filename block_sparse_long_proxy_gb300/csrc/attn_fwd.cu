@@ -41,34 +41,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
   tmem_st16(taddr + 16, r + 16);
 }
 
+// One unit's cached blocks, built once by the producer warp (its lanes read
+// the top-k row and the page table in parallel) for the MMA and softmax warps.
+struct UnitList {
+  int32_t n, nh, h0, q_begin, rows, pos0, pad[10];
+  int32_t j[kMaxTopk];    // selected blocks, padding and out-of-range entries dropped
+  int32_t row[kMaxTopk];  // their first K/V tensor-map row
+};
+constexpr int kListSlots = 2;
+
 template <int D>
 struct AttnSmem {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16, in D/64 swizzled chunks of 16 KB
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kListOff = kVOff + kStages * kTileBytes;  // block lists: producer, MMA, softmax
-  static constexpr int kBarOff = kListOff + 3 * kMaxTopk * 4;
+  static constexpr int kListOff = kVOff + kStages * kTileBytes;
+  static constexpr int kBarOff = kListOff + kListSlots * static_cast<int>(sizeof(UnitList));
   static constexpr int kBytes = kBarOff + 8 * 32;
 };
-
-// The cached blocks of a unit's (tile, group), padding skipped; entries past
-// the tile's valid blocks are dropped (and reported when `report`).
-__device__ __forceinline__ int unit_blocks(const AttnUnit& u, const TileInfo& tl, const int32_t* __restrict__ idx,
-                                           int hkv, int topk, int32_t* out, uint32_t* err, bool report) {
-  const int32_t* row = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
-  int n = 0;
-  for (int k = 0; k < topk; ++k) {
-    const int j = row[k];
-    if (j < 0) continue;
-    if (j >= tl.nvp) {
-      if (report) atomicOr(err, kErrDeviceCheck);
-      continue;
-    }
-    out[n++] = j;
-  }
-  return n;
-}
 
 // Persistent: CTA b takes units b, b + gridDim.x, ... (heaviest first).
 // Tensor memory, barriers and the K/V ring live across units; every
@@ -90,22 +81,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* q_s = smem + L::kQOff;
   uint8_t* k_s = smem + L::kKOff;
   uint8_t* v_s = smem + L::kVOff;
-  int32_t* list_p = reinterpret_cast<int32_t*>(smem + L::kListOff);
-  int32_t* list_m = list_p + kMaxTopk;
-  int32_t* list_s = list_m + kMaxTopk;
+  UnitList* lists = reinterpret_cast<UnitList*>(smem + L::kListOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;
-  uint64_t* v_full = k_full + kStages;
-  uint64_t* kv_empty = v_full + kStages;
+  uint64_t* kv_full = bars + 2;              // [kStages]: K and V of a block
+  uint64_t* kv_empty = kv_full + kStages;
   uint64_t* s_full = kv_empty + kStages;  // [2]
   uint64_t* p_full = s_full + 2;          // [2]
-  uint64_t* o_done = p_full + 2;          // [2]
+  uint64_t* o_done = p_full + 2;          // [2]: a unit's last P.V of head h
   uint64_t* o_free = o_done + 2;          // [2]
-  uint64_t* drain = o_free + 2;
-  volatile int32_t* n_soft = reinterpret_cast<int32_t*>(drain + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* list_full = o_free + 2;       // [kListSlots]
+  uint64_t* list_empty = list_full + kListSlots;
+  uint64_t* drain = list_empty + kListSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -115,8 +104,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(k_full + s, 1);
-      mbar_init(v_full + s, 1);
+      mbar_init(kv_full + s, 1);
       mbar_init(kv_empty + s, 1);
     }
     for (int h = 0; h < 2; ++h) {
@@ -124,6 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full + h, 4);
       mbar_init(o_done + h, 1);
       mbar_init(o_free + h, 4);
+    }
+    for (int i = 0; i < kListSlots; ++i) {
+      mbar_init(list_full + i, 1);
+      mbar_init(list_empty + i, 1 + kSoftWarps);  // the MMA thread and every softmax warp
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -139,96 +131,158 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8) {
     // ---------------------------------------------------------- producer
-    if (lane == 0) {
-      int kv_it = 0;
-      bool ok = true;
-      for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
-        const AttnUnit u = units[ui];
-        const TileInfo tl = tiles[u.tile];
-        const int n = unit_blocks(u, tl, idx, hkv, topk, list_p, err, true);
-        if (k > 0 && !(ok = mbar_wait(q_empty, (k - 1) & 1, err))) break;
-        mbar_expect_tx(q_full, u.nh * L::kTileBytes);
-        for (int h = 0; h < u.nh; ++h)
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_3d(q_s + h * L::kTileBytes + c * 16384, &q_map, q_full, c * 64, u.h0 + h, tl.q_begin);
-        for (int i = 0; i < n; ++i, ++kv_it) {
-          const int s = kv_it % kStages;
-          if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
-          int64_t page = kv_indices[tl.page_base + list_p[i]];
+    int kv_it = 0;
+    bool ok = true;
+    for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
+      UnitList& ls = lists[k % kListSlots];
+      const AttnUnit u = units[ui];
+      const TileInfo tl = tiles[u.tile];
+      const int32_t* sel = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
+      if (lane == 0) ok = mbar_wait(list_empty + k % kListSlots, ((k / kListSlots) & 1) ^ 1, err);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      __syncwarp();
+      if (!ok) break;
+      // the unit's blocks: padding skipped, entries past the tile's valid
+      // blocks dropped and reported, pages checked against the pool
+      int n = 0;
+      for (int b = 0; b < topk; b += 32) {
+        const int kk = b + lane;
+        const int j = kk < topk ? sel[kk] : -1;
+        const bool valid = j >= 0 && j < tl.nvp;
+        if (j >= tl.nvp) atomicOr(err, kErrDeviceCheck);
+        int row = 0;
+        if (valid) {
+          int64_t page = kv_indices[tl.page_base + j];
           if (page < 0 || page >= num_pages) {
             atomicOr(err, kErrDeviceCheck);
             page = 0;
           }
           // K/V head of the unit's group, or the single head of a one-head pool
-          const int row = static_cast<int>((kOneKvHead ? page : page * hkv + u.g) * 128);
-          mbar_expect_tx(k_full + s, L::kTileBytes);
+          row = static_cast<int>((kOneKvHead ? page : page * hkv + u.g) * 128);
+        }
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, valid);
+        if (valid) {
+          const int o = n + __popc(m & ((1u << lane) - 1u));
+          ls.j[o] = j;
+          ls.row[o] = row;
+        }
+        n += __popc(m);
+      }
+      if (lane == 0) {
+        ls.n = n;
+        ls.nh = u.nh;
+        ls.h0 = u.h0;
+        ls.q_begin = tl.q_begin;
+        ls.rows = tl.rows;
+        ls.pos0 = tl.pos0;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(list_full + k % kListSlots);
+        if (k > 0) ok = mbar_wait(q_empty, (k - 1) & 1, err);
+        if (ok) {
+          mbar_expect_tx(q_full, u.nh * L::kTileBytes);
+          for (int h = 0; h < u.nh; ++h)
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_3d(q_s + h * L::kTileBytes + c * 16384, &q_map, q_full, c * 64, u.h0 + h, tl.q_begin);
+        }
+        for (int i = 0; ok && i < n; ++i, ++kv_it) {
+          const int s = kv_it % kStages;
+          if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
+          const int row = ls.row[i];
+          mbar_expect_tx(kv_full + s, 2 * L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, k_full + s, c * 64, row);
-          mbar_expect_tx(v_full + s, L::kTileBytes);
+            tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, kv_full + s, c * 64, row);
           for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, v_full + s, c * 64, row);
+            tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, kv_full + s, c * 64, row);
         }
       }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     }
   } else if (warp == 9) {
     // --------------------------------------------------------------- MMA
     if (lane == 0) {
+      // The issuing thread runs only a step ahead of the tensor pipe, so
+      // anything between two MMA groups (a wait, a commit, address
+      // arithmetic) idles the pipe: descriptors are precomputed, K and V of
+      // a block share one barrier, O_h's barrier is committed once per unit
+      // (a block's S_h commit already covers the previous P_h.V), and the
+      // per-head phase counters are scalars.
       constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
-      const uint32_t q0 = smem_u32(q_s), k0 = smem_u32(k_s), v0 = smem_u32(v_s);
+      constexpr uint64_t kTileDesc = L::kTileBytes >> 4;
+      const uint64_t qd0 = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128);
+      const uint64_t kd0 = smem_desc(smem_u32(k_s), 16, 1024, kSwizzle128);
+      const uint64_t vd0 = smem_desc(smem_u32(v_s), 16384, 1024, kSwizzle128);
       auto qk = [&](int h, int s) {
+        const uint64_t qd = qd0 + h * kTileDesc, kd = kd0 + s * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + h * 128, smem_desc(q0 + h * L::kTileBytes + off, 16, 1024, kSwizzle128),
-                 smem_desc(k0 + s * L::kTileBytes + off, 16, 1024, kSwizzle128), id_qk, kk > 0);
+          const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          mma_ss(tmem + h * 128, qd + off, kd + off, id_qk, kk > 0);
         }
         mma_commit(s_full + h);
       };
       auto pv = [&](int h, int s, bool acc) {
+        const uint64_t vd = vd0 + s * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(tmem + 256 + h * D, tmem + h * 128 + kk * 8,
-                 smem_desc(v0 + s * L::kTileBytes + kk * 2048, 16384, 1024, kSwizzle128), id_pv, acc || (kk > 0));
-        mma_commit(o_done + h);
+          mma_ts(tmem + 256 + h * D, tmem + h * 128 + kk * 8, vd + ((kk * 2048) >> 4), id_pv, acc || (kk > 0));
       };
-      int kv_it = 0, ch[2] = {0, 0};
+      int kv_it = 0, ch0 = 0, ch1 = 0;
       bool ok = true;
       for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
-        const AttnUnit u = units[ui];
-        const TileInfo tl = tiles[u.tile];
-        const int n = unit_blocks(u, tl, idx, hkv, topk, list_m, err, false);
+        if (!(ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err))) break;
+        const int n = lists[k % kListSlots].n;
+        const bool two = lists[k % kListSlots].nh == 2;
+        mbar_arrive(list_empty + k % kListSlots);
         if (!(ok = mbar_wait(q_full, k & 1, err))) break;
         tc_fence_after();
         if (n == 0) {
           mma_commit(q_empty);
           continue;
         }
-        if (!(ok = mbar_wait(k_full + kv_it % kStages, (kv_it / kStages) & 1, err))) break;
+        if (!(ok = mbar_wait(kv_full + (kv_it & 1), (kv_it >> 1) & 1, err))) break;
         tc_fence_after();
-        for (int h = 0; h < u.nh; ++h) qk(h, kv_it % kStages);
+        qk(0, kv_it & 1);
+        if (two) qk(1, kv_it & 1);
         if (n == 1) mma_commit(q_empty);  // the unit's last QK is issued
-        for (int i = 0; ok && i < n; ++i) {
+        for (int i = 0; i < n; ++i) {
           const int it = kv_it + i;
-          const int s = it % kStages, s1 = (it + 1) % kStages;
-          for (int h = 0; h < u.nh; ++h) {
-            if (!(ok = mbar_wait(p_full + h, (ch[h] + i) & 1, err))) break;
-            if (h == 0 && !(ok = mbar_wait(v_full + s, (it / kStages) & 1, err))) break;
-            // the first P.V of a unit overwrites O_h: the previous unit's
-            // epilogue must have read it (the QKs above already overlap it)
-            if (i == 0 && k > 0 && !(ok = mbar_wait(o_free + h, (k - 1) & 1, err))) break;
+          const int s = it & 1, s1 = s ^ 1;
+          const bool more = i + 1 < n;
+          // head 0: P_0 . V, then S_0 of the next block
+          if (!(ok = mbar_wait(p_full, (ch0 + i) & 1, err))) break;
+          // the first P.V of a unit overwrites O_h: the previous unit's
+          // epilogue must have read it (the QKs above already overlap it)
+          if (i == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, err))) break;
+          tc_fence_after();
+          pv(0, s, i > 0);
+          if (!two) mma_commit(kv_empty + s);
+          if (more) {
+            if (!(ok = mbar_wait(kv_full + s1, ((it + 1) >> 1) & 1, err))) break;
             tc_fence_after();
-            pv(h, s, i > 0);
-            if (h == u.nh - 1) mma_commit(kv_empty + s);
-            if (i + 1 < n) {
-              if (h == 0 && !(ok = mbar_wait(k_full + s1, ((it + 1) / kStages) & 1, err))) break;
-              tc_fence_after();
-              qk(h, s1);
-              if (i + 1 == n - 1 && h == u.nh - 1) mma_commit(q_empty);
-            }
+            qk(0, s1);
+            if (!two && i + 1 == n - 1) mma_commit(q_empty);
+          } else {
+            mma_commit(o_done);
+          }
+          if (!two) continue;
+          // head 1
+          if (!(ok = mbar_wait(p_full + 1, (ch1 + i) & 1, err))) break;
+          if (i == 0 && k > 0 && !(ok = mbar_wait(o_free + 1, (k - 1) & 1, err))) break;
+          tc_fence_after();
+          pv(1, s, i > 0);
+          mma_commit(kv_empty + s);
+          if (more) {
+            qk(1, s1);
+            if (i + 1 == n - 1) mma_commit(q_empty);
+          } else {
+            mma_commit(o_done + 1);
           }
         }
-        for (int h = 0; h < u.nh; ++h) ch[h] += n;
+        ch0 += n;
+        if (two) ch1 += n;
         kv_it += n;
       }
       mma_commit(drain);
@@ -242,18 +296,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + h * 128;
     const uint32_t o_addr = tmem + lane_base + 256 + h * D;
-    int ch = 0;
+    int ch = 0, od = 0;  // blocks and units (with blocks) of head h so far
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
-      const AttnUnit u = units[ui];
-      const TileInfo tl = tiles[u.tile];
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kSoftWarps) : "memory");  // previous list no longer read
-      if (threadIdx.x == 0) *n_soft = unit_blocks(u, tl, idx, hkv, topk, list_s, err, false);
-      asm volatile("bar.sync 2, %0;" ::"n"(32 * kSoftWarps) : "memory");
-      const int n = *n_soft;
-      const bool active = ok && h < u.nh;
-      const bool row_ok = r < tl.rows;
-      const int qpos = tl.pos0 + r;
+      const UnitList& ls = lists[k % kListSlots];
+      if (ok) ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
+      const int rows = ls.rows, pos0 = ls.pos0;
+      const bool active = ok && h < nh;
+      const bool row_ok = r < rows;
+      const int qpos = pos0 + r;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; active && ok && i < n; ++i) {
         if (!(ok = mbar_wait(s_full + h, (ch + i) & 1, err))) break;
@@ -262,8 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
         tmem_wait_ld();
-        const int j = list_s[i];
-        const bool need_mask = (j * 128 + 127 > tl.pos0) || (tl.rows < 128);
+        const int j = ls.j[i];
+        const bool need_mask = (j * 128 + 127 > pos0) || (rows < 128);
         if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
           const int limit = row_ok ? qpos - j * 128 : -1;
 #pragma unroll
@@ -309,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         l = l * alpha + (sum0 + sum1);
         // rescale O_h (written by P.V of the previous block, already complete
         // because the S_h MMA of this block was issued after it)
+        // (P_h.V of the previous block is complete: the MMA thread issued
+        // this block's S_h after it, and s_full covers every earlier MMA)
         if (i > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-          if (!(ok = mbar_wait(o_done + h, (ch + i - 1) & 1, err))) break;
-          tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -329,9 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = m_new;
       }
       if (active && ok) {
-        if (n > 0) ok = mbar_wait(o_done + h, (ch + n - 1) & 1, err);
+        if (n > 0) ok = mbar_wait(o_done + h, (od++) & 1, err);
         tc_fence_after();
-        const int64_t orow = static_cast<int64_t>(tl.q_begin + r) * hq + u.h0 + h;
+        const int64_t orow = static_cast<int64_t>(ls.q_begin + r) * hq + ls.h0 + h;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -359,11 +412,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && row_ok && lse != nullptr)
           lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (h < u.nh) ch += n;
-      // O_h may be overwritten by the next unit (every warp arrives, active or not)
+      if (h < nh) ch += n;
+      // O_h may be overwritten by the next unit, and the list slot refilled
+      // (every warp arrives, active or not)
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free + h);
+      if (lane == 0) {
+        mbar_arrive(o_free + h);
+        mbar_arrive(list_empty + k % kListSlots);
+      }
     }
   }
   tc_fence_before();

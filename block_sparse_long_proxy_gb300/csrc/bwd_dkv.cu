@@ -237,8 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T, Sp^T
       constexpr uint32_t id_d = idesc_bf16_f32(128, 128, false, true);   // dV, dK (B rows-major)
       constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpk
-      const uint32_t v0 = smem_u32(v_s), pk0 = smem_u32(pk_s);
-      const uint32_t qd0 = smem_u32(qd_s), pq0 = smem_u32(pq_s);
+      // descriptors precomputed (one add per MMA): the issuing thread runs
+      // only a step ahead of the tensor pipe
+      constexpr uint64_t kQdDesc = L::kQdBytes >> 4;
+      const uint64_t v_km = smem_desc(smem_u32(v_s), 16, 1024, kSwizzle128);
+      const uint64_t pk_km = smem_desc(smem_u32(pk_s), 16, 1024, kSwizzle128);
+      const uint64_t q_km = smem_desc(smem_u32(qd_s), 16, 1024, kSwizzle128);         // Q half (S^T = K Q^T)
+      const uint64_t do_km = smem_desc(smem_u32(qd_s) + 16384, 16, 1024, kSwizzle128); // dO half (dP^T = V dO^T)
+      const uint64_t q_mn = smem_desc(smem_u32(qd_s), 8192, 1024, kSwizzle128);       // Q as rows-major B (dK)
+      const uint64_t do_mn = smem_desc(smem_u32(qd_s) + 16384, 8192, 1024, kSwizzle128);
+      const uint64_t pq_km = smem_desc(smem_u32(pq_s), 16, 1024, kSwizzle128);
+      const uint64_t pq_mn = smem_desc(smem_u32(pq_s), 8192, 1024, kSwizzle128);
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(init_done, 0, err);
       tc_fence_after();
       int qi = 0, pi = 0;
@@ -247,26 +256,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int halves = tl.rows > 64 ? 2 : 1;
         for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
           const int ps = pi % kPqStages;
-          const uint32_t pqa = pq0 + ps * 8192;
+          const uint64_t po = static_cast<uint64_t>(ps) * (8192 >> 4);
           if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
           tc_fence_after();
 #pragma unroll
-          for (int kk = 0; kk < kDP / 16; ++kk)
-            mma_ss(tmem + kColS, smem_desc(pk0 + kk * 32, 16, 1024, kSwizzle128),
-                   smem_desc(pqa + kk * 32, 16, 1024, kSwizzle128), id_s, kk > 0);
+          for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
           mma_commit(sp_full);
           for (int hh = 0; ok && hh < G; ++hh, ++qi) {
             const int s = qi % kQStages;
-            const uint32_t qa = qd0 + s * L::kQdBytes, da = qa + 16384;
+            const uint64_t so = static_cast<uint64_t>(s) * kQdDesc;
             if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
             tc_fence_after();
             auto dpt = [&]() {  // dP^T = V . dO^T
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t oa = (kk / 4) * 16384 + (kk % 4) * 32, ob = (kk / 4) * 8192 + (kk % 4) * 32;
-                mma_ss(tmem + kColDP, smem_desc(v0 + oa, 16, 1024, kSwizzle128),
-                       smem_desc(da + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
-              }
+              for (int kk = 0; kk < kD / 16; ++kk)
+                mma_ss(tmem + kColDP, v_km + (((kk / 4) * 16384 + (kk % 4) * 32) >> 4),
+                       do_km + so + (((kk / 4) * 8192 + (kk % 4) * 32) >> 4), id_s, kk > 0);
               mma_commit(dp_full);
             };
             if (hh == 0) {  // dP^T of the first head overlaps the proxy softmax
@@ -275,14 +280,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk),
-                       smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128), id_p, 1);
+                mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
             }
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint32_t ob = (kk / 4) * 8192 + (kk % 4) * 32;
-              mma_ts(tmem + kColS, tmem + kColK + kk * 8, smem_desc(qa + ob, 16, 1024, kSwizzle128), id_s, kk > 0);
-            }
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ts(tmem + kColS, tmem + kColK + kk * 8, q_km + so + (((kk / 4) * 8192 + (kk % 4) * 32) >> 4), id_s,
+                     kk > 0);
             mma_commit(s_full);
             if (hh > 0) dpt();  // the softmax starts on S^T while dP^T runs
             // dV and dpk need only P^T; dK waits for dS^T
@@ -290,17 +293,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), smem_desc(da + kk * 2048, 8192, 1024, kSwizzle128),
-                     id_d, 1);
-              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), smem_desc(pqa + kk * 2048, 8192, 1024, kSwizzle128),
-                     id_p, 1);
+              mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), do_mn + so + kk * 128, id_d, 1);
+              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
             }
             if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), smem_desc(qa + kk * 2048, 8192, 1024, kSwizzle128),
-                     id_d, 1);
+              mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), q_mn + so + kk * 128, id_d, 1);
             mma_commit(qd_empty + s);
           }
           if (!ok) break;

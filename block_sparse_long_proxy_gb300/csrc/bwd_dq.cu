@@ -136,26 +136,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // S, dP
       constexpr uint32_t id_q = idesc_bf16_f32(128, 128, false, true);   // dQ (B keys-major)
       constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpq
-      const uint32_t d0 = smem_u32(do_s), r0 = smem_u32(ring);
+      // descriptors precomputed (one add per MMA): the issuing thread runs
+      // only a step ahead of the tensor pipe
+      constexpr uint64_t kStageDesc = L::kStageBytes >> 4;
+      const uint32_t r0 = smem_u32(ring);
+      const uint64_t k_km = smem_desc(r0, 16, 1024, kSwizzle128);             // K, keys x d (S = Q K^T)
+      const uint64_t v_km = smem_desc(r0 + 32768, 16, 1024, kSwizzle128);     // V (dP = dO V^T)
+      const uint64_t k_mn = smem_desc(r0, 16384, 1024, kSwizzle128);          // K as keys-major B (dQ += dS K)
+      const uint64_t pk_mn = smem_desc(r0 + 65536, 16384, 1024, kSwizzle128); // pk (dpq += P pk)
+      const uint64_t do_km = smem_desc(smem_u32(do_s), 16, 1024, kSwizzle128);
       bool ok = mbar_wait(q_full, 0, err) && mbar_wait(q_tm, 0, err);
       tc_fence_after();
       int it = 0;
       for (int k = 0; ok && k < topk; ++k) {
         if (!valid_block(row_idx[k], tl.nvp)) continue;
         const int s = it % kStages;
-        const uint32_t ka = r0 + s * L::kStageBytes, va = ka + 32768, pa = ka + 65536;
+        const uint64_t so = static_cast<uint64_t>(s) * kStageDesc;
         if (!(ok = mbar_wait(kv_full + s, (it / kStages) & 1, err))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ts(tmem + kColS, tmem + kColQ + kk * 8, smem_desc(ka + off, 16, 1024, kSwizzle128), id_s, kk > 0);
+          const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          mma_ts(tmem + kColS, tmem + kColQ + kk * 8, k_km + so + off, id_s, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_ss(tmem + kColDP, smem_desc(d0 + off, 16, 1024, kSwizzle128),
-                 smem_desc(va + off, 16, 1024, kSwizzle128), id_s, kk > 0);
+          const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          mma_ss(tmem + kColDP, do_km + off, v_km + so + off, id_s, kk > 0);
         }
         mma_commit(s_full);
         if (!(ok = mbar_wait(p_full, it & 1, err))) break;
@@ -163,10 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
-          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, smem_desc(ka + kk * 2048, 16384, 1024, kSwizzle128), id_q,
-                 it > 0 || kk > 0);
-          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, smem_desc(pa + kk * 2048, 16384, 1024, kSwizzle128), id_p,
-                 it > 0 || kk > 0);
+          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
+          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + so + kk * 128, id_p, it > 0 || kk > 0);
         }
         mma_commit(kv_empty + s);
         ++it;

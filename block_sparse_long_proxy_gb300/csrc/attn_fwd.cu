@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
       const int rows = ls.rows, pos0 = ls.pos0;
       const bool active = ok && h < nh;
+      bool o_released = false;
       const bool row_ok = r < rows;
       const int qpos = pos0 + r;
       float m = -INFINITY, l = 0.f;
@@ -386,27 +387,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int64_t orow = static_cast<int64_t>(ls.q_begin + r) * hq + ls.h0 + h;
         const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        // all of O_h in one round of loads; O_h is then released to the next
+        // unit's P.V before the stores
+        uint32_t ov[D];
+        if (n > 0) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          if (n > 0) {
-            tmem_ld32(o_addr + c * 32, ov);
-            tmem_wait_ld();
-          } else {
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(o_addr + c * 32, ov + c * 32);
+          tmem_wait_ld();
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = 0u;
-          }
-          if (ok && row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(out + orow * D + c * 32);
+          for (int e = 0; e < D; ++e) ov[e] = 0u;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free + h);
+        o_released = true;
+        if (ok && row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(out + orow * D);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
-              dst[e] = w;
-            }
+          for (int e = 0; e < D / 8; ++e) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
+            dst[e] = w;
           }
         }
         if (ok && row_ok && lse != nullptr)
@@ -414,11 +419,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (h < nh) ch += n;
       // O_h may be overwritten by the next unit, and the list slot refilled
-      // (every warp arrives, active or not)
+      // (every warp arrives once per unit, active or not)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(o_free + h);
+        if (!o_released) mbar_arrive(o_free + h);
         mbar_arrive(list_empty + k % kListSlots);
       }
     }

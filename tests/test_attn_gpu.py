@@ -41,6 +41,46 @@ def test_sparse_attn_random_indexes(cuda_dev, case):
     assert np.abs(lg[fin] - lse_ref[fin]).max() <= 1e-3
 
 
+IRREGULAR = [
+    # more selected blocks than one 32-lane pass of the unit-list builder
+    synth.Case("topk 36 over 40 blocks", [5120], [5120], 2, 1, 128, 1, 64, 36, page_perm_seed=2),
+    synth.Case("shuffled and empty rows", [1024, 700, 300], [1024, 900, 300], 8, 2, 128, 2, 64, 6,
+               page_perm_seed=4),
+]
+
+
+def irregular_idx(case, rng):
+    """Selections in random order with the -1 padding spread through the row,
+    and every fifth (tile, group) row empty: its rows get out = 0, lse = -inf."""
+    idx = random_idx(case, rng)
+    nt, hkv, _ = idx.shape
+    for t in range(nt):
+        for g in range(hkv):
+            idx[t, g] = idx[t, g][rng.permutation(case.topk)]
+            if (t * hkv + g) % 5 == 3:
+                idx[t, g] = -1
+    return idx
+
+
+@pytest.mark.parametrize("case", IRREGULAR, ids=lambda c: c.name)
+def test_sparse_attn_irregular_indexes(cuda_dev, case):
+    inp = synth.make_inputs(case, device=cuda_dev)
+    idx = irregular_idx(case, np.random.default_rng(9))
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"],
+                                torch.from_numpy(idx).to(cuda_dev))
+    torch.cuda.synchronize()
+    plan.check_errors()
+    o_ref, lse_ref = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                                        inp["kv_indices"].cpu().numpy(), idx, case.qo_lens, case.kv_lens)
+    compare_out(out.float().cpu().numpy(), o_ref, O_ATOL_BF16)
+    lg = lse.cpu().numpy()
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    assert np.isneginf(lse_ref).any()  # the empty rows are in the case
+    fin = np.isfinite(lse_ref)
+    assert np.abs(lg[fin] - lse_ref[fin]).max() <= 1e-3
+
+
 @pytest.mark.parametrize("case", [synth.tiny(),
                                   synth.Case("varlen planted small", [1024, 2048, 640], [1024, 2048, 900],
                                              8, 2, 128, 2, 64, 4, page_perm_seed=1, planted=True)],

@@ -59,36 +59,40 @@ __global__ void __launch_bounds__(kThreads)
                     float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t total_q, float kl_weight) {
   const int t = blockIdx.x / hkv, g = blockIdx.x % hkv;
   const TileInfo tl = tiles[t];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   const int G = hq / hkv;
 
-  // D = rowsum(dout * out): two lanes per row, 64 d values each
-  for (int h = g * G; h < (g + 1) * G; ++h)
-    for (int r = warp * 16 + (lane >> 1); r < 128; r += 128) {
-      float acc = 0.f;
-      if (r < tl.rows) {
-        const int64_t off = (static_cast<int64_t>(tl.q_begin + r) * hq + h) * kD + (lane & 1) * 64;
-        const uint4* a = reinterpret_cast<const uint4*>(out + off);
-        const uint4* b = reinterpret_cast<const uint4*>(dout + off);
+  // D = rowsum(dout * out): eight lanes per (row, head), 16 d values each,
+  // so that every thread has its few loads in flight at once and the block's
+  // 256 threads cover 32 rows per pass
+  static_assert(kThreads % 8 == 0 && 128 % (kThreads / 8) == 0, "row passes");
+  const int sub = lane & 7;
+  for (int e = threadIdx.x >> 3; e < G * 128; e += kThreads / 8) {
+    const int h = g * G + e / 128, r = e % 128;
+    float acc = 0.f;
+    if (r < tl.rows) {
+      const int64_t off = (static_cast<int64_t>(tl.q_begin + r) * hq + h) * kD + sub * 16;
+      const uint4* a = reinterpret_cast<const uint4*>(out + off);
+      const uint4* b = reinterpret_cast<const uint4*>(dout + off);
+      const uint4 x0 = a[0], x1 = a[1], y0 = b[0], y1 = b[1];
+      const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+      const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint4 x = a[c], y = b[c];
-          const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[e]));
-            const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[e]));
-            acc += fx.x * fy.x + fx.y * fy.y;
-          }
-        }
-      }
-      acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
-      if ((lane & 1) == 0 && r < tl.rows) {
-        const int64_t q_row = tl.q_begin + r;
-        dsumt[static_cast<int64_t>(h) * total_q + q_row] = acc;
-        lse2t[static_cast<int64_t>(h) * total_q + q_row] = lse[q_row * hq + h] * kLog2e;
+      for (int c = 0; c < 8; ++c) {
+        const float2 fx = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xs[c]));
+        const float2 fy = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ys[c]));
+        acc += fx.x * fy.x + fx.y * fy.y;
       }
     }
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
+    if (sub == 0 && r < tl.rows) {
+      const int64_t q_row = tl.q_begin + r;
+      dsumt[static_cast<int64_t>(h) * total_q + q_row] = acc;
+      lse2t[static_cast<int64_t>(h) * total_q + q_row] = lse[q_row * hq + h] * kLog2e;
+    }
+  }
 
   // proxy LSE in log2 units, and dpq's proxy term
   const float f = kl_weight * rsqrtf(static_cast<float>(kDP));

@@ -262,33 +262,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
           mma_commit(sp_full);
-          for (int hh = 0; ok && hh < G; ++hh, ++qi) {
-            const int s = qi % kQStages;
-            const uint64_t so = static_cast<uint64_t>(s) * kQdDesc;
-            if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
-            tc_fence_after();
-            auto dpt = [&]() {  // dP^T = V . dO^T
+          auto dpt = [&](uint64_t so) {  // dP^T = V . dO^T
 #pragma unroll
-              for (int kk = 0; kk < kD / 16; ++kk)
-                mma_ss(tmem + kColDP, v_km + (((kk / 4) * 16384 + (kk % 4) * 32) >> 4),
-                       do_km + so + (((kk / 4) * 8192 + (kk % 4) * 32) >> 4), id_s, kk > 0);
-              mma_commit(dp_full);
-            };
-            if (hh == 0) {  // dP^T of the first head overlaps the proxy softmax
-              dpt();
-              if (!(ok = mbar_wait(pp_full, pi & 1, err))) break;
-              tc_fence_after();
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
-            }
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss(tmem + kColDP, v_km + (((kk / 4) * 16384 + (kk % 4) * 32) >> 4),
+                     do_km + so + (((kk / 4) * 8192 + (kk % 4) * 32) >> 4), id_s, kk > 0);
+            mma_commit(dp_full);
+          };
+          auto st = [&](uint64_t so) {  // S^T = K . Q^T (K from tensor memory)
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
               mma_ts(tmem + kColS, tmem + kColK + kk * 8, q_km + so + (((kk / 4) * 8192 + (kk % 4) * 32) >> 4), id_s,
                      kk > 0);
             mma_commit(s_full);
-            if (hh > 0) dpt();  // the softmax starts on S^T while dP^T runs
-            // dV and dpk need only P^T; dK waits for dS^T
+          };
+          // head 0: dP^T overlaps the proxy softmax, then the proxy term of
+          // dpk reads -G Pp^T from the S^T columns before S^T overwrites them
+          {
+            const int s = qi % kQStages;
+            const uint64_t so = static_cast<uint64_t>(s) * kQdDesc;
+            if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
+            tc_fence_after();
+            dpt(so);
+            if (!(ok = mbar_wait(pp_full, pi & 1, err))) break;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
+            st(so);
+          }
+          // heads pipelined: S^T of head h+1 is issued as soon as dV, dpk of
+          // head h have taken P^T out of its columns, so the softmax of h+1
+          // can start right after dS^T of h; dP^T of h+1 follows dK of h,
+          // which takes dS^T out of the dP^T columns
+          for (int hh = 0; ok && hh < G; ++hh, ++qi) {
+            const int s = qi % kQStages;
+            const uint64_t so = static_cast<uint64_t>(s) * kQdDesc;
             if (!(ok = mbar_wait(p_full, qi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
@@ -296,12 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1)
               mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), do_mn + so + kk * 128, id_d, 1);
               mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
             }
+            const bool next = hh + 1 < G;
+            const int s1 = (qi + 1) % kQStages;
+            const uint64_t so1 = static_cast<uint64_t>(s1) * kQdDesc;
+            if (next) {
+              if (!(ok = mbar_wait(qd_full + s1, ((qi + 1) / kQStages) & 1, err))) break;
+              tc_fence_after();
+              st(so1);
+            }
             if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), q_mn + so + kk * 128, id_d, 1);
             mma_commit(qd_empty + s);
+            if (next) dpt(so1);
           }
           if (!ok) break;
           mma_commit(pq_empty + ps);

@@ -250,18 +250,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pq_mn = smem_desc(smem_u32(pq_s), 8192, 1024, kSwizzle128);
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(init_done, 0, err);
       tc_fence_after();
+      // Sp^T = pk . pq^T of half p, in the S^T columns
+      auto sp = [&](int p) -> bool {
+        const int ps = p % kPqStages;
+        const uint64_t po = static_cast<uint64_t>(ps) * (8192 >> 4);
+        if (!mbar_wait(pq_full + ps, (p / kPqStages) & 1, err)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
+        mma_commit(sp_full);
+        return true;
+      };
       int qi = 0, pi = 0;
+      bool sp_issued = false;  // the current half's Sp^T went out with the previous half's last head
       for (int it = 0; ok && it < n; ++it) {
         const TileInfo tl = tiles[tile_at(it)];
         const int halves = tl.rows > 64 ? 2 : 1;
         for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
           const int ps = pi % kPqStages;
           const uint64_t po = static_cast<uint64_t>(ps) * (8192 >> 4);
-          if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
-          mma_commit(sp_full);
+          const bool more_halves = hf + 1 < halves || it + 1 < n;
+          if (!sp_issued && !(ok = sp(pi))) break;
+          sp_issued = false;
           auto dpt = [&](uint64_t so) {  // dP^T = V . dO^T
 #pragma unroll
             for (int kk = 0; kk < kD / 16; ++kk)
@@ -312,6 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait(qd_full + s1, ((qi + 1) / kQStages) & 1, err))) break;
               tc_fence_after();
               st(so1);
+            } else if (more_halves) {  // the next half's proxy scores, so its proxy softmax follows dS^T at once
+              if (!(ok = sp(pi + 1))) break;
+              sp_issued = true;
             }
             if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
             tc_fence_after();

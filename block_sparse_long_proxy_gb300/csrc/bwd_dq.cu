@@ -8,9 +8,11 @@
 //   S  = Q_h . K_j^T (Q from TMEM)   dP = dO_h . V_j^T        (M = rows, N = 128 keys)
 //   P  = exp2(S sl2 - lse2) (masked)   dS = P * (dP - D)
 //   dQ += dS . K_j       dpq += P . pk_j                     (dS, P from TMEM)
-// The products are bound by shared-memory operand reads, so they use the
-// widest N and take Q from tensor memory; the softmax of a block runs
-// between its products (its two warpgroups split the 128 keys).
+// The products use N = 128 and take Q from tensor memory.  Blocks are
+// pipelined through split handoffs: the softmax hands P over before dS, and
+// the MMA thread issues S of block j+1 right after dpq of block j and dP of
+// j+1 right after dQ of j, so the tensor pipe has work while the softmax
+// runs (its two warpgroups split the 128 keys).
 // At the end dQ / sqrt(d) is stored and dpq * (-w / (G sqrt(dp))) is added
 // with fp32 atomics: the G heads of a group add into the same dpq row, whose
 // proxy term the prep kernel stored first.
@@ -71,9 +73,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_tm = bars + 1;                 // Q copied into tensor memory
   uint64_t* kv_full = bars + 2;              // [kStages]
   uint64_t* kv_empty = kv_full + kStages;    // [kStages]
-  uint64_t* s_full = kv_empty + kStages;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* done = p_full + 1;
+  uint64_t* s_full = kv_empty + kStages;   // S computed
+  uint64_t* p_full = s_full + 1;           // P written (bf16, over S)
+  uint64_t* dp_full = p_full + 1;          // dP computed
+  uint64_t* ds_full = dp_full + 1;         // dS written (bf16, over dP)
+  uint64_t* done = ds_full + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,6 +95,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, kSoftWarps);
+    mbar_init(dp_full, 1);
+    mbar_init(ds_full, kSoftWarps);
     mbar_init(done, 1);
     fence_mbar_init();
   }
@@ -147,34 +153,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_km = smem_desc(smem_u32(do_s), 16, 1024, kSwizzle128);
       bool ok = mbar_wait(q_full, 0, err) && mbar_wait(q_tm, 0, err);
       tc_fence_after();
-      int it = 0;
-      for (int k = 0; ok && k < topk; ++k) {
-        if (!valid_block(row_idx[k], tl.nvp)) continue;
-        const int s = it % kStages;
-        const uint64_t so = static_cast<uint64_t>(s) * kStageDesc;
-        if (!(ok = mbar_wait(kv_full + s, (it / kStages) & 1, err))) break;
-        tc_fence_after();
+      int nb = 0;  // cached blocks of the tile
+      for (int k = 0; k < topk; ++k) nb += valid_block(row_idx[k], tl.nvp) ? 1 : 0;
+      auto sq = [&](uint64_t so) {  // S = Q . K^T (Q from tensor memory)
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
           mma_ts(tmem + kColS, tmem + kColQ + kk * 8, k_km + so + off, id_s, kk > 0);
         }
+        mma_commit(s_full);
+      };
+      auto dp = [&](uint64_t so) {  // dP = dO . V^T
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
           mma_ss(tmem + kColDP, do_km + off, v_km + so + off, id_s, kk > 0);
         }
-        mma_commit(s_full);
+        mma_commit(dp_full);
+      };
+      // Blocks are pipelined: S of block i+1 goes out as soon as dpq of block
+      // i has taken P out of the S columns, and dP of i+1 as soon as dQ of i
+      // has taken dS out of the dP columns, so the softmax computes P of i+1
+      // while dQ of i runs and dS of i+1 while dpq of i+1 runs.
+      if (nb > 0) {
+        if ((ok = ok && mbar_wait(kv_full, 0, err))) {
+          tc_fence_after();
+          sq(0);
+          dp(0);
+        }
+      }
+      for (int it = 0; ok && it < nb; ++it) {
+        const int s = it % kStages, s1 = (it + 1) % kStages;
+        const uint64_t so = static_cast<uint64_t>(s) * kStageDesc, so1 = static_cast<uint64_t>(s1) * kStageDesc;
+        const bool next = it + 1 < nb;
         if (!(ok = mbar_wait(p_full, it & 1, err))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
-          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
           mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + so + kk * 128, id_p, it > 0 || kk > 0);
         }
+        if (next) {
+          if (!(ok = mbar_wait(kv_full + s1, ((it + 1) / kStages) & 1, err))) break;
+          tc_fence_after();
+          sq(so1);
+        }
+        if (!(ok = mbar_wait(ds_full, it & 1, err))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;
+          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
+        }
         mma_commit(kv_empty + s);
-        ++it;
+        if (next) dp(so1);
       }
       mma_commit(done);
     }
@@ -217,41 +249,58 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int kbase = j * 128 + kc0;
       const bool need_mask = j * 128 + 127 > tl.pos0 || tl.rows < 128;  // diagonal block or ragged tile
+      // P first (dpq needs only P; dP may still be running), then dS
+      float pr[64];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {  // 32 keys at a time; packed pairs land in columns already read
-        uint32_t sv[32], dv_[32], pa[16], da[16];
+        uint32_t sv[32], pa[16];
         tmem_ld32(lane_base + kColS + kc0 + 32 * c, sv);
-        tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
         tmem_wait_ld();
         if (!need_mask) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
-            float x0, x1, t0, t1, d0, d1;
+            float x0, x1;
             ffma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, -l2);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            fadd2v(t0, t1, __uint_as_float(dv_[i]), __uint_as_float(dv_[i + 1]), -dd, -dd);
-            fmul2(d0, d1, t0, t1, p0, p1);
-            pa[i >> 1] = pack_bf16x2(p0, p1);
-            da[i >> 1] = pack_bf16x2(d0, d1);
+            pr[32 * c + i] = ex2_approx(x0);
+            pr[32 * c + i + 1] = ex2_approx(x1);
+            pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
           }
         } else {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) {
             const int kp = kbase + 32 * c + i;
             const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
-            const float p0 = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
-            const float p1 = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
-            pa[i >> 1] = pack_bf16x2(p0, p1);
-            da[i >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv_[i]) - dd), p1 * (__uint_as_float(dv_[i + 1]) - dd));
+            pr[32 * c + i] = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
+            pr[32 * c + i + 1] = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
+            pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
           }
         }
         tmem_st16(lane_base + kColS + kc0 + 16 * c, pa);
-        tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
+      if (!(ok = mbar_wait(dp_full, it & 1, err))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t dv_[32], da[16];
+        tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float t0, t1, d0, d1;
+          fadd2v(t0, t1, __uint_as_float(dv_[i]), __uint_as_float(dv_[i + 1]), -dd, -dd);
+          fmul2(d0, d1, t0, t1, pr[32 * c + i], pr[32 * c + i + 1]);
+          da[i >> 1] = pack_bf16x2(d0, d1);
+        }
+        tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
       ++it;
     }
     if (ok) ok = mbar_wait(done, 0, err);

@@ -7,18 +7,25 @@
 // kv_indices, kv_block_indexes); Flash-MSA article, "three key
 // differences": the main attention is GQA).
 //
-// One CTA per (tile, GQA group, pair of query heads of the group): both heads
-// share every K/V block the TMA producer gathers through the page table.
-// Tensor memory holds S0, S1 (128 columns each) and O0, O1 (d columns each);
-// the bf16 probabilities P_h overwrite the first 64 columns of S_h and feed
-// the P.V MMA straight from tensor memory.  Roles:
+// A work unit is (tile, GQA group, pair of query heads of the group): both
+// heads share every K/V block the TMA producer gathers through the page
+// table.  Tensor memory holds S0, S1 (128 columns each) and O0, O1 (d
+// columns each); the bf16 probabilities P_h overwrite the first 64 columns
+// of S_h and feed the P.V MMA straight from tensor memory.  Roles:
 //   warps 0-3  softmax of head 0 (thread = query row), warps 4-7 head 1,
-//   warp 8     TMA producer (Q once, then K/V blocks in a 2-stage ring),
+//   warp 8     producer: builds each unit's block list (top-k row and page
+//              rows, all 32 lanes at once) into a two-slot ring, loads Q per
+//              unit and the K/V blocks into a 2-stage ring (one barrier per
+//              stage for K and V),
 //   warp 9     MMA issuer: S_h = Q_h K^T (smem x smem), O_h += P_h V
 //              (tmem x smem), ordered QK0 QK1 | PV0 QK0' PV1 QK1' | ... so
 //              that one head's softmax overlaps the other head's MMAs.
+// The issuing thread runs only about one MMA ahead of the tensor pipe, so
+// its loop does nothing between MMA groups that it can avoid: three waits
+// and three commits per block step, descriptors precomputed.
 // Online softmax in the log2 domain; the O rescale runs in the softmax
-// warps between P.V steps.
+// warps between P.V steps, and the epilogue releases O_h to the next unit
+// as soon as it is in registers.
 #include "msa_internal.h"
 #include "ptx.cuh"
 

@@ -167,7 +167,8 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   attn_plan_tables(p, aux);
   bwd_plan_tables(p, aux);
 
-  // device block: tiles | nvp | error word | aux tables | decode partials
+  // device block: tiles | nvp | error word | aux tables | decode partials |
+  // backward scratch | fused top-k counters and candidates
   const size_t tiles_bytes = sizeof(TileInfo) * p->n_tiles;
   const size_t nvp_off = (tiles_bytes + 255) & ~size_t(255);
   const size_t err_off = nvp_off + ((sizeof(int32_t) * p->n_tiles + 255) & ~size_t(255));
@@ -175,7 +176,8 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   const size_t part_off = aux_off + ((sizeof(int32_t) * aux.size() + 255) & ~size_t(255));
   const size_t part_bytes = (sizeof(float) * decode_partial_floats(p) + 255) & ~size_t(255);
   const size_t bwd_off = part_off + part_bytes;
-  const size_t total = bwd_off + bwd_scratch_bytes(p);
+  const size_t fz_off = bwd_off + ((bwd_scratch_bytes(p) + 255) & ~size_t(255));
+  const size_t total = fz_off + fused_topk_scratch_bytes(p);
   if (cudaMalloc(&p->dev_block, total) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -188,6 +190,7 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   p->aux_d = reinterpret_cast<int32_t*>(base + aux_off);
   p->partial_d = part_bytes ? reinterpret_cast<float*>(base + part_off) : nullptr;
   p->bwd_d = bwd_scratch_bytes(p) ? base + bwd_off : nullptr;
+  p->fused_topk_d = fused_topk_scratch_bytes(p) ? base + fz_off : nullptr;
 
   std::vector<char> host(part_off, 0);
   memcpy(host.data(), p->tiles.data(), tiles_bytes);
@@ -199,6 +202,8 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
                             "msa_plan: upload");
   if (s == MSA_OK && part_bytes)  // decode partials and per-row counters start at zero
     s = cuda_check(cudaMemsetAsync(base + part_off, 0, part_bytes, st), "msa_plan: clear decode workspace");
+  if (s == MSA_OK && p->fused_topk_d)  // the fused top-k's row counters start at zero
+    s = cuda_check(cudaMemsetAsync(p->fused_topk_d, 0, fused_topk_counter_bytes(p), st), "msa_plan: clear counters");
   if (s == MSA_OK) s = cuda_check(cudaStreamSynchronize(st), "msa_plan: upload sync");
   if (s != MSA_OK) {
     cudaFree(p->dev_block);
@@ -241,6 +246,16 @@ msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* p
     return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore_fp8: FP8 proxy K is implemented for decode batches only");
   return launch_proxy_decode_fp8(plan, pq, pk_pages, pk_scale, kv_indices, max_score,
                                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                          float* max_score, int32_t* kv_block_indexes, msa_stream_t stream) {
+  if (!plan || !pq || !pk_pages || !kv_indices || !kv_block_indexes)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_topk: NULL argument");
+  if (!aligned16(pq) || !aligned16(pk_pages))
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_topk: pq and pk_pages must be 16-byte aligned");
+  return launch_proxy_topk(plan, pq, pk_pages, kv_indices, max_score, kv_block_indexes,
+                           reinterpret_cast<cudaStream_t>(stream));
 }
 
 msa_status msa_topk_select(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,

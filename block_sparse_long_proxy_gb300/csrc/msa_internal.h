@@ -34,6 +34,18 @@ static_assert(sizeof(TileInfo) == 32, "TileInfo is uploaded as raw bytes");
 // Bits of the device error word.
 enum : uint32_t { kErrDeviceCheck = 1u, kErrTimeout = 2u };
 
+#ifdef __CUDACC__
+// Order-preserving 32-bit key of a block score for the top-k selection:
+// -0.0 is folded onto +0.0, and -inf maps to 0, which no finite score maps
+// to (0 marks "not a candidate").
+__device__ __forceinline__ uint32_t order_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;                        // -0.0 == +0.0
+  if (u == 0xFF800000u) return 0u;                     // -inf is never a candidate
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // monotone in the float order
+}
+#endif
+
 }  // namespace msa
 
 struct msa_plan_s {
@@ -59,6 +71,9 @@ struct msa_plan_s {
   int64_t proxy_units_off = 0;       // prefill proxy work units
   int32_t n_proxy_units = 0;
   int64_t proxy_unit_start_off = 0;  // decode proxy: first unit of each tile
+  int64_t proxy_chunk_base_off = 0;  // prefill proxy: first 32-block chunk of each tile
+  int32_t proxy_n_chunks = 0;        // sum over tiles of ceil(nvp / 32)
+  void* fused_topk_d = nullptr;      // msa_proxy_topk scratch: per-row counters, chunk candidates
   int64_t attn_units_off = 0;        // prefill attention work units
   int32_t n_attn_units = 0;
   int64_t proxy_attn_units_off = 0;  // backward proxy softmax work units
@@ -78,6 +93,8 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
+size_t fused_topk_scratch_bytes(const msa_plan_s* p);  // 0 when msa_proxy_topk is unsupported
+size_t fused_topk_counter_bytes(const msa_plan_s* p);  // leading part that starts at zero
 // The backward's proxy softmax (attn_fwd.cu): Op = sum_k p_proxy(k) pk[k]
 // (bf16 [total_q, Hp, 64]) and its natural-log LSE ([total_q, Hp]).
 msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
@@ -101,6 +118,9 @@ msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, i
 
 msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages,
                                 const int32_t* kv_indices, float* max_score, cudaStream_t st);
+msa_status launch_proxy_topk(const msa_plan_s* p, const void* pq, const void* pk_pages,
+                             const int32_t* kv_indices, float* max_score, int32_t* kv_block_indexes,
+                             cudaStream_t st);
 msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages,
                                const int32_t* kv_indices, float* max_score, cudaStream_t st);
 // decode proxy scan over e4m3 proxy K pages with one fp32 scale (device pointer)

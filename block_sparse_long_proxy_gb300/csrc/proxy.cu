@@ -48,6 +48,34 @@ __device__ __forceinline__ int32_t f2ord(float f) {
 }
 __device__ __forceinline__ float ord2f(int32_t o) { return __int_as_float(o ^ ((o >> 31) & 0x7FFFFFFF)); }
 
+// The top-k selection fused into the proxy pass (msa_proxy_topk; Flash-MSA
+// article, kernel-design paragraph: the proxy pass keeps a streaming top-k
+// of blocks instead of accumulating outputs).  Each
+// chunk CTA of a (tile, group of 8 proxy heads) leaves, per head, its best
+// topk-1 candidates among the blocks below the diagonal; the last of those
+// CTAs to finish (a counter per row group, no waiting) merges them, adds the
+// diagonal block and writes the ascending, -1 padded index row: the same
+// selection as msa_topk_select on the same scores, since the best topk-1 of
+// a union are among the best topk-1 of its parts.  A candidate is the 64-bit
+// key (order_key(score) << 32) | ~j, so larger is better and ties go to the
+// lower block; 0 is "none".
+struct FusedTopk {
+  int32_t* out;                // kv_block_indexes [n_tiles, hp, topk]; nullptr: max_score only
+  int32_t* counters;           // [n_tiles * n_hgroups], zero between launches
+  unsigned long long* cand;    // [((chunk_base[t] + c) * n_hgroups + hg) * 8 + h][32]
+  const int32_t* chunk_base;   // [n_tiles]
+  int32_t topk, n_hgroups;
+};
+constexpr int kFusedMaxTopk = 32;     // one lane per selected block
+constexpr int kFusedMaxChunks = 32;   // max_blocks <= 1024
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+  const uint32_t hi = static_cast<uint32_t>(v >> 32);
+  const uint32_t mhi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  const uint32_t mlo = __reduce_max_sync(0xFFFFFFFFu, hi == mhi ? static_cast<uint32_t>(v) : 0u);
+  return (static_cast<unsigned long long>(mhi) << 32) | mlo;
+}
+
 template <int DP>
 struct ProxySmem {
   static constexpr int kQBytes = 128 * DP * 2;   // one head's Q tile
@@ -64,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     proxy_prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                          const ProxyUnit* __restrict__ units, const TileInfo* __restrict__ tiles,
                          const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
-                         int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+                         int32_t hp, int32_t max_blocks, float scale, FusedTopk fz, uint32_t* err) {
   using L = ProxySmem<DP>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,10 +249,88 @@ __global__ void __launch_bounds__(kThreads, 1)
         int32_t m = part[(i * kHeadsPerCta + h) * kEpiWarps];
 #pragma unroll
         for (int w = 1; w < 4; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
-        max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = ord2f(m) * scale;
+        const float v = ord2f(m) * scale;
+        if (max_score) max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = v;
+        part[(i * kHeadsPerCta + h) * kEpiWarps + 4] = __float_as_int(v);  // the fused selection reads it
       }
     }
-    if (u.fill_tail) {
+    if (fz.out) {
+      // ---- fused top-k: this chunk's candidates, then the row group's merge
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      const int ew = warp - 2;  // head of the group handled by this warp
+      const bool wok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform: the selections below are warp-collective
+      const int hg = u.h0 / kHeadsPerCta;
+      const int n = tl.nvp < 1 ? 1 : (tl.nvp > max_blocks ? max_blocks : tl.nvp);
+      const int need = fz.topk - 1;
+      const bool all = fz.topk >= n;  // every valid block is selected
+      const int n_chunks = (tl.nvp + kChunk - 1) / kChunk;
+      auto slot = [&](int c, int h) -> int64_t {
+        return ((static_cast<int64_t>(fz.chunk_base[u.tile] + c) * fz.n_hgroups + hg) * kHeadsPerCta + h) * 32;
+      };
+      if (wok && !all && ew < u.nh) {
+        const int j = u.j0 + lane;
+        unsigned long long ck = 0ull;
+        if (lane < nblk && j < n - 1) {
+          const uint32_t key = order_key(__int_as_float(part[(lane * kHeadsPerCta + ew) * kEpiWarps + 4]));
+          if (key) ck = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+        }
+        unsigned long long mine = 0ull;
+        bool taken = false;
+        for (int q = 0; q < need; ++q) {
+          const unsigned long long m = warp_max_u64(taken ? 0ull : ck);
+          if (m == 0ull) break;
+          if (ck == m) taken = true;
+          if (lane == q) mine = m;
+        }
+        if (lane < need) fz.cand[slot(u.j0 / kChunk, ew) + lane] = mine;
+      }
+      // the CTA barrier orders every thread's candidates before thread 0's
+      // release; its acquire (in the last CTA) orders the merge's reads after
+      // every chunk's release
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      if (et == 0) {
+        int32_t* ctr = fz.counters + static_cast<int64_t>(u.tile) * fz.n_hgroups + hg;
+        int32_t prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+        const bool last = prev == n_chunks - 1;
+        if (last) *ctr = 0;  // every chunk of the row group has counted: ready for the next launch
+        part[5] = last;
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      if (part[5] && wok && ew < u.nh) {
+        int32_t* dst = fz.out + (static_cast<int64_t>(u.tile) * hp + u.h0 + ew) * fz.topk;
+        if (all) {
+          if (lane < fz.topk) dst[lane] = lane < n ? lane : -1;
+        } else {
+          // a k-way merge of the chunks' lists, each already best-first:
+          // lane c holds chunk c's list and shifts it as its head is taken
+          unsigned long long v[kFusedMaxTopk - 1];
+#pragma unroll
+          for (int r = 0; r < kFusedMaxTopk - 1; ++r)
+            v[r] = (lane < n_chunks && r < need) ? __ldcg(fz.cand + slot(lane, ew) + r) : 0ull;
+          uint32_t sel = 0xFFFFFFFFu;  // lane q: the q-th best block
+          int found = 0;
+          for (int q = 0; q < need; ++q) {
+            const unsigned long long m = warp_max_u64(v[0]);
+            if (m == 0ull) break;
+            if (v[0] == m) {
+#pragma unroll
+              for (int r = 0; r < kFusedMaxTopk - 2; ++r) v[r] = v[r + 1];
+              v[kFusedMaxTopk - 2] = 0ull;
+            }
+            if (lane == q) sel = 0xFFFFFFFFu - static_cast<uint32_t>(m);
+            ++found;
+          }
+          if (lane == found) sel = static_cast<uint32_t>(n - 1);  // the diagonal block
+          // ascending: each selected block's rank among the selected ones
+          int rank = 0;
+          for (int l = 0; l < 32; ++l) rank += __shfl_sync(0xFFFFFFFFu, sel, l) < sel;
+          if (sel != 0xFFFFFFFFu) dst[rank] = static_cast<int32_t>(sel);
+          if (lane > found && lane < fz.topk) dst[lane] = -1;
+        }
+      }
+    }
+    if (u.fill_tail && max_score) {
       const int tail = max_blocks - tl.nvp;
       for (int it = et; it < tail * u.nh; it += 32 * kEpiWarps) {
         const int h = it / tail, j = tl.nvp + it % tail;
@@ -576,6 +682,14 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   }
   std::stable_sort(us.begin(), us.end(),
                    [](const ProxyUnit& a, const ProxyUnit& b) { return (a.j1 - a.j0) > (b.j1 - b.j0); });
+  // the fused top-k's candidate slots: chunk c of tile t is slot chunk_base[t] + c
+  p->proxy_chunk_base_off = static_cast<int64_t>(aux.size());
+  int32_t chunks = 0;
+  for (int t = 0; t < p->n_tiles; ++t) {
+    aux.push_back(chunks);
+    chunks += (p->tiles[t].nvp + kChunk - 1) / kChunk;
+  }
+  p->proxy_n_chunks = chunks;
   p->proxy_units_off = static_cast<int64_t>(aux.size());
   p->n_proxy_units = static_cast<int32_t>(us.size());
   const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
@@ -597,8 +711,8 @@ static bool make_pk_map(CUtensorMap* m, const msa_plan_s* p, const void* pk_page
   return encode_tensor_map(m, 2, pk_pages, dims, strides, box, 1, p->dp * 2);
 }
 
-msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
-                                float* max_score, cudaStream_t st) {
+static msa_status proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                                float* max_score, const FusedTopk& fz, cudaStream_t st) {
   CUtensorMap qm, km;
   const uint64_t qdims[3] = {static_cast<uint64_t>(p->dp), static_cast<uint64_t>(p->hp),
                              static_cast<uint64_t>(p->total_q)};
@@ -612,14 +726,48 @@ msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void*
     const int smem = ProxySmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     proxy_prefill_kernel<64><<<p->n_proxy_units, kThreads, smem, st>>>(
-        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
+        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   } else {
     const int smem = ProxySmem<32>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     proxy_prefill_kernel<32><<<p->n_proxy_units, kThreads, smem, st>>>(
-        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
+        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: prefill launch");
+}
+
+msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                                float* max_score, cudaStream_t st) {
+  return proxy_prefill(p, pq, pk_pages, kv_indices, max_score, FusedTopk{}, st);
+}
+
+size_t fused_topk_counter_bytes(const msa_plan_s* p) {
+  if (p->decode || p->topk > kFusedMaxTopk || p->max_blocks > kChunk * kFusedMaxChunks) return 0;
+  const int64_t hg = (p->hp + kHeadsPerCta - 1) / kHeadsPerCta;
+  return (sizeof(int32_t) * p->n_tiles * hg + 255) & ~size_t(255);
+}
+
+size_t fused_topk_scratch_bytes(const msa_plan_s* p) {
+  const size_t c = fused_topk_counter_bytes(p);
+  if (c == 0) return 0;
+  const int64_t hg = (p->hp + kHeadsPerCta - 1) / kHeadsPerCta;
+  return c + sizeof(unsigned long long) * static_cast<size_t>(p->proxy_n_chunks) * hg * kHeadsPerCta * 32;
+}
+
+msa_status launch_proxy_topk(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
+                             float* max_score, int32_t* kv_block_indexes, cudaStream_t st) {
+  if (p->decode) return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_topk: prefill plans only");
+  if (!p->fused_topk_d)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_topk: needs topk <= %d and at most %d blocks per sequence",
+                     kFusedMaxTopk, kChunk * kFusedMaxChunks);
+  FusedTopk fz{};
+  fz.out = kv_block_indexes;
+  fz.counters = static_cast<int32_t*>(p->fused_topk_d);
+  fz.cand = reinterpret_cast<unsigned long long*>(static_cast<char*>(p->fused_topk_d) + fused_topk_counter_bytes(p));
+  fz.chunk_base = p->aux_d + p->proxy_chunk_base_off;
+  fz.topk = p->topk;
+  fz.n_hgroups = (p->hp + kHeadsPerCta - 1) / kHeadsPerCta;
+  return proxy_prefill(p, pq, pk_pages, kv_indices, max_score, fz, st);
 }
 
 msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,

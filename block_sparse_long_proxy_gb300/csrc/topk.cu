@@ -22,12 +22,6 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;                        // -0.0 == +0.0
-  if (u == 0xFF800000u) return 0u;                     // -inf is never a candidate
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);   // monotone in the float order
-}
 
 // Keys held in registers: KPL per lane covers rows of up to 32*KPL blocks.
 template <int KPL>

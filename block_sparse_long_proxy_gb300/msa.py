@@ -40,6 +40,7 @@ SIGNATURES = {
     "msa_plan_num_valid_pages": (_p, [_p]),
     "msa_proxy_maxscore": (_i32, [_p, _p, _p, _p, _p, _p]),
     "msa_proxy_maxscore_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _p]),
+    "msa_proxy_topk": (_i32, [_p, _p, _p, _p, _p, _p, _p]),
     "msa_topk_select": (_i32, [_p, _i32, _i32, _i32, _i32, _p, _p, _p]),
     "msa_sparse_attn": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
     "msa_sparse_attn_bwd": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _f32, _p, _p, _p, _p, _p, _p]),
@@ -193,6 +194,22 @@ class Plan:
         _need(out, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
         _check(_lib.msa_proxy_maxscore_fp8(self._h, _ptr(pq), _ptr(pk_pages), _ptr(pk_scale), _ptr(kv_indices),
                                            _ptr(out), _stream(stream)), "msa_proxy_maxscore_fp8")
+        return out
+
+    def proxy_topk(self, pq, pk_pages, kv_indices, out=None, max_score=None, stream=None):
+        """Stages 1 and 2 in one launch (msa_proxy_topk): the kv_block_indexes
+        msa_topk_select would pick from this plan's proxy scores; max_score,
+        when given, receives those scores too."""
+        _need(pq, torch.bfloat16, (self.total_q, self.hp, self.dp), "pq")
+        _need(pk_pages, torch.bfloat16, (self.num_pages, 1, 128, self.dp), "pk_pages")
+        _need(kv_indices, torch.int32, (self.n_page_entries,), "kv_indices")
+        if out is None:
+            out = torch.empty((self.n_tiles, self.hp, self.topk), dtype=torch.int32, device=pq.device)
+        _need(out, torch.int32, (self.n_tiles, self.hp, self.topk), "kv_block_indexes")
+        if max_score is not None:
+            _need(max_score, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
+        _check(_lib.msa_proxy_topk(self._h, _ptr(pq), _ptr(pk_pages), _ptr(kv_indices), _ptr(max_score), _ptr(out),
+                                   _stream(stream)), "msa_proxy_topk")
         return out
 
     # -- stage 3

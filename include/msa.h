@@ -179,6 +179,32 @@ msa_status msa_topk_select(const float* max_score, int32_t n_tiles, int32_t head
                            int32_t* kv_block_indexes, msa_stream_t stream);
 
 /*
+ * msa_proxy_topk -- stages 1 and 2 fused ([FLASH], kernel-design
+ * paragraph: the forward proxy pass keeps a streaming top-k over blocks in
+ * registers instead of accumulating outputs).  The proxy pass and the
+ * selection of msa_proxy_maxscore + msa_topk_select in one launch, with no
+ * max_score round trip.
+ *
+ * Writes the same kv_block_indexes as msa_topk_select(max_score, ...,
+ * plan topk, msa_plan_num_valid_pages(plan), ...) would on the scores that
+ * msa_proxy_maxscore writes: bit-exact, ties to the lower block, ascending,
+ * -1 padded.  The work units of one tile report their candidates and the
+ * last of them merges; nothing waits on another CTA.
+ *
+ *  pq, pk_pages, kv_indices  as for msa_proxy_maxscore.
+ *  max_score         fp32 [num_tiles, Hp, max_blocks] (output) or NULL.
+ *  kv_block_indexes  int32 [num_tiles, Hp, topk] (output).
+ * Prefill plans with topk <= 32 and at most 1024 blocks per sequence;
+ * others return MSA_ERR_UNSUPPORTED (use the two separate calls).  The
+ * plan's counters are reset by every complete launch, so two calls on one
+ * plan must not overlap in time; after a launch that failed with a device
+ * error the plan must be rebuilt.
+ */
+msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages,
+                          const int32_t* kv_indices, float* max_score, int32_t* kv_block_indexes,
+                          msa_stream_t stream);
+
+/*
  * msa_sparse_attn -- stage 3, GQA block-sparse attention forward ([README]
  * "Usage": fmha_sm100(q, k_pages, v_pages, sparse_plan, kv_indices,
  * kv_block_indexes); [STACKS]: paged FP8 decode; [FLASH]: GQA main

@@ -197,11 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = kv_it % kStages;
           if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
           const int row = ls.row[i];
-          mbar_expect_tx(kv_full + s, 2 * L::kTileBytes);
+          // a one-head pool's keys are its values: one load serves both
+          mbar_expect_tx(kv_full + s, (kOneKvHead ? 1 : 2) * L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
             tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, kv_full + s, c * 64, row);
-          for (int c = 0; c < kChunks; ++c)
-            tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, kv_full + s, c * 64, row);
+          if (!kOneKvHead)
+            for (int c = 0; c < kChunks; ++c)
+              tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, kv_full + s, c * 64, row);
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint64_t kTileDesc = L::kTileBytes >> 4;
       const uint64_t qd0 = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128);
       const uint64_t kd0 = smem_desc(smem_u32(k_s), 16, 1024, kSwizzle128);
-      const uint64_t vd0 = smem_desc(smem_u32(v_s), 16384, 1024, kSwizzle128);
+      const uint64_t vd0 = smem_desc(smem_u32(kOneKvHead ? k_s : v_s), 16384, 1024, kSwizzle128);
       auto qk = [&](int h, int s) {
         const uint64_t qd = qd0 + h * kTileDesc, kd = kd0 + s * kTileDesc;
 #pragma unroll

@@ -17,8 +17,12 @@
 //
 // Tensor memory (512 columns): S^T 64 | dP^T 64 | dV 128 | dpk 64 | dK 128 | K 64.
 // K is copied into tensor memory once, so S^T = K . Q^T reads only Q from
-// shared memory (the products are bound by shared-memory operand reads).
-// The softmax warps overwrite S^T (or Sp^T) and dP^T in place with bf16 pairs.
+// shared memory.  The softmax warps overwrite S^T (or Sp^T) and dP^T in
+// place with bf16 pairs, handing P^T over before dS^T.  The MMA stream is
+// pipelined across heads: S^T of head h+1 goes out as soon as dV and dpk of
+// head h have taken P^T out of the S^T columns (the next 64 rows' Sp^T after
+// the last head), dP^T of h+1 right after dK of h, so the softmax of one
+// head overlaps the products of the other.
 // Each warpgroup owns 32 of the 64 rows, and each writes its packed pairs
 // into the first half of its own 32 columns, so a k-step of 16 rows of an
 // A operand in TMEM starts at column (kk / 2) * 32 + (kk % 2) * 8.

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "msa_internal.h"
+#include "ptx.cuh"
 
 namespace msa {
 
@@ -73,6 +74,23 @@ bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* di
 using namespace msa;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+namespace msa {
+namespace {
+// One thread waits on a barrier that nothing arrives on.  The bounded wait
+// gives up after its limit, sets kErrTimeout in the error word and returns,
+// as any kernel's wait would; a completed wait would set the top bit.
+__global__ void selftest_wait_kernel(uint32_t* err) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && mbar_wait(&bar, 0, err)) atomicOr(err, 0x80000000u);
+}
+}  // namespace
+}  // namespace msa
 
 extern "C" {
 
@@ -303,6 +321,27 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
     return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: bf16 K/V only");
   return launch_attn_bwd(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, dout, pq, pk_pages,
                          kl_weight, dq, dk_pages, dv_pages, dpq, dpk_pages, reinterpret_cast<cudaStream_t>(stream));
+}
+
+msa_status msa_selftest_wait_timeout(msa_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t* word_d = nullptr;
+  if (cudaMalloc(&word_d, sizeof(uint32_t)) != cudaSuccess) {
+    cudaGetLastError();
+    return set_error(MSA_ERR_NO_MEMORY, "msa_selftest_wait_timeout: cudaMalloc failed");
+  }
+  msa_status s = cuda_check(cudaMemsetAsync(word_d, 0, sizeof(uint32_t), st), "msa_selftest_wait_timeout: memset");
+  if (s == MSA_OK) {
+    selftest_wait_kernel<<<1, 32, 0, st>>>(word_d);
+    s = cuda_check(cudaGetLastError(), "msa_selftest_wait_timeout: launch");
+  }
+  if (s == MSA_OK) s = cuda_check(cudaStreamSynchronize(st), "msa_selftest_wait_timeout: sync");
+  uint32_t word = 0;
+  if (s == MSA_OK) s = cuda_check(cudaMemcpy(&word, word_d, sizeof(word), cudaMemcpyDeviceToHost), "msa_selftest_wait_timeout: read");
+  cudaFree(word_d);
+  if (s != MSA_OK) return s;
+  if (word == kErrTimeout) return set_error(MSA_ERR_TIMEOUT, "msa_selftest_wait_timeout: the bounded wait gave up (word 0x%x)", word);
+  return set_error(MSA_ERR_CUDA, "msa_selftest_wait_timeout: unexpected error word 0x%x", word);
 }
 
 msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream) {

@@ -47,6 +47,7 @@ SIGNATURES = {
     "msa_sparse_decode_noalloc": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, _i32, _i32, _i64,
                                          _p, _p, _p, _p]),
     "msa_check_errors": (_i32, [_p, _p]),
+    "msa_selftest_wait_timeout": (_i32, [_p]),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_version": (ctypes.c_char_p, []),
 }
@@ -88,6 +89,14 @@ def _need(t, dtype, shape, name):
 
 def version():
     return _lib.msa_version().decode()
+
+
+def selftest_wait_timeout(stream=None):
+    """Runs the device-side failure path once (msa_selftest_wait_timeout): a
+    kernel whose bounded wait cannot complete gives up after its limit.
+    Raises MsaError with status MSA_ERR_TIMEOUT, as a timed-out kernel would
+    through check_errors."""
+    _check(_lib.msa_selftest_wait_timeout(_stream(stream)), "msa_selftest_wait_timeout")
 
 
 def topk_select(max_score, topk, num_valid_pages, out=None, stream=None):

@@ -316,6 +316,17 @@ msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pages, const v
  */
 msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream);
 
+/*
+ * msa_selftest_wait_timeout -- the failure-detection path, on the device:
+ * launches one kernel whose bounded mbarrier wait cannot complete (nothing
+ * arrives on the barrier).  The wait gives up after its 2 s limit, the
+ * kernel records the timeout in an error word and returns, the context stays
+ * usable, and the call reports what msa_check_errors reports for any kernel
+ * whose wait ran out: MSA_ERR_TIMEOUT.  Any other error word gives
+ * MSA_ERR_CUDA.  Synchronises `stream`; allocates and frees 4 bytes.
+ */
+msa_status msa_selftest_wait_timeout(msa_stream_t stream);
+
 /* Message for the calling thread's last failed call ("" if none). */
 const char* msa_last_error(void);
 

@@ -483,3 +483,62 @@ def test_rows_without_visible_keys():
     assert np.all(o[early] == 0.0) and np.all(np.isneginf(lse[early]))
     ref = _dense_route(inp, case, idx)
     np.testing.assert_allclose(o[~early], ref[~early], rtol=1e-10, atol=1e-12)
+
+
+def test_unit_values_give_unit_output():
+    """V == 1: O = sum_k P[k] * 1, so every row with a visible key has O = 1
+    (the rows of P sum to 1) and every row without one has O = 0."""
+    case = synth.Case("ragged", [200, 64, 1], [333, 64, 500], 4, 2, 64, 2, 32, 2, page_perm_seed=1)
+    inp = _mk(case)
+    inp["v_pages"].fill_(1.0)
+    idx = _rand_idx(case, np.random.default_rng(11))
+    # tile 0 (positions 133..260) keeps only its diagonal block 2 (keys 256..):
+    # its rows at positions below 256 see nothing (R7)
+    idx[0, 0, :] = [2, -1]
+    o, lse = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                                inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens)
+    seen = np.isfinite(lse)
+    assert seen.any() and (~seen).any()
+    np.testing.assert_allclose(o[seen], 1.0, rtol=0, atol=1e-12)
+    assert (o[~seen] == 0.0).all()
+
+
+def test_topk_diagonal_always_present():
+    """Every selected row holds the diagonal block num_valid_pages - 1, is
+    ascending, and has min(topk, nvp) entries followed by -1 padding."""
+    rng = np.random.default_rng(17)
+    for topk in (1, 2, 5, 16):
+        nb = 40
+        ms = rng.standard_normal((60, 3, nb)).astype(np.float32)
+        ms[rng.random(ms.shape) < 0.2] = -np.inf
+        nvp = rng.integers(1, nb + 1, 60).astype(np.int32)
+        idx = O.topk_select(ms, topk, nvp)
+        for t in range(60):
+            for h in range(3):
+                row = idx[t, h]
+                n = min(topk, int(nvp[t]))
+                sel = row[row >= 0]
+                assert int(nvp[t]) - 1 in sel
+                assert len(sel) <= n and (row[len(sel):] == -1).all()
+                assert (np.diff(sel) > 0).all()
+
+
+def test_proxy_max_dominates_visible_pairs():
+    """Each block score is at least every visible pair's logit in that block
+    (a sample of pairs, computed here straight from the definition): a mask
+    that drops visible keys, or a wrong pairing of rows and keys, fails."""
+    case = synth.Case("t", [300], [460], 2, 2, 64, 2, 32, 2, page_perm_seed=2)
+    inp = _mk(case)
+    ms = O.proxy_max_score(synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]), inp["kv_indices"].numpy(),
+                           case.qo_lens, case.kv_lens)
+    pq = inp["pq"].double().numpy()
+    pk = inp["pk_pages"].double().numpy()[:, 0]                  # [pages, 128, dp]
+    table = inp["kv_indices"].numpy()
+    off = 460 - 300
+    rng = np.random.default_rng(5)
+    for _ in range(400):
+        i = int(rng.integers(0, 300))
+        k = int(rng.integers(0, off + i + 1))                      # visible to row i
+        h = int(rng.integers(0, 2))
+        logit = float(pq[i, h] @ pk[table[k // PAGE], k % PAGE]) / math.sqrt(case.dp)
+        assert logit <= float(ms[i // 128, h, k // PAGE]) * (1 + 1e-6) + 1e-6

@@ -220,8 +220,11 @@ msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages,
  *  k_pages, v_pages  [num_pages, Hkv, 128, d], bf16 or e4m3 per the plan.
  *  kv_indices        int32 page table.
  *  kv_block_indexes  int32 [num_tiles, Hkv, topk], as msa_topk_select writes
- *                    them (any order of distinct valid blocks is accepted;
- *                    the diagonal block must be present).
+ *                    them.  Any order of distinct valid blocks is accepted,
+ *                    with -1 entries anywhere.  In prefill a query row that
+ *                    sees no key of its selection gets out = 0 and
+ *                    lse = -inf (a row of only -1 included); decode
+ *                    selections must hold the diagonal (last) block.
  *  k_scale, v_scale  fp32 [Hkv] for FP8 K/V, NULL for bf16.
  *  out               bf16 [total_q, Hq, d] (output).
  *  lse               fp32 [total_q, Hq] (output) or NULL.

@@ -28,7 +28,7 @@ Sources (page title, section):
               - "backward pass" paragraph: the gradient of the KL loss with
                 respect to a proxy score is p_proxy - p_main.
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
   R1  causal alignment is bottom-right: query row r of a sequence with
       qo_len rows and kv_len keys sits at position kv_len - qo_len + r and
       sees key k iff k <= that position.
@@ -50,7 +50,9 @@ Readings where the pages are silent (each is listed in the design doc):
       Parity of R6's domain and mean is unpinned by the pages.
   R7  a query row that sees no key of its tile's selected blocks (possible
       only when a tile straddles two blocks and its earlier block is not
-      selected) has O = 0 and LSE = -inf.
+      selected, or when its selection row holds only -1) has O = 0 and
+      LSE = -inf; in the backward its P and p_proxy are 0, so its KL term,
+      dZ and every gradient it sends are 0.
   R11 an FP8 e4m3 proxy K (decode) carries one fp32 scale for the single
       shared proxy head, dequantised like R5: logit =
       (pq.pk_code)*pk_scale/sqrt(dp).
@@ -272,6 +274,18 @@ def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_le
 # training extension: backward with the KL-coupled proxy gradient (R6)
 # ---------------------------------------------------------------------------
 
+def _masked_softmax(s, empty):
+    """Row softmax of logits s [R, n] whose masked entries are -inf, and its
+    natural-log LSE [R, 1].  Rows flagged in empty [R, 1] (no visible key,
+    R7) get probabilities 0 and LSE -inf instead of 0/0."""
+    m = np.where(empty, 0.0, s.max(axis=1, keepdims=True, initial=-np.inf))
+    e = np.where(empty, 0.0, np.exp(s - m))
+    l = np.where(empty, 1.0, e.sum(axis=1, keepdims=True))
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, m + np.log(l))
+    return e / l, lse
+
+
 def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
                          dout_bits, pq_bits, pk_bits, kl_weight=1.0, tile_ids=None):
     """Gradients of sum(O * dO) with respect to q, k, v restricted to the
@@ -312,16 +326,17 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
         for g in range(hkv):
             ks = _selected_keys(tl, kv_block_indexes[ti, g])
             vis = ks[None, :] <= qpos[:, None]
+            # R7: a row that sees no selected key has P = 0, O = 0, LSE = -inf,
+            # and so no gradient; its proxy distribution is empty as well
+            # (p_proxy = 0), which makes its KL term and dZ zero
+            empty = ~vis.any(axis=1, keepdims=True)                      # [R, 1]
             kmat, vmat = kseq[ks, g, :], vseq[ks, g, :]
             dkmat = np.zeros_like(kmat)
             dvmat = np.zeros_like(vmat)
             p_main = np.zeros(vis.shape)
             for h in range(g * grp, (g + 1) * grp):
                 s = np.where(vis, q[rows, h, :] @ kmat.T / math.sqrt(d), -np.inf)
-                m = s.max(axis=1, keepdims=True)
-                l = np.exp(s - m).sum(axis=1, keepdims=True)
-                lse_h = m + np.log(l)
-                p = np.exp(s - lse_h)                                   # [R, n]
+                p, lse_h = _masked_softmax(s, empty)                    # [R, n], [R, 1]
                 oh = p @ vmat
                 o[rows, h, :] = oh
                 lse[rows, h] = lse_h[:, 0]
@@ -335,9 +350,7 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
                 p_main += p / grp
             # proxy distribution over the same selected, visible keys
             z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
-            zm = z.max(axis=1, keepdims=True)
-            ez = np.exp(z - zm)
-            p_proxy = ez / ez.sum(axis=1, keepdims=True)
+            p_proxy, _ = _masked_softmax(z, empty)
             dz = kl_weight * (p_proxy - p_main)
             dpq[rows, g, :] = dz @ pkseq[ks] / math.sqrt(dp)
             dpk_keys = dz.T @ pq[rows, g, :] / math.sqrt(dp)            # [n, dp]
@@ -372,15 +385,15 @@ def kl_objective(pq, pk, q_bits, k_bits, kv_indices, kv_block_indexes, qo_lens, 
         for g in range(hkv):
             ks = _selected_keys(tl, kv_block_indexes[ti, g])
             vis = ks[None, :] <= qpos[:, None]
+            empty = ~vis.any(axis=1, keepdims=True)        # R7 rows contribute nothing
             p_main = np.zeros(vis.shape)
             for h in range(g * grp, (g + 1) * grp):
                 s = np.where(vis, q[rows, h, :] @ kseq[ks, g, :].T / math.sqrt(d), -np.inf)
-                e = np.exp(s - s.max(axis=1, keepdims=True))
-                p_main += e / e.sum(axis=1, keepdims=True) / grp
+                p_main += _masked_softmax(s, empty)[0] / grp
             z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
-            zm = z.max(axis=1, keepdims=True)
-            log_pp = z - zm - np.log(np.exp(z - zm).sum(axis=1, keepdims=True))
+            _, lse_z = _masked_softmax(z, empty)
             with np.errstate(divide="ignore", invalid="ignore"):
+                log_pp = z - lse_z
                 terms = np.where(p_main > 0, p_main * (np.log(p_main) - log_pp), 0.0)
             total += kl_weight * terms.sum()
     return total

@@ -350,22 +350,27 @@ def _autograd_route(inp, case, idx, w):
                 for j in idx[t0 + r // 128, g]:
                     if j >= 0:
                         sel[r, j * PAGE:(j + 1) * PAGE] = True
-            m = vis & sel
+            # rows that see no selected key (R7) are left out of both losses:
+            # the library softmax would give 0/0 there
+            live = (vis & sel).any(1)
+            rows = torch.arange(q0, q0 + ql)[live]
+            m = (vis & sel)[live]
             pmain = 0.0
             for h in range(g * grp, (g + 1) * grp):
-                qh = q[q0:q0 + ql, h]
+                qh = q[rows, h]
                 oh = F.scaled_dot_product_attention(qh[None], ks[g][None], vs[g][None], attn_mask=m[None])[0]
-                loss_main = loss_main + (oh * do[q0:q0 + ql, h]).sum()
+                loss_main = loss_main + (oh * do[rows, h]).sum()
                 s = (qh @ ks[g].T / math.sqrt(case.d)).masked_fill(~m, -math.inf)
                 pmain = pmain + torch.softmax(s, -1).detach() / grp
-            z = (pq[q0:q0 + ql, g] @ pks.T / math.sqrt(case.dp)).masked_fill(~m, -math.inf)
+            z = (pq[rows, g] @ pks.T / math.sqrt(case.dp)).masked_fill(~m, -math.inf)
             logp = torch.log_softmax(z, -1).masked_fill(~m, 0.0)
             loss_kl = loss_kl + w * F.kl_div(logp, pmain, reduction="sum")
         q0 += ql
         p0 += nb
         t0 += (ql + 127) // 128
     (loss_main + loss_kl).backward()
-    return q.grad.numpy(), kp.grad.numpy(), vp.grad.numpy(), pq.grad.numpy(), pk.grad.numpy()
+    grads = [t.grad if t.grad is not None else torch.zeros_like(t) for t in (q, kp, vp, pq, pk)]
+    return tuple(gr.numpy() for gr in grads)
 
 
 @pytest.mark.parametrize("qo,kv,topk,w", [([256], [256], 2, 1.0), ([150, 40], [300, 200], 2, 0.5)])
@@ -379,6 +384,67 @@ def test_bwd_vs_autograd(qo, kv, topk, w):
     dq, dk, dv, dpq, dpk = _autograd_route(inp, case, idx, w)
     for name, ref in [("dq", dq), ("dk", dk), ("dv", dv), ("dpq", dpq), ("dpk", dpk)]:
         np.testing.assert_allclose(g[name], ref, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def _r7_cases():
+    """Selections that leave query rows with no visible key (R7): a tile
+    straddling two blocks with only its diagonal block selected; a group
+    whose selection row holds only -1; -1 entries between valid ones."""
+    a = synth.Case("straddle topk 1", [128], [200], 4, 2, 64, 2, 32, 1)
+    ia = np.array([[[1], [1]]], dtype=np.int32)             # rows 0..55 sit in block 0
+    b = synth.Case("ragged, -1 rows", [150, 40, 1], [300, 200, 129], 4, 2, 64, 2, 32, 3,
+                   page_perm_seed=4, extra_pages=1)
+    ib = _rand_idx(b, np.random.default_rng(12))
+    ib[0, 0, :] = [2, -1, -1]          # tile 0 of seq 0 (positions 150..277): rows < 256 see nothing
+    ib[1, 1, :] = -1                   # tile 1, group 1: no block at all
+    ib[2, 0, :] = [-1, 1, -1]          # seq 1 tile: diagonal block only, -1 on both sides
+    return [(a, ia), (b, ib)]
+
+
+@pytest.mark.parametrize("ci", [0, 1])
+def test_bwd_rows_without_visible_keys(ci):
+    """R7 in the backward: rows that see no selected key get zero dq and
+    dpq and send nothing into dk, dv or dpk; every gradient is finite and
+    the rest equals autograd with those rows left out of both losses."""
+    case, idx = _r7_cases()[ci]
+    inp = synth.make_inputs(case, with_dout=True)
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens, synth.bits(inp["dout"]),
+                               synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]), kl_weight=0.7)
+    for name in ("dq", "dk", "dv", "dpq", "dpk", "o"):
+        assert np.isfinite(g[name]).all(), name
+    empty = np.isneginf(g["lse"])                                 # [total_q, Hq]
+    assert empty.any() and (~empty).any()
+    assert (g["dq"][empty] == 0.0).all() and (g["o"][empty] == 0.0).all()
+    grp = case.hq // case.hkv
+    empty_g = empty.reshape(case.total_q, case.hkv, grp).all(2)   # [total_q, Hkv]: same for the group's heads
+    assert (empty_g == empty.reshape(case.total_q, case.hkv, grp).any(2)).all()
+    assert (g["dpq"][empty_g] == 0.0).all()
+    dq, dk, dv, dpq, dpk = _autograd_route(inp, case, idx, 0.7)
+    for name, ref in [("dq", dq), ("dk", dk), ("dv", dv), ("dpq", dpq), ("dpk", dpk)]:
+        np.testing.assert_allclose(g[name], ref, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_kl_objective_finite_with_empty_rows():
+    """The KL objective is defined (finite) when some rows see no key, and
+    its finite differences still match the closed-form proxy gradient."""
+    case, idx = _r7_cases()[0]
+    inp = synth.make_inputs(case, with_dout=True)
+    args = (synth.bits(inp["q"]), synth.bits(inp["k_pages"]), inp["kv_indices"].numpy(), idx,
+            case.qo_lens, case.kv_lens)
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens,
+                               synth.bits(inp["dout"]), synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]))
+    pq = O.bf16_to_f64(synth.bits(inp["pq"]))
+    pk = O.bf16_to_f64(synth.bits(inp["pk_pages"]))
+    assert np.isfinite(O.kl_objective(pq, pk, *args))
+    h = 1e-6
+    for i, hh, c in [(3, 0, 5), (100, 1, 17), (127, 0, 31), (60, 1, 0)]:   # rows 0..55 are empty
+        a, b = pq.copy(), pq.copy()
+        a[i, hh, c] += h
+        b[i, hh, c] -= h
+        fd = (O.kl_objective(a, pk, *args) - O.kl_objective(b, pk, *args)) / (2 * h)
+        assert abs(fd - g["dpq"][i, hh, c]) <= 1e-6 * max(1.0, abs(fd)), (i, hh, c, fd, g["dpq"][i, hh, c])
 
 
 def test_kl_grad_finite_differences():

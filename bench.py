@@ -40,8 +40,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # an ncu capture, valid only for the kernel source it was taken on.
 # Captured on S=16384 (15424 selected tile-blocks: 247.8 MB read + 108.4 MB
 # written) and scaled by selected tile-blocks to the S=32768 launch (31808).
-NCU_TRAFFIC = {"attn_fwd.cu": {"src": "bd30baa3cf914cf1", "bytes": int((243888384 + 108123904) * 31808 / 15424),
-                               "source": "profiles/attn_fwd_prefill.md"}}
+NCU_TRAFFIC = {"attn_fwd.cu": {"src": "bd30baa3cf914cf1", "bytes": int((243888384 + 108123904) * 31808 / 15424)}}
 
 
 def peaks():

@@ -7,6 +7,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "msa_internal.h"
@@ -15,6 +16,8 @@
 namespace msa {
 
 static thread_local std::string g_last_error;
+// Allocation failures still to inject into msa_plan (msa_test_fail_plan_allocs).
+static std::atomic<int32_t> g_fail_allocs{0};
 
 msa_status set_error(msa_status s, const char* fmt, ...) {
   char buf[512];
@@ -183,7 +186,6 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   std::vector<int32_t> aux;
   proxy_plan_tables(p, aux);
   attn_plan_tables(p, aux);
-  bwd_plan_tables(p, aux);
 
   // device block: tiles | nvp | error word | aux tables | decode partials |
   // backward scratch | fused top-k counters and candidates
@@ -196,6 +198,13 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   const size_t bwd_off = part_off + part_bytes;
   const size_t fz_off = bwd_off + ((bwd_scratch_bytes(p) + 255) & ~size_t(255));
   const size_t total = fz_off + fused_topk_scratch_bytes(p);
+  int32_t inject = g_fail_allocs.load();
+  while (inject > 0 && !g_fail_allocs.compare_exchange_weak(inject, inject - 1)) {
+  }
+  if (inject > 0) {  // an injected failure: the same path as a real one, without the call
+    delete p;
+    return set_error(MSA_ERR_NO_MEMORY, "msa_plan: cudaMalloc of %zu bytes failed (injected)", total);
+  }
   if (cudaMalloc(&p->dev_block, total) != cudaSuccess) {
     cudaGetLastError();
     delete p;
@@ -322,6 +331,8 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
   return launch_attn_bwd(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, dout, pq, pk_pages,
                          kl_weight, dq, dk_pages, dv_pages, dpq, dpk_pages, reinterpret_cast<cudaStream_t>(stream));
 }
+
+void msa_test_fail_plan_allocs(int32_t count) { g_fail_allocs.store(count > 0 ? count : 0); }
 
 msa_status msa_selftest_wait_timeout(msa_stream_t stream) {
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

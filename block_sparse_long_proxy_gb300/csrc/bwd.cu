@@ -23,13 +23,13 @@
 //   prep     per (tile, group): D of the group's heads and lse * log2(e),
 //            both stored [head][row]; the proxy LSE in log2 units
 //            ([group][row]) and dpq's proxy term (plain store)
-//   index    block -> tiles inverse index of the cached selections
+//   index    page owners, then the page -> selections inverse index
 //   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
 //            store) and dpq's main term (fp32 atomics, G per element)
-//   dkv      per (cached block, group), tcgen05 (bwd_dkv.cu): loops over
-//            the tiles that selected the block (sorted, so sums are
-//            deterministic); dk, dv (owned, plain store) and dpk (both
-//            terms, fp32 atomics across groups)
+//   dkv      per (physical page, group), tcgen05 (bwd_dkv.cu): loops over
+//            the selections of the page by any page-table entry (sorted, so
+//            sums are deterministic); dk, dv (owned, plain store) and dpk
+//            (both terms, fp32 atomics across groups)
 
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -116,11 +116,35 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ------------------------------------------------------------ inverse index
+//
+// The key-side kernel has one CTA per (page-table entry, group) and writes
+// dK / dV of the entry's physical page with plain stores.  Several entries
+// may name one physical page (a prefix shared by sequences), so every
+// selection is filed under the page's owner, the lowest entry that names
+// it; the owner's CTA sums the contributions of all of them and the other
+// entries' CTAs leave the page alone.
 
-// count[e*hkv + g] = number of tiles whose cached blocks of group g include
-// page-table entry e (entry = sequence's page_base + logical block).
+// owner[page] = min over entries e with kv_indices[e] == page of e (owner
+// starts at INT_MAX).  Entries with a page id out of range own themselves.
+__global__ void bwd_owner_kernel(const int32_t* __restrict__ kv_indices, int32_t n_entries, int64_t num_pages,
+                                 int32_t* __restrict__ owner) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n_entries) return;
+  const int64_t page = kv_indices[e];
+  if (page >= 0 && page < num_pages) atomicMin(owner + page, e);
+}
+
+__device__ __forceinline__ int32_t owner_of(const int32_t* __restrict__ kv_indices, const int32_t* __restrict__ owner,
+                                            int64_t num_pages, int32_t e) {
+  const int64_t page = kv_indices[e];
+  return (page >= 0 && page < num_pages) ? owner[page] : e;
+}
+
+// count[o*hkv + g] = number of selections (tile, group g, slot) whose block
+// maps to a page owned by entry o.
 __global__ void bwd_count_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx, int32_t n_tiles,
-                                 int32_t hkv, int32_t topk, int32_t* __restrict__ count) {
+                                 int32_t hkv, int32_t topk, const int32_t* __restrict__ kv_indices,
+                                 const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ count) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(n_tiles) * hkv * topk) return;
   const int t = static_cast<int>(e / (static_cast<int64_t>(hkv) * topk));
@@ -128,7 +152,7 @@ __global__ void bwd_count_kernel(const TileInfo* __restrict__ tiles, const int32
   const int j = idx[e];
   const TileInfo tl = tiles[t];
   if (j < 0 || j >= tl.nvp) return;
-  atomicAdd(count + (tl.page_base + j) * hkv + g, 1);
+  atomicAdd(count + owner_of(kv_indices, owner, num_pages, tl.page_base + j) * hkv + g, 1);
 }
 
 // Exclusive scan of n counts into off[0..n] (one CTA of 1024 threads);
@@ -157,8 +181,13 @@ __global__ void __launch_bounds__(1024) bwd_scan_kernel(const int32_t* __restric
   if (threadIdx.x == 1023) off[n] = part[1023];
 }
 
+// Files each selection under its page owner and group; the list item is the
+// flat selection index (t * hkv + g) * topk + slot, which gives both the
+// tile and the logical block (and sorts by tile).
 __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx, int32_t n_tiles,
-                                int32_t hkv, int32_t topk, int32_t* __restrict__ cursor, int32_t* __restrict__ list) {
+                                int32_t hkv, int32_t topk, const int32_t* __restrict__ kv_indices,
+                                const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ cursor,
+                                int32_t* __restrict__ list) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(n_tiles) * hkv * topk) return;
   const int t = static_cast<int>(e / (static_cast<int64_t>(hkv) * topk));
@@ -166,7 +195,8 @@ __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_
   const int j = idx[e];
   const TileInfo tl = tiles[t];
   if (j < 0 || j >= tl.nvp) return;
-  list[atomicAdd(cursor + (tl.page_base + j) * hkv + g, 1)] = t;
+  list[atomicAdd(cursor + owner_of(kv_indices, owner, num_pages, tl.page_base + j) * hkv + g, 1)] =
+      static_cast<int32_t>(e);
 }
 
 // dpk rows of every referenced page start at zero (they are reduced by
@@ -185,7 +215,8 @@ __global__ void bwd_zero_dpk_kernel(const int32_t* __restrict__ kv_indices, int3
 
 // The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
 // fp32), lsept ([Hkv][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
-// Hp, dp]) and LSE (fp32 [total_q, Hp]), then the inverse index (int32).
+// Hp, dp]) and LSE (fp32 [total_q, Hp]), the inverse index (int32), then the
+// page owners (int32 [num_pages]).
 static size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 size_t bwd_scratch_bytes(const msa_plan_s* p) {
@@ -193,15 +224,8 @@ size_t bwd_scratch_bytes(const msa_plan_s* p) {
   const size_t tq = static_cast<size_t>(p->total_q);
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
   return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hkv) + al256(2 * tq * p->hkv * kDP) + al256(4 * tq * p->hkv) +
-         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk));
-}
-
-void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
-  p->blk_j_off = static_cast<int64_t>(aux.size());
-  for (int s = 0; s < p->batch; ++s) {
-    const int nb = (p->kv_lens[s] + kPage - 1) / kPage;
-    for (int j = 0; j < nb; ++j) aux.push_back(j);
-  }
+         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk)) +
+         al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
 }
 
 msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
@@ -230,7 +254,8 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   int32_t* off = cnt + ent;
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
-  const int32_t* blk_j = p->aux_d + p->blk_j_off;
+  sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk));
+  int32_t* owner = reinterpret_cast<int32_t*>(sp);                    // [num_pages]
   const auto* O = static_cast<const __nv_bfloat16*>(out);
   const auto* dO = static_cast<const __nv_bfloat16*>(dout);
   const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hkv * p->topk;
@@ -242,17 +267,23 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                                                            dpq, p->hq, p->hkv, static_cast<int32_t>(p->total_q),
                                                            kl_weight);
   s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
+  if (s == MSA_OK)  // 0x7F7F7F7F: above every entry index
+    s = cuda_check(cudaMemsetAsync(owner, 0x7F, sizeof(int32_t) * static_cast<size_t>(p->num_pages), st),
+                   "msa_sparse_attn_bwd: memset");
   if (s != MSA_OK) return s;
+  bwd_owner_kernel<<<(n_ent + 255) / 256, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, owner);
   const int sel_blocks = static_cast<int>((n_sel + 255) / 256);
-  bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, cnt);
+  bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, kv_indices, owner,
+                                               p->num_pages, cnt);
   bwd_scan_kernel<<<1, 1024, 0, st>>>(cnt, static_cast<int32_t>(ent), off, cur);
-  bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, cur, list);
+  bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, kv_indices, owner,
+                                              p->num_pages, cur, list);
   s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
   if (s != MSA_OK) return s;
   s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
   if (s != MSA_OK) return s;
-  return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, blk_j, off, list, lse2t, dsumt,
-                           lsept, dk, dv, dpk, kl_weight, st);
+  return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, idx, owner, off, list, lse2t,
+                           dsumt, lsept, dk, dv, dpk, kl_weight, st);
 }
 
 }  // namespace msa

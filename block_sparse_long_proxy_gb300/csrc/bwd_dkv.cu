@@ -2,9 +2,12 @@
 // block-sparse GQA attention with the KL-coupled proxy (Flash-MSA article,
 // backward-pass paragraph), on the tcgen05 tensor cores.
 //
-// One CTA per (cached block e, GQA group g).  It walks the tiles that cached
-// block e for group g (the inverse index, sorted so sums are deterministic),
-// 64 query rows at a time, and for each of the group's G heads:
+// One CTA per (page-table entry e, GQA group g).  The lowest entry that
+// names a physical page owns it: its CTA walks every selection of that page
+// for group g, by this entry or any other that names the same page (the
+// inverse index, sorted so sums are deterministic), 64 query rows at a time,
+// and the CTAs of the other entries return at once.  Per selection, for each
+// of the group's G heads:
 //   S^T  = K . Q_h^T            dP^T = V . dO_h^T       (M = keys, N = rows)
 //   P^T  = exp2(S^T sl2 - lse2)  dS^T = P^T * (dP^T - D)  (masked: causal, ragged)
 //   dV  += P^T . dO_h           dK  += dS^T . Q_h       (P^T, dS^T from TMEM)
@@ -68,8 +71,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
                       const __grid_constant__ CUtensorMap pq_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap pk_map,
-                      const TileInfo* __restrict__ tiles, const int32_t* __restrict__ blk_j,
-                      const int32_t* __restrict__ inv_off, const int32_t* __restrict__ inv_list,
+                      const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
+                      const int32_t* __restrict__ owner, const int32_t* __restrict__ inv_off,
+                      const int32_t* __restrict__ inv_list, int32_t topk,
                       const int32_t* __restrict__ kv_indices, int64_t num_pages, const float* __restrict__ lse2t,
                       const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
                       float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, int32_t total_q,
@@ -79,9 +83,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int e = blockIdx.x / hkv, g = blockIdx.x % hkv;
   const int G = hq / hkv;
-  const int j = blk_j[e];
   int64_t page = kv_indices[e];
   const bool page_ok = page >= 0 && page < num_pages;
+  if (page_ok && owner[page] != e) return;  // another entry's CTA owns this page
   if (!page_ok) page = 0;
   const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
   const int64_t kv_off = (page * hkv + g) * 128 * kD;
@@ -148,7 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done, 1);
     fence_mbar_init();
   }
-  // the tile list, sorted so that every run sums in the same order
+  // the selection list (flat indexes (t * hkv + g) * topk + slot), sorted so
+  // that every run sums in the same order
   const bool sorted = n <= kMaxList;
   if (sorted) {
     int pow2 = 1;
@@ -179,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  auto tile_at = [&](int it) { return sorted ? list[it] : inv_list[lb + it]; };
+  auto sel_at = [&](int it) { return sorted ? list[it] : inv_list[lb + it]; };
+  const int sel_per_tile = hkv * topk;
 
   if (warp == 8) {
     // ---------------------------------------------------------- producer
@@ -195,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int qi = 0, pi = 0;
     for (int it = 0; ok && it < n; ++it) {
-      const TileInfo tl = tiles[tile_at(it)];
+      const TileInfo tl = tiles[sel_at(it) / sel_per_tile];
       const int halves = tl.rows > 64 ? 2 : 1;
       for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
         const int r0 = tl.q_begin + hf * 64;
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int qi = 0, pi = 0;
       bool sp_issued = false;  // the current half's Sp^T went out with the previous half's last head
       for (int it = 0; ok && it < n; ++it) {
-        const TileInfo tl = tiles[tile_at(it)];
+        const TileInfo tl = tiles[sel_at(it) / sel_per_tile];
         const int halves = tl.rows > 64 ? 2 : 1;
         for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
           const int ps = pi % kPqStages;
@@ -350,7 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = quarter * 32 + lane;
     const int c0 = wg * 32;  // this warpgroup's rows within the 64-row half
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int kpos = j * 128 + key;
     const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
     const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
     const float neg_g = -static_cast<float>(G);
@@ -381,7 +386,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int qi = 0, pi = 0;
     for (int it = 0; ok && it < n; ++it) {
-      const TileInfo tl = tiles[tile_at(it)];
+      const int sel = sel_at(it);
+      const TileInfo tl = tiles[sel / sel_per_tile];
+      const int j = idx[sel];  // the block's logical index in the selecting tile's sequence
+      const int kpos = j * 128 + key;
       const int halves = tl.rows > 64 ? 2 : 1;
       for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
         const int ps = pi % kPqStages;
@@ -512,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                              const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
-                             const int32_t* blk_j, const int32_t* inv_off, const int32_t* inv_list,
+                             const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
+                             const int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
                              float* dpk, float kl_weight, cudaStream_t st) {
   CUtensorMap qm, dom, pqm, km, vm, pkm;
@@ -538,7 +547,8 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   const int smem = DkvSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
-      qm, dom, pqm, km, vm, pkm, p->tiles_d, blk_j, inv_off, inv_list, kv_indices, p->num_pages, lse2t, dsumt, lsept,
+      qm, dom, pqm, km, vm, pkm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
+      dsumt, lsept,
       dk, dv, dpk, p->hq, p->hkv, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
 }

@@ -577,11 +577,16 @@ msa_status static_scratch(StaticDevice* out) {
 
 // Tile table of a decode batch (one query row per sequence) from device
 // kv_lens / kv_indptr.  A sequence whose page range is shorter than its
-// kv_len needs gets no valid blocks and raises the device-check bit.
+// kv_len needs gets no valid blocks and raises the device-check bit.  The
+// split-K arrival counters of the sequence's rows are cleared here on every
+// call, so a row left half-counted by an earlier call that failed (a wait
+// that gave up) cannot make this call merge too early or never.
 __global__ void decode_tiles_kernel(const int32_t* __restrict__ kv_lens, const int32_t* __restrict__ kv_indptr,
-                                    int32_t batch, TileInfo* __restrict__ tiles, uint32_t* err) {
+                                    int32_t batch, int32_t num_kv_heads, TileInfo* __restrict__ tiles,
+                                    int32_t* __restrict__ row_cnt, uint32_t* err) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= batch) return;
+  for (int g = 0; g < num_kv_heads; ++g) row_cnt[static_cast<int64_t>(t) * num_kv_heads + g] = 0;
   TileInfo ti;
   const int kl = kv_lens[t];
   const int base = kv_indptr[t], next = kv_indptr[t + 1];
@@ -646,8 +651,8 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
   uint32_t* err = err_word ? err_word : reinterpret_cast<uint32_t*>(sd.base + kStaticErrOff);
   float* part_o = reinterpret_cast<float*>(sd.base + kStaticPartOff);
   float* part_ml = part_o + n_units * G * kD;
-  // per-row arrival counters: zero when the module loads, reset to zero by
-  // the CTA that merges a row, so every call finds them at zero
+  // per-row arrival counters: cleared for this call's rows by the tile-table
+  // kernel, which runs first on the same stream
   int32_t* row_cnt = reinterpret_cast<int32_t*>(sd.base + kStaticCntOff);
   auto* o_ptr = static_cast<__nv_bfloat16*>(out);
 
@@ -659,7 +664,8 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
       !encode_tensor_map(&vm, 2, v_pages, dims, str, box, 0, 128))
     return set_error(MSA_ERR_CUDA, "%s: tensor map encoding failed", fn);
 
-  decode_tiles_kernel<<<(batch + 127) / 128, 128, 0, st>>>(kv_lens, kv_indptr, batch, tiles, err);
+  decode_tiles_kernel<<<(batch + 127) / 128, 128, 0, st>>>(kv_lens, kv_indptr, batch, num_kv_heads, tiles, row_cnt,
+                                                           err);
   s = cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: tile table launch");
   if (s != MSA_OK) return s;
   const int nu = static_cast<int>(n_units);

@@ -78,7 +78,6 @@ struct msa_plan_s {
   int32_t n_attn_units = 0;
   int64_t proxy_attn_units_off = 0;  // backward proxy softmax work units
   int32_t n_proxy_attn_units = 0;
-  int64_t blk_j_off = 0;             // backward: logical block of each page-table entry
   int32_t n_page_entries = 0;        // sum over sequences of ceil(kv_len / 128)
   void* bwd_d = nullptr;             // backward scratch (D, proxy LSE, inverse index)
 };
@@ -91,7 +90,6 @@ msa_status cuda_check(cudaError_t e, const char* what);
 // ---- plan-time tables (host), appended to the plan's aux array ----
 void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
-void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
 size_t fused_topk_scratch_bytes(const msa_plan_s* p);  // 0 when msa_proxy_topk is unsupported
 size_t fused_topk_counter_bytes(const msa_plan_s* p);  // leading part that starts at zero
@@ -108,7 +106,8 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
 // the row statistics written by the prep kernel, [heads][total_q].
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                              const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
-                             const int32_t* blk_j, const int32_t* inv_off, const int32_t* inv_list,
+                             const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
+                             const int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
                              float* dpk, float kl_weight, cudaStream_t st);
 

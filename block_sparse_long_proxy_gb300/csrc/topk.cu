@@ -34,8 +34,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
   const int tile = static_cast<int>(row / heads);
   const float* src = max_score + row * max_blocks;
   int32_t* dst = out + row * topk;
-  int n = nvp_arr[tile];
-  n = n < 1 ? 1 : (n > max_blocks ? max_blocks : n);
+  const int n = nvp_arr[tile];
+  if (n < 1 || n > max_blocks) {  // outside the contract: select nothing
+    for (int j = lane; j < topk; j += 32) dst[j] = -1;
+    return;
+  }
   const uint32_t lt_mask = (1u << lane) - 1u;
 
   if (topk >= n) {  // every valid block is selected
@@ -106,8 +109,11 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
   const int tile = static_cast<int>(row / heads);
   const float* src = max_score + row * max_blocks;
   int32_t* dst = out + row * topk;
-  int n = nvp_arr[tile];
-  n = n < 1 ? 1 : (n > max_blocks ? max_blocks : n);
+  const int n = nvp_arr[tile];
+  if (n < 1 || n > max_blocks) {  // outside the contract: select nothing
+    for (int j = lane; j < topk; j += 32) dst[j] = -1;
+    return;
+  }
   const uint32_t lt_mask = (1u << lane) - 1u;
   if (topk >= n) {
     for (int j = lane; j < topk; j += 32) dst[j] = j < n ? j : -1;

@@ -48,6 +48,7 @@ SIGNATURES = {
                                          _p, _p, _p, _p]),
     "msa_check_errors": (_i32, [_p, _p]),
     "msa_selftest_wait_timeout": (_i32, [_p]),
+    "msa_test_fail_plan_allocs": (None, [_i32]),
     "msa_last_error": (ctypes.c_char_p, []),
     "msa_version": (ctypes.c_char_p, []),
 }
@@ -99,6 +100,12 @@ def selftest_wait_timeout(stream=None):
     _check(_lib.msa_selftest_wait_timeout(_stream(stream)), "msa_selftest_wait_timeout")
 
 
+def inject_plan_alloc_failures(count):
+    """Failure injection (msa_test_fail_plan_allocs): the next `count` plan
+    creations fail at their device allocation with MSA_ERR_NO_MEMORY."""
+    _lib.msa_test_fail_plan_allocs(int(count))
+
+
 def topk_select(max_score, topk, num_valid_pages, out=None, stream=None):
     """kv_block_indexes [n_tiles, heads, topk] int32 from max_score [n_tiles,
     heads, max_blocks] fp32 (msa_topk_select)."""
@@ -128,6 +135,7 @@ def sparse_decode_noalloc(q, k_pages, v_pages, kv_lens, kv_indptr, kv_indices, k
     _need(v_pages, torch.float8_e4m3fn, tuple(k_pages.shape), "v_pages")
     _need(kv_lens, torch.int32, (b,), "kv_lens")
     _need(kv_indptr, torch.int32, (b + 1,), "kv_indptr")
+    _need(kv_indices, torch.int32, (kv_indices.numel(),), "kv_indices")
     _need(kv_block_indexes, torch.int32, (b, hkv, topk), "kv_block_indexes")
     _need(k_scale, torch.float32, (hkv,), "k_scale")
     _need(v_scale, torch.float32, (hkv,), "v_scale")
@@ -136,6 +144,11 @@ def sparse_decode_noalloc(q, k_pages, v_pages, kv_lens, kv_indptr, kv_indices, k
     _need(out, torch.bfloat16, (b, hq, d), "out")
     if lse is not None:
         _need(lse, torch.float32, (b, hq), "lse")
+    if err_word is not None:
+        if err_word.dtype not in (torch.int32, torch.uint32) or err_word.numel() != 1:
+            raise TypeError("err_word: want one 4-byte integer, got %s %s" % (err_word.dtype, tuple(err_word.shape)))
+        if not err_word.is_cuda:
+            raise ValueError("err_word: must be a CUDA tensor")
     _check(_lib.msa_sparse_decode_noalloc(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(kv_lens), _ptr(kv_indptr),
                                           _ptr(kv_indices), _ptr(kv_block_indexes), _ptr(k_scale), _ptr(v_scale),
                                           b, hq, hkv, d, topk, k_pages.shape[0], _ptr(out), _ptr(lse),

@@ -48,7 +48,7 @@ class Case:
         return int(sum((k + PAGE - 1) // PAGE for k in self.kv_lens))
 
 
-# The five workloads of the method's evaluation (sizes stated in the design doc).
+# The five workloads of the method's evaluation, at their stated sizes.
 def tiny():
     return Case("tiny causal MSA forward S=1024", [1024], [1024], 8, 2, 64, 2, 32, 4)
 

@@ -170,7 +170,10 @@ msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* p
  * the contract.
  *
  *  max_score        fp32 [n_tiles, heads, max_blocks].
- *  num_valid_pages  int32 [n_tiles], each in [1, max_blocks].
+ *  num_valid_pages  int32 [n_tiles], each in [1, max_blocks].  A row whose
+ *                   value lies outside that range selects nothing: it is
+ *                   written as topk entries of -1 (the attention then
+ *                   treats its query rows as seeing no key).
  *  kv_block_indexes int32 [n_tiles, heads, topk] (output).
  *  1 <= topk <= 1024, max_blocks <= 65536.
  */
@@ -287,14 +290,17 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
  *              kv_indices (kv_indptr[s+1] - kv_indptr[s] >= ceil(kv_len/128)).
  * q, k_pages, v_pages, kv_indices, kv_block_indexes ([batch, Hkv, topk]),
  * k_scale, v_scale, out and lse (nullable) are as in msa_sparse_attn.
- * err_word: optional DEVICE uint32 that device-side bounds checks OR into
- * (bit 0: a bad page id or page range; the block is skipped or read from
- * page 0); NULL discards them.
+ * err_word: optional DEVICE uint32 that the kernels OR status bits into;
+ * NULL discards them.  Bit 0: a device-side bounds check fired (a bad page
+ * id or page range; that block is skipped or read from page 0).  Bit 1: a
+ * bounded device-side wait gave up; the call's out and lse are then
+ * unspecified.  The caller clears the word.
  *
  * Scratch: all of it (a tile table and the split-K partials) lives in one
  * fixed 24 MiB device array inside libmsa, held by every GPU that loads the
  * library until the process exits.  The call allocates nothing and calls no
- * allocating routine.  It rejects, with MSA_ERR_INVALID_ARG, batch > 4096 or
+ * allocating routine.  Each call clears the split-K counters of its own rows
+ * before using them, so a call that failed does not disturb later ones.  It rejects, with MSA_ERR_INVALID_ARG, batch > 4096 or
  * batch * num_qo_heads * topk above 47,639 (the partials that fit in the
  * array at head_dim 128) or batch * num_kv_heads above 65,536.  The first call on a device looks up the array's
  * device address for that device (cudaGetSymbolAddress) with that device
@@ -329,6 +335,15 @@ msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream);
  * MSA_ERR_CUDA.  Synchronises `stream`; allocates and frees 4 bytes.
  */
 msa_status msa_selftest_wait_timeout(msa_stream_t stream);
+
+/*
+ * msa_test_fail_plan_allocs -- failure injection on the host, for tests of a
+ * caller's out-of-memory handling: the next `count` calls of msa_plan that
+ * reach their device allocation fail there exactly as a failed cudaMalloc
+ * does (MSA_ERR_NO_MEMORY, nothing allocated, *out left NULL), without
+ * calling cudaMalloc.  count <= 0 cancels what is left.  Process-wide.
+ */
+void msa_test_fail_plan_allocs(int32_t count);
 
 /* Message for the calling thread's last failed call ("" if none). */
 const char* msa_last_error(void);

@@ -27,6 +27,19 @@ def random_idx(case, rng):
     return idx
 
 
+def irregular_idx(case, rng):
+    """Selections in random order with the -1 padding spread through the row,
+    and every fifth (tile, group) row empty: its rows get out = 0, lse = -inf."""
+    idx = random_idx(case, rng)
+    nt, hkv, _ = idx.shape
+    for t in range(nt):
+        for g in range(hkv):
+            idx[t, g] = idx[t, g][rng.permutation(case.topk)]
+            if (t * hkv + g) % 5 == 3:
+                idx[t, g] = -1
+    return idx
+
+
 def make_plan(case, inp):
     from block_sparse_long_proxy_gb300 import msa
     return msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,

@@ -6,7 +6,7 @@ import torch
 
 from block_sparse_long_proxy_gb300 import synth
 from oracle import msa_oracle as O
-from tests.gpu_cases import (O_ATOL_BF16, compare_out, random_idx, make_plan, rows_of_tiles,
+from tests.gpu_cases import (O_ATOL_BF16, compare_out, random_idx, irregular_idx, make_plan, rows_of_tiles,
                              check_indices_with_gap, MS_ATOL)
 
 pytestmark = pytest.mark.gpu
@@ -47,19 +47,6 @@ IRREGULAR = [
     synth.Case("shuffled and empty rows", [1024, 700, 300], [1024, 900, 300], 8, 2, 128, 2, 64, 6,
                page_perm_seed=4),
 ]
-
-
-def irregular_idx(case, rng):
-    """Selections in random order with the -1 padding spread through the row,
-    and every fifth (tile, group) row empty: its rows get out = 0, lse = -inf."""
-    idx = random_idx(case, rng)
-    nt, hkv, _ = idx.shape
-    for t in range(nt):
-        for g in range(hkv):
-            idx[t, g] = idx[t, g][rng.permutation(case.topk)]
-            if (t * hkv + g) % 5 == 3:
-                idx[t, g] = -1
-    return idx
 
 
 @pytest.mark.parametrize("case", IRREGULAR, ids=lambda c: c.name)

@@ -6,7 +6,7 @@ import torch
 
 from block_sparse_long_proxy_gb300 import synth
 from oracle import msa_oracle as O
-from tests.gpu_cases import O_ATOL_BF16, compare_out, make_plan, random_idx, rows_of_tiles
+from tests.gpu_cases import O_ATOL_BF16, compare_out, irregular_idx, make_plan, random_idx, rows_of_tiles
 
 pytestmark = pytest.mark.gpu
 PAGE = 128
@@ -46,6 +46,75 @@ def test_bwd_small(cuda_dev, case, w):
     ref = _oracle(case, inp, idx, w)
     for name in ("dq", "dpq", "dk", "dv", "dpk"):
         compare_out(got[name], ref[name], O_ATOL_BF16, name)
+
+
+def _check_all(got, ref):
+    for name in ("dq", "dpq", "dk", "dv", "dpk"):
+        assert np.isfinite(got[name]).all(), "%s has non-finite entries" % name
+        assert np.isfinite(ref[name]).all(), "oracle %s has non-finite entries" % name
+        compare_out(got[name], ref[name], O_ATOL_BF16, name)
+
+
+def test_bwd_rows_without_visible_keys(cuda_dev):
+    """Tiles straddling two blocks with topk 1 (only the diagonal block): the
+    early rows see no key (R7), so their dq and dpq are exactly 0 and they
+    add nothing to dk, dv, dpk; everything else matches the oracle."""
+    case = synth.Case("straddle topk 1", [128, 100, 64], [200, 300, 1000], 8, 2, 128, 2, 64, 1,
+                      page_perm_seed=6, extra_pages=1)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    idx = random_idx(case, np.random.default_rng(2))
+    got = _run_gpu(case, inp, torch.from_numpy(idx).to(cuda_dev), 1.0)
+    ref = _oracle(case, inp, idx, 1.0)
+    empty = np.isneginf(ref["lse"])
+    assert empty.any()
+    assert (got["dq"][empty] == 0.0).all()
+    grp = case.hq // case.hkv
+    empty_g = empty.reshape(case.total_q, case.hkv, grp).all(2)
+    assert (got["dpq"][empty_g] == 0.0).all()
+    _check_all(got, ref)
+
+
+@pytest.mark.parametrize("case", [
+    synth.Case("shuffled and empty rows", [1024, 700, 300], [1024, 900, 300], 8, 2, 128, 2, 64, 6,
+               page_perm_seed=4),
+    synth.Case("shuffled, ragged, topk 3", [300, 77, 129], [300, 500, 129], 4, 2, 128, 2, 64, 3,
+               page_perm_seed=3, extra_pages=2),
+], ids=lambda c: c.name)
+def test_bwd_irregular_indexes(cuda_dev, case):
+    """Selections in random order with -1 entries anywhere in the row and
+    every fifth (tile, group) row holding only -1 (R7 for all its rows)."""
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    idx = irregular_idx(case, np.random.default_rng(4))
+    got = _run_gpu(case, inp, torch.from_numpy(idx).to(cuda_dev), 0.8)
+    ref = _oracle(case, inp, idx, 0.8)
+    assert np.isneginf(ref["lse"]).any()
+    _check_all(got, ref)
+
+
+def test_bwd_shared_pages(cuda_dev):
+    """Several page-table entries naming one physical page (a shared prefix,
+    and one page listed twice): dK, dV and dpk of that page are the sums over
+    every entry, as the oracle's scatter-add gives them."""
+    case = synth.Case("shared prefix", [256, 300, 129], [512, 600, 384], 8, 2, 128, 2, 64, 3,
+                      page_perm_seed=8, extra_pages=1)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    table = inp["kv_indices"].clone()
+    # entries: seq 0 -> 0..3, seq 1 -> 4..8, seq 2 -> 9..11
+    table[4] = table[0]          # seq 1 block 0 = seq 0 block 0
+    table[5] = table[1]          # seq 1 block 1 = seq 0 block 1
+    table[9] = table[0]          # seq 2 block 0 = the same page again
+    table[11] = table[6]         # seq 2 block 2 = seq 1 block 2
+    inp["kv_indices"] = table
+    idx = random_idx(case, np.random.default_rng(3))
+    # make sure the shared blocks are selected by several sequences
+    tl = O.tiles_of(case.qo_lens, case.kv_lens)
+    for t, tile in enumerate(tl):
+        for g in range(case.hkv):
+            if tile.nvp > 2 and case.topk >= 3:
+                idx[t, g, :3] = sorted({0, 1, tile.nvp - 1}) + [-1] * (3 - len({0, 1, tile.nvp - 1}))
+    got = _run_gpu(case, inp, torch.from_numpy(idx).to(cuda_dev), 1.0)
+    ref = _oracle(case, inp, idx, 1.0)
+    _check_all(got, ref)
 
 
 def test_bwd_unsupported_head_dim(cuda_dev):

@@ -29,3 +29,26 @@ def test_bounded_wait_times_out_and_context_survives(cuda_dev):
     nvp = np.array([1, 10, 20, 39, 40], np.int32)
     got = msa.topk_select(torch.from_numpy(ms).to(cuda_dev), 4, torch.from_numpy(nvp).to(cuda_dev)).cpu().numpy()
     assert np.array_equal(got, O.topk_select(ms, 4, nvp))
+
+
+def test_plan_allocation_failure_is_reported(cuda_dev):
+    """Host-side failure injection: a plan whose device allocation fails
+    returns MSA_ERR_NO_MEMORY with nothing allocated, and the next plan (the
+    injection used up) is built and works."""
+    from block_sparse_long_proxy_gb300 import msa
+    MSA_ERR_NO_MEMORY = 4
+    before = torch.cuda.mem_get_info()[0]
+    msa.inject_plan_alloc_failures(2)
+    try:
+        for _ in range(2):
+            with pytest.raises(msa.MsaError) as e:
+                msa.Plan([256], [256], 4, 2, 2, 128, 64, 2, num_pages=2)
+            assert e.value.status == MSA_ERR_NO_MEMORY and "injected" in str(e.value)
+    finally:
+        msa.inject_plan_alloc_failures(0)
+    assert torch.cuda.mem_get_info()[0] >= before - (1 << 20)
+    plan = msa.Plan([256], [256], 4, 2, 2, 128, 64, 2, num_pages=2)
+    rng = np.random.default_rng(1)
+    ms = torch.from_numpy(rng.standard_normal((plan.n_tiles, 2, plan.max_blocks)).astype(np.float32)).to(cuda_dev)
+    got = msa.topk_select(ms, 2, plan.num_valid_pages).cpu().numpy()
+    assert np.array_equal(got, O.topk_select(ms.cpu().numpy(), 2, O.num_valid_pages([256], [256])))

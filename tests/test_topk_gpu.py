@@ -48,3 +48,20 @@ def test_topk_config_shapes(cuda_dev, n, h, nb):
         ms[t, :, nvp[t]:] = -np.inf
     got = msa.topk_select(torch.from_numpy(ms).to(cuda_dev), 16, torch.from_numpy(nvp).to(cuda_dev)).cpu().numpy()
     assert np.array_equal(got, O.topk_select(ms, 16, nvp))
+
+
+@pytest.mark.parametrize("nb", [8, 600, 2000])
+def test_topk_out_of_range_nvp_selects_nothing(cuda_dev, nb):
+    """num_valid_pages outside [1, max_blocks] is outside the contract: the
+    row is written as all -1 (no clamping to a valid count); the other rows
+    are unaffected."""
+    from block_sparse_long_proxy_gb300 import msa
+    rng = np.random.default_rng(nb)
+    n, h, topk = 6, 2, 5
+    ms = rng.standard_normal((n, h, nb)).astype(np.float32)
+    nvp = np.array([0, -3, nb + 1, nb, 1, 1 << 30], dtype=np.int32)
+    got = msa.topk_select(torch.from_numpy(ms).to(cuda_dev), topk, torch.from_numpy(nvp).to(cuda_dev)).cpu().numpy()
+    for t in (0, 1, 2, 5):
+        assert (got[t] == -1).all(), (t, got[t])
+    good = [3, 4]
+    assert np.array_equal(got[good], O.topk_select(ms[good], topk, nvp[good]))

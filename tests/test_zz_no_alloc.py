@@ -57,7 +57,43 @@ def test_noalloc_rejects_oversized_batch(cuda_dev):
     """batch * num_qo_heads * topk above the static scratch's capacity is
     refused on the host before any work is enqueued."""
     from block_sparse_long_proxy_gb300 import msa
-    b, hq, hkv, topk = 64, 64, 8, 16          # 65536 > 48143 partial rows
+    b, hq, hkv, topk = 64, 64, 8, 16          # 65536 > 47,639 partial rows
+    q = torch.zeros((b, hq, 128), dtype=torch.bfloat16, device=cuda_dev)
+    kp = torch.zeros((8, hkv, 128, 128), dtype=torch.float8_e4m3fn, device=cuda_dev)
+    lens = torch.full((b,), 128, dtype=torch.int32, device=cuda_dev)
+    indptr = torch.arange(b + 1, dtype=torch.int32, device=cuda_dev)
+    table = torch.zeros((b,), dtype=torch.int32, device=cuda_dev)
+    idx = torch.zeros((b, hkv, topk), dtype=torch.int32, device=cuda_dev)
+    sc = torch.ones(hkv, dtype=torch.float32, device=cuda_dev)
+    with pytest.raises(msa.MsaError) as e:
+        msa.sparse_decode_noalloc(q, kp, kp, lens, indptr, table, idx, sc, sc)
+    assert e.value.status == 1 and "static scratch" in str(e.value)
+
+
+def test_noalloc_capacity_boundary(cuda_dev):
+    """The capacity is 47,639 partial rows (batch * num_qo_heads * topk) at
+    head_dim 128.  47,639 is prime, so the largest product a valid shape can
+    reach is 47,637 = 67 * 9 * 79: it runs and matches the planned decode;
+    47,640 = 40 * 3 * 397 is refused."""
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("67 x 12800, 9/1 heads, topk 79", [1] * 67, [12800] * 67, 9, 1, 128, 1, 64, 79,
+                      kv_dtype="e4m3", page_perm_seed=3)
+    assert 67 * 9 * 79 == 47637
+    inp = synth.make_inputs(case, device=cuda_dev)
+    plan = make_plan(case, inp)
+    lens, indptr = _batch_arrays(case, cuda_dev)
+    idx = torch.from_numpy(random_idx(case, np.random.default_rng(7))).to(cuda_dev)
+    ref, _ = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx,
+                              k_scale=inp["k_scale"], v_scale=inp["v_scale"])
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_dev)
+    out, _ = msa.sparse_decode_noalloc(inp["q"], inp["k_pages"], inp["v_pages"], lens, indptr, inp["kv_indices"],
+                                       idx, inp["k_scale"], inp["v_scale"], err_word=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert (out.float() - ref.float()).abs().max().item() <= O_ATOL_FP8
+
+    b, hq, hkv, topk = 40, 3, 1, 397
+    assert b * hq * topk == 47640
     q = torch.zeros((b, hq, 128), dtype=torch.bfloat16, device=cuda_dev)
     kp = torch.zeros((8, hkv, 128, 128), dtype=torch.float8_e4m3fn, device=cuda_dev)
     lens = torch.full((b,), 128, dtype=torch.int32, device=cuda_dev)

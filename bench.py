@@ -419,6 +419,7 @@ def run_ours(args):
 
     decode = bench_decode(args, dev, pk_info, peak_kind, world)
     train = bench_train(args, dev, pk_info, peak_kind)
+    fp8_prefill = bench_prefill_fp8(args, dev, pk_info, peak_kind, attn_tflops)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -438,6 +439,8 @@ def run_ours(args):
             "gpu_launches": 3 * args.steps,
             "clocks": clk.summary(),
             "wall_s": t_wall}
+    if fp8_prefill:
+        line["prefill_fp8"] = fp8_prefill
     if decode:
         line["decode"] = decode
     if train:
@@ -481,6 +484,54 @@ def cpu_baseline(case):
     return {"value": rows / dt, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
             "sample": "%d random 128-row query tiles of the same workload through the whole fp64 oracle chain "
                       "(proxy max-score, top-k, attention), %.1f s" % (len(ids), dt)}
+
+
+def bench_prefill_fp8(args, dev, pk_info, peak_kind, bf16_tflops):
+    """The S=32768 prefill attention with e4m3 K/V (per-KV-head scales):
+    msa_sparse_attn on the selections of its own proxy and top-k, TFLOP/s
+    counted on the selected blocks, beside the bf16 figure."""
+    import torch
+    from block_sparse_long_proxy_gb300 import msa, synth
+    case = synth.prefill_32k()
+    case.kv_dtype = "e4m3"
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype="e4m3")
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    out = torch.empty_like(inp["q"])
+    lse = torch.empty((plan.total_q, case.hq), dtype=torch.float32, device=dev)
+
+    def attn():
+        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx,
+                         k_scale=inp["k_scale"], v_scale=inp["v_scale"], out=out, lse=lse)
+    for _ in range(max(3, args.warmup)):
+        attn()
+    torch.cuda.synchronize()
+    plan.check_errors()
+    flops, n_sel = selected_flops(idx.cpu().numpy(), case)
+    flush = L2Flush(dev)
+    stream = torch.cuda.current_stream()
+    times = []
+    for _ in range(max(10, min(args.steps, 200))):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        attn()
+        b.record(stream)
+        times.append((a, b))
+    torch.cuda.synchronize()
+    plan.check_errors()
+    ms_ = statistics.mean(a.elapsed_time(b) for a, b in times)
+    tf = flops / (ms_ / 1e3) / 1e12
+    peak = pk_info.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    del inp
+    return {"workload": "sparse prefill S=32768, e4m3 K/V", "sparse_attn_ms": ms_, "tflops_selected": tf,
+            "vs_bf16": tf / bf16_tflops,
+            "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128, fp8> (msa_sparse_attn)", "achieved": tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": "%s bf16 dense burst (cuBLAS); the MMAs run f16 at the same rate" % peak_kind},
+            "kv_bytes_read": n_sel * 2 * 128 * case.d}
 
 
 def bench_decode(args, dev, pk_info, peak_kind, world):

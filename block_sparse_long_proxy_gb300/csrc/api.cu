@@ -309,13 +309,11 @@ msa_status msa_sparse_attn(msa_plan_t plan, const void* q, const void* k_pages, 
   if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr))
     return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn: k_scale/v_scale must be given exactly for FP8 K/V");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (fp8) {
-    if (!plan->decode)
-      return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 K/V is implemented for decode batches only");
+  if (fp8 && plan->decode)
     return launch_attn_decode(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale, out,
                               lse, st);
-  }
-  return launch_attn_prefill(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, st);
+  return launch_attn_prefill(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale, out, lse,
+                             st);
 }
 
 msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pages, const void* v_pages,

@@ -1,4 +1,4 @@
-// Stage 3 (prefill): GQA block-sparse flash attention forward with bf16 K/V.
+// Stage 3 (prefill): GQA block-sparse flash attention forward, bf16 or FP8 K/V.
 //
 // For query row i of tile t and head h (group g = h / G): softmax over the
 // keys of the selected blocks kv_block_indexes[t, g, :] that are visible to
@@ -26,6 +26,19 @@
 // Online softmax in the log2 domain; the O rescale runs in the softmax
 // warps between P.V steps, and the epilogue releases O_h to the next unit
 // as soon as it is in registers.
+//
+// FP8 K/V ("MiniMax-AI/MSA" README, section "Stacks": sparse prefill in FP8
+// next to BF16).  K/V pages hold e4m3 codes with one fp32 scale per KV
+// head: logit = (q . k_code) * k_scale / sqrt(d), v = v_code * v_scale.  The
+// producer gathers the 16 KB code blocks by TMA into the upper half of the
+// K / V ring stages, and two converter warps (warps 10-11) expand them in
+// place to f16 (exact: every e4m3 value is an f16) in the 128-byte-swizzled
+// layout the MMAs read, and convert each unit's Q tiles in place from bf16
+// to f16.  The MMAs then run kind::f16 with f16 operands (Q, K, P and V),
+// k_scale folds into the softmax scale and v_scale into the epilogue.
+// Rounding: Q to f16 is exact for |q| in [2^-14, 65504] (smaller values
+// lose at most 2^-25, larger ones saturate) and P is rounded to f16 instead
+// of bf16.
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -36,8 +49,9 @@ namespace {
 
 constexpr int kStages = 2;
 constexpr int kSoftWarps = 8;
-constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kConvWarps = 2;  // FP8 K/V only
 constexpr int kMaxTopk = 1024;
+__host__ __device__ constexpr int attn_threads(bool fp8) { return 32 * (kSoftWarps + 2 + (fp8 ? kConvWarps : 0)); }
 
 struct AttnUnit {
   int32_t tile, g, h0, nh;
@@ -51,7 +65,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 // One unit's cached blocks, built once by the producer warp (its lanes read
 // the top-k row and the page table in parallel) for the MMA and softmax warps.
 struct UnitList {
-  int32_t n, nh, h0, q_begin, rows, pos0, pad[10];
+  int32_t n, nh, h0, q_begin, rows, pos0, g, pad[9];
   int32_t j[kMaxTopk];    // selected blocks, padding and out-of-range entries dropped
   int32_t row[kMaxTopk];  // their first K/V tensor-map row
 };
@@ -73,16 +87,17 @@ struct AttnSmem {
 // barrier's phase comes from a running count (per head for the S / P / O
 // barriers), and Q is released right after a unit's last QK so the next
 // unit's Q load overlaps the tail of the current one.
-template <int D, bool kOneKvHead>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, bool kOneKvHead, bool kFp8>
+__global__ void __launch_bounds__(attn_threads(kFp8), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
-                    uint32_t* err) {
+                    const float* __restrict__ k_scale, const float* __restrict__ v_scale, uint32_t* err) {
   using L = AttnSmem<D>;
   constexpr int kChunks = D / 64;
+  static_assert(!kFp8 || (D == 128 && !kOneKvHead), "FP8 K/V: head_dim 128, main attention");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem + L::kQOff;
@@ -101,7 +116,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* list_full = o_free + 2;       // [kListSlots]
   uint64_t* list_empty = list_full + kListSlots;
   uint64_t* drain = list_empty + kListSlots;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* raw_full = drain + 1;          // [kStages], FP8: e4m3 K and V codes landed
+  uint64_t* q_ready = raw_full + kStages;  // FP8: Q converted to f16
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -111,9 +128,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full + s, 1);
+      mbar_init(kv_full + s, kFp8 ? kConvWarps : 1);
       mbar_init(kv_empty + s, 1);
+      mbar_init(raw_full + s, 1);
     }
+    mbar_init(q_ready, kConvWarps);
     for (int h = 0; h < 2; ++h) {
       mbar_init(s_full + h, 1);
       mbar_init(p_full + h, 4);
@@ -122,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kListSlots; ++i) {
       mbar_init(list_full + i, 1);
-      mbar_init(list_empty + i, 1 + kSoftWarps);  // the MMA thread and every softmax warp
+      mbar_init(list_empty + i, 1 + kSoftWarps + (kFp8 ? kConvWarps : 0));  // MMA thread, softmax (and converter) warps
     }
     mbar_init(drain, 1);
     fence_mbar_init();
@@ -182,6 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ls.q_begin = tl.q_begin;
         ls.rows = tl.rows;
         ls.pos0 = tl.pos0;
+        ls.g = u.g;
       }
       __syncwarp();
       if (lane == 0) {
@@ -197,6 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = kv_it % kStages;
           if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
           const int row = ls.row[i];
+          if (kFp8) {  // e4m3 codes into the upper half of the stage; the converters expand them
+            mbar_expect_tx(raw_full + s, 2 * 16384);
+            tma_load_2d(k_s + s * L::kTileBytes + 16384, &k_map, raw_full + s, 0, row);
+            tma_load_2d(v_s + s * L::kTileBytes + 16384, &v_map, raw_full + s, 0, row);
+            continue;
+          }
           // a one-head pool's keys are its values: one load serves both
           mbar_expect_tx(kv_full + s, (kOneKvHead ? 1 : 2) * L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
@@ -217,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a block share one barrier, O_h's barrier is committed once per unit
       // (a block's S_h commit already covers the previous P_h.V), and the
       // per-head phase counters are scalars.
-      constexpr uint32_t id_qk = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, D, false, true);
+      constexpr uint32_t id_qk = kFp8 ? idesc_f16_f32(128, 128, false, false) : idesc_bf16_f32(128, 128, false, false);
+      constexpr uint32_t id_pv = kFp8 ? idesc_f16_f32(128, D, false, true) : idesc_bf16_f32(128, D, false, true);
       constexpr uint64_t kTileDesc = L::kTileBytes >> 4;
       const uint64_t qd0 = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128);
       const uint64_t kd0 = smem_desc(smem_u32(k_s), 16, 1024, kSwizzle128);
@@ -245,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = lists[k % kListSlots].n;
         const bool two = lists[k % kListSlots].nh == 2;
         mbar_arrive(list_empty + k % kListSlots);
-        if (!(ok = mbar_wait(q_full, k & 1, err))) break;
+        if (!(ok = mbar_wait(kFp8 ? q_ready : q_full, k & 1, err))) break;
         tc_fence_after();
         if (n == 0) {
           mma_commit(q_empty);
@@ -297,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, err);
     }
-  } else {
+  } else if (warp < kSoftWarps) {
     // ----------------------------------------------------------- softmax
     const int h = warp >> 2;
     const int quarter = warp & 3;
@@ -313,6 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xFFFFFFFFu, ok);
       const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
       const int rows = ls.rows, pos0 = ls.pos0;
+      // FP8: the scores are q . k_code, scaled by k_scale of the unit's KV head
+      const float sl2 = kFp8 ? scale_log2 * k_scale[ls.g] : scale_log2;
+      const float o_scale = kFp8 ? v_scale[ls.g] : 1.f;
       const bool active = ok && h < nh;
       bool o_released = false;
       const bool row_ok = r < rows;
@@ -348,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lazy rescaling: the reference max moves only when the row max grows
         // by more than 2^8, so probabilities stay below 256 and O is rescaled
         // rarely
-        const float mx2 = mx * scale_log2;
+        const float mx2 = mx * sl2;
         const float m_new = mx2 > m + 8.f ? mx2 : m;
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = m_new == m ? 1.f : ex2_approx(m - m_use);
@@ -357,13 +386,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           float x0, x1;
-          ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), scale_log2, -m_use);
+          ffma2(x0, x1, __uint_as_float(sv[2 * c]), __uint_as_float(sv[2 * c + 1]), sl2, -m_use);
           const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (c & 1)
             fadd2(sum2, sum3, p0, p1);
           else
             fadd2(sum0, sum1, p0, p1);
-          pk[c] = pack_bf16x2(p0, p1);
+          pk[c] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
         }
         sum0 += sum2;
         sum1 += sum3;
@@ -395,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (n > 0) ok = mbar_wait(o_done + h, (od++) & 1, err);
         tc_fence_after();
         const int64_t orow = static_cast<int64_t>(ls.q_begin + r) * hq + ls.h0 + h;
-        const float inv_l = l > 0.f ? 1.f / l : 0.f;
+        const float inv_l = l > 0.f ? o_scale / l : 0.f;
         // all of O_h in one round of loads; O_h is then released to the next
         // unit's P.V before the stores
         uint32_t ov[D];
@@ -436,6 +465,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(list_empty + k % kListSlots);
       }
     }
+  } else if (kFp8) {
+    // -------------------------------------------------- FP8 converters
+    // Thread ct of the two warps owns rows ct and ct + 64 of every K / V
+    // block: it reads a row's 128 e4m3 codes (eight 16-byte units of the
+    // swizzled upper half of the stage) before it writes any of the row's
+    // f16 units, and the only f16 units that land in that upper half are the
+    // same row's, so no other thread's codes are overwritten.
+    const int ct = threadIdx.x - 32 * (kSoftWarps + 2);
+    auto expand = [&](uint8_t* buf) {  // buf: one ring stage, 2 chunks x [128 rows][128 B] of f16
+#pragma unroll 1
+      for (int rr = 0; rr < 2; ++rr) {
+        const int r = ct + 64 * rr, sw = r & 7;
+        const uint8_t* raw = buf + 16384 + r * 128;
+        uint4 u[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) u[c] = *reinterpret_cast<const uint4*>(raw + ((c ^ sw) << 4));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {  // codes of d in [16c, 16c + 16) -> two f16 units
+          uint4 lo, hi;
+          lo.x = e4m3x2_to_f16x2(u[c].x);
+          lo.y = e4m3x2_to_f16x2(u[c].x >> 16);
+          lo.z = e4m3x2_to_f16x2(u[c].y);
+          lo.w = e4m3x2_to_f16x2(u[c].y >> 16);
+          hi.x = e4m3x2_to_f16x2(u[c].z);
+          hi.y = e4m3x2_to_f16x2(u[c].z >> 16);
+          hi.z = e4m3x2_to_f16x2(u[c].w);
+          hi.w = e4m3x2_to_f16x2(u[c].w >> 16);
+          uint8_t* dst = buf + (c >> 2) * 16384 + r * 128;
+          const int u0 = (c & 3) * 2;
+          *reinterpret_cast<uint4*>(dst + ((u0 ^ sw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((u0 + 1) ^ sw) << 4)) = hi;
+        }
+      }
+    };
+    int kv_it = 0;
+    bool ok = true;
+    for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
+      const UnitList& ls = lists[k % kListSlots];
+      ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      const int n = ls.n, nh = ls.nh;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(list_empty + k % kListSlots);
+      // Q of the unit's heads, bf16 -> f16 in place
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(q_full, k & 1, err)))) break;
+      for (int hh = 0; hh < nh; ++hh) {
+        uint4* qv = reinterpret_cast<uint4*>(q_s + hh * L::kTileBytes);
+#pragma unroll 4
+        for (int e = ct; e < L::kTileBytes / 16; e += 32 * kConvWarps) {
+          uint4 v = qv[e];
+          v.x = bf16x2_to_f16x2(v.x);
+          v.y = bf16x2_to_f16x2(v.y);
+          v.z = bf16x2_to_f16x2(v.z);
+          v.w = bf16x2_to_f16x2(v.w);
+          qv[e] = v;
+        }
+      }
+      fence_async_shared();  // the MMAs read these through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+      for (int i = 0; i < n; ++i, ++kv_it) {
+        const int s = kv_it % kStages;
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + s, (kv_it / kStages) & 1, err)))) break;
+        expand(k_s + s * L::kTileBytes);
+        expand(v_s + s * L::kTileBytes);
+        fence_async_shared();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kv_full + s);
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -473,37 +573,48 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
 }
 
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
-                               const int32_t* kv_indices, const int32_t* idx, void* out, float* lse,
-                               cudaStream_t st) {
+                               const int32_t* kv_indices, const int32_t* idx, const float* k_scale,
+                               const float* v_scale, void* out, float* lse, cudaStream_t st) {
   if (p->topk > kMaxTopk) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: topk above 1024");
+  const bool fp8 = p->kv_dtype == MSA_KV_FP8_E4M3;
+  if (fp8 && p->d != 128)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 K/V prefill needs head_dim 128");
   CUtensorMap qm, km, vm;
   const uint64_t qdims[3] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->hq),
                              static_cast<uint64_t>(p->total_q)};
   const uint64_t qstr[2] = {static_cast<uint64_t>(p->d) * 2, static_cast<uint64_t>(p->hq) * p->d * 2};
   const uint32_t qbox[3] = {64, 1, 128};
+  const int kv_elem = fp8 ? 1 : 2;
   const uint64_t kdims[2] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
-  const uint64_t kstr[1] = {static_cast<uint64_t>(p->d) * 2};
-  const uint32_t kbox[2] = {64, 128};
+  const uint64_t kstr[1] = {static_cast<uint64_t>(p->d) * kv_elem};
+  // bf16: 64-column boxes (128 B rows); e4m3: whole 128-byte rows of codes
+  const uint32_t kbox[2] = {fp8 ? 128u : 64u, 128};
   if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
-      !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
-      !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, 1, 128))
+      !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, fp8 ? 0 : 1, 128) ||
+      !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, fp8 ? 0 : 1, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
   const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->attn_units_off);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->d));
   auto* o = static_cast<__nv_bfloat16*>(out);
   const int grid = std::min(p->n_attn_units, p->num_sms);  // persistent: one CTA per SM
-  if (p->d == 128) {
+  if (fp8) {
     const int smem = AttnSmem<128>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<128, false><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx,
-                                                              kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-                                                              scale_log2, p->err_d);
+    cudaFuncSetAttribute(attn_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<128, false, true><<<grid, attn_threads(true), smem, st>>>(
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+        scale_log2, k_scale, v_scale, p->err_d);
+  } else if (p->d == 128) {
+    const int smem = AttnSmem<128>::kBytes + 1024;
+    cudaFuncSetAttribute(attn_fwd_kernel<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<128, false, false><<<grid, attn_threads(false), smem, st>>>(
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+        scale_log2, nullptr, nullptr, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<64, false><<<grid, kThreads, smem, st>>>(qm, km, vm, units, p->n_attn_units, p->tiles_d, idx,
-                                                             kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-                                                             scale_log2, p->err_d);
+    cudaFuncSetAttribute(attn_fwd_kernel<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attn_fwd_kernel<64, false, false><<<grid, attn_threads(false), smem, st>>>(
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
+        scale_log2, nullptr, nullptr, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
 }
@@ -532,10 +643,10 @@ msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void*
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // 1 / sqrt(64)
   const int grid = std::min(p->n_proxy_attn_units, p->num_sms);
   const int smem = AttnSmem<64>::kBytes + 1024;
-  cudaFuncSetAttribute(attn_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  attn_fwd_kernel<64, true><<<grid, kThreads, smem, st>>>(qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx,
-                                                          kv_indices, p->num_pages, static_cast<__nv_bfloat16*>(op),
-                                                          lse, p->hp, p->hkv, p->topk, scale_log2, p->err_d);
+  cudaFuncSetAttribute(attn_fwd_kernel<64, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  attn_fwd_kernel<64, true, false><<<grid, attn_threads(false), smem, st>>>(
+      qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx, kv_indices, p->num_pages,
+      static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: proxy softmax launch");
 }
 

@@ -128,7 +128,8 @@ msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const vo
 
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages,
                                const void* v_pages, const int32_t* kv_indices, const int32_t* idx,
-                               void* out, float* lse, cudaStream_t st);
+                               const float* k_scale, const float* v_scale, void* out, float* lse,
+                               cudaStream_t st);
 // one CTA per (sequence, group) row with warp-private half-block streams
 // (decode_ws.cu); used by launch_attn_decode when decode_ws_applies(p)
 bool decode_ws_applies(const msa_plan_s* p);

@@ -84,18 +84,6 @@ def test_bf16_decode_batch(cuda_dev):
            cuda_dev)
 
 
-def test_fp8_prefill_rejected(cuda_dev):
-    from block_sparse_long_proxy_gb300 import msa
-    case = synth.Case("fp8 prefill", [256], [256], 8, 2, 128, 2, 64, 2, kv_dtype="e4m3")
-    inp = synth.make_inputs(case, device=cuda_dev)
-    plan = make_plan(case, inp)
-    idx = torch.from_numpy(random_idx(case, np.random.default_rng(0))).to(cuda_dev)
-    with pytest.raises(msa.MsaError) as e:
-        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx,
-                         k_scale=inp["k_scale"], v_scale=inp["v_scale"])
-    assert e.value.status == 2
-
-
 def test_paged_decode_full_size_sampled(cuda_dev):
     """32 sequences x 131072 keys, 64/8 heads, topk 16: the whole chain on
     the GPU, the oracle on sampled sequences (indices with the gap rule,

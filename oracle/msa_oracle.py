@@ -53,6 +53,13 @@ Readings where the pages are silent:
       selected, or when its selection row holds only -1) has O = 0 and
       LSE = -inf; in the backward its P and p_proxy are 0, so its KL term,
       dZ and every gradient it sends are 0.
+  R8  several proxy heads per GQA group: with Hp = m * Hkv proxy heads (m >=
+      1, Hq divisible by Hp) each proxy head picks its own block set, and
+      the G = Hq/Hkv query heads of a GQA group are split into m equal
+      "MSA groups" of Hq/Hp consecutive heads: query head h attends over the
+      blocks kv_block_indexes[t, h // (Hq/Hp)] of KV head h // (Hq/Hkv), and
+      proxy head p = h // (Hq/Hp) distils the mean distribution of its own
+      Hq/Hp heads.  m = 1 is one proxy head per GQA group.
   R11 an FP8 e4m3 proxy K (decode) carries one fp32 scale for the single
       shared proxy head, dequantised like R5: logit =
       (pq.pk_code)*pk_scale/sqrt(dp).
@@ -228,11 +235,12 @@ def _decode_kv(bits, fp8: bool):
 
 def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
                      k_scale=None, v_scale=None, tile_ids=None):
-    """For query i of tile t and head h (group g = h // G): softmax over the
-    keys of the blocks kv_block_indexes[t, g, :] that are visible to i of
-    q.k/sqrt(d), O = P.V, LSE = ln sum exp.  bf16 K/V, or e4m3 K/V with
-    per-KV-head scales when k_scale/v_scale are given.  Returns (O, LSE) in
-    float64; rows of tiles not in tile_ids are NaN."""
+    """For query i of tile t and head h (KV head g = h // (Hq/Hkv), proxy
+    head p = h // (Hq/Hp), R8): softmax over the keys of the blocks
+    kv_block_indexes[t, p, :] that are visible to i of q.k_g/sqrt(d),
+    O = P.V_g, LSE = ln sum exp.  Hp is kv_block_indexes.shape[1].  bf16
+    K/V, or e4m3 K/V with per-KV-head scales when k_scale/v_scale are given.
+    Returns (O, LSE) in float64; rows of tiles not in tile_ids are NaN."""
     fp8 = k_scale is not None
     q_bits, k_bits, v_bits = np.asarray(q_bits), np.asarray(k_bits), np.asarray(v_bits)
     tiles = tiles_of(qo_lens, kv_lens)
@@ -240,6 +248,9 @@ def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_le
     hq, d = q_bits.shape[1], q_bits.shape[2]
     hkv = k_bits.shape[1]
     grp = hq // hkv
+    hs = kv_block_indexes.shape[1]                     # proxy heads = block sets per tile
+    assert hs % hkv == 0 and hq % hs == 0
+    msa_grp = hq // hs                                 # query heads per proxy head
     o = np.full(q_bits.shape, np.nan)
     lse = np.full(q_bits.shape[:2], np.nan)
     for ti in (range(len(tiles)) if tile_ids is None else tile_ids):
@@ -251,7 +262,7 @@ def sparse_attention(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, qo_le
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
         for h in range(hq):
             g = h // grp
-            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+            ks = _selected_keys(tl, kv_block_indexes[ti, h // msa_grp])
             kmat = _decode_kv(kseq[ks, g, :], fp8)
             vmat = _decode_kv(vseq[ks, g, :], fp8)
             if fp8:
@@ -305,7 +316,9 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
     indptr = kv_indptr(kv_lens)
     hq, d = q.shape[1], q.shape[2]
     hkv = kp.shape[1]
-    grp = hq // hkv
+    hs = pq.shape[1]                                   # proxy heads (R8)
+    assert kv_block_indexes.shape[1] == hs and hs % hkv == 0 and hq % hs == 0
+    msa_grp = hq // hs                                 # query heads per proxy head
     dp = pq.shape[2]
     dq = np.full(q.shape, np.nan)
     dpq = np.full(pq.shape, np.nan)
@@ -323,8 +336,9 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
         vseq = gather_seq(vp, kv_indices, indptr, tl.seq, tl.kv_len)
         pkseq = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
-        for g in range(hkv):
-            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+        for hp_ in range(hs):
+            g = hp_ // (hs // hkv)                       # KV head of proxy head hp_
+            ks = _selected_keys(tl, kv_block_indexes[ti, hp_])
             vis = ks[None, :] <= qpos[:, None]
             # R7: a row that sees no selected key has P = 0, O = 0, LSE = -inf,
             # and so no gradient; its proxy distribution is empty as well
@@ -334,7 +348,7 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
             dkmat = np.zeros_like(kmat)
             dvmat = np.zeros_like(vmat)
             p_main = np.zeros(vis.shape)
-            for h in range(g * grp, (g + 1) * grp):
+            for h in range(hp_ * msa_grp, (hp_ + 1) * msa_grp):
                 s = np.where(vis, q[rows, h, :] @ kmat.T / math.sqrt(d), -np.inf)
                 p, lse_h = _masked_softmax(s, empty)                    # [R, n], [R, 1]
                 oh = p @ vmat
@@ -347,13 +361,13 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
                 dq[rows, h, :] = dS @ kmat / math.sqrt(d)
                 dkmat += dS.T @ q[rows, h, :] / math.sqrt(d)
                 dvmat += p.T @ dov
-                p_main += p / grp
+                p_main += p / msa_grp
             # proxy distribution over the same selected, visible keys
-            z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
+            z = np.where(vis, pq[rows, hp_, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
             p_proxy, _ = _masked_softmax(z, empty)
             dz = kl_weight * (p_proxy - p_main)
-            dpq[rows, g, :] = dz @ pkseq[ks] / math.sqrt(dp)
-            dpk_keys = dz.T @ pq[rows, g, :] / math.sqrt(dp)            # [n, dp]
+            dpq[rows, hp_, :] = dz @ pkseq[ks] / math.sqrt(dp)
+            dpk_keys = dz.T @ pq[rows, hp_, :] / math.sqrt(dp)          # [n, dp]
             # scatter per-key gradients back to physical pages
             pg = page_ids[ks // PAGE]
             np.add.at(dk, (pg, g, ks % PAGE), dkmat)
@@ -364,7 +378,7 @@ def sparse_attention_bwd(q_bits, k_bits, v_bits, kv_indices, kv_block_indexes, q
 
 def kl_objective(pq, pk, q_bits, k_bits, kv_indices, kv_block_indexes, qo_lens, kv_lens,
                  kl_weight=1.0):
-    """w * sum over rows and groups of KL(p_main || p_proxy) as a function of
+    """w * sum over rows and proxy heads of KL(p_main || p_proxy) as a function of
     float64 proxy inputs pq [total_q,Hp,dp], pk [P,1,128,dp], with p_main
     from the bf16 main q/k (held fixed).  Used to pin the closed-form proxy
     gradient by finite differences."""
@@ -374,7 +388,8 @@ def kl_objective(pq, pk, q_bits, k_bits, kv_indices, kv_block_indexes, qo_lens, 
     indptr = kv_indptr(kv_lens)
     hq, d = q.shape[1], q.shape[2]
     hkv = kp.shape[1]
-    grp = hq // hkv
+    hs = pq.shape[1]
+    msa_grp = hq // hs
     dp = pq.shape[2]
     total = 0.0
     for ti, tl in enumerate(tiles):
@@ -382,15 +397,16 @@ def kl_objective(pq, pk, q_bits, k_bits, kv_indices, kv_block_indexes, qo_lens, 
         kseq = gather_seq(kp, kv_indices, indptr, tl.seq, tl.kv_len)
         pkseq = gather_seq(pk, kv_indices, indptr, tl.seq, tl.kv_len)[:, 0, :]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)
-        for g in range(hkv):
-            ks = _selected_keys(tl, kv_block_indexes[ti, g])
+        for hp_ in range(hs):
+            g = hp_ // (hs // hkv)
+            ks = _selected_keys(tl, kv_block_indexes[ti, hp_])
             vis = ks[None, :] <= qpos[:, None]
             empty = ~vis.any(axis=1, keepdims=True)        # R7 rows contribute nothing
             p_main = np.zeros(vis.shape)
-            for h in range(g * grp, (g + 1) * grp):
+            for h in range(hp_ * msa_grp, (hp_ + 1) * msa_grp):
                 s = np.where(vis, q[rows, h, :] @ kseq[ks, g, :].T / math.sqrt(d), -np.inf)
-                p_main += _masked_softmax(s, empty)[0] / grp
-            z = np.where(vis, pq[rows, g, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
+                p_main += _masked_softmax(s, empty)[0] / msa_grp
+            z = np.where(vis, pq[rows, hp_, :] @ pkseq[ks].T / math.sqrt(dp), -np.inf)
             _, lse_z = _masked_softmax(z, empty)
             with np.errstate(divide="ignore", invalid="ignore"):
                 log_pp = z - lse_z

@@ -15,12 +15,12 @@ GAP = 1e-3
 
 
 def random_idx(case, rng):
-    """Valid kv_block_indexes: the diagonal block plus topk-1 random others,
-    ascending, -1 padded."""
+    """Valid kv_block_indexes, one row per proxy head: the diagonal block plus
+    topk-1 random others, ascending, -1 padded."""
     tl = O.tiles_of(case.qo_lens, case.kv_lens)
-    idx = np.full((len(tl), case.hkv, case.topk), -1, np.int32)
+    idx = np.full((len(tl), case.hp, case.topk), -1, np.int32)
     for t, tile in enumerate(tl):
-        for g in range(case.hkv):
+        for g in range(case.hp):
             others = rng.permutation(tile.nvp - 1)[: case.topk - 1]
             sel = sorted(list(others) + [tile.nvp - 1])
             idx[t, g, :len(sel)] = sel

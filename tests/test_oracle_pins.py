@@ -237,7 +237,7 @@ def _dense_route(inp, case, idx, fp8=False):
             g = h // grp
             sel = torch.zeros(ql, kl, dtype=torch.bool)
             for r in range(ql):
-                for j in idx[t0 + r // 128, g]:
+                for j in idx[t0 + r // 128, h // (case.hq // idx.shape[1])]:
                     if j >= 0:
                         sel[r, j * PAGE:(j + 1) * PAGE] = True
             o[:, h] = F.scaled_dot_product_attention(q[q0:q0 + ql, h][None], ks[g][None],
@@ -250,10 +250,11 @@ def _dense_route(inp, case, idx, fp8=False):
 
 
 def _rand_idx(case, rng):
+    """Random valid selections, one row per proxy head (R8)."""
     tl = O.tiles_of(case.qo_lens, case.kv_lens)
-    idx = np.full((len(tl), case.hkv, case.topk), -1, np.int32)
+    idx = np.full((len(tl), case.hp, case.topk), -1, np.int32)
     for t, tile in enumerate(tl):
-        for g in range(case.hkv):
+        for g in range(case.hp):
             others = rng.permutation(tile.nvp - 1)[: case.topk - 1]
             sel = sorted(list(others) + [tile.nvp - 1])
             idx[t, g, :len(sel)] = sel
@@ -344,10 +345,12 @@ def _autograd_route(inp, case, idx, w):
         pks = torch.cat([pk[table[p0 + j], 0] for j in range(nb)], 0)[:kl]
         qpos = (kl - ql) + torch.arange(ql)
         vis = torch.arange(kl)[None, :] <= qpos[:, None]
-        for g in range(case.hkv):
+        msa_grp = case.hq // case.hp                 # query heads per proxy head (R8)
+        for p in range(case.hp):
+            g = p // (case.hp // case.hkv)
             sel = torch.zeros(ql, kl, dtype=torch.bool)
             for r in range(ql):
-                for j in idx[t0 + r // 128, g]:
+                for j in idx[t0 + r // 128, p]:
                     if j >= 0:
                         sel[r, j * PAGE:(j + 1) * PAGE] = True
             # rows that see no selected key (R7) are left out of both losses:
@@ -356,13 +359,13 @@ def _autograd_route(inp, case, idx, w):
             rows = torch.arange(q0, q0 + ql)[live]
             m = (vis & sel)[live]
             pmain = 0.0
-            for h in range(g * grp, (g + 1) * grp):
+            for h in range(p * msa_grp, (p + 1) * msa_grp):
                 qh = q[rows, h]
                 oh = F.scaled_dot_product_attention(qh[None], ks[g][None], vs[g][None], attn_mask=m[None])[0]
                 loss_main = loss_main + (oh * do[rows, h]).sum()
                 s = (qh @ ks[g].T / math.sqrt(case.d)).masked_fill(~m, -math.inf)
-                pmain = pmain + torch.softmax(s, -1).detach() / grp
-            z = (pq[rows, g] @ pks.T / math.sqrt(case.dp)).masked_fill(~m, -math.inf)
+                pmain = pmain + torch.softmax(s, -1).detach() / msa_grp
+            z = (pq[rows, p] @ pks.T / math.sqrt(case.dp)).masked_fill(~m, -math.inf)
             logp = torch.log_softmax(z, -1).masked_fill(~m, 0.0)
             loss_kl = loss_kl + w * F.kl_div(logp, pmain, reduction="sum")
         q0 += ql
@@ -608,3 +611,80 @@ def test_proxy_max_dominates_visible_pairs():
         h = int(rng.integers(0, 2))
         logit = float(pq[i, h] @ pk[table[k // PAGE], k % PAGE]) / math.sqrt(case.dp)
         assert logit <= float(ms[i // 128, h, k // PAGE]) * (1 + 1e-6) + 1e-6
+
+
+# ------------------------------------- several proxy heads per group (R8) --
+
+def _hp2_case(**kw):
+    """Hp = 2 Hkv: two proxy heads (two block sets) per GQA group of 4."""
+    return synth.Case("hp2", kw.get("qo", [300, 129]), kw.get("kv", [460, 129]), 8, 2, 64, 4, 32,
+                      kw.get("topk", 2), page_perm_seed=3, extra_pages=1)
+
+
+def test_hp2_attention_vs_library():
+    """Each query head attends over its own proxy head's blocks: the oracle
+    equals torch's attention with the per-head block mask."""
+    case = _hp2_case()
+    inp = _mk(case)
+    idx = _rand_idx(case, np.random.default_rng(21))
+    assert idx.shape[1] == 4
+    o, _ = O.sparse_attention(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                              inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens)
+    ref = _dense_route(inp, case, idx)
+    np.testing.assert_allclose(o, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_hp2_attention_reduces_to_one_proxy_head_per_group():
+    """With Hp = 2 Hkv, head h of group g gives what the one-proxy-head
+    attention gives when group g's block set is proxy head 2g + s's, s the
+    half of the group h sits in: heads 0-1 of a group of 4 use s = 0,
+    heads 2-3 use s = 1."""
+    case = _hp2_case()
+    inp = _mk(case)
+    idx = _rand_idx(case, np.random.default_rng(22))
+    args = (synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+            inp["kv_indices"].numpy())
+    o2, l2 = O.sparse_attention(*args, idx, case.qo_lens, case.kv_lens)
+    for s in range(2):
+        o1, l1 = O.sparse_attention(*args, np.ascontiguousarray(idx[:, s::2]), case.qo_lens, case.kv_lens)
+        for h in range(case.hq):
+            if (h % 4) // 2 == s:
+                np.testing.assert_array_equal(o2[:, h], o1[:, h])
+                np.testing.assert_array_equal(l2[:, h], l1[:, h])
+
+
+def test_hp2_bwd_vs_autograd():
+    """All five gradients with Hp = 2 Hkv against autograd: each proxy head
+    distils the mean distribution of its own two query heads over its own
+    blocks; dK / dV of a KV head sum both proxy heads' selections."""
+    case = _hp2_case(qo=[150, 40], kv=[300, 200])
+    inp = synth.make_inputs(case, with_dout=True)
+    idx = _rand_idx(case, np.random.default_rng(23))
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens, synth.bits(inp["dout"]),
+                               synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]), kl_weight=0.6)
+    dq, dk, dv, dpq, dpk = _autograd_route(inp, case, idx, 0.6)
+    for name, ref in [("dq", dq), ("dk", dk), ("dv", dv), ("dpq", dpq), ("dpk", dpk)]:
+        np.testing.assert_allclose(g[name], ref, rtol=1e-9, atol=1e-11, err_msg=name)
+
+
+def test_hp2_kl_grad_finite_differences():
+    """The closed-form dpq of every proxy head equals central differences of
+    the fp64 KL objective with Hp = 2 Hkv."""
+    case = _hp2_case(qo=[256], kv=[256])
+    inp = synth.make_inputs(case, with_dout=True)
+    idx = _rand_idx(case, np.random.default_rng(24))
+    args = (synth.bits(inp["q"]), synth.bits(inp["k_pages"]), inp["kv_indices"].numpy(), idx,
+            case.qo_lens, case.kv_lens)
+    g = O.sparse_attention_bwd(synth.bits(inp["q"]), synth.bits(inp["k_pages"]), synth.bits(inp["v_pages"]),
+                               inp["kv_indices"].numpy(), idx, case.qo_lens, case.kv_lens,
+                               synth.bits(inp["dout"]), synth.bits(inp["pq"]), synth.bits(inp["pk_pages"]))
+    pq = O.bf16_to_f64(synth.bits(inp["pq"]))
+    pk = O.bf16_to_f64(synth.bits(inp["pk_pages"]))
+    h = 1e-6
+    for i, hh, c in [(10, 0, 3), (130, 1, 7), (200, 2, 30), (255, 3, 0)]:
+        a, b = pq.copy(), pq.copy()
+        a[i, hh, c] += h
+        b[i, hh, c] -= h
+        fd = (O.kl_objective(a, pk, *args) - O.kl_objective(b, pk, *args)) / (2 * h)
+        assert abs(fd - g["dpq"][i, hh, c]) <= 1e-6 * max(1.0, abs(fd)), (i, hh, c, fd, g["dpq"][i, hh, c])

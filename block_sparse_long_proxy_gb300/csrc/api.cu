@@ -111,8 +111,9 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
     return set_error(MSA_ERR_INVALID_ARG, "msa_plan: head counts must be >= 1");
   if (num_qo_heads % num_kv_heads != 0)
     return set_error(MSA_ERR_INVALID_ARG, "msa_plan: num_qo_heads %% num_kv_heads != 0");
-  if (num_proxy_heads != num_kv_heads)
-    return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: one proxy head per GQA group is required (Hp == Hkv)");
+  if (num_proxy_heads % num_kv_heads != 0 || num_qo_heads % num_proxy_heads != 0)
+    return set_error(MSA_ERR_UNSUPPORTED,
+                     "msa_plan: num_proxy_heads must be a multiple of num_kv_heads and divide num_qo_heads");
   if (head_dim != 64 && head_dim != 128) return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: head_dim must be 64 or 128");
   if (proxy_head_dim != 32 && proxy_head_dim != 64)
     return set_error(MSA_ERR_UNSUPPORTED, "msa_plan: proxy_head_dim must be 32 or 64");

@@ -1,15 +1,17 @@
 // Stage 3 (prefill): GQA block-sparse flash attention forward, bf16 or FP8 K/V.
 //
-// For query row i of tile t and head h (group g = h / G): softmax over the
-// keys of the selected blocks kv_block_indexes[t, g, :] that are visible to
-// i, of q.k/sqrt(d); out = P.V and lse = ln sum exp ("MiniMax-AI/MSA"
-// README, section "Usage": fmha_sm100(q, k_pages, v_pages, sparse_plan,
-// kv_indices, kv_block_indexes); Flash-MSA article, "three key
-// differences": the main attention is GQA).
+// For query row i of tile t and head h (KV head g = h / (Hq/Hkv), proxy
+// head p = h / (Hq/Hp)): softmax over the keys of the selected blocks
+// kv_block_indexes[t, p, :] that are visible to i, of q.k_g/sqrt(d); out =
+// P.V_g and lse = ln sum exp ("MiniMax-AI/MSA" README, section "Usage":
+// fmha_sm100(q, k_pages, v_pages, sparse_plan, kv_indices,
+// kv_block_indexes); Flash-MSA article, "three key differences": the main
+// attention is GQA and each proxy head picks its own block set).  With one
+// proxy head per GQA group, p = g.
 //
-// A work unit is (tile, GQA group, pair of query heads of the group): both
-// heads share every K/V block the TMA producer gathers through the page
-// table.  Tensor memory holds S0, S1 (128 columns each) and O0, O1 (d
+// A work unit is (tile, proxy head, pair of the query heads that use its
+// blocks): both heads share every K/V block the TMA producer gathers
+// through the page table.  Tensor memory holds S0, S1 (128 columns each) and O0, O1 (d
 // columns each); the bf16 probabilities P_h overwrite the first 64 columns
 // of S_h and feed the P.V MMA straight from tensor memory.  Roles:
 //   warps 0-3  softmax of head 0 (thread = query row), warps 4-7 head 1,
@@ -93,8 +95,12 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
                     const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
-                    float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
-                    const float* __restrict__ k_scale, const float* __restrict__ v_scale, uint32_t* err) {
+                    float* __restrict__ lse, int32_t hq, int32_t hsel, int32_t kv_div, int32_t topk,
+                    float scale_log2, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
+                    uint32_t* err) {
+  // hsel block sets (proxy heads) per tile; a unit's u.g is its proxy head,
+  // whose blocks are read from KV head u.g / kv_div of hsel / kv_div
+  const int hkv = hsel / kv_div;
   using L = AttnSmem<D>;
   constexpr int kChunks = D / 64;
   static_assert(!kFp8 || (D == 128 && !kOneKvHead), "FP8 K/V: head_dim 128, main attention");
@@ -163,7 +169,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       UnitList& ls = lists[k % kListSlots];
       const AttnUnit u = units[ui];
       const TileInfo tl = tiles[u.tile];
-      const int32_t* sel = idx + (static_cast<int64_t>(u.tile) * hkv + u.g) * topk;
+      const int32_t* sel = idx + (static_cast<int64_t>(u.tile) * hsel + u.g) * topk;
       if (lane == 0) ok = mbar_wait(list_empty + k % kListSlots, ((k / kListSlots) & 1) ^ 1, err);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
@@ -183,8 +189,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
             atomicOr(err, kErrDeviceCheck);
             page = 0;
           }
-          // K/V head of the unit's group, or the single head of a one-head pool
-          row = static_cast<int>((kOneKvHead ? page : page * hkv + u.g) * 128);
+          // K/V head of the unit's proxy head, or the single head of a one-head pool
+          row = static_cast<int>((kOneKvHead ? page : page * hkv + u.g / kv_div) * 128);
         }
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, valid);
         if (valid) {
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         ls.q_begin = tl.q_begin;
         ls.rows = tl.rows;
         ls.pos0 = tl.pos0;
-        ls.g = u.g;
+        ls.g = u.g / kv_div;
       }
       __syncwarp();
       if (lane == 0) {
@@ -546,10 +552,12 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
 }  // namespace
 
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
+  // a unit: (tile, proxy head g, a pair of the query heads that use g's
+  // blocks); with one proxy head per GQA group g is the group
   std::vector<AttnUnit> us;
-  const int grp = p->hq / p->hkv;
+  const int grp = p->hq / p->hp;
   for (int t = 0; t < p->n_tiles; ++t)
-    for (int g = 0; g < p->hkv; ++g)
+    for (int g = 0; g < p->hp; ++g)
       for (int h = 0; h < grp; h += 2) us.push_back(AttnUnit{t, g, g * grp + h, std::min(2, grp - h)});
   // heaviest first: a unit visits at most min(num_valid_pages, topk) blocks
   std::stable_sort(us.begin(), us.end(), [&](const AttnUnit& a, const AttnUnit& b) {
@@ -559,10 +567,10 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   p->n_attn_units = static_cast<int32_t>(us.size());
   const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
   aux.insert(aux.end(), raw, raw + us.size() * 4);
-  // the proxy softmax of the backward: proxy head g over group g's blocks
+  // the proxy softmax of the backward: proxy head g over its own blocks
   std::vector<AttnUnit> ps;
   for (int t = 0; t < p->n_tiles; ++t)
-    for (int g = 0; g < p->hkv; ++g) ps.push_back(AttnUnit{t, g, g, 1});
+    for (int g = 0; g < p->hp; ++g) ps.push_back(AttnUnit{t, g, g, 1});
   std::stable_sort(ps.begin(), ps.end(), [&](const AttnUnit& a, const AttnUnit& b) {
     return std::min(p->tiles[a.tile].nvp, p->topk) > std::min(p->tiles[b.tile].nvp, p->topk);
   });
@@ -601,20 +609,20 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attn_fwd_kernel<128, false, true><<<grid, attn_threads(true), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-        scale_log2, k_scale, v_scale, p->err_d);
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
+        p->hp / p->hkv, p->topk, scale_log2, k_scale, v_scale, p->err_d);
   } else if (p->d == 128) {
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attn_fwd_kernel<128, false, false><<<grid, attn_threads(false), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-        scale_log2, nullptr, nullptr, p->err_d);
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
+        p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     attn_fwd_kernel<64, false, false><<<grid, attn_threads(false), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hkv, p->topk,
-        scale_log2, nullptr, nullptr, p->err_d);
+        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
+        p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
 }
@@ -646,7 +654,7 @@ msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void*
   cudaFuncSetAttribute(attn_fwd_kernel<64, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   attn_fwd_kernel<64, true, false><<<grid, attn_threads(false), smem, st>>>(
       qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx, kv_indices, p->num_pages,
-      static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
+      static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hp, p->hp, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: proxy softmax launch");
 }
 

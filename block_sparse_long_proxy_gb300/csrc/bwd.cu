@@ -5,11 +5,11 @@
 // gradient of the KL loss with respect to a proxy score is p_proxy - p_main;
 // the block indexes are the ones cached by the forward).
 //
-// For row i, head h (group g), key set Omega = visible keys of the cached
-// blocks of (tile, g):
+// For row i, head h (KV head g, proxy head p: the G = Hq/Hp heads of p use
+// p's blocks), key set Omega = visible keys of the cached blocks of (tile, p):
 //   P = exp(q.k/sqrt(d) - lse), D = rowsum(dout*out), dS = P*(dout.v - D)
 //   dq = dS.K/sqrt(d), dk = sum_h dS^T.q/sqrt(d), dv = sum_h P^T.dout
-//   p_proxy = softmax_Omega(pq.pk/sqrt(dp)), p_main = mean_h P
+//   p_proxy = softmax_Omega(pq_p.pk/sqrt(dp)), p_main = mean over p's heads of P
 //   dZ = w*(p_proxy - p_main), dpq = dZ.pk/sqrt(dp), dpk = dZ^T.pq/sqrt(dp)
 // Both dpq and dpk split into a proxy term and a main term:
 //   dpq = w/sqrt(dp) * (p_proxy.pk - (1/G) sum_h P_h.pk)
@@ -20,9 +20,9 @@
 //   proxy    the proxy softmax over Omega on the tensor cores: the forward
 //            attention kernel (attn_fwd.cu) with pq as queries and the shared
 //            proxy K head as keys and values gives p_proxy . pk and its LSE
-//   prep     per (tile, group): D of the group's heads and lse * log2(e),
+//   prep     per (tile, proxy head p): D of p's heads and lse * log2(e),
 //            both stored [head][row]; the proxy LSE in log2 units
-//            ([group][row]) and dpq's proxy term (plain store)
+//            ([proxy head][row]) and dpq's proxy term (plain store)
 //   index    page owners, then the page -> selections inverse index
 //   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
 //            store) and dpq's main term (fp32 atomics, G per element)
@@ -47,20 +47,21 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 // ------------------------------------------------------------------ prep
 
-// Per (tile, group): D[row, h] = rowsum(dout * out) and lse * log2(e) of the
-// group's heads, both stored [head][row]; the proxy LSE of the group in log2
-// units, [group][row]; and dpq's proxy term w/sqrt(dp) * p_proxy . pk, from
-// the proxy softmax (launch_proxy_softmax) run just before.
+// Per (tile, proxy head g): D[row, h] = rowsum(dout * out) and lse * log2(e)
+// of the G query heads that use g's blocks, both stored [head][row]; the
+// proxy LSE of g in log2 units, [proxy head][row]; and dpq's proxy term
+// w/sqrt(dp) * p_proxy . pk, from the proxy softmax (launch_proxy_softmax)
+// run just before.
 __global__ void __launch_bounds__(kThreads)
     bwd_prep_kernel(const TileInfo* __restrict__ tiles, const __nv_bfloat16* __restrict__ out,
                     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
                     const __nv_bfloat16* __restrict__ op, const float* __restrict__ lse_p,
                     float* __restrict__ dsumt, float* __restrict__ lse2t, float* __restrict__ lsept,
-                    float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t total_q, float kl_weight) {
-  const int t = blockIdx.x / hkv, g = blockIdx.x % hkv;
+                    float* __restrict__ dpq, int32_t hq, int32_t hsel, int32_t total_q, float kl_weight) {
+  const int t = blockIdx.x / hsel, g = blockIdx.x % hsel;
   const TileInfo tl = tiles[t];
   const int lane = threadIdx.x & 31;
-  const int G = hq / hkv;
+  const int G = hq / hsel;
 
   // D = rowsum(dout * out): eight lanes per (row, head), 16 d values each,
   // so that every thread has its few loads in flight at once and the block's
@@ -98,11 +99,11 @@ __global__ void __launch_bounds__(kThreads)
   const float f = kl_weight * rsqrtf(static_cast<float>(kDP));
   for (int r = threadIdx.x; r < tl.rows; r += blockDim.x) {
     const int64_t q_row = tl.q_begin + r;
-    lsept[static_cast<int64_t>(g) * total_q + q_row] = lse_p[q_row * hkv + g] * kLog2e;
+    lsept[static_cast<int64_t>(g) * total_q + q_row] = lse_p[q_row * hsel + g] * kLog2e;
   }
   for (int e = threadIdx.x; e < tl.rows * (kDP / 8); e += blockDim.x) {
     const int r = e / (kDP / 8), c = e % (kDP / 8);
-    const int64_t base = (static_cast<int64_t>(tl.q_begin + r) * hkv + g) * kDP + c * 8;
+    const int64_t base = (static_cast<int64_t>(tl.q_begin + r) * hsel + g) * kDP + c * 8;
     const uint4 v = *reinterpret_cast<const uint4*>(op + base);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     float4* dst = reinterpret_cast<float4*>(dpq + base);
@@ -140,15 +141,17 @@ __device__ __forceinline__ int32_t owner_of(const int32_t* __restrict__ kv_indic
   return (page >= 0 && page < num_pages) ? owner[page] : e;
 }
 
-// count[o*hkv + g] = number of selections (tile, group g, slot) whose block
-// maps to a page owned by entry o.
+// count[o*hkv + g] = number of selections (tile, proxy head p, slot) of a
+// proxy head p of KV head g = p / kv_div whose block maps to a page owned by
+// entry o.
 __global__ void bwd_count_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx, int32_t n_tiles,
-                                 int32_t hkv, int32_t topk, const int32_t* __restrict__ kv_indices,
+                                 int32_t hsel, int32_t kv_div, int32_t topk, const int32_t* __restrict__ kv_indices,
                                  const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ count) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= static_cast<int64_t>(n_tiles) * hkv * topk) return;
-  const int t = static_cast<int>(e / (static_cast<int64_t>(hkv) * topk));
-  const int g = static_cast<int>((e / topk) % hkv);
+  if (e >= static_cast<int64_t>(n_tiles) * hsel * topk) return;
+  const int hkv = hsel / kv_div;
+  const int t = static_cast<int>(e / (static_cast<int64_t>(hsel) * topk));
+  const int g = static_cast<int>((e / topk) % hsel) / kv_div;
   const int j = idx[e];
   const TileInfo tl = tiles[t];
   if (j < 0 || j >= tl.nvp) return;
@@ -181,17 +184,18 @@ __global__ void __launch_bounds__(1024) bwd_scan_kernel(const int32_t* __restric
   if (threadIdx.x == 1023) off[n] = part[1023];
 }
 
-// Files each selection under its page owner and group; the list item is the
-// flat selection index (t * hkv + g) * topk + slot, which gives both the
-// tile and the logical block (and sorts by tile).
+// Files each selection under its page owner and KV head; the list item is
+// the flat selection index (t * hsel + p) * topk + slot, which gives the
+// tile, the proxy head and the logical block (and sorts by tile).
 __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx, int32_t n_tiles,
-                                int32_t hkv, int32_t topk, const int32_t* __restrict__ kv_indices,
+                                int32_t hsel, int32_t kv_div, int32_t topk, const int32_t* __restrict__ kv_indices,
                                 const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ cursor,
                                 int32_t* __restrict__ list) {
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (e >= static_cast<int64_t>(n_tiles) * hkv * topk) return;
-  const int t = static_cast<int>(e / (static_cast<int64_t>(hkv) * topk));
-  const int g = static_cast<int>((e / topk) % hkv);
+  if (e >= static_cast<int64_t>(n_tiles) * hsel * topk) return;
+  const int hkv = hsel / kv_div;
+  const int t = static_cast<int>(e / (static_cast<int64_t>(hsel) * topk));
+  const int g = static_cast<int>((e / topk) % hsel) / kv_div;
   const int j = idx[e];
   const TileInfo tl = tiles[t];
   if (j < 0 || j >= tl.nvp) return;
@@ -214,7 +218,7 @@ __global__ void bwd_zero_dpk_kernel(const int32_t* __restrict__ kv_indices, int3
 }  // namespace
 
 // The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
-// fp32), lsept ([Hkv][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
+// fp32), lsept ([Hp][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
 // Hp, dp]) and LSE (fp32 [total_q, Hp]), the inverse index (int32), then the
 // page owners (int32 [num_pages]).
 static size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -223,8 +227,8 @@ size_t bwd_scratch_bytes(const msa_plan_s* p) {
   if (p->decode) return 0;
   const size_t tq = static_cast<size_t>(p->total_q);
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
-  return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hkv) + al256(2 * tq * p->hkv * kDP) + al256(4 * tq * p->hkv) +
-         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk)) +
+  return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hp) + al256(2 * tq * p->hp * kDP) + al256(4 * tq * p->hp) +
+         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk)) +
          al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
 }
 
@@ -244,28 +248,29 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   sp += al256(4 * tq * p->hq);
   float* lse2t = reinterpret_cast<float*>(sp);                        // [hq][total_q], lse * log2(e)
   sp += al256(4 * tq * p->hq);
-  float* lsept = reinterpret_cast<float*>(sp);                        // [hkv][total_q], log2 units
-  sp += al256(4 * tq * p->hkv);
+  float* lsept = reinterpret_cast<float*>(sp);                        // [hp][total_q], log2 units
+  sp += al256(4 * tq * p->hp);
   auto* op = reinterpret_cast<__nv_bfloat16*>(sp);                    // [total_q, hp, dp] bf16
-  sp += al256(2 * tq * p->hkv * kDP);
+  sp += al256(2 * tq * p->hp * kDP);
   float* lse_p = reinterpret_cast<float*>(sp);                        // [total_q, hp], natural log
-  sp += al256(4 * tq * p->hkv);
+  sp += al256(4 * tq * p->hp);
   int32_t* cnt = reinterpret_cast<int32_t*>(sp);
   int32_t* off = cnt + ent;
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
-  sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hkv * p->topk));
+  sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk));
   int32_t* owner = reinterpret_cast<int32_t*>(sp);                    // [num_pages]
   const auto* O = static_cast<const __nv_bfloat16*>(out);
   const auto* dO = static_cast<const __nv_bfloat16*>(dout);
-  const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hkv * p->topk;
+  const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hp * p->topk;
+  const int kv_div = p->hp / p->hkv;
 
   bwd_zero_dpk_kernel<<<n_ent, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, dpk);
   msa_status s = launch_proxy_softmax(p, pq, pk_pages, kv_indices, idx, op, lse_p, st);
   if (s != MSA_OK) return s;
-  bwd_prep_kernel<<<p->n_tiles * p->hkv, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
-                                                           dpq, p->hq, p->hkv, static_cast<int32_t>(p->total_q),
-                                                           kl_weight);
+  bwd_prep_kernel<<<p->n_tiles * p->hp, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
+                                                          dpq, p->hq, p->hp, static_cast<int32_t>(p->total_q),
+                                                          kl_weight);
   s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)  // 0x7F7F7F7F: above every entry index
     s = cuda_check(cudaMemsetAsync(owner, 0x7F, sizeof(int32_t) * static_cast<size_t>(p->num_pages), st),
@@ -273,11 +278,11 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   if (s != MSA_OK) return s;
   bwd_owner_kernel<<<(n_ent + 255) / 256, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, owner);
   const int sel_blocks = static_cast<int>((n_sel + 255) / 256);
-  bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, kv_indices, owner,
-                                               p->num_pages, cnt);
+  bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hp, kv_div, p->topk, kv_indices,
+                                               owner, p->num_pages, cnt);
   bwd_scan_kernel<<<1, 1024, 0, st>>>(cnt, static_cast<int32_t>(ent), off, cur);
-  bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hkv, p->topk, kv_indices, owner,
-                                              p->num_pages, cur, list);
+  bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hp, kv_div, p->topk, kv_indices,
+                                              owner, p->num_pages, cur, list);
   s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
   if (s != MSA_OK) return s;
   s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);

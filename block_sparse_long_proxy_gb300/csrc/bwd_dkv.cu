@@ -2,12 +2,13 @@
 // block-sparse GQA attention with the KL-coupled proxy (Flash-MSA article,
 // backward-pass paragraph), on the tcgen05 tensor cores.
 //
-// One CTA per (page-table entry e, GQA group g).  The lowest entry that
-// names a physical page owns it: its CTA walks every selection of that page
-// for group g, by this entry or any other that names the same page (the
-// inverse index, sorted so sums are deterministic), 64 query rows at a time,
-// and the CTAs of the other entries return at once.  Per selection, for each
-// of the group's G heads:
+// One CTA per (page-table entry e, KV head g).  The lowest entry that names
+// a physical page owns it: its CTA walks every selection of that page by a
+// proxy head of KV head g (a group has Hp/Hkv proxy heads, each with its own
+// blocks), by this entry or any other that names the same page (the inverse
+// index, sorted so sums are deterministic), 64 query rows at a time, and the
+// CTAs of the other entries return at once.  Per selection by proxy head p,
+// for each of the G = Hq/Hp query heads that use p's blocks:
 //   S^T  = K . Q_h^T            dP^T = V . dO_h^T       (M = keys, N = rows)
 //   P^T  = exp2(S^T sl2 - lse2)  dS^T = P^T * (dP^T - D)  (masked: causal, ragged)
 //   dV  += P^T . dO_h           dK  += dS^T . Q_h       (P^T, dS^T from TMEM)
@@ -16,7 +17,7 @@
 // the same keys (in the S^T columns):
 //   Sp^T = pk . pq^T,  Pp^T = exp2(Sp^T zsl2 - lsep),  dpk += (-G Pp^T) . pq
 // so that at the end dpk * (-w / (G sqrt(dp))) = w/sqrt(dp) (Pp - mean_h P_h)^T pq,
-// this group's share of the KL gradient with respect to the proxy keys.
+// this KV head's share of the KL gradient with respect to the proxy keys.
 //
 // Tensor memory (512 columns): S^T 64 | dP^T 64 | dV 128 | dpk 64 | dK 128 | K 64.
 // K is copied into tensor memory once, so S^T = K . Q^T reads only Q from
@@ -76,13 +77,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const int32_t* __restrict__ inv_list, int32_t topk,
                       const int32_t* __restrict__ kv_indices, int64_t num_pages, const float* __restrict__ lse2t,
                       const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
-                      float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, int32_t total_q,
+                      float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, int32_t hsel,
+                      int32_t total_q,
                       float kl_weight, uint32_t* err) {
   using L = DkvSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int e = blockIdx.x / hkv, g = blockIdx.x % hkv;
-  const int G = hq / hkv;
+  const int G = hq / hsel;  // query heads per proxy head
   int64_t page = kv_indices[e];
   const bool page_ok = page >= 0 && page < num_pages;
   if (page_ok && owner[page] != e) return;  // another entry's CTA owns this page
@@ -152,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(done, 1);
     fence_mbar_init();
   }
-  // the selection list (flat indexes (t * hkv + g) * topk + slot), sorted so
+  // the selection list (flat indexes (t * hsel + p) * topk + slot), sorted so
   // that every run sums in the same order
   const bool sorted = n <= kMaxList;
   if (sorted) {
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   auto sel_at = [&](int it) { return sorted ? list[it] : inv_list[lb + it]; };
-  const int sel_per_tile = hkv * topk;
+  const int sel_per_tile = hsel * topk;
 
   if (warp == 8) {
     // ---------------------------------------------------------- producer
@@ -201,7 +203,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     int qi = 0, pi = 0;
     for (int it = 0; ok && it < n; ++it) {
-      const TileInfo tl = tiles[sel_at(it) / sel_per_tile];
+      const int sel = sel_at(it);
+      const TileInfo tl = tiles[sel / sel_per_tile];
+      const int pp = (sel / topk) % hsel;  // the selecting proxy head
       const int halves = tl.rows > 64 ? 2 : 1;
       for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
         const int r0 = tl.q_begin + hf * 64;
@@ -209,16 +213,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait(pq_empty + ps, ((pi / kPqStages) & 1) ^ 1, err))) break;
         if (lane == 0) {
           mbar_expect_tx(pq_full + ps, 8192);
-          tma_load_3d(pq_s + ps * 8192, &pq_map, pq_full + ps, 0, g, r0);
+          tma_load_3d(pq_s + ps * 8192, &pq_map, pq_full + ps, 0, pp, r0);
         }
         for (int rr = lane; rr < 64; rr += 32) {
           const int r = hf * 64 + rr;
-          lsep_s[ps * 64 + rr] = r < tl.rows ? -lsept[static_cast<int64_t>(g) * total_q + tl.q_begin + r] : 0.f;
+          lsep_s[ps * 64 + rr] = r < tl.rows ? -lsept[static_cast<int64_t>(pp) * total_q + tl.q_begin + r] : 0.f;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(pq_full + ps);
         for (int hh = 0; hh < G; ++hh, ++qi) {
-          const int h = g * G + hh;
+          const int h = pp * G + hh;
           const int s = qi % kQStages;
           if (!(ok = mbar_wait(qd_empty + s, ((qi / kQStages) & 1) ^ 1, err))) break;
           uint8_t* st = qd_s + s * L::kQdBytes;
@@ -529,9 +533,9 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
                              static_cast<uint64_t>(p->total_q)};
   const uint64_t qstr[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(p->hq) * kD * 2};
   const uint32_t qbox[3] = {64, 1, 64};
-  const uint64_t pqdims[3] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->hkv),
+  const uint64_t pqdims[3] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->hp),
                               static_cast<uint64_t>(p->total_q)};
-  const uint64_t pqstr[2] = {static_cast<uint64_t>(kDP) * 2, static_cast<uint64_t>(p->hkv) * kDP * 2};
+  const uint64_t pqstr[2] = {static_cast<uint64_t>(kDP) * 2, static_cast<uint64_t>(p->hp) * kDP * 2};
   const uint64_t kdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
   const uint64_t kstr[1] = {static_cast<uint64_t>(kD) * 2};
   const uint32_t kbox[2] = {64, 128};
@@ -549,7 +553,7 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
       qm, dom, pqm, km, vm, pkm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
       dsumt, lsept,
-      dk, dv, dpk, p->hq, p->hkv, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+      dk, dv, dpk, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
 }
 

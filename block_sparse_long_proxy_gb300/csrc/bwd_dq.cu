@@ -14,7 +14,8 @@
 // j+1 right after dQ of j, so the tensor pipe has work while the softmax
 // runs (its two warpgroups split the 128 keys).
 // At the end dQ / sqrt(d) is stored and dpq * (-w / (G sqrt(dp))) is added
-// with fp32 atomics: the G heads of a group add into the same dpq row, whose
+// with fp32 atomics: the G = Hq/Hp heads that use one proxy head's blocks
+// add into that proxy head's dpq row, whose
 // proxy term the prep kernel stored first.
 //
 // Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 | Q 64 columns.  Warpgroup
@@ -55,15 +56,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap pk_map, const TileInfo* __restrict__ tiles,
                      const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                      const float* __restrict__ lse2t, const float* __restrict__ dsumt, float* __restrict__ dq,
-                     float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t topk, int32_t total_q,
+                     float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q,
                      float kl_weight, uint32_t* err) {
   using L = DqSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int t = blockIdx.x / hq, h = blockIdx.x % hq;
-  const int G = hq / hkv, g = h / G;
+  // head h reads KV head g and the blocks of proxy head ps; G heads share ps
+  const int G = hq / hsel, ps = h / G, g = h / (hq / hkv);
   const TileInfo tl = tiles[t];
-  const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hkv + g) * topk;
+  const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hsel + ps) * topk;
 
   uint8_t* q_s = smem + L::kQOff;
   uint8_t* do_s = smem + L::kDOOff;
@@ -333,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t a[32];
         tmem_ld32(lane_base + kColDPQ + wg * 32, a);
         tmem_wait_ld();
-        float* dpr = dpq + (q_row * hkv + g) * kDP + wg * 32;
+        float* dpr = dpq + (q_row * hsel + ps) * kDP + wg * 32;
         if (row_ok)
 #pragma unroll
           for (int i = 0; i < 32; ++i) atomicAdd(dpr + i, __uint_as_float(a[i]) * f);
@@ -371,7 +373,7 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
   const int smem = DqSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dq_tc_kernel<<<p->n_tiles * p->hq, kThreads, smem, st>>>(
-      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, p->hq, p->hkv, p->topk,
+      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, p->hq, p->hkv, p->hp, p->topk,
       static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
 }

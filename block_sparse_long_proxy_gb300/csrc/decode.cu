@@ -78,8 +78,12 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
                   const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                   const float* __restrict__ k_scale, const float* __restrict__ v_scale, float* __restrict__ part_o,
                   float* __restrict__ part_ml, int32_t* __restrict__ row_cnt, __nv_bfloat16* __restrict__ out,
-                  float* __restrict__ lse, int32_t n_units, int32_t hq, int32_t hkv, int32_t topk, float scale_log2,
-                  uint32_t* err) {
+                  float* __restrict__ lse, int32_t n_units, int32_t hq, int32_t hsel, int32_t kv_div, int32_t topk,
+                  float scale_log2, uint32_t* err) {
+  // A row is (sequence, proxy head p): the G = hq / hsel query heads of p
+  // attend over p's blocks of KV head p / kv_div (kv_div proxy heads per KV
+  // head; 1 when there is one proxy head per GQA group).
+  const int hkv = hsel / kv_div;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   using L = DecodeSmem<NT>;
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
   volatile int32_t* merge_flag = reinterpret_cast<int32_t*>(smem + L::kFlagOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = hq / hkv;
+  const int G = hq / hsel;
   const int ub = range_start(blockIdx.x, n_units, gridDim.x);
   const int ue = range_start(blockIdx.x + 1, n_units, gridDim.x);
 
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
       int j = -1, row_off = 0;
       if (u < ue) {
         const int row = u / topk;
-        const int t = row / hkv, g = row % hkv;
+        const int t = row / hsel, g = row % hsel;
         j = idx[u];
         const TileInfo tl = tiles[t];
         if (j >= tl.nvp) {
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
             atomicOr(err, kErrDeviceCheck);
             page = 0;
           }
-          row_off = static_cast<int>((page * hkv + g) * 128);
+          row_off = static_cast<int>((page * hkv + g / kv_div) * 128);
         }
       }
       const int n = min(32, ue - base);
@@ -224,9 +228,9 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
           o += p[d] * sc;
         }
         if (whole) {  // this CTA holds the whole row: write the result directly
-          const int t = row / hkv, g = row % hkv;
+          const int t = row / hsel, g = row % hsel;
           const int64_t orow = static_cast<int64_t>(tiles[t].q_begin) * hq + g * G + h;
-          out[orow * kD + kHalf * rnd + d] = __float2bfloat16_rn(Lsum > 0.f ? o / Lsum * v_scale[g] : 0.f);
+          out[orow * kD + kHalf * rnd + d] = __float2bfloat16_rn(Lsum > 0.f ? o / Lsum * v_scale[g / kv_div] : 0.f);
           if (d == 0 && rnd == 0 && lse != nullptr)
             lse[orow] = Lsum > 0.f ? (mm + log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
         } else {
@@ -263,8 +267,8 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
       // thread owns one d column of all G heads, so the loads of a segment
       // (m, l and O of each head) are independent and issue together.
       __threadfence();
-      const int t = row / hkv, g = row % hkv;
-      const float vs = v_scale[g];
+      const int t = row / hsel, g = row % hsel;
+      const float vs = v_scale[g / kv_div];
       const int64_t q_row = tiles[t].q_begin;
       for (int d = threadIdx.x; d < kD; d += 32 * kCWarps)
 #pragma unroll 1
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
 
   for (int u = ub; u < ue; ++u) {
     const int row = u / topk;
-    const int t = row / hkv, g = row % hkv;
+    const int t = row / hsel, g = row % hsel;
     if (row != cur_row) {
       if (cur_row >= 0) flush(cur_row, seg);
       cur_row = row;
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
       }
       const TileInfo tl = tiles[t];
       qpos = tl.pos0;
-      sl2 = scale_log2 * k_scale[g];
+      sl2 = scale_log2 * k_scale[g / kv_div];
       // q^T fragments: head n = gi + 8nt of the group, d = 16kc + 4t4 + {0,1} | {2,3}
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -465,16 +469,18 @@ int decode_grid_rows(int rows, int topk, int num_sms, int G) {
 
 size_t decode_partial_floats(const msa_plan_s* p) {
   if (!p->decode) return 0;
-  const size_t units = static_cast<size_t>(p->n_tiles) * p->hkv * p->topk;
-  const size_t g = p->hq / p->hkv;
-  return units * g * (kD + 2) + static_cast<size_t>(p->n_tiles) * p->hkv;  // partials + per-row counters
+  // rows are (sequence, proxy head): one block set each
+  const size_t units = static_cast<size_t>(p->n_tiles) * p->hp * p->topk;
+  const size_t g = p->hq / p->hp;
+  return units * g * (kD + 2) + static_cast<size_t>(p->n_tiles) * p->hp;  // partials + per-row counters
 }
 
 msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                               const int32_t* kv_indices, const int32_t* idx, const float* k_scale,
                               const float* v_scale, void* out, float* lse, cudaStream_t st) {
   if (p->d != kD) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs head_dim 128");
-  if (p->hq / p->hkv > 16) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs G <= 16");
+  if (p->hq / p->hp > 16)
+    return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 decode needs at most 16 query heads per proxy head");
   if (decode_ws_applies(p))
     return launch_attn_decode_ws(p, q, k_pages, v_pages, kv_indices, idx, k_scale, v_scale, out, lse, st);
   CUtensorMap km, vm;
@@ -484,10 +490,11 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
   if (!encode_tensor_map(&km, 2, k_pages, dims, str, box, 0, 128) ||
       !encode_tensor_map(&vm, 2, v_pages, dims, str, box, 0, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
-  const int n_units = p->n_tiles * p->hkv * p->topk;
-  const int grid = decode_grid_rows(p->n_tiles * p->hkv, p->topk, p->num_sms, p->hq / p->hkv);
+  const int n_units = p->n_tiles * p->hp * p->topk;
+  const int grid = decode_grid_rows(p->n_tiles * p->hp, p->topk, p->num_sms, p->hq / p->hp);
   const size_t units = static_cast<size_t>(n_units);
-  const int G = p->hq / p->hkv;
+  const int G = p->hq / p->hp;
+  const int kv_div = p->hp / p->hkv;
   float* part_o = p->partial_d;
   float* part_ml = p->partial_d + units * G * kD;
   int32_t* row_cnt = reinterpret_cast<int32_t*>(part_ml + units * G * 2);  // zeroed by msa_plan
@@ -499,13 +506,13 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
                                                      v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
-                                                     p->hkv, p->topk, scale_log2, p->err_d);
+                                                     p->hp, kv_div, p->topk, scale_log2, p->err_d);
   } else {
     const int smem = DecodeSmem<2>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
                                                      v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
-                                                     p->hkv, p->topk, scale_log2, p->err_d);
+                                                     p->hp, kv_div, p->topk, scale_log2, p->err_d);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
 }
@@ -677,13 +684,13 @@ extern "C" msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pag
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
                                                      k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, nu,
-                                                     num_qo_heads, num_kv_heads, topk, scale_log2, err);
+                                                     num_qo_heads, num_kv_heads, 1, topk, scale_log2, err);
   } else {
     const int smem = DecodeSmem<2>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, tiles, kv_block_indexes, kv_indices, num_pages,
                                                      k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, nu,
-                                                     num_qo_heads, num_kv_heads, topk, scale_log2, err);
+                                                     num_qo_heads, num_kv_heads, 1, topk, scale_log2, err);
   }
   return cuda_check(cudaGetLastError(), "msa_sparse_decode_noalloc: decode launch");
 }

@@ -60,14 +60,17 @@ __global__ void __launch_bounds__(kWsThreads, 2)
                      const __nv_bfloat16* __restrict__ q, const TileInfo* __restrict__ tiles,
                      const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                      const float* __restrict__ k_scale, const float* __restrict__ v_scale,
-                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t hq, int32_t hkv, int32_t topk,
-                     float scale_log2, uint32_t* err) {
+                     __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t hq, int32_t hsel,
+                     int32_t kv_div, int32_t topk, float scale_log2, uint32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // row = (sequence, proxy head g): the G = hq / hsel query heads of g over
+  // g's blocks of KV head g / kv_div
   const int row = blockIdx.x;
-  const int t = row / hkv, g = row % hkv;
-  const int G = hq / hkv;
+  const int t = row / hsel, g = row % hsel;
+  const int G = hq / hsel;
+  const int hkv = hsel / kv_div, kvh = g / kv_div;
   const TileInfo tl = tiles[t];
   uint8_t* buf = smem + WsSmem::kBufOff + warp * kBufBytes;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + WsSmem::kBarOff) + warp * kStg;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
         page = 0;
       }
       ukey = j * 128 + (u % kParts) * kKeys;
-      urow = static_cast<int>((page * hkv + g) * 128 + (u % kParts) * kKeys);
+      urow = static_cast<int>((page * hkv + kvh) * 128 + (u % kParts) * kKeys);
     }
   }
   // compact the valid units to the low lanes (padding slots load nothing)
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
       }
     }
   }
-  const float sl2 = scale_log2 * k_scale[g];
+  const float sl2 = scale_log2 * k_scale[kvh];
   const int qpos = tl.pos0;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f}, oacc[8][4];
 #pragma unroll
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
     }
   }
   __syncthreads();
-  const float vs = v_scale[g];
+  const float vs = v_scale[kvh];
   for (int e = threadIdx.x; e < G * kD; e += kWsThreads) {
     const int h = e / kD, d = e % kD;
     float mm = -INFINITY;
@@ -288,7 +291,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
 }  // namespace
 
 bool decode_ws_applies(const msa_plan_s* p) {
-  return p->n_tiles * p->hkv >= p->num_sms && p->hq / p->hkv <= 8 && p->topk <= kMaxTopk && p->d == kD;
+  return p->n_tiles * p->hp >= p->num_sms && p->hq / p->hp <= 8 && p->topk <= kMaxTopk && p->d == kD;
 }
 
 msa_status launch_attn_decode_ws(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
@@ -303,10 +306,10 @@ msa_status launch_attn_decode_ws(const msa_plan_s* p, const void* q, const void*
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
   const int smem = WsSmem::kBytes + 1024;
   cudaFuncSetAttribute(decode_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  decode_ws_kernel<<<p->n_tiles * p->hkv, kWsThreads, smem, st>>>(
+  decode_ws_kernel<<<p->n_tiles * p->hp, kWsThreads, smem, st>>>(
       km, vm, static_cast<const __nv_bfloat16*>(q), p->tiles_d, idx, kv_indices, p->num_pages, k_scale, v_scale,
-      static_cast<__nv_bfloat16*>(out), lse, p->hq, p->hkv, p->topk, 1.4426950408889634f / sqrtf(static_cast<float>(kD)),
-      p->err_d);
+      static_cast<__nv_bfloat16*>(out), lse, p->hq, p->hp, p->hp / p->hkv, p->topk,
+      1.4426950408889634f / sqrtf(static_cast<float>(kD)), p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
 }
 

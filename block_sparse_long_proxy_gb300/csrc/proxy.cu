@@ -464,51 +464,64 @@ __global__ void __launch_bounds__(32 * kDecWarps)
     const int t = __shfl_sync(0xFFFFFFFFu, ct, i & 31);
     const int j = __shfl_sync(0xFFFFFFFFu, cj, i & 31);
     const TileInfo tl = tiles[t];
-    // B fragments: pq[row, head n = g, dims]; heads >= hp contribute zeros
+    // B fragments: pq[row, head n = hb + g, dims] of eight heads from hb;
+    // heads >= hp contribute zeros
     uint32_t bf[DP / 16][2];
-    const __nv_bfloat16* qrow = pq + (static_cast<int64_t>(tl.q_begin) * hp + g) * DP;
+    const __nv_bfloat16* qrow0 = pq + static_cast<int64_t>(tl.q_begin) * hp * DP;
+    auto load_bf = [&](int hb) {
+      const __nv_bfloat16* qrow = qrow0 + static_cast<int64_t>(hb + g) * DP;
 #pragma unroll
-    for (int kt = 0; kt < DP / 16; ++kt) {
-      if (g < hp) {
-        bf[kt][0] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 2 * t4);
-        bf[kt][1] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 8 + 2 * t4);
-      } else {
-        bf[kt][0] = bf[kt][1] = 0u;
+      for (int kt = 0; kt < DP / 16; ++kt) {
+        if (hb + g < hp) {
+          bf[kt][0] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 2 * t4);
+          bf[kt][1] = *reinterpret_cast<const uint32_t*>(qrow + kt * 16 + 8 + 2 * t4);
+        } else {
+          bf[kt][0] = bf[kt][1] = 0u;
+        }
       }
-    }
+    };
+    load_bf(0);
     const int s = i % kDecStages;
     if (!mbar_wait(bars + s, (i / kDecStages) & 1, err)) break;
     const uint32_t base = smem_u32(ring + s * kBlk);
     const int nkeys = min(128, tl.kv_len - j * 128);  // keys past kv_len are not visible
-    float mx0 = -INFINITY, mx1 = -INFINITY;
+    for (int hb = 0;;) {  // eight proxy heads per pass over the page (one pass when hp <= 8)
+      float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int mt = 0; mt < 8; ++mt) {
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int kt = 0; kt < DP / 16; ++kt) {
-        const int row = mt * 16 + (lane & 15);
-        const int chunk16 = kt * 2 + (lane >> 4);
-        const int sw = DP == 64 ? (chunk16 ^ (row & 7)) : (chunk16 ^ ((row >> 1) & 3));
-        uint32_t a0, a1, a2, a3;
-        ldmatrix_x4(base + row * kRowBytes + sw * 16, a0, a1, a2, a3);
-        mma_16816(c, a0, a1, a2, a3, bf[kt][0], bf[kt][1]);
+        for (int kt = 0; kt < DP / 16; ++kt) {
+          const int row = mt * 16 + (lane & 15);
+          const int chunk16 = kt * 2 + (lane >> 4);
+          const int sw = DP == 64 ? (chunk16 ^ (row & 7)) : (chunk16 ^ ((row >> 1) & 3));
+          uint32_t a0, a1, a2, a3;
+          ldmatrix_x4(base + row * kRowBytes + sw * 16, a0, a1, a2, a3);
+          mma_16816(c, a0, a1, a2, a3, bf[kt][0], bf[kt][1]);
+        }
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        if (r0 < nkeys) { mx0 = fmaxf(mx0, c[0]); mx1 = fmaxf(mx1, c[1]); }
+        if (r1 < nkeys) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
       }
-      const int r0 = mt * 16 + g, r1 = r0 + 8;
-      if (r0 < nkeys) { mx0 = fmaxf(mx0, c[0]); mx1 = fmaxf(mx1, c[1]); }
-      if (r1 < nkeys) { mx0 = fmaxf(mx0, c[2]); mx1 = fmaxf(mx1, c[3]); }
-    }
-    __syncwarp();
-    issue(i + kDecStages);
+      const bool last = hb + 8 >= hp;
+      if (last) {  // the stage is free once the last pass has read it
+        __syncwarp();
+        issue(i + kDecStages);
+      }
 #pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
-    }
-    if (lane < 4) {
-      const int h0 = 2 * lane, h1 = 2 * lane + 1;
-      float* dst = max_score + static_cast<int64_t>(t) * hp * max_blocks + j;
-      if (h0 < hp) dst[static_cast<int64_t>(h0) * max_blocks] = mx0 * scale;
-      if (h1 < hp) dst[static_cast<int64_t>(h1) * max_blocks] = mx1 * scale;
+      for (int o = 4; o < 32; o <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+      }
+      if (lane < 4) {
+        const int h0 = hb + 2 * lane, h1 = h0 + 1;
+        float* dst = max_score + static_cast<int64_t>(t) * hp * max_blocks + j;
+        if (h0 < hp) dst[static_cast<int64_t>(h0) * max_blocks] = mx0 * scale;
+        if (h1 < hp) dst[static_cast<int64_t>(h1) * max_blocks] = mx1 * scale;
+      }
+      if (last) break;
+      hb += 8;
+      load_bf(hb);
     }
   }
 }
@@ -772,7 +785,6 @@ msa_status launch_proxy_topk(const msa_plan_s* p, const void* pq, const void* pk
 
 msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                                float* max_score, cudaStream_t st) {
-  if (p->hp > 8) return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore: decode path supports up to 8 proxy heads");
   CUtensorMap km;
   if (!make_pk_map(&km, p, pk_pages)) return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore: tensor map encoding failed");
   const int32_t* ustart = p->aux_d + p->proxy_unit_start_off;

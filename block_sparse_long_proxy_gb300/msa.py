@@ -242,7 +242,7 @@ class Plan:
         _need(k_pages, kvt, (self.num_pages, self.hkv, 128, self.d), "k_pages")
         _need(v_pages, kvt, (self.num_pages, self.hkv, 128, self.d), "v_pages")
         _need(kv_indices, torch.int32, (self.n_page_entries,), "kv_indices")
-        _need(kv_block_indexes, torch.int32, (self.n_tiles, self.hkv, self.topk), "kv_block_indexes")
+        _need(kv_block_indexes, torch.int32, (self.n_tiles, self.hp, self.topk), "kv_block_indexes")
         if self.kv_dtype != "bf16":
             _need(k_scale, torch.float32, (self.hkv,), "k_scale")
             _need(v_scale, torch.float32, (self.hkv,), "v_scale")
@@ -266,7 +266,7 @@ class Plan:
         _need(lse, torch.float32, (self.total_q, self.hq), "lse")
         _need(pq, torch.bfloat16, (self.total_q, self.hp, self.dp), "pq")
         _need(pk_pages, torch.bfloat16, (self.num_pages, 1, 128, self.dp), "pk_pages")
-        _need(kv_block_indexes, torch.int32, (self.n_tiles, self.hkv, self.topk), "kv_block_indexes")
+        _need(kv_block_indexes, torch.int32, (self.n_tiles, self.hp, self.topk), "kv_block_indexes")
         dev = q.device
         if grads is None:
             grads = dict(dq=torch.empty(q.shape, dtype=torch.float32, device=dev),

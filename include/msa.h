@@ -85,12 +85,17 @@ typedef struct msa_plan_s* msa_plan_t;
  *                    kv_lens[s] >= 1.  Copied; the caller keeps ownership.
  *  num_qo_heads      Hq, query heads of the main attention.
  *  num_kv_heads      Hkv, KV heads (GQA groups); Hq % Hkv == 0.
- *  num_proxy_heads   Hp, proxy query heads; must equal Hkv (one proxy head
- *                    per GQA group, [FLASH]).
+ *  num_proxy_heads   Hp, proxy query heads, a multiple of Hkv that divides
+ *                    Hq ([FLASH]: at least one proxy head per GQA group,
+ *                    each with its own block set).  Proxy head p serves
+ *                    query heads [p*Hq/Hp, (p+1)*Hq/Hp), all of KV head
+ *                    p / (Hp/Hkv): with Hp = Hkv that is one proxy head per
+ *                    GQA group; with Hp = m*Hkv each group's query heads
+ *                    split into m sets with a block set each.
  *  head_dim          d in {64, 128}.
  *  proxy_head_dim    dp in {32, 64}.
  *  page_size         must be 128 ([README] "page_size, topk = 128, 16").
- *  topk              K >= 1 selected blocks per (tile, group), the
+ *  topk              K >= 1 selected blocks per (tile, proxy head), the
  *                    diagonal block included.
  *  num_pages         physical pages in the K/V page pool (and the proxy K
  *                    pool, which shares page ids).
@@ -213,16 +218,19 @@ msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages,
  * kv_block_indexes); [STACKS]: paged FP8 decode; [FLASH]: GQA main
  * attention over the selected blocks).
  *
- * For query row i of tile t and head h (group g = h / (Hq/Hkv)): softmax
- * over the keys k of blocks kv_block_indexes[t, g, :] (entries < 0 are
- * skipped) with k visible to i of s = q[i,h].k[k] / sqrt(d); out = P.V,
- * lse = natural-log logsumexp of s.  With FP8 K/V: s uses k*k_scale[g] and
- * V is v*v_scale[g].
+ * For query row i of tile t and head h (KV head g = h / (Hq/Hkv), proxy
+ * head p = h / (Hq/Hp)): softmax over the keys k of KV head g in blocks
+ * kv_block_indexes[t, p, :] (entries < 0 are skipped) with k visible to i
+ * of s = q[i,h].k[k] / sqrt(d); out = P.V, lse = natural-log logsumexp of
+ * s.  With FP8 K/V: s uses k*k_scale[g] and V is v*v_scale[g]
+ * ([STACKS]: FP8 for the paged decode and the sparse prefill).
  *
  *  q                 bf16 [total_q, Hq, d].
- *  k_pages, v_pages  [num_pages, Hkv, 128, d], bf16 or e4m3 per the plan.
+ *  k_pages, v_pages  [num_pages, Hkv, 128, d], bf16 or e4m3 per the plan
+ *                    (e4m3 prefill: head_dim 128; the MMAs run in f16, with
+ *                    q rounded to f16, exact for |q| in [2^-14, 65504]).
  *  kv_indices        int32 page table.
- *  kv_block_indexes  int32 [num_tiles, Hkv, topk], as msa_topk_select writes
+ *  kv_block_indexes  int32 [num_tiles, Hp, topk], as msa_topk_select writes
  *                    them.  Any order of distinct valid blocks is accepted,
  *                    with -1 entries anywhere.  In prefill a query row that
  *                    sees no key of its selection gets out = 0 and
@@ -250,10 +258,14 @@ msa_status msa_sparse_attn(msa_plan_t plan, const void* q, const void* k_pages, 
  * Main part, restricted to the cached blocks and the causal mask, for the
  * scalar sum(out * dout):  D = rowsum(dout*out), dS = P*(dP - D),
  * dq = dS.K/sqrt(d), dk = dS^T.q/sqrt(d) and dv = P^T.dout summed over the
- * G heads of a group.  KL part, per row i and group g over the same keys:
- * p_main = mean of the G heads' P (no gradient), p_proxy = softmax of
- * pq[i,g].pk/sqrt(dp), dZ = kl_weight*(p_proxy - p_main),
- * dpq = dZ.pk/sqrt(dp), dpk = dZ^T.pq/sqrt(dp).
+ * heads (and selections) of a KV head.  KL part, per row i and proxy head p
+ * over the same keys as p's query heads: p_main = mean of the P of the
+ * Hq/Hp heads that use p's blocks (no gradient), p_proxy = softmax of
+ * pq[i,p].pk/sqrt(dp), dZ = kl_weight*(p_proxy - p_main), dpq =
+ * dZ.pk/sqrt(dp), dpk = dZ^T.pq/sqrt(dp).  A page named by several
+ * page-table entries (a shared prefix) gets the sum over all of them in
+ * dk_pages, dv_pages and dpk_pages.  Rows that see no key of their
+ * selection get dq = 0 and dpq = 0 and add nothing elsewhere.
  *
  *  q, k_pages, v_pages, kv_indices, kv_block_indexes  as in the forward
  *                    (bf16 K/V only).

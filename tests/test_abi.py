@@ -55,7 +55,9 @@ def test_host_validation_without_gpu(lib):
     assert b"qo_len <= kv_len" in f.msa_last_error()
     kl[0] = 100
     assert f.msa_plan(ql, kl, 1, 8, 2, 2, 96, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2   # head_dim 96
-    assert f.msa_plan(ql, kl, 1, 8, 2, 4, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2   # Hp != Hkv
+    assert f.msa_plan(ql, kl, 1, 8, 2, 3, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2   # Hp % Hkv != 0
+    assert f.msa_plan(ql, kl, 1, 8, 2, 16, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2  # Hp does not divide Hq
+    assert f.msa_plan(ql, kl, 1, 8, 2, 1, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2   # Hp < Hkv
     assert f.msa_plan(ql, kl, 1, 8, 3, 3, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 1   # Hq % Hkv
     assert f.msa_plan(ql, kl, 1, 8, 2, 2, 64, 32, 64, 4, 16, 0, 0, None, ctypes.byref(h)) == 2    # page 64
     assert f.msa_version() == b"0.1.0"

@@ -8,6 +8,8 @@ Layouts (shared contract, see include/msa.h):
   q, dout        [total_q, Hq, d]          bf16
   k_pages,v_pages[P, Hkv, 128, d]          bf16, or e4m3 with k_scale/v_scale [Hkv] fp32
   pk_pages_e4m3 [P, 1, 128, dp], pk_scale [1]  e4m3 proxy K (e4m3 cases only)
+  pk_fp4_codes [P, 1, 128, dp/2] uint8, pk_fp4_scales [P, 1, 128, dp/16] e4m3,
+  pk_fp4_global [1]                          NVFP4 proxy K (e4m3 cases only)
   pq             [total_q, Hp, dp]         bf16
   pk_pages       [P, 1, 128, dp]           bf16 (one shared proxy K head)
   kv_indices     [sum_s ceil(kv_len_s/128)] int32 page table, logical -> physical
@@ -149,10 +151,36 @@ def make_inputs(case: Case, device="cpu", with_dout=False):
         ps = pk.abs().amax() / 448.0
         out["pk_pages_e4m3"] = (pk / ps).to(torch.float8_e4m3fn)
         out["pk_scale"] = ps.float().reshape(1).contiguous()
+        # ... and in NVFP4: e2m1 code pairs, e4m3 scales of 16 dims, one fp32 scale
+        out.update(nvfp4_quantize(pk))
     if with_dout:
         out["dout"] = _randn((tq, case.hq, case.d), gen, dev).to(torch.bfloat16)
     del q, k, v, pq, pk
     return out
+
+
+E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)   # codes 0..7 of the OCP FP4 E2M1 format
+
+
+def nvfp4_quantize(x):
+    """Quantise x [..., D] (D a multiple of 16) to NVFP4 inputs: each block of
+    16 dims gets an e4m3 scale amax/6 (relative to one fp32 global scale
+    amax/(448*6)), and each value the nearest e2m1 code (ties to the smaller
+    magnitude); code pairs are packed with the even dim in the low nibble.
+    Returns pk_fp4_codes uint8 [..., D/2], pk_fp4_scales e4m3 [..., D/16],
+    pk_fp4_global fp32 [1]."""
+    x = x.float()
+    gs = (x.abs().amax() / (448.0 * 6.0)).clamp_min(1e-30)
+    blk = x.reshape(*x.shape[:-1], x.shape[-1] // 16, 16)
+    bs = (blk.abs().amax(-1) / (6.0 * gs)).to(torch.float8_e4m3fn)
+    denom = (bs.float() * gs).unsqueeze(-1)
+    y = torch.where(denom > 0, blk / torch.where(denom > 0, denom, torch.ones_like(denom)), torch.zeros_like(blk))
+    mags = torch.tensor(E2M1_MAGNITUDES, dtype=torch.float32, device=x.device)
+    k = (y.abs().unsqueeze(-1) - mags).abs().argmin(-1)                  # nearest magnitude, lower on ties
+    code = (k | ((y < 0) & (k > 0)).to(k.dtype) << 3).to(torch.uint8).reshape(x.shape)
+    packed = code[..., 0::2] | (code[..., 1::2] << 4)
+    return {"pk_fp4_codes": packed.contiguous(), "pk_fp4_scales": bs.contiguous(),
+            "pk_fp4_global": gs.reshape(1).float().contiguous()}
 
 
 def bits(t: torch.Tensor):

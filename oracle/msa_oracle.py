@@ -63,6 +63,10 @@ Readings where the pages are silent:
   R11 an FP8 e4m3 proxy K (decode) carries one fp32 scale for the single
       shared proxy head, dequantised like R5: logit =
       (pq.pk_code)*pk_scale/sqrt(dp).
+  R12 an NVFP4 proxy K (the FP4 block-score indexer) follows the public
+      NVFP4 format: e2m1 codes, two per byte with the even dimension in the
+      low nibble, one e4m3 scale per 16 consecutive dimensions of a key and
+      one fp32 scale for the head; pk = code * block scale * global scale.
 """
 from __future__ import annotations
 
@@ -99,6 +103,30 @@ def e4m3_to_f64(bits) -> np.ndarray:
     v = sign * np.where(e == 0, sub, normal)
     v = np.where((e == 15) & (m == 7), np.nan, v)
     return v
+
+
+def e2m1_to_f64(nibbles) -> np.ndarray:
+    """OCP FP4 E2M1 4-bit codes -> float64 from the format's definition:
+    1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit; exponent field 0
+    is subnormal (m * 2^-1); no infinities or NaN."""
+    b = np.asarray(nibbles).astype(np.int64) & 0xF
+    sign = np.where(b >> 3, -1.0, 1.0)
+    e = (b >> 1) & 0x3
+    m = b & 0x1
+    normal = np.ldexp(1.0 + m / 2.0, (e - 1).astype(np.int64))
+    return sign * np.where(e == 0, m * 0.5, normal)
+
+
+def nvfp4_to_f64(code_bytes, scale_bits, global_scale) -> np.ndarray:
+    """NVFP4 values (R12): code bytes [..., D/2] (byte b holds dims 2b in
+    its low nibble and 2b+1 in its high nibble), e4m3 block scales
+    [..., D/16] (one per 16 consecutive dims) and one fp32 global scale ->
+    float64 [..., D] = e2m1(code) * e4m3(block scale) * global_scale."""
+    cb = np.ascontiguousarray(code_bytes).view(np.uint8)
+    vals = np.stack([e2m1_to_f64(cb & 0xF), e2m1_to_f64(cb >> 4)], axis=-1)
+    vals = vals.reshape(cb.shape[:-1] + (2 * cb.shape[-1],))
+    sc = np.repeat(e4m3_to_f64(scale_bits), 16, axis=-1)
+    return vals * sc * float(global_scale)
 
 
 # ---------------------------------------------------------------------------
@@ -159,14 +187,16 @@ def gather_seq(pages: np.ndarray, kv_indices, indptr, seq: int, kv_len: int) -> 
 # stage 1: proxy max score (R2)
 # ---------------------------------------------------------------------------
 
-def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=None, pk_scale=None):
+def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=None, pk_scale=None,
+                    pk_nvfp4=None):
     """max_score[t, h, j] = max over rows i of tile t and keys k of block j
     with k visible to i of pq[i,h].pk[k]/sqrt(dp), rounded once to fp32;
     -inf where no pair is visible.  pq: [total_q, Hp, dp] bf16 bits;
     pk: [P, 1, 128, dp] bf16 bits (one shared proxy K head, [README]
     "num_kv_heads=1"), or e4m3 codes (uint8) with pk_scale, pk = code *
-    pk_scale (R11).  Returns float32 [n_tiles, Hp, nb_max]; tiles not in
-    tile_ids stay -inf."""
+    pk_scale (R11), or NVFP4 code bytes [P, 1, 128, dp/2] with pk_nvfp4 =
+    (block scale bits [P, 1, 128, dp/16], global scale) (R12).  Returns
+    float32 [n_tiles, Hp, nb_max]; tiles not in tile_ids stay -inf."""
     # bit patterns are decoded per tile (the decode is exact), so that large
     # page pools never need a float64 copy
     pq_bits, pk_bits = np.asarray(pq_bits), np.asarray(pk_bits)
@@ -178,7 +208,13 @@ def proxy_max_score(pq_bits, pk_bits, kv_indices, qo_lens, kv_lens, tile_ids=Non
         tl = tiles[ti]
         nk = min(tl.nvp * PAGE, tl.kv_len)
         raw = gather_seq(pk_bits, kv_indices, indptr, tl.seq, tl.kv_len)[:nk, 0, :]
-        keys = bf16_to_f64(raw) if pk_scale is None else e4m3_to_f64(raw) * float(pk_scale)  # [nk, dp]
+        if pk_nvfp4 is not None:
+            sbits = gather_seq(np.asarray(pk_nvfp4[0]), kv_indices, indptr, tl.seq, tl.kv_len)[:nk, 0, :]
+            keys = nvfp4_to_f64(raw, sbits, pk_nvfp4[1])                          # [nk, dp]
+        elif pk_scale is not None:
+            keys = e4m3_to_f64(raw) * float(pk_scale)
+        else:
+            keys = bf16_to_f64(raw)
         qrows = bf16_to_f64(pq_bits[tl.q_begin: tl.q_end])                     # [R, hp, dp]
         logits = np.matmul(qrows.transpose(1, 0, 2), keys.T) / math.sqrt(dp)   # [hp, R, nk]
         qpos = tl.pos0 + np.arange(tl.q_end - tl.q_begin)

@@ -688,3 +688,40 @@ def test_hp2_kl_grad_finite_differences():
         b[i, hh, c] -= h
         fd = (O.kl_objective(a, pk, *args) - O.kl_objective(b, pk, *args)) / (2 * h)
         assert abs(fd - g["dpq"][i, hh, c]) <= 1e-6 * max(1.0, abs(fd)), (i, hh, c, fd, g["dpq"][i, hh, c])
+
+
+# ------------------------------------------------ NVFP4 proxy K (R12) -------
+
+def test_e2m1_decode_all_codes():
+    """The 16 e2m1 codes decode to the format's published values: +-{0, 0.5,
+    1, 1.5, 2, 3, 4, 6} (code 8 is -0)."""
+    got = O.e2m1_to_f64(np.arange(16))
+    want = np.array(list(synth.E2M1_MAGNITUDES) + [-m for m in synth.E2M1_MAGNITUDES])
+    assert np.array_equal(got, want)
+    assert np.signbit(got[8])
+
+
+def test_proxy_nvfp4_reduces_to_bf16_route():
+    """NVFP4 proxy keys whose values are exact in bf16 (a power-of-two global
+    scale) give exactly the scores of the bf16 route on those values, which
+    this test builds from the published e2m1 table and torch's e4m3
+    conversion: a swapped nibble order, a wrong 16-dim scale grouping or a
+    dropped scale fails."""
+    qo, kv, dp = [1, 1, 2], [300, 129, 700], 64
+    gen = torch.Generator().manual_seed(13)
+    nb = sum((k + PAGE - 1) // PAGE for k in kv)
+    codes = torch.randint(0, 256, (nb + 1, 1, PAGE, dp // 2), generator=gen, dtype=torch.int32).to(torch.uint8)
+    scales = (torch.rand(nb + 1, 1, PAGE, dp // 16, generator=gen) * 30 + 0.01).to(torch.float8_e4m3fn)
+    gscale = 0.125
+    mags = torch.tensor(synth.E2M1_MAGNITUDES, dtype=torch.float64)
+    lo, hi = codes.long() & 0xF, codes.long() >> 4
+    nib = torch.stack([lo, hi], -1).reshape(nb + 1, 1, PAGE, dp)
+    vals = torch.where(nib >= 8, -1.0, 1.0).double() * mags[nib & 7]
+    vals = vals * scales.double().repeat_interleave(16, -1) * gscale
+    assert torch.equal(vals.to(torch.bfloat16).double(), vals)          # exact in bf16
+    pq = torch.randn(4, 2, dp, generator=gen).to(torch.bfloat16)
+    table = torch.randperm(nb + 1, generator=gen)[:nb].numpy()
+    ref = O.proxy_max_score(synth.bits(pq), synth.bits(vals.to(torch.bfloat16)), table, qo, kv)
+    got = O.proxy_max_score(synth.bits(pq), codes.numpy(), table, qo, kv, pk_nvfp4=(synth.bits(scales), gscale))
+    assert np.array_equal(got, ref)
+    assert np.isfinite(got[:, :, 0]).all()

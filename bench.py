@@ -589,6 +589,9 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
     # the same scan over the e4m3 proxy K (msa_proxy_maxscore_fp8)
     tp8 = per_launch_s(lambda: plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"],
                                                        inp["kv_indices"], out=ms))
+    # ... and over the NVFP4 proxy K, the FP4 block-score indexer (msa_proxy_maxscore_nvfp4)
+    tp4 = per_launch_s(lambda: plan.proxy_maxscore_nvfp4(inp["pq"], inp["pk_fp4_codes"], inp["pk_fp4_scales"],
+                                                         inp["pk_fp4_global"], inp["kv_indices"], out=ms))
     plan.check_errors()
     gbs = (kv_bytes + io_bytes) / t / 1e9
     proxy_bytes = sum((k + 127) // 128 for k in case.kv_lens) * 128 * case.dp * 2
@@ -600,6 +603,9 @@ def bench_decode(args, dev, pk_info, peak_kind, world):
             "proxy_scan_frac": proxy_bytes / tp / 1e9 / hbm,
             "proxy_scan_fp8_us": tp8 * 1e6, "proxy_scan_fp8_gbs": proxy_bytes / 2 / tp8 / 1e9,
             "proxy_scan_fp8_frac": proxy_bytes / 2 / tp8 / 1e9 / hbm,
+            # NVFP4: 32 code bytes and 4 scale bytes per key at dp = 64
+            "proxy_scan_nvfp4_us": tp4 * 1e6, "proxy_scan_nvfp4_gbs": proxy_bytes * 9 / 32 / tp4 / 1e9,
+            "proxy_scan_nvfp4_frac": proxy_bytes * 9 / 32 / tp4 / 1e9 / hbm,
             "timing": "per launch = (T(N x [L2 flush, kernel]) - T(N x [L2 flush])) / N, N = %d, median of 5" % n_batch}
 
 

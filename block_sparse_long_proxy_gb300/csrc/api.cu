@@ -276,6 +276,21 @@ msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* p
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+msa_status msa_proxy_maxscore_nvfp4(msa_plan_t plan, const void* pq, const void* pk_codes,
+                                    const void* pk_block_scales, const float* pk_global_scale,
+                                    const int32_t* kv_indices, float* max_score, msa_stream_t stream) {
+  if (!plan || !pq || !pk_codes || !pk_block_scales || !pk_global_scale || !kv_indices || !max_score)
+    return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore_nvfp4: NULL argument");
+  if (!aligned16(pq) || !aligned16(pk_codes) || !aligned16(pk_block_scales))
+    return set_error(MSA_ERR_INVALID_ARG,
+                     "msa_proxy_maxscore_nvfp4: pq, pk_codes and pk_block_scales must be 16-byte aligned");
+  if (!plan->decode)
+    return set_error(MSA_ERR_UNSUPPORTED,
+                     "msa_proxy_maxscore_nvfp4: the NVFP4 proxy K is implemented for decode batches only");
+  return launch_proxy_decode_nvfp4(plan, pq, pk_codes, pk_block_scales, pk_global_scale, kv_indices, max_score,
+                                   reinterpret_cast<cudaStream_t>(stream));
+}
+
 msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                           float* max_score, int32_t* kv_block_indexes, msa_stream_t stream) {
   if (!plan || !pq || !pk_pages || !kv_indices || !kv_block_indexes)

@@ -125,6 +125,11 @@ msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* 
 // decode proxy scan over e4m3 proxy K pages with one fp32 scale (device pointer)
 msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const void* pk_pages, const float* pk_scale,
                                    const int32_t* kv_indices, float* max_score, cudaStream_t st);
+// decode proxy scan over an NVFP4 proxy K (proxy_fp4.cu): e2m1 codes [P, 128, dp/2],
+// e4m3 block scales [P, 128, dp/16] and one fp32 scale (device pointer)
+msa_status launch_proxy_decode_nvfp4(const msa_plan_s* p, const void* pq, const void* pk_codes,
+                                     const void* pk_block_scales, const float* pk_global_scale,
+                                     const int32_t* kv_indices, float* max_score, cudaStream_t st);
 
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages,
                                const void* v_pages, const int32_t* kv_indices, const int32_t* idx,

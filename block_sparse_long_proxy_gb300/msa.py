@@ -40,6 +40,7 @@ SIGNATURES = {
     "msa_plan_num_valid_pages": (_p, [_p]),
     "msa_proxy_maxscore": (_i32, [_p, _p, _p, _p, _p, _p]),
     "msa_proxy_maxscore_fp8": (_i32, [_p, _p, _p, _p, _p, _p, _p]),
+    "msa_proxy_maxscore_nvfp4": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p]),
     "msa_proxy_topk": (_i32, [_p, _p, _p, _p, _p, _p, _p]),
     "msa_topk_select": (_i32, [_p, _i32, _i32, _i32, _i32, _p, _p, _p]),
     "msa_sparse_attn": (_i32, [_p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p]),
@@ -216,6 +217,24 @@ class Plan:
         _need(out, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
         _check(_lib.msa_proxy_maxscore_fp8(self._h, _ptr(pq), _ptr(pk_pages), _ptr(pk_scale), _ptr(kv_indices),
                                            _ptr(out), _stream(stream)), "msa_proxy_maxscore_fp8")
+        return out
+
+    def proxy_maxscore_nvfp4(self, pq, pk_codes, pk_block_scales, pk_global_scale, kv_indices, out=None,
+                             stream=None):
+        """Decode proxy pass over an NVFP4 proxy K (msa_proxy_maxscore_nvfp4):
+        uint8 e2m1 code pairs [P, 1, 128, dp/2], e4m3 block scales [P, 1, 128,
+        dp/16] and one fp32 global scale."""
+        _need(pq, torch.bfloat16, (self.total_q, self.hp, self.dp), "pq")
+        _need(pk_codes, torch.uint8, (self.num_pages, 1, 128, self.dp // 2), "pk_codes")
+        _need(pk_block_scales, torch.float8_e4m3fn, (self.num_pages, 1, 128, self.dp // 16), "pk_block_scales")
+        _need(pk_global_scale, torch.float32, (1,), "pk_global_scale")
+        _need(kv_indices, torch.int32, (self.n_page_entries,), "kv_indices")
+        if out is None:
+            out = torch.empty((self.n_tiles, self.hp, self.max_blocks), dtype=torch.float32, device=pq.device)
+        _need(out, torch.float32, (self.n_tiles, self.hp, self.max_blocks), "max_score")
+        _check(_lib.msa_proxy_maxscore_nvfp4(self._h, _ptr(pq), _ptr(pk_codes), _ptr(pk_block_scales),
+                                             _ptr(pk_global_scale), _ptr(kv_indices), _ptr(out), _stream(stream)),
+               "msa_proxy_maxscore_nvfp4")
         return out
 
     def proxy_topk(self, pq, pk_pages, kv_indices, out=None, max_score=None, stream=None):

@@ -162,6 +162,34 @@ msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* p
                                   msa_stream_t stream);
 
 /*
+ * msa_proxy_maxscore_nvfp4 -- stage 1 at decode with the proxy K stored in
+ * NVFP4, the FP4 block-score indexer ("MiniMax-AI/MSA" README, section
+ * "Stacks": the FP4 block-score indexer; Flash-MSA article, "what's next":
+ * the indexer in low precision).  The shared proxy head's keys are e2m1
+ * codes with one e4m3 scale per 16 consecutive dimensions and one fp32
+ * scale for the head:
+ *   pk[k, d] = e2m1(code[k, d]) * e4m3(block_scale[k, d / 16]) * global_scale
+ * and the logit of a pair is pq[i,h] . pk[k] / sqrt(dp); otherwise max_score
+ * is defined as in msa_proxy_maxscore.  The proxy K read is a quarter of the
+ * bf16 one (plus 1/8 for the scales).
+ *
+ *  pq               bf16 [total_q, Hp, dp].
+ *  pk_codes         uint8 [num_pages, 1, 128, dp / 2], 16-byte aligned: byte
+ *                   b of a key holds dims 2b (low nibble) and 2b + 1 (high
+ *                   nibble), each e2m1 (1 sign, 2 exponent bits with bias 1,
+ *                   1 mantissa bit; exponent 0 is 0 or 0.5).
+ *  pk_block_scales  e4m3 [num_pages, 1, 128, dp / 16], 16-byte aligned.
+ *  pk_global_scale  device pointer to one fp32 scale (> 0).
+ * Decode plans (every qo_len == 1) with dp = 64 and Hp <= 8 only; others
+ * return MSA_ERR_UNSUPPORTED.  The products run on f16 tensor cores with pq
+ * rounded to f16 (exact for |pq| in [2^-14, 65504]); code * block scale is
+ * exact in f16.
+ */
+msa_status msa_proxy_maxscore_nvfp4(msa_plan_t plan, const void* pq, const void* pk_codes,
+                                    const void* pk_block_scales, const float* pk_global_scale,
+                                    const int32_t* kv_indices, float* max_score, msa_stream_t stream);
+
+/*
  * msa_topk_select -- stage 2 ([README] sparse_topk_select(max_score, topk,
  * num_valid_pages); [FLASH]: each proxy head picks its own block set, the
  * local block is always visible).  Plan-free, like the reference call.

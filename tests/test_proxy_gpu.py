@@ -110,3 +110,59 @@ def test_proxy_fp8_rejects_prefill_plans(cuda_dev):
     with pytest.raises(msa.MsaError) as e:
         plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"])
     assert e.value.status == 2
+
+
+def _run_nvfp4(case, dev, tile_ids=None):
+    """msa_proxy_maxscore_nvfp4 (the FP4 block-score indexer) against the
+    oracle's R12 route on the same codes and scales; the top-k of the GPU's
+    scores equals the oracle's top-k of them (bit-exact)."""
+    from block_sparse_long_proxy_gb300 import msa
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
+    ms = plan.proxy_maxscore_nvfp4(inp["pq"], inp["pk_fp4_codes"], inp["pk_fp4_scales"], inp["pk_fp4_global"],
+                                   inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    torch.cuda.synchronize()
+    plan.check_errors()
+    got = ms.cpu().numpy()
+    ref = O.proxy_max_score(synth.bits(inp["pq"]), inp["pk_fp4_codes"].cpu().numpy(), inp["kv_indices"].cpu().numpy(),
+                            case.qo_lens, case.kv_lens, tile_ids=tile_ids,
+                            pk_nvfp4=(synth.bits(inp["pk_fp4_scales"]), float(inp["pk_fp4_global"][0])))
+    nvp = O.num_valid_pages(case.qo_lens, case.kv_lens)
+    ids = list(range(len(nvp))) if tile_ids is None else tile_ids
+    assert np.array_equal(idx.cpu().numpy()[ids], O.topk_select(got[ids], case.topk, nvp[ids]))
+    got, ref = got[ids], ref[ids]
+    assert np.array_equal(np.isneginf(got), np.isneginf(ref))
+    fin = np.isfinite(ref)
+    err = np.abs(got[fin] - ref[fin]).max() if fin.any() else 0.0
+    assert err <= ATOL, err
+    return err
+
+
+@pytest.mark.parametrize("case", [
+    synth.Case("nvfp4 proxy decode ragged", [1] * 5, [700, 129, 128, 1, 5000], 16, 8, 128, 8, 64, 4,
+               kv_dtype="e4m3", page_perm_seed=2, extra_pages=3),
+    synth.Case("nvfp4 proxy decode 3 heads", [1] * 3, [300, 4096, 77], 6, 3, 128, 3, 64, 4, kv_dtype="e4m3",
+               page_perm_seed=4),
+    synth.Case("nvfp4 proxy decode 70 sequences", [1] * 70, [int(x) for x in np.arange(70) * 211 + 1], 16, 8, 128, 8,
+               64, 6, kv_dtype="e4m3", page_perm_seed=5),
+], ids=lambda c: c.name)
+def test_proxy_decode_nvfp4_small(cuda_dev, case):
+    _run_nvfp4(case, cuda_dev)
+
+
+def test_proxy_decode_nvfp4_full_size_sampled(cuda_dev):
+    _run_nvfp4(synth.paged_decode(), cuda_dev, tile_ids=[0, 7, 31])
+
+
+def test_proxy_nvfp4_rejects_prefill_plans(cuda_dev):
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("nvfp4 proxy prefill", [256], [256], 4, 2, 128, 2, 64, 2, kv_dtype="e4m3")
+    inp = synth.make_inputs(case, device=cuda_dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0], kv_dtype=case.kv_dtype)
+    with pytest.raises(msa.MsaError) as e:
+        plan.proxy_maxscore_nvfp4(inp["pq"], inp["pk_fp4_codes"], inp["pk_fp4_scales"], inp["pk_fp4_global"],
+                                  inp["kv_indices"])
+    assert e.value.status == 2

@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
                     float* __restrict__ lse, int32_t hq, int32_t hsel, int32_t kv_div, int32_t topk,
                     float scale_log2, const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                     uint32_t* err) {
+  pdl_wait();
   // hsel block sets (proxy heads) per tile; a unit's u.g is its proxy head,
   // whose blocks are read from KV head u.g / kv_div of hsel / kv_div
   const int hkv = hsel / kv_div;
@@ -605,26 +606,27 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->d));
   auto* o = static_cast<__nv_bfloat16*>(out);
   const int grid = std::min(p->n_attn_units, p->num_sms);  // persistent: one CTA per SM
+  cudaError_t e;
   if (fp8) {
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<128, false, true><<<grid, attn_threads(true), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
-        p->hp / p->hkv, p->topk, scale_log2, k_scale, v_scale, p->err_d);
+    e = launch_pdl(attn_fwd_kernel<128, false, true>, dim3(grid), dim3(attn_threads(true)), smem, st, qm, km, vm, units,
+                   p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp, p->hp / p->hkv,
+                   p->topk, scale_log2, k_scale, v_scale, p->err_d);
   } else if (p->d == 128) {
     const int smem = AttnSmem<128>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<128, false, false><<<grid, attn_threads(false), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
-        p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
+    e = launch_pdl(attn_fwd_kernel<128, false, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm, km, vm,
+                   units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
+                   p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   } else {
     const int smem = AttnSmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(attn_fwd_kernel<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attn_fwd_kernel<64, false, false><<<grid, attn_threads(false), smem, st>>>(
-        qm, km, vm, units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
-        p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
+    e = launch_pdl(attn_fwd_kernel<64, false, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm, km, vm,
+                   units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
+                   p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
   }
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn: prefill launch");
+  return cuda_check(e, "msa_sparse_attn: prefill launch");
 }
 
 // The proxy softmax of the backward (the KL term's p_proxy): for proxy head g
@@ -652,10 +654,11 @@ msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void*
   const int grid = std::min(p->n_proxy_attn_units, p->num_sms);
   const int smem = AttnSmem<64>::kBytes + 1024;
   cudaFuncSetAttribute(attn_fwd_kernel<64, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  attn_fwd_kernel<64, true, false><<<grid, attn_threads(false), smem, st>>>(
-      qm, km, km, units, p->n_proxy_attn_units, p->tiles_d, idx, kv_indices, p->num_pages,
-      static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hp, p->hp, p->topk, scale_log2, nullptr, nullptr, p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: proxy softmax launch");
+  return cuda_check(launch_pdl(attn_fwd_kernel<64, true, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm,
+                                km, km, units, p->n_proxy_attn_units, p->tiles_d, idx, kv_indices, p->num_pages,
+                                static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hp, p->hp, p->topk, scale_log2,
+                                static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), p->err_d),
+                    "msa_sparse_attn_bwd: proxy softmax launch");
 }
 
 }  // namespace msa

@@ -80,6 +80,7 @@ __global__ void __launch_bounds__(kDThreads, NT == 1 ? 2 : 1)
                   float* __restrict__ part_ml, int32_t* __restrict__ row_cnt, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int32_t n_units, int32_t hq, int32_t hsel, int32_t kv_div, int32_t topk,
                   float scale_log2, uint32_t* err) {
+  pdl_wait();
   // A row is (sequence, proxy head p): the G = hq / hsel query heads of p
   // attend over p's blocks of KV head p / kv_div (kv_div proxy heads per KV
   // head; 1 when there is one proxy head per GQA group).
@@ -501,20 +502,21 @@ msa_status launch_attn_decode(const msa_plan_s* p, const void* q, const void* k_
   auto* o_ptr = static_cast<__nv_bfloat16*>(out);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(kD));
   const auto* qq = static_cast<const __nv_bfloat16*>(q);
+  cudaError_t e;
   if (G <= 8) {
     const int smem = DecodeSmem<1>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    decode_kernel<1><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
-                                                     v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
-                                                     p->hp, kv_div, p->topk, scale_log2, p->err_d);
+    e = launch_pdl(decode_kernel<1>, dim3(grid), dim3(kDThreads), smem, st, km, vm, qq, p->tiles_d, idx, kv_indices,
+                   p->num_pages, k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq, p->hp, kv_div,
+                   p->topk, scale_log2, p->err_d);
   } else {
     const int smem = DecodeSmem<2>::kBytes + 1024;
     cudaFuncSetAttribute(decode_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    decode_kernel<2><<<grid, kDThreads, smem, st>>>(km, vm, qq, p->tiles_d, idx, kv_indices, p->num_pages, k_scale,
-                                                     v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq,
-                                                     p->hp, kv_div, p->topk, scale_log2, p->err_d);
+    e = launch_pdl(decode_kernel<2>, dim3(grid), dim3(kDThreads), smem, st, km, vm, qq, p->tiles_d, idx, kv_indices,
+                   p->num_pages, k_scale, v_scale, part_o, part_ml, row_cnt, o_ptr, lse, n_units, p->hq, p->hp, kv_div,
+                   p->topk, scale_log2, p->err_d);
   }
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
+  return cuda_check(e, "msa_sparse_attn: decode launch");
 }
 
 }  // namespace msa

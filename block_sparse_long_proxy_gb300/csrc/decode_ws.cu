@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(kWsThreads, 2)
                      const float* __restrict__ k_scale, const float* __restrict__ v_scale,
                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse, int32_t hq, int32_t hsel,
                      int32_t kv_div, int32_t topk, float scale_log2, uint32_t* err) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -306,11 +307,12 @@ msa_status launch_attn_decode_ws(const msa_plan_s* p, const void* q, const void*
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
   const int smem = WsSmem::kBytes + 1024;
   cudaFuncSetAttribute(decode_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  decode_ws_kernel<<<p->n_tiles * p->hp, kWsThreads, smem, st>>>(
-      km, vm, static_cast<const __nv_bfloat16*>(q), p->tiles_d, idx, kv_indices, p->num_pages, k_scale, v_scale,
-      static_cast<__nv_bfloat16*>(out), lse, p->hq, p->hp, p->hp / p->hkv, p->topk,
-      1.4426950408889634f / sqrtf(static_cast<float>(kD)), p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn: decode launch");
+  return cuda_check(launch_pdl(decode_ws_kernel, dim3(p->n_tiles * p->hp), dim3(kWsThreads), smem, st, km, vm,
+                                static_cast<const __nv_bfloat16*>(q), p->tiles_d, idx, kv_indices, p->num_pages,
+                                k_scale, v_scale, static_cast<__nv_bfloat16*>(out), lse, p->hq, p->hp,
+                                p->hp / p->hkv, p->topk, 1.4426950408889634f / sqrtf(static_cast<float>(kD)),
+                                p->err_d),
+                    "msa_sparse_attn: decode launch");
 }
 
 }  // namespace msa

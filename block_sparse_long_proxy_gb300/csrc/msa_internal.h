@@ -84,6 +84,26 @@ struct msa_plan_s {
 
 namespace msa {
 
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel in the stream drains, which hides the
+// launch gap between the short kernels of a decode step; the kernel must
+// call pdl_wait() (ptx.cuh) before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 msa_status set_error(msa_status s, const char* fmt, ...);
 msa_status cuda_check(cudaError_t e, const char* what);
 

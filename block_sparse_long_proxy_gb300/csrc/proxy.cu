@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const ProxyUnit* __restrict__ units, const TileInfo* __restrict__ tiles,
                          const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
                          int32_t hp, int32_t max_blocks, float scale, FusedTopk fz, uint32_t* err) {
+  pdl_wait();
   using L = ProxySmem<DP>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -381,6 +382,7 @@ __global__ void __launch_bounds__(32 * kDecWarps)
                         const TileInfo* __restrict__ tiles, const int32_t* __restrict__ unit_start, int32_t n_tiles,
                         const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
                         int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+  pdl_wait();
   constexpr int kBlk = 128 * DP * 2;
   constexpr int kRowBytes = DP * 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -544,6 +546,7 @@ __global__ void __launch_bounds__(32 * W)
                             const int32_t* __restrict__ unit_start, int32_t n_tiles,
                             const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
                             int32_t hp, int32_t max_blocks, float scale, uint32_t* err) {
+  pdl_wait();
   constexpr int DP = 64;
   constexpr int kBlk = 128 * DP;  // bytes of one e4m3 proxy K page
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -735,18 +738,19 @@ static msa_status proxy_prefill(const msa_plan_s* p, const void* pq, const void*
     return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore: tensor map encoding failed");
   const ProxyUnit* units = reinterpret_cast<const ProxyUnit*>(p->aux_d + p->proxy_units_off);
   const float scale = 1.0f / sqrtf(static_cast<float>(p->dp));
+  cudaError_t e;
   if (p->dp == 64) {
     const int smem = ProxySmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    proxy_prefill_kernel<64><<<p->n_proxy_units, kThreads, smem, st>>>(
-        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
+    e = launch_pdl(proxy_prefill_kernel<64>, dim3(p->n_proxy_units), dim3(kThreads), smem, st, qm, km, units,
+                   p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   } else {
     const int smem = ProxySmem<32>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    proxy_prefill_kernel<32><<<p->n_proxy_units, kThreads, smem, st>>>(
-        qm, km, units, p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
+    e = launch_pdl(proxy_prefill_kernel<32>, dim3(p->n_proxy_units), dim3(kThreads), smem, st, qm, km, units,
+                   p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   }
-  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: prefill launch");
+  return cuda_check(e, "msa_proxy_maxscore: prefill launch");
 }
 
 msa_status launch_proxy_prefill(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
@@ -791,20 +795,19 @@ msa_status launch_proxy_decode(const msa_plan_s* p, const void* pq, const void* 
   const float scale = 1.0f / sqrtf(static_cast<float>(p->dp));
   const int grid = p->num_sms;
   const auto* q = static_cast<const __nv_bfloat16*>(pq);
+  cudaError_t e;
   if (p->dp == 64) {
     const int smem = kDecWarps * kDecStages * 128 * 64 * 2 + kDecWarps * kDecStages * 8 + 1024;
     cudaFuncSetAttribute(proxy_decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    proxy_decode_kernel<64><<<grid, 32 * kDecWarps, smem, st>>>(km, q, p->tiles_d, ustart, p->n_tiles, kv_indices,
-                                                                 p->num_pages, max_score, p->hp, p->max_blocks, scale,
-                                                                 p->err_d);
+    e = launch_pdl(proxy_decode_kernel<64>, dim3(grid), dim3(32 * kDecWarps), smem, st, km, q, p->tiles_d, ustart,
+                   p->n_tiles, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
   } else {
     const int smem = kDecWarps * kDecStages * 128 * 32 * 2 + kDecWarps * kDecStages * 8 + 1024;
     cudaFuncSetAttribute(proxy_decode_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    proxy_decode_kernel<32><<<grid, 32 * kDecWarps, smem, st>>>(km, q, p->tiles_d, ustart, p->n_tiles, kv_indices,
-                                                                 p->num_pages, max_score, p->hp, p->max_blocks, scale,
-                                                                 p->err_d);
+    e = launch_pdl(proxy_decode_kernel<32>, dim3(grid), dim3(32 * kDecWarps), smem, st, km, q, p->tiles_d, ustart,
+                   p->n_tiles, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d);
   }
-  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore: decode launch");
+  return cuda_check(e, "msa_proxy_maxscore: decode launch");
 }
 
 msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const void* pk_pages, const float* pk_scale,
@@ -822,10 +825,10 @@ msa_status launch_proxy_decode_fp8(const msa_plan_s* p, const void* pq, const vo
   constexpr int W = kDec8Warps, S = kDec8Stages;
   const int smem = W * S * 128 * 64 + W * S * 8 + 1024;
   cudaFuncSetAttribute(proxy_decode_fp8_kernel<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  proxy_decode_fp8_kernel<W, S><<<p->num_sms, 32 * W, smem, st>>>(
-      km, static_cast<const __nv_bfloat16*>(pq), pk_scale, p->tiles_d, ustart, p->n_tiles, kv_indices, p->num_pages,
-      max_score, p->hp, p->max_blocks, scale, p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore_fp8: launch");
+  return cuda_check(launch_pdl(proxy_decode_fp8_kernel<W, S>, dim3(p->num_sms), dim3(32 * W), smem, st, km,
+                                static_cast<const __nv_bfloat16*>(pq), pk_scale, p->tiles_d, ustart, p->n_tiles,
+                                kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, p->err_d),
+                    "msa_proxy_maxscore_fp8: launch");
 }
 
 }  // namespace msa

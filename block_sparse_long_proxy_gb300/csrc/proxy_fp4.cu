@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(32 * W)
                               int32_t n_tiles, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                               float* __restrict__ max_score, int32_t hp, int32_t max_blocks, float scale,
                               uint32_t* err) {
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -229,11 +230,12 @@ msa_status launch_proxy_decode_nvfp4(const msa_plan_s* p, const void* pq, const 
   constexpr int W = kFp4Warps, S = kFp4Stages;
   const int smem = W * S * kStageBytes + W * S * 8 + 1024;
   cudaFuncSetAttribute(proxy_decode_nvfp4_kernel<W, S>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  proxy_decode_nvfp4_kernel<W, S><<<p->num_sms, 32 * W, smem, st>>>(
-      static_cast<const uint8_t*>(pk_codes), static_cast<const uint8_t*>(pk_block_scales), pk_global_scale,
-      static_cast<const __nv_bfloat16*>(pq), p->tiles_d, ustart, p->n_tiles, kv_indices, p->num_pages, max_score,
-      p->hp, p->max_blocks, 1.0f / sqrtf(static_cast<float>(kDP)), p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_proxy_maxscore_nvfp4: launch");
+  return cuda_check(launch_pdl(proxy_decode_nvfp4_kernel<W, S>, dim3(p->num_sms), dim3(32 * W), smem, st,
+                                static_cast<const uint8_t*>(pk_codes), static_cast<const uint8_t*>(pk_block_scales),
+                                pk_global_scale, static_cast<const __nv_bfloat16*>(pq), p->tiles_d, ustart,
+                                p->n_tiles, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks,
+                                1.0f / sqrtf(static_cast<float>(kDP)), p->err_d),
+                    "msa_proxy_maxscore_nvfp4: launch");
 }
 
 }  // namespace msa

@@ -14,6 +14,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may start
+// while the kernel before it in the stream is still finishing; pdl_wait()
+// returns once that kernel has completed and its writes are visible.  Every
+// such kernel calls it before its first global read or write.  Without the
+// launch attribute it returns at once.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -16,6 +16,7 @@
 // are still needed in ascending j order, then j_d: the result is bit-exact
 // and already sorted.  HBM traffic is one coalesced read of the row.
 #include "msa_internal.h"
+#include "ptx.cuh"
 
 namespace msa {
 namespace {
@@ -28,6 +29,7 @@ template <int KPL>
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     topk_kernel(const float* __restrict__ max_score, int32_t rows, int32_t heads, int32_t max_blocks,
                 int32_t topk, const int32_t* __restrict__ nvp_arr, int32_t* __restrict__ out) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -103,6 +105,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock)
 __global__ void __launch_bounds__(32 * kWarpsPerBlock)
     topk_kernel_long(const float* __restrict__ max_score, int32_t rows, int32_t heads, int32_t max_blocks,
                      int32_t topk, const int32_t* __restrict__ nvp_arr, int32_t* __restrict__ out) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -167,13 +170,14 @@ msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, i
                        const int32_t* nvp, int32_t* out, cudaStream_t st) {
   const int32_t rows = n_tiles * heads;
   const dim3 grid((rows + kWarpsPerBlock - 1) / kWarpsPerBlock), block(32 * kWarpsPerBlock);
+  cudaError_t e;
   if (max_blocks <= 256)
-    topk_kernel<8><<<grid, block, 0, st>>>(max_score, rows, heads, max_blocks, topk, nvp, out);
+    e = launch_pdl(topk_kernel<8>, grid, block, 0, st, max_score, rows, heads, max_blocks, topk, nvp, out);
   else if (max_blocks <= 1024)
-    topk_kernel<32><<<grid, block, 0, st>>>(max_score, rows, heads, max_blocks, topk, nvp, out);
+    e = launch_pdl(topk_kernel<32>, grid, block, 0, st, max_score, rows, heads, max_blocks, topk, nvp, out);
   else
-    topk_kernel_long<<<grid, block, 0, st>>>(max_score, rows, heads, max_blocks, topk, nvp, out);
-  return cuda_check(cudaGetLastError(), "msa_topk_select: launch");
+    e = launch_pdl(topk_kernel_long, grid, block, 0, st, max_score, rows, heads, max_blocks, topk, nvp, out);
+  return cuda_check(e, "msa_topk_select: launch");
 }
 
 }  // namespace msa

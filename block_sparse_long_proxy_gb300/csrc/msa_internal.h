@@ -68,8 +68,10 @@ struct msa_plan_s {
   int32_t decode_ctas = 0;           // persistent decode grid size
   // per-kernel work tables, one int32 array carved by offsets
   int32_t* aux_d = nullptr;
-  int64_t proxy_units_off = 0;       // prefill proxy work units
+  int64_t proxy_units_off = 0;       // prefill proxy work units, grouped by persistent CTA
   int32_t n_proxy_units = 0;
+  int64_t proxy_cta_off = 0;         // prefill proxy: first unit of each CTA, [proxy_n_ctas + 1]
+  int32_t proxy_n_ctas = 0;
   int64_t proxy_unit_start_off = 0;  // decode proxy: first unit of each tile
   int64_t proxy_chunk_base_off = 0;  // prefill proxy: first 32-block chunk of each tile
   int32_t proxy_n_chunks = 0;        // sum over tiles of ceil(nvp / 32)

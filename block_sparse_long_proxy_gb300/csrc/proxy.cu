@@ -84,17 +84,28 @@ struct ProxySmem {
   static constexpr int kKOff = kQOff + kHeadsPerCta * kQBytes;
   static constexpr int kPartOff = kKOff + kStages * kKBytes;
   static constexpr int kBarOff = kPartOff + kChunk * kHeadsPerCta * kEpiWarps * 4;
-  static constexpr int kBytes = kBarOff + 8 * (1 + 2 * kStages + 2 * kNBuf + 1) + 16;
+  static constexpr int kBytes = kBarOff + 8 * (1 + 2 * kStages + 2 * kNBuf + 1 + kHeadsPerCta) + 16;
 };
 
+// Persistent: CTA b takes the units cta_off[b] .. cta_off[b + 1] - 1, dealt at
+// plan time longest first to the least-loaded CTA.  The
+// K ring, the two TMEM accumulators and every barrier live across units; the
+// ring counter and the accumulator counter run on across units (a unit's
+// block count is padded to even with an empty stage, so that block pairs
+// always sit in adjacent stages), and each head's Q tile is reloaded as soon
+// as the previous unit's last MMA of that head has read it, so the next
+// unit's loads overlap the current unit's last products and its epilogue
+// (the block maxima and the fused selection).
 template <int DP>
 __global__ void __launch_bounds__(kThreads, 1)
     proxy_prefill_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                         const ProxyUnit* __restrict__ units, const TileInfo* __restrict__ tiles,
+                         const ProxyUnit* __restrict__ units, const int32_t* __restrict__ cta_off,
+                         const TileInfo* __restrict__ tiles,
                          const int32_t* __restrict__ kv_indices, int64_t num_pages, float* __restrict__ max_score,
                          int32_t hp, int32_t max_blocks, float scale, FusedTopk fz, uint32_t* err) {
   pdl_wait();
   using L = ProxySmem<DP>;
+  static_assert(kStages % 2 == 0, "block pairs occupy adjacent stages");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* q_s = smem + L::kQOff;
@@ -107,17 +118,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* t_full = k_empty + kStages;
   uint64_t* t_empty = t_full + kNBuf;
   uint64_t* drain = t_empty + kNBuf;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* q_empty = drain + 1;  // [kHeadsPerCta]: head h's Q tile read by the unit's last MMA of h
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_empty + kHeadsPerCta);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const ProxyUnit u = units[blockIdx.x];
-  const TileInfo tl = tiles[u.tile];
-  const int nblk = u.j1 - u.j0;
 
   if (threadIdx.x == 0) {
     prefetch_tmap(&q_map);
     prefetch_tmap(&k_map);
     mbar_init(q_full, 1);
+    for (int h = 0; h < kHeadsPerCta; ++h) mbar_init(q_empty + h, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_empty + s, 1);
@@ -140,18 +150,35 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      mbar_expect_tx(q_full, u.nh * L::kQBytes);
-      for (int h = 0; h < u.nh; ++h) tma_load_3d(q_s + h * L::kQBytes, &q_map, q_full, 0, u.h0 + h, tl.q_begin);
-      for (int i = 0; i < nblk; ++i) {
-        const int s = i % kStages;
-        if (!mbar_wait(k_empty + s, ((i / kStages) & 1) ^ 1, err)) break;
-        int64_t page = kv_indices[tl.page_base + u.j0 + i];
-        if (page < 0 || page >= num_pages) {
-          atomicOr(err, kErrDeviceCheck);
-          page = 0;
+      int kit = 0;  // ring position, across units
+      bool ok = true;
+      for (int k = 0, ui = cta_off[blockIdx.x]; ok && ui < cta_off[blockIdx.x + 1]; ++k, ++ui) {
+        const ProxyUnit u = units[ui];
+        const TileInfo tl = tiles[u.tile];
+        const int nblk = u.j1 - u.j0;
+        for (int h = 0; ok && h < u.nh; ++h) {
+          if (k > 0 && !(ok = mbar_wait(q_empty + h, (k - 1) & 1, err))) break;
+          // after head 0's slot is free the previous unit's q_full phase is
+          // complete (its MMAs waited for it), so this arrival opens the next
+          if (h == 0) mbar_expect_tx(q_full, u.nh * L::kQBytes);
+          tma_load_3d(q_s + h * L::kQBytes, &q_map, q_full, 0, u.h0 + h, tl.q_begin);
         }
-        mbar_expect_tx(k_full + s, L::kKBytes);
-        tma_load_2d(k_s + s * L::kKBytes, &k_map, k_full + s, 0, static_cast<int>(page * 128));
+        if (!ok) break;
+        for (int i = 0; i < nblk + (nblk & 1); ++i, ++kit) {
+          const int s = kit % kStages;
+          if (!(ok = mbar_wait(k_empty + s, ((kit / kStages) & 1) ^ 1, err))) break;
+          if (i == nblk) {  // the empty stage that keeps the next unit's pairs aligned
+            mbar_arrive(k_full + s);
+            continue;
+          }
+          int64_t page = kv_indices[tl.page_base + u.j0 + i];
+          if (page < 0 || page >= num_pages) {
+            atomicOr(err, kErrDeviceCheck);
+            page = 0;
+          }
+          mbar_expect_tx(k_full + s, L::kKBytes);
+          tma_load_2d(k_s + s * L::kKBytes, &k_map, k_full + s, 0, static_cast<int>(page * 128));
+        }
       }
     }
   } else if (warp == 1) {
@@ -162,28 +189,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id128 = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t sw = DP == 64 ? kSwizzle128 : kSwizzle64;
       constexpr uint32_t sbo = DP == 64 ? 1024 : 512;
-      bool ok = mbar_wait(q_full, 0, err);
-      int item = 0;
-      for (int i = 0; ok && i < nblk; i += 2) {
-        const bool pair = i + 1 < nblk;
-        const int s = i % kStages;
-        if (!(ok = mbar_wait(k_full + s, (i / kStages) & 1, err))) break;
-        if (pair && !(ok = mbar_wait(k_full + s + 1, ((i + 1) / kStages) & 1, err))) break;
-        tc_fence_after();
-        const uint32_t kaddr = smem_u32(k_s + s * L::kKBytes);
-        for (int h = 0; h < u.nh; ++h, ++item) {
-          const int b = item & 1;  // accumulator b: 256 columns, read by epilogue group b
-          if (!(ok = mbar_wait(t_empty + b, ((item >> 1) & 1) ^ 1, err))) break;
+      int kit = 0, item = 0;
+      bool ok = true;
+      for (int k = 0, ui = cta_off[blockIdx.x]; ok && ui < cta_off[blockIdx.x + 1]; ++k, ++ui) {
+        const ProxyUnit u = units[ui];
+        const int nblk = u.j1 - u.j0;
+        if (!(ok = mbar_wait(q_full, k & 1, err))) break;
+        for (int i = 0; ok && i < nblk; i += 2, kit += 2) {
+          const bool pair = i + 1 < nblk;
+          const int s = kit % kStages;
+          // the second stage of a pair (or the empty stage after an odd last block)
+          if (!(ok = mbar_wait(k_full + s, (kit / kStages) & 1, err))) break;
+          if (!(ok = mbar_wait(k_full + s + 1, ((kit + 1) / kStages) & 1, err))) break;
           tc_fence_after();
-          const uint32_t qaddr = smem_u32(q_s + h * L::kQBytes);
+          const uint32_t kaddr = smem_u32(k_s + s * L::kKBytes);
+          for (int h = 0; h < u.nh; ++h, ++item) {
+            const int b = item & 1;  // accumulator b: 256 columns, read by epilogue group b
+            if (!(ok = mbar_wait(t_empty + b, ((item >> 1) & 1) ^ 1, err))) break;
+            tc_fence_after();
+            const uint32_t qaddr = smem_u32(q_s + h * L::kQBytes);
 #pragma unroll
-          for (int kk = 0; kk < DP / 16; ++kk)
-            mma_ss(tmem + b * 256, smem_desc(qaddr + kk * 32, 16, sbo, sw), smem_desc(kaddr + kk * 32, 16, sbo, sw),
-                   pair ? id256 : id128, kk > 0);
-          mma_commit(t_full + b);
+            for (int kk = 0; kk < DP / 16; ++kk)
+              mma_ss(tmem + b * 256, smem_desc(qaddr + kk * 32, 16, sbo, sw), smem_desc(kaddr + kk * 32, 16, sbo, sw),
+                     pair ? id256 : id128, kk > 0);
+            mma_commit(t_full + b);
+            if (i + 2 >= nblk) mma_commit(q_empty + h);  // the unit's last MMA of head h
+          }
+          mma_commit(k_empty + s);
+          mma_commit(k_empty + s + 1);
         }
-        mma_commit(k_empty + s);
-        if (pair) mma_commit(k_empty + s + 1);
+        // heads the unit does not have: their Q slots are free as well (every
+        // unit completes each q_empty once)
+        for (int h = u.nh; ok && h < kHeadsPerCta; ++h) mma_commit(q_empty + h);
       }
       mma_commit(drain);
       mbar_wait(drain, 0, err);
@@ -197,146 +234,153 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;
     const int grp = ew >> 2;
     const int r = quarter * 32 + lane;
-    const bool row_ok = r < tl.rows;
-    const int qpos = tl.pos0 + r;
+    const int et = threadIdx.x - 64;
     int item = 0;
     bool ok = true;
-    for (int i = 0; ok && i < nblk; i += 2) {
-      const int nb = i + 1 < nblk ? 2 : 1;
-      for (int h = 0; h < u.nh; ++h, ++item) {
-        if ((item & 1) != grp) continue;
-        if (!(ok = mbar_wait(t_full + grp, (item >> 1) & 1, err))) break;
-        tc_fence_after();
-        for (int bi = 0; bi < nb; ++bi) {
-          uint32_t v[128];
-          const uint32_t taddr = tmem + grp * 256 + bi * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
-          tmem_ld32(taddr, v);
-          tmem_ld32(taddr + 32, v + 32);
-          tmem_ld32(taddr + 64, v + 64);
-          tmem_ld32(taddr + 96, v + 96);
-          tmem_wait_ld();
-          if (bi == nb - 1) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(t_empty + grp);
-          }
-          const int j = u.j0 + i + bi;
-          if ((j * 128 + 127 > tl.pos0) || (tl.rows < 128)) {  // diagonal / ragged: mask the future
-            const int limit = row_ok ? qpos - j * 128 : -1;
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c > limit) v[c] = __float_as_uint(-INFINITY);
-          }
-          float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
-#pragma unroll
-          for (int c = 0; c < 128; c += 8) {
-            m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
-            m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
-            m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
-            m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
-          }
-          const float m = fmax3(fmaxf(m0, m1), m2, m3);
-          const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
-          if (lane == 0) part[((i + bi) * kHeadsPerCta + h) * kEpiWarps + quarter] = wm;
-        }
-      }
-    }
-    // all epilogue warps: combine the eight partial maxima of each item
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-    const int et = threadIdx.x - 64;
-    if (ok) {
-      for (int it = et; it < nblk * u.nh; it += 32 * kEpiWarps) {
-        const int h = it / nblk, i = it % nblk;
-        int32_t m = part[(i * kHeadsPerCta + h) * kEpiWarps];
-#pragma unroll
-        for (int w = 1; w < 4; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
-        const float v = ord2f(m) * scale;
-        if (max_score) max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = v;
-        part[(i * kHeadsPerCta + h) * kEpiWarps + 4] = __float_as_int(v);  // the fused selection reads it
-      }
-    }
-    if (fz.out) {
-      // ---- fused top-k: this chunk's candidates, then the row group's merge
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-      const int ew = warp - 2;  // head of the group handled by this warp
-      const bool wok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform: the selections below are warp-collective
-      const int hg = u.h0 / kHeadsPerCta;
-      const int n = tl.nvp < 1 ? 1 : (tl.nvp > max_blocks ? max_blocks : tl.nvp);
-      const int need = fz.topk - 1;
-      const bool all = fz.topk >= n;  // every valid block is selected
-      const int n_chunks = (tl.nvp + kChunk - 1) / kChunk;
-      auto slot = [&](int c, int h) -> int64_t {
-        return ((static_cast<int64_t>(fz.chunk_base[u.tile] + c) * fz.n_hgroups + hg) * kHeadsPerCta + h) * 32;
-      };
-      if (wok && !all && ew < u.nh) {
-        const int j = u.j0 + lane;
-        unsigned long long ck = 0ull;
-        if (lane < nblk && j < n - 1) {
-          const uint32_t key = order_key(__int_as_float(part[(lane * kHeadsPerCta + ew) * kEpiWarps + 4]));
-          if (key) ck = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
-        }
-        unsigned long long mine = 0ull;
-        bool taken = false;
-        for (int q = 0; q < need; ++q) {
-          const unsigned long long m = warp_max_u64(taken ? 0ull : ck);
-          if (m == 0ull) break;
-          if (ck == m) taken = true;
-          if (lane == q) mine = m;
-        }
-        if (lane < need) fz.cand[slot(u.j0 / kChunk, ew) + lane] = mine;
-      }
-      // the CTA barrier orders every thread's candidates before thread 0's
-      // release; its acquire (in the last CTA) orders the merge's reads after
-      // every chunk's release
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-      if (et == 0) {
-        int32_t* ctr = fz.counters + static_cast<int64_t>(u.tile) * fz.n_hgroups + hg;
-        int32_t prev;
-        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
-        const bool last = prev == n_chunks - 1;
-        if (last) *ctr = 0;  // every chunk of the row group has counted: ready for the next launch
-        part[5] = last;
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
-      if (part[5] && wok && ew < u.nh) {
-        int32_t* dst = fz.out + (static_cast<int64_t>(u.tile) * hp + u.h0 + ew) * fz.topk;
-        if (all) {
-          if (lane < fz.topk) dst[lane] = lane < n ? lane : -1;
-        } else {
-          // a k-way merge of the chunks' lists, each already best-first:
-          // lane c holds chunk c's list and shifts it as its head is taken
-          unsigned long long v[kFusedMaxTopk - 1];
-#pragma unroll
-          for (int r = 0; r < kFusedMaxTopk - 1; ++r)
-            v[r] = (lane < n_chunks && r < need) ? __ldcg(fz.cand + slot(lane, ew) + r) : 0ull;
-          uint32_t sel = 0xFFFFFFFFu;  // lane q: the q-th best block
-          int found = 0;
-          for (int q = 0; q < need; ++q) {
-            const unsigned long long m = warp_max_u64(v[0]);
-            if (m == 0ull) break;
-            if (v[0] == m) {
-#pragma unroll
-              for (int r = 0; r < kFusedMaxTopk - 2; ++r) v[r] = v[r + 1];
-              v[kFusedMaxTopk - 2] = 0ull;
+    for (int k = 0, ui = cta_off[blockIdx.x]; ui < cta_off[blockIdx.x + 1]; ++k, ++ui) {
+      const ProxyUnit u = units[ui];
+      const TileInfo tl = tiles[u.tile];
+      const int nblk = u.j1 - u.j0;
+      const bool row_ok = r < tl.rows;
+      const int qpos = tl.pos0 + r;
+      for (int i = 0; i < nblk; i += 2) {
+        const int nb = i + 1 < nblk ? 2 : 1;
+        for (int h = 0; h < u.nh; ++h, ++item) {
+          if ((item & 1) != grp || !ok) continue;
+          if (!(ok = mbar_wait(t_full + grp, (item >> 1) & 1, err))) continue;
+          tc_fence_after();
+          for (int bi = 0; bi < nb; ++bi) {
+            uint32_t v[128];
+            const uint32_t taddr = tmem + grp * 256 + bi * 128 + (static_cast<uint32_t>(quarter * 32) << 16);
+            tmem_ld32(taddr, v);
+            tmem_ld32(taddr + 32, v + 32);
+            tmem_ld32(taddr + 64, v + 64);
+            tmem_ld32(taddr + 96, v + 96);
+            tmem_wait_ld();
+            if (bi == nb - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(t_empty + grp);
             }
-            if (lane == q) sel = 0xFFFFFFFFu - static_cast<uint32_t>(m);
-            ++found;
+            const int j = u.j0 + i + bi;
+            if ((j * 128 + 127 > tl.pos0) || (tl.rows < 128)) {  // diagonal / ragged: mask the future
+              const int limit = row_ok ? qpos - j * 128 : -1;
+#pragma unroll
+              for (int c = 0; c < 128; ++c)
+                if (c > limit) v[c] = __float_as_uint(-INFINITY);
+            }
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; c += 8) {
+              m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+              m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+              m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+              m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+            }
+            const float m = fmax3(fmaxf(m0, m1), m2, m3);
+            const int32_t wm = __reduce_max_sync(0xFFFFFFFFu, f2ord(m));
+            if (lane == 0) part[((i + bi) * kHeadsPerCta + h) * kEpiWarps + quarter] = wm;
           }
-          if (lane == found) sel = static_cast<uint32_t>(n - 1);  // the diagonal block
-          // ascending: each selected block's rank among the selected ones
-          int rank = 0;
-          for (int l = 0; l < 32; ++l) rank += __shfl_sync(0xFFFFFFFFu, sel, l) < sel;
-          if (sel != 0xFFFFFFFFu) dst[rank] = static_cast<int32_t>(sel);
-          if (lane > found && lane < fz.topk) dst[lane] = -1;
         }
       }
-    }
-    if (u.fill_tail && max_score) {
-      const int tail = max_blocks - tl.nvp;
-      for (int it = et; it < tail * u.nh; it += 32 * kEpiWarps) {
-        const int h = it / tail, j = tl.nvp + it % tail;
-        max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + j] = -INFINITY;
+      ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform: the barriers and selections below are collective
+      // all epilogue warps: combine the eight partial maxima of each item
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+      if (ok) {
+        for (int it = et; it < nblk * u.nh; it += 32 * kEpiWarps) {
+          const int h = it / nblk, i = it % nblk;
+          int32_t m = part[(i * kHeadsPerCta + h) * kEpiWarps];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) m = max(m, part[(i * kHeadsPerCta + h) * kEpiWarps + w]);
+          const float v = ord2f(m) * scale;
+          if (max_score) max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + u.j0 + i] = v;
+          part[(i * kHeadsPerCta + h) * kEpiWarps + 4] = __float_as_int(v);  // the fused selection reads it
+        }
       }
+      if (fz.out) {
+        // ---- fused top-k: this chunk's candidates, then the row group's merge
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        const bool wok = ok;
+        const int hg = u.h0 / kHeadsPerCta;
+        const int n = tl.nvp < 1 ? 1 : (tl.nvp > max_blocks ? max_blocks : tl.nvp);
+        const int need = fz.topk - 1;
+        const bool all = fz.topk >= n;  // every valid block is selected
+        const int n_chunks = (tl.nvp + kChunk - 1) / kChunk;
+        auto slot = [&](int c, int h) -> int64_t {
+          return ((static_cast<int64_t>(fz.chunk_base[u.tile] + c) * fz.n_hgroups + hg) * kHeadsPerCta + h) * 32;
+        };
+        if (wok && !all && ew < u.nh) {
+          const int j = u.j0 + lane;
+          unsigned long long ck = 0ull;
+          if (lane < nblk && j < n - 1) {
+            const uint32_t key = order_key(__int_as_float(part[(lane * kHeadsPerCta + ew) * kEpiWarps + 4]));
+            if (key) ck = (static_cast<unsigned long long>(key) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(j));
+          }
+          unsigned long long mine = 0ull;
+          bool taken = false;
+          for (int q = 0; q < need; ++q) {
+            const unsigned long long m = warp_max_u64(taken ? 0ull : ck);
+            if (m == 0ull) break;
+            if (ck == m) taken = true;
+            if (lane == q) mine = m;
+          }
+          if (lane < need) fz.cand[slot(u.j0 / kChunk, ew) + lane] = mine;
+        }
+        // the CTA barrier orders every thread's candidates before thread 0's
+        // release; its acquire (in the last CTA) orders the merge's reads after
+        // every chunk's release
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        if (et == 0) {
+          int32_t* ctr = fz.counters + static_cast<int64_t>(u.tile) * fz.n_hgroups + hg;
+          int32_t prev;
+          asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(ctr) : "memory");
+          const bool last = prev == n_chunks - 1;
+          if (last) *ctr = 0;  // every chunk of the row group has counted: ready for the next launch
+          part[5] = last;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
+        if (part[5] && wok && ew < u.nh) {
+          int32_t* dst = fz.out + (static_cast<int64_t>(u.tile) * hp + u.h0 + ew) * fz.topk;
+          if (all) {
+            if (lane < fz.topk) dst[lane] = lane < n ? lane : -1;
+          } else {
+            // a k-way merge of the chunks' lists, each already best-first:
+            // lane c holds chunk c's list and shifts it as its head is taken
+            unsigned long long v[kFusedMaxTopk - 1];
+#pragma unroll
+            for (int rr = 0; rr < kFusedMaxTopk - 1; ++rr)
+              v[rr] = (lane < n_chunks && rr < need) ? __ldcg(fz.cand + slot(lane, ew) + rr) : 0ull;
+            uint32_t sel = 0xFFFFFFFFu;  // lane q: the q-th best block
+            int found = 0;
+            for (int q = 0; q < need; ++q) {
+              const unsigned long long m = warp_max_u64(v[0]);
+              if (m == 0ull) break;
+              if (v[0] == m) {
+#pragma unroll
+                for (int rr = 0; rr < kFusedMaxTopk - 2; ++rr) v[rr] = v[rr + 1];
+                v[kFusedMaxTopk - 2] = 0ull;
+              }
+              if (lane == q) sel = 0xFFFFFFFFu - static_cast<uint32_t>(m);
+              ++found;
+            }
+            if (lane == found) sel = static_cast<uint32_t>(n - 1);  // the diagonal block
+            // ascending: each selected block's rank among the selected ones
+            int rank = 0;
+            for (int l = 0; l < 32; ++l) rank += __shfl_sync(0xFFFFFFFFu, sel, l) < sel;
+            if (sel != 0xFFFFFFFFu) dst[rank] = static_cast<int32_t>(sel);
+            if (lane > found && lane < fz.topk) dst[lane] = -1;
+          }
+        }
+      }
+      if (u.fill_tail && max_score) {
+        const int tail = max_blocks - tl.nvp;
+        for (int it = et; it < tail * u.nh; it += 32 * kEpiWarps) {
+          const int h = it / tail, j = tl.nvp + it % tail;
+          max_score[(static_cast<int64_t>(u.tile) * hp + u.h0 + h) * max_blocks + j] = -INFINITY;
+        }
+      }
+      // the next unit's partial maxima may overwrite this unit's
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kEpiWarps) : "memory");
     }
   }
   tc_fence_before();
@@ -706,10 +750,35 @@ void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
     chunks += (p->tiles[t].nvp + kChunk - 1) / kChunk;
   }
   p->proxy_n_chunks = chunks;
+  // persistent CTAs: units dealt longest first to the least-loaded CTA (a
+  // unit costs its block-head products plus a fixed tail), each CTA's units
+  // stored contiguously; proxy_cta_off[b] .. [b + 1] are CTA b's
+  const int n_ctas = std::max(1, std::min(static_cast<int>(us.size()), p->num_sms));
+  std::vector<std::vector<ProxyUnit>> per(n_ctas);
+  std::vector<std::pair<int64_t, int>> heap;  // (load, cta), a min-heap
+  for (int b = 0; b < n_ctas; ++b) heap.push_back({0, b});
+  auto later = [](const std::pair<int64_t, int>& a, const std::pair<int64_t, int>& b) { return a > b; };
+  for (const ProxyUnit& u : us) {
+    std::pop_heap(heap.begin(), heap.end(), later);
+    auto& top = heap.back();
+    per[top.second].push_back(u);
+    top.first += static_cast<int64_t>(u.j1 - u.j0) * u.nh + 8;
+    std::push_heap(heap.begin(), heap.end(), later);
+  }
+  p->proxy_cta_off = static_cast<int64_t>(aux.size());
+  p->proxy_n_ctas = n_ctas;
+  int32_t off = 0;
+  for (int b = 0; b < n_ctas; ++b) {
+    aux.push_back(off);
+    off += static_cast<int32_t>(per[b].size());
+  }
+  aux.push_back(off);
   p->proxy_units_off = static_cast<int64_t>(aux.size());
   p->n_proxy_units = static_cast<int32_t>(us.size());
-  const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
-  aux.insert(aux.end(), raw, raw + us.size() * (sizeof(ProxyUnit) / 4));
+  for (int b = 0; b < n_ctas; ++b) {
+    const int32_t* raw = reinterpret_cast<const int32_t*>(per[b].data());
+    aux.insert(aux.end(), raw, raw + per[b].size() * (sizeof(ProxyUnit) / 4));
+  }
   // decode: first unit of each tile
   p->proxy_unit_start_off = static_cast<int64_t>(aux.size());
   int32_t acc = 0;
@@ -737,17 +806,19 @@ static msa_status proxy_prefill(const msa_plan_s* p, const void* pq, const void*
   if (!encode_tensor_map(&qm, 3, pq, qdims, qstr, qbox, 1, p->dp * 2) || !make_pk_map(&km, p, pk_pages))
     return set_error(MSA_ERR_CUDA, "msa_proxy_maxscore: tensor map encoding failed");
   const ProxyUnit* units = reinterpret_cast<const ProxyUnit*>(p->aux_d + p->proxy_units_off);
+  const int32_t* cta_off = p->aux_d + p->proxy_cta_off;
   const float scale = 1.0f / sqrtf(static_cast<float>(p->dp));
+  const int grid = p->proxy_n_ctas;  // persistent: one CTA per SM
   cudaError_t e;
   if (p->dp == 64) {
     const int smem = ProxySmem<64>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    e = launch_pdl(proxy_prefill_kernel<64>, dim3(p->n_proxy_units), dim3(kThreads), smem, st, qm, km, units,
+    e = launch_pdl(proxy_prefill_kernel<64>, dim3(grid), dim3(kThreads), smem, st, qm, km, units, cta_off,
                    p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   } else {
     const int smem = ProxySmem<32>::kBytes + 1024;
     cudaFuncSetAttribute(proxy_prefill_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    e = launch_pdl(proxy_prefill_kernel<32>, dim3(p->n_proxy_units), dim3(kThreads), smem, st, qm, km, units,
+    e = launch_pdl(proxy_prefill_kernel<32>, dim3(grid), dim3(kThreads), smem, st, qm, km, units, cta_off,
                    p->tiles_d, kv_indices, p->num_pages, max_score, p->hp, p->max_blocks, scale, fz, p->err_d);
   }
   return cuda_check(e, "msa_proxy_maxscore: prefill launch");

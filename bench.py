@@ -38,9 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # dram bytes of one attention-forward launch at the 32K prefill workload from
 # an ncu capture, valid only for the kernel source it was taken on.
-# Captured on S=16384 (15424 selected tile-blocks: 247.8 MB read + 108.4 MB
+# Captured on S=16384 (15424 selected tile-blocks: 244.9 MB read + 108.7 MB
 # written) and scaled by selected tile-blocks to the S=32768 launch (31808).
-NCU_TRAFFIC = {"attn_fwd.cu": {"src": "bd30baa3cf914cf1", "bytes": int((243888384 + 108123904) * 31808 / 15424)}}
+NCU_TRAFFIC = {"attn_fwd.cu": {"src": "113d91ff3bd0593c", "bytes": int((244937472 + 108676352) * 31808 / 15424)}}
 
 
 def peaks():
@@ -613,6 +613,7 @@ def run_ncu_case(args):
     """A small case of one kernel for profiler captures (no JSON line):
     inputs above the 129 MB L2 but a few hundred MB on the device.
       attn / proxy / topk: sparse prefill S=16384 (32q/8kv, d=128, topk 16)
+      attn_fp8: the same with e4m3 K/V
       decode: FP8 paged decode, 32 sequences x 16384 keys
       bwd: the KL-coupled backward of the S=16384 prefill."""
     import torch
@@ -622,6 +623,8 @@ def run_ncu_case(args):
     if args.ncu_case == "decode":
         case = synth.Case("decode 32x16384 fp8", [1] * 32, [16384] * 32, 64, 8, 128, 8, 64, 16, kv_dtype="e4m3",
                           page_perm_seed=1)
+    elif args.ncu_case == "attn_fp8":
+        case = synth.Case("prefill S=16384 fp8", [16384], [16384], 32, 8, 128, 8, 64, 16, kv_dtype="e4m3")
     else:
         case = synth.Case("prefill S=16384", [16384], [16384], 32, 8, 128, 8, 64, 16)
     inp = synth.make_inputs(case, device=dev, with_dout=args.ncu_case == "bwd")
@@ -642,9 +645,11 @@ def run_ncu_case(args):
             plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
         if args.ncu_case == "decode":
             plan.proxy_maxscore_fp8(inp["pq"], inp["pk_pages_e4m3"], inp["pk_scale"], inp["kv_indices"], out=ms)
+            plan.proxy_maxscore_nvfp4(inp["pq"], inp["pk_fp4_codes"], inp["pk_fp4_scales"], inp["pk_fp4_global"],
+                                      inp["kv_indices"], out=ms)
         if args.ncu_case == "topk":
             msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
-        if args.ncu_case in ("attn", "decode"):
+        if args.ncu_case in ("attn", "attn_fp8", "decode"):
             plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, **kw)
     torch.cuda.synchronize()
     plan.check_errors()
@@ -715,7 +720,7 @@ def bench_train(args, dev, pk_info, peak_kind):
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--ncu-case", choices=["attn", "proxy", "topk", "decode", "bwd"], default=None,
+    ap.add_argument("--ncu-case", choices=["attn", "attn_fp8", "proxy", "topk", "decode", "bwd"], default=None,
                     help="run a small case of one kernel for a profiler capture and exit")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)

@@ -65,23 +65,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 }
 
 // One unit's cached blocks, built once by the producer warp (its lanes read
-// the top-k row and the page table in parallel) for the MMA and softmax warps.
-struct UnitList {
+// the top-k row and the page table in parallel) for the MMA and softmax
+// warps: a 16-int header, then j[cap] (selected blocks, padding and
+// out-of-range entries dropped) and row[cap] (their first K/V tensor-map
+// row), cap >= topk.
+struct UnitHdr {
   int32_t n, nh, h0, q_begin, rows, pos0, g, pad[9];
-  int32_t j[kMaxTopk];    // selected blocks, padding and out-of-range entries dropped
-  int32_t row[kMaxTopk];  // their first K/V tensor-map row
 };
 constexpr int kListSlots = 2;
+constexpr int kHdrInts = 16;
 
-template <int D>
+// Shared memory: Q (two heads), the K and V rings, the O staging buffer
+// (kStageO: one head's bf16 O tile, for the TMA stores of full tiles),
+// barriers, then the two list slots, whose size follows topk.
+template <int D, bool kStageO>
 struct AttnSmem {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16, in D/64 swizzled chunks of 16 KB
   static constexpr int kQOff = 0;
   static constexpr int kKOff = kQOff + 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
-  static constexpr int kListOff = kVOff + kStages * kTileBytes;
-  static constexpr int kBarOff = kListOff + kListSlots * static_cast<int>(sizeof(UnitList));
-  static constexpr int kBytes = kBarOff + 8 * 32;
+  static constexpr int kOOff = kVOff + kStages * kTileBytes;
+  static constexpr int kOChunkBytes = 128 * 64 * 2;  // 64 columns of 128 rows
+  static constexpr int kBarOff = kOOff + (kStageO ? kTileBytes : 0);
+  static constexpr int kListOff = kBarOff + 8 * 32;
+  static __host__ __device__ constexpr int slot_ints(int cap) { return kHdrInts + 2 * cap; }
+  static __host__ __device__ constexpr int bytes(int cap) { return kListOff + kListSlots * slot_ints(cap) * 4; }
 };
 
 // Persistent: CTA b takes units b, b + gridDim.x, ... (heaviest first).
@@ -89,10 +97,11 @@ struct AttnSmem {
 // barrier's phase comes from a running count (per head for the S / P / O
 // barriers), and Q is released right after a unit's last QK so the next
 // unit's Q load overlaps the tail of the current one.
-template <int D, bool kOneKvHead, bool kFp8>
+template <int D, bool kOneKvHead, bool kFp8, bool kStageO>
 __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
-                    const __grid_constant__ CUtensorMap v_map, const AttnUnit* __restrict__ units, int32_t n_units,
+                    const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap o_map,
+                    int32_t list_cap, const AttnUnit* __restrict__ units, int32_t n_units,
                     const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                     const int32_t* __restrict__ kv_indices, int64_t num_pages, __nv_bfloat16* __restrict__ out,
                     float* __restrict__ lse, int32_t hq, int32_t hsel, int32_t kv_div, int32_t topk,
@@ -102,7 +111,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
   // hsel block sets (proxy heads) per tile; a unit's u.g is its proxy head,
   // whose blocks are read from KV head u.g / kv_div of hsel / kv_div
   const int hkv = hsel / kv_div;
-  using L = AttnSmem<D>;
+  using L = AttnSmem<D, kStageO>;
   constexpr int kChunks = D / 64;
   static_assert(!kFp8 || (D == 128 && !kOneKvHead), "FP8 K/V: head_dim 128, main attention");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -110,7 +119,14 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
   uint8_t* q_s = smem + L::kQOff;
   uint8_t* k_s = smem + L::kKOff;
   uint8_t* v_s = smem + L::kVOff;
-  UnitList* lists = reinterpret_cast<UnitList*>(smem + L::kListOff);
+  int32_t* const list_base = reinterpret_cast<int32_t*>(smem + L::kListOff);
+  // the staged layout sizes the list slots by topk; the other keeps them at
+  // the compile-time maximum (constant offsets in the issue loops)
+  const int cap = kStageO ? list_cap : kMaxTopk;
+  const int slot_ints = L::slot_ints(cap);
+  auto lhdr = [&](int k) -> UnitHdr& { return *reinterpret_cast<UnitHdr*>(list_base + (k % kListSlots) * slot_ints); };
+  auto lj = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts; };
+  auto lrow = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts + cap; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
@@ -125,7 +141,9 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
   uint64_t* drain = list_empty + kListSlots;
   uint64_t* raw_full = drain + 1;          // [kStages], FP8: e4m3 K and V codes landed
   uint64_t* q_ready = raw_full + kStages;  // FP8: Q converted to f16
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(q_ready + 1);
+  uint64_t* ost_ready = q_ready + 1;       // a head's O staged (kStageO)
+  uint64_t* ost_free = ost_ready + 1;      // the TMA store has read it
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ost_free + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -140,6 +158,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       mbar_init(raw_full + s, 1);
     }
     mbar_init(q_ready, kConvWarps);
+    mbar_init(ost_ready, 4);  // the four warps of the head that stages
+    mbar_init(ost_free, 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(s_full + h, 1);
       mbar_init(p_full + h, 4);
@@ -167,7 +187,9 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     int kv_it = 0;
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
-      UnitList& ls = lists[k % kListSlots];
+      UnitHdr& ls = lhdr(k);
+      int32_t* const ls_j = lj(k);
+      int32_t* const ls_row = lrow(k);
       const AttnUnit u = units[ui];
       const TileInfo tl = tiles[u.tile];
       const int32_t* sel = idx + (static_cast<int64_t>(u.tile) * hsel + u.g) * topk;
@@ -196,8 +218,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         const uint32_t m = __ballot_sync(0xFFFFFFFFu, valid);
         if (valid) {
           const int o = n + __popc(m & ((1u << lane) - 1u));
-          ls.j[o] = j;
-          ls.row[o] = row;
+          ls_j[o] = j;
+          ls_row[o] = row;
         }
         n += __popc(m);
       }
@@ -223,7 +245,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         for (int i = 0; ok && i < n; ++i, ++kv_it) {
           const int s = kv_it % kStages;
           if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
-          const int row = ls.row[i];
+          const int row = ls_row[i];
           if (kFp8) {  // e4m3 codes into the upper half of the stage; the converters expand them
             mbar_expect_tx(raw_full + s, 2 * 16384);
             tma_load_2d(k_s + s * L::kTileBytes + 16384, &k_map, raw_full + s, 0, row);
@@ -275,8 +297,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       bool ok = true;
       for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
         if (!(ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err))) break;
-        const int n = lists[k % kListSlots].n;
-        const bool two = lists[k % kListSlots].nh == 2;
+        const int n = lhdr(k).n;
+        const bool two = lhdr(k).nh == 2;
         mbar_arrive(list_empty + k % kListSlots);
         if (!(ok = mbar_wait(kFp8 ? q_ready : q_full, k & 1, err))) break;
         tc_fence_after();
@@ -339,9 +361,11 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     const uint32_t s_addr = tmem + lane_base + h * 128;
     const uint32_t o_addr = tmem + lane_base + 256 + h * D;
     int ch = 0, od = 0;  // blocks and units (with blocks) of head h so far
+    int ost_uses = 0;    // (unit, head) uses of the O staging buffer so far
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
-      const UnitList& ls = lists[k % kListSlots];
+      const UnitHdr& ls = lhdr(k);
+      const int32_t* const ls_j = lj(k);
       if (ok) ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
@@ -361,7 +385,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
         tmem_wait_ld();
-        const int j = ls.j[i];
+        const int j = ls_j[i];
         const bool need_mask = (j * 128 + 127 > pos0) || (rows < 128);
         if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
           const int limit = row_ok ? qpos - j * 128 : -1;
@@ -447,7 +471,42 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free + h);
         o_released = true;
-        if (ok && row_ok) {
+        if (kStageO && rows == 128) {
+          // a full tile: the bf16 O rows go to the staging buffer (the TMA
+          // box layout: 64-column chunks of 128-byte rows, 16-byte units
+          // swizzled by row % 8), then one thread stores the boxes.  The
+          // buffer is shared by both heads and used once per (unit, head) in
+          // order; every hand-off is a bounded mbarrier wait.
+          const int use = ost_uses + h;
+          uint8_t* ob = smem + L::kOOff + r * 128;
+          if (use > 0 && ok) ok = mbar_wait(ost_free, (use - 1) & 1, err);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t* x = ov + 64 * c + 8 * e;
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
+              *reinterpret_cast<uint4*>(ob + c * L::kOChunkBytes + ((e ^ (r & 7)) << 4)) = w;
+            }
+          fence_async_shared();  // the TMA store reads them through the async proxy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ost_ready);
+          if (quarter == 0 && lane == 0) {
+            if (ok) ok = mbar_wait(ost_ready, use & 1, err);
+            if (ok) {
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c)
+                tma_store_3d(&o_map, smem + L::kOOff + c * L::kOChunkBytes, 64 * c, ls.h0 + h, ls.q_begin);
+              bulk_commit_group();
+              bulk_wait_group_read0();
+            }
+            mbar_arrive(ost_free);
+          }
+        } else if (ok && row_ok) {
           uint4* dst = reinterpret_cast<uint4*>(out + orow * D);
 #pragma unroll
           for (int e = 0; e < D / 8; ++e) {
@@ -463,6 +522,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
           lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
       if (h < nh) ch += n;
+      if (kStageO && rows == 128) ost_uses += nh;  // the staging buffer's uses, the same count in every warp
       // O_h may be overwritten by the next unit, and the list slot refilled
       // (every warp arrives once per unit, active or not)
       tc_fence_before();
@@ -472,6 +532,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         mbar_arrive(list_empty + k % kListSlots);
       }
     }
+    if (kStageO && quarter == 0 && lane == 0) bulk_wait_group0();  // this head's stores are complete
   } else if (kFp8) {
     // -------------------------------------------------- FP8 converters
     // Thread ct of the two warps owns rows ct and ct + 64 of every K / V
@@ -509,7 +570,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     int kv_it = 0;
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
-      const UnitList& ls = lists[k % kListSlots];
+      const UnitHdr& ls = lhdr(k);
       ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
@@ -581,6 +642,50 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   aux.insert(aux.end(), raw, raw + ps.size() * 4);
 }
 
+namespace {
+
+constexpr int kMaxSmem = 232448;  // 227 KB of dynamic shared memory per CTA
+
+// Launches one instantiation: with O staged through shared memory (full
+// tiles stored by TMA) for FP8 K/V when the list slots for this topk leave
+// room for the staging buffer, else with per-thread stores.  Measured at
+// S=32768: FP8 973 -> 1019 TFLOP/s staged; bf16 0.808 -> 0.826 ms staged,
+// so bf16 keeps the per-thread stores.
+template <int D, bool kOneKvHead, bool kFp8>
+cudaError_t launch_attn_variant(dim3 grid, cudaStream_t st, const CUtensorMap& qm, const CUtensorMap& km,
+                                const CUtensorMap& vm, const CUtensorMap& om, int32_t topk, const AttnUnit* units,
+                                int32_t n_units, const TileInfo* tiles, const int32_t* idx,
+                                const int32_t* kv_indices, int64_t num_pages, __nv_bfloat16* o, float* lse,
+                                int32_t hq, int32_t hsel, int32_t kv_div, float scale_log2, const float* k_scale,
+                                const float* v_scale, uint32_t* err) {
+  const int cap = (topk + 3) & ~3;
+  if constexpr (kFp8) {
+    const int staged = AttnSmem<D, true>::bytes(cap) + 1024;
+    if (staged <= kMaxSmem) {
+      auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, true>;
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, staged);
+      return launch_pdl(kern, grid, dim3(attn_threads(kFp8)), staged, st, qm, km, vm, om, cap, units, n_units,
+                        tiles, idx, kv_indices, num_pages, o, lse, hq, hsel, kv_div, topk, scale_log2, k_scale,
+                        v_scale, err);
+    }
+  }
+  const int plain = AttnSmem<D, false>::bytes(kMaxTopk) + 1024;
+  auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, false>;
+  cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plain);
+  return launch_pdl(kern, grid, dim3(attn_threads(kFp8)), plain, st, qm, km, vm, om, cap, units, n_units, tiles, idx,
+                    kv_indices, num_pages, o, lse, hq, hsel, kv_div, topk, scale_log2, k_scale, v_scale, err);
+}
+
+// [total_q, heads, D] bf16 rows as 3-D boxes of 64 columns x 1 head x 128 rows, 128-byte swizzle
+bool rows_map(CUtensorMap* m, const void* base, int d, int heads, int64_t total_q) {
+  const uint64_t dims[3] = {static_cast<uint64_t>(d), static_cast<uint64_t>(heads), static_cast<uint64_t>(total_q)};
+  const uint64_t str[2] = {static_cast<uint64_t>(d) * 2, static_cast<uint64_t>(heads) * d * 2};
+  const uint32_t box[3] = {64, 1, 128};
+  return encode_tensor_map(m, 3, base, dims, str, box, 1, 128);
+}
+
+}  // namespace
+
 msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                                const int32_t* kv_indices, const int32_t* idx, const float* k_scale,
                                const float* v_scale, void* out, float* lse, cudaStream_t st) {
@@ -588,44 +693,34 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
   const bool fp8 = p->kv_dtype == MSA_KV_FP8_E4M3;
   if (fp8 && p->d != 128)
     return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn: FP8 K/V prefill needs head_dim 128");
-  CUtensorMap qm, km, vm;
-  const uint64_t qdims[3] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->hq),
-                             static_cast<uint64_t>(p->total_q)};
-  const uint64_t qstr[2] = {static_cast<uint64_t>(p->d) * 2, static_cast<uint64_t>(p->hq) * p->d * 2};
-  const uint32_t qbox[3] = {64, 1, 128};
+  CUtensorMap qm, km, vm, om;
   const int kv_elem = fp8 ? 1 : 2;
   const uint64_t kdims[2] = {static_cast<uint64_t>(p->d), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
   const uint64_t kstr[1] = {static_cast<uint64_t>(p->d) * kv_elem};
   // bf16: 64-column boxes (128 B rows); e4m3: whole 128-byte rows of codes
   const uint32_t kbox[2] = {fp8 ? 128u : 64u, 128};
-  if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
+  if (!rows_map(&qm, q, p->d, p->hq, p->total_q) || !rows_map(&om, out, p->d, p->hq, p->total_q) ||
       !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, fp8 ? 0 : 1, 128) ||
       !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, fp8 ? 0 : 1, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn: tensor map encoding failed");
   const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->attn_units_off);
   const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->d));
   auto* o = static_cast<__nv_bfloat16*>(out);
-  const int grid = std::min(p->n_attn_units, p->num_sms);  // persistent: one CTA per SM
+  const dim3 grid(std::min(p->n_attn_units, p->num_sms));  // persistent: one CTA per SM
+  const int kv_div = p->hp / p->hkv;
   cudaError_t e;
-  if (fp8) {
-    const int smem = AttnSmem<128>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    e = launch_pdl(attn_fwd_kernel<128, false, true>, dim3(grid), dim3(attn_threads(true)), smem, st, qm, km, vm, units,
-                   p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp, p->hp / p->hkv,
-                   p->topk, scale_log2, k_scale, v_scale, p->err_d);
-  } else if (p->d == 128) {
-    const int smem = AttnSmem<128>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    e = launch_pdl(attn_fwd_kernel<128, false, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm, km, vm,
-                   units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
-                   p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
-  } else {
-    const int smem = AttnSmem<64>::kBytes + 1024;
-    cudaFuncSetAttribute(attn_fwd_kernel<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    e = launch_pdl(attn_fwd_kernel<64, false, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm, km, vm,
-                   units, p->n_attn_units, p->tiles_d, idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp,
-                   p->hp / p->hkv, p->topk, scale_log2, nullptr, nullptr, p->err_d);
-  }
+  if (fp8)
+    e = launch_attn_variant<128, false, true>(grid, st, qm, km, vm, om, p->topk, units, p->n_attn_units, p->tiles_d,
+                                              idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp, kv_div, scale_log2,
+                                              k_scale, v_scale, p->err_d);
+  else if (p->d == 128)
+    e = launch_attn_variant<128, false, false>(grid, st, qm, km, vm, om, p->topk, units, p->n_attn_units, p->tiles_d,
+                                               idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp, kv_div,
+                                               scale_log2, nullptr, nullptr, p->err_d);
+  else
+    e = launch_attn_variant<64, false, false>(grid, st, qm, km, vm, om, p->topk, units, p->n_attn_units, p->tiles_d,
+                                              idx, kv_indices, p->num_pages, o, lse, p->hq, p->hp, kv_div, scale_log2,
+                                              nullptr, nullptr, p->err_d);
   return cuda_check(e, "msa_sparse_attn: prefill launch");
 }
 
@@ -639,25 +734,20 @@ msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void*
                                 const int32_t* idx, void* op, float* lse, cudaStream_t st) {
   if (p->dp != 64) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: proxy_head_dim 64 only");
   if (p->topk > kMaxTopk) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: topk above 1024");
-  CUtensorMap qm, km;
-  const uint64_t qdims[3] = {64, static_cast<uint64_t>(p->hp), static_cast<uint64_t>(p->total_q)};
-  const uint64_t qstr[2] = {128, static_cast<uint64_t>(p->hp) * 128};
-  const uint32_t qbox[3] = {64, 1, 128};
+  CUtensorMap qm, km, om;
   const uint64_t kdims[2] = {64, static_cast<uint64_t>(p->num_pages) * 128};
   const uint64_t kstr[1] = {128};
   const uint32_t kbox[2] = {64, 128};
-  if (!encode_tensor_map(&qm, 3, pq, qdims, qstr, qbox, 1, 128) ||
+  if (!rows_map(&qm, pq, 64, p->hp, p->total_q) || !rows_map(&om, op, 64, p->hp, p->total_q) ||
       !encode_tensor_map(&km, 2, pk_pages, kdims, kstr, kbox, 1, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
   const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->proxy_attn_units_off);
   const float scale_log2 = 1.4426950408889634f / 8.0f;  // 1 / sqrt(64)
-  const int grid = std::min(p->n_proxy_attn_units, p->num_sms);
-  const int smem = AttnSmem<64>::kBytes + 1024;
-  cudaFuncSetAttribute(attn_fwd_kernel<64, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  return cuda_check(launch_pdl(attn_fwd_kernel<64, true, false>, dim3(grid), dim3(attn_threads(false)), smem, st, qm,
-                                km, km, units, p->n_proxy_attn_units, p->tiles_d, idx, kv_indices, p->num_pages,
-                                static_cast<__nv_bfloat16*>(op), lse, p->hp, p->hp, p->hp, p->topk, scale_log2,
-                                static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), p->err_d),
+  const dim3 grid(std::min(p->n_proxy_attn_units, p->num_sms));
+  return cuda_check(launch_attn_variant<64, true, false>(grid, st, qm, km, km, om, p->topk, units,
+                                                          p->n_proxy_attn_units, p->tiles_d, idx, kv_indices,
+                                                          p->num_pages, static_cast<__nv_bfloat16*>(op), lse, p->hp,
+                                                          p->hp, p->hp, scale_log2, nullptr, nullptr, p->err_d),
                     "msa_sparse_attn_bwd: proxy softmax launch");
 }
 

@@ -40,7 +40,21 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # an ncu capture, valid only for the kernel source it was taken on.
 # Captured on S=16384 (15424 selected tile-blocks: 244.9 MB read + 108.7 MB
 # written) and scaled by selected tile-blocks to the S=32768 launch (31808).
-NCU_TRAFFIC = {"attn_fwd.cu": {"src": "113d91ff3bd0593c", "bytes": int((244937472 + 108676352) * 31808 / 15424)}}
+NCU_TRAFFIC = {
+    # (DRAM bytes read + written) of one launch of the small S=16384 capture and the
+    # (tile, group, block) selections it processed; scaled to a launch by selections.
+    "attn_fwd.cu": {"src": "385a039e2bdecff2", "bytes": 243900928 + 108315392, "sel": 15424},
+    "attn_fwd.cu:fp8": {"src": "385a039e2bdecff2", "bytes": 182092544 + 102819328, "sel": 15424},
+}
+
+
+def ncu_traffic(key, n_sel):
+    """DRAM traffic of one launch from the committed ncu capture, or None when
+    the kernel source has changed since the counters were taken."""
+    t = NCU_TRAFFIC.get(key)
+    if not t or t["src"] != src_hash(key.split(":")[0]):
+        return None
+    return int(t["bytes"] * n_sel / t["sel"])
 
 
 def peaks():
@@ -344,12 +358,10 @@ def run_ours(args):
     attn_tflops = flops / (attn_ms / 1e3) / 1e12
     proxy_tflops = proxy_flops / (proxy_ms / 1e3) / 1e12
     peak_bf16 = pk_info.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    traffic = NCU_TRAFFIC.get("attn_fwd.cu")
-    if traffic and traffic.get("src") != src_hash("attn_fwd.cu"):
-        traffic = None
+    traffic = ncu_traffic("attn_fwd.cu", n_sel)
     roofline = {"bound": "tensor", "kernel": "attn_fwd_kernel<128> (msa_sparse_attn)", "achieved": attn_tflops,
                 "peak": peak_bf16, "unit": "TFLOP/s", "frac": attn_tflops / peak_bf16,
-                "traffic": traffic["bytes"] if traffic else None,
+                "traffic": traffic,
                 "peak_kind": "%s bf16 dense burst (cuBLAS)" % peak_kind,
                 "flops_per_launch": flops, "selected_blocks": n_sel,
                 "visible_pair_flops": visible_pair_flops(idx.cpu().numpy(), case),
@@ -530,7 +542,8 @@ def bench_prefill_fp8(args, dev, pk_info, peak_kind, bf16_tflops):
             "vs_bf16": tf / bf16_tflops,
             "roofline": {"bound": "tensor", "kernel": "attn_fwd_kernel<128, fp8> (msa_sparse_attn)", "achieved": tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
-                         "peak_kind": "%s bf16 dense burst (cuBLAS); the MMAs run f16 at the same rate" % peak_kind},
+                         "peak_kind": "%s bf16 dense burst (cuBLAS); the MMAs run f16 at the same rate" % peak_kind,
+                         "traffic": ncu_traffic("attn_fwd.cu:fp8", n_sel)},
             "kv_bytes_read": n_sel * 2 * 128 * case.d}
 
 

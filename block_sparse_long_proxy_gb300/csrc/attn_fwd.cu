@@ -52,8 +52,19 @@ namespace {
 constexpr int kStages = 2;
 constexpr int kSoftWarps = 8;
 constexpr int kConvWarps = 2;  // FP8 K/V only
+constexpr int kEpiWarp0 = 12;  // warps 12-15: epilogue
 constexpr int kMaxTopk = 1024;
-__host__ __device__ constexpr int attn_threads(bool fp8) { return 32 * (kSoftWarps + 2 + (fp8 ? kConvWarps : 0)); }
+// Four warpgroups: softmax (two), producer / MMA / FP8 converters, epilogue.
+// Launched at 128 registers a thread; the softmax warpgroups then take
+// kSoftRegs and the other two give theirs back down to kWg2Regs and
+// kEpiRegs, which adds up to the launch's 512 x 128 (an increase waits for
+// the decreases otherwise).
+constexpr int kAttnThreads = 512;
+constexpr int kLaunchRegs = 128;
+constexpr int kSoftRegs = 168;
+constexpr int kWg2Regs = 104;
+constexpr int kEpiRegs = 72;
+static_assert(256 * kSoftRegs + 128 * kWg2Regs + 128 * kEpiRegs == kAttnThreads * kLaunchRegs, "register split");
 
 struct AttnUnit {
   int32_t tile, g, h0, nh;
@@ -75,6 +86,13 @@ struct UnitHdr {
 constexpr int kListSlots = 2;
 constexpr int kHdrInts = 16;
 
+// A head's row statistics at the end of a unit, from the softmax warps to
+// the epilogue warps (two buffers per head, alternating by unit).
+struct UnitStats {
+  int32_t n, active, ok, h0, q_begin, rows, g, pad[9];
+  float m[128], l[128];
+};
+
 // Shared memory: Q (two heads), the K and V rings, the O staging buffer
 // (kStageO: one head's bf16 O tile, for the TMA stores of full tiles),
 // barriers, then the two list slots, whose size follows topk.
@@ -87,7 +105,8 @@ struct AttnSmem {
   static constexpr int kOOff = kVOff + kStages * kTileBytes;
   static constexpr int kOChunkBytes = 128 * 64 * 2;  // 64 columns of 128 rows
   static constexpr int kBarOff = kOOff + (kStageO ? kTileBytes : 0);
-  static constexpr int kListOff = kBarOff + 8 * 32;
+  static constexpr int kStatOff = kBarOff + 8 * 64;
+  static constexpr int kListOff = kStatOff + 4 * static_cast<int>(sizeof(UnitStats));
   static __host__ __device__ constexpr int slot_ints(int cap) { return kHdrInts + 2 * cap; }
   static __host__ __device__ constexpr int bytes(int cap) { return kListOff + kListSlots * slot_ints(cap) * 4; }
 };
@@ -98,7 +117,7 @@ struct AttnSmem {
 // barriers), and Q is released right after a unit's last QK so the next
 // unit's Q load overlaps the tail of the current one.
 template <int D, bool kOneKvHead, bool kFp8, bool kStageO>
-__global__ void __launch_bounds__(attn_threads(kFp8), 1)
+__global__ void __launch_bounds__(kAttnThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap k_map,
                     const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap o_map,
                     int32_t list_cap, const AttnUnit* __restrict__ units, int32_t n_units,
@@ -143,7 +162,10 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
   uint64_t* q_ready = raw_full + kStages;  // FP8: Q converted to f16
   uint64_t* ost_ready = q_ready + 1;       // a head's O staged (kStageO)
   uint64_t* ost_free = ost_ready + 1;      // the TMA store has read it
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ost_free + 1);
+  uint64_t* stat_full = ost_free + 1;      // [head * 2 + buffer]
+  uint64_t* stat_empty = stat_full + 4;    // [head * 2 + buffer]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stat_empty + 4);
+  UnitStats* const stats = reinterpret_cast<UnitStats*>(smem + L::kStatOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -158,13 +180,17 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       mbar_init(raw_full + s, 1);
     }
     mbar_init(q_ready, kConvWarps);
-    mbar_init(ost_ready, 4);  // the four warps of the head that stages
+    mbar_init(ost_ready, 4);  // the four epilogue warps
     mbar_init(ost_free, 1);
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(stat_full + i, 4);   // the head's four softmax warps
+      mbar_init(stat_empty + i, 4);  // the four epilogue warps
+    }
     for (int h = 0; h < 2; ++h) {
       mbar_init(s_full + h, 1);
       mbar_init(p_full + h, 4);
       mbar_init(o_done + h, 1);
-      mbar_init(o_free + h, 4);
+      mbar_init(o_free + h, 4);  // the epilogue warps
     }
     for (int i = 0; i < kListSlots; ++i) {
       mbar_init(list_full + i, 1);
@@ -181,9 +207,11 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // each role's branch starts with its warpgroup's register share
 
   if (warp == 8) {
     // ---------------------------------------------------------- producer
+    setmaxnreg_dec<kWg2Regs>();
     int kv_it = 0;
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
@@ -193,7 +221,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       const AttnUnit u = units[ui];
       const TileInfo tl = tiles[u.tile];
       const int32_t* sel = idx + (static_cast<int64_t>(u.tile) * hsel + u.g) * topk;
-      if (lane == 0) ok = mbar_wait(list_empty + k % kListSlots, ((k / kListSlots) & 1) ^ 1, err);
+      if (lane == 0) ok = mbar_wait_inl(list_empty + k % kListSlots, ((k / kListSlots) & 1) ^ 1, err);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       __syncwarp();
       if (!ok) break;
@@ -235,7 +263,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(list_full + k % kListSlots);
-        if (k > 0) ok = mbar_wait(q_empty, (k - 1) & 1, err);
+        if (k > 0) ok = mbar_wait_inl(q_empty, (k - 1) & 1, err);
         if (ok) {
           mbar_expect_tx(q_full, u.nh * L::kTileBytes);
           for (int h = 0; h < u.nh; ++h)
@@ -244,7 +272,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         }
         for (int i = 0; ok && i < n; ++i, ++kv_it) {
           const int s = kv_it % kStages;
-          if (!(ok = mbar_wait(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
+          if (!(ok = mbar_wait_inl(kv_empty + s, ((kv_it / kStages) & 1) ^ 1, err))) break;
           const int row = ls_row[i];
           if (kFp8) {  // e4m3 codes into the upper half of the stage; the converters expand them
             mbar_expect_tx(raw_full + s, 2 * 16384);
@@ -265,6 +293,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     }
   } else if (warp == 9) {
     // --------------------------------------------------------------- MMA
+    setmaxnreg_dec<kWg2Regs>();
     if (lane == 0) {
       // The issuing thread runs only a step ahead of the tensor pipe, so
       // anything between two MMA groups (a wait, a commit, address
@@ -296,17 +325,23 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       int kv_it = 0, ch0 = 0, ch1 = 0;
       bool ok = true;
       for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
-        if (!(ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err))) break;
+        if (!(ok = mbar_wait_inl(list_full + k % kListSlots, (k / kListSlots) & 1, err))) break;
         const int n = lhdr(k).n;
         const bool two = lhdr(k).nh == 2;
         mbar_arrive(list_empty + k % kListSlots);
-        if (!(ok = mbar_wait(kFp8 ? q_ready : q_full, k & 1, err))) break;
+        if (!(ok = mbar_wait_inl(kFp8 ? q_ready : q_full, k & 1, err))) break;
         tc_fence_after();
+        // O_h of every unit is released by the epilogue once per unit; the
+        // MMA thread waits for that release in every unit (also where it
+        // issues nothing into O_h), so that a parity wait never meets a
+        // barrier two phases behind
         if (n == 0) {
           mma_commit(q_empty);
+          if (k > 0 && !(ok = mbar_wait_inl(o_free, (k - 1) & 1, err) && mbar_wait_inl(o_free + 1, (k - 1) & 1, err)))
+            break;
           continue;
         }
-        if (!(ok = mbar_wait(kv_full + (kv_it & 1), (kv_it >> 1) & 1, err))) break;
+        if (!(ok = mbar_wait_inl(kv_full + (kv_it & 1), (kv_it >> 1) & 1, err))) break;
         tc_fence_after();
         qk(0, kv_it & 1);
         if (two) qk(1, kv_it & 1);
@@ -316,15 +351,16 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
           const int s = it & 1, s1 = s ^ 1;
           const bool more = i + 1 < n;
           // head 0: P_0 . V, then S_0 of the next block
-          if (!(ok = mbar_wait(p_full, (ch0 + i) & 1, err))) break;
+          if (!(ok = mbar_wait_inl(p_full, (ch0 + i) & 1, err))) break;
           // the first P.V of a unit overwrites O_h: the previous unit's
           // epilogue must have read it (the QKs above already overlap it)
-          if (i == 0 && k > 0 && !(ok = mbar_wait(o_free, (k - 1) & 1, err))) break;
+          if (i == 0 && k > 0 && !(ok = mbar_wait_inl(o_free, (k - 1) & 1, err))) break;
+          if (i == 0 && k > 0 && !two && !(ok = mbar_wait_inl(o_free + 1, (k - 1) & 1, err))) break;
           tc_fence_after();
           pv(0, s, i > 0);
           if (!two) mma_commit(kv_empty + s);
           if (more) {
-            if (!(ok = mbar_wait(kv_full + s1, ((it + 1) >> 1) & 1, err))) break;
+            if (!(ok = mbar_wait_inl(kv_full + s1, ((it + 1) >> 1) & 1, err))) break;
             tc_fence_after();
             qk(0, s1);
             if (!two && i + 1 == n - 1) mma_commit(q_empty);
@@ -333,8 +369,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
           }
           if (!two) continue;
           // head 1
-          if (!(ok = mbar_wait(p_full + 1, (ch1 + i) & 1, err))) break;
-          if (i == 0 && k > 0 && !(ok = mbar_wait(o_free + 1, (k - 1) & 1, err))) break;
+          if (!(ok = mbar_wait_inl(p_full + 1, (ch1 + i) & 1, err))) break;
+          if (i == 0 && k > 0 && !(ok = mbar_wait_inl(o_free + 1, (k - 1) & 1, err))) break;
           tc_fence_after();
           pv(1, s, i > 0);
           mma_commit(kv_empty + s);
@@ -350,36 +386,36 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         kv_it += n;
       }
       mma_commit(drain);
-      mbar_wait(drain, 0, err);
+      mbar_wait_inl(drain, 0, err);
     }
   } else if (warp < kSoftWarps) {
     // ----------------------------------------------------------- softmax
+    setmaxnreg_inc<kSoftRegs>();
+    // Each unit's row statistics go to the epilogue warps, which normalise
+    // and store O while these warps go on to the next unit's blocks.
     const int h = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t s_addr = tmem + lane_base + h * 128;
     const uint32_t o_addr = tmem + lane_base + 256 + h * D;
-    int ch = 0, od = 0;  // blocks and units (with blocks) of head h so far
-    int ost_uses = 0;    // (unit, head) uses of the O staging buffer so far
+    int ch = 0;  // blocks of head h so far
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
       const UnitHdr& ls = lhdr(k);
       const int32_t* const ls_j = lj(k);
-      if (ok) ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
+      if (ok) ok = mbar_wait_inl(list_full + k % kListSlots, (k / kListSlots) & 1, err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
       const int rows = ls.rows, pos0 = ls.pos0;
       // FP8: the scores are q . k_code, scaled by k_scale of the unit's KV head
       const float sl2 = kFp8 ? scale_log2 * k_scale[ls.g] : scale_log2;
-      const float o_scale = kFp8 ? v_scale[ls.g] : 1.f;
       const bool active = ok && h < nh;
-      bool o_released = false;
       const bool row_ok = r < rows;
       const int qpos = pos0 + r;
       float m = -INFINITY, l = 0.f;
       for (int i = 0; active && ok && i < n; ++i) {
-        if (!(ok = mbar_wait(s_full + h, (ch + i) & 1, err))) break;
+        if (!(ok = mbar_wait_inl(s_full + h, (ch + i) & 1, err))) break;
         tc_fence_after();
         uint32_t sv[128];
 #pragma unroll
@@ -451,90 +487,137 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         if (lane == 0) mbar_arrive(p_full + h);
         m = m_new;
       }
-      if (active && ok) {
-        if (n > 0) ok = mbar_wait(o_done + h, (od++) & 1, err);
-        tc_fence_after();
-        const int64_t orow = static_cast<int64_t>(ls.q_begin + r) * hq + ls.h0 + h;
-        const float inv_l = l > 0.f ? o_scale / l : 0.f;
-        // all of O_h in one round of loads; O_h is then released to the next
-        // unit's P.V before the stores
-        uint32_t ov[D];
-        if (n > 0) {
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tmem_ld32(o_addr + c * 32, ov + c * 32);
-          tmem_wait_ld();
-        } else {
-#pragma unroll
-          for (int e = 0; e < D; ++e) ov[e] = 0u;
-        }
-        tc_fence_before();
+      // this head's statistics (buffer k % 2, reused once the epilogue has
+      // read its contents from two units back)
+      const int b = k & 1;
+      UnitStats& st = stats[h * 2 + b];
+      if (k >= 2 && ok) ok = mbar_wait_inl(stat_empty + h * 2 + b, ((k >> 1) - 1) & 1, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      st.m[r] = m;
+      st.l[r] = l;
+      if (quarter == 0 && lane == 0) {
+        st.n = n;
+        st.active = active ? 1 : 0;
+        st.ok = ok ? 1 : 0;
+        st.h0 = ls.h0;
+        st.q_begin = ls.q_begin;
+        st.rows = rows;
+        st.g = ls.g;
+      }
+      if (h < nh) ch += n;
+      // the list slot may be refilled (every warp arrives once per unit, active or not)
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(stat_full + h * 2 + b);
+        mbar_arrive(list_empty + k % kListSlots);
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ---------------------------------------------------------- epilogue
+    setmaxnreg_dec<kEpiRegs>();
+    // Per unit, head 0 then head 1: wait for the softmax's statistics and
+    // for the unit's last P.V, read O_h in 32-column chunks, release it to
+    // the next unit's P.V, and write bf16 O = O_h / l (times v_scale for
+    // FP8) and the natural-log LSE.  Full tiles of FP8 plans go through the
+    // shared staging buffer and TMA tensor stores.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    int od0 = 0, od1 = 0;  // units with blocks of head 0 / head 1 so far
+    int ost_uses = 0;      // (unit, head) uses of the O staging buffer so far
+    bool ok = true;
+    for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
+      const int b = k & 1;
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        const UnitStats& st = stats[h * 2 + b];
+        if (ok) ok = mbar_wait_inl(stat_full + h * 2 + b, (k >> 1) & 1, err);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        const int n = st.n, rows = st.rows, q_begin = st.q_begin, h0 = st.h0;
+        const bool active = ok && st.active != 0;
+        const bool unit_ok = ok && st.ok != 0;
+        const float m = st.m[r], l = st.l[r];
+        const float o_scale = kFp8 ? v_scale[st.g] : 1.f;
         __syncwarp();
-        if (lane == 0) mbar_arrive(o_free + h);
-        o_released = true;
-        if (kStageO && rows == 128) {
-          // a full tile: the bf16 O rows go to the staging buffer (the TMA
-          // box layout: 64-column chunks of 128-byte rows, 16-byte units
-          // swizzled by row % 8), then one thread stores the boxes.  The
-          // buffer is shared by both heads and used once per (unit, head) in
-          // order; every hand-off is a bounded mbarrier wait.
-          const int use = ost_uses + h;
-          uint8_t* ob = smem + L::kOOff + r * 128;
-          if (use > 0 && ok) ok = mbar_wait(ost_free, (use - 1) & 1, err);
+        if (lane == 0) mbar_arrive(stat_empty + h * 2 + b);
+        if (!active) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free + h);
+          continue;
+        }
+        const bool has_o = n > 0;
+        if (has_o && ok) ok = mbar_wait_inl(o_done + h, (h == 0 ? od0++ : od1++) & 1, err);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        tc_fence_after();
+        const uint32_t o_addr = tmem + lane_base + 256 + h * D;
+        const float inv_l = l > 0.f ? o_scale / l : 0.f;
+        const bool row_ok = r < rows;
+        const int64_t orow = static_cast<int64_t>(q_begin + r) * hq + h0 + h;
+        const bool staged = kStageO && rows == 128;
+        if (staged) {
+          const int use = ost_uses++;
+          if (use > 0 && ok) ok = mbar_wait_inl(ost_free, (use - 1) & 1, err);
+        }
+        uint8_t* const ob = smem + L::kOOff + r * 128;
+        uint4* const dst = reinterpret_cast<uint4*>(out + orow * D);
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          if (has_o) {
+            tmem_ld32(o_addr + c * 32, ov);
+            tmem_wait_ld();
+          } else {
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c)
+            for (int e = 0; e < 32; ++e) ov[e] = 0u;
+          }
+          if (c == D / 32 - 1) {  // all of O_h is in registers: the next unit's P.V may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free + h);
+          }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              const uint32_t* x = ov + 64 * c + 8 * e;
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
-              *reinterpret_cast<uint4*>(ob + c * L::kOChunkBytes + ((e ^ (r & 7)) << 4)) = w;
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t* x = ov + 8 * e;
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(x[0]) * inv_l, __uint_as_float(x[1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(x[2]) * inv_l, __uint_as_float(x[3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(x[4]) * inv_l, __uint_as_float(x[5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(x[6]) * inv_l, __uint_as_float(x[7]) * inv_l);
+            if (staged) {
+              // the TMA box layout: 64-column chunks of 128-byte rows, 16-byte
+              // units swizzled by row % 8
+              const int unit = (c & 1) * 4 + e;
+              *reinterpret_cast<uint4*>(ob + (c >> 1) * L::kOChunkBytes + ((unit ^ (r & 7)) << 4)) = w;
+            } else if (unit_ok && row_ok) {
+              dst[c * 4 + e] = w;
             }
+          }
+        }
+        if (staged) {
           fence_async_shared();  // the TMA store reads them through the async proxy
           __syncwarp();
           if (lane == 0) mbar_arrive(ost_ready);
           if (quarter == 0 && lane == 0) {
-            if (ok) ok = mbar_wait(ost_ready, use & 1, err);
-            if (ok) {
+            if (ok) ok = mbar_wait_inl(ost_ready, (ost_uses - 1) & 1, err);
+            if (ok && unit_ok) {
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
-                tma_store_3d(&o_map, smem + L::kOOff + c * L::kOChunkBytes, 64 * c, ls.h0 + h, ls.q_begin);
+                tma_store_3d(&o_map, smem + L::kOOff + c * L::kOChunkBytes, 64 * c, h0 + h, q_begin);
               bulk_commit_group();
-              bulk_wait_group_read0();
             }
+            bulk_wait_group_read0();
             mbar_arrive(ost_free);
           }
-        } else if (ok && row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(out + orow * D);
-#pragma unroll
-          for (int e = 0; e < D / 8; ++e) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv_l, __uint_as_float(ov[8 * e + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv_l, __uint_as_float(ov[8 * e + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv_l, __uint_as_float(ov[8 * e + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv_l, __uint_as_float(ov[8 * e + 7]) * inv_l);
-            dst[e] = w;
-          }
         }
-        if (ok && row_ok && lse != nullptr)
+        if (unit_ok && row_ok && lse != nullptr)
           lse[orow] = l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
       }
-      if (h < nh) ch += n;
-      if (kStageO && rows == 128) ost_uses += nh;  // the staging buffer's uses, the same count in every warp
-      // O_h may be overwritten by the next unit, and the list slot refilled
-      // (every warp arrives once per unit, active or not)
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (!o_released) mbar_arrive(o_free + h);
-        mbar_arrive(list_empty + k % kListSlots);
-      }
     }
-    if (kStageO && quarter == 0 && lane == 0) bulk_wait_group0();  // this head's stores are complete
+    if (kStageO && quarter == 0 && lane == 0) bulk_wait_group0();  // the stores are complete
   } else if (kFp8) {
     // -------------------------------------------------- FP8 converters
+    setmaxnreg_dec<kWg2Regs>();
     // Thread ct of the two warps owns rows ct and ct + 64 of every K / V
     // block: it reads a row's 128 e4m3 codes (eight 16-byte units of the
     // swizzled upper half of the stage) before it writes any of the row's
@@ -571,14 +654,14 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ok && ui < n_units; ++k, ui += gridDim.x) {
       const UnitHdr& ls = lhdr(k);
-      ok = mbar_wait(list_full + k % kListSlots, (k / kListSlots) & 1, err);
+      ok = mbar_wait_inl(list_full + k % kListSlots, (k / kListSlots) & 1, err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (!ok) break;
       const int n = ls.n, nh = ls.nh;
       __syncwarp();
       if (lane == 0) mbar_arrive(list_empty + k % kListSlots);
       // Q of the unit's heads, bf16 -> f16 in place
-      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(q_full, k & 1, err)))) break;
+      if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait_inl(q_full, k & 1, err)))) break;
       for (int hh = 0; hh < nh; ++hh) {
         uint4* qv = reinterpret_cast<uint4*>(q_s + hh * L::kTileBytes);
 #pragma unroll 4
@@ -596,7 +679,7 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
       if (lane == 0) mbar_arrive(q_ready);
       for (int i = 0; i < n; ++i, ++kv_it) {
         const int s = kv_it % kStages;
-        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait(raw_full + s, (kv_it / kStages) & 1, err)))) break;
+        if (!(ok = __all_sync(0xFFFFFFFFu, mbar_wait_inl(raw_full + s, (kv_it / kStages) & 1, err)))) break;
         expand(k_s + s * L::kTileBytes);
         expand(v_s + s * L::kTileBytes);
         fence_async_shared();
@@ -604,6 +687,8 @@ __global__ void __launch_bounds__(attn_threads(kFp8), 1)
         if (lane == 0) mbar_arrive(kv_full + s);
       }
     }
+  } else {
+    setmaxnreg_dec<kWg2Regs>();  // warps 10-11 without FP8 K/V: idle
   }
   tc_fence_before();
   __syncthreads();
@@ -651,6 +736,17 @@ constexpr int kMaxSmem = 232448;  // 227 KB of dynamic shared memory per CTA
 // room for the staging buffer, else with per-thread stores.  Measured at
 // S=32768: FP8 973 -> 1019 TFLOP/s staged; bf16 0.808 -> 0.826 ms staged,
 // so bf16 keeps the per-thread stores.
+// The register split above assumes the kernel is launched at exactly
+// kLaunchRegs a thread; any other count would leave an increase waiting, so
+// such a build is not launched.
+template <typename K>
+cudaError_t check_launch_regs(K kern) {
+  cudaFuncAttributes a;
+  const cudaError_t e = cudaFuncGetAttributes(&a, kern);
+  if (e != cudaSuccess) return e;
+  return a.numRegs == kLaunchRegs ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 template <int D, bool kOneKvHead, bool kFp8>
 cudaError_t launch_attn_variant(dim3 grid, cudaStream_t st, const CUtensorMap& qm, const CUtensorMap& km,
                                 const CUtensorMap& vm, const CUtensorMap& om, int32_t topk, const AttnUnit* units,
@@ -663,16 +759,18 @@ cudaError_t launch_attn_variant(dim3 grid, cudaStream_t st, const CUtensorMap& q
     const int staged = AttnSmem<D, true>::bytes(cap) + 1024;
     if (staged <= kMaxSmem) {
       auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, true>;
+      if (const cudaError_t e = check_launch_regs(kern)) return e;
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, staged);
-      return launch_pdl(kern, grid, dim3(attn_threads(kFp8)), staged, st, qm, km, vm, om, cap, units, n_units,
+      return launch_pdl(kern, grid, dim3(kAttnThreads), staged, st, qm, km, vm, om, cap, units, n_units,
                         tiles, idx, kv_indices, num_pages, o, lse, hq, hsel, kv_div, topk, scale_log2, k_scale,
                         v_scale, err);
     }
   }
   const int plain = AttnSmem<D, false>::bytes(kMaxTopk) + 1024;
   auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, false>;
+  if (const cudaError_t e = check_launch_regs(kern)) return e;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plain);
-  return launch_pdl(kern, grid, dim3(attn_threads(kFp8)), plain, st, qm, km, vm, om, cap, units, n_units, tiles, idx,
+  return launch_pdl(kern, grid, dim3(kAttnThreads), plain, st, qm, km, vm, om, cap, units, n_units, tiles, idx,
                     kv_indices, num_pages, o, lse, hq, hsel, kv_div, topk, scale_log2, k_scale, v_scale, err);
 }
 

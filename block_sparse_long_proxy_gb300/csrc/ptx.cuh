@@ -93,6 +93,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, err);
 }
+// The same wait with its slow path inlined, for kernels whose warpgroups run
+// at different register counts (setmaxnreg): such regions cannot share a
+// called function.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_hint(bar, parity, 100000u)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (err) atomicOr(err, 2u);
+      return false;
+    }
+  }
+  return true;
+}
 
 // ---------------------------------------------------------------------- TMA
 
@@ -147,6 +161,17 @@ __device__ __forceinline__ void tmem_relinquish() {
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Warpgroup register reallocation: every warp of the warpgroup executes the
+// same one.  An increase waits until other warpgroups' decreases have freed
+// the registers, so the shares must add up to the launch's total.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");

@@ -94,8 +94,9 @@ struct UnitStats {
 };
 
 // Shared memory: Q (two heads), the K and V rings, the O staging buffer
-// (kStageO: one head's bf16 O tile, for the TMA stores of full tiles),
-// barriers, then the two list slots, whose size follows topk.
+// (kStageO: one 64-column box of a head's bf16 O tile, for the TMA stores of
+// full tiles), barriers, the units' row statistics, then the two list slots,
+// whose size follows topk.
 template <int D, bool kStageO>
 struct AttnSmem {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16, in D/64 swizzled chunks of 16 KB
@@ -104,7 +105,7 @@ struct AttnSmem {
   static constexpr int kVOff = kKOff + kStages * kTileBytes;
   static constexpr int kOOff = kVOff + kStages * kTileBytes;
   static constexpr int kOChunkBytes = 128 * 64 * 2;  // 64 columns of 128 rows
-  static constexpr int kBarOff = kOOff + (kStageO ? kTileBytes : 0);
+  static constexpr int kBarOff = kOOff + (kStageO ? kOChunkBytes : 0);
   static constexpr int kStatOff = kBarOff + 8 * 64;
   static constexpr int kListOff = kStatOff + 4 * static_cast<int>(sizeof(UnitStats));
   static __host__ __device__ constexpr int slot_ints(int cap) { return kHdrInts + 2 * cap; }
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int od0 = 0, od1 = 0;  // units with blocks of head 0 / head 1 so far
-    int ost_uses = 0;      // (unit, head) uses of the O staging buffer so far
+    int ost_uses = 0;      // 64-column boxes staged so far
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
       const int b = k & 1;
@@ -555,10 +556,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const bool row_ok = r < rows;
         const int64_t orow = static_cast<int64_t>(q_begin + r) * hq + h0 + h;
         const bool staged = kStageO && rows == 128;
-        if (staged) {
-          const int use = ost_uses++;
-          if (use > 0 && ok) ok = mbar_wait_inl(ost_free, (use - 1) & 1, err);
-        }
         uint8_t* const ob = smem + L::kOOff + r * 128;
         uint4* const dst = reinterpret_cast<uint4*>(out + orow * D);
 #pragma unroll 1
@@ -576,6 +573,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free + h);
           }
+          // staged: one 64-column box at a time, once the previous box's
+          // store has read the buffer
+          if (staged && (c & 1) == 0 && ost_uses > 0 && ok) ok = mbar_wait_inl(ost_free, (ost_uses - 1) & 1, err);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t* x = ov + 8 * e;
@@ -588,26 +588,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
               // the TMA box layout: 64-column chunks of 128-byte rows, 16-byte
               // units swizzled by row % 8
               const int unit = (c & 1) * 4 + e;
-              *reinterpret_cast<uint4*>(ob + (c >> 1) * L::kOChunkBytes + ((unit ^ (r & 7)) << 4)) = w;
+              *reinterpret_cast<uint4*>(ob + ((unit ^ (r & 7)) << 4)) = w;
             } else if (unit_ok && row_ok) {
               dst[c * 4 + e] = w;
             }
           }
-        }
-        if (staged) {
-          fence_async_shared();  // the TMA store reads them through the async proxy
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ost_ready);
-          if (quarter == 0 && lane == 0) {
-            if (ok) ok = mbar_wait_inl(ost_ready, (ost_uses - 1) & 1, err);
-            if (ok && unit_ok) {
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c)
-                tma_store_3d(&o_map, smem + L::kOOff + c * L::kOChunkBytes, 64 * c, h0 + h, q_begin);
-              bulk_commit_group();
+          if (staged && (c & 1) == 1) {  // the box is complete: one thread stores it
+            fence_async_shared();        // the TMA store reads it through the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ost_ready);
+            if (quarter == 0 && lane == 0) {
+              if (ok) ok = mbar_wait_inl(ost_ready, ost_uses & 1, err);
+              if (ok && unit_ok) {
+                tma_store_3d(&o_map, smem + L::kOOff, 64 * (c >> 1), h0 + h, q_begin);
+                bulk_commit_group();
+              }
+              bulk_wait_group_read0();
+              mbar_arrive(ost_free);
             }
-            bulk_wait_group_read0();
-            mbar_arrive(ost_free);
+            ++ost_uses;
           }
         }
         if (unit_ok && row_ok && lse != nullptr)

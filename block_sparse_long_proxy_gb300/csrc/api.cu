@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 #include <cuda.h>
 #include <stdarg.h>
+#include <stdlib.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -95,6 +96,87 @@ __global__ void selftest_wait_kernel(uint32_t* err) {
 }  // namespace
 }  // namespace msa
 
+namespace msa {
+namespace {
+
+// MSA_CHECKS: one read of a call's inputs and outputs; any NaN raises
+// kErrNonFinite.  The test is on the bits, so infinities pass: fp32 and bf16
+// NaN have an all-ones exponent and a non-zero mantissa, an e4m3 NaN is
+// S.1111.111.
+template <typename T>
+__device__ __forceinline__ bool nan_bits(T v) {
+  const uint32_t u = static_cast<uint32_t>(v);
+  if (sizeof(T) == 4) return (u & 0x7FFFFFFFu) > 0x7F800000u;
+  if (sizeof(T) == 2) return (u & 0x7FFFu) > 0x7F80u;
+  return (u & 0x7Fu) == 0x7Fu;
+}
+
+template <typename T>
+__global__ void nan_scan_kernel(const T* __restrict__ x, int64_t n, uint32_t* err) {
+  bool bad = false;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    bad |= nan_bits(x[i]);
+  if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, kErrNonFinite);
+}
+
+// The pages a plan's page table names, per_page elements each (out-of-range
+// ids are skipped: the compute kernels report those).
+template <typename T>
+__global__ void nan_scan_pages_kernel(const T* __restrict__ pool, const int32_t* __restrict__ kv_indices,
+                                      int32_t n_entries, int64_t num_pages, int64_t per_page, uint32_t* err) {
+  for (int e = blockIdx.x; e < n_entries; e += gridDim.x) {
+    const int64_t page = kv_indices[e];
+    if (page < 0 || page >= num_pages) continue;  // uniform over the CTA
+    const T* x = pool + page * per_page;
+    bool bad = false;
+    for (int64_t i = threadIdx.x; i < per_page; i += blockDim.x) bad |= nan_bits(x[i]);
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(err, kErrNonFinite);
+  }
+}
+
+// n elements of `elem` bytes (4: fp32, 2: bf16, 1: e4m3) of an array, when
+// the plan was created under MSA_CHECKS; otherwise nothing.
+msa_status scan_rows(const msa_plan_s* p, const void* x, int64_t n, int elem, cudaStream_t st) {
+  if (!p->checks || x == nullptr || n <= 0) return MSA_OK;
+  const int grid = static_cast<int>(std::min<int64_t>(int64_t(p->num_sms) * 8, (n + 255) / 256));
+  if (elem == 4)
+    nan_scan_kernel<uint32_t><<<grid, 256, 0, st>>>(static_cast<const uint32_t*>(x), n, p->err_d);
+  else if (elem == 2)
+    nan_scan_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(x), n, p->err_d);
+  else
+    nan_scan_kernel<uint8_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(x), n, p->err_d);
+  return cuda_check(cudaGetLastError(), "MSA_CHECKS: scan launch");
+}
+
+// The referenced pages of a pool, per_page elements of `elem` bytes each.
+msa_status scan_pages(const msa_plan_s* p, const void* pool, const int32_t* kv_indices, int64_t per_page, int elem,
+                      cudaStream_t st) {
+  if (!p->checks || pool == nullptr) return MSA_OK;
+  const int grid = std::min(p->n_page_entries, p->num_sms * 8);
+  const int n = p->n_page_entries;
+  if (elem == 2)
+    nan_scan_pages_kernel<uint16_t><<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(pool), kv_indices, n,
+                                                          p->num_pages, per_page, p->err_d);
+  else
+    nan_scan_pages_kernel<uint8_t><<<grid, 256, 0, st>>>(static_cast<const uint8_t*>(pool), kv_indices, n,
+                                                         p->num_pages, per_page, p->err_d);
+  return cuda_check(cudaGetLastError(), "MSA_CHECKS: scan launch");
+}
+
+// After a proxy call: its pq rows and referenced pk pages (bf16 or e4m3),
+// then its max_score.
+msa_status scan_proxy(const msa_plan_s* p, msa_status s, const void* pq, const void* pk_pages,
+                      const int32_t* kv_indices, int pk_elem, const float* ms, cudaStream_t st) {
+  if (s == MSA_OK) s = scan_rows(p, pq, p->total_q * p->hp * p->dp, 2, st);
+  if (s == MSA_OK && pk_elem > 0) s = scan_pages(p, pk_pages, kv_indices, int64_t(128) * p->dp, pk_elem, st);
+  if (s == MSA_OK) s = scan_rows(p, ms, int64_t(p->n_tiles) * p->hp * p->max_blocks, 4, st);
+  return s;
+}
+
+}  // namespace
+}  // namespace msa
+
 extern "C" {
 
 const char* msa_last_error(void) { return g_last_error.c_str(); }
@@ -173,6 +255,10 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   p->n_page_entries = static_cast<int32_t>(page_base);
   p->n_tiles = static_cast<int32_t>(p->tiles.size());
   p->decode = all_one;
+  {  // debug mode: scan every call's outputs for NaN
+    const char* c = getenv("MSA_CHECKS");
+    p->checks = c != nullptr && c[0] != '\0' && strcmp(c, "0") != 0;
+  }
   if (p->n_tiles == 0) {
     delete p;
     return set_error(MSA_ERR_INVALID_ARG, "msa_plan: no query rows in the batch");
@@ -260,8 +346,9 @@ msa_status msa_proxy_maxscore(msa_plan_t plan, const void* pq, const void* pk_pa
   if (!aligned16(pq) || !aligned16(pk_pages))
     return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore: pq and pk_pages must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (plan->decode) return launch_proxy_decode(plan, pq, pk_pages, kv_indices, max_score, st);
-  return launch_proxy_prefill(plan, pq, pk_pages, kv_indices, max_score, st);
+  const msa_status s = plan->decode ? launch_proxy_decode(plan, pq, pk_pages, kv_indices, max_score, st)
+                                    : launch_proxy_prefill(plan, pq, pk_pages, kv_indices, max_score, st);
+  return scan_proxy(plan, s, pq, pk_pages, kv_indices, 2, max_score, st);
 }
 
 msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* pk_pages, const float* pk_scale,
@@ -272,8 +359,9 @@ msa_status msa_proxy_maxscore_fp8(msa_plan_t plan, const void* pq, const void* p
     return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_maxscore_fp8: pq and pk_pages must be 16-byte aligned");
   if (!plan->decode)
     return set_error(MSA_ERR_UNSUPPORTED, "msa_proxy_maxscore_fp8: FP8 proxy K is implemented for decode batches only");
-  return launch_proxy_decode_fp8(plan, pq, pk_pages, pk_scale, kv_indices, max_score,
-                                 reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return scan_proxy(plan, launch_proxy_decode_fp8(plan, pq, pk_pages, pk_scale, kv_indices, max_score, st), pq,
+                    pk_pages, kv_indices, 1, max_score, st);
 }
 
 msa_status msa_proxy_maxscore_nvfp4(msa_plan_t plan, const void* pq, const void* pk_codes,
@@ -287,8 +375,12 @@ msa_status msa_proxy_maxscore_nvfp4(msa_plan_t plan, const void* pq, const void*
   if (!plan->decode)
     return set_error(MSA_ERR_UNSUPPORTED,
                      "msa_proxy_maxscore_nvfp4: the NVFP4 proxy K is implemented for decode batches only");
-  return launch_proxy_decode_nvfp4(plan, pq, pk_codes, pk_block_scales, pk_global_scale, kv_indices, max_score,
-                                   reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // e2m1 codes have no NaN: pq and max_score are scanned
+  return scan_proxy(plan,
+                    launch_proxy_decode_nvfp4(plan, pq, pk_codes, pk_block_scales, pk_global_scale, kv_indices,
+                                              max_score, st),
+                    pq, nullptr, kv_indices, 0, max_score, st);
 }
 
 msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages, const int32_t* kv_indices,
@@ -297,8 +389,9 @@ msa_status msa_proxy_topk(msa_plan_t plan, const void* pq, const void* pk_pages,
     return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_topk: NULL argument");
   if (!aligned16(pq) || !aligned16(pk_pages))
     return set_error(MSA_ERR_INVALID_ARG, "msa_proxy_topk: pq and pk_pages must be 16-byte aligned");
-  return launch_proxy_topk(plan, pq, pk_pages, kv_indices, max_score, kv_block_indexes,
-                           reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return scan_proxy(plan, launch_proxy_topk(plan, pq, pk_pages, kv_indices, max_score, kv_block_indexes, st), pq,
+                    pk_pages, kv_indices, 2, max_score, st);
 }
 
 msa_status msa_topk_select(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,
@@ -325,11 +418,20 @@ msa_status msa_sparse_attn(msa_plan_t plan, const void* q, const void* k_pages, 
   if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr))
     return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn: k_scale/v_scale must be given exactly for FP8 K/V");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  if (fp8 && plan->decode)
-    return launch_attn_decode(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale, out,
-                              lse, st);
-  return launch_attn_prefill(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale, out, lse,
-                             st);
+  msa_status s = fp8 && plan->decode
+                     ? launch_attn_decode(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale,
+                                          out, lse, st)
+                     : launch_attn_prefill(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, k_scale, v_scale,
+                                           out, lse, st);
+  const int64_t rows = plan->total_q * plan->hq;
+  const int kv_elem = fp8 ? 1 : 2;
+  const int64_t per_page = int64_t(plan->hkv) * 128 * plan->d;
+  if (s == MSA_OK) s = scan_rows(plan, q, rows * plan->d, 2, st);
+  if (s == MSA_OK) s = scan_pages(plan, k_pages, kv_indices, per_page, kv_elem, st);
+  if (s == MSA_OK) s = scan_pages(plan, v_pages, kv_indices, per_page, kv_elem, st);
+  if (s == MSA_OK) s = scan_rows(plan, out, rows * plan->d, 2, st);
+  if (s == MSA_OK) s = scan_rows(plan, lse, rows, 4, st);
+  return s;
 }
 
 msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pages, const void* v_pages,
@@ -342,8 +444,20 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
     return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn_bwd: NULL argument");
   if (plan->kv_dtype != MSA_KV_BF16)
     return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: bf16 K/V only");
-  return launch_attn_bwd(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, dout, pq, pk_pages,
-                         kl_weight, dq, dk_pages, dv_pages, dpq, dpk_pages, reinterpret_cast<cudaStream_t>(stream));
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  msa_status s = launch_attn_bwd(plan, q, k_pages, v_pages, kv_indices, kv_block_indexes, out, lse, dout, pq,
+                                 pk_pages, kl_weight, dq, dk_pages, dv_pages, dpq, dpk_pages, st);
+  const int64_t rows = plan->total_q * plan->hq;
+  const int64_t per_page = int64_t(plan->hkv) * 128 * plan->d;
+  if (s == MSA_OK) s = scan_rows(plan, q, rows * plan->d, 2, st);
+  if (s == MSA_OK) s = scan_rows(plan, dout, rows * plan->d, 2, st);
+  if (s == MSA_OK) s = scan_rows(plan, pq, plan->total_q * plan->hp * plan->dp, 2, st);
+  if (s == MSA_OK) s = scan_pages(plan, k_pages, kv_indices, per_page, 2, st);
+  if (s == MSA_OK) s = scan_pages(plan, v_pages, kv_indices, per_page, 2, st);
+  if (s == MSA_OK) s = scan_pages(plan, pk_pages, kv_indices, int64_t(128) * plan->dp, 2, st);
+  if (s == MSA_OK) s = scan_rows(plan, dq, rows * plan->d, 4, st);
+  if (s == MSA_OK) s = scan_rows(plan, dpq, plan->total_q * plan->hp * plan->dp, 4, st);
+  return s;
 }
 
 void msa_test_fail_plan_allocs(int32_t count) { g_fail_allocs.store(count > 0 ? count : 0); }
@@ -381,7 +495,9 @@ msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream) {
   s = cuda_check(cudaMemset(plan->err_d, 0, sizeof(uint32_t)), "msa_check_errors: clear");
   if (s != MSA_OK) return s;
   if (word & kErrTimeout) return set_error(MSA_ERR_TIMEOUT, "a bounded device-side wait gave up (word 0x%x)", word);
-  return set_error(MSA_ERR_DEVICE_CHECK, "a device-side bounds check fired: page id out of range (word 0x%x)", word);
+  if (word & kErrDeviceCheck)
+    return set_error(MSA_ERR_DEVICE_CHECK, "a device-side bounds check fired: page id out of range (word 0x%x)", word);
+  return set_error(MSA_ERR_NONFINITE, "MSA_CHECKS: an output held a NaN (word 0x%x)", word);
 }
 
 }  // extern "C"

@@ -16,7 +16,6 @@
 //   dpk = w/sqrt(dp) * (p_proxy^T.pq - (1/G) sum_h P_h^T.pq)
 //
 // Kernels, in stream order:
-//   zero     dpk rows of every referenced page (it is reduced by atomics)
 //   proxy    the proxy softmax over Omega on the tensor cores: the forward
 //            attention kernel (attn_fwd.cu) with pq as queries and the shared
 //            proxy K head as keys and values gives p_proxy . pk and its LSE
@@ -25,11 +24,15 @@
 //            ([proxy head][row]) and dpq's proxy term (plain store)
 //   index    page owners, then the page -> selections inverse index
 //   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
-//            store) and dpq's main term (fp32 atomics, G per element)
+//            store) and dpq's main term (a partial per head; the last of the
+//            G heads adds them in head order to the proxy term)
 //   dkv      per (physical page, group), tcgen05 (bwd_dkv.cu): loops over
 //            the selections of the page by any page-table entry (sorted, so
 //            sums are deterministic); dk, dv (owned, plain store) and dpk
-//            (both terms, fp32 atomics across groups)
+//            (both terms; a partial per KV head, the last of them adds them
+//            in KV-head order)
+// No gradient is reduced by atomics: every sum has a fixed order, so the
+// backward gives the same bits on every run.
 
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -203,24 +206,14 @@ __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_
       static_cast<int32_t>(e);
 }
 
-// dpk rows of every referenced page start at zero (they are reduced by
-// atomics across groups).
-__global__ void bwd_zero_dpk_kernel(const int32_t* __restrict__ kv_indices, int32_t n_entries, int64_t num_pages,
-                                    float* __restrict__ dpk) {
-  const int e = blockIdx.x;
-  if (e >= n_entries) return;
-  const int64_t page = kv_indices[e];
-  if (page < 0 || page >= num_pages) return;
-  float4* p = reinterpret_cast<float4*>(dpk + page * 128 * kDP);
-  for (int i = threadIdx.x; i < 128 * kDP / 4; i += blockDim.x) p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 }  // namespace
 
 // The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
 // fp32), lsept ([Hp][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
-// Hp, dp]) and LSE (fp32 [total_q, Hp]), the inverse index (int32), then the
-// page owners (int32 [num_pages]).
+// Hp, dp]) and LSE (fp32 [total_q, Hp]), the inverse index (int32), the page
+// owners (int32 [num_pages]), dpq's per-head partials (fp32 [n_tiles][Hq]
+// [128][dp]) and their counters ([n_tiles][Hp]), dpk's per-KV-head partials
+// (fp32 [entries][Hkv][128][dp]) and their counters ([entries]).
 static size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 size_t bwd_scratch_bytes(const msa_plan_s* p) {
@@ -229,7 +222,9 @@ size_t bwd_scratch_bytes(const msa_plan_s* p) {
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
   return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hp) + al256(2 * tq * p->hp * kDP) + al256(4 * tq * p->hp) +
          al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk)) +
-         al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
+         al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages)) +
+         al256(4 * static_cast<size_t>(p->n_tiles) * p->hq * 128 * kDP) + al256(4 * static_cast<size_t>(p->n_tiles) * p->hp) +
+         al256(4 * ent * 128 * kDP) + al256(4 * static_cast<size_t>(p->n_page_entries));
 }
 
 msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
@@ -260,18 +255,30 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   int32_t* list = cur + ent;
   sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk));
   int32_t* owner = reinterpret_cast<int32_t*>(sp);                    // [num_pages]
+  sp += al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
+  float* dpq_part = reinterpret_cast<float*>(sp);                     // [n_tiles][hq][128][dp]
+  sp += al256(4 * static_cast<size_t>(p->n_tiles) * p->hq * 128 * kDP);
+  int32_t* dpq_cnt = reinterpret_cast<int32_t*>(sp);                  // [n_tiles][hp]
+  sp += al256(4 * static_cast<size_t>(p->n_tiles) * p->hp);
+  float* dpk_part = reinterpret_cast<float*>(sp);                     // [entries][hkv][128][dp]
+  sp += al256(4 * ent * 128 * kDP);
+  int32_t* dpk_cnt = reinterpret_cast<int32_t*>(sp);                  // [entries]
   const auto* O = static_cast<const __nv_bfloat16*>(out);
   const auto* dO = static_cast<const __nv_bfloat16*>(dout);
   const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hp * p->topk;
   const int kv_div = p->hp / p->hkv;
 
-  bwd_zero_dpk_kernel<<<n_ent, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, dpk);
   msa_status s = launch_proxy_softmax(p, pq, pk_pages, kv_indices, idx, op, lse_p, st);
   if (s != MSA_OK) return s;
   bwd_prep_kernel<<<p->n_tiles * p->hp, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
                                                           dpq, p->hq, p->hp, static_cast<int32_t>(p->total_q),
                                                           kl_weight);
   s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
+  if (s == MSA_OK)
+    s = cuda_check(cudaMemsetAsync(dpq_cnt, 0, 4 * static_cast<size_t>(p->n_tiles) * p->hp, st),
+                   "msa_sparse_attn_bwd: memset");
+  if (s == MSA_OK)
+    s = cuda_check(cudaMemsetAsync(dpk_cnt, 0, 4 * static_cast<size_t>(n_ent), st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)  // 0x7F7F7F7F: above every entry index
     s = cuda_check(cudaMemsetAsync(owner, 0x7F, sizeof(int32_t) * static_cast<size_t>(p->num_pages), st),
                    "msa_sparse_attn_bwd: memset");
@@ -285,10 +292,11 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                                               owner, p->num_pages, cur, list);
   s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
   if (s != MSA_OK) return s;
-  s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
+  s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, dpq_part,
+                       dpq_cnt, kl_weight, st);
   if (s != MSA_OK) return s;
   return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, idx, owner, off, list, lse2t,
-                           dsumt, lsept, dk, dv, dpk, kl_weight, st);
+                           dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, kl_weight, st);
 }
 
 }  // namespace msa

@@ -61,7 +61,8 @@ struct DkvSmem {
   static constexpr int kLsepOff = kRowOff + kQStages * 128 * 4;
   static constexpr int kListOff = kLsepOff + kPqStages * 64 * 4;
   static constexpr int kBarOff = kListOff + kMaxList * 4;
-  static constexpr int kBytes = kBarOff + 8 * 26;
+  static constexpr int kFlagOff = kBarOff + 8 * 26;  // the dpk reduction's "last" flag
+  static constexpr int kBytes = kFlagOff + 16;
 };
 
 __device__ __forceinline__ uint32_t ts_col(uint32_t base, int kk) {
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const int32_t* __restrict__ inv_list, int32_t topk,
                       const int32_t* __restrict__ kv_indices, int64_t num_pages, const float* __restrict__ lse2t,
                       const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
-                      float* __restrict__ dv, float* __restrict__ dpk, int32_t hq, int32_t hkv, int32_t hsel,
+                      float* __restrict__ dv, float* __restrict__ dpk, float* __restrict__ dpk_part,
+                      int32_t* __restrict__ dpk_cnt, int32_t hq, int32_t hkv, int32_t hsel,
                       int32_t total_q,
                       float kl_weight, uint32_t* err) {
   using L = DkvSmem;
@@ -92,14 +94,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
   const int64_t kv_off = (page * hkv + g) * 128 * kD;
 
-  if (n == 0) {  // never cached: dK = dV = 0, nothing to add to dpk
+  // dpk of the page: each of its hkv CTAs leaves a partial, and the last of
+  // them to count itself adds the partials in KV-head order (the same sum on
+  // every run).  Threads [0, nthr) of the CTA take part.
+  float* const part_e = dpk_part + (static_cast<int64_t>(e) * hkv + g) * 128 * kDP;
+  auto finish_dpk = [&](int tid, int nthr, int bar_id) {
+    __threadfence();
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthr) : "memory");
+    int32_t* const flag = reinterpret_cast<int32_t*>(smem + DkvSmem::kFlagOff);
+    if (tid == 0) {
+      int32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(dpk_cnt + e) : "memory");
+      *flag = prev == hkv - 1;
+    }
+    asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthr) : "memory");
+    if (!*flag) return;
+    float4* dst = reinterpret_cast<float4*>(dpk + page * 128 * kDP);
+    const float4* src0 = reinterpret_cast<const float4*>(dpk_part + static_cast<int64_t>(e) * hkv * 128 * kDP);
+    for (int i = tid; i < 128 * kDP / 4; i += nthr) {
+      float4 acc = __ldcg(src0 + i);
+      for (int gg = 1; gg < hkv; ++gg) {
+        const float4 v = __ldcg(src0 + static_cast<int64_t>(gg) * 128 * kDP / 4 + i);
+        acc.x += v.x;
+        acc.y += v.y;
+        acc.z += v.z;
+        acc.w += v.w;
+      }
+      dst[i] = acc;
+    }
+  };
+
+  if (n == 0) {  // never cached: dK = dV = 0 and a zero dpk partial
     if (!page_ok) return;
     float4* a = reinterpret_cast<float4*>(dk + kv_off);
     float4* b = reinterpret_cast<float4*>(dv + kv_off);
+    float4* c = reinterpret_cast<float4*>(part_e);
     for (int i = threadIdx.x; i < 128 * kD / 4; i += blockDim.x) {
       a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       b[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
+    for (int i = threadIdx.x; i < 128 * kDP / 4; i += blockDim.x) c[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    finish_dpk(threadIdx.x, kThreads, 2);
     return;
   }
 
@@ -480,8 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // epilogue: dV and dK rows are owned (plain stores), dpk is shared by the
-    // groups (fp32 atomics)
+    // epilogue: dV and dK rows are owned (plain stores); this KV head's dpk
+    // partial goes to the scratch for the page's reduction
     if (ok) ok = mbar_wait(done, 0, err);
     tc_fence_after();
     ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
@@ -509,10 +544,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t a[32];
       tmem_ld32(lane_base + kColDPK + wg * 32, a);
       tmem_wait_ld();
-      float* dpkr = dpk + (page * 128 + key) * kDP + wg * 32;
+      float4* pr = reinterpret_cast<float4*>(part_e + key * kDP + wg * 32);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) atomicAdd(dpkr + i, __uint_as_float(a[i]) * f_main);
+      for (int i = 0; i < 8; ++i)
+        pr[i] = make_float4(__uint_as_float(a[4 * i]) * f_main, __uint_as_float(a[4 * i + 1]) * f_main,
+                            __uint_as_float(a[4 * i + 2]) * f_main, __uint_as_float(a[4 * i + 3]) * f_main);
     }
+    if (page_ok) finish_dpk(threadIdx.x, 32 * kSoftWarps, 1);  // the softmax warps: threads 0-255
   }
   tc_fence_before();
   __syncthreads();
@@ -527,7 +565,7 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
                              const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
                              const int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
-                             float* dpk, float kl_weight, cudaStream_t st) {
+                             float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st) {
   CUtensorMap qm, dom, pqm, km, vm, pkm;
   const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
                              static_cast<uint64_t>(p->total_q)};
@@ -552,8 +590,8 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
       qm, dom, pqm, km, vm, pkm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
-      dsumt, lsept,
-      dk, dv, dpk, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+      dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), kl_weight,
+      p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
 }
 

@@ -13,10 +13,11 @@
 // the MMA thread issues S of block j+1 right after dpq of block j and dP of
 // j+1 right after dQ of j, so the tensor pipe has work while the softmax
 // runs (its two warpgroups split the 128 keys).
-// At the end dQ / sqrt(d) is stored and dpq * (-w / (G sqrt(dp))) is added
-// with fp32 atomics: the G = Hq/Hp heads that use one proxy head's blocks
-// add into that proxy head's dpq row, whose
-// proxy term the prep kernel stored first.
+// At the end dQ / sqrt(d) is stored, and dpq * (-w / (G sqrt(dp))) goes to
+// this head's slot of a scratch array; the G = Hq/Hp heads that use one
+// proxy head's blocks each count themselves on a per-(tile, proxy head)
+// counter, and the last to do so adds the G partials, in head order, to the
+// proxy term the prep kernel stored first: the sum is the same on every run.
 //
 // Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 | Q 64 columns.  Warpgroup
 // w owns keys 64w..64w+63 and writes its bf16 pairs into the first 32 of
@@ -45,7 +46,8 @@ struct DqSmem {
   static constexpr int kRingOff = kDOOff + 32768;     // stage: K 32 KB | V 32 KB | pk 16 KB
   static constexpr int kStageBytes = 81920;
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kBytes = kBarOff + 8 * 14;
+  static constexpr int kFlagOff = kBarOff + 8 * 14;  // the dpq reduction's "last" flag
+  static constexpr int kBytes = kFlagOff + 16;
 };
 
 __device__ __forceinline__ bool valid_block(int j, int nvp) { return j >= 0 && j < nvp; }
@@ -56,8 +58,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap pk_map, const TileInfo* __restrict__ tiles,
                      const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                      const float* __restrict__ lse2t, const float* __restrict__ dsumt, float* __restrict__ dq,
-                     float* __restrict__ dpq, int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q,
-                     float kl_weight, uint32_t* err) {
+                     float* __restrict__ dpq, float* __restrict__ dpq_part, int32_t* __restrict__ dpq_cnt,
+                     int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q, float kl_weight,
+                     uint32_t* err) {
   using L = DqSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -330,16 +333,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_float4(__uint_as_float(a[4 * i]) * qs, __uint_as_float(a[4 * i + 1]) * qs,
                             __uint_as_float(a[4 * i + 2]) * qs, __uint_as_float(a[4 * i + 3]) * qs);
       }
-      if (it > 0) {
-        const float f = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
-        uint32_t a[32];
+    }
+    // this head's dpq partial (every row of the tile's slot, zeros without
+    // blocks), then the count; the last head of the proxy head sums
+    {
+      const float f = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
+      uint32_t a[32];
+      if (ok && it > 0) {
         tmem_ld32(lane_base + kColDPQ + wg * 32, a);
         tmem_wait_ld();
-        float* dpr = dpq + (q_row * hsel + ps) * kDP + wg * 32;
-        if (row_ok)
+      } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) atomicAdd(dpr + i, __uint_as_float(a[i]) * f);
+        for (int i = 0; i < 32; ++i) a[i] = 0u;
       }
+      float4* part = reinterpret_cast<float4*>(dpq_part + ((static_cast<int64_t>(t) * hq + h) * 128 + r) * kDP + wg * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        part[i] = make_float4(__uint_as_float(a[4 * i]) * f, __uint_as_float(a[4 * i + 1]) * f,
+                              __uint_as_float(a[4 * i + 2]) * f, __uint_as_float(a[4 * i + 3]) * f);
+    }
+    // every thread's partial is ordered before thread 0's release; its
+    // acquire (in the last head's CTA) orders the sum's reads after every
+    // head's release
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
+    int32_t* const flag = reinterpret_cast<int32_t*>(smem + L::kFlagOff);
+    if (threadIdx.x == 0) {
+      int32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                   : "=r"(prev)
+                   : "l"(dpq_cnt + static_cast<int64_t>(t) * hsel + ps)
+                   : "memory");
+      *flag = prev == G - 1;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
+    if (*flag && row_ok) {
+      const int64_t q_row = tl.q_begin + r;
+      float4* dpr = reinterpret_cast<float4*>(dpq + (q_row * hsel + ps) * kDP + wg * 32);
+      float4 acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = __ldcg(dpr + i);
+      for (int hh = 0; hh < G; ++hh) {
+        const float4* src = reinterpret_cast<const float4*>(
+            dpq_part + ((static_cast<int64_t>(t) * hq + ps * G + hh) * 128 + r) * kDP + wg * 32);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 v = __ldcg(src + i);
+          acc[i].x += v.x;
+          acc[i].y += v.y;
+          acc[i].z += v.z;
+          acc[i].w += v.w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dpr[i] = acc[i];
     }
   }
   tc_fence_before();
@@ -352,8 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
-                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
-                            cudaStream_t st) {
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float* dpq_part,
+                            int32_t* dpq_cnt, float kl_weight, cudaStream_t st) {
   CUtensorMap qm, dom, km, vm, pkm;
   const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
                              static_cast<uint64_t>(p->total_q)};
@@ -373,8 +420,8 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
   const int smem = DqSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dq_tc_kernel<<<p->n_tiles * p->hq, kThreads, smem, st>>>(
-      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, p->hq, p->hkv, p->hp, p->topk,
-      static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, dpq_part, dpq_cnt, p->hq,
+      p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
 }
 

@@ -32,7 +32,7 @@ struct TileInfo {
 static_assert(sizeof(TileInfo) == 32, "TileInfo is uploaded as raw bytes");
 
 // Bits of the device error word.
-enum : uint32_t { kErrDeviceCheck = 1u, kErrTimeout = 2u };
+enum : uint32_t { kErrDeviceCheck = 1u, kErrTimeout = 2u, kErrNonFinite = 4u };
 
 #ifdef __CUDACC__
 // Order-preserving 32-bit key of a block score for the top-k selection:
@@ -57,6 +57,7 @@ struct msa_plan_s {
   int32_t n_tiles = 0, max_blocks = 0;
   int64_t total_q = 0;
   bool decode = false;               // every qo_len == 1
+  bool checks = false;               // MSA_CHECKS set at plan creation: scan outputs for NaN
   std::vector<int32_t> qo_lens, kv_lens;
   std::vector<msa::TileInfo> tiles;  // host copy
   // device memory owned by the plan (one allocation, carved up)
@@ -119,19 +120,22 @@ size_t fused_topk_counter_bytes(const msa_plan_s* p);  // leading part that star
 // (bf16 [total_q, Hp, 64]) and its natural-log LSE ([total_q, Hp]).
 msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                                 const int32_t* idx, void* op, float* lse, cudaStream_t st);
-// dQ and dpq's main term on the tensor cores (bwd_dq.cu).
+// dQ and dpq's main term on the tensor cores (bwd_dq.cu); dpq_part is
+// [n_tiles][hq][128][64] fp32 scratch, dpq_cnt [n_tiles][hp] int32 zeroed.
 msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
-                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
-                            cudaStream_t st);
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float* dpq_part,
+                            int32_t* dpq_cnt, float kl_weight, cudaStream_t st);
 // dK, dV and dpk on the tensor cores (bwd_dkv.cu); lse2t, dsumt, lsept are
-// the row statistics written by the prep kernel, [heads][total_q].
+// the row statistics written by the prep kernel, [heads][total_q]; dpk_part
+// is [page-table entries][hkv][128][64] fp32 scratch, dpk_cnt [entries]
+// int32 zeroed.
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                              const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                              const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
                              const int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
-                             float* dpk, float kl_weight, cudaStream_t st);
+                             float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st);
 
 // ---- launchers (each returns MSA_OK or an error with its message set) ----
 msa_status launch_topk(const float* max_score, int32_t n_tiles, int32_t heads, int32_t max_blocks,

@@ -27,7 +27,8 @@ _u32 = ctypes.c_uint32
 _f32 = ctypes.c_float
 
 STATUS = {0: "MSA_OK", 1: "MSA_ERR_INVALID_ARG", 2: "MSA_ERR_UNSUPPORTED", 3: "MSA_ERR_CUDA",
-          4: "MSA_ERR_NO_MEMORY", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE_CHECK"}
+          4: "MSA_ERR_NO_MEMORY", 5: "MSA_ERR_TIMEOUT", 6: "MSA_ERR_DEVICE_CHECK",
+          7: "MSA_ERR_NONFINITE"}
 KV_BF16, KV_FP8_E4M3 = 0, 1
 
 # Every symbol include/msa.h declares, with its ctypes signature.

@@ -46,6 +46,16 @@
  *    MSA_ERR_UNSUPPORTED before anything is enqueued; a failed launch
  *    returns MSA_ERR_CUDA.  msa_last_error() gives a message for the
  *    calling thread's last failure.
+ *  - NaN inputs are outside the contract and are not scanned for.  A plan
+ *    created while the environment variable MSA_CHECKS is set (to anything
+ *    but "0") adds, after each of its calls, scans of that call's
+ *    floating-point inputs (the query-side arrays q, pq, dout, and the pages
+ *    of k/v/pk that kv_indices names; bf16 or e4m3, not the NVFP4 codes) and
+ *    outputs (max_score, out, lse, dq, dpq; not dk/dv/dpk, whose unreferenced
+ *    pages keep the caller's contents), and raises MSA_ERR_NONFINITE in the
+ *    error word when one holds a NaN.  -inf in max_score and lse is a
+ *    defined value (no visible key) and is not flagged.  Each scan is one
+ *    read of its array.
  */
 #ifndef MSA_H
 #define MSA_H
@@ -66,7 +76,8 @@ typedef enum {
   MSA_ERR_CUDA = 3,          /* CUDA runtime / launch failure */
   MSA_ERR_NO_MEMORY = 4,     /* plan workspace allocation failed */
   MSA_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up */
-  MSA_ERR_DEVICE_CHECK = 6   /* a device-side bounds check fired (bad page id) */
+  MSA_ERR_DEVICE_CHECK = 6,  /* a device-side bounds check fired (bad page id) */
+  MSA_ERR_NONFINITE = 7      /* MSA_CHECKS: a NaN reached an output */
 } msa_status;
 
 typedef enum {
@@ -359,9 +370,11 @@ msa_status msa_sparse_decode_noalloc(const void* q, const void* k_pages, const v
 
 /*
  * msa_check_errors -- waits for `stream`, then reads and clears the plan's
- * device error word: MSA_OK, MSA_ERR_DEVICE_CHECK (a kernel skipped a block
- * whose page id was out of range) or MSA_ERR_TIMEOUT (a bounded wait inside
- * a kernel gave up; that kernel's outputs are unspecified).
+ * device error word: MSA_OK, MSA_ERR_TIMEOUT (a bounded wait inside a kernel
+ * gave up; that kernel's outputs are unspecified), MSA_ERR_DEVICE_CHECK (a
+ * kernel skipped a block whose page id was out of range) or, for plans
+ * created under MSA_CHECKS, MSA_ERR_NONFINITE (an output held a NaN), in
+ * that order when several are set.
  */
 msa_status msa_check_errors(msa_plan_t plan, msa_stream_t stream);
 

@@ -117,6 +117,34 @@ def test_bwd_shared_pages(cuda_dev):
     _check_all(got, ref)
 
 
+def test_bwd_bitwise_reproducible(cuda_dev):
+    """No gradient is reduced by atomics: repeated backward calls give the same
+    bits for all five gradients, with four query heads per proxy head (the dpq
+    sum over heads), several KV heads (the dpk sum over them), shared pages and
+    ragged tiles."""
+    case = synth.Case("repro", [700, 300, 129], [900, 600, 384], 16, 4, 128, 4, 64, 4,
+                      page_perm_seed=12, extra_pages=1)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    table = inp["kv_indices"].clone()
+    table[8] = table[0]  # seq 1 block 0 = seq 0 block 0
+    inp["kv_indices"] = table
+    idx_t = torch.from_numpy(random_idx(case, np.random.default_rng(21))).to(cuda_dev)
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t)
+    runs = []
+    for _ in range(3):
+        g = plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t, out, lse,
+                                 inp["dout"], inp["pq"], inp["pk_pages"], kl_weight=0.7)
+        torch.cuda.synchronize()
+        plan.check_errors()
+        runs.append({k: v.clone() for k, v in g.items()})
+    for name in ("dq", "dpq", "dk", "dv", "dpk"):
+        for r in runs[1:]:
+            assert torch.equal(runs[0][name], r[name]), "%s differs between runs" % name
+    ref = _oracle(case, inp, idx_t.cpu().numpy(), 0.7)
+    _check_all({k: v.cpu().numpy() for k, v in runs[0].items()}, ref)
+
+
 def test_bwd_unsupported_head_dim(cuda_dev):
     from block_sparse_long_proxy_gb300 import msa
     case = synth.Case("d64", [256], [256], 4, 2, 64, 2, 32, 2)

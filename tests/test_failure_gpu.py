@@ -52,3 +52,45 @@ def test_plan_allocation_failure_is_reported(cuda_dev):
     ms = torch.from_numpy(rng.standard_normal((plan.n_tiles, 2, plan.max_blocks)).astype(np.float32)).to(cuda_dev)
     got = msa.topk_select(ms, 2, plan.num_valid_pages).cpu().numpy()
     assert np.array_equal(got, O.topk_select(ms.cpu().numpy(), 2, O.num_valid_pages([256], [256])))
+
+
+def test_checks_mode_flags_nan_outputs(cuda_dev, monkeypatch):
+    """MSA_CHECKS: a plan created with it set scans each call's inputs and
+    outputs; a NaN planted in pq (which the block maxima would not carry: a
+    max drops NaN operands) and one planted in q both come back as
+    MSA_ERR_NONFINITE.  Clean inputs, and the same NaN under a plan made
+    without the variable, raise nothing."""
+    from block_sparse_long_proxy_gb300 import msa, synth
+    from tests.gpu_cases import make_plan
+    MSA_ERR_NONFINITE = 7
+    case = synth.Case("checks", [300], [300], 4, 2, 128, 2, 64, 2)
+    inp = synth.make_inputs(case, device=cuda_dev)
+    monkeypatch.setenv("MSA_CHECKS", "1")
+    plan = make_plan(case, inp)
+    monkeypatch.delenv("MSA_CHECKS")
+    plain = make_plan(case, inp)
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    plan.check_errors()  # clean inputs: nothing to report
+    bad_pq = inp["pq"].clone()
+    bad_pq[5, 1, 3] = float("nan")
+    plan.proxy_maxscore(bad_pq, inp["pk_pages"], inp["kv_indices"])
+    with pytest.raises(msa.MsaError) as e:
+        plan.check_errors()
+    assert e.value.status == MSA_ERR_NONFINITE
+    plain.proxy_maxscore(bad_pq, inp["pk_pages"], inp["kv_indices"])
+    plain.check_errors()  # no scan without MSA_CHECKS
+    bad_q = inp["q"].clone()
+    bad_q[7, 2, 11] = float("nan")
+    plan.sparse_attn(bad_q, inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    with pytest.raises(msa.MsaError) as e:
+        plan.check_errors()
+    assert e.value.status == MSA_ERR_NONFINITE
+    plan.check_errors()  # the word was cleared by the read
+    bad_k = inp["k_pages"].clone()
+    bad_k[int(inp["kv_indices"][1]), 1, 17, 5] = float("nan")  # a referenced page
+    plan.sparse_attn(inp["q"], bad_k, inp["v_pages"], inp["kv_indices"], idx)
+    with pytest.raises(msa.MsaError) as e:
+        plan.check_errors()
+    assert e.value.status == MSA_ERR_NONFINITE

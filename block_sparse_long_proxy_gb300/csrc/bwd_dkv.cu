@@ -30,9 +30,13 @@
 // Each warpgroup owns 32 of the 64 rows, and each writes its packed pairs
 // into the first half of its own 32 columns, so a k-step of 16 rows of an
 // A operand in TMEM starts at column (kk / 2) * 32 + (kk % 2) * 8.
+// dV and dpk sit side by side in tensor memory and share their A operand
+// P^T, and each stage holds pq right after dO's two chunks, so one N = 192
+// product P^T . [dO | pq] adds to both (an N = 64 product takes as long as
+// an N = 128 one).
 // Roles: warps 0-7 softmax (warp w reads TMEM lanes 32 (w % 4) ...), warp 8
-// TMA producer (K, V, pk once; then rings of Q/dO halves and pq halves,
-// with their per-row lse2 / D / lsep staged by the same warp), warp 9 MMA.
+// TMA producer (K, V, pk once; then a ring of Q/dO/pq halves, with their
+// per-row lse2 / D / lsep staged by the same warp), warp 9 MMA.
 #include "msa_internal.h"
 #include "ptx.cuh"
 
@@ -42,7 +46,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kDP = 64;
 constexpr int kQStages = 3;
-constexpr int kPqStages = 2;
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
 constexpr int kMaxList = 2048;
@@ -54,12 +57,12 @@ struct DkvSmem {
   static constexpr int kKOff = 0;                               // K block: 2 x [128 keys][128 B]
   static constexpr int kVOff = kKOff + 32768;                   // V block
   static constexpr int kPkOff = kVOff + 32768;                  // pk block: [128 keys][128 B]
-  static constexpr int kQdOff = kPkOff + 16384;                 // ring: Q half 2 x [64][128 B] | dO half
-  static constexpr int kQdBytes = 32768;
-  static constexpr int kPqOff = kQdOff + kQStages * kQdBytes;   // ring: pq half [64 rows][128 B]
-  static constexpr int kRowOff = kPqOff + kPqStages * 8192;     // Q stage s: lse2[64], D[64]; pq stage: lsep[64]
-  static constexpr int kLsepOff = kRowOff + kQStages * 128 * 4;
-  static constexpr int kListOff = kLsepOff + kPqStages * 64 * 4;
+  // ring: Q half 2 x [64][128 B] | dO half 2 x [64][128 B] | pq half [64][128 B]:
+  // dO's two chunks and pq sit 8 KB apart, one rows-major operand of N = 192
+  static constexpr int kQdOff = kPkOff + 16384;
+  static constexpr int kQdBytes = 40960;
+  static constexpr int kRowOff = kQdOff + kQStages * kQdBytes;  // stage s: lse2[64], D[64], lsep[64]
+  static constexpr int kListOff = kRowOff + kQStages * 192 * 4;
   static constexpr int kBarOff = kListOff + kMaxList * 4;
   static constexpr int kFlagOff = kBarOff + 8 * 26;  // the dpk reduction's "last" flag
   static constexpr int kBytes = kFlagOff + 16;
@@ -142,18 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* v_s = smem + L::kVOff;
   uint8_t* pk_s = smem + L::kPkOff;
   uint8_t* qd_s = smem + L::kQdOff;
-  uint8_t* pq_s = smem + L::kPqOff;
   float* row_s = reinterpret_cast<float*>(smem + L::kRowOff);
-  float* lsep_s = reinterpret_cast<float*>(smem + L::kLsepOff);
   int32_t* list = reinterpret_cast<int32_t*>(smem + L::kListOff);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* kv_full = bars;
   uint64_t* init_done = bars + 1;  // accumulators zeroed, K in tensor memory
   uint64_t* qd_full = bars + 2;                 // [kQStages]
   uint64_t* qd_empty = qd_full + kQStages;      // [kQStages]
-  uint64_t* pq_full = qd_empty + kQStages;      // [kPqStages]
-  uint64_t* pq_empty = pq_full + kPqStages;     // [kPqStages]
-  uint64_t* sp_full = pq_empty + kPqStages;
+  uint64_t* sp_full = qd_empty + kQStages;
   uint64_t* pp_full = sp_full + 1;
   uint64_t* s_full = pp_full + 1;    // S^T computed
   uint64_t* dp_full = s_full + 1;    // dP^T computed
@@ -175,10 +174,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kQStages; ++s) {
       mbar_init(qd_full + s, 2);  // expect_tx arrival + the staged lse2 / D
       mbar_init(qd_empty + s, 1);
-    }
-    for (int s = 0; s < kPqStages; ++s) {
-      mbar_init(pq_full + s, 2);
-      mbar_init(pq_empty + s, 1);
     }
     mbar_init(sp_full, 1);
     mbar_init(pp_full, kSoftWarps);
@@ -236,26 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tma_load_2d(pk_s, &pk_map, kv_full, 0, static_cast<int>(page * 128));
     }
-    int qi = 0, pi = 0;
+    int qi = 0;
     for (int it = 0; ok && it < n; ++it) {
       const int sel = sel_at(it);
       const TileInfo tl = tiles[sel / sel_per_tile];
       const int pp = (sel / topk) % hsel;  // the selecting proxy head
       const int halves = tl.rows > 64 ? 2 : 1;
-      for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
+      for (int hf = 0; ok && hf < halves; ++hf) {
         const int r0 = tl.q_begin + hf * 64;
-        const int ps = pi % kPqStages;
-        if (!(ok = mbar_wait(pq_empty + ps, ((pi / kPqStages) & 1) ^ 1, err))) break;
-        if (lane == 0) {
-          mbar_expect_tx(pq_full + ps, 8192);
-          tma_load_3d(pq_s + ps * 8192, &pq_map, pq_full + ps, 0, pp, r0);
-        }
-        for (int rr = lane; rr < 64; rr += 32) {
-          const int r = hf * 64 + rr;
-          lsep_s[ps * 64 + rr] = r < tl.rows ? -lsept[static_cast<int64_t>(pp) * total_q + tl.q_begin + r] : 0.f;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(pq_full + ps);
         for (int hh = 0; hh < G; ++hh, ++qi) {
           const int h = pp * G + hh;
           const int s = qi % kQStages;
@@ -267,13 +250,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(st + c * 8192, &q_map, qd_full + s, c * 64, h, r0);
               tma_load_3d(st + 16384 + c * 8192, &do_map, qd_full + s, c * 64, h, r0);
             }
+            tma_load_3d(st + 32768, &pq_map, qd_full + s, 0, pp, r0);
           }
           for (int rr = lane; rr < 64; rr += 32) {
             const int r = hf * 64 + rr;
             const bool rok = r < tl.rows;
             const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
-            row_s[s * 128 + rr] = rok ? -lse2t[ei] : 0.f;  // negated: the softmax adds them
-            row_s[s * 128 + 64 + rr] = rok ? -dsumt[ei] : 0.f;
+            row_s[s * 192 + rr] = rok ? -lse2t[ei] : 0.f;  // negated: the softmax adds them
+            row_s[s * 192 + 64 + rr] = rok ? -dsumt[ei] : 0.f;
+            row_s[s * 192 + 128 + rr] = rok ? -lsept[static_cast<int64_t>(pp) * total_q + tl.q_begin + r] : 0.f;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(qd_full + s);
@@ -285,7 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 64, false, false);   // S^T, dP^T, Sp^T
       constexpr uint32_t id_d = idesc_bf16_f32(128, 128, false, true);   // dV, dK (B rows-major)
-      constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpk
+      constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpk (proxy term)
+      constexpr uint32_t id_vp = idesc_bf16_f32(128, 192, false, true);  // [dV | dpk] += P^T [dO | pq]
       // descriptors precomputed (one add per MMA): the issuing thread runs
       // only a step ahead of the tensor pipe
       constexpr uint64_t kQdDesc = L::kQdBytes >> 4;
@@ -295,15 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_km = smem_desc(smem_u32(qd_s) + 16384, 16, 1024, kSwizzle128); // dO half (dP^T = V dO^T)
       const uint64_t q_mn = smem_desc(smem_u32(qd_s), 8192, 1024, kSwizzle128);       // Q as rows-major B (dK)
       const uint64_t do_mn = smem_desc(smem_u32(qd_s) + 16384, 8192, 1024, kSwizzle128);
-      const uint64_t pq_km = smem_desc(smem_u32(pq_s), 16, 1024, kSwizzle128);
-      const uint64_t pq_mn = smem_desc(smem_u32(pq_s), 8192, 1024, kSwizzle128);
+      const uint64_t pq_km = smem_desc(smem_u32(qd_s) + 32768, 16, 1024, kSwizzle128);
+      const uint64_t pq_mn = smem_desc(smem_u32(qd_s) + 32768, 8192, 1024, kSwizzle128);
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(init_done, 0, err);
       tc_fence_after();
-      // Sp^T = pk . pq^T of half p, in the S^T columns
-      auto sp = [&](int p) -> bool {
-        const int ps = p % kPqStages;
-        const uint64_t po = static_cast<uint64_t>(ps) * (8192 >> 4);
-        if (!mbar_wait(pq_full + ps, (p / kPqStages) & 1, err)) return false;
+      // Sp^T = pk . pq^T of the half whose first head sits in stage qa, in
+      // the S^T columns
+      auto sp = [&](int qa) -> bool {
+        const uint64_t po = static_cast<uint64_t>(qa % kQStages) * kQdDesc;
+        if (!mbar_wait(qd_full + qa % kQStages, (qa / kQStages) & 1, err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
@@ -316,10 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileInfo tl = tiles[sel_at(it) / sel_per_tile];
         const int halves = tl.rows > 64 ? 2 : 1;
         for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
-          const int ps = pi % kPqStages;
-          const uint64_t po = static_cast<uint64_t>(ps) * (8192 >> 4);
+          const uint64_t po = static_cast<uint64_t>(qi % kQStages) * kQdDesc;  // the half's pq: its first head's stage
           const bool more_halves = hf + 1 < halves || it + 1 < n;
-          if (!sp_issued && !(ok = sp(pi))) break;
+          if (!sp_issued && !(ok = sp(qi))) break;
           sp_issued = false;
           auto dpt = [&](uint64_t so) {  // dP^T = V . dO^T
 #pragma unroll
@@ -360,10 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait(p_full, qi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), do_mn + so + kk * 128, id_d, 1);
-              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
-            }
+            for (int kk = 0; kk < 4; ++kk)  // dV and dpk (side by side in TMEM) in one product
+              mma_ts(tmem + kColDV, ts_col(tmem + kColS, kk), do_mn + so + kk * 128, id_vp, 1);
             const bool next = hh + 1 < G;
             const int s1 = (qi + 1) % kQStages;
             const uint64_t so1 = static_cast<uint64_t>(s1) * kQdDesc;
@@ -372,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_fence_after();
               st(so1);
             } else if (more_halves) {  // the next half's proxy scores, so its proxy softmax follows dS^T at once
-              if (!(ok = sp(pi + 1))) break;
+              if (!(ok = sp(qi + 1))) break;
               sp_issued = true;
             }
             if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
@@ -384,7 +367,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (next) dpt(so1);
           }
           if (!ok) break;
-          mma_commit(pq_empty + ps);
         }
       }
       mma_commit(done);
@@ -431,19 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kpos = j * 128 + key;
       const int halves = tl.rows > 64 ? 2 : 1;
       for (int hf = 0; ok && hf < halves; ++hf, ++pi) {
-        const int ps = pi % kPqStages;
+        const int s0 = qi % kQStages;  // the half's first head's stage: its pq and proxy LSE
         const int rbase = hf * 64 + c0;  // tile row of column 0 of this warpgroup
         // every key of the block visible to all 32 rows: no per-element mask
         const bool need_mask = j * 128 + 127 > tl.pos0 + rbase || rbase + 32 > tl.rows;
         // proxy probabilities over this block's keys, scaled by -G
-        if (!(ok = mbar_wait(pq_full + ps, (pi / kPqStages) & 1, err))) break;
+        if (!(ok = mbar_wait(qd_full + s0, (qi / kQStages) & 1, err))) break;
         if (!(ok = mbar_wait(sp_full, pi & 1, err))) break;
         tc_fence_after();
         {
           uint32_t sv[32], pk[16];
           tmem_ld32(lane_base + kColS + c0, sv);
           tmem_wait_ld();
-          const float2* nlp = reinterpret_cast<const float2*>(lsep_s + ps * 64 + c0);
+          const float2* nlp = reinterpret_cast<const float2*>(row_s + s0 * 192 + 128 + c0);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 nl = nlp[c >> 1];
@@ -473,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float pr[32];
           tmem_ld32(lane_base + kColS + c0, sv);
           tmem_wait_ld();
-          const float2* nl2 = reinterpret_cast<const float2*>(row_s + s * 128 + c0);
-          const float2* ndd = reinterpret_cast<const float2*>(row_s + s * 128 + 64 + c0);
+          const float2* nl2 = reinterpret_cast<const float2*>(row_s + s * 192 + c0);
+          const float2* ndd = reinterpret_cast<const float2*>(row_s + s * 192 + 64 + c0);
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 nl = nl2[c >> 1];

@@ -4,7 +4,7 @@
 //
 // One CTA per (query tile t, head h of group g).  Q_h is copied into tensor
 // memory once, dO_h stays in shared memory, and the tile's cached blocks
-// stream through a 2-stage TMA ring (K, V and pk of each block).  Per block j:
+// stream through TMA rings (K three stages, V and pk two).  Per block j:
 //   S  = Q_h . K_j^T (Q from TMEM)   dP = dO_h . V_j^T        (M = rows, N = 128 keys)
 //   P  = exp2(S sl2 - lse2) (masked)   dS = P * (dP - D)
 //   dQ += dS . K_j       dpq += P . pk_j                     (dS, P from TMEM)
@@ -33,7 +33,12 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kDP = 64;
-constexpr int kStages = 2;
+// K, V and pk of a block stream through rings of their own: V is read by
+// dP and pk by dpq early in a block's turn, K last (by dQ), so K's ring is
+// one deeper (its third stage is Q's shared memory, free once Q is in
+// tensor memory)
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
 constexpr float kLog2e = 1.4426950408889634f;
@@ -41,12 +46,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDPQ = 384, kColQ = 448;
 
 struct DqSmem {
-  static constexpr int kQOff = 0;                     // Q_h: 2 x [128 rows][128 B]
-  static constexpr int kDOOff = kQOff + 32768;        // dO_h
-  static constexpr int kRingOff = kDOOff + 32768;     // stage: K 32 KB | V 32 KB | pk 16 KB
-  static constexpr int kStageBytes = 81920;
-  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kFlagOff = kBarOff + 8 * 14;  // the dpq reduction's "last" flag
+  static constexpr int kDOOff = 0;                                  // dO_h: 2 x [128 rows][128 B]
+  static constexpr int kKOff = 32768;                               // K ring: kKStages x 32 KB
+  static constexpr int kQOff = kKOff + 2 * 32768;                   // Q_h, at first, in K's third stage
+  static constexpr int kVOff = kKOff + kKStages * 32768;            // V ring: kVStages x 32 KB
+  static constexpr int kPkOff = kVOff + kVStages * 32768;           // pk ring: kVStages x 16 KB
+  static constexpr int kBarOff = kPkOff + kVStages * 16384;
+  static constexpr int kFlagOff = kBarOff + 8 * 24;  // the dpq reduction's "last" flag
   static constexpr int kBytes = kFlagOff + 16;
 };
 
@@ -72,13 +78,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint8_t* q_s = smem + L::kQOff;
   uint8_t* do_s = smem + L::kDOOff;
-  uint8_t* ring = smem + L::kRingOff;
+  uint8_t* k_s = smem + L::kKOff;
+  uint8_t* v_s = smem + L::kVOff;
+  uint8_t* pk_s = smem + L::kPkOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
-  uint64_t* q_tm = bars + 1;                 // Q copied into tensor memory
-  uint64_t* kv_full = bars + 2;              // [kStages]
-  uint64_t* kv_empty = kv_full + kStages;    // [kStages]
-  uint64_t* s_full = kv_empty + kStages;   // S computed
+  uint64_t* q_tm = bars + 1;                 // Q copied into tensor memory (its shared memory free)
+  uint64_t* k_full = bars + 2;               // [kKStages]
+  uint64_t* k_empty = k_full + kKStages;     // [kKStages]
+  uint64_t* v_full = k_empty + kKStages;     // [kVStages]
+  uint64_t* v_empty = v_full + kVStages;     // [kVStages]
+  uint64_t* pk_full = v_empty + kVStages;    // [kVStages]
+  uint64_t* pk_empty = pk_full + kVStages;   // [kVStages]
+  uint64_t* s_full = pk_empty + kVStages;  // S computed
   uint64_t* p_full = s_full + 1;           // P written (bf16, over S)
   uint64_t* dp_full = p_full + 1;          // dP computed
   uint64_t* ds_full = dp_full + 1;         // dS written (bf16, over dP)
@@ -94,9 +106,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&pk_map);
     mbar_init(q_full, 1);
     mbar_init(q_tm, kSoftWarps);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full + s, 1);
-      mbar_init(kv_empty + s, 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(k_full + s, 1);
+      mbar_init(k_empty + s, 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(v_full + s, 1);
+      mbar_init(v_empty + s, 1);
+      mbar_init(pk_full + s, 1);
+      mbar_init(pk_empty + s, 1);
     }
     mbar_init(s_full, 1);
     mbar_init(p_full, kSoftWarps);
@@ -126,18 +144,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < topk; ++k) {
         const int j = row_idx[k];
         if (!valid_block(j, tl.nvp)) continue;
-        const int s = it % kStages;
-        if (!mbar_wait(kv_empty + s, ((it / kStages) & 1) ^ 1, err)) break;
         int64_t page = kv_indices[tl.page_base + j];
         if (page < 0 || page >= num_pages) page = 0;  // reported by the prep kernel
-        uint8_t* st = ring + s * L::kStageBytes;
         const int row = static_cast<int>((page * hkv + g) * 128);
-        mbar_expect_tx(kv_full + s, L::kStageBytes);
-        for (int c = 0; c < 2; ++c) {
-          tma_load_2d(st + c * 16384, &k_map, kv_full + s, c * 64, row);
-          tma_load_2d(st + 32768 + c * 16384, &v_map, kv_full + s, c * 64, row);
-        }
-        tma_load_2d(st + 65536, &pk_map, kv_full + s, 0, static_cast<int>(page * 128));
+        // K (needed first, by S of the block), then V, then pk
+        const int ks = it % kKStages, vs = it % kVStages;
+        if (!mbar_wait(k_empty + ks, ((it / kKStages) & 1) ^ 1, err)) break;
+        if (it == kKStages - 1 && !mbar_wait(q_tm, 0, err)) break;  // K's third stage held Q
+        mbar_expect_tx(k_full + ks, 32768);
+        for (int c = 0; c < 2; ++c) tma_load_2d(k_s + ks * 32768 + c * 16384, &k_map, k_full + ks, c * 64, row);
+        if (!mbar_wait(v_empty + vs, ((it / kVStages) & 1) ^ 1, err)) break;
+        mbar_expect_tx(v_full + vs, 32768);
+        for (int c = 0; c < 2; ++c) tma_load_2d(v_s + vs * 32768 + c * 16384, &v_map, v_full + vs, c * 64, row);
+        if (!mbar_wait(pk_empty + vs, ((it / kVStages) & 1) ^ 1, err)) break;
+        mbar_expect_tx(pk_full + vs, 16384);
+        tma_load_2d(pk_s + vs * 16384, &pk_map, pk_full + vs, 0, static_cast<int>(page * 128));
         ++it;
       }
     }
@@ -149,69 +170,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_p = idesc_bf16_f32(128, 64, false, true);    // dpq
       // descriptors precomputed (one add per MMA): the issuing thread runs
       // only a step ahead of the tensor pipe
-      constexpr uint64_t kStageDesc = L::kStageBytes >> 4;
-      const uint32_t r0 = smem_u32(ring);
-      const uint64_t k_km = smem_desc(r0, 16, 1024, kSwizzle128);             // K, keys x d (S = Q K^T)
-      const uint64_t v_km = smem_desc(r0 + 32768, 16, 1024, kSwizzle128);     // V (dP = dO V^T)
-      const uint64_t k_mn = smem_desc(r0, 16384, 1024, kSwizzle128);          // K as keys-major B (dQ += dS K)
-      const uint64_t pk_mn = smem_desc(r0 + 65536, 16384, 1024, kSwizzle128); // pk (dpq += P pk)
+      const uint64_t k_km = smem_desc(smem_u32(k_s), 16, 1024, kSwizzle128);       // K, keys x d (S = Q K^T)
+      const uint64_t v_km = smem_desc(smem_u32(v_s), 16, 1024, kSwizzle128);       // V (dP = dO V^T)
+      const uint64_t k_mn = smem_desc(smem_u32(k_s), 16384, 1024, kSwizzle128);    // K as keys-major B (dQ += dS K)
+      const uint64_t pk_mn = smem_desc(smem_u32(pk_s), 16384, 1024, kSwizzle128);  // pk (dpq += P pk)
       const uint64_t do_km = smem_desc(smem_u32(do_s), 16, 1024, kSwizzle128);
+      constexpr uint64_t kTile = 32768 >> 4, kPkTile = 16384 >> 4;
       bool ok = mbar_wait(q_full, 0, err) && mbar_wait(q_tm, 0, err);
       tc_fence_after();
       int nb = 0;  // cached blocks of the tile
       for (int k = 0; k < topk; ++k) nb += valid_block(row_idx[k], tl.nvp) ? 1 : 0;
-      auto sq = [&](uint64_t so) {  // S = Q . K^T (Q from tensor memory)
+      auto sq = [&](int b) -> bool {  // S = Q . K^T (Q from tensor memory) of block b
+        const int ks = b % kKStages;
+        if (!mbar_wait(k_full + ks, (b / kKStages) & 1, err)) return false;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>(ks) * kTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
           mma_ts(tmem + kColS, tmem + kColQ + kk * 8, k_km + so + off, id_s, kk > 0);
         }
         mma_commit(s_full);
+        return true;
       };
-      auto dp = [&](uint64_t so) {  // dP = dO . V^T
+      auto dp = [&](int b) -> bool {  // dP = dO . V^T of block b, then V's stage is free
+        const int vs = b % kVStages;
+        if (!mbar_wait(v_full + vs, (b / kVStages) & 1, err)) return false;
+        tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>(vs) * kTile;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
           mma_ss(tmem + kColDP, do_km + off, v_km + so + off, id_s, kk > 0);
         }
         mma_commit(dp_full);
+        mma_commit(v_empty + vs);
+        return true;
       };
       // Blocks are pipelined: S of block i+1 goes out as soon as dpq of block
       // i has taken P out of the S columns, and dP of i+1 as soon as dQ of i
       // has taken dS out of the dP columns, so the softmax computes P of i+1
       // while dQ of i runs and dS of i+1 while dpq of i+1 runs.
-      if (nb > 0) {
-        if ((ok = ok && mbar_wait(kv_full, 0, err))) {
-          tc_fence_after();
-          sq(0);
-          dp(0);
-        }
-      }
+      if (nb > 0) ok = ok && sq(0) && dp(0);
       for (int it = 0; ok && it < nb; ++it) {
-        const int s = it % kStages, s1 = (it + 1) % kStages;
-        const uint64_t so = static_cast<uint64_t>(s) * kStageDesc, so1 = static_cast<uint64_t>(s1) * kStageDesc;
         const bool next = it + 1 < nb;
+        const int vs = it % kVStages, ks = it % kKStages;
         if (!(ok = mbar_wait(p_full, it & 1, err))) break;
+        if (!(ok = mbar_wait(pk_full + vs, (it / kVStages) & 1, err))) break;
         tc_fence_after();
+        const uint64_t po = static_cast<uint64_t>(vs) * kPkTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
-          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + so + kk * 128, id_p, it > 0 || kk > 0);
+          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + po + kk * 128, id_p, it > 0 || kk > 0);
         }
-        if (next) {
-          if (!(ok = mbar_wait(kv_full + s1, ((it + 1) / kStages) & 1, err))) break;
-          tc_fence_after();
-          sq(so1);
-        }
+        mma_commit(pk_empty + vs);
+        if (next && !(ok = sq(it + 1))) break;
         if (!(ok = mbar_wait(ds_full, it & 1, err))) break;
         tc_fence_after();
+        const uint64_t so = static_cast<uint64_t>(ks) * kTile;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;
           mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
         }
-        mma_commit(kv_empty + s);
-        if (next) dp(so1);
+        mma_commit(k_empty + ks);
+        if (next && !(ok = dp(it + 1))) break;
       }
       mma_commit(done);
     }
@@ -243,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st16(lane_base + kColQ + 32 * wg + 16, qv + 16);
       tmem_wait_st();
       tc_fence_before();
+      fence_async_shared();  // Q's shared memory is K's third stage next: TMA writes follow these reads
       __syncwarp();
       if (lane == 0) mbar_arrive(q_tm);
     }

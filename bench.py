@@ -432,6 +432,7 @@ def run_ours(args):
     decode = bench_decode(args, dev, pk_info, peak_kind, world)
     train = bench_train(args, dev, pk_info, peak_kind)
     fp8_prefill = bench_prefill_fp8(args, dev, pk_info, peak_kind, attn_tflops)
+    varlen = bench_varlen(args, dev, pk_info, peak_kind)
 
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
@@ -453,6 +454,8 @@ def run_ours(args):
             "wall_s": t_wall}
     if fp8_prefill:
         line["prefill_fp8"] = fp8_prefill
+    if varlen:
+        line["varlen_paged"] = varlen
     if decode:
         line["decode"] = decode
     if train:
@@ -667,6 +670,56 @@ def run_ncu_case(args):
     torch.cuda.synchronize()
     plan.check_errors()
     print("ncu case %s done: %d launches" % (args.ncu_case, args.steps))
+
+
+def bench_varlen(args, dev, pk_info, peak_kind):
+    """Varlen paged prefill (4 packed sequences of 8192/16384/32768/131072
+    tokens, pages under a random permutation, planted block signal): the
+    step proxy -> top-k -> attention, with the L2 flushed before each timed
+    step; tokens/s and the two tensor-core stages' TFLOP/s (proxy on the
+    causal lower triangle of blocks, attention on the selected blocks)."""
+    import torch
+    from block_sparse_long_proxy_gb300 import msa, synth
+    case = synth.varlen_paged()
+    inp = synth.make_inputs(case, device=dev)
+    plan = msa.Plan(case.qo_lens, case.kv_lens, case.hq, case.hkv, case.hp, case.d, case.dp, case.topk,
+                    num_pages=inp["k_pages"].shape[0])
+    ms = plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"])
+    idx = msa.topk_select(ms, case.topk, plan.num_valid_pages)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    stream = torch.cuda.current_stream()
+    flush = L2Flush(dev)
+    for _ in range(3):
+        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
+        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out=out, lse=lse)
+    torch.cuda.synchronize()
+    plan.check_errors()
+    t_step, t_proxy, t_attn = [], [], []
+    for _ in range(max(3, min(args.steps, 8))):
+        flush()
+        a, b, c, d = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+        a.record(stream)
+        plan.proxy_maxscore(inp["pq"], inp["pk_pages"], inp["kv_indices"], out=ms)
+        b.record(stream)
+        msa.topk_select(ms, case.topk, plan.num_valid_pages, out=idx)
+        c.record(stream)
+        plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out=out, lse=lse)
+        d.record(stream)
+        torch.cuda.synchronize()
+        t_step.append(a.elapsed_time(d))
+        t_proxy.append(a.elapsed_time(b))
+        t_attn.append(c.elapsed_time(d))
+    plan.check_errors()
+    step_ms, proxy_ms, attn_ms = (statistics.median(v) for v in (t_step, t_proxy, t_attn))
+    flops, n_sel = selected_flops(idx.cpu().numpy(), case)
+    proxy_flops = sum(t.nvp for t in plan_tiles(case)) * case.hp * 2.0 * 128 * 128 * case.dp
+    peak = pk_info.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    at, pt = flops / (attn_ms / 1e3) / 1e12, proxy_flops / (proxy_ms / 1e3) / 1e12
+    return {"workload": case.name, "tokens": case.total_q, "ms_per_step": step_ms,
+            "tokens_per_s": case.total_q / (step_ms / 1e3), "proxy_ms": proxy_ms, "sparse_attn_ms": attn_ms,
+            "proxy_tflops": pt, "attn_tflops_selected": at, "proxy_frac": pt / peak, "attn_frac": at / peak,
+            "peak_kind": "%s bf16 dense burst" % peak_kind}
 
 
 def bench_train(args, dev, pk_info, peak_kind):

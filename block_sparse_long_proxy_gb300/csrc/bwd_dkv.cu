@@ -14,7 +14,7 @@
 //   dV  += P^T . dO_h           dK  += dS^T . Q_h       (P^T, dS^T from TMEM)
 //   dpk += P^T . pq
 // and once per 64 rows, before the heads, for the proxy distribution over
-// the same keys (in the S^T columns):
+// the same keys (in the dP^T columns):
 //   Sp^T = pk . pq^T,  Pp^T = exp2(Sp^T zsl2 - lsep),  dpk += (-G Pp^T) . pq
 // so that at the end dpk * (-w / (G sqrt(dp))) = w/sqrt(dp) (Pp - mean_h P_h)^T pq,
 // this KV head's share of the KL gradient with respect to the proxy keys.
@@ -24,9 +24,10 @@
 // shared memory.  The softmax warps overwrite S^T (or Sp^T) and dP^T in
 // place with bf16 pairs, handing P^T over before dS^T.  The MMA stream is
 // pipelined across heads: S^T of head h+1 goes out as soon as dV and dpk of
-// head h have taken P^T out of the S^T columns (the next 64 rows' Sp^T after
-// the last head), dP^T of h+1 right after dK of h, so the softmax of one
-// head overlaps the products of the other.
+// head h have taken P^T out of the S^T columns, dP^T of h+1 right after dK of
+// h (after the last head, the next 64 rows' Sp^T), so the softmax of one
+// head overlaps the products of the other; a half's first S^T goes out
+// before its proxy term, while the proxy softmax runs.
 // Each warpgroup owns 32 of the 64 rows, and each writes its packed pairs
 // into the first half of its own 32 columns, so a k-step of 16 rows of an
 // A operand in TMEM starts at column (kk / 2) * 32 + (kk % 2) * 8.
@@ -286,13 +287,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait(kv_full, 0, err) && mbar_wait(init_done, 0, err);
       tc_fence_after();
       // Sp^T = pk . pq^T of the half whose first head sits in stage qa, in
-      // the S^T columns
+      // the dP^T columns (so that the half's first S^T can go out while the
+      // proxy softmax runs)
       auto sp = [&](int qa) -> bool {
         const uint64_t po = static_cast<uint64_t>(qa % kQStages) * kQdDesc;
         if (!mbar_wait(qd_full + qa % kQStages, (qa / kQStages) & 1, err)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColS, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
+        for (int kk = 0; kk < kDP / 16; ++kk) mma_ss(tmem + kColDP, pk_km + kk * 2, pq_km + po + kk * 2, id_s, kk > 0);
         mma_commit(sp_full);
         return true;
       };
@@ -320,20 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                      kk > 0);
             mma_commit(s_full);
           };
-          // head 0: dP^T overlaps the proxy softmax, then the proxy term of
-          // dpk reads -G Pp^T from the S^T columns before S^T overwrites them
+          // head 0: S^T overlaps the proxy softmax, then the proxy term of
+          // dpk reads -G Pp^T from the dP^T columns before dP^T overwrites them
           {
             const int s = qi % kQStages;
             const uint64_t so = static_cast<uint64_t>(s) * kQdDesc;
             if (!(ok = mbar_wait(qd_full + s, (qi / kQStages) & 1, err))) break;
             tc_fence_after();
-            dpt(so);
+            st(so);
             if (!(ok = mbar_wait(pp_full, pi & 1, err))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColDPK, ts_col(tmem + kColS, kk), pq_mn + po + kk * 128, id_p, 1);
-            st(so);
+              mma_ts(tmem + kColDPK, ts_col(tmem + kColDP, kk), pq_mn + po + kk * 128, id_p, 1);
+            dpt(so);
           }
           // heads pipelined: S^T of head h+1 is issued as soon as dV, dpk of
           // head h have taken P^T out of its columns, so the softmax of h+1
@@ -354,9 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!(ok = mbar_wait(qd_full + s1, ((qi + 1) / kQStages) & 1, err))) break;
               tc_fence_after();
               st(so1);
-            } else if (more_halves) {  // the next half's proxy scores, so its proxy softmax follows dS^T at once
-              if (!(ok = sp(qi + 1))) break;
-              sp_issued = true;
             }
             if (!(ok = mbar_wait(ds_full, qi & 1, err))) break;
             tc_fence_after();
@@ -364,7 +363,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + kColDK, ts_col(tmem + kColDP, kk), q_mn + so + kk * 128, id_d, 1);
             mma_commit(qd_empty + s);
-            if (next) dpt(so1);
+            if (next) {
+              dpt(so1);
+            } else if (more_halves) {  // the next half's proxy scores, once dK has read dS^T out of their columns
+              if (!(ok = sp(qi + 1))) break;
+              sp_issued = true;
+            }
           }
           if (!ok) break;
         }
@@ -423,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         {
           uint32_t sv[32], pk[16];
-          tmem_ld32(lane_base + kColS + c0, sv);
+          tmem_ld32(lane_base + kColDP + c0, sv);
           tmem_wait_ld();
           const float2* nlp = reinterpret_cast<const float2*>(row_s + s0 * 192 + 128 + c0);
 #pragma unroll
@@ -439,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             pk[c >> 1] = pack_bf16x2(p0 * neg_g, p1 * neg_g);
           }
-          tmem_st16(lane_base + kColS + c0, pk);
+          tmem_st16(lane_base + kColDP + c0, pk);
           tmem_wait_st();
         }
         tc_fence_before();

@@ -829,17 +829,19 @@ msa_status launch_attn_prefill(const msa_plan_s* p, const void* q, const void* k
 // [total_q, Hp].
 msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                                 const int32_t* idx, void* op, float* lse, cudaStream_t st) {
-  if (p->dp != 64) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: proxy_head_dim 64 only");
   if (p->topk > kMaxTopk) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: topk above 1024");
   CUtensorMap qm, km, om;
-  const uint64_t kdims[2] = {64, static_cast<uint64_t>(p->num_pages) * 128};
-  const uint64_t kstr[1] = {128};
+  // pq and pk at dp = 32 are read as 64-column boxes whose upper half lies
+  // past the tensor's edge: TMA fills it with zeros, so the dp = 64 kernel
+  // computes the same scores and an Op whose columns [dp, 64) are zero
+  const uint64_t kdims[2] = {static_cast<uint64_t>(p->dp), static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t kstr[1] = {static_cast<uint64_t>(p->dp) * 2};
   const uint32_t kbox[2] = {64, 128};
-  if (!rows_map(&qm, pq, 64, p->hp, p->total_q) || !rows_map(&om, op, 64, p->hp, p->total_q) ||
+  if (!rows_map(&qm, pq, p->dp, p->hp, p->total_q) || !rows_map(&om, op, 64, p->hp, p->total_q) ||
       !encode_tensor_map(&km, 2, pk_pages, kdims, kstr, kbox, 1, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
   const AttnUnit* units = reinterpret_cast<const AttnUnit*>(p->aux_d + p->proxy_attn_units_off);
-  const float scale_log2 = 1.4426950408889634f / 8.0f;  // 1 / sqrt(64)
+  const float scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(p->dp));
   const dim3 grid(std::min(p->n_proxy_attn_units, p->num_sms));
   return cuda_check(launch_attn_variant<64, true, false>(grid, st, qm, km, km, om, p->topk, units,
                                                           p->n_proxy_attn_units, p->tiles_d, idx, kv_indices,

@@ -33,6 +33,13 @@
 //            in KV-head order)
 // No gradient is reduced by atomics: every sum has a fixed order, so the
 // backward gives the same bits on every run.
+//
+// The tensor-core kernels are built for d = 128 and dp = 64.  At d = 64 or
+// dp = 32 they read q, out, dout, K, V, pq and pk through tensor maps of the
+// true width with the same 64-column boxes: the columns past the edge arrive
+// as zeros, every contraction over d (or dp) is unchanged, and the products
+// whose columns run over d (dq, dk, dv) or dp (dpq, dpk) have zeros there,
+// which the kernels do not store.  The scales are those of the true widths.
 
 #include "msa_internal.h"
 #include "ptx.cuh"
@@ -42,8 +49,7 @@
 namespace msa {
 namespace {
 
-constexpr int kD = 128;    // head dim of this kernel
-constexpr int kDP = 64;    // proxy head dim of this kernel
+constexpr int kDP = 64;    // columns of the proxy softmax's Op and of the partials
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -54,31 +60,37 @@ constexpr float kLog2e = 1.4426950408889634f;
 // of the G query heads that use g's blocks, both stored [head][row]; the
 // proxy LSE of g in log2 units, [proxy head][row]; and dpq's proxy term
 // w/sqrt(dp) * p_proxy . pk, from the proxy softmax (launch_proxy_softmax)
-// run just before.
+// run just before.  out and dout are [total_q, Hq, d] (d = 64 or 128), dpq
+// [total_q, Hp, dp] (dp = 32 or 64); the proxy softmax's Op keeps 64 columns.
 __global__ void __launch_bounds__(kThreads)
     bwd_prep_kernel(const TileInfo* __restrict__ tiles, const __nv_bfloat16* __restrict__ out,
                     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ lse,
                     const __nv_bfloat16* __restrict__ op, const float* __restrict__ lse_p,
                     float* __restrict__ dsumt, float* __restrict__ lse2t, float* __restrict__ lsept,
-                    float* __restrict__ dpq, int32_t hq, int32_t hsel, int32_t total_q, float kl_weight) {
+                    float* __restrict__ dpq, int32_t hq, int32_t hsel, int32_t total_q, int32_t d, int32_t dp,
+                    float kl_weight) {
   const int t = blockIdx.x / hsel, g = blockIdx.x % hsel;
   const TileInfo tl = tiles[t];
   const int lane = threadIdx.x & 31;
   const int G = hq / hsel;
 
-  // D = rowsum(dout * out): eight lanes per (row, head), 16 d values each,
-  // so that every thread has its few loads in flight at once and the block's
-  // 256 threads cover 32 rows per pass
+  // D = rowsum(dout * out): eight lanes per (row, head), d / 8 values each
+  // (two 16-byte loads apiece at d = 128, one at d = 64), so that every
+  // thread has its few loads in flight at once and the block's 256 threads
+  // cover 32 rows per pass
   static_assert(kThreads % 8 == 0 && 128 % (kThreads / 8) == 0, "row passes");
   const int sub = lane & 7;
+  const int nv = d >> 6;  // 16-byte loads per lane
   for (int e = threadIdx.x >> 3; e < G * 128; e += kThreads / 8) {
     const int h = g * G + e / 128, r = e % 128;
     float acc = 0.f;
     if (r < tl.rows) {
-      const int64_t off = (static_cast<int64_t>(tl.q_begin + r) * hq + h) * kD + sub * 16;
+      const int64_t off = (static_cast<int64_t>(tl.q_begin + r) * hq + h) * d + sub * nv * 8;
       const uint4* a = reinterpret_cast<const uint4*>(out + off);
       const uint4* b = reinterpret_cast<const uint4*>(dout + off);
-      const uint4 x0 = a[0], x1 = a[1], y0 = b[0], y1 = b[1];
+      const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 x0 = a[0], y0 = b[0];
+      const uint4 x1 = nv > 1 ? a[1] : zero, y1 = nv > 1 ? b[1] : zero;
       const uint32_t xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
       const uint32_t ys[8] = {y0.x, y0.y, y0.z, y0.w, y1.x, y1.y, y1.z, y1.w};
 #pragma unroll
@@ -99,17 +111,18 @@ __global__ void __launch_bounds__(kThreads)
   }
 
   // proxy LSE in log2 units, and dpq's proxy term
-  const float f = kl_weight * rsqrtf(static_cast<float>(kDP));
+  const float f = kl_weight * rsqrtf(static_cast<float>(dp));
   for (int r = threadIdx.x; r < tl.rows; r += blockDim.x) {
     const int64_t q_row = tl.q_begin + r;
     lsept[static_cast<int64_t>(g) * total_q + q_row] = lse_p[q_row * hsel + g] * kLog2e;
   }
-  for (int e = threadIdx.x; e < tl.rows * (kDP / 8); e += blockDim.x) {
-    const int r = e / (kDP / 8), c = e % (kDP / 8);
-    const int64_t base = (static_cast<int64_t>(tl.q_begin + r) * hsel + g) * kDP + c * 8;
-    const uint4 v = *reinterpret_cast<const uint4*>(op + base);
+  const int cpr = dp / 8;  // 8-column groups of a dpq row
+  for (int e = threadIdx.x; e < tl.rows * cpr; e += blockDim.x) {
+    const int r = e / cpr, c = e % cpr;
+    const int64_t row = static_cast<int64_t>(tl.q_begin + r) * hsel + g;
+    const uint4 v = *reinterpret_cast<const uint4*>(op + row * kDP + c * 8);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float4* dst = reinterpret_cast<float4*>(dpq + base);
+    float4* dst = reinterpret_cast<float4*>(dpq + row * dp + c * 8);
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2 * k]));
@@ -232,8 +245,6 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                            const void* dout, const void* pq, const void* pk_pages, float kl_weight, float* dq,
                            float* dk, float* dv, float* dpq, float* dpk, cudaStream_t st) {
   if (p->decode) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: decode batches have no backward");
-  if (p->d != kD || p->dp != kDP)
-    return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: head_dim 128 and proxy_head_dim 64 only");
   if (p->bwd_d == nullptr) return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: plan has no backward scratch");
   const int n_ent = p->n_page_entries;
   const size_t ent = static_cast<size_t>(n_ent) * p->hkv;
@@ -272,7 +283,7 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   if (s != MSA_OK) return s;
   bwd_prep_kernel<<<p->n_tiles * p->hp, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
                                                           dpq, p->hq, p->hp, static_cast<int32_t>(p->total_q),
-                                                          kl_weight);
+                                                          p->d, p->dp, kl_weight);
   s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)
     s = cuda_check(cudaMemsetAsync(dpq_cnt, 0, 4 * static_cast<size_t>(p->n_tiles) * p->hp, st),

@@ -84,8 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
                       float* __restrict__ dv, float* __restrict__ dpk, float* __restrict__ dpk_part,
                       int32_t* __restrict__ dpk_cnt, int32_t hq, int32_t hkv, int32_t hsel,
-                      int32_t total_q,
-                      float kl_weight, uint32_t* err) {
+                      int32_t total_q, int32_t d, int32_t dp, float kl_weight, uint32_t* err) {
   using L = DkvSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -96,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (page_ok && owner[page] != e) return;  // another entry's CTA owns this page
   if (!page_ok) page = 0;
   const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
-  const int64_t kv_off = (page * hkv + g) * 128 * kD;
+  const int64_t kv_off = (page * hkv + g) * 128 * d;
 
   // dpk of the page: each of its hkv CTAs leaves a partial, and the last of
   // them to count itself adds the partials in KV-head order (the same sum on
@@ -113,12 +112,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("bar.sync %0, %1;" ::"r"(bar_id), "r"(nthr) : "memory");
     if (!*flag) return;
-    float4* dst = reinterpret_cast<float4*>(dpk + page * 128 * kDP);
+    // partials keep 64 columns a row; dpk rows have dp (columns [dp, 64) are
+    // padding at dp = 32)
+    float4* dst = reinterpret_cast<float4*>(dpk + page * 128 * dp);
     const float4* src0 = reinterpret_cast<const float4*>(dpk_part + static_cast<int64_t>(e) * hkv * 128 * kDP);
-    for (int i = tid; i < 128 * kDP / 4; i += nthr) {
-      float4 acc = __ldcg(src0 + i);
+    const int q4 = dp / 4;  // float4s of a dpk row
+    for (int i = tid; i < 128 * q4; i += nthr) {
+      const int src_i = (i / q4) * (kDP / 4) + i % q4;
+      float4 acc = __ldcg(src0 + src_i);
       for (int gg = 1; gg < hkv; ++gg) {
-        const float4 v = __ldcg(src0 + static_cast<int64_t>(gg) * 128 * kDP / 4 + i);
+        const float4 v = __ldcg(src0 + static_cast<int64_t>(gg) * 128 * kDP / 4 + src_i);
         acc.x += v.x;
         acc.y += v.y;
         acc.z += v.z;
@@ -133,7 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float4* a = reinterpret_cast<float4*>(dk + kv_off);
     float4* b = reinterpret_cast<float4*>(dv + kv_off);
     float4* c = reinterpret_cast<float4*>(part_e);
-    for (int i = threadIdx.x; i < 128 * kD / 4; i += blockDim.x) {
+    for (int i = threadIdx.x; i < 128 * d / 4; i += blockDim.x) {
       a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       b[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
@@ -381,8 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key = quarter * 32 + lane;
     const int c0 = wg * 32;  // this warpgroup's rows within the 64-row half
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
-    const float zsl2 = kLog2e * rsqrtf(static_cast<float>(kDP));
+    const float sl2 = kLog2e * rsqrtf(static_cast<float>(d));
+    const float zsl2 = kLog2e * rsqrtf(static_cast<float>(dp));
     const float neg_g = -static_cast<float>(G);
     bool ok = mbar_wait(kv_full, 0, err);
     {  // dV, dpk, dK start at zero (columns 128..447, 160 per warpgroup); K row
@@ -507,12 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
     if (ok && page_ok) {
-      const float ks = rsqrtf(static_cast<float>(kD));
-      const float f_main = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
-      float* dvr = dv + kv_off + static_cast<int64_t>(key) * kD + wg * 64;
-      float* dkr = dk + kv_off + static_cast<int64_t>(key) * kD + wg * 64;
+      const float ks = rsqrtf(static_cast<float>(d));
+      const float f_main = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
+      float* dvr = dv + kv_off + static_cast<int64_t>(key) * d + wg * 64;
+      float* dkr = dk + kv_off + static_cast<int64_t>(key) * d + wg * 64;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
+        if (wg * 64 >= d) break;  // at d = 64 the second warpgroup's columns are padding
         uint32_t a[32], b[32];
         tmem_ld32(lane_base + kColDV + wg * 64 + c * 32, a);
         tmem_ld32(lane_base + kColDK + wg * 64 + c * 32, b);
@@ -552,19 +556,20 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
                              const int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
                              float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st) {
+  // tensors of their true width d (dp); the 64-column boxes read zeros past
+  // the edge at d = 64 (dp = 32)
   CUtensorMap qm, dom, pqm, km, vm, pkm;
-  const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
-                             static_cast<uint64_t>(p->total_q)};
-  const uint64_t qstr[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(p->hq) * kD * 2};
+  const uint64_t d = static_cast<uint64_t>(p->d), dp = static_cast<uint64_t>(p->dp);
+  const uint64_t qdims[3] = {d, static_cast<uint64_t>(p->hq), static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {d * 2, static_cast<uint64_t>(p->hq) * d * 2};
   const uint32_t qbox[3] = {64, 1, 64};
-  const uint64_t pqdims[3] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->hp),
-                              static_cast<uint64_t>(p->total_q)};
-  const uint64_t pqstr[2] = {static_cast<uint64_t>(kDP) * 2, static_cast<uint64_t>(p->hp) * kDP * 2};
-  const uint64_t kdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
-  const uint64_t kstr[1] = {static_cast<uint64_t>(kD) * 2};
+  const uint64_t pqdims[3] = {dp, static_cast<uint64_t>(p->hp), static_cast<uint64_t>(p->total_q)};
+  const uint64_t pqstr[2] = {dp * 2, static_cast<uint64_t>(p->hp) * dp * 2};
+  const uint64_t kdims[2] = {d, static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t kstr[1] = {d * 2};
   const uint32_t kbox[2] = {64, 128};
-  const uint64_t pkdims[2] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->num_pages) * 128};
-  const uint64_t pkstr[1] = {static_cast<uint64_t>(kDP) * 2};
+  const uint64_t pkdims[2] = {dp, static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t pkstr[1] = {dp * 2};
   if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&dom, 3, dout, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&pqm, 3, pq, pqdims, pqstr, qbox, 1, 128) ||
@@ -576,8 +581,8 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
       qm, dom, pqm, km, vm, pkm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
-      dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), kl_weight,
-      p->err_d);
+      dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), p->d,
+      p->dp, kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
 }
 

@@ -65,8 +65,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                      const float* __restrict__ lse2t, const float* __restrict__ dsumt, float* __restrict__ dq,
                      float* __restrict__ dpq, float* __restrict__ dpq_part, int32_t* __restrict__ dpq_cnt,
-                     int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q, float kl_weight,
-                     uint32_t* err) {
+                     int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q, int32_t d,
+                     int32_t dp, float kl_weight, uint32_t* err) {
   using L = DqSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full);
         return true;
       };
-      auto dp = [&](int b) -> bool {  // dP = dO . V^T of block b, then V's stage is free
+      auto dpv = [&](int b) -> bool {  // dP = dO . V^T of block b, then V's stage is free
         const int vs = b % kVStages;
         if (!mbar_wait(v_full + vs, (b / kVStages) & 1, err)) return false;
         tc_fence_after();
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // i has taken P out of the S columns, and dP of i+1 as soon as dQ of i
       // has taken dS out of the dP columns, so the softmax computes P of i+1
       // while dQ of i runs and dS of i+1 while dpq of i+1 runs.
-      if (nb > 0) ok = ok && sq(0) && dp(0);
+      if (nb > 0) ok = ok && sq(0) && dpv(0);
       for (int it = 0; ok && it < nb; ++it) {
         const bool next = it + 1 < nb;
         const int vs = it % kVStages, ks = it % kKStages;
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
         }
         mma_commit(k_empty + ks);
-        if (next && !(ok = dp(it + 1))) break;
+        if (next && !(ok = dpv(it + 1))) break;
       }
       mma_commit(done);
     }
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
     const float l2 = row_ok ? lse2t[ei] : 0.f;
     const float dd = row_ok ? dsumt[ei] : 0.f;
-    const float sl2 = kLog2e * rsqrtf(static_cast<float>(kD));
+    const float sl2 = kLog2e * rsqrtf(static_cast<float>(d));
     bool ok = mbar_wait(q_full, 0, err);
     {  // Q_h row r, d in [64 wg, 64 wg + 64), into tensor memory as bf16 pairs
       const uint8_t* qrow = q_s + wg * 16384 + r * 128;
@@ -339,8 +339,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.ld is warp-collective: every lane loads, only valid rows store
     if (ok) {
       const int64_t q_row = tl.q_begin + r;
-      float* dqr = dq + (q_row * hq + h) * kD + wg * 64;
-      const float qs = rsqrtf(static_cast<float>(kD));
+      float* dqr = dq + (q_row * hq + h) * d + wg * 64;
+      const float qs = rsqrtf(static_cast<float>(d));
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t a[32];
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) a[i] = 0u;
         }
-        if (row_ok)
+        if (row_ok && wg * 64 < d)  // at d = 64 the second warpgroup's columns are padding
 #pragma unroll
           for (int i = 0; i < 8; ++i)
             reinterpret_cast<float4*>(dqr + c * 32)[i] =
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this head's dpq partial (every row of the tile's slot, zeros without
     // blocks), then the count; the last head of the proxy head sums
     {
-      const float f = -kl_weight * rsqrtf(static_cast<float>(kDP)) / static_cast<float>(G);
+      const float f = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
       uint32_t a[32];
       if (ok && it > 0) {
         tmem_ld32(lane_base + kColDPQ + wg * 32, a);
@@ -392,9 +392,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       *flag = prev == G - 1;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
-    if (*flag && row_ok) {
+    if (*flag && row_ok && wg * 32 < dp) {  // at dp = 32 the second warpgroup's columns are padding
       const int64_t q_row = tl.q_begin + r;
-      float4* dpr = reinterpret_cast<float4*>(dpq + (q_row * hsel + ps) * kDP + wg * 32);
+      float4* dpr = reinterpret_cast<float4*>(dpq + (q_row * hsel + ps) * dp + wg * 32);
       float4 acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = __ldcg(dpr + i);
@@ -426,16 +426,18 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
                             const float* lse2t, const float* dsumt, float* dq, float* dpq, float* dpq_part,
                             int32_t* dpq_cnt, float kl_weight, cudaStream_t st) {
+  // tensors of their true width d (dp); the 64-column boxes read zeros past
+  // the edge at d = 64 (dp = 32)
   CUtensorMap qm, dom, km, vm, pkm;
-  const uint64_t qdims[3] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->hq),
-                             static_cast<uint64_t>(p->total_q)};
-  const uint64_t qstr[2] = {static_cast<uint64_t>(kD) * 2, static_cast<uint64_t>(p->hq) * kD * 2};
+  const uint64_t d = static_cast<uint64_t>(p->d), dp = static_cast<uint64_t>(p->dp);
+  const uint64_t qdims[3] = {d, static_cast<uint64_t>(p->hq), static_cast<uint64_t>(p->total_q)};
+  const uint64_t qstr[2] = {d * 2, static_cast<uint64_t>(p->hq) * d * 2};
   const uint32_t qbox[3] = {64, 1, 128};
-  const uint64_t kdims[2] = {static_cast<uint64_t>(kD), static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
-  const uint64_t kstr[1] = {static_cast<uint64_t>(kD) * 2};
+  const uint64_t kdims[2] = {d, static_cast<uint64_t>(p->num_pages) * p->hkv * 128};
+  const uint64_t kstr[1] = {d * 2};
   const uint32_t kbox[2] = {64, 128};
-  const uint64_t pkdims[2] = {static_cast<uint64_t>(kDP), static_cast<uint64_t>(p->num_pages) * 128};
-  const uint64_t pkstr[1] = {static_cast<uint64_t>(kDP) * 2};
+  const uint64_t pkdims[2] = {dp, static_cast<uint64_t>(p->num_pages) * 128};
+  const uint64_t pkstr[1] = {dp * 2};
   if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&dom, 3, dout, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
@@ -446,7 +448,7 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
   cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dq_tc_kernel<<<p->n_tiles * p->hq, kThreads, smem, st>>>(
       qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, dpq_part, dpq_cnt, p->hq,
-      p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), kl_weight, p->err_d);
+      p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), p->d, p->dp, kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
 }
 

@@ -146,6 +146,7 @@ def test_bwd_bitwise_reproducible(cuda_dev):
 
 
 NARROW = [
+    (synth.tiny(), 1.0),
     (synth.Case("d64 dp32", [256], [256], 4, 2, 64, 2, 32, 2), 1.0),
     (synth.Case("d64 dp32 ragged paged G=4", [300, 77, 129], [300, 500, 129], 8, 2, 64, 2, 32, 3,
                 page_perm_seed=3, extra_pages=2), 0.6),

@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # (DRAM bytes read + written) of one launch of the small S=16384 capture and the
     # (tile, group, block) selections it processed; scaled to a launch by selections.
-    "attn_fwd.cu": {"src": "f2b289e451fe3566", "bytes": 244493568 + 108109312, "sel": 15424},
-    "attn_fwd.cu:fp8": {"src": "f2b289e451fe3566", "bytes": 180835840 + 101754880, "sel": 15424},
+    "attn_fwd.cu": {"src": "1135c1938e315513", "bytes": 244261888 + 107886592, "sel": 15424},
+    "attn_fwd.cu:fp8": {"src": "1135c1938e315513", "bytes": 180615424 + 101479680, "sel": 15424},
 }
 
 

@@ -66,7 +66,9 @@ bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* di
   if (swizzle_bytes == 128) sw = CU_TENSOR_MAP_SWIZZLE_128B;
   if (swizzle_bytes == 64) sw = CU_TENSOR_MAP_SWIZZLE_64B;
   if (swizzle_bytes == 32) sw = CU_TENSOR_MAP_SWIZZLE_32B;
-  CUtensorMapDataType dt = dtype_bf16_or_u8 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUtensorMapDataType dt = dtype_bf16_or_u8 == 2   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dtype_bf16_or_u8 == 1 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   CUresult r = fn(reinterpret_cast<CUtensorMap*>(map), dt, rank, const_cast<void*>(base), gdim, gstride, bdim,
                   estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -78,6 +80,7 @@ bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* di
 using namespace msa;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+static bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
 
 namespace msa {
 namespace {
@@ -442,6 +445,11 @@ msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pag
   if (!plan || !q || !k_pages || !v_pages || !kv_indices || !kv_block_indexes || !out || !lse || !dout || !pq ||
       !pk_pages || !dq || !dk_pages || !dv_pages || !dpq || !dpk_pages)
     return set_error(MSA_ERR_INVALID_ARG, "msa_sparse_attn_bwd: NULL argument");
+  if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(out) || !aligned16(dout) ||
+      !aligned16(pq) || !aligned16(pk_pages) || !aligned32(dq) || !aligned32(dk_pages) || !aligned32(dv_pages) ||
+      !aligned32(dpq) || !aligned32(dpk_pages))
+    return set_error(MSA_ERR_INVALID_ARG,
+                     "msa_sparse_attn_bwd: inputs must be 16-byte aligned and gradients 32-byte aligned");
   if (plan->kv_dtype != MSA_KV_BF16)
     return set_error(MSA_ERR_UNSUPPORTED, "msa_sparse_attn_bwd: bf16 K/V only");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -23,9 +23,10 @@
 //            both stored [head][row]; the proxy LSE in log2 units
 //            ([proxy head][row]) and dpq's proxy term (plain store)
 //   index    page owners, then the page -> selections inverse index
-//   dq       per (tile, head), tcgen05 (bwd_dq.cu): dq (owned, plain
-//            store) and dpq's main term (a partial per head; the last of the
-//            G heads adds them in head order to the proxy term)
+//   dq       per (tile, proxy head), tcgen05 (bwd_dq.cu): the proxy head's
+//            G query heads one after the other; dq (owned, plain store) and
+//            dpq's main term (accumulated over the G heads in tensor memory,
+//            then added to the proxy term)
 //   dkv      per (physical page, group), tcgen05 (bwd_dkv.cu): loops over
 //            the selections of the page by any page-table entry (sorted, so
 //            sums are deterministic); dk, dv (owned, plain store) and dpk
@@ -224,9 +225,8 @@ __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_
 // The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
 // fp32), lsept ([Hp][total_q] fp32), the proxy softmax's Op (bf16 [total_q,
 // Hp, dp]) and LSE (fp32 [total_q, Hp]), the inverse index (int32), the page
-// owners (int32 [num_pages]), dpq's per-head partials (fp32 [n_tiles][Hq]
-// [128][dp]) and their counters ([n_tiles][Hp]), dpk's per-KV-head partials
-// (fp32 [entries][Hkv][128][dp]) and their counters ([entries]).
+// owners (int32 [num_pages]), dpk's per-KV-head partials (fp32 [entries]
+// [Hkv][128][dp]) and their counters ([entries]).
 static size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 size_t bwd_scratch_bytes(const msa_plan_s* p) {
@@ -236,7 +236,6 @@ size_t bwd_scratch_bytes(const msa_plan_s* p) {
   return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hp) + al256(2 * tq * p->hp * kDP) + al256(4 * tq * p->hp) +
          al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk)) +
          al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages)) +
-         al256(4 * static_cast<size_t>(p->n_tiles) * p->hq * 128 * kDP) + al256(4 * static_cast<size_t>(p->n_tiles) * p->hp) +
          al256(4 * ent * 128 * kDP) + al256(4 * static_cast<size_t>(p->n_page_entries));
 }
 
@@ -267,10 +266,6 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk));
   int32_t* owner = reinterpret_cast<int32_t*>(sp);                    // [num_pages]
   sp += al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
-  float* dpq_part = reinterpret_cast<float*>(sp);                     // [n_tiles][hq][128][dp]
-  sp += al256(4 * static_cast<size_t>(p->n_tiles) * p->hq * 128 * kDP);
-  int32_t* dpq_cnt = reinterpret_cast<int32_t*>(sp);                  // [n_tiles][hp]
-  sp += al256(4 * static_cast<size_t>(p->n_tiles) * p->hp);
   float* dpk_part = reinterpret_cast<float*>(sp);                     // [entries][hkv][128][dp]
   sp += al256(4 * ent * 128 * kDP);
   int32_t* dpk_cnt = reinterpret_cast<int32_t*>(sp);                  // [entries]
@@ -286,9 +281,6 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                                                           p->d, p->dp, kl_weight);
   s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)
-    s = cuda_check(cudaMemsetAsync(dpq_cnt, 0, 4 * static_cast<size_t>(p->n_tiles) * p->hp, st),
-                   "msa_sparse_attn_bwd: memset");
-  if (s == MSA_OK)
     s = cuda_check(cudaMemsetAsync(dpk_cnt, 0, 4 * static_cast<size_t>(n_ent), st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)  // 0x7F7F7F7F: above every entry index
     s = cuda_check(cudaMemsetAsync(owner, 0x7F, sizeof(int32_t) * static_cast<size_t>(p->num_pages), st),
@@ -303,8 +295,7 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                                               owner, p->num_pages, cur, list);
   s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
   if (s != MSA_OK) return s;
-  s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, dpq_part,
-                       dpq_cnt, kl_weight, st);
+  s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
   if (s != MSA_OK) return s;
   return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, idx, owner, off, list, lse2t,
                            dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, kl_weight, st);

@@ -77,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
                       const __grid_constant__ CUtensorMap pq_map, const __grid_constant__ CUtensorMap k_map,
                       const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap pk_map,
+                      const __grid_constant__ CUtensorMap dk_map, const __grid_constant__ CUtensorMap dv_map,
                       const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                       const int32_t* __restrict__ owner, const int32_t* __restrict__ inv_off,
                       const int32_t* __restrict__ inv_list, int32_t topk,
@@ -116,19 +117,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     // padding at dp = 32)
     float4* dst = reinterpret_cast<float4*>(dpk + page * 128 * dp);
     const float4* src0 = reinterpret_cast<const float4*>(dpk_part + static_cast<int64_t>(e) * hkv * 128 * kDP);
+    // each thread keeps up to eight outputs (2048 float4s at most over 256 or
+    // more threads) and sums the KV heads' partials in head order, one load
+    // per output in flight for each head
     const int q4 = dp / 4;  // float4s of a dpk row
-    for (int i = tid; i < 128 * q4; i += nthr) {
-      const int src_i = (i / q4) * (kDP / 4) + i % q4;
-      float4 acc = __ldcg(src0 + src_i);
-      for (int gg = 1; gg < hkv; ++gg) {
-        const float4 v = __ldcg(src0 + static_cast<int64_t>(gg) * 128 * kDP / 4 + src_i);
-        acc.x += v.x;
-        acc.y += v.y;
-        acc.z += v.z;
-        acc.w += v.w;
-      }
-      dst[i] = acc;
+    constexpr int kPer = 8;
+    float4 acc[kPer];
+    int src_i[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int i = tid + k * nthr;
+      src_i[k] = i < 128 * q4 ? (i / q4) * (kDP / 4) + i % q4 : -1;
     }
+    for (int gg = 0; gg < hkv; ++gg) {
+      const float4* src = src0 + static_cast<int64_t>(gg) * 128 * kDP / 4;
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        if (src_i[k] < 0) continue;
+        const float4 v = __ldcg(src + src_i[k]);
+        if (gg == 0) {
+          acc[k] = v;
+        } else {
+          acc[k].x += v.x;
+          acc[k].y += v.y;
+          acc[k].z += v.z;
+          acc[k].w += v.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPer; ++k)
+      if (src_i[k] >= 0) dst[tid + k * nthr] = acc[k];
   };
 
   if (n == 0) {  // never cached: dK = dV = 0 and a zero dpk partial
@@ -191,7 +210,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the selection list (flat indexes (t * hsel + p) * topk + slot), sorted so
   // that every run sums in the same order
   const bool sorted = n <= kMaxList;
-  if (sorted) {
+  if (n <= 32) {  // one warp, in registers (bitonic network over lanes)
+    if (warp == 0) {
+      int v = lane < n ? inv_list[lb + lane] : 0x7FFFFFFF;
+#pragma unroll
+      for (int size = 2; size <= 32; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          const int o = __shfl_xor_sync(0xFFFFFFFFu, v, stride);
+          const bool up = (lane & size) == 0, lower = (lane & stride) == 0;
+          v = lower == up ? min(v, o) : max(v, o);  // the lower lane of an ascending pair keeps the smaller
+        }
+      if (lane < n) list[lane] = v;
+    }
+  } else if (sorted) {
     int pow2 = 1;
     while (pow2 < n) pow2 <<= 1;
     for (int i = threadIdx.x; i < pow2; i += blockDim.x) list[i] = i < n ? inv_list[lb + i] : 0x7FFFFFFF;
@@ -509,11 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = mbar_wait(done, 0, err);
     tc_fence_after();
     ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
+    // dV and dK of the CTA's 128 keys leave through shared memory (all of it
+    // is free once every product is complete): 32-column fp32 TMA boxes in
+    // the 128-byte swizzled layout, so the 16-byte writes here meet no bank
+    // conflicts and the stores write whole lines
+    const int nbox = d / 32;  // boxes per tensor
     if (ok && page_ok) {
       const float ks = rsqrtf(static_cast<float>(d));
-      const float f_main = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
-      float* dvr = dv + kv_off + static_cast<int64_t>(key) * d + wg * 64;
-      float* dkr = dk + kv_off + static_cast<int64_t>(key) * d + wg * 64;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         if (wg * 64 >= d) break;  // at d = 64 the second warpgroup's columns are padding
@@ -521,26 +555,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(lane_base + kColDV + wg * 64 + c * 32, a);
         tmem_ld32(lane_base + kColDK + wg * 64 + c * 32, b);
         tmem_wait_ld();
+        uint8_t* bv = smem + (wg * 2 + c) * 16384 + key * 128;
+        uint8_t* bk = smem + (nbox + wg * 2 + c) * 16384 + key * 128;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          reinterpret_cast<float4*>(dvr + c * 32)[i] =
-              make_float4(__uint_as_float(a[4 * i]), __uint_as_float(a[4 * i + 1]), __uint_as_float(a[4 * i + 2]),
-                          __uint_as_float(a[4 * i + 3]));
-          reinterpret_cast<float4*>(dkr + c * 32)[i] =
-              make_float4(__uint_as_float(b[4 * i]) * ks, __uint_as_float(b[4 * i + 1]) * ks,
-                          __uint_as_float(b[4 * i + 2]) * ks, __uint_as_float(b[4 * i + 3]) * ks);
+        for (int e = 0; e < 8; ++e) {
+          const int off = (e ^ (key & 7)) << 4;
+          *reinterpret_cast<float4*>(bv + off) =
+              make_float4(__uint_as_float(a[4 * e]), __uint_as_float(a[4 * e + 1]), __uint_as_float(a[4 * e + 2]),
+                          __uint_as_float(a[4 * e + 3]));
+          *reinterpret_cast<float4*>(bk + off) =
+              make_float4(__uint_as_float(b[4 * e]) * ks, __uint_as_float(b[4 * e + 1]) * ks,
+                          __uint_as_float(b[4 * e + 2]) * ks, __uint_as_float(b[4 * e + 3]) * ks);
         }
       }
+      fence_async_shared();  // the TMA stores read the boxes through the async proxy
+    }
+    // every softmax thread has staged its rows (or none of the CTA's stores go out)
+    const bool staged = bar_sync_and(1, 32 * kSoftWarps, ok && page_ok);
+    if (staged && threadIdx.x == 0) {
+      const int row0 = static_cast<int>((page * hkv + g) * 128);
+      for (int b = 0; b < nbox; ++b) {
+        tma_store_2d(&dv_map, smem + b * 16384, 32 * b, row0);
+        tma_store_2d(&dk_map, smem + (nbox + b) * 16384, 32 * b, row0);
+      }
+      bulk_commit_group();
+    }
+    // this KV head's dpk partial (full 32-byte sectors), then the page's sum
+    if (ok && page_ok) {
+      const float f_main = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
       uint32_t a[32];
       tmem_ld32(lane_base + kColDPK + wg * 32, a);
       tmem_wait_ld();
-      float4* pr = reinterpret_cast<float4*>(part_e + key * kDP + wg * 32);
+      float* pr = part_e + key * kDP + wg * 32;
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        pr[i] = make_float4(__uint_as_float(a[4 * i]) * f_main, __uint_as_float(a[4 * i + 1]) * f_main,
-                            __uint_as_float(a[4 * i + 2]) * f_main, __uint_as_float(a[4 * i + 3]) * f_main);
+      for (int i = 0; i < 4; ++i)
+        st_global_v8(pr + 8 * i, __uint_as_float(a[8 * i]) * f_main, __uint_as_float(a[8 * i + 1]) * f_main,
+                     __uint_as_float(a[8 * i + 2]) * f_main, __uint_as_float(a[8 * i + 3]) * f_main,
+                     __uint_as_float(a[8 * i + 4]) * f_main, __uint_as_float(a[8 * i + 5]) * f_main,
+                     __uint_as_float(a[8 * i + 6]) * f_main, __uint_as_float(a[8 * i + 7]) * f_main);
     }
     if (page_ok) finish_dpk(threadIdx.x, 32 * kSoftWarps, 1);  // the softmax warps: threads 0-255
+    if (staged && threadIdx.x == 0) bulk_wait_group_read0();  // the boxes are read before the CTA's memory goes
   }
   tc_fence_before();
   __syncthreads();
@@ -558,7 +613,7 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
                              float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st) {
   // tensors of their true width d (dp); the 64-column boxes read zeros past
   // the edge at d = 64 (dp = 32)
-  CUtensorMap qm, dom, pqm, km, vm, pkm;
+  CUtensorMap qm, dom, pqm, km, vm, pkm, dkm, dvm;
   const uint64_t d = static_cast<uint64_t>(p->d), dp = static_cast<uint64_t>(p->dp);
   const uint64_t qdims[3] = {d, static_cast<uint64_t>(p->hq), static_cast<uint64_t>(p->total_q)};
   const uint64_t qstr[2] = {d * 2, static_cast<uint64_t>(p->hq) * d * 2};
@@ -570,17 +625,22 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   const uint32_t kbox[2] = {64, 128};
   const uint64_t pkdims[2] = {dp, static_cast<uint64_t>(p->num_pages) * 128};
   const uint64_t pkstr[1] = {dp * 2};
+  // dK / dV pages, fp32 [num_pages * Hkv * 128][d]: 32-column boxes of 128 rows
+  const uint64_t gstr[1] = {d * 4};
+  const uint32_t gbox[2] = {32, 128};
   if (!encode_tensor_map(&qm, 3, q, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&dom, 3, dout, qdims, qstr, qbox, 1, 128) ||
       !encode_tensor_map(&pqm, 3, pq, pqdims, pqstr, qbox, 1, 128) ||
       !encode_tensor_map(&km, 2, k_pages, kdims, kstr, kbox, 1, 128) ||
       !encode_tensor_map(&vm, 2, v_pages, kdims, kstr, kbox, 1, 128) ||
-      !encode_tensor_map(&pkm, 2, pk_pages, pkdims, pkstr, kbox, 1, 128))
+      !encode_tensor_map(&pkm, 2, pk_pages, pkdims, pkstr, kbox, 1, 128) ||
+      !encode_tensor_map(&dkm, 2, dk, kdims, gstr, gbox, 2, 128) ||
+      !encode_tensor_map(&dvm, 2, dv, kdims, gstr, gbox, 2, 128))
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
   const int smem = DkvSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
-      qm, dom, pqm, km, vm, pkm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
+      qm, dom, pqm, km, vm, pkm, dkm, dvm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
       dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), p->d,
       p->dp, kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");

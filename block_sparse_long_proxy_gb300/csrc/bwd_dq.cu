@@ -2,22 +2,27 @@
 // gradient dpq of block-sparse GQA attention with the KL-coupled proxy
 // (Flash-MSA article, backward-pass paragraph), on the tcgen05 tensor cores.
 //
-// One CTA per (query tile t, head h of group g).  Q_h is copied into tensor
-// memory once, dO_h stays in shared memory, and the tile's cached blocks
-// stream through TMA rings (K three stages, V and pk two).  Per block j:
+// One CTA per (query tile t, proxy head p): it runs the G = Hq/Hp query
+// heads that use p's cached blocks one after the other.  Each head's Q_h is
+// copied into tensor memory, dO_h stays in shared memory, and the tile's
+// cached blocks stream through TMA rings (K three stages, V and pk two),
+// one continuous stream over the G heads.  Per head h and block j:
 //   S  = Q_h . K_j^T (Q from TMEM)   dP = dO_h . V_j^T        (M = rows, N = 128 keys)
 //   P  = exp2(S sl2 - lse2) (masked)   dS = P * (dP - D)
 //   dQ += dS . K_j       dpq += P . pk_j                     (dS, P from TMEM)
-// The products use N = 128 and take Q from tensor memory.  Blocks are
-// pipelined through split handoffs: the softmax hands P over before dS, and
-// the MMA thread issues S of block j+1 right after dpq of block j and dP of
-// j+1 right after dQ of j, so the tensor pipe has work while the softmax
-// runs (its two warpgroups split the 128 keys).
-// At the end dQ / sqrt(d) is stored, and dpq * (-w / (G sqrt(dp))) goes to
-// this head's slot of a scratch array; the G = Hq/Hp heads that use one
-// proxy head's blocks each count themselves on a per-(tile, proxy head)
-// counter, and the last to do so adds the G partials, in head order, to the
-// proxy term the prep kernel stored first: the sum is the same on every run.
+// Blocks are pipelined through split handoffs: the softmax hands P over
+// before dS, and the MMA thread issues S of block j+1 right after dpq of
+// block j and dP of j+1 right after dQ of j, so the tensor pipe has work
+// while the softmax runs (its two warpgroups split the 128 keys).
+// After each head dQ / sqrt(d) is stored.  dpq accumulates over all G heads
+// in tensor memory (the pk rows are the same for the G heads), and at the
+// end dpq * (-w / (G sqrt(dp))) is added to the proxy term the prep kernel
+// stored: no partial sums leave the CTA and the order of the sum is fixed.
+//
+// Head switches: Q of the next head goes into the K stage of the previous
+// head's last block; the next head's first two blocks are loaded while the
+// previous head finishes, and its Q and dO once the previous head's
+// products are done (dO's shared memory is theirs until then).
 //
 // Tensor memory: S 128 | dP 128 | dQ 128 | dpq 64 | Q 64 columns.  Warpgroup
 // w owns keys 64w..64w+63 and writes its bf16 pairs into the first 32 of
@@ -32,11 +37,10 @@ namespace msa {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kDP = 64;
 // K, V and pk of a block stream through rings of their own: V is read by
 // dP and pk by dpq early in a block's turn, K last (by dQ), so K's ring is
-// one deeper (its third stage is Q's shared memory, free once Q is in
-// tensor memory)
+// one deeper (one of its stages holds a head's Q until Q is in tensor
+// memory)
 constexpr int kKStages = 3;
 constexpr int kVStages = 2;
 constexpr int kSoftWarps = 8;
@@ -48,15 +52,30 @@ constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256, kColDPQ = 384, kColQ =
 struct DqSmem {
   static constexpr int kDOOff = 0;                                  // dO_h: 2 x [128 rows][128 B]
   static constexpr int kKOff = 32768;                               // K ring: kKStages x 32 KB
-  static constexpr int kQOff = kKOff + 2 * 32768;                   // Q_h, at first, in K's third stage
   static constexpr int kVOff = kKOff + kKStages * 32768;            // V ring: kVStages x 32 KB
   static constexpr int kPkOff = kVOff + kVStages * 32768;           // pk ring: kVStages x 16 KB
   static constexpr int kBarOff = kPkOff + kVStages * 16384;
-  static constexpr int kFlagOff = kBarOff + 8 * 24;  // the dpq reduction's "last" flag
-  static constexpr int kBytes = kFlagOff + 16;
+  static constexpr int kNbOff = kBarOff + 8 * 24;  // the tile's cached block count
+  static constexpr int kBytes = kNbOff + 16;
 };
 
 __device__ __forceinline__ bool valid_block(int j, int nvp) { return j >= 0 && j < nvp; }
+
+// 64 fp32 values times s, from registers to a 32-byte aligned row: full
+// 32-byte sectors
+__device__ __forceinline__ void store_row_v8(float* dst, const uint32_t (&a)[64], float s) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    st_global_v8(dst + 8 * i, __uint_as_float(a[8 * i]) * s, __uint_as_float(a[8 * i + 1]) * s,
+                 __uint_as_float(a[8 * i + 2]) * s, __uint_as_float(a[8 * i + 3]) * s,
+                 __uint_as_float(a[8 * i + 4]) * s, __uint_as_float(a[8 * i + 5]) * s,
+                 __uint_as_float(a[8 * i + 6]) * s, __uint_as_float(a[8 * i + 7]) * s);
+}
+
+// K stage that holds head hh's Q until it is in tensor memory: the stage of
+// the previous head's last block (stage 2 for the first head), never one of
+// the head's first two blocks
+__device__ __forceinline__ int q_stage(int hh, int nb) { return (hh * nb + 2) % kKStages; }
 
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap do_map,
@@ -64,26 +83,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const __grid_constant__ CUtensorMap pk_map, const TileInfo* __restrict__ tiles,
                      const int32_t* __restrict__ idx, const int32_t* __restrict__ kv_indices, int64_t num_pages,
                      const float* __restrict__ lse2t, const float* __restrict__ dsumt, float* __restrict__ dq,
-                     float* __restrict__ dpq, float* __restrict__ dpq_part, int32_t* __restrict__ dpq_cnt,
-                     int32_t hq, int32_t hkv, int32_t hsel, int32_t topk, int32_t total_q, int32_t d,
-                     int32_t dp, float kl_weight, uint32_t* err) {
+                     float* __restrict__ dpq, const int32_t* __restrict__ heavy_tiles, int32_t hq, int32_t hkv,
+                     int32_t hsel, int32_t topk, int32_t total_q, int32_t d, int32_t dp, float kl_weight,
+                     uint32_t* err) {
   using L = DqSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int t = blockIdx.x / hq, h = blockIdx.x % hq;
-  // head h reads KV head g and the blocks of proxy head ps; G heads share ps
-  const int G = hq / hsel, ps = h / G, g = h / (hq / hkv);
+  const int t = heavy_tiles[blockIdx.x / hsel], ps = blockIdx.x % hsel;  // heaviest tiles first
+  // the G heads ps*G .. ps*G+G-1 read KV head g and the blocks of proxy head ps
+  const int G = hq / hsel, g = ps / (hsel / hkv);
   const TileInfo tl = tiles[t];
   const int32_t* row_idx = idx + (static_cast<int64_t>(t) * hsel + ps) * topk;
 
-  uint8_t* q_s = smem + L::kQOff;
   uint8_t* do_s = smem + L::kDOOff;
   uint8_t* k_s = smem + L::kKOff;
   uint8_t* v_s = smem + L::kVOff;
   uint8_t* pk_s = smem + L::kPkOff;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* q_full = bars;
-  uint64_t* q_tm = bars + 1;                 // Q copied into tensor memory (its shared memory free)
+  uint64_t* q_full = bars;                   // Q_h and dO_h loaded
+  uint64_t* q_tm = bars + 1;                 // Q_h copied into tensor memory (its K stage free)
   uint64_t* k_full = bars + 2;               // [kKStages]
   uint64_t* k_empty = k_full + kKStages;     // [kKStages]
   uint64_t* v_full = k_empty + kKStages;     // [kVStages]
@@ -94,8 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = s_full + 1;           // P written (bf16, over S)
   uint64_t* dp_full = p_full + 1;          // dP computed
   uint64_t* ds_full = dp_full + 1;         // dS written (bf16, over dP)
-  uint64_t* done = ds_full + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  uint64_t* done = ds_full + 1;            // a head's products complete
+  uint64_t* dq_free = done + 1;            // a head's dQ read out of tensor memory
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dq_free + 1);
+  int32_t* nb_s = reinterpret_cast<int32_t*>(smem + L::kNbOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -121,7 +141,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_full, 1);
     mbar_init(ds_full, kSoftWarps);
     mbar_init(done, 1);
+    mbar_init(dq_free, kSoftWarps);
     fence_mbar_init();
+  }
+  if (warp == 8) {  // the tile's cached blocks (the same for the G heads)
+    int c = 0;
+    for (int k = lane; k < topk; k += 32) c += valid_block(row_idx[k], tl.nvp) ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if (lane == 0) *nb_s = c;
   }
   if (warp == 9) {
     tmem_alloc(tmem_slot, 512);
@@ -131,35 +159,77 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int nb = *nb_s;
 
-  if (warp == 8) {
+  if (nb == 0) {
+    // no cached block: dQ = 0 for the G heads; dpq keeps the proxy term
+    if (warp < kSoftWarps) {
+      const int wg = warp >> 2, r = (warp & 3) * 32 + lane;
+      if (r < tl.rows && wg * 64 < d)
+        for (int hh = 0; hh < G; ++hh) {
+          float4* dqr = reinterpret_cast<float4*>(
+              dq + (static_cast<int64_t>(tl.q_begin + r) * hq + ps * G + hh) * d + wg * 64);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) dqr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+  } else if (warp == 8) {
     // ---------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_expect_tx(q_full, 65536);
-      for (int c = 0; c < 2; ++c) {
-        tma_load_3d(q_s + c * 16384, &q_map, q_full, c * 64, h, tl.q_begin);
-        tma_load_3d(do_s + c * 16384, &do_map, q_full, c * 64, h, tl.q_begin);
-      }
-      int it = 0;
-      for (int k = 0; k < topk; ++k) {
-        const int j = row_idx[k];
-        if (!valid_block(j, tl.nvp)) continue;
+      bool ok = true;
+      int pend = -1;  // head whose Q sits in a K stage and is not yet known to be in tensor memory
+      // confirms the pending Q copy, at the latest before the next head's Q
+      // load (so that q_tm never runs two phases ahead of this wait)
+      auto confirm_q = [&]() -> bool {
+        if (pend < 0) return true;
+        const bool r = mbar_wait(q_tm, pend & 1, err);
+        pend = -1;
+        return r;
+      };
+      auto load_qd = [&](int hh) -> bool {
+        if (!confirm_q()) return false;
+        if (hh > 0 && !mbar_wait(done, (hh - 1) & 1, err)) return false;  // dO and Q's stage free
+        const int h = ps * G + hh;
+        uint8_t* q_s = k_s + q_stage(hh, nb) * 32768;
+        mbar_expect_tx(q_full, 65536);
+        for (int c = 0; c < 2; ++c) {
+          tma_load_3d(q_s + c * 16384, &q_map, q_full, c * 64, h, tl.q_begin);
+          tma_load_3d(do_s + c * 16384, &do_map, q_full, c * 64, h, tl.q_begin);
+        }
+        pend = hh;
+        return true;
+      };
+      // K, V and pk of the tile's block j as block gi of the stream
+      auto load_block = [&](int gi, int j) -> bool {
         int64_t page = kv_indices[tl.page_base + j];
         if (page < 0 || page >= num_pages) page = 0;  // reported by the prep kernel
         const int row = static_cast<int>((page * hkv + g) * 128);
-        // K (needed first, by S of the block), then V, then pk
-        const int ks = it % kKStages, vs = it % kVStages;
-        if (!mbar_wait(k_empty + ks, ((it / kKStages) & 1) ^ 1, err)) break;
-        if (it == kKStages - 1 && !mbar_wait(q_tm, 0, err)) break;  // K's third stage held Q
+        const int ks = gi % kKStages, vs = gi % kVStages;
+        if (!mbar_wait(k_empty + ks, ((gi / kKStages) & 1) ^ 1, err)) return false;
+        if (pend >= 0 && ks == q_stage(pend, nb) && !confirm_q()) return false;  // the stage holds Q
         mbar_expect_tx(k_full + ks, 32768);
         for (int c = 0; c < 2; ++c) tma_load_2d(k_s + ks * 32768 + c * 16384, &k_map, k_full + ks, c * 64, row);
-        if (!mbar_wait(v_empty + vs, ((it / kVStages) & 1) ^ 1, err)) break;
+        if (!mbar_wait(v_empty + vs, ((gi / kVStages) & 1) ^ 1, err)) return false;
         mbar_expect_tx(v_full + vs, 32768);
         for (int c = 0; c < 2; ++c) tma_load_2d(v_s + vs * 32768 + c * 16384, &v_map, v_full + vs, c * 64, row);
-        if (!mbar_wait(pk_empty + vs, ((it / kVStages) & 1) ^ 1, err)) break;
+        if (!mbar_wait(pk_empty + vs, ((gi / kVStages) & 1) ^ 1, err)) return false;
         mbar_expect_tx(pk_full + vs, 16384);
         tma_load_2d(pk_s + vs * 16384, &pk_map, pk_full + vs, 0, static_cast<int>(page * 128));
-        ++it;
+        return true;
+      };
+      // head hh's blocks: the first two before its Q and dO (from the second
+      // head on they stream in while the previous head finishes)
+      for (int hh = 0; ok && hh < G; ++hh) {
+        if (hh == 0) ok = load_qd(0);
+        int b = 0;
+        for (int k = 0; ok && k < topk; ++k) {
+          const int j = row_idx[k];
+          if (!valid_block(j, tl.nvp)) continue;
+          if (hh > 0 && b == 2 && !(ok = load_qd(hh))) break;
+          ok = load_block(hh * nb + b, j);
+          ++b;
+        }
+        if (ok && hh > 0 && b < 3) ok = load_qd(hh);  // a head of one or two blocks
       }
     }
   } else if (warp == 9) {
@@ -176,13 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pk_mn = smem_desc(smem_u32(pk_s), 16384, 1024, kSwizzle128);  // pk (dpq += P pk)
       const uint64_t do_km = smem_desc(smem_u32(do_s), 16, 1024, kSwizzle128);
       constexpr uint64_t kTile = 32768 >> 4, kPkTile = 16384 >> 4;
-      bool ok = mbar_wait(q_full, 0, err) && mbar_wait(q_tm, 0, err);
-      tc_fence_after();
-      int nb = 0;  // cached blocks of the tile
-      for (int k = 0; k < topk; ++k) nb += valid_block(row_idx[k], tl.nvp) ? 1 : 0;
-      auto sq = [&](int b) -> bool {  // S = Q . K^T (Q from tensor memory) of block b
-        const int ks = b % kKStages;
-        if (!mbar_wait(k_full + ks, (b / kKStages) & 1, err)) return false;
+      bool ok = true;
+      auto sq = [&](int gi) -> bool {  // S = Q . K^T (Q from tensor memory) of stream block gi
+        const int ks = gi % kKStages;
+        if (!mbar_wait(k_full + ks, (gi / kKStages) & 1, err)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(ks) * kTile;
 #pragma unroll
@@ -193,9 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full);
         return true;
       };
-      auto dpv = [&](int b) -> bool {  // dP = dO . V^T of block b, then V's stage is free
-        const int vs = b % kVStages;
-        if (!mbar_wait(v_full + vs, (b / kVStages) & 1, err)) return false;
+      auto dpv = [&](int gi) -> bool {  // dP = dO . V^T of stream block gi, then V's stage is free
+        const int vs = gi % kVStages;
+        if (!mbar_wait(v_full + vs, (gi / kVStages) & 1, err)) return false;
         tc_fence_after();
         const uint64_t so = static_cast<uint64_t>(vs) * kTile;
 #pragma unroll
@@ -211,33 +278,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       // i has taken P out of the S columns, and dP of i+1 as soon as dQ of i
       // has taken dS out of the dP columns, so the softmax computes P of i+1
       // while dQ of i runs and dS of i+1 while dpq of i+1 runs.
-      if (nb > 0) ok = ok && sq(0) && dpv(0);
-      for (int it = 0; ok && it < nb; ++it) {
-        const bool next = it + 1 < nb;
-        const int vs = it % kVStages, ks = it % kKStages;
-        if (!(ok = mbar_wait(p_full, it & 1, err))) break;
-        if (!(ok = mbar_wait(pk_full + vs, (it / kVStages) & 1, err))) break;
+      for (int hh = 0; ok && hh < G; ++hh) {
+        const int base = hh * nb;
+        ok = mbar_wait(q_full, hh & 1, err) && mbar_wait(q_tm, hh & 1, err);  // dO_h in smem, Q_h in TMEM
         tc_fence_after();
-        const uint64_t po = static_cast<uint64_t>(vs) * kPkTile;
+        ok = ok && sq(base) && dpv(base);
+        for (int b = 0; ok && b < nb; ++b) {
+          const int gi = base + b;
+          const bool next = b + 1 < nb;
+          const int vs = gi % kVStages, ks = gi % kKStages;
+          if (!(ok = mbar_wait(p_full, gi & 1, err))) break;
+          if (!(ok = mbar_wait(pk_full + vs, (gi / kVStages) & 1, err))) break;
+          tc_fence_after();
+          const uint64_t po = static_cast<uint64_t>(vs) * kPkTile;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
-          mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + po + kk * 128, id_p, it > 0 || kk > 0);
-        }
-        mma_commit(pk_empty + vs);
-        if (next && !(ok = sq(it + 1))) break;
-        if (!(ok = mbar_wait(ds_full, it & 1, err))) break;
-        tc_fence_after();
-        const uint64_t so = static_cast<uint64_t>(ks) * kTile;
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;  // warpgroup kk/4 packed its keys there
+            mma_ts(tmem + kColDPQ, tmem + kColS + a_col, pk_mn + po + kk * 128, id_p, gi > 0 || kk > 0);
+          }
+          mma_commit(pk_empty + vs);
+          if (next && !(ok = sq(gi + 1))) break;
+          if (!(ok = mbar_wait(ds_full, gi & 1, err))) break;
+          // the head's first dQ overwrites the previous head's, once read out
+          if (b == 0 && hh > 0 && !(ok = mbar_wait(dq_free, (hh - 1) & 1, err))) break;
+          tc_fence_after();
+          const uint64_t so = static_cast<uint64_t>(ks) * kTile;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;
-          mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, it > 0 || kk > 0);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t a_col = (kk >> 2) * 64 + (kk & 3) * 8;
+            mma_ts(tmem + kColDQ, tmem + kColDP + a_col, k_mn + so + kk * 128, id_q, b > 0 || kk > 0);
+          }
+          mma_commit(k_empty + ks);
+          if (next && !(ok = dpv(gi + 1))) break;
         }
-        mma_commit(k_empty + ks);
-        if (next && !(ok = dpv(it + 1))) break;
+        mma_commit(done);
       }
-      mma_commit(done);
     }
   } else {
     // ----------------------------------------------------------- softmax
@@ -247,171 +322,135 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool row_ok = r < tl.rows;
     const int qpos = tl.pos0 + r;
-    const int64_t ei = static_cast<int64_t>(h) * total_q + tl.q_begin + r;
-    const float l2 = row_ok ? lse2t[ei] : 0.f;
-    const float dd = row_ok ? dsumt[ei] : 0.f;
+    const int64_t q_row = tl.q_begin + r;
     const float sl2 = kLog2e * rsqrtf(static_cast<float>(d));
-    bool ok = mbar_wait(q_full, 0, err);
-    {  // Q_h row r, d in [64 wg, 64 wg + 64), into tensor memory as bf16 pairs
-      const uint8_t* qrow = q_s + wg * 16384 + r * 128;
-      uint32_t qv[32];
+    const float qsc = rsqrtf(static_cast<float>(d));
+    bool ok = true;
+    for (int hh = 0; hh < G; ++hh) {
+      const int h = ps * G + hh, base = hh * nb;
+      const int64_t ei = static_cast<int64_t>(h) * total_q + q_row;
+      const float l2 = row_ok ? lse2t[ei] : 0.f;
+      const float dd = row_ok ? dsumt[ei] : 0.f;
+      if (ok) ok = mbar_wait(q_full, hh & 1, err);
+      ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM stores below are warp-collective
+      if (!ok) break;
+      {  // Q_h row r, d in [64 wg, 64 wg + 64), into tensor memory as bf16 pairs
+        const uint8_t* qrow = k_s + q_stage(hh, nb) * 32768 + wg * 16384 + r * 128;
+        uint32_t qv[32];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
-        qv[4 * u] = v.x;
-        qv[4 * u + 1] = v.y;
-        qv[4 * u + 2] = v.z;
-        qv[4 * u + 3] = v.w;
-      }
-      tmem_st16(lane_base + kColQ + 32 * wg, qv);
-      tmem_st16(lane_base + kColQ + 32 * wg + 16, qv + 16);
-      tmem_wait_st();
-      tc_fence_before();
-      fence_async_shared();  // Q's shared memory is K's third stage next: TMA writes follow these reads
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_tm);
-    }
-    int it = 0;
-    for (int k = 0; ok && k < topk; ++k) {
-      const int j = row_idx[k];
-      if (!valid_block(j, tl.nvp)) continue;
-      if (!(ok = mbar_wait(s_full, it & 1, err))) break;
-      tc_fence_after();
-      const int kbase = j * 128 + kc0;
-      const bool need_mask = j * 128 + 127 > tl.pos0 || tl.rows < 128;  // diagonal block or ragged tile
-      // P first (dpq needs only P; dP may still be running), then dS
-      float pr[64];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {  // 32 keys at a time; packed pairs land in columns already read
-        uint32_t sv[32], pa[16];
-        tmem_ld32(lane_base + kColS + kc0 + 32 * c, sv);
-        tmem_wait_ld();
-        if (!need_mask) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float x0, x1;
-            ffma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, -l2);
-            pr[32 * c + i] = ex2_approx(x0);
-            pr[32 * c + i + 1] = ex2_approx(x1);
-            pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            const int kp = kbase + 32 * c + i;
-            const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
-            pr[32 * c + i] = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
-            pr[32 * c + i + 1] = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
-            pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
-          }
+        for (int u = 0; u < 8; ++u) {
+          const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((u ^ (r & 7)) << 4));
+          qv[4 * u] = v.x;
+          qv[4 * u + 1] = v.y;
+          qv[4 * u + 2] = v.z;
+          qv[4 * u + 3] = v.w;
         }
-        tmem_st16(lane_base + kColS + kc0 + 16 * c, pa);
+        tmem_st16(lane_base + kColQ + 32 * wg, qv);
+        tmem_st16(lane_base + kColQ + 32 * wg + 16, qv + 16);
+        tmem_wait_st();
+        tc_fence_before();
+        fence_async_shared();  // Q's shared memory is a K stage next: TMA writes follow these reads
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_tm);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-      if (!(ok = mbar_wait(dp_full, it & 1, err))) break;
-      tc_fence_after();
+      int b = 0;
+      for (int k = 0; ok && k < topk; ++k) {
+        const int j = row_idx[k];
+        if (!valid_block(j, tl.nvp)) continue;
+        const int gi = base + b;
+        if (!(ok = mbar_wait(s_full, gi & 1, err))) break;
+        tc_fence_after();
+        const int kbase = j * 128 + kc0;
+        const bool need_mask = j * 128 + 127 > tl.pos0 || tl.rows < 128;  // diagonal block or ragged tile
+        // P first (dpq needs only P; dP may still be running), then dS
+        float pr[64];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t dv_[32], da[16];
-        tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float t0, t1, d0, d1;
-          fadd2v(t0, t1, __uint_as_float(dv_[i]), __uint_as_float(dv_[i + 1]), -dd, -dd);
-          fmul2(d0, d1, t0, t1, pr[32 * c + i], pr[32 * c + i + 1]);
-          da[i >> 1] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
-      ++it;
-    }
-    if (ok) ok = mbar_wait(done, 0, err);
-    tc_fence_after();
-    ok = __all_sync(0xFFFFFFFFu, ok);  // the TMEM loads below are warp-collective
-    // tcgen05.ld is warp-collective: every lane loads, only valid rows store
-    if (ok) {
-      const int64_t q_row = tl.q_begin + r;
-      float* dqr = dq + (q_row * hq + h) * d + wg * 64;
-      const float qs = rsqrtf(static_cast<float>(d));
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t a[32];
-        if (it > 0) {
-          tmem_ld32(lane_base + kColDQ + wg * 64 + c * 32, a);
+        for (int c = 0; c < 2; ++c) {  // 32 keys at a time; packed pairs land in columns already read
+          uint32_t sv[32], pa[16];
+          tmem_ld32(lane_base + kColS + kc0 + 32 * c, sv);
           tmem_wait_ld();
-        } else {
+          if (!need_mask) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) a[i] = 0u;
+            for (int i = 0; i < 32; i += 2) {
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]), sl2, -l2);
+              pr[32 * c + i] = ex2_approx(x0);
+              pr[32 * c + i + 1] = ex2_approx(x1);
+              pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const int kp = kbase + 32 * c + i;
+              const bool ok0 = row_ok && kp <= qpos, ok1 = row_ok && kp + 1 <= qpos;
+              pr[32 * c + i] = ok0 ? ex2_approx(__uint_as_float(sv[i]) * sl2 - l2) : 0.f;
+              pr[32 * c + i + 1] = ok1 ? ex2_approx(__uint_as_float(sv[i + 1]) * sl2 - l2) : 0.f;
+              pa[i >> 1] = pack_bf16x2(pr[32 * c + i], pr[32 * c + i + 1]);
+            }
+          }
+          tmem_st16(lane_base + kColS + kc0 + 16 * c, pa);
         }
-        if (row_ok && wg * 64 < d)  // at d = 64 the second warpgroup's columns are padding
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
+        if (!(ok = mbar_wait(dp_full, gi & 1, err))) break;
+        tc_fence_after();
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            reinterpret_cast<float4*>(dqr + c * 32)[i] =
-                make_float4(__uint_as_float(a[4 * i]) * qs, __uint_as_float(a[4 * i + 1]) * qs,
-                            __uint_as_float(a[4 * i + 2]) * qs, __uint_as_float(a[4 * i + 3]) * qs);
+        for (int c = 0; c < 2; ++c) {
+          uint32_t dv_[32], da[16];
+          tmem_ld32(lane_base + kColDP + kc0 + 32 * c, dv_);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float t0, t1, d0, d1;
+            fadd2v(t0, t1, __uint_as_float(dv_[i]), __uint_as_float(dv_[i + 1]), -dd, -dd);
+            fmul2(d0, d1, t0, t1, pr[32 * c + i], pr[32 * c + i + 1]);
+            da[i >> 1] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(lane_base + kColDP + kc0 + 16 * c, da);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ds_full);
+        ++b;
       }
+      // the head's dQ: read out of tensor memory (the next head's dQ may then
+      // start), then stored while the next head's Q and dO load
+      if (ok) ok = mbar_wait(done, hh & 1, err);
+      tc_fence_after();
+      ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is warp-collective: every lane loads, valid rows store
+      if (!ok) break;
+      uint32_t a[64];
+      tmem_ld32(lane_base + kColDQ + wg * 64, a);
+      tmem_ld32(lane_base + kColDQ + wg * 64 + 32, a + 32);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && hh + 1 < G) mbar_arrive(dq_free);
+      // at d = 64 the second warpgroup's columns are padding
+      if (row_ok && wg * 64 < d) store_row_v8(dq + (q_row * hq + h) * d + wg * 64, a, qsc);
     }
-    // this head's dpq partial (every row of the tile's slot, zeros without
-    // blocks), then the count; the last head of the proxy head sums
-    {
+    // dpq: the main term over the G heads, added to the proxy term the prep
+    // kernel stored (the last head's products are complete: waited above)
+    if (ok) {
       const float f = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
       uint32_t a[32];
-      if (ok && it > 0) {
-        tmem_ld32(lane_base + kColDPQ + wg * 32, a);
-        tmem_wait_ld();
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) a[i] = 0u;
-      }
-      float4* part = reinterpret_cast<float4*>(dpq_part + ((static_cast<int64_t>(t) * hq + h) * 128 + r) * kDP + wg * 32);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        part[i] = make_float4(__uint_as_float(a[4 * i]) * f, __uint_as_float(a[4 * i + 1]) * f,
-                              __uint_as_float(a[4 * i + 2]) * f, __uint_as_float(a[4 * i + 3]) * f);
-    }
-    // every thread's partial is ordered before thread 0's release; its
-    // acquire (in the last head's CTA) orders the sum's reads after every
-    // head's release
-    __threadfence();
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
-    int32_t* const flag = reinterpret_cast<int32_t*>(smem + L::kFlagOff);
-    if (threadIdx.x == 0) {
-      int32_t prev;
-      asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                   : "=r"(prev)
-                   : "l"(dpq_cnt + static_cast<int64_t>(t) * hsel + ps)
-                   : "memory");
-      *flag = prev == G - 1;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kSoftWarps) : "memory");
-    if (*flag && row_ok && wg * 32 < dp) {  // at dp = 32 the second warpgroup's columns are padding
-      const int64_t q_row = tl.q_begin + r;
-      float4* dpr = reinterpret_cast<float4*>(dpq + (q_row * hsel + ps) * dp + wg * 32);
-      float4 acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = __ldcg(dpr + i);
-      for (int hh = 0; hh < G; ++hh) {
-        const float4* src = reinterpret_cast<const float4*>(
-            dpq_part + ((static_cast<int64_t>(t) * hq + ps * G + hh) * 128 + r) * kDP + wg * 32);
+      tmem_ld32(lane_base + kColDPQ + wg * 32, a);
+      tmem_wait_ld();
+      if (row_ok && wg * 32 < dp) {  // at dp = 32 the second warpgroup's columns are padding
+        float4* dpr = reinterpret_cast<float4*>(dpq + (q_row * hsel + ps) * dp + wg * 32);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 v = __ldcg(src + i);
-          acc[i].x += v.x;
-          acc[i].y += v.y;
-          acc[i].z += v.z;
-          acc[i].w += v.w;
+          float4 v = dpr[i];
+          v.x += __uint_as_float(a[4 * i]) * f;
+          v.y += __uint_as_float(a[4 * i + 1]) * f;
+          v.z += __uint_as_float(a[4 * i + 2]) * f;
+          v.w += __uint_as_float(a[4 * i + 3]) * f;
+          dpr[i] = v;
         }
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) dpr[i] = acc[i];
     }
   }
   tc_fence_before();
@@ -424,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
-                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float* dpq_part,
-                            int32_t* dpq_cnt, float kl_weight, cudaStream_t st) {
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
+                            cudaStream_t st) {
   // tensors of their true width d (dp); the 64-column boxes read zeros past
   // the edge at d = 64 (dp = 32)
   CUtensorMap qm, dom, km, vm, pkm;
@@ -446,9 +485,11 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
   const int smem = DqSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_dq_tc_kernel<<<p->n_tiles * p->hq, kThreads, smem, st>>>(
-      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq, dpq_part, dpq_cnt, p->hq,
-      p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), p->d, p->dp, kl_weight, p->err_d);
+  // one CTA per (tile, proxy head), looping over the proxy head's query heads
+  bwd_dq_tc_kernel<<<p->n_tiles * p->hp, kThreads, smem, st>>>(
+      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq,
+      p->aux_d + p->heavy_tiles_off, p->hq, p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), p->d, p->dp,
+      kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
 }
 

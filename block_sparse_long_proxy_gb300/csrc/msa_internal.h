@@ -81,6 +81,7 @@ struct msa_plan_s {
   int32_t n_attn_units = 0;
   int64_t proxy_attn_units_off = 0;  // backward proxy softmax work units
   int32_t n_proxy_attn_units = 0;
+  int64_t heavy_tiles_off = 0;       // tile ids, most cached blocks first (the backward's dq order)
   int32_t n_page_entries = 0;        // sum over sequences of ceil(kv_len / 128)
   void* bwd_d = nullptr;             // backward scratch (D, proxy LSE, inverse index)
 };
@@ -120,12 +121,12 @@ size_t fused_topk_counter_bytes(const msa_plan_s* p);  // leading part that star
 // (bf16 [total_q, Hp, 64]) and its natural-log LSE ([total_q, Hp]).
 msa_status launch_proxy_softmax(const msa_plan_s* p, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                                 const int32_t* idx, void* op, float* lse, cudaStream_t st);
-// dQ and dpq's main term on the tensor cores (bwd_dq.cu); dpq_part is
-// [n_tiles][hq][128][64] fp32 scratch, dpq_cnt [n_tiles][hp] int32 zeroed.
+// dQ and dpq's main term on the tensor cores (bwd_dq.cu); dpq holds the
+// proxy term on entry and gets the main term added.
 msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                             const void* dout, const void* pk_pages, const int32_t* idx, const int32_t* kv_indices,
-                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float* dpq_part,
-                            int32_t* dpq_cnt, float kl_weight, cudaStream_t st);
+                            const float* lse2t, const float* dsumt, float* dq, float* dpq, float kl_weight,
+                            cudaStream_t st);
 // dK, dV and dpk on the tensor cores (bwd_dkv.cu); lse2t, dsumt, lsept are
 // the row statistics written by the prep kernel, [heads][total_q]; dpk_part
 // is [page-table entries][hkv][128][64] fp32 scratch, dpk_cnt [entries]
@@ -180,6 +181,7 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
                            float* dpq, float* dpk, cudaStream_t st);
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+// dtype_bf16_or_u8: 0 uint8, 1 bf16, 2 fp32.
 bool encode_tensor_map(void* map, int rank, const void* base, const uint64_t* dims,
                        const uint64_t* strides_bytes, const uint32_t* box, int dtype_bf16_or_u8,
                        int swizzle_bytes);

@@ -133,6 +133,11 @@ __device__ __forceinline__ void tma_store_3d(const void* map, const void* src, i
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const void* map, const void* src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared memory of every committed bulk store has been read
 __device__ __forceinline__ void bulk_wait_group_read0() {
@@ -371,6 +376,27 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
+}
+// Named barrier `id` over n threads that also returns the AND of p over them.
+__device__ __forceinline__ bool bar_sync_and(int id, int n, bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, %2, %3, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(p)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
+}
+// One 32-byte global store of eight consecutive fp32 values (a full L2
+// sector); p must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(float* p, float a0, float a1, float a2, float a3, float a4, float a5,
+                                             float a6, float a7) {
+  asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "f"(a0), "f"(a1), "f"(a2),
+               "f"(a3), "f"(a4), "f"(a5), "f"(a6), "f"(a7)
+               : "memory");
 }
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;

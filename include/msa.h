@@ -317,6 +317,8 @@ msa_status msa_sparse_attn(msa_plan_t plan, const void* q, const void* k_pages, 
  *                    untouched)
  *  dpq               fp32 [total_q, Hp, dp]           (output, overwritten)
  *  dpk_pages         fp32 [num_pages, 1, 128, dp]     (output, as dk_pages)
+ * q, k_pages, v_pages, out, dout, pq and pk_pages must be 16-byte aligned and
+ * the five gradients 32-byte aligned (MSA_ERR_INVALID_ARG otherwise).
  */
 msa_status msa_sparse_attn_bwd(msa_plan_t plan, const void* q, const void* k_pages,
                                const void* v_pages, const int32_t* kv_indices,

@@ -168,3 +168,28 @@ def test_bwd_narrow_heads(cuda_dev, case, w):
     for name, shape in (("dq", (case.total_q, case.hq, case.d)), ("dpq", (case.total_q, case.hp, case.dp))):
         assert got[name].shape == shape, name
     _check_all(got, ref)
+
+
+def test_bwd_refuses_misaligned_gradients(cuda_dev):
+    """The gradients are written with 32-byte stores: a buffer that is only
+    16-byte aligned is refused on the host (MSA_ERR_INVALID_ARG) and nothing
+    is launched."""
+    from block_sparse_long_proxy_gb300 import msa
+    case = synth.Case("align", [256], [256], 4, 2, 128, 2, 64, 2)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    idx = torch.from_numpy(random_idx(case, np.random.default_rng(0))).to(cuda_dev)
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx)
+    n = inp["q"].numel()
+    buf = torch.zeros(n + 8, dtype=torch.float32, device=cuda_dev)
+    grads = dict(dq=buf[4:4 + n].view(inp["q"].shape),  # 16 bytes past a 256-byte boundary
+                 dk=torch.zeros(inp["k_pages"].shape, dtype=torch.float32, device=cuda_dev),
+                 dv=torch.zeros(inp["v_pages"].shape, dtype=torch.float32, device=cuda_dev),
+                 dpq=torch.zeros(inp["pq"].shape, dtype=torch.float32, device=cuda_dev),
+                 dpk=torch.zeros(inp["pk_pages"].shape, dtype=torch.float32, device=cuda_dev))
+    with pytest.raises(msa.MsaError) as e:
+        plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx, out, lse,
+                             inp["dout"], inp["pq"], inp["pk_pages"], grads=grads)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert (buf == 0).all()

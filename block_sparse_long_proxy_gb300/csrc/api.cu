@@ -276,6 +276,7 @@ msa_status msa_plan(const int32_t* qo_lens, const int32_t* kv_lens, int32_t batc
   std::vector<int32_t> aux;
   proxy_plan_tables(p, aux);
   attn_plan_tables(p, aux);
+  bwd_plan_tables(p, aux);
 
   // device block: tiles | nvp | error word | aux tables | decode partials |
   // backward scratch | fused top-k counters and candidates

@@ -724,15 +724,6 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   p->n_proxy_attn_units = static_cast<int32_t>(ps.size());
   raw = reinterpret_cast<const int32_t*>(ps.data());
   aux.insert(aux.end(), raw, raw + ps.size() * 4);
-  // the tiles, heaviest first (the backward's dq CTAs, one per tile and
-  // proxy head, run the most blocks first so the last wave is the lightest)
-  std::vector<int32_t> order(p->n_tiles);
-  for (int t = 0; t < p->n_tiles; ++t) order[t] = t;
-  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
-    return std::min(p->tiles[a].nvp, p->topk) > std::min(p->tiles[b].nvp, p->topk);
-  });
-  p->heavy_tiles_off = static_cast<int64_t>(aux.size());
-  aux.insert(aux.end(), order.begin(), order.end());
 }
 
 namespace {

@@ -46,6 +46,7 @@
 #include "ptx.cuh"
 
 #include <algorithm>
+#include <vector>
 
 namespace msa {
 namespace {
@@ -221,6 +222,19 @@ __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_
 }
 
 }  // namespace
+
+// The backward's plan table: the tiles, heaviest first (the dq CTAs, one
+// per tile and proxy head, run the most blocks first so the last wave is
+// the lightest).
+void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
+  std::vector<int32_t> order(p->n_tiles);
+  for (int t = 0; t < p->n_tiles; ++t) order[t] = t;
+  std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
+    return std::min(p->tiles[a].nvp, p->topk) > std::min(p->tiles[b].nvp, p->topk);
+  });
+  p->heavy_tiles_off = static_cast<int64_t>(aux.size());
+  aux.insert(aux.end(), order.begin(), order.end());
+}
 
 // The backward scratch, each part 256-byte aligned: dsumt, lse2t ([Hq][total_q]
 // fp32), lsept ([Hp][total_q] fp32), the proxy softmax's Op (bf16 [total_q,

@@ -114,6 +114,7 @@ msa_status cuda_check(cudaError_t e, const char* what);
 // ---- plan-time tables (host), appended to the plan's aux array ----
 void proxy_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
+void bwd_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux);
 size_t bwd_scratch_bytes(const msa_plan_s* p);
 size_t fused_topk_scratch_bytes(const msa_plan_s* p);  // 0 when msa_proxy_topk is unsupported
 size_t fused_topk_counter_bytes(const msa_plan_s* p);  // leading part that starts at zero

@@ -35,6 +35,10 @@ SMALL = [
                 page_perm_seed=3, extra_pages=2), 0.5),
     (synth.Case("G=1", [384], [384], 2, 2, 128, 2, 64, 2, page_perm_seed=1), 1.0),
     (synth.Case("long rows topk 16", [2048], [2048], 8, 2, 128, 2, 64, 16, page_perm_seed=5), 1.0),
+    # dq runs the G heads of a proxy head in one CTA: G = 3 and G = 2 (Hp = 2 Hkv), with tiles of one,
+    # two and more cached blocks (the head's Q sits in a different K stage for each)
+    (synth.Case("G=3 ragged", [300, 129, 77], [900, 129, 333], 6, 2, 128, 2, 64, 3, page_perm_seed=9), 0.9),
+    (synth.Case("G=2 Hp=2Hkv", [640, 200], [640, 700], 8, 2, 128, 4, 64, 5, page_perm_seed=10), 1.0),
 ]
 
 

@@ -183,8 +183,16 @@ __global__ void __launch_bounds__(1024) bwd_scan_kernel(const int32_t* __restric
   __shared__ int32_t part[1024];
   const int per = (n + 1023) / 1024;
   const int b = threadIdx.x * per, e = min(n, b + per);
+  // a list longer than the key-side kernel sorts in shared memory gets a
+  // power-of-two capacity (at most twice its length) to be sorted in place
+  auto cap = [](int c) {
+    if (c <= kBwdSmemList) return c;
+    int p2 = 1;
+    while (p2 < c) p2 <<= 1;
+    return p2;
+  };
   int s = 0;
-  for (int i = b; i < e; ++i) s += count[i];
+  for (int i = b; i < e; ++i) s += cap(count[i]);
   part[threadIdx.x] = s;
   __syncthreads();
   for (int o = 1; o < 1024; o <<= 1) {
@@ -197,7 +205,7 @@ __global__ void __launch_bounds__(1024) bwd_scan_kernel(const int32_t* __restric
   for (int i = b; i < e; ++i) {
     off[i] = run;
     cursor[i] = run;
-    run += count[i];
+    run += cap(count[i]);
   }
   if (threadIdx.x == 1023) off[n] = part[1023];
 }
@@ -248,7 +256,7 @@ size_t bwd_scratch_bytes(const msa_plan_s* p) {
   const size_t tq = static_cast<size_t>(p->total_q);
   const size_t ent = static_cast<size_t>(p->n_page_entries) * p->hkv;
   return 2 * al256(4 * tq * p->hq) + al256(4 * tq * p->hp) + al256(2 * tq * p->hp * kDP) + al256(4 * tq * p->hp) +
-         al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk)) +
+         al256(sizeof(int32_t) * (3 * ent + 1 + 2 * static_cast<size_t>(p->n_tiles) * p->hp * p->topk)) +
          al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages)) +
          al256(4 * ent * 128 * kDP) + al256(4 * static_cast<size_t>(p->n_page_entries));
 }
@@ -277,7 +285,7 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   int32_t* off = cnt + ent;
   int32_t* cur = off + ent + 1;
   int32_t* list = cur + ent;
-  sp += al256(sizeof(int32_t) * (3 * ent + 1 + static_cast<size_t>(p->n_tiles) * p->hp * p->topk));
+  sp += al256(sizeof(int32_t) * (3 * ent + 1 + 2 * static_cast<size_t>(p->n_tiles) * p->hp * p->topk));
   int32_t* owner = reinterpret_cast<int32_t*>(sp);                    // [num_pages]
   sp += al256(sizeof(int32_t) * static_cast<size_t>(p->num_pages));
   float* dpk_part = reinterpret_cast<float*>(sp);                     // [entries][hkv][128][dp]
@@ -311,8 +319,8 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   if (s != MSA_OK) return s;
   s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
   if (s != MSA_OK) return s;
-  return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, idx, owner, off, list, lse2t,
-                           dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, kl_weight, st);
+  return launch_bwd_dkv_tc(p, q, k_pages, v_pages, dout, pq, pk_pages, kv_indices, idx, owner, off, cnt, list,
+                           lse2t, dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, kl_weight, st);
 }
 
 }  // namespace msa

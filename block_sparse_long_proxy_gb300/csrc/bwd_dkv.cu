@@ -49,7 +49,7 @@ constexpr int kDP = 64;
 constexpr int kQStages = 3;
 constexpr int kSoftWarps = 8;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
-constexpr int kMaxList = 2048;
+constexpr int kMaxList = kBwdSmemList;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr uint32_t kColS = 0, kColDP = 64, kColDV = 128, kColDPK = 256, kColDK = 320, kColK = 448;
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap dk_map, const __grid_constant__ CUtensorMap dv_map,
                       const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx,
                       const int32_t* __restrict__ owner, const int32_t* __restrict__ inv_off,
-                      const int32_t* __restrict__ inv_list, int32_t topk,
+                      const int32_t* __restrict__ inv_cnt, int32_t* __restrict__ inv_list, int32_t topk,
                       const int32_t* __restrict__ kv_indices, int64_t num_pages, const float* __restrict__ lse2t,
                       const float* __restrict__ dsumt, const float* __restrict__ lsept, float* __restrict__ dk,
                       float* __restrict__ dv, float* __restrict__ dpk, float* __restrict__ dpk_part,
@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool page_ok = page >= 0 && page < num_pages;
   if (page_ok && owner[page] != e) return;  // another entry's CTA owns this page
   if (!page_ok) page = 0;
-  const int lb = inv_off[e * hkv + g], n = inv_off[e * hkv + g + 1] - lb;
+  const int lb = inv_off[e * hkv + g], n = inv_cnt[e * hkv + g];
   const int64_t kv_off = (page * hkv + g) * 128 * d;
 
   // dpk of the page: each of its hkv CTAs leaves a partial, and the last of
@@ -208,7 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   // the selection list (flat indexes (t * hsel + p) * topk + slot), sorted so
-  // that every run sums in the same order
+  // that every run sums in the same order: in registers (up to 32 entries),
+  // in shared memory (up to kMaxList) or in place in the inverse index
   const bool sorted = n <= kMaxList;
   if (n <= 32) {  // one warp, in registers (bitonic network over lanes)
     if (warp == 0) {
@@ -238,6 +239,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((a > b) == up) {
               list[i] = b;
               list[o] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+  } else {
+    // a list too long for shared memory: sorted in place in the inverse
+    // index, whose capacity for it is the next power of two (the scan gives
+    // it that), padded with the largest key; rare, and off the common path
+    int pow2 = 1;
+    while (pow2 < n) pow2 <<= 1;
+    int32_t* gl = inv_list + lb;
+    for (int i = n + threadIdx.x; i < pow2; i += blockDim.x) gl[i] = 0x7FFFFFFF;
+    __syncthreads();
+    for (int size = 2; size <= pow2; size <<= 1)
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = threadIdx.x; i < pow2; i += blockDim.x) {
+          const int o = i ^ stride;
+          if (o > i) {
+            const bool up = (i & size) == 0;
+            const int a = gl[i], b = gl[o];
+            if ((a > b) == up) {
+              gl[i] = b;
+              gl[o] = a;
             }
           }
         }
@@ -608,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                              const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                              const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
-                             const int32_t* inv_list,
+                             const int32_t* inv_cnt, int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
                              float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st) {
   // tensors of their true width d (dp); the 64-column boxes read zeros past
@@ -640,7 +665,7 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
   const int smem = DkvSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
-      qm, dom, pqm, km, vm, pkm, dkm, dvm, p->tiles_d, idx, owner, inv_off, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
+      qm, dom, pqm, km, vm, pkm, dkm, dvm, p->tiles_d, idx, owner, inv_off, inv_cnt, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
       dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), p->d,
       p->dp, kl_weight, p->err_d);
   return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");

@@ -132,10 +132,14 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
 // the row statistics written by the prep kernel, [heads][total_q]; dpk_part
 // is [page-table entries][hkv][128][64] fp32 scratch, dpk_cnt [entries]
 // int32 zeroed.
+// Selection lists (per page owner and KV head) of up to kBwdSmemList entries
+// are sorted in shared memory by the key-side kernel; a longer list gets a
+// power-of-two capacity in the inverse index and is sorted in place there.
+constexpr int kBwdSmemList = 2048;
 msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_pages, const void* v_pages,
                              const void* dout, const void* pq, const void* pk_pages, const int32_t* kv_indices,
                              const int32_t* idx, const int32_t* owner, const int32_t* inv_off,
-                             const int32_t* inv_list,
+                             const int32_t* inv_cnt, int32_t* inv_list,
                              const float* lse2t, const float* dsumt, const float* lsept, float* dk, float* dv,
                              float* dpk, float* dpk_part, int32_t* dpk_cnt, float kl_weight, cudaStream_t st);
 

@@ -197,3 +197,38 @@ def test_bwd_refuses_misaligned_gradients(cuda_dev):
     assert e.value.status == 1
     torch.cuda.synchronize()
     assert (buf == 0).all()
+
+
+def test_bwd_long_selection_list_is_sorted_in_place(cuda_dev):
+    """1025 one-tile sequences whose page tables all name one physical page,
+    with two proxy heads per KV head: 2050 selections of that page by one KV
+    head, more than the key-side kernel sorts in shared memory, so the list
+    is sorted in place in the inverse index.  All five gradients match the
+    oracle (dK, dV and dpk of the shared page sum every sequence) and two
+    runs give the same bits."""
+    n_seq = 1025
+    case = synth.Case("long list", [128] * n_seq, [128] * n_seq, 2, 1, 64, 2, 32, 1)
+    inp = synth.make_inputs(case, device=cuda_dev, with_dout=True)
+    inp["kv_indices"] = torch.zeros_like(inp["kv_indices"])  # every sequence's only block is physical page 0
+    idx_np = random_idx(case, np.random.default_rng(5))
+    idx_t = torch.from_numpy(idx_np).to(cuda_dev)
+    plan = make_plan(case, inp)
+    out, lse = plan.sparse_attn(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t)
+    runs = []
+    for _ in range(2):
+        g = plan.sparse_attn_bwd(inp["q"], inp["k_pages"], inp["v_pages"], inp["kv_indices"], idx_t, out, lse,
+                                 inp["dout"], inp["pq"], inp["pk_pages"], kl_weight=0.9)
+        torch.cuda.synchronize()
+        plan.check_errors()
+        runs.append({k: v.clone() for k, v in g.items()})
+    for name in ("dq", "dpq", "dk", "dv", "dpk"):
+        assert torch.equal(runs[0][name], runs[1][name]), "%s differs between runs" % name
+    ref = _oracle(case, inp, idx_np, 0.9)
+    got = {k: v.cpu().numpy() for k, v in runs[0].items()}
+    for name in ("dq", "dpq"):
+        compare_out(got[name], ref[name], O_ATOL_BF16, name)
+    # the shared page's dK, dV and dpk sum 2050 selections (magnitudes up to
+    # ~740): the bar is the same relative precision as for an O(1) output
+    for name in ("dk", "dv", "dpk"):
+        assert np.isfinite(got[name]).all(), name
+        compare_out(got[name], ref[name], O_ATOL_BF16 * max(1.0, float(np.abs(ref[name]).max())), name)

@@ -97,7 +97,7 @@ struct UnitStats {
 // (kStageO: one 64-column box of a head's bf16 O tile, for the TMA stores of
 // full tiles), barriers, the units' row statistics, then the two list slots,
 // whose size follows topk.
-template <int D, bool kStageO>
+template <int D, bool kStageO, int kLists = 1>
 struct AttnSmem {
   static constexpr int kTileBytes = 128 * D * 2;  // 128 rows x D bf16, in D/64 swizzled chunks of 16 KB
   static constexpr int kQOff = 0;
@@ -108,7 +108,7 @@ struct AttnSmem {
   static constexpr int kBarOff = kOOff + (kStageO ? kOChunkBytes : 0);
   static constexpr int kStatOff = kBarOff + 8 * 64;
   static constexpr int kListOff = kStatOff + 4 * static_cast<int>(sizeof(UnitStats));
-  static __host__ __device__ constexpr int slot_ints(int cap) { return kHdrInts + 2 * cap; }
+  static __host__ __device__ constexpr int slot_ints(int cap) { return kHdrInts + 2 * kLists * cap; }
   static __host__ __device__ constexpr int bytes(int cap) { return kListOff + kListSlots * slot_ints(cap) * 4; }
 };
 
@@ -131,7 +131,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   // hsel block sets (proxy heads) per tile; a unit's u.g is its proxy head,
   // whose blocks are read from KV head u.g / kv_div of hsel / kv_div
   const int hkv = hsel / kv_div;
-  using L = AttnSmem<D, kStageO>;
+  // a one-head K/V pool (the backward's proxy softmax) pairs two proxy heads
+  // per unit, each over its own blocks: one (j, row) list per head
+  using L = AttnSmem<D, kStageO, kOneKvHead ? 2 : 1>;
   constexpr int kChunks = D / 64;
   static_assert(!kFp8 || (D == 128 && !kOneKvHead), "FP8 K/V: head_dim 128, main attention");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -147,6 +149,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
   auto lhdr = [&](int k) -> UnitHdr& { return *reinterpret_cast<UnitHdr*>(list_base + (k % kListSlots) * slot_ints); };
   auto lj = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts; };
   auto lrow = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts + cap; };
+  auto lj1 = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts + 2 * cap; };
+  auto lrow1 = [&](int k) -> int32_t* { return list_base + (k % kListSlots) * slot_ints + kHdrInts + 3 * cap; };
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 1;
@@ -252,6 +256,46 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         n += __popc(m);
       }
+      const bool pair = kOneKvHead && u.nh == 2;
+      if (pair) {
+        // the second proxy head's own blocks (selection row g + 1); the
+        // shorter list is padded with j = -1 (fully masked, page row 0)
+        int32_t* const ls_j1 = lj1(k);
+        int32_t* const ls_row1 = lrow1(k);
+        const int32_t* sel1 = sel + topk;
+        int n1 = 0;
+        for (int b = 0; b < topk; b += 32) {
+          const int kk = b + lane;
+          const int j = kk < topk ? sel1[kk] : -1;
+          const bool valid = j >= 0 && j < tl.nvp;
+          if (j >= tl.nvp) atomicOr(err, kErrDeviceCheck);
+          int row = 0;
+          if (valid) {
+            int64_t page = kv_indices[tl.page_base + j];
+            if (page < 0 || page >= num_pages) {
+              atomicOr(err, kErrDeviceCheck);
+              page = 0;
+            }
+            row = static_cast<int>(page * 128);
+          }
+          const uint32_t m = __ballot_sync(0xFFFFFFFFu, valid);
+          if (valid) {
+            const int o = n1 + __popc(m & ((1u << lane) - 1u));
+            ls_j1[o] = j;
+            ls_row1[o] = row;
+          }
+          n1 += __popc(m);
+        }
+        for (int i = n + lane; i < n1; i += 32) {
+          ls_j[i] = -1;
+          ls_row[i] = 0;
+        }
+        for (int i = n1 + lane; i < n; i += 32) {
+          ls_j1[i] = -1;
+          ls_row1[i] = 0;
+        }
+        n = n > n1 ? n : n1;
+      }
       if (lane == 0) {
         ls.n = n;
         ls.nh = u.nh;
@@ -281,13 +325,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tma_load_2d(v_s + s * L::kTileBytes + 16384, &v_map, raw_full + s, 0, row);
             continue;
           }
-          // a one-head pool's keys are its values: one load serves both
-          mbar_expect_tx(kv_full + s, (kOneKvHead ? 1 : 2) * L::kTileBytes);
+          // a one-head pool's keys are its values: one load serves both, and
+          // a paired unit's second head reads its own block from the V region
+          const bool pair = kOneKvHead && u.nh == 2;
+          const int row1 = pair ? lrow1(k)[i] : row;
+          mbar_expect_tx(kv_full + s, (kOneKvHead && !pair ? 1 : 2) * L::kTileBytes);
           for (int c = 0; c < kChunks; ++c)
             tma_load_2d(k_s + s * L::kTileBytes + c * 16384, &k_map, kv_full + s, c * 64, row);
-          if (!kOneKvHead)
+          if (!kOneKvHead || pair)
             for (int c = 0; c < kChunks; ++c)
-              tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, kv_full + s, c * 64, row);
+              tma_load_2d(v_s + s * L::kTileBytes + c * 16384, &v_map, kv_full + s, c * 64, row1);
         }
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -308,8 +355,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       const uint64_t qd0 = smem_desc(smem_u32(q_s), 16, 1024, kSwizzle128);
       const uint64_t kd0 = smem_desc(smem_u32(k_s), 16, 1024, kSwizzle128);
       const uint64_t vd0 = smem_desc(smem_u32(kOneKvHead ? k_s : v_s), 16384, 1024, kSwizzle128);
+      // a paired one-head unit: head 1's block sits in the V region, as its
+      // keys (K-major) and its values (rows-major)
+      const uint64_t kd1 = smem_desc(smem_u32(v_s), 16, 1024, kSwizzle128);
+      const uint64_t vd1 = smem_desc(smem_u32(v_s), 16384, 1024, kSwizzle128);
       auto qk = [&](int h, int s) {
-        const uint64_t qd = qd0 + h * kTileDesc, kd = kd0 + s * kTileDesc;
+        const uint64_t qd = qd0 + h * kTileDesc, kd = (kOneKvHead && h == 1 ? kd1 : kd0) + s * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
@@ -318,7 +369,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mma_commit(s_full + h);
       };
       auto pv = [&](int h, int s, bool acc) {
-        const uint64_t vd = vd0 + s * kTileDesc;
+        const uint64_t vd = (kOneKvHead && h == 1 ? vd1 : vd0) + s * kTileDesc;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tmem + 256 + h * D, tmem + h * 128 + kk * 8, vd + ((kk * 2048) >> 4), id_pv, acc || (kk > 0));
@@ -404,7 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     bool ok = true;
     for (int k = 0, ui = blockIdx.x; ui < n_units; ++k, ui += gridDim.x) {
       const UnitHdr& ls = lhdr(k);
-      const int32_t* const ls_j = lj(k);
+      const int32_t* const ls_j = kOneKvHead && h == 1 ? lj1(k) : lj(k);  // a paired unit's heads: own blocks
       if (ok) ok = mbar_wait_inl(list_full + k % kListSlots, (k / kListSlots) & 1, err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       const int n = ok ? ls.n : 0, nh = ok ? ls.nh : 0;
@@ -423,9 +474,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, sv + c * 32);
         tmem_wait_ld();
         const int j = ls_j[i];
-        const bool need_mask = (j * 128 + 127 > pos0) || (rows < 128);
+        const bool pad = kOneKvHead && j < 0;  // the shorter list of a paired unit: every key masked
+        const bool need_mask = pad || (j * 128 + 127 > pos0) || (rows < 128);
         if (need_mask) {  // only diagonal / ragged blocks: -inf past the row's position
-          const int limit = row_ok ? qpos - j * 128 : -1;
+          const int limit = row_ok && !pad ? qpos - j * 128 : -1;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > limit) sv[c] = __float_as_uint(-INFINITY);
@@ -713,10 +765,12 @@ void attn_plan_tables(msa_plan_s* p, std::vector<int32_t>& aux) {
   p->n_attn_units = static_cast<int32_t>(us.size());
   const int32_t* raw = reinterpret_cast<const int32_t*>(us.data());
   aux.insert(aux.end(), raw, raw + us.size() * 4);
-  // the proxy softmax of the backward: proxy head g over its own blocks
+  // the proxy softmax of the backward: proxy heads g and g + 1 of a tile in
+  // one unit, each over its own blocks (the two heads' softmaxes overlap each
+  // other's products)
   std::vector<AttnUnit> ps;
   for (int t = 0; t < p->n_tiles; ++t)
-    for (int g = 0; g < p->hp; ++g) ps.push_back(AttnUnit{t, g, g, 1});
+    for (int g = 0; g < p->hp; g += 2) ps.push_back(AttnUnit{t, g, g, std::min(2, p->hp - g)});
   std::stable_sort(ps.begin(), ps.end(), [&](const AttnUnit& a, const AttnUnit& b) {
     return std::min(p->tiles[a.tile].nvp, p->topk) > std::min(p->tiles[b.tile].nvp, p->topk);
   });
@@ -755,7 +809,7 @@ cudaError_t launch_attn_variant(dim3 grid, cudaStream_t st, const CUtensorMap& q
                                 const float* v_scale, uint32_t* err) {
   const int cap = (topk + 3) & ~3;
   if constexpr (kFp8) {
-    const int staged = AttnSmem<D, true>::bytes(cap) + 1024;
+    const int staged = AttnSmem<D, true, kOneKvHead ? 2 : 1>::bytes(cap) + 1024;
     if (staged <= kMaxSmem) {
       auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, true>;
       if (const cudaError_t e = check_launch_regs(kern)) return e;
@@ -765,7 +819,7 @@ cudaError_t launch_attn_variant(dim3 grid, cudaStream_t st, const CUtensorMap& q
                         v_scale, err);
     }
   }
-  const int plain = AttnSmem<D, false>::bytes(kMaxTopk) + 1024;
+  const int plain = AttnSmem<D, false, kOneKvHead ? 2 : 1>::bytes(kMaxTopk) + 1024;
   auto kern = attn_fwd_kernel<D, kOneKvHead, kFp8, false>;
   if (const cudaError_t e = check_launch_regs(kern)) return e;
   cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, plain);

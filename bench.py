@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # (DRAM bytes read + written) of one launch of the small S=16384 capture and the
     # (tile, group, block) selections it processed; scaled to a launch by selections.
-    "attn_fwd.cu": {"src": "1135c1938e315513", "bytes": 244261888 + 107886592, "sel": 15424},
-    "attn_fwd.cu:fp8": {"src": "1135c1938e315513", "bytes": 180615424 + 101479680, "sel": 15424},
+    "attn_fwd.cu": {"src": "ddc78d865d0567a3", "bytes": 244076288 + 108070400, "sel": 15424},
+    "attn_fwd.cu:fp8": {"src": "ddc78d865d0567a3", "bytes": 180636416 + 101585152, "sel": 15424},
 }
 
 

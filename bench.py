@@ -224,6 +224,14 @@ def cpu_cores():
         return os.cpu_count()
 
 
+def bench_config(case, world):
+    """The workload of the JSON line, the same for both arms."""
+    return {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
+            "proxy_heads": 8, "proxy_dim": 64, "topk": 16, "page_size": 128,
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)"}
+
+
 def run_reference(args):
     """The oracle, as it stands, on the host cores, on the same workload."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -246,8 +254,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * secs / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
-                       "proxy_heads": 8, "proxy_dim": 64, "topk": 16},
+            "config": bench_config(case, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
                              "sample": "%d random query tiles of 128 rows per step through the whole oracle chain "
                                        "(proxy max-score, top-k, attention)" % per_step_tiles},
@@ -437,10 +444,7 @@ def run_ours(args):
     line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": case.name, "batch": 1, "seq_len": 32768, "heads": "32q/8kv", "head_dim": 128,
-                       "proxy_heads": 8, "proxy_dim": 64, "topk": 16, "page_size": 128,
-                       "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "flushed between timed steps (256 MiB write, then 256 MiB read)"},
+            "config": bench_config(case, world),
             "stages_ms": {"proxy_maxscore": proxy_ms, "topk_select": topk_ms, "sparse_attn": attn_ms},
             "proxy_topk_fused_ms": statistics.median(fused_ms),
             "tflops_selected": attn_tflops, "proxy_tflops": proxy_tflops,

@@ -39,6 +39,8 @@ SMALL = [
     # two and more cached blocks (the head's Q sits in a different K stage for each)
     (synth.Case("G=3 ragged", [300, 129, 77], [900, 129, 333], 6, 2, 128, 2, 64, 3, page_perm_seed=9), 0.9),
     (synth.Case("G=2 Hp=2Hkv", [640, 200], [640, 700], 8, 2, 128, 4, 64, 5, page_perm_seed=10), 1.0),
+    # an odd number of proxy heads: the proxy softmax pairs heads 0 and 1 and runs head 2 alone
+    (synth.Case("Hp=3", [300, 129], [300, 500], 6, 3, 128, 3, 64, 3, page_perm_seed=11), 0.7),
 ]
 
 

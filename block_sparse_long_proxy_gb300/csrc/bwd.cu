@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(kThreads)
                     float* __restrict__ dsumt, float* __restrict__ lse2t, float* __restrict__ lsept,
                     float* __restrict__ dpq, int32_t hq, int32_t hsel, int32_t total_q, int32_t d, int32_t dp,
                     float kl_weight) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   const int t = blockIdx.x / hsel, g = blockIdx.x % hsel;
   const TileInfo tl = tiles[t];
   const int lane = threadIdx.x & 31;
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kThreads)
 // starts at INT_MAX).  Entries with a page id out of range own themselves.
 __global__ void bwd_owner_kernel(const int32_t* __restrict__ kv_indices, int32_t n_entries, int64_t num_pages,
                                  int32_t* __restrict__ owner) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e >= n_entries) return;
   const int64_t page = kv_indices[e];
@@ -165,6 +167,7 @@ __device__ __forceinline__ int32_t owner_of(const int32_t* __restrict__ kv_indic
 __global__ void bwd_count_kernel(const TileInfo* __restrict__ tiles, const int32_t* __restrict__ idx, int32_t n_tiles,
                                  int32_t hsel, int32_t kv_div, int32_t topk, const int32_t* __restrict__ kv_indices,
                                  const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ count) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(n_tiles) * hsel * topk) return;
   const int hkv = hsel / kv_div;
@@ -180,6 +183,7 @@ __global__ void bwd_count_kernel(const TileInfo* __restrict__ tiles, const int32
 // cursor[] is reset to off[].
 __global__ void __launch_bounds__(1024) bwd_scan_kernel(const int32_t* __restrict__ count, int32_t n,
                                                         int32_t* __restrict__ off, int32_t* __restrict__ cursor) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   __shared__ int32_t part[1024];
   const int per = (n + 1023) / 1024;
   const int b = threadIdx.x * per, e = min(n, b + per);
@@ -217,6 +221,7 @@ __global__ void bwd_fill_kernel(const TileInfo* __restrict__ tiles, const int32_
                                 int32_t hsel, int32_t kv_div, int32_t topk, const int32_t* __restrict__ kv_indices,
                                 const int32_t* __restrict__ owner, int64_t num_pages, int32_t* __restrict__ cursor,
                                 int32_t* __restrict__ list) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (e >= static_cast<int64_t>(n_tiles) * hsel * topk) return;
   const int hkv = hsel / kv_div;
@@ -296,26 +301,36 @@ msa_status launch_attn_bwd(const msa_plan_s* p, const void* q, const void* k_pag
   const int64_t n_sel = static_cast<int64_t>(p->n_tiles) * p->hp * p->topk;
   const int kv_div = p->hp / p->hkv;
 
-  msa_status s = launch_proxy_softmax(p, pq, pk_pages, kv_indices, idx, op, lse_p, st);
-  if (s != MSA_OK) return s;
-  bwd_prep_kernel<<<p->n_tiles * p->hp, kThreads, 0, st>>>(p->tiles_d, O, dO, lse, op, lse_p, dsumt, lse2t, lsept,
-                                                          dpq, p->hq, p->hp, static_cast<int32_t>(p->total_q),
-                                                          p->d, p->dp, kl_weight);
-  s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
+  // the counters first, so that the kernels follow one another with
+  // programmatic dependent launch (each waits for its predecessor's writes)
+  msa_status s = cuda_check(cudaMemsetAsync(cnt, 0, sizeof(int32_t) * ent, st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)
     s = cuda_check(cudaMemsetAsync(dpk_cnt, 0, 4 * static_cast<size_t>(n_ent), st), "msa_sparse_attn_bwd: memset");
   if (s == MSA_OK)  // 0x7F7F7F7F: above every entry index
     s = cuda_check(cudaMemsetAsync(owner, 0x7F, sizeof(int32_t) * static_cast<size_t>(p->num_pages), st),
                    "msa_sparse_attn_bwd: memset");
+  if (s == MSA_OK) s = launch_proxy_softmax(p, pq, pk_pages, kv_indices, idx, op, lse_p, st);
   if (s != MSA_OK) return s;
-  bwd_owner_kernel<<<(n_ent + 255) / 256, 256, 0, st>>>(kv_indices, n_ent, p->num_pages, owner);
   const int sel_blocks = static_cast<int>((n_sel + 255) / 256);
-  bwd_count_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hp, kv_div, p->topk, kv_indices,
-                                               owner, p->num_pages, cnt);
-  bwd_scan_kernel<<<1, 1024, 0, st>>>(cnt, static_cast<int32_t>(ent), off, cur);
-  bwd_fill_kernel<<<sel_blocks, 256, 0, st>>>(p->tiles_d, idx, p->n_tiles, p->hp, kv_div, p->topk, kv_indices,
-                                              owner, p->num_pages, cur, list);
-  s = cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: launch");
+  cudaError_t e = launch_pdl(bwd_prep_kernel, dim3(p->n_tiles * p->hp), dim3(kThreads), 0, st, p->tiles_d, O, dO,
+                             lse, static_cast<const __nv_bfloat16*>(op), static_cast<const float*>(lse_p), dsumt,
+                             lse2t, lsept, dpq, p->hq, p->hp, static_cast<int32_t>(p->total_q), p->d, p->dp,
+                             kl_weight);
+  if (e == cudaSuccess)
+    e = launch_pdl(bwd_owner_kernel, dim3((n_ent + 255) / 256), dim3(256), 0, st, kv_indices, n_ent, p->num_pages,
+                   owner);
+  if (e == cudaSuccess)
+    e = launch_pdl(bwd_count_kernel, dim3(sel_blocks), dim3(256), 0, st, static_cast<const TileInfo*>(p->tiles_d),
+                   idx, p->n_tiles, p->hp, kv_div, p->topk, kv_indices, static_cast<const int32_t*>(owner),
+                   p->num_pages, cnt);
+  if (e == cudaSuccess)
+    e = launch_pdl(bwd_scan_kernel, dim3(1), dim3(1024), 0, st, static_cast<const int32_t*>(cnt),
+                   static_cast<int32_t>(ent), off, cur);
+  if (e == cudaSuccess)
+    e = launch_pdl(bwd_fill_kernel, dim3(sel_blocks), dim3(256), 0, st, static_cast<const TileInfo*>(p->tiles_d), idx,
+                   p->n_tiles, p->hp, kv_div, p->topk, kv_indices, static_cast<const int32_t*>(owner),
+                   p->num_pages, cur, list);
+  s = cuda_check(e, "msa_sparse_attn_bwd: launch");
   if (s != MSA_OK) return s;
   s = launch_bwd_dq_tc(p, q, k_pages, v_pages, dout, pk_pages, idx, kv_indices, lse2t, dsumt, dq, dpq, kl_weight, st);
   if (s != MSA_OK) return s;

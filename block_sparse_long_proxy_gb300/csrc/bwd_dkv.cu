@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       float* __restrict__ dv, float* __restrict__ dpk, float* __restrict__ dpk_part,
                       int32_t* __restrict__ dpk_cnt, int32_t hq, int32_t hkv, int32_t hsel,
                       int32_t total_q, int32_t d, int32_t dp, float kl_weight, uint32_t* err) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   using L = DkvSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -664,11 +665,12 @@ msa_status launch_bwd_dkv_tc(const msa_plan_s* p, const void* q, const void* k_p
     return set_error(MSA_ERR_CUDA, "msa_sparse_attn_bwd: tensor map encoding failed");
   const int smem = DkvSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dkv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  bwd_dkv_tc_kernel<<<p->n_page_entries * p->hkv, kThreads, smem, st>>>(
-      qm, dom, pqm, km, vm, pkm, dkm, dvm, p->tiles_d, idx, owner, inv_off, inv_cnt, inv_list, p->topk, kv_indices, p->num_pages, lse2t,
-      dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt, p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), p->d,
-      p->dp, kl_weight, p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dkv launch");
+return cuda_check(launch_pdl(bwd_dkv_tc_kernel, dim3(p->n_page_entries * p->hkv), dim3(kThreads), smem, st, qm,
+                               dom, pqm, km, vm, pkm, dkm, dvm, p->tiles_d, idx, owner, inv_off, inv_cnt, inv_list,
+                               p->topk, kv_indices, p->num_pages, lse2t, dsumt, lsept, dk, dv, dpk, dpk_part, dpk_cnt,
+                               p->hq, p->hkv, p->hp, static_cast<int32_t>(p->total_q), p->d, p->dp, kl_weight,
+                               p->err_d),
+                    "msa_sparse_attn_bwd: dkv launch");
 }
 
 }  // namespace msa

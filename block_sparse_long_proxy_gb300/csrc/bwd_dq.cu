@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                      float* __restrict__ dpq, const int32_t* __restrict__ heavy_tiles, int32_t hq, int32_t hkv,
                      int32_t hsel, int32_t topk, int32_t total_q, int32_t d, int32_t dp, float kl_weight,
                      uint32_t* err) {
+  pdl_wait();  // launched with programmatic dependent launch: the previous kernel's writes first
   using L = DqSmem;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -486,11 +487,11 @@ msa_status launch_bwd_dq_tc(const msa_plan_s* p, const void* q, const void* k_pa
   const int smem = DqSmem::kBytes + 1024;
   cudaFuncSetAttribute(bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   // one CTA per (tile, proxy head), looping over the proxy head's query heads
-  bwd_dq_tc_kernel<<<p->n_tiles * p->hp, kThreads, smem, st>>>(
-      qm, dom, km, vm, pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq,
-      p->aux_d + p->heavy_tiles_off, p->hq, p->hkv, p->hp, p->topk, static_cast<int32_t>(p->total_q), p->d, p->dp,
-      kl_weight, p->err_d);
-  return cuda_check(cudaGetLastError(), "msa_sparse_attn_bwd: dq launch");
+  return cuda_check(launch_pdl(bwd_dq_tc_kernel, dim3(p->n_tiles * p->hp), dim3(kThreads), smem, st, qm, dom, km, vm,
+                               pkm, p->tiles_d, idx, kv_indices, p->num_pages, lse2t, dsumt, dq, dpq,
+                               p->aux_d + p->heavy_tiles_off, p->hq, p->hkv, p->hp, p->topk,
+                               static_cast<int32_t>(p->total_q), p->d, p->dp, kl_weight, p->err_d),
+                    "msa_sparse_attn_bwd: dq launch");
 }
 
 }  // namespace msa

@@ -436,6 +436,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       mma_commit(done);
     }
+    // dV and dK out of the softmax warps' staging boxes (see their epilogue)
+    const bool staged = bar_sync_and(1, 32 * kSoftWarps + 32, true);
+    if (staged && lane == 0) {
+      const int nbox = d / 32;
+      const int row0 = static_cast<int>((page * hkv + g) * 128);
+      for (int b = 0; b < nbox; ++b) {
+        tma_store_2d(&dv_map, smem + b * 16384, 32 * b, row0);
+        tma_store_2d(&dk_map, smem + (nbox + b) * 16384, 32 * b, row0);
+      }
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the boxes are read before the CTA's memory goes
+    }
   } else {
     // ----------------------------------------------------------- softmax
     const int wg = warp >> 2, quarter = warp & 3;
@@ -596,16 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_async_shared();  // the TMA stores read the boxes through the async proxy
     }
-    // every softmax thread has staged its rows (or none of the CTA's stores go out)
-    const bool staged = bar_sync_and(1, 32 * kSoftWarps, ok && page_ok);
-    if (staged && threadIdx.x == 0) {
-      const int row0 = static_cast<int>((page * hkv + g) * 128);
-      for (int b = 0; b < nbox; ++b) {
-        tma_store_2d(&dv_map, smem + b * 16384, 32 * b, row0);
-        tma_store_2d(&dk_map, smem + (nbox + b) * 16384, 32 * b, row0);
-      }
-      bulk_commit_group();
-    }
+    // every softmax thread has staged its rows (or none of the CTA's stores
+    // go out); the MMA warp, idle by now, issues the stores
+    bar_sync_and(1, 32 * kSoftWarps + 32, ok && page_ok);
     // this KV head's dpk partial (full 32-byte sectors), then the page's sum
     if (ok && page_ok) {
       const float f_main = -kl_weight * rsqrtf(static_cast<float>(dp)) / static_cast<float>(G);
@@ -621,7 +626,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                      __uint_as_float(a[8 * i + 6]) * f_main, __uint_as_float(a[8 * i + 7]) * f_main);
     }
     if (page_ok) finish_dpk(threadIdx.x, 32 * kSoftWarps, 1);  // the softmax warps: threads 0-255
-    if (staged && threadIdx.x == 0) bulk_wait_group_read0();  // the boxes are read before the CTA's memory goes
   }
   tc_fence_before();
   __syncthreads();

@@ -1,8 +1,9 @@
 """msa_proxy_maxscore on the GPU against the oracle.
 
-Tolerance: |gpu - oracle| <= 1e-3 on every finite entry (the north-star
-bound for proxy scores; the fp32 accumulation of exact bf16 products is
-~1e-6 off in practice) and an identical -inf pattern."""
+Tolerance: |gpu - oracle| <= 1e-3 on every finite entry (the parity bound
+for proxy scores, equal to the score-gap rule of the selections; the fp32
+accumulation of exact bf16 products is ~1e-6 off in practice) and an
+identical -inf pattern."""
 import numpy as np
 import pytest
 import torch

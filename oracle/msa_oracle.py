@@ -87,7 +87,9 @@ def bf16_to_f64(bits) -> np.ndarray:
     """bfloat16 bit patterns (uint16) -> float64, exactly (bf16 is the upper
     half of an IEEE binary32)."""
     u = np.ascontiguousarray(bits).view(np.uint16).astype(np.uint32) << np.uint32(16)
-    return u.view(np.float32).astype(np.float64)
+    # signalling-NaN patterns raise the invalid flag when widened; they stay NaN
+    with np.errstate(invalid="ignore"):
+        return u.view(np.float32).astype(np.float64)
 
 
 def e4m3_to_f64(bits) -> np.ndarray:

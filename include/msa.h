@@ -93,7 +93,11 @@ typedef struct msa_plan_s* msa_plan_t;
  * heads, num_kv_heads, page_size, kv_block_num=topk)).
  *
  *  qo_lens, kv_lens  HOST int32[batch]; 0 <= qo_lens[s] <= kv_lens[s],
- *                    kv_lens[s] >= 1.  Copied; the caller keeps ownership.
+ *                    kv_lens[s] >= 1, and at least one qo_lens[s] > 0 (a
+ *                    sequence with qo_len 0 has no tiles; its pages keep
+ *                    their page-table entries).  Otherwise
+ *                    MSA_ERR_INVALID_ARG.  Copied; the caller keeps
+ *                    ownership.
  *  num_qo_heads      Hq, query heads of the main attention.
  *  num_kv_heads      Hkv, KV heads (GQA groups); Hq % Hkv == 0.
  *  num_proxy_heads   Hp, proxy query heads, a multiple of Hkv that divides

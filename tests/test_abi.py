@@ -60,4 +60,13 @@ def test_host_validation_without_gpu(lib):
     assert f.msa_plan(ql, kl, 1, 8, 2, 1, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 2   # Hp < Hkv
     assert f.msa_plan(ql, kl, 1, 8, 3, 3, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 1   # Hq % Hkv
     assert f.msa_plan(ql, kl, 1, 8, 2, 2, 64, 32, 64, 4, 16, 0, 0, None, ctypes.byref(h)) == 2    # page 64
+    # sequence lengths: a negative qo_len, an empty kv_len and a batch without query rows are refused
+    ql2 = (ctypes.c_int32 * 2)(0, 0)
+    kl2 = (ctypes.c_int32 * 2)(100, 300)
+    assert f.msa_plan(ql2, kl2, 2, 8, 2, 2, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 1
+    assert b"no query rows" in f.msa_last_error()
+    ql2[1] = -1
+    assert f.msa_plan(ql2, kl2, 2, 8, 2, 2, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 1
+    ql2[1], kl2[1] = 0, 0
+    assert f.msa_plan(ql2, kl2, 2, 8, 2, 2, 64, 32, 128, 4, 16, 0, 0, None, ctypes.byref(h)) == 1
     assert f.msa_version() == b"0.1.0"

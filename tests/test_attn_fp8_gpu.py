@@ -20,6 +20,8 @@ CASES = [
     synth.Case("G=3 odd group", [200], [333], 6, 2, 128, 2, 64, 2, kv_dtype="e4m3", page_perm_seed=1),
     synth.Case("topk above blocks", [640], [640], 4, 1, 128, 1, 64, 9, kv_dtype="e4m3"),
     synth.Case("topk 1 straddling tile", [128, 100], [200, 300], 2, 1, 128, 1, 64, 1, kv_dtype="e4m3"),
+    synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
+               kv_dtype="e4m3", page_perm_seed=6),
     synth.Case("long 40-block rows topk 16", [5120], [5120], 8, 2, 128, 2, 64, 16, kv_dtype="e4m3",
                page_perm_seed=11),
 ]

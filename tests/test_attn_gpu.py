@@ -20,6 +20,9 @@ SMALL = [
     synth.Case("topk above blocks", [640], [640], 4, 1, 128, 1, 64, 9),
     synth.Case("topk 1 straddling tile", [128, 100], [200, 300], 2, 1, 64, 1, 32, 1),
     synth.Case("long 40-block rows topk 16", [5120], [5120], 8, 2, 128, 2, 64, 16, page_perm_seed=11),
+    # a sequence with keys but no query rows: no tiles, its pages still in the page table
+    synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
+               page_perm_seed=6),
 ]
 
 
@@ -70,7 +73,9 @@ def test_sparse_attn_irregular_indexes(cuda_dev, case):
 
 @pytest.mark.parametrize("case", [synth.tiny(),
                                   synth.Case("varlen planted small", [1024, 2048, 640], [1024, 2048, 900],
-                                             8, 2, 128, 2, 64, 4, page_perm_seed=1, planted=True)],
+                                             8, 2, 128, 2, 64, 4, page_perm_seed=1, planted=True),
+                                  synth.Case("empty query sequence mid-batch, chain", [300, 0, 129],
+                                             [300, 500, 129], 8, 2, 128, 2, 64, 3, page_perm_seed=6)],
                          ids=lambda c: c.name)
 def test_end_to_end_small(cuda_dev, case):
     """proxy -> top-k -> attention, every stage against the oracle: max_score

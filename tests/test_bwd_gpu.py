@@ -41,6 +41,9 @@ SMALL = [
     (synth.Case("G=2 Hp=2Hkv", [640, 200], [640, 700], 8, 2, 128, 4, 64, 5, page_perm_seed=10), 1.0),
     # an odd number of proxy heads: the proxy softmax pairs heads 0 and 1 and runs head 2 alone
     (synth.Case("Hp=3", [300, 129], [300, 500], 6, 3, 128, 3, 64, 3, page_perm_seed=11), 0.7),
+    # a sequence with keys but no query rows: its pages are never selected, so their dK, dV, dpk are 0
+    (synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
+                page_perm_seed=6), 1.0),
 ]
 
 

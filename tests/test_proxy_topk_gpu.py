@@ -20,6 +20,8 @@ CASES = [
     synth.Case("topk 32 over 100 blocks", [2048], [12800], 4, 2, 64, 2, 32, 32, page_perm_seed=2),
     synth.Case("topk 1", [640], [4500], 4, 2, 64, 2, 32, 1),
     synth.Case("16 proxy heads, two head groups", [1024], [5000], 16, 16, 64, 16, 64, 8),
+    synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
+               page_perm_seed=6),
 ]
 
 

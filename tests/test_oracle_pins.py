@@ -37,6 +37,12 @@ def test_e4m3_decode_all_codes():
     assert np.array_equal(np.isnan(ours), nan)
     assert np.array_equal(ours[~nan], ref[~nan])
     assert ours[0x7E] == 448.0 and ours[0x01] == 2.0 ** -9
+    # the K/V decode of the attention oracle looks the codes up in a table of
+    # this function's values: same bytes in any shape, same results
+    grid = np.random.default_rng(0).integers(0, 256, (3, 5, 7), dtype=np.uint8)
+    looked = O._decode_kv(grid, True)
+    assert looked.shape == grid.shape
+    assert np.array_equal(looked, O.e4m3_to_f64(grid), equal_nan=True)
 
 
 # ------------------------------------------------------------------ tiling --

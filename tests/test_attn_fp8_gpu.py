@@ -22,6 +22,8 @@ CASES = [
     synth.Case("topk 1 straddling tile", [128, 100], [200, 300], 2, 1, 128, 1, 64, 1, kv_dtype="e4m3"),
     synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
                kv_dtype="e4m3", page_perm_seed=6),
+    synth.Case("topk 1024 (the maximum) over 16 blocks", [2048], [2048], 4, 1, 128, 1, 64, 1024, kv_dtype="e4m3",
+               page_perm_seed=7),
     synth.Case("long 40-block rows topk 16", [5120], [5120], 8, 2, 128, 2, 64, 16, kv_dtype="e4m3",
                page_perm_seed=11),
 ]

@@ -23,6 +23,8 @@ SMALL = [
     # a sequence with keys but no query rows: no tiles, its pages still in the page table
     synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
                page_perm_seed=6),
+    # topk at the largest value a plan accepts; every tile takes all of its blocks
+    synth.Case("topk 1024 (the maximum) over 16 blocks", [2048], [2048], 4, 1, 128, 1, 64, 1024, page_perm_seed=7),
 ]
 
 

@@ -44,6 +44,9 @@ SMALL = [
     # a sequence with keys but no query rows: its pages are never selected, so their dK, dV, dpk are 0
     (synth.Case("empty query sequence mid-batch", [300, 0, 129], [300, 500, 129], 8, 2, 128, 2, 64, 3,
                 page_perm_seed=6), 1.0),
+    # topk at the largest value a plan accepts: every tile caches all of its blocks
+    (synth.Case("topk 1024 (the maximum) over 16 blocks", [2048], [2048], 4, 1, 128, 1, 64, 1024,
+                page_perm_seed=7), 1.0),
 ]
 
 

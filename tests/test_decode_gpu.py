@@ -18,6 +18,9 @@ CASES = [
     synth.Case("G=16 two n-tiles", [1] * 2, [2048, 777], 32, 2, 128, 2, 64, 5, kv_dtype="e4m3", page_perm_seed=6),
     synth.Case("G=1", [1] * 4, [1024, 200, 3000, 129], 3, 3, 128, 3, 32, 3, kv_dtype="e4m3", page_perm_seed=8),
     synth.Case("topk above blocks", [1] * 2, [256, 1000], 8, 1, 128, 1, 64, 12, kv_dtype="e4m3"),
+    # topk at the largest value a plan accepts, over a 1094-block sequence (and a 24-block one)
+    synth.Case("topk 1024 (the maximum)", [1] * 2, [140000, 3000], 8, 1, 128, 1, 64, 1024, kv_dtype="e4m3",
+               page_perm_seed=12),
 ]
 
 

@@ -21,7 +21,9 @@ def _scores(rng, n, h, nb, kind):
 @pytest.mark.parametrize("nb,topk,kind", [(8, 4, "ties"), (8, 1, "normal"), (200, 16, "normal"),
                                           (256, 16, "ties"), (257, 16, "normal"), (1000, 40, "ties"),
                                           (1024, 16, "normal"), (3000, 16, "ties"), (3000, 300, "normal"),
-                                          (64, 64, "normal"), (64, 65, "normal")])
+                                          (64, 64, "normal"), (64, 65, "normal"),
+                                          # the maxima the API accepts: topk 1024, 65536 blocks per row
+                                          (1025, 1024, "ties"), (65536, 1024, "normal"), (65536, 1024, "ties")])
 def test_topk_bit_exact(cuda_dev, nb, topk, kind):
     from block_sparse_long_proxy_gb300 import msa
     rng = np.random.default_rng(nb * 7 + topk)
